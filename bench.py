@@ -1,0 +1,403 @@
+"""Benchmark: MM-DiT joint attention (QK-RMSNorm + softmax attention) fwd+bwd on GB300.
+
+One step = jattn_fwd + jattn_bwd over one batch of the 512 px workload
+(B=16, H=12, N = 1024 image + 77 text tokens, d=64), inputs resident in HBM.
+The metric is TFLOP/s of the fwd+bwd pair at 14*B*H*N^2*d FLOP per step
+(forward 4 B H N^2 d; backward 10 B H N^2 d, the five N x N x d products
+including the recomputed scores), with the true N, so tile padding counts
+against the kernels.
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own
+replica of the workload (the path has no exchange step: (b, h) pairs are
+independent), a barrier + synchronize brackets the timed region, the time is
+the max over ranks and the value is the work of all ranks over that time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "joint-attn fwd+bwd TFLOP/s and % of GB300 dense-BF16 peak at B16 H12 N1101 d64"
+UNIT = "TFLOP/s"
+WORKLOAD = "512px"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Rotating input sets: 3 x (q, k, v, dout, out, lse, dq, dk, dv) at 512 px is
+# about 3 x 245 MB, well beyond the 129 MB L2, so no step starts warm.
+N_SETS = 3
+
+
+def flops_fwd(B, H, N, d):
+    return 4.0 * B * H * N * N * d
+
+
+def flops_bwd(B, H, N, d):
+    return 10.0 * B * H * N * N * d
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            data = json.load(open(path))
+            flat = {}
+
+            def walk(o):
+                if isinstance(o, dict):
+                    for key, val in o.items():
+                        if isinstance(val, (int, float)) and key in FALLBACK_PEAKS:
+                            flat[key] = float(val)
+                        walk(val)
+            walk(data)
+            if "bf16_tflops" in flat and "hbm_gbs" in flat:
+                flat.setdefault("bf16_tflops_sustained", flat["bf16_tflops"])
+                return flat, "measured"
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_median": statistics.median([num(r[3]) for r in rows if num(r[3]) is not None] or [0])}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(B, H, N, d, seed, budget_s: float, max_heads: int):
+    """Times the float64 oracle on whole heads of the workload until budget_s."""
+    import numpy as np
+
+    import oracle
+    from joint_attention_gb300.inputs import make_inputs
+
+    inp = make_inputs(1, 1, N, d, seed=seed)
+    heads = 0
+    t0 = time.perf_counter()
+    while heads < max_heads:
+        oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    fl = (flops_fwd(1, 1, N, d) + flops_bwd(1, 1, N, d)) * heads
+    del np
+    return {"value": fl / el / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{heads} head(s) of the {WORKLOAD} workload (N={N}, d={d}) fwd+bwd in float64 NumPy, "
+                      f"materialised N x N scores, {el:.2f} s; BLAS threads = all host cores"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from joint_attention_gb300.inputs import CONFIGS
+
+    c = CONFIGS[WORKLOAD]
+    import numpy as np
+
+    import oracle
+    from joint_attention_gb300.inputs import make_inputs
+
+    inp = make_inputs(1, 1, c.N, c.d, seed=c.seed)
+    for _ in range(args.warmup):
+        oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    el = time.perf_counter() - t0
+    fl = (flops_fwd(1, 1, c.N, c.d) + flops_bwd(1, 1, c.N, c.d)) * args.steps
+    val = fl / el / 1e12
+    del np
+    sample = (f"each step = one (b, h) head of the {WORKLOAD} workload (N={c.N}, d={c.d}) fwd+bwd in float64 "
+              f"NumPy with materialised scores")
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"{WORKLOAD} B16 H12 N_img1024 N_txt77 d64 (one head per step)",
+                       "sample": sample},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from joint_attention_gb300.build import build
+
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    import joint_attention_gb300 as ja
+    from joint_attention_gb300.inputs import CONFIGS, make_config_inputs
+
+    ja.load_library()
+    c = CONFIGS[WORKLOAD]
+    B, H, N, d = c.B, c.H, c.N, c.d
+    inp = make_config_inputs(c)
+
+    def bf(a):
+        return torch.from_numpy(a).to(dev).to(torch.bfloat16).contiguous()
+
+    gq = torch.from_numpy(inp.gq).to(dev).float().contiguous()
+    gk = torch.from_numpy(inp.gk).to(dev).float().contiguous()
+    sets = []
+    for s in range(N_SETS):
+        # set 0 is the seeded workload; the others are permutations of it
+        # (same values and statistics, different addresses).
+        roll = s * 7
+        q = bf(inp.q).roll(roll, dims=2).contiguous()
+        k = bf(inp.k).roll(roll, dims=2).contiguous()
+        v = bf(inp.v).roll(roll, dims=2).contiguous()
+        do = bf(inp.dout).roll(roll, dims=2).contiguous()
+        sets.append(dict(q=q, k=k, v=v, dout=do, out=torch.empty_like(q),
+                         lse=torch.empty((B, H, N), device=dev, dtype=torch.float32),
+                         dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
+                         dgq=torch.empty_like(gq), dgk=torch.empty_like(gk)))
+    stream = torch.cuda.current_stream(dev)
+    n_img, n_txt = c.N_img, c.N_txt
+
+    def step(i):
+        t = sets[i % N_SETS]
+        ja.jattn_fwd(t["q"], t["k"], t["v"], gq, gk, B, H, n_img, n_txt, d, t["out"], t["lse"], stream)
+        ja.jattn_bwd(t["q"], t["k"], t["v"], gq, gk, t["out"], t["lse"], t["dout"], t["dq"], t["dk"], t["dv"],
+                     t["dgq"], t["dgk"], B, H, n_img, n_txt, d, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if ja.jattn_last_device_error(stream) != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    # ---- timed region (device time, CUDA events on the launching stream) ----
+    ja.jattn_profile_reset()
+    ja.jattn_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+    ja.jattn_profile_enable(False)
+    ms_total = ev0.elapsed_time(ev1)
+    prof = ja.profile_snapshot()
+    if ja.jattn_last_device_error(stream) != 0:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    fl_step = flops_fwd(B, H, N, d) + flops_bwd(B, H, N, d)
+    value = fl_step * args.steps * world / (ms_total * 1e-3) / 1e12
+
+    # ---- end to end: pinned host buffers, copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        t = sets[0]
+        h_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "dout")}
+        h_g = {"gq": gq.cpu().pin_memory(), "gk": gk.cpu().pin_memory()}
+        h_out = {n: torch.empty_like(t[n], device="cpu").pin_memory()
+                 for n in ("out", "lse", "dq", "dk", "dv", "dgq", "dgk")}
+        d_g = {"gq": torch.empty_like(gq), "gk": torch.empty_like(gk)}
+        h2d = sum(x.numel() * x.element_size() for x in list(h_in.values()) + list(h_g.values()))
+        d2h = sum(x.numel() * x.element_size() for x in h_out.values())
+
+        def e2e_step():
+            for n, x in h_in.items():
+                t[n].copy_(x, non_blocking=True)
+            for n, x in h_g.items():
+                d_g[n].copy_(x, non_blocking=True)
+            ja.jattn_fwd(t["q"], t["k"], t["v"], d_g["gq"], d_g["gk"], B, H, n_img, n_txt, d, t["out"], t["lse"],
+                         stream)
+            ja.jattn_bwd(t["q"], t["k"], t["v"], d_g["gq"], d_g["gk"], t["out"], t["lse"], t["dout"], t["dq"],
+                         t["dk"], t["dv"], t["dgq"], t["dgk"], B, H, n_img, n_txt, d, stream)
+            for n, x in h_out.items():
+                x.copy_(t[n], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n_e2e = max(3, args.steps // 3)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        e2e = {"value": fl_step * n_e2e * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": ms_e2e / n_e2e}
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel ----
+    peaks, peak_src = load_peaks()
+    kern = {name: {"launches": n, "total_ms": ms, "avg_us": (ms / n * 1e3) if n else None}
+            for name, (n, ms) in prof.items()}
+    tot = sum(v["total_ms"] for v in kern.values()) or 1.0
+    for v in kern.values():
+        v["share"] = v["total_ms"] / tot
+    dom = max(kern, key=lambda k: kern[k]["total_ms"])
+    algo = {  # algorithmic work per launch (FLOP for contractions, bytes for HBM-bound kernels)
+        "attn_fwd": ("tensor", flops_fwd(B, H, N, d)),
+        "attn_bwd": ("tensor", flops_bwd(B, H, N, d)),
+        "qk_norm_fwd": ("hbm", 4.0 * B * H * N * d * 2),
+        "bwd_prep": ("hbm", B * H * N * d * 2 * 4 + B * H * N * d * 2 * 2 + B * H * N * d * 4 + B * H * N * 4 * 5),
+        "q_norm_bwd": ("hbm", B * H * N * d * (4 + 2 + 2) + B * H * N * 4),
+        "dg_reduce": ("hbm", 0.0),
+    }
+    bound, work = algo[dom]
+    avg_s = kern[dom]["avg_us"] * 1e-6
+    if bound == "tensor":
+        achieved = work / avg_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_sample(B, H, N, d, c.seed, args.cpu_budget_s, max_heads=64)
+    launches = sum(v["launches"] for v in kern.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} MM-DiT joint attention fwd+bwd: B={B} H={H} N_img={c.N_img} "
+                               f"N_txt={c.N_txt} (N={N}) d={d}, QK-RMSNorm eps=1e-6",
+                   "flop_per_step": fl_step, "l2": f"{N_SETS} rotating input sets, each larger than L2 "
+                                                   f"together (~{N_SETS * 245} MB vs 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak_bf16": value / world / peaks["bf16_tflops"] * 100.0,
+        "peak_bf16_tflops": peaks["bf16_tflops"], "peak_source": peak_src,
+        "images_equiv_per_s": B * world / (12 * ms_step * 1e-3),
+        "model_tflops": 12.0 * B * H * N * N * d * args.steps * world / (ms_total * 1e-3) / 1e12,
+        "roofline": roofline, "kernels": kern, "gpu_launches": launches,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,132 @@
+/*
+ * jattn.h — C ABI of libjattn: MM-DiT joint self-attention with QK-RMSNorm,
+ * forward and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (re-diffusion README — "architecture flowchart": inside each
+ * DiT layer the caption-stream and image-stream Q/K/V are concatenated as
+ * [c; x] and one multi-head self-attention runs over the joint sequence;
+ * "design notes" table, row "QK norm": RMSNorm on Q and on K; "attention fix"
+ * section: scaled-dot-product attention over the same [B, H, N, d] Q/K/V
+ * layout, without materialising the B x H x N x N score matrix):
+ *
+ *   r(x)   = (mean_c x_c^2 + eps)^(-1/2),  eps = 1e-6          (per row)
+ *   q_hat  = bf16(gq * q * r(q)),  k_hat = bf16(gk * k * r(k))
+ *   S      = q_hat k_hat^T / sqrt(d)                           (per b, h)
+ *   LSE_i  = ln sum_j exp(S_ij),   O = exp(S - LSE) V
+ *
+ * Layout.  q, k, v, out, dout, dq, dk, dv are contiguous row-major
+ * [B, H, N, d] bfloat16 (stored as uint16_t bit patterns), N = N_txt + N_img
+ * with the N_txt caption rows first, then the N_img image rows.  lse is
+ * [B, H, N] float32, natural log.  gq, gk, dgq, dgk are [d] float32, one gain
+ * vector shared by all heads.  No mask, dropout or causality: N_txt and N_img
+ * only define N and the row order.
+ *
+ * Pointers.  Every array pointer is a DEVICE pointer (CUDA global memory),
+ * 16-byte aligned.  `stream` is a cudaStream_t passed as void* (NULL = the
+ * legacy default stream); all work is enqueued on it and the call returns
+ * without synchronising.  The caller owns every buffer.  The library
+ * allocates its scratch memory per call, stream-ordered on `stream`
+ * (cudaMallocAsync / cudaFreeAsync), and keeps no state between calls.
+ *
+ * Errors.  Every entry point returns a jattn_status and never aborts or
+ * prints.  Arguments are validated before anything is enqueued; a non-OK
+ * status from validation means nothing ran.  JATTN_ERR_CUDA reports a failed
+ * launch or allocation.  The kernels' internal waits are bounded: a wait
+ * that gives up ends the kernel early and jattn_last_device_error() then
+ * reports it (it synchronises `stream`).  Asynchronous faults surface, as
+ * usual in CUDA, at the caller's next synchronisation.
+ */
+#ifndef JATTN_H
+#define JATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t jattn_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+  JATTN_OK = 0,
+  JATTN_ERR_INVALID_ARG = 1, /* null pointer, B/H/d <= 0, N_img/N_txt < 0, N < 1, size overflow */
+  JATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128} */
+  JATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  JATTN_ERR_ALIAS = 4,       /* an output buffer overlaps an input or another output */
+  JATTN_ERR_CUDA = 5,        /* a CUDA launch or allocation failed */
+  JATTN_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up (reported by jattn_last_device_error) */
+} jattn_status;
+
+/*
+ * Forward.  Computes out = softmax(q_hat k_hat^T / sqrt(d)) v and lse (the
+ * natural-log row log-sum-exp of the scaled scores) for every (b, h).
+ *   q, k, v : [B, H, N, d] bf16, read only.
+ *   gq, gk  : [d] float32 RMSNorm gains for q and k, read only.
+ *   B, H    : batch size and heads (>= 1).
+ *   N_img   : image-token rows, N_txt: caption-token rows (>= 0 each,
+ *             N = N_img + N_txt >= 1).
+ *   d       : head dimension, 64 or 128.
+ *   out     : [B, H, N, d] bf16, overwritten.
+ *   lse     : [B, H, N] float32, overwritten.
+ * Limits: B*H*N*d < 2^31.
+ */
+int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+              int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse, void* stream);
+
+/*
+ * Backward.  Given the forward's inputs, its outputs (out, lse) and the
+ * upstream gradient dout, computes the gradients of L = sum(dout * out):
+ *   dq, dk, dv : [B, H, N, d] bf16, overwritten.
+ *   dgq, dgk   : [d] float32, overwritten (summed over all b, h, n).
+ * The bf16 rounding of q_hat/k_hat is treated as the identity.  The
+ * normalised q_hat/k_hat are recomputed from q, k (nothing is cached from
+ * the forward call).  dq is accumulated in float32 with atomics across key
+ * tiles, so it may differ in the last bits between runs; dk, dv, dgq and dgk
+ * are computed in a fixed order and are bitwise reproducible.
+ */
+int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+              const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq, jattn_bf16* dk,
+              jattn_bf16* dv, float* dgq, float* dgk, int B, int H, int N_img, int N_txt, int d, void* stream);
+
+/*
+ * Synchronises `stream` and returns JATTN_ERR_TIMEOUT if any kernel launched
+ * by this library on the current device since the previous call gave up a
+ * bounded wait, JATTN_ERR_CUDA if the synchronisation itself failed, else
+ * JATTN_OK.  Clears the recorded device error.
+ */
+int jattn_last_device_error(void* stream);
+
+/*
+ * Kernel timing (off by default; no counterpart on the pages: measurement
+ * support).  While enabled, every kernel launch made by jattn_fwd / jattn_bwd
+ * on the calling thread's device is bracketed by two CUDA events recorded on
+ * the caller's stream.  jattn_profile_read synchronises on those events and
+ * adds, for one kernel kind, the number of launches and their summed
+ * event-to-event milliseconds since the last jattn_profile_reset.
+ */
+typedef enum {
+  JATTN_KERNEL_QK_NORM_FWD = 0,  /* RMSNorm of q and k (forward) */
+  JATTN_KERNEL_ATTN_FWD = 1,     /* tensor-core attention forward */
+  JATTN_KERNEL_BWD_PREP = 2,     /* norm recompute + rowsum(dO*O) + dq accumulator clear */
+  JATTN_KERNEL_ATTN_BWD = 3,     /* tensor-core attention backward (+ K-norm backward) */
+  JATTN_KERNEL_Q_NORM_BWD = 4,   /* Q-norm backward from the dq accumulator */
+  JATTN_KERNEL_DG_REDUCE = 5,    /* fixed-order reduction of the gain gradients */
+  JATTN_KERNEL_COUNT = 6
+} jattn_kernel_kind;
+
+int jattn_profile_enable(int on);
+int jattn_profile_reset(void);
+int jattn_profile_read(int kind, int* launches, double* total_ms);
+const char* jattn_kernel_name(int kind);
+
+/* Static description of a status code (never NULL). */
+const char* jattn_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int jattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JATTN_H */

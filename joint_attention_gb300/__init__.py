@@ -1,0 +1,39 @@
+"""GB300-native MM-DiT joint attention with QK-RMSNorm (forward and backward).
+
+The compute path is libjattn.so (hand-written sm_103a CUDA kernels behind a C
+ABI, declared in include/jattn.h); this package is its thin ctypes binding
+plus small conveniences that allocate the output tensors with torch.
+"""
+from __future__ import annotations
+
+from ._binding import (KERNEL_KINDS, STATUS, STATUS_CODE, JattnError, declared_symbols, jattn_bwd, jattn_fwd,
+                       jattn_kernel_name, jattn_last_device_error, jattn_profile_enable, jattn_profile_read,
+                       jattn_profile_reset, jattn_status_string, jattn_version, load_library, profile_snapshot)
+
+__all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd", "jattn_fwd",
+           "jattn_last_device_error", "jattn_status_string", "jattn_version", "load_library", "forward",
+           "backward", "KERNEL_KINDS", "jattn_kernel_name", "jattn_profile_enable", "jattn_profile_read",
+           "jattn_profile_reset", "profile_snapshot"]
+
+
+def forward(q, k, v, gq, gk, n_txt: int, stream=None):
+    """out, lse = joint attention of [B, H, N, d] bf16 CUDA tensors (text rows first)."""
+    import torch
+
+    B, H, N, d = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    jattn_fwd(q, k, v, gq, gk, B, H, N - n_txt, n_txt, d, out, lse, stream)
+    return out, lse
+
+
+def backward(q, k, v, gq, gk, out, lse, dout, n_txt: int, stream=None):
+    """dq, dk, dv, dgq, dgk for the upstream gradient dout."""
+    import torch
+
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dgq = torch.empty_like(gq)
+    dgk = torch.empty_like(gk)
+    jattn_bwd(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, B, H, N - n_txt, n_txt, d, stream)
+    return dq, dk, dv, dgq, dgk

@@ -1,0 +1,188 @@
+"""ctypes binding of libjattn (include/jattn.h): argument marshalling only.
+
+Every function here forwards to the C ABI of the same name; torch tensors are
+accepted for convenience and passed as raw device pointers (torch provides
+device memory and streams, nothing else).  There is no fallback: if the
+library is missing the import of a call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+HEADER = os.path.join(ROOT, "include", "jattn.h")
+LIB_PATH = os.path.join(PKG, "libjattn.so")
+
+STATUS = {
+    0: "JATTN_OK",
+    1: "JATTN_ERR_INVALID_ARG",
+    2: "JATTN_ERR_UNSUPPORTED",
+    3: "JATTN_ERR_MISALIGNED",
+    4: "JATTN_ERR_ALIAS",
+    5: "JATTN_ERR_CUDA",
+    6: "JATTN_ERR_TIMEOUT",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+
+class JattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({jattn_status_string(status)})")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL:
+    """Loads libjattn.so (building it first only if asked)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        if build_if_missing:
+            from .build import build
+            p = build()
+        else:
+            raise FileNotFoundError(f"{p} not found: run joint_attention_gb300/build.py (or __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.jattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.jattn_fwd.restype = i32
+    lib.jattn_bwd.argtypes = [vp] * 13 + [i32] * 5 + [vp]
+    lib.jattn_bwd.restype = i32
+    lib.jattn_last_device_error.argtypes = [vp]
+    lib.jattn_last_device_error.restype = i32
+    lib.jattn_status_string.argtypes = [i32]
+    lib.jattn_status_string.restype = ctypes.c_char_p
+    lib.jattn_version.argtypes = []
+    lib.jattn_version.restype = i32
+    lib.jattn_profile_enable.argtypes = [i32]
+    lib.jattn_profile_enable.restype = i32
+    lib.jattn_profile_reset.argtypes = []
+    lib.jattn_profile_reset.restype = i32
+    lib.jattn_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
+    lib.jattn_profile_read.restype = i32
+    lib.jattn_kernel_name.argtypes = [i32]
+    lib.jattn_kernel_name.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+KERNEL_KINDS = 6
+
+
+def jattn_profile_enable(on: bool = True) -> int:
+    return load_library().jattn_profile_enable(1 if on else 0)
+
+
+def jattn_profile_reset() -> int:
+    return load_library().jattn_profile_reset()
+
+
+def jattn_profile_read(kind: int) -> tuple[int, float]:
+    """(launches, total milliseconds) of one kernel kind since the last reset."""
+    n, ms = ctypes.c_int(0), ctypes.c_double(0.0)
+    rc = load_library().jattn_profile_read(int(kind), ctypes.byref(n), ctypes.byref(ms))
+    if rc != 0:
+        raise JattnError(rc, "jattn_profile_read")
+    return n.value, ms.value
+
+
+def jattn_kernel_name(kind: int) -> str:
+    return load_library().jattn_kernel_name(int(kind)).decode()
+
+
+def profile_snapshot() -> dict:
+    """{kernel name: (launches, total ms)} for every kernel kind."""
+    return {jattn_kernel_name(k): jattn_profile_read(k) for k in range(KERNEL_KINDS)}
+
+
+def declared_symbols(header: str = HEADER) -> list[str]:
+    """Names of the functions include/jattn.h declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(jattn_\w+)\s*\(", text, flags=re.M)))
+
+
+def _ptr(x, name: str, dtype=None, numel: int | None = None):
+    """Raw pointer of a tensor (checked) or an int / None passed through."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor or an int pointer")
+    if not x.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {x.dtype}")
+    if numel is not None and x.numel() != numel:
+        raise ValueError(f"{name}: expected {numel} elements, got {x.numel()}")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def jattn_fwd(q, k, v, gq, gk, B: int, H: int, N_img: int, N_txt: int, d: int, out, lse, stream=None,
+              check: bool = True) -> int:
+    """C ABI jattn_fwd.  Tensors: q/k/v/out [B,H,N,d] bf16, gq/gk [d] fp32, lse [B,H,N] fp32."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e, r = B * H * N * d, B * H * N
+    bf, f32 = torch.bfloat16, torch.float32
+    rc = lib.jattn_fwd(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e), _ptr(gq, "gq", f32, d),
+                       _ptr(gk, "gk", f32, d), B, H, N_img, N_txt, d, _ptr(out, "out", bf, e),
+                       _ptr(lse, "lse", f32, r), _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_fwd")
+    return rc
+
+
+def jattn_bwd(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, B: int, H: int, N_img: int, N_txt: int,
+              d: int, stream=None, check: bool = True) -> int:
+    """C ABI jattn_bwd.  Gradients dq/dk/dv [B,H,N,d] bf16 and dgq/dgk [d] fp32 are overwritten."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e, r = B * H * N * d, B * H * N
+    bf, f32 = torch.bfloat16, torch.float32
+    rc = lib.jattn_bwd(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e), _ptr(gq, "gq", f32, d),
+                       _ptr(gk, "gk", f32, d), _ptr(out, "out", bf, e), _ptr(lse, "lse", f32, r),
+                       _ptr(dout, "dout", bf, e), _ptr(dq, "dq", bf, e), _ptr(dk, "dk", bf, e),
+                       _ptr(dv, "dv", bf, e), _ptr(dgq, "dgq", f32, d), _ptr(dgk, "dgk", f32, d), B, H, N_img,
+                       N_txt, d, _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_bwd")
+    return rc
+
+
+def jattn_last_device_error(stream=None) -> int:
+    return load_library().jattn_last_device_error(_stream(stream))
+
+
+def jattn_status_string(status: int) -> str:
+    return load_library().jattn_status_string(int(status)).decode()
+
+
+def jattn_version() -> int:
+    return load_library().jattn_version()

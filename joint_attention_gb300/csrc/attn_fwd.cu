@@ -1,0 +1,376 @@
+// attn_fwd.cu — softmax attention forward on tcgen05 tensor cores.
+//
+// Computes, per (b, h), O = softmax(s * q_hat k_hat^T) v and the natural-log
+// row log-sum-exp, streaming over 128-key tiles with an online softmax so the
+// N x N score matrix never leaves the SM (re-diffusion README, "attention
+// fix" section: the materialised B x 12 x 1101 x 1101 scores were the memory
+// wall; the same [B, H, N, d] Q/K/V layout goes through a fused kernel).
+//
+// One CTA owns 256 query rows of one (b, h) as two 128-row tiles A and B and
+// streams all key/value tiles of that head through a shared-memory ring:
+//
+//   warp 8      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into
+//               a ring of 128 x d bf16 slots (128-byte swizzle).
+//   warp 9      MMA issuer (one thread): S_X = Q_X K_j^T into TMEM, and
+//               O_X += P_X V_j, ordered S_A(j+1) after PV_A(j) and S_B(j+1)
+//               after PV_B(j) so each tile's softmax overlaps the other
+//               tile's MMAs.
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread
+//               per query row (TMEM lane), 128 scores per key tile; running
+//               max kept in the log2 domain and O in TMEM rescaled only when
+//               the max grows by more than 2^8 (the probabilities stay <= 256,
+//               exact in fp32 and well inside bf16 range); P is written to
+//               shared memory in the MMA's K-major swizzled layout.
+//
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+d),
+// O_B [256+d, 256+2d).  Rows past N in the last query tile read zeros (TMA
+// fill) and are not stored; key columns past N in the last key tile are
+// masked to -inf.
+#include <cuda_bf16.h>
+
+#include "jattn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace jattn {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kQTileBytes = kTileM * D * 2;
+  static constexpr int kSlotBytes = kTileN * D * 2;
+  static constexpr int kPBytes = kTileM * kTileN * 2;
+  static constexpr int kSlots = (D == 64) ? 6 : 3;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kOffQ + 2 * kQTileBytes;
+  static constexpr int kOffRing = kOffP + 2 * kPBytes;
+  static constexpr int kTileBytes = kOffRing + kSlots * kSlotBytes;
+  static constexpr int kDynSmem = kTileBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+};
+
+struct FwdBars {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t q_full;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+template <int D>
+__device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k, const CUtensorMap* map_v,
+                             uint8_t* sm, FwdBars& bars, int bh, int q0, bool hasB, int nkv, uint32_t* dev_err) {
+  using C = FwdCfg<D>;
+  tma_prefetch_desc(map_q);
+  tma_prefetch_desc(map_k);
+  tma_prefetch_desc(map_v);
+  mbar_arrive_expect_tx(&bars.q_full, (hasB ? 2u : 1u) * C::kQTileBytes);
+  for (int x = 0; x < (hasB ? 2 : 1); ++x)
+    for (int blk = 0; blk < D / 64; ++blk)
+      tma_load_3d(sm + C::kOffQ + x * C::kQTileBytes + blk * 16384, map_q, &bars.q_full, blk * 64, q0 + x * 128, bh);
+  const int total = 2 * nkv;
+  int issued = 0;
+  for (; issued < total; ++issued) {
+    const int slot = issued % C::kSlots;
+    if (issued >= C::kSlots) {
+      if (!mbar_wait(&bars.empty[slot], ((issued / C::kSlots) - 1) & 1, &bars.abort, dev_err)) break;
+    }
+    mbar_arrive_expect_tx(&bars.full[slot], C::kSlotBytes);
+    const CUtensorMap* m = (issued & 1) ? map_v : map_k;
+    const int kv0 = (issued >> 1) * kTileN;
+    for (int blk = 0; blk < D / 64; ++blk)
+      tma_load_3d(sm + C::kOffRing + slot * C::kSlotBytes + blk * 16384, m, &bars.full[slot], blk * 64, kv0, bh);
+  }
+  if (issued < total) {
+    // Aborted: let the copies already in flight land before the CTA exits.
+    mbar_wait_drain(&bars.q_full, 0);
+    for (int s = 0; s < C::kSlots; ++s) {
+      int last = -1;
+      for (int i = issued - 1; i >= 0 && i >= issued - C::kSlots; --i)
+        if (i % C::kSlots == s) { last = i; break; }
+      if (last >= 0) mbar_wait_drain(&bars.full[s], (last / C::kSlots) & 1);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+  using C = FwdCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+    umma_bf16_ss(tmem_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), C::kIdescS,
+                 kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t p_addr, uint32_t v_addr, bool accumulate) {
+  using C = FwdCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < kTileN / 16; ++kk) {
+    const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+    umma_bf16_ss(tmem_o, sdesc_sw128(p_addr + aoff, 16, 1024), sdesc_sw128(v_addr + kk * 2048, 16384, 1024),
+                 C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, int nkv, uint32_t* dev_err) {
+  using C = FwdCfg<D>;
+  const uint32_t q_addr[2] = {smem_u32(sm + C::kOffQ), smem_u32(sm + C::kOffQ + C::kQTileBytes)};
+  const uint32_t p_addr[2] = {smem_u32(sm + C::kOffP), smem_u32(sm + C::kOffP + C::kPBytes)};
+  const uint32_t ring = smem_u32(sm + C::kOffRing);
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+  auto slot_of = [](int i) { return i % C::kSlots; };
+  auto phase_of = [](int i) { return (uint32_t)((i / C::kSlots) & 1); };
+  bool ok = mbar_wait(&bars.q_full, 0, &bars.abort, dev_err);
+  if (ok) ok = mbar_wait(&bars.full[slot_of(0)], phase_of(0), &bars.abort, dev_err);
+  if (ok) {
+    tc_fence_after();
+    const uint32_t k0 = ring + slot_of(0) * C::kSlotBytes;
+    issue_qk<D>(tS[0], q_addr[0], k0);
+    umma_commit(&bars.s_full[0]);
+    if (hasB) {
+      issue_qk<D>(tS[1], q_addr[1], k0);
+      umma_commit(&bars.s_full[1]);
+    }
+    umma_commit(&bars.empty[slot_of(0)]);
+  }
+  for (int j = 0; ok && j < nkv; ++j) {
+    const int iv = 2 * j + 1, ik = 2 * j + 2;
+    const uint32_t v_addr = ring + slot_of(iv) * C::kSlotBytes;
+    const uint32_t kn_addr = ring + slot_of(ik) * C::kSlotBytes;
+    if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), &bars.abort, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.p_full[0], j & 1, &bars.abort, dev_err))) break;
+    tc_fence_after();
+    issue_pv<D>(tO[0], p_addr[0], v_addr, j > 0);
+    if (j == nkv - 1) umma_commit(&bars.o_done[0]);
+    if (j + 1 < nkv) {
+      if (!(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), &bars.abort, dev_err))) break;
+      tc_fence_after();
+      issue_qk<D>(tS[0], q_addr[0], kn_addr);
+      umma_commit(&bars.s_full[0]);
+    }
+    if (hasB) {
+      if (!(ok = mbar_wait(&bars.p_full[1], j & 1, &bars.abort, dev_err))) break;
+      tc_fence_after();
+      issue_pv<D>(tO[1], p_addr[1], v_addr, j > 0);
+      if (j == nkv - 1) umma_commit(&bars.o_done[1]);
+    }
+    umma_commit(&bars.empty[slot_of(iv)]);
+    if (j + 1 < nkv) {
+      if (hasB) {
+        issue_qk<D>(tS[1], q_addr[1], kn_addr);
+        umma_commit(&bars.s_full[1]);
+      }
+      umma_commit(&bars.empty[slot_of(ik)]);
+    }
+  }
+  // Every MMA issued above has completed once this barrier flips.
+  umma_commit(&bars.drain);
+  mbar_wait_drain(&bars.drain, 0);
+}
+
+// Softmax / epilogue of one 128-row query tile (x = 0: tile A, 1: tile B).
+template <int D>
+__device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int bh, int q0, int N, int nkv,
+                            float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                            uint32_t* dev_err) {
+  using C = FwdCfg<D>;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wq = warp & 3;
+  const int row = wq * 32 + lane;
+  const int n = q0 + x * 128 + row;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_base + x * 128;
+  const uint32_t tO = tmem + lane_base + 256 + x * D;
+  const uint32_t p_row = smem_u32(sm + C::kOffP + x * C::kPBytes) + row * 128;
+  const uint32_t swz = static_cast<uint32_t>(row & 7);
+
+  float m_ref = -INFINITY;
+  float l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    ok = mbar_wait(&bars.s_full[x], j & 1, &bars.abort, dev_err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t s[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+    tmem_wait_ld();
+    const int nvalid = N - j * kTileN;
+    if (nvalid < kTileN) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e >= nvalid) s[c][e] = __float_as_uint(-INFINITY);
+    }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(s[c][e]));
+    const float m_tile = mt * scale_log2;
+    const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
+    const bool need = (m_new != m_ref) && (j > 0);
+    const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(tO + c * 32, o);
+      }
+      tmem_wait_st();
+    }
+    l *= alpha;
+    m_ref = m_new;
+    const float neg_m = -m_ref;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {  // 8 columns = one 16-byte chunk
+        uint32_t packed[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][g * 8 + 2 * h]), scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][g * 8 + 2 * h + 1]), scale_log2, neg_m));
+          l += p0 + p1;
+          packed[h] = pack_bf16x2(p0, p1);
+        }
+        const int col = c * 32 + g * 8;           // first key column of the chunk
+        const uint32_t blk = col >> 6;            // 64-column block
+        const uint32_t chunk = (col & 63) >> 3;   // 16-byte chunk in the 128-byte row
+        st_shared_v4(p_row + blk * 16384 + ((chunk ^ swz) << 4), packed[0], packed[1], packed[2], packed[3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&bars.p_full[x]);
+  }
+  if (!ok) return;
+  ok = mbar_wait(&bars.o_done[x], 0, &bars.abort, dev_err);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return;
+  tc_fence_after();
+  const float inv_l = 1.f / l;
+  const bool live = n < N;
+  uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + (live ? n : 0)) * D);
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld();
+    if (live) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l);
+        w.y = pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l);
+        w.z = pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l);
+        w.w = pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l);
+        orow[c * 4 + g] = w;
+      }
+    }
+  }
+  if (live) lse[static_cast<size_t>(bh) * N + n] = (m_ref + log2f(l)) * kLn2;
+}
+
+template <int D>
+__global__ void __maxnreg__(200)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, int N, float scale_log2,
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ FwdBars bars;
+  uint8_t* sm = align1024(smem_raw);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.y;
+  const int q0 = blockIdx.x * 2 * kTileM;
+  const bool hasB = q0 + kTileM < N;
+  const int nkv = (N + kTileN - 1) / kTileN;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(&bars.full[i], 1);
+      mbar_init(&bars.empty[i], 1);
+    }
+    mbar_init(&bars.q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.p_full[x], 128);
+      mbar_init(&bars.o_done[x], 1);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 8) {
+    if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, bh, q0, hasB, nkv, dev_err);
+  } else if (warp == 9) {
+    if (lane == 0) fwd_mma<D>(sm, bars, tmem, hasB, nkv, dev_err);
+  } else {
+    const int x = warp >> 2;
+    if (x == 0 || hasB) fwd_softmax<D>(sm, bars, tmem, x, bh, q0, N, nkv, scale_log2, out, lse, dev_err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnShape& s,
+                         uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  static_assert(C::kDynSmem + static_cast<int>(sizeof(FwdBars)) <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((s.N + 2 * kTileM - 1) / (2 * kTileM), s.BH);
+  const float scale_log2 = s.scale * 1.4426950408889634f;
+  attn_fwd_kernel<D><<<grid, kFwdThreads, C::kDynSmem, st>>>(mq, mk, mv, s.N, scale_log2,
+                                                             reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
+                            const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
+  if (s.d == 64) return launch_fwd_d<64>(map_q, map_k, map_v, s, out, lse, dev_err, st);
+  if (s.d == 128) return launch_fwd_d<128>(map_q, map_k, map_v, s, out, lse, dev_err, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace jattn

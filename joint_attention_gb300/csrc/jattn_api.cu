@@ -1,0 +1,400 @@
+// jattn_api.cu — the C ABI of libjattn (declared in include/jattn.h):
+// argument validation, per-call scratch, TMA tensor maps and the launch
+// sequence of the forward and backward passes.
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "jattn.h"
+#include "jattn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace jattn {
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+
+// Device error word written by the kernels' bounded waits (one per device).
+__device__ uint32_t g_dev_err;
+
+uint32_t* dev_err_ptr() {
+  static uint32_t* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel timing: CUDA event pairs around each launch while enabled.
+// ---------------------------------------------------------------------------
+struct Prof {
+  std::mutex mu;
+  bool on = false;
+  struct Rec {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+  long long launches[JATTN_KERNEL_COUNT] = {0};
+  double ms[JATTN_KERNEL_COUNT] = {0};
+
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+};
+Prof& prof() {
+  static Prof p;
+  return p;
+}
+
+// Brackets one launch; a no-op unless timing is enabled.
+class Timed {
+ public:
+  Timed(int kind, cudaStream_t st) : kind_(kind), st_(st) {
+    Prof& p = prof();
+    std::lock_guard<std::mutex> lock(p.mu);
+    if (!p.on) return;
+    a_ = p.get();
+    b_ = p.get();
+    if (a_ && b_) cudaEventRecord(a_, st_);
+  }
+  ~Timed() {
+    if (!a_ || !b_) return;
+    cudaEventRecord(b_, st_);
+    Prof& p = prof();
+    std::lock_guard<std::mutex> lock(p.mu);
+    p.pending.push_back({kind_, a_, b_});
+  }
+
+ private:
+  int kind_;
+  cudaStream_t st_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range range_of(const void* p, size_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + bytes};
+}
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Shape {
+  int B, H, N, d, BH, n_pad;
+  size_t rows;   // BH * N
+  size_t elems;  // BH * N * d
+};
+
+int check_shape(int B, int H, int N_img, int N_txt, int d, Shape* s) {
+  if (B <= 0 || H <= 0 || d <= 0 || N_img < 0 || N_txt < 0) return JATTN_ERR_INVALID_ARG;
+  const int64_t N = static_cast<int64_t>(N_img) + N_txt;
+  if (N < 1) return JATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return JATTN_ERR_UNSUPPORTED;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > 65535) return JATTN_ERR_INVALID_ARG;  // grid y extent
+  const int64_t elems = BH * N * d;
+  if (elems >= (int64_t{1} << 31)) return JATTN_ERR_INVALID_ARG;
+  s->B = B;
+  s->H = H;
+  s->N = static_cast<int>(N);
+  s->d = d;
+  s->BH = static_cast<int>(BH);
+  s->n_pad = static_cast<int>((N + 127) / 128 * 128);
+  s->rows = static_cast<size_t>(BH * N);
+  s->elems = static_cast<size_t>(elems);
+  return JATTN_OK;
+}
+
+// Bump allocator over one stream-ordered allocation.
+struct Carve {
+  uint8_t* base = nullptr;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    T* p = reinterpret_cast<T*>(base + off);
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+size_t fwd_scratch_bytes(const Shape& s) { return 2 * (s.elems * 2 + 256) + 256; }
+
+size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
+  size_t b = 0;
+  b += 2 * (s.elems * 2 + 256);                                   // q_hat, k_hat
+  b += 2 * (s.rows * 4 + 256);                                    // rq, rk
+  b += 2 * (static_cast<size_t>(s.BH) * s.n_pad * 4 + 256);       // lse2, delta
+  b += s.elems * 4 + 256;                                         // dq accumulator
+  b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
+  return b + 256;
+}
+
+}  // namespace
+
+bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace jattn
+
+using namespace jattn;
+
+extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                         const float* gk, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse,
+                         void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  const void* ptrs[] = {q, k, v, gq, gk, out, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
+  const size_t tb = s.elems * 2;
+  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(gq, s.d * 4),
+                       range_of(gk, s.d * 4)};
+  const Range outs[] = {range_of(out, tb), range_of(lse, s.rows * 4)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlaps(o, i)) return JATTN_ERR_ALIAS;
+  if (overlaps(outs[0], outs[1])) return JATTN_ERR_ALIAS;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = dev_err_ptr();
+  if (!err) return JATTN_ERR_CUDA;
+  Carve cv;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&cv.base), fwd_scratch_bytes(s), st) != cudaSuccess)
+    return JATTN_ERR_CUDA;
+  uint16_t* qhat = cv.take<uint16_t>(s.elems);
+  uint16_t* khat = cv.take<uint16_t>(s.elems);
+  int status = JATTN_OK;
+  CUtensorMap mq, mk, mv;
+  cudaError_t ce;
+  {
+    Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
+    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, st);
+  }
+  if (ce != cudaSuccess) {
+    status = JATTN_ERR_CUDA;
+  } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
+             !encode_bhnd_map(&mv, v, s.BH, s.N, s.d)) {
+    status = JATTN_ERR_CUDA;
+  } else {
+    AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
+    Timed t(JATTN_KERNEL_ATTN_FWD, st);
+    if (launch_attn_fwd(mq, mk, mv, as, out, lse, err, st) != cudaSuccess) status = JATTN_ERR_CUDA;
+  }
+  if (cudaFreeAsync(cv.base, st) != cudaSuccess) status = JATTN_ERR_CUDA;
+  return status;
+}
+
+extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                         const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
+                         jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, int B, int H,
+                         int N_img, int N_txt, int d, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !dq || !dk || !dv || !dgq || !dgk)
+    return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  const void* ptrs[] = {q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
+  const size_t tb = s.elems * 2;
+  const size_t gb = static_cast<size_t>(s.d) * 4;
+  const Range ins[] = {range_of(q, tb),  range_of(k, tb),   range_of(v, tb),           range_of(gq, gb),
+                       range_of(gk, gb), range_of(out, tb), range_of(lse, s.rows * 4), range_of(dout, tb)};
+  const Range outs[] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb), range_of(dgq, gb), range_of(dgk, gb)};
+  for (size_t a = 0; a < sizeof(outs) / sizeof(outs[0]); ++a) {
+    for (const Range& i : ins)
+      if (overlaps(outs[a], i)) return JATTN_ERR_ALIAS;
+    for (size_t b = a + 1; b < sizeof(outs) / sizeof(outs[0]); ++b)
+      if (overlaps(outs[a], outs[b])) return JATTN_ERR_ALIAS;
+  }
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = dev_err_ptr();
+  if (!err) return JATTN_ERR_CUDA;
+  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
+  const int nparts_q = q_norm_bwd_parts();
+  const int nparts_k = attn_bwd_dgk_parts(as);
+  Carve cv;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k), st) !=
+      cudaSuccess)
+    return JATTN_ERR_CUDA;
+  uint16_t* qhat = cv.take<uint16_t>(s.elems);
+  uint16_t* khat = cv.take<uint16_t>(s.elems);
+  float* rq = cv.take<float>(s.rows);
+  float* rk = cv.take<float>(s.rows);
+  float* lse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
+  float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
+  float* dqacc = cv.take<float>(s.elems);
+  float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
+  float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
+
+  int status = JATTN_OK;
+  CUtensorMap mq, mk, mv, mdo;
+  cudaError_t ce;
+  {
+    Timed t(JATTN_KERNEL_BWD_PREP, st);
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, lse2, delta, dqacc, s.BH, s.N, s.n_pad,
+                         s.d, st);
+  }
+  if (ce != cudaSuccess) {
+    status = JATTN_ERR_CUDA;
+  } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
+             !encode_bhnd_map(&mv, v, s.BH, s.N, s.d) || !encode_bhnd_map(&mdo, dout, s.BH, s.N, s.d)) {
+    status = JATTN_ERR_CUDA;
+  } else {
+    {
+      Timed t(JATTN_KERNEL_ATTN_BWD, st);
+      ce = launch_attn_bwd(mq, mk, mv, mdo, as, lse2, delta, k, rk, gk, dk, dv, dqacc, dgk_part, err, st);
+    }
+    if (ce == cudaSuccess) {
+      Timed t(JATTN_KERNEL_Q_NORM_BWD, st);
+      ce = launch_q_norm_bwd(dqacc, q, rq, gq, as.scale, dq, dgq_part, nparts_q, static_cast<int64_t>(s.rows), s.d,
+                             st);
+    }
+    if (ce == cudaSuccess) {
+      Timed t(JATTN_KERNEL_DG_REDUCE, st);
+      ce = launch_dg_reduce(dgq_part, nparts_q, dgk_part, nparts_k, s.d, dgq, dgk, st);
+    }
+    if (ce != cudaSuccess) status = JATTN_ERR_CUDA;
+  }
+  if (cudaFreeAsync(cv.base, st) != cudaSuccess) status = JATTN_ERR_CUDA;
+  return status;
+}
+
+extern "C" int jattn_last_device_error(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return JATTN_ERR_CUDA;
+  uint32_t* p = dev_err_ptr();
+  if (!p) return JATTN_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return JATTN_ERR_CUDA;
+  if (v == 0) return JATTN_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return JATTN_ERR_CUDA;
+  return (v & DEV_ERR_WAIT_TIMEOUT) ? JATTN_ERR_TIMEOUT : JATTN_ERR_CUDA;
+}
+
+extern "C" int jattn_profile_enable(int on) {
+  Prof& p = prof();
+  std::lock_guard<std::mutex> lock(p.mu);
+  p.on = on != 0;
+  return JATTN_OK;
+}
+
+extern "C" int jattn_profile_reset(void) {
+  Prof& p = prof();
+  std::lock_guard<std::mutex> lock(p.mu);
+  int status = JATTN_OK;
+  for (auto& r : p.pending) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) status = JATTN_ERR_CUDA;
+    p.pool.push_back(r.a);
+    p.pool.push_back(r.b);
+  }
+  p.pending.clear();
+  for (int i = 0; i < JATTN_KERNEL_COUNT; ++i) {
+    p.launches[i] = 0;
+    p.ms[i] = 0;
+  }
+  return status;
+}
+
+extern "C" int jattn_profile_read(int kind, int* launches, double* total_ms) {
+  if (kind < 0 || kind >= JATTN_KERNEL_COUNT || !launches || !total_ms) return JATTN_ERR_INVALID_ARG;
+  Prof& p = prof();
+  std::lock_guard<std::mutex> lock(p.mu);
+  int status = JATTN_OK;
+  for (auto& r : p.pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      status = JATTN_ERR_CUDA;
+    } else {
+      p.launches[r.kind] += 1;
+      p.ms[r.kind] += ms;
+    }
+    p.pool.push_back(r.a);
+    p.pool.push_back(r.b);
+  }
+  p.pending.clear();
+  *launches = static_cast<int>(p.launches[kind]);
+  *total_ms = p.ms[kind];
+  return status;
+}
+
+extern "C" const char* jattn_kernel_name(int kind) {
+  switch (kind) {
+    case JATTN_KERNEL_QK_NORM_FWD: return "qk_norm_fwd";
+    case JATTN_KERNEL_ATTN_FWD: return "attn_fwd";
+    case JATTN_KERNEL_BWD_PREP: return "bwd_prep";
+    case JATTN_KERNEL_ATTN_BWD: return "attn_bwd";
+    case JATTN_KERNEL_Q_NORM_BWD: return "q_norm_bwd";
+    case JATTN_KERNEL_DG_REDUCE: return "dg_reduce";
+    default: return "unknown";
+  }
+}
+
+extern "C" const char* jattn_status_string(int status) {
+  switch (status) {
+    case JATTN_OK: return "ok";
+    case JATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive or overflowing size)";
+    case JATTN_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 64 or 128)";
+    case JATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case JATTN_ERR_ALIAS: return "an output buffer overlaps another buffer";
+    case JATTN_ERR_CUDA: return "CUDA launch or allocation failed";
+    case JATTN_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int jattn_version(void) { return kVersion; }

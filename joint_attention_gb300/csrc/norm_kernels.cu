@@ -1,0 +1,299 @@
+// norm_kernels.cu — the HBM-bound steps around the attention kernels.
+//
+// QK-RMSNorm (re-diffusion README, "design notes" table, row "QK norm":
+// RMSNorm on Q and K): per row of d values,
+//     r = (mean_c x_c^2 + eps)^(-1/2),   x_hat = g * x * r  (rounded to bf16)
+// and its gradient with u = g * dx_hat:
+//     dx = r * u - (r^3 / d) * x * sum_c(u_c x_c),   dg = sum_rows dx_hat * x * r.
+//
+// Row layout: every row is d contiguous values, d/8 threads per row, each
+// thread holding one 16-byte chunk (8 bf16) so global accesses are fully
+// coalesced 16-byte vectors; the row reduction is a shuffle within the
+// d/8-lane group.  Grids are a multiple of the SM count and stride over rows.
+#include <cuda_bf16.h>
+
+#include "jattn_internal.h"
+
+namespace jattn {
+namespace {
+
+constexpr float kEps = 1e-6f;
+constexpr int kNormThreads = 256;
+
+__device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+  return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+}
+// Sum over the TPR lanes that share a row (TPR = d/8 = 8 or 16).
+template <int TPR>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = TPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Normalises one 8-element chunk of a row; returns r through *r_out.
+template <int TPR>
+__device__ __forceinline__ uint4 norm_chunk(const uint4 w, const float (&g)[8], float* r_out) {
+  float x[8];
+  unpack8(w, x);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+  ss = row_sum<TPR>(ss);
+  const float r = rsqrtf(ss * (1.f / (TPR * 8)) + kEps);
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = g[i] * x[i] * r;
+  *r_out = r;
+  return pack8(y);
+}
+
+// q, k -> q_hat, k_hat (bf16).  Rows [0, rows) are q rows, [rows, 2 rows) k rows.
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* __restrict__ q,
+                                                                   const uint4* __restrict__ k,
+                                                                   const float* __restrict__ gq,
+                                                                   const float* __restrict__ gk,
+                                                                   uint4* __restrict__ qhat,
+                                                                   uint4* __restrict__ khat, int64_t rows) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = kNormThreads / TPR;  // rows per block per iteration
+  const int sub = threadIdx.x % TPR;
+  float g_q[8], g_k[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    g_q[i] = gq[sub * 8 + i];
+    g_k[i] = gk[sub * 8 + i];
+  }
+  const int64_t total = 2 * rows;
+  // The loop bound is block-uniform so every lane reaches the row shuffles.
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < total;
+       base += static_cast<int64_t>(gridDim.x) * RPB) {
+    const int64_t rr = base + threadIdx.x / TPR;
+    const bool valid = rr < total;
+    const bool is_k = rr >= rows;
+    const int64_t idx = (is_k ? rr - rows : rr) * TPR + sub;
+    const uint4 w = valid ? (is_k ? k[idx] : q[idx]) : make_uint4(0u, 0u, 0u, 0u);
+    float g[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = is_k ? g_k[i] : g_q[i];
+    float r;
+    const uint4 y = norm_chunk<TPR>(w, g, &r);
+    if (valid) (is_k ? khat : qhat)[idx] = y;
+  }
+}
+
+// Backward preparation, one pass over the padded rows (bh, n), n < n_pad:
+// for n < N it writes q_hat, k_hat, 1/rms of q and k, D = rowsum(dout * out),
+// LSE in the log2 domain and a zeroed fp32 dq accumulator row; pad rows get
+// LSE = +inf and D = 0 so the attention backward sees zero probabilities.
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
+    const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
+    const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
+    const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
+    float* __restrict__ rk, float* __restrict__ lse2, float* __restrict__ delta, float4* __restrict__ dqacc,
+    int N, int n_pad, int64_t padded_rows) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = kNormThreads / TPR;
+  const int sub = threadIdx.x % TPR;
+  float g_q[8], g_k[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    g_q[i] = gq[sub * 8 + i];
+    g_k[i] = gk[sub * 8 + i];
+  }
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < padded_rows;
+       base += static_cast<int64_t>(gridDim.x) * RPB) {
+    const int64_t prow = base + threadIdx.x / TPR;
+    const int64_t bh = prow / n_pad;
+    const int n = static_cast<int>(prow - bh * n_pad);
+    const bool in_range = prow < padded_rows;
+    const bool valid = in_range && n < N;
+    const int64_t row = bh * N + n;
+    const int64_t idx = (valid ? row : 0) * TPR + sub;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 wq = valid ? q[idx] : zero, wk = valid ? k[idx] : zero;
+    const uint4 wo = valid ? out[idx] : zero, wd = valid ? dout[idx] : zero;
+    float r1, r2;
+    const uint4 yq = norm_chunk<TPR>(wq, g_q, &r1);
+    const uint4 yk = norm_chunk<TPR>(wk, g_k, &r2);
+    float o[8], dd[8];
+    unpack8(wo, o);
+    unpack8(wd, dd);
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dot = fmaf(o[i], dd[i], dot);
+    dot = row_sum<TPR>(dot);
+    if (!in_range) continue;
+    if (sub == 0) {
+      lse2[prow] = valid ? lse[row] * 1.4426950408889634f : INFINITY;
+      delta[prow] = valid ? dot : 0.f;
+    }
+    if (!valid) continue;
+    qhat[idx] = yq;
+    khat[idx] = yk;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    dqacc[idx * 2] = z;
+    dqacc[idx * 2 + 1] = z;
+    if (sub == 0) {
+      rq[row] = r1;
+      rk[row] = r2;
+    }
+  }
+}
+
+// dq from the fp32 accumulator of dS k_hat (times `scale`), plus per-block
+// partial sums of dgq.  Each block writes partial[blockIdx.x][d]; the grid
+// size is fixed, so the reduction order is fixed.
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* __restrict__ dqacc,
+                                                                  const uint4* __restrict__ q,
+                                                                  const float* __restrict__ rq,
+                                                                  const float* __restrict__ gq, float scale,
+                                                                  uint4* __restrict__ dq,
+                                                                  float* __restrict__ partial, int64_t rows) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = kNormThreads / TPR;
+  const int sub = threadIdx.x % TPR;
+  float g[8], acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    g[i] = gq[sub * 8 + i];
+    acc[i] = 0.f;
+  }
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < rows;
+       base += static_cast<int64_t>(gridDim.x) * RPB) {
+    const int64_t row = base + threadIdx.x / TPR;
+    const bool valid = row < rows;
+    const int64_t idx = (valid ? row : 0) * TPR + sub;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 a = valid ? dqacc[idx * 2] : z4, b = valid ? dqacc[idx * 2 + 1] : z4;
+    const float dh[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
+                         b.x * scale, b.y * scale, b.z * scale, b.w * scale};
+    float x[8];
+    unpack8(valid ? q[idx] : make_uint4(0u, 0u, 0u, 0u), x);
+    const float r = valid ? rq[row] : 0.f;
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dot = fmaf(g[i] * dh[i], x[i], dot);
+    dot = row_sum<TPR>(dot);
+    const float c = r * r * r * (1.f / D) * dot;
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[i] = r * g[i] * dh[i] - c * x[i];
+      acc[i] = fmaf(dh[i], x[i] * r, acc[i]);
+    }
+    if (valid) dq[idx] = pack8(y);
+  }
+  // Block reduction of acc over the RPB row slots (fixed order).
+  __shared__ float red[kNormThreads / TPR][D];
+  const int slot = threadIdx.x / TPR;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[slot][sub * 8 + i] = acc[i];
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float s = 0.f;
+    for (int t = 0; t < RPB; ++t) s += red[t][c];
+    partial[static_cast<size_t>(blockIdx.x) * D + c] = s;
+  }
+}
+
+// Block 0 reduces the dgq partials, block 1 the dgk partials; one thread per
+// column, partials summed in index order.
+__global__ void dg_reduce_kernel(const float* __restrict__ part_q, int nq, const float* __restrict__ part_k, int nk,
+                                 int d, float* __restrict__ dgq, float* __restrict__ dgk) {
+  const int c = threadIdx.x;
+  if (c >= d) return;
+  const float* part = blockIdx.x == 0 ? part_q : part_k;
+  const int nparts = blockIdx.x == 0 ? nq : nk;
+  float s = 0.f;
+  for (int p = 0; p < nparts; ++p) s += part[static_cast<size_t>(p) * d + c];
+  (blockIdx.x == 0 ? dgq : dgk)[c] = s;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  }
+  return n;
+}
+
+int row_grid(int64_t rows, int d) {
+  const int64_t rpb = kNormThreads / (d / 8);
+  const int64_t need = (rows + rpb - 1) / rpb;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+}  // namespace
+
+int q_norm_bwd_parts() { return sm_count() * 4; }
+
+cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
+                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, cudaStream_t st) {
+  const int grid = row_grid(2 * rows, d);
+  auto* a = reinterpret_cast<const uint4*>(q);
+  auto* b = reinterpret_cast<const uint4*>(k);
+  if (d == 64)
+    qk_norm_fwd_kernel<64><<<grid, kNormThreads, 0, st>>>(a, b, gq, gk, reinterpret_cast<uint4*>(qhat),
+                                                           reinterpret_cast<uint4*>(khat), rows);
+  else
+    qk_norm_fwd_kernel<128><<<grid, kNormThreads, 0, st>>>(a, b, gq, gk, reinterpret_cast<uint4*>(qhat),
+                                                            reinterpret_cast<uint4*>(khat), rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
+                            const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
+                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc, int BH,
+                            int N, int n_pad, int d, cudaStream_t st) {
+  const int64_t padded_rows = static_cast<int64_t>(BH) * n_pad;
+  const int grid = row_grid(padded_rows, d);
+  auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
+  if (d == 64)
+    bwd_prep_kernel<64><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
+                                                        reinterpret_cast<uint4*>(qhat),
+                                                        reinterpret_cast<uint4*>(khat), rq, rk, lse2, delta,
+                                                        reinterpret_cast<float4*>(dqacc), N, n_pad, padded_rows);
+  else
+    bwd_prep_kernel<128><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
+                                                         reinterpret_cast<uint4*>(qhat),
+                                                         reinterpret_cast<uint4*>(khat), rq, rk, lse2, delta,
+                                                         reinterpret_cast<float4*>(dqacc), N, n_pad, padded_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
+                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, cudaStream_t st) {
+  auto* a = reinterpret_cast<const float4*>(dqacc);
+  auto* x = reinterpret_cast<const uint4*>(q);
+  auto* y = reinterpret_cast<uint4*>(dq);
+  if (d == 64) q_norm_bwd_kernel<64><<<nparts, kNormThreads, 0, st>>>(a, x, rq, gq, scale, y, dgq_part, rows);
+  else q_norm_bwd_kernel<128><<<nparts, kNormThreads, 0, st>>>(a, x, rq, gq, scale, y, dgq_part, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* dgq, float* dgk,
+                             cudaStream_t st) {
+  dg_reduce_kernel<<<2, 128, 0, st>>>(part_q, nq, part_k, nk, d, dgq, dgk);
+  return cudaGetLastError();
+}
+
+}  // namespace jattn

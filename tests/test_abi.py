@@ -1,0 +1,100 @@
+"""The C ABI library: builds, loads, exports every declared symbol, and rejects
+bad arguments before touching the GPU (these calls never reach CUDA, so they
+run on a machine without one)."""
+import pytest
+
+import joint_attention_gb300 as ja
+from joint_attention_gb300 import STATUS_CODE
+from joint_attention_gb300.build import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return ja.load_library()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = ja.declared_symbols()
+    assert {"jattn_fwd", "jattn_bwd", "jattn_last_device_error", "jattn_status_string",
+            "jattn_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_kernel_names_and_profile_argument_checks(lib):
+    names = [ja.jattn_kernel_name(k) for k in range(ja.KERNEL_KINDS)]
+    assert names == ["qk_norm_fwd", "attn_fwd", "bwd_prep", "attn_bwd", "q_norm_bwd", "dg_reduce"]
+    assert ja.jattn_kernel_name(ja.KERNEL_KINDS) == "unknown"
+    import ctypes
+    n, ms = ctypes.c_int(0), ctypes.c_double(0)
+    assert lib.jattn_profile_read(-1, ctypes.byref(n), ctypes.byref(ms)) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]
+    assert lib.jattn_profile_read(0, None, None) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]
+
+
+def test_version_and_status_strings(lib):
+    assert ja.jattn_version() >= 100
+    for code in range(7):
+        s = ja.jattn_status_string(code)
+        assert isinstance(s, str) and s
+    assert ja.jattn_status_string(99) == "unknown status"
+
+
+# Fake, never-dereferenced device addresses: validation happens first.
+A = 0x7F0000000000
+
+
+def fwd(lib, q=A, k=A + 0x1000000, v=A + 0x2000000, gq=A + 0x3000000, gk=A + 0x3001000, B=1, H=2, N_img=16,
+        N_txt=8, d=64, out=A + 0x4000000, lse=A + 0x5000000):
+    return lib.jattn_fwd(q, k, v, gq, gk, B, H, N_img, N_txt, d, out, lse, None)
+
+
+def bwd(lib, **kw):
+    p = dict(q=A, k=A + 0x1000000, v=A + 0x2000000, gq=A + 0x3000000, gk=A + 0x3001000, out=A + 0x4000000,
+             lse=A + 0x5000000, dout=A + 0x6000000, dq=A + 0x7000000, dk=A + 0x8000000, dv=A + 0x9000000,
+             dgq=A + 0xA000000, dgk=A + 0xA001000, B=1, H=2, N_img=16, N_txt=8, d=64)
+    p.update(kw)
+    return lib.jattn_bwd(p["q"], p["k"], p["v"], p["gq"], p["gk"], p["out"], p["lse"], p["dout"], p["dq"], p["dk"],
+                         p["dv"], p["dgq"], p["dgk"], p["B"], p["H"], p["N_img"], p["N_txt"], p["d"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), "JATTN_ERR_INVALID_ARG"),
+    (dict(lse=None), "JATTN_ERR_INVALID_ARG"),
+    (dict(B=0), "JATTN_ERR_INVALID_ARG"),
+    (dict(H=-1), "JATTN_ERR_INVALID_ARG"),
+    (dict(N_img=-1), "JATTN_ERR_INVALID_ARG"),
+    (dict(N_img=0, N_txt=0), "JATTN_ERR_INVALID_ARG"),
+    (dict(d=0), "JATTN_ERR_INVALID_ARG"),
+    (dict(d=96), "JATTN_ERR_UNSUPPORTED"),
+    (dict(d=256), "JATTN_ERR_UNSUPPORTED"),
+    (dict(B=65536, H=2), "JATTN_ERR_INVALID_ARG"),
+    (dict(B=1000, H=16, N_img=2000, N_txt=77, d=128), "JATTN_ERR_INVALID_ARG"),
+    (dict(q=A + 8), "JATTN_ERR_MISALIGNED"),
+    (dict(gk=A + 0x3001004), "JATTN_ERR_MISALIGNED"),
+    (dict(out=A + 0x1000000), "JATTN_ERR_ALIAS"),           # out == k
+    (dict(lse=A + 0x4000000 + 0x100), "JATTN_ERR_ALIAS"),   # lse inside out
+    (dict(out=A + 0x3000000 - 0x10), "JATTN_ERR_ALIAS"),    # out runs into gq
+])
+def test_fwd_validation(lib, kw, expect):
+    assert fwd(lib, **kw) == STATUS_CODE[expect]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dout=None), "JATTN_ERR_INVALID_ARG"),
+    (dict(dgk=None), "JATTN_ERR_INVALID_ARG"),
+    (dict(N_txt=-5), "JATTN_ERR_INVALID_ARG"),
+    (dict(d=32), "JATTN_ERR_UNSUPPORTED"),
+    (dict(dv=A + 0x9000002), "JATTN_ERR_MISALIGNED"),
+    (dict(dq=A), "JATTN_ERR_ALIAS"),                        # dq == q
+    (dict(dk=A + 0x7000000 + 0x400), "JATTN_ERR_ALIAS"),    # dk inside dq
+    (dict(dgq=A + 0xA001000), "JATTN_ERR_ALIAS"),           # dgq == dgk
+    (dict(dgq=A + 0x5000000), "JATTN_ERR_ALIAS"),           # dgq == lse
+])
+def test_bwd_validation(lib, kw, expect):
+    assert bwd(lib, **kw) == STATUS_CODE[expect]
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        ja.load_library(str(tmp_path / "missing.so"))
