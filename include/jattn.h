@@ -122,6 +122,10 @@ const char* jattn_kernel_name(int kind);
 /* Static description of a status code (never NULL). */
 const char* jattn_status_string(int status);
 
+/* Human-readable detail of the last failing CUDA call or driver step seen
+ * by an entry point on the calling thread (never NULL). */
+const char* jattn_last_error_message(void);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int jattn_version(void);
 

@@ -31,7 +31,9 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 class JattnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)} ({jattn_status_string(status)})")
+        detail = jattn_last_error_message() if status == 5 else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({jattn_status_string(status)})"
+                         + (f" [{detail}]" if detail else ""))
 
 
 _lib = None
@@ -61,6 +63,8 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     lib.jattn_status_string.restype = ctypes.c_char_p
     lib.jattn_version.argtypes = []
     lib.jattn_version.restype = i32
+    lib.jattn_last_error_message.argtypes = []
+    lib.jattn_last_error_message.restype = ctypes.c_char_p
     lib.jattn_profile_enable.argtypes = [i32]
     lib.jattn_profile_enable.restype = i32
     lib.jattn_profile_reset.argtypes = []
@@ -182,6 +186,10 @@ def jattn_last_device_error(stream=None) -> int:
 
 def jattn_status_string(status: int) -> str:
     return load_library().jattn_status_string(int(status)).decode()
+
+
+def jattn_last_error_message() -> str:
+    return load_library().jattn_last_error_message().decode()
 
 
 def jattn_version() -> int:

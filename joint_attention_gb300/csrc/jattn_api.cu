@@ -3,6 +3,7 @@
 // sequence of the forward and backward passes.
 #include <cstddef>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -23,6 +24,17 @@ constexpr int kMaxDevices = 64;
 
 // Device error word written by the kernels' bounded waits (one per device).
 __device__ uint32_t g_dev_err;
+
+// Text of the last failure seen by an entry point on this thread.
+thread_local char g_last_msg[256] = "no error";
+
+int fail(int status, const char* where, cudaError_t e = cudaSuccess) {
+  if (e != cudaSuccess)
+    snprintf(g_last_msg, sizeof(g_last_msg), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  else
+    snprintf(g_last_msg, sizeof(g_last_msg), "%s", where);
+  return status;
+}
 
 uint32_t* dev_err_ptr() {
   static uint32_t* ptrs[kMaxDevices] = {nullptr};
@@ -209,30 +221,31 @@ extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = dev_err_ptr();
-  if (!err) return JATTN_ERR_CUDA;
+  if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
   Carve cv;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&cv.base), fwd_scratch_bytes(s), st) != cudaSuccess)
-    return JATTN_ERR_CUDA;
+  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), fwd_scratch_bytes(s), st);
+  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
   uint16_t* qhat = cv.take<uint16_t>(s.elems);
   uint16_t* khat = cv.take<uint16_t>(s.elems);
   int status = JATTN_OK;
   CUtensorMap mq, mk, mv;
-  cudaError_t ce;
   {
     Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
     ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, st);
   }
   if (ce != cudaSuccess) {
-    status = JATTN_ERR_CUDA;
+    status = fail(JATTN_ERR_CUDA, "qk_norm_fwd launch", ce);
   } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
              !encode_bhnd_map(&mv, v, s.BH, s.N, s.d)) {
-    status = JATTN_ERR_CUDA;
+    status = fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   } else {
     AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
     Timed t(JATTN_KERNEL_ATTN_FWD, st);
-    if (launch_attn_fwd(mq, mk, mv, as, out, lse, err, st) != cudaSuccess) status = JATTN_ERR_CUDA;
+    ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
+    if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
   }
-  if (cudaFreeAsync(cv.base, st) != cudaSuccess) status = JATTN_ERR_CUDA;
+  ce = cudaFreeAsync(cv.base, st);
+  if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "cudaFreeAsync", ce);
   return status;
 }
 
@@ -262,14 +275,13 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = dev_err_ptr();
-  if (!err) return JATTN_ERR_CUDA;
+  if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
   AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
   const int nparts_q = q_norm_bwd_parts();
   const int nparts_k = attn_bwd_dgk_parts(as);
   Carve cv;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k), st) !=
-      cudaSuccess)
-    return JATTN_ERR_CUDA;
+  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k), st);
+  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
   uint16_t* qhat = cv.take<uint16_t>(s.elems);
   uint16_t* khat = cv.take<uint16_t>(s.elems);
   float* rq = cv.take<float>(s.rows);
@@ -282,34 +294,37 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
 
   int status = JATTN_OK;
   CUtensorMap mq, mk, mv, mdo;
-  cudaError_t ce;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
     ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, lse2, delta, dqacc, s.BH, s.N, s.n_pad,
                          s.d, st);
   }
   if (ce != cudaSuccess) {
-    status = JATTN_ERR_CUDA;
+    status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
   } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
              !encode_bhnd_map(&mv, v, s.BH, s.N, s.d) || !encode_bhnd_map(&mdo, dout, s.BH, s.N, s.d)) {
-    status = JATTN_ERR_CUDA;
+    status = fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   } else {
+    const char* stage = "attn_bwd launch";
     {
       Timed t(JATTN_KERNEL_ATTN_BWD, st);
       ce = launch_attn_bwd(mq, mk, mv, mdo, as, lse2, delta, k, rk, gk, dk, dv, dqacc, dgk_part, err, st);
     }
     if (ce == cudaSuccess) {
+      stage = "q_norm_bwd launch";
       Timed t(JATTN_KERNEL_Q_NORM_BWD, st);
       ce = launch_q_norm_bwd(dqacc, q, rq, gq, as.scale, dq, dgq_part, nparts_q, static_cast<int64_t>(s.rows), s.d,
                              st);
     }
     if (ce == cudaSuccess) {
+      stage = "dg_reduce launch";
       Timed t(JATTN_KERNEL_DG_REDUCE, st);
       ce = launch_dg_reduce(dgq_part, nparts_q, dgk_part, nparts_k, s.d, dgq, dgk, st);
     }
-    if (ce != cudaSuccess) status = JATTN_ERR_CUDA;
+    if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, stage, ce);
   }
-  if (cudaFreeAsync(cv.base, st) != cudaSuccess) status = JATTN_ERR_CUDA;
+  ce = cudaFreeAsync(cv.base, st);
+  if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "cudaFreeAsync", ce);
   return status;
 }
 
@@ -398,3 +413,5 @@ extern "C" const char* jattn_status_string(int status) {
 }
 
 extern "C" int jattn_version(void) { return kVersion; }
+
+extern "C" const char* jattn_last_error_message(void) { return g_last_msg; }
