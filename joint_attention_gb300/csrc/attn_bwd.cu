@@ -227,29 +227,27 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, i
     if (ok) ok = mbar_wait(&bars.q_full[st], (i / C::kStages) & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
-    float p[128];
-    {
-      uint32_t s[4][32];
+    // P^T row as packed bf16 pairs: the exact operand of the dV MMA, and the
+    // factor reused for dS below.
+    uint32_t pp[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+    for (int c = 0; c < 4; ++c) {
+      uint32_t s[32];
+      tmem_ld32(tS + c * 32, s);
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.s_free);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[st][c * 32 + e]);
-          p[c * 32 + e + 0] = ex2_approx(fmaf(__uint_as_float(s[c][e + 0]), scale_log2, -l4.x));
-          p[c * 32 + e + 1] = ex2_approx(fmaf(__uint_as_float(s[c][e + 1]), scale_log2, -l4.y));
-          p[c * 32 + e + 2] = ex2_approx(fmaf(__uint_as_float(s[c][e + 2]), scale_log2, -l4.z));
-          p[c * 32 + e + 3] = ex2_approx(fmaf(__uint_as_float(s[c][e + 3]), scale_log2, -l4.w));
-        }
+      for (int e = 0; e < 32; e += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[st][c * 32 + e]);
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[e + 0]), scale_log2, -l4.x));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), scale_log2, -l4.y));
+        const float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), scale_log2, -l4.z));
+        const float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), scale_log2, -l4.w));
+        pp[(c * 32 + e) / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
+        pp[(c * 32 + e) / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
+      }
     }
-    if (!key_live) {
-#pragma unroll
-      for (int c = 0; c < 128; ++c) p[c] = 0.f;
-    }
+    tc_fence_before();
+    mbar_arrive(&bars.s_free);
     // P^T / dS^T buffers are free once the previous tile's dV/dK/dQ MMAs ran.
     if (i > 0) {
       ok = mbar_wait(&bars.dq_full, (i - 1) & 1, ab, dev_err);
@@ -258,8 +256,7 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, i
 #pragma unroll
     for (int col = 0; col < 128; col += 8) {
       const uint32_t off = (col >> 6) * 16384 + ((((col & 63) >> 3) ^ swz) << 4);
-      st_shared_v4(p_row + off, pack_bf16x2(p[col], p[col + 1]), pack_bf16x2(p[col + 2], p[col + 3]),
-                   pack_bf16x2(p[col + 4], p[col + 5]), pack_bf16x2(p[col + 6], p[col + 7]));
+      st_shared_v4(p_row + off, pp[col / 2], pp[col / 2 + 1], pp[col / 2 + 2], pp[col / 2 + 3]);
     }
     fence_proxy_async_smem();
     mbar_arrive(&bars.p_ready);
@@ -277,17 +274,18 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, i
         const int col = c * 32 + e;
         const float4 d0 = *reinterpret_cast<const float4*>(&bars.delta[st][col]);
         const float4 d1 = *reinterpret_cast<const float4*>(&bars.delta[st][col + 4]);
-        const float ds0 = p[col + 0] * (__uint_as_float(dpv[e + 0]) - d0.x);
-        const float ds1 = p[col + 1] * (__uint_as_float(dpv[e + 1]) - d0.y);
-        const float ds2 = p[col + 2] * (__uint_as_float(dpv[e + 2]) - d0.z);
-        const float ds3 = p[col + 3] * (__uint_as_float(dpv[e + 3]) - d0.w);
-        const float ds4 = p[col + 4] * (__uint_as_float(dpv[e + 4]) - d1.x);
-        const float ds5 = p[col + 5] * (__uint_as_float(dpv[e + 5]) - d1.y);
-        const float ds6 = p[col + 6] * (__uint_as_float(dpv[e + 6]) - d1.z);
-        const float ds7 = p[col + 7] * (__uint_as_float(dpv[e + 7]) - d1.w);
+        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint32_t pw = pp[col / 2 + h];
+          const float pa = __uint_as_float(pw << 16), pb = __uint_as_float(pw & 0xFFFF0000u);
+          const float ds0 = pa * (__uint_as_float(dpv[e + 2 * h]) - dd[2 * h]);
+          const float ds1 = pb * (__uint_as_float(dpv[e + 2 * h + 1]) - dd[2 * h + 1]);
+          w[h] = pack_bf16x2(ds0, ds1);
+        }
         const uint32_t off = (col >> 6) * 16384 + ((((col & 63) >> 3) ^ swz) << 4);
-        st_shared_v4(ds_row + off, pack_bf16x2(ds0, ds1), pack_bf16x2(ds2, ds3), pack_bf16x2(ds4, ds5),
-                     pack_bf16x2(ds6, ds7));
+        st_shared_v4(ds_row + off, w[0], w[1], w[2], w[3]);
       }
     }
     tc_fence_before();
@@ -323,29 +321,27 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, i
     }
   }
   // dk_hat = scale * acc; u = g * dk_hat; dk = r u - (r^3/d) k sum(u k);
-  // dgk partial = sum over this tile's rows of dk_hat * k * r.
-  float dkh[D];
+  // dgk partial = sum over this tile's rows of dk_hat * k * r.  Two passes
+  // over the TMEM row (the dot product first), 32 columns at a time.
+  const float r = key_live ? rk[static_cast<size_t>(bh) * N + n] : 0.f;
+  const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
+  const uint32_t tDK = tmem + lane_base + C::kColDK;
+  float dot = 0.f;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t a[32];
-    tmem_ld32(tmem + lane_base + C::kColDK + c * 32, a);
+    tmem_ld32(tDK + c * 32, a);
     tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dkh[c * 32 + e] = key_live ? __uint_as_float(a[e]) * scale : 0.f;
-  }
-  const float r = key_live ? rk[static_cast<size_t>(bh) * N + n] : 0.f;
-  const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
-  float dot = 0.f;
+    for (int c8 = 0; c8 < 4; ++c8) {
+      const uint4 w = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int c8 = 0; c8 < D / 8; ++c8) {
-    const uint4 w = key_live ? krow[c8] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float x0 = __uint_as_float(u[h] << 16), x1 = __uint_as_float(u[h] & 0xFFFF0000u);
-      const int c = c8 * 8 + 2 * h;
-      dot = fmaf(gk[c] * dkh[c], x0, dot);
-      dot = fmaf(gk[c + 1] * dkh[c + 1], x1, dot);
+      for (int h = 0; h < 4; ++h) {
+        const int e = c8 * 8 + 2 * h, col = c * 32 + e;
+        dot = fmaf(gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(u[h] << 16), dot);
+        dot = fmaf(gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(u[h] & 0xFFFF0000u), dot);
+      }
     }
   }
   const float coef = r * r * r * (1.f / D) * dot;
@@ -356,30 +352,38 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, i
   constexpr int kRedStride = D + 4;
   uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
 #pragma unroll
-  for (int c8 = 0; c8 < D / 8; ++c8) {
-    const uint4 w = key_live ? krow[c8] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    float y[8], gpart[8];
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t a[32];
+    tmem_ld32(tDK + c * 32, a);
+    tmem_wait_ld();
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float x0 = __uint_as_float(u[h] << 16), x1 = __uint_as_float(u[h] & 0xFFFF0000u);
-      const int c = c8 * 8 + 2 * h;
-      y[2 * h] = r * gk[c] * dkh[c] - coef * x0;
-      y[2 * h + 1] = r * gk[c + 1] * dkh[c + 1] - coef * x1;
-      gpart[2 * h] = dkh[c] * x0 * r;
-      gpart[2 * h + 1] = dkh[c + 1] * x1 * r;
+    for (int c8 = 0; c8 < 4; ++c8) {
+      const uint4 w = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+      float y[8], gpart[8];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int e = c8 * 8 + 2 * h, col = c * 32 + e;
+        const float x0 = __uint_as_float(u[h] << 16), x1 = __uint_as_float(u[h] & 0xFFFF0000u);
+        const float dk0 = key_live ? __uint_as_float(a[e]) * scale : 0.f;
+        const float dk1 = key_live ? __uint_as_float(a[e + 1]) * scale : 0.f;
+        y[2 * h] = r * gk[col] * dk0 - coef * x0;
+        y[2 * h + 1] = r * gk[col + 1] * dk1 - coef * x1;
+        gpart[2 * h] = dk0 * x0 * r;
+        gpart[2 * h + 1] = dk1 * x1 * r;
+      }
+      if (key_live) {
+        uint4 o;
+        o.x = pack_bf16x2(y[0], y[1]);
+        o.y = pack_bf16x2(y[2], y[3]);
+        o.z = pack_bf16x2(y[4], y[5]);
+        o.w = pack_bf16x2(y[6], y[7]);
+        dkrow[c * 4 + c8] = o;
+      }
+      float4* dst = reinterpret_cast<float4*>(red + kr * kRedStride + c * 32 + c8 * 8);
+      dst[0] = make_float4(gpart[0], gpart[1], gpart[2], gpart[3]);
+      dst[1] = make_float4(gpart[4], gpart[5], gpart[6], gpart[7]);
     }
-    if (key_live) {
-      uint4 o;
-      o.x = pack_bf16x2(y[0], y[1]);
-      o.y = pack_bf16x2(y[2], y[3]);
-      o.z = pack_bf16x2(y[4], y[5]);
-      o.w = pack_bf16x2(y[6], y[7]);
-      dkrow[c8] = o;
-    }
-    float4* dst = reinterpret_cast<float4*>(red + kr * kRedStride + c8 * 8);
-    dst[0] = make_float4(gpart[0], gpart[1], gpart[2], gpart[3]);
-    dst[1] = make_float4(gpart[4], gpart[5], gpart[6], gpart[7]);
   }
   // Bounded barrier among the 128 key-row threads.
   mbar_arrive(&bars.epi);
@@ -405,25 +409,29 @@ __device__ void bwd_dq_drain(BwdBars& bars, uint32_t tmem, int bh, int N, int nq
     bool ok = mbar_wait(&bars.dq_full, i & 1, ab, dev_err);
     if (!__all_sync(0xffffffffu, ok)) return;
     tc_fence_after();
-    uint32_t a[D];
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) tmem_ld32(tQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&a[c * 32]));
-    tmem_wait_ld();
-    tc_fence_before();
-    mbar_arrive(&bars.dq_free);
     const int qrow = i * 128 + qr;
-    if (qrow < N) {
-      float4* dst = reinterpret_cast<float4*>(dqacc + (static_cast<size_t>(bh) * N + qrow) * D);
+    float4* dst = reinterpret_cast<float4*>(dqacc + (static_cast<size_t>(bh) * N + (qrow < N ? qrow : 0)) * D);
 #pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4)
-        atomicAdd(dst + c4, make_float4(__uint_as_float(a[4 * c4]), __uint_as_float(a[4 * c4 + 1]),
-                                        __uint_as_float(a[4 * c4 + 2]), __uint_as_float(a[4 * c4 + 3])));
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tQ + c * 32, a);
+      tmem_wait_ld();
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        mbar_arrive(&bars.dq_free);
+      }
+      if (qrow < N) {
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          atomicAdd(dst + c * 8 + c4, make_float4(__uint_as_float(a[4 * c4]), __uint_as_float(a[4 * c4 + 1]),
+                                                  __uint_as_float(a[4 * c4 + 2]), __uint_as_float(a[4 * c4 + 3])));
+      }
     }
   }
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do, int N,
                     float scale, const float* __restrict__ lse2_pad, const float* __restrict__ delta_pad,

@@ -209,23 +209,21 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     tc_fence_after();
-    uint32_t s[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
-    tmem_wait_ld();
+    // Pass 1: row max over the tile (scores re-read from TMEM in pass 2, so
+    // only 32 of them are live in registers at a time).
     const int nvalid = N - j * kTileN;
-    if (nvalid < kTileN) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e >= nvalid) s[c][e] = __float_as_uint(-INFINITY);
-    }
     float mt = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 4; ++c) {
+      uint32_t s[32];
+      tmem_ld32(tS + c * 32, s);
+      tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(s[c][e]));
+      for (int e = 0; e < 32; ++e) {
+        const float v = (c * 32 + e < nvalid) ? __uint_as_float(s[e]) : -INFINITY;
+        mt = fmaxf(mt, v);
+      }
+    }
     const float m_tile = mt * scale_log2;
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
     const bool need = (m_new != m_ref) && (j > 0);
@@ -245,15 +243,22 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     l *= alpha;
     m_ref = m_new;
     const float neg_m = -m_ref;
+    // Pass 2: probabilities, row sum, bf16 P into shared memory.
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
+      uint32_t s[32];
+      tmem_ld32(tS + c * 32, s);
+      tmem_wait_ld();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {  // 8 columns = one 16-byte chunk
         uint32_t packed[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][g * 8 + 2 * h]), scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][g * 8 + 2 * h + 1]), scale_log2, neg_m));
+          const int e0 = g * 8 + 2 * h;
+          const float s0 = (c * 32 + e0 < nvalid) ? __uint_as_float(s[e0]) : -INFINITY;
+          const float s1 = (c * 32 + e0 + 1 < nvalid) ? __uint_as_float(s[e0 + 1]) : -INFINITY;
+          const float p0 = ex2_approx(fmaf(s0, scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(s1, scale_log2, neg_m));
           l += p0 + p1;
           packed[h] = pack_bf16x2(p0, p1);
         }
@@ -296,7 +301,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, int N, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
