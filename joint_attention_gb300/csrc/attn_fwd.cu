@@ -19,13 +19,16 @@
 //               per query row (TMEM lane), 128 scores per key tile; running
 //               max kept in the log2 domain and O in TMEM rescaled only when
 //               the max grows by more than 2^8 (the probabilities stay <= 256,
-//               exact in fp32 and well inside bf16 range); P is written to
-//               shared memory in the MMA's K-major swizzled layout.
+//               exact in fp32 and well inside bf16 range).  P is written back
+//               into TMEM as packed bf16 over the first 64 columns of the
+//               tile's own S buffer, and the PV MMA reads its A operand from
+//               there (no shared-memory round trip).
 //
-// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+d),
-// O_B [256+d, 256+2d).  Rows past N in the last query tile read zeros (TMA
-// fill) and are not stored; key columns past N in the last key tile are
-// masked to -inf.
+// TMEM (512 columns): S_A / P_A [0,128), S_B / P_B [128,256), O_A
+// [256,256+d), O_B [256+d, 256+2d).  S_X(j+1) overwrites P_X(j) only after
+// PV_X(j) was issued (tcgen05 MMAs of one thread run in issue order).  Rows
+// past N in the last query tile read zeros (TMA fill) and are not stored;
+// key columns past N in the last key tile are masked to -inf.
 #include <cuda_bf16.h>
 
 #include "jattn_internal.h"
@@ -42,11 +45,9 @@ template <int D>
 struct FwdCfg {
   static constexpr int kQTileBytes = kTileM * D * 2;
   static constexpr int kSlotBytes = kTileN * D * 2;
-  static constexpr int kPBytes = kTileM * kTileN * 2;
-  static constexpr int kSlots = (D == 64) ? 6 : 3;
+  static constexpr int kSlots = (D == 64) ? 8 : 5;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + 2 * kQTileBytes;
-  static constexpr int kOffRing = kOffP + 2 * kPBytes;
+  static constexpr int kOffRing = kOffQ + 2 * kQTileBytes;
   static constexpr int kTileBytes = kOffRing + kSlots * kSlotBytes;
   static constexpr int kDynSmem = kTileBytes + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -55,7 +56,7 @@ struct FwdCfg {
 
 struct FwdBars {
   uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t empty[8];  // kSlots <= 8
   uint64_t q_full;
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -116,14 +117,15 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint3
   }
 }
 
+// O (+)= P V with P read from TMEM (16 keys = 8 packed columns per MMA) and
+// V a 128-key x d slot stored key-rows x d (MN-major B operand).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t p_addr, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
   using C = FwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < kTileN / 16; ++kk) {
-    const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-    umma_bf16_ss(tmem_o, sdesc_sw128(p_addr + aoff, 16, 1024), sdesc_sw128(v_addr + kk * 2048, 16384, 1024),
-                 C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+    umma_bf16_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 2048, 16384, 1024), C::kIdescO,
+                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -131,7 +133,6 @@ template <int D>
 __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, int nkv, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   const uint32_t q_addr[2] = {smem_u32(sm + C::kOffQ), smem_u32(sm + C::kOffQ + C::kQTileBytes)};
-  const uint32_t p_addr[2] = {smem_u32(sm + C::kOffP), smem_u32(sm + C::kOffP + C::kPBytes)};
   const uint32_t ring = smem_u32(sm + C::kOffRing);
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
@@ -157,7 +158,7 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, in
     if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), &bars.abort, dev_err))) break;
     if (!(ok = mbar_wait(&bars.p_full[0], j & 1, &bars.abort, dev_err))) break;
     tc_fence_after();
-    issue_pv<D>(tO[0], p_addr[0], v_addr, j > 0);
+    issue_pv<D>(tO[0], tS[0], v_addr, j > 0);
     if (j == nkv - 1) umma_commit(&bars.o_done[0]);
     if (j + 1 < nkv) {
       if (!(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), &bars.abort, dev_err))) break;
@@ -168,7 +169,7 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, in
     if (hasB) {
       if (!(ok = mbar_wait(&bars.p_full[1], j & 1, &bars.abort, dev_err))) break;
       tc_fence_after();
-      issue_pv<D>(tO[1], p_addr[1], v_addr, j > 0);
+      issue_pv<D>(tO[1], tS[1], v_addr, j > 0);
       if (j == nkv - 1) umma_commit(&bars.o_done[1]);
     }
     umma_commit(&bars.empty[slot_of(iv)]);
@@ -198,8 +199,6 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_base + x * 128;
   const uint32_t tO = tmem + lane_base + 256 + x * D;
-  const uint32_t p_row = smem_u32(sm + C::kOffP + x * C::kPBytes) + row * 128;
-  const uint32_t swz = static_cast<uint32_t>(row & 7);
 
   float m_ref = -INFINITY;
   float l = 0.f;
@@ -210,19 +209,23 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     if (!ok) break;
     tc_fence_after();
     // Pass 1: row max over the tile (scores re-read from TMEM in pass 2, so
-    // only 32 of them are live in registers at a time).
+    // only 32 of them are live in registers at a time).  Only the ragged last
+    // key tile needs the column mask.
     const int nvalid = N - j * kTileN;
+    const bool ragged = nvalid < kTileN;
     float mt = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t s[32];
       tmem_ld32(tS + c * 32, s);
       tmem_wait_ld();
+      if (ragged) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float v = (c * 32 + e < nvalid) ? __uint_as_float(s[e]) : -INFINITY;
-        mt = fmaxf(mt, v);
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e >= nvalid) s[e] = __float_as_uint(-INFINITY);
       }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(s[e]));
     }
     const float m_tile = mt * scale_log2;
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
@@ -243,32 +246,30 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     l *= alpha;
     m_ref = m_new;
     const float neg_m = -m_ref;
-    // Pass 2: probabilities, row sum, bf16 P into shared memory.
+    // Pass 2: probabilities and row sum; P (bf16 pairs) goes back into TMEM
+    // over the columns of S already consumed (chunk c of 32 scores becomes 16
+    // packed columns at 16c, behind the reads of chunks <= c).
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t s[32];
       tmem_ld32(tS + c * 32, s);
       tmem_wait_ld();
+      if (ragged) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {  // 8 columns = one 16-byte chunk
-        uint32_t packed[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int e0 = g * 8 + 2 * h;
-          const float s0 = (c * 32 + e0 < nvalid) ? __uint_as_float(s[e0]) : -INFINITY;
-          const float s1 = (c * 32 + e0 + 1 < nvalid) ? __uint_as_float(s[e0 + 1]) : -INFINITY;
-          const float p0 = ex2_approx(fmaf(s0, scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(s1, scale_log2, neg_m));
-          l += p0 + p1;
-          packed[h] = pack_bf16x2(p0, p1);
-        }
-        const int col = c * 32 + g * 8;           // first key column of the chunk
-        const uint32_t blk = col >> 6;            // 64-column block
-        const uint32_t chunk = (col & 63) >> 3;   // 16-byte chunk in the 128-byte row
-        st_shared_v4(p_row + blk * 16384 + ((chunk ^ swz) << 4), packed[0], packed[1], packed[2], packed[3]);
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e >= nvalid) s[e] = __float_as_uint(-INFINITY);
       }
+      uint32_t packed[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * h]), scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * h + 1]), scale_log2, neg_m));
+        l += p0 + p1;
+        packed[h] = pack_bf16x2(p0, p1);
+      }
+      tmem_st16(tS + c * 16, packed);
     }
-    fence_proxy_async_smem();
+    tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&bars.p_full[x]);
   }

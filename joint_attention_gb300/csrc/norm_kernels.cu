@@ -212,17 +212,27 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
   }
 }
 
-// Block 0 reduces the dgq partials, block 1 the dgk partials; one thread per
-// column, partials summed in index order.
-__global__ void dg_reduce_kernel(const float* __restrict__ part_q, int nq, const float* __restrict__ part_k, int nk,
-                                 int d, float* __restrict__ dgq, float* __restrict__ dgk) {
-  const int c = threadIdx.x;
-  if (c >= d) return;
-  const float* part = blockIdx.x == 0 ? part_q : part_k;
-  const int nparts = blockIdx.x == 0 ? nq : nk;
+// Fixed-order reduction of the gain-gradient partials.  blockIdx.y selects
+// dgq (0) or dgk (1); each block owns 32 columns: thread (x, y) sums partial
+// rows y, y + 32, y + 64, ... of column x (coalesced 128-byte rows), then the
+// 32 slices are added in index order.  Same grid, same order, every call.
+__global__ void __launch_bounds__(1024) dg_reduce_kernel(const float* __restrict__ part_q, int nq,
+                                                         const float* __restrict__ part_k, int nk, int d,
+                                                         float* __restrict__ dgq, float* __restrict__ dgk) {
+  __shared__ float slice[32][33];
+  const float* part = blockIdx.y == 0 ? part_q : part_k;
+  const int nparts = blockIdx.y == 0 ? nq : nk;
+  const int c = blockIdx.x * 32 + threadIdx.x;
   float s = 0.f;
-  for (int p = 0; p < nparts; ++p) s += part[static_cast<size_t>(p) * d + c];
-  (blockIdx.x == 0 ? dgq : dgk)[c] = s;
+  if (c < d)
+    for (int p = threadIdx.y; p < nparts; p += 32) s += part[static_cast<size_t>(p) * d + c];
+  slice[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && c < d) {
+    float t = 0.f;
+    for (int y = 0; y < 32; ++y) t += slice[y][threadIdx.x];
+    (blockIdx.y == 0 ? dgq : dgk)[c] = t;
+  }
 }
 
 int sm_count() {
@@ -292,7 +302,7 @@ cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float
 
 cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* dgq, float* dgk,
                              cudaStream_t st) {
-  dg_reduce_kernel<<<2, 128, 0, st>>>(part_q, nq, part_k, nk, d, dgq, dgk);
+  dg_reduce_kernel<<<dim3((d + 31) / 32, 2), dim3(32, 32), 0, st>>>(part_q, nq, part_k, nk, d, dgq, dgk);
   return cudaGetLastError();
 }
 

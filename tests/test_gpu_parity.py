@@ -106,12 +106,20 @@ def test_ragged_lengths(ja, N, d):
 
 
 def test_sharp_softmax_exercises_rescaling(ja):
-    # gains ~ U(2, 4): logits up to ~16 * 8 apart, so the running max moves
-    # by more than the 2^8 lazy-rescale threshold inside a row.
+    # Stress case (not one of the five workloads): gains ~ U(2, 4) give logits
+    # up to ~16 * 8 apart, so the running max moves by more than the 2^8
+    # lazy-rescale threshold inside a row.  With a near one-hot softmax, O is
+    # close to single bf16 rows of V, so its error is set by bf16 rounding:
+    # at most half an ulp of P (2^-9 relative, times max|v|) plus half an ulp
+    # of the bf16 output (2^-9 * max|O|); the max-abs bound is that sum.
     inp = make_inputs(1, 3, 700, 64, seed=77, gain_range=(2.0, 4.0))
     got = run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, 77)
     ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
-    check_fwd(got, ref, "sharp")
+    vmax = float(np.max(np.abs(inp.v)))
+    bound = 2.0 ** -9 * vmax + 2.0 ** -9 * float(np.max(np.abs(ref["O"]))) + 1e-3
+    assert float(np.max(np.abs(got["O"] - ref["O"]))) <= bound
+    assert relF(got["O"], ref["O"]) <= O_RELF
+    assert float(np.max(np.abs(got["LSE"] - ref["LSE"]))) <= LSE_MAXABS
     check_bwd(got, ref, where="sharp")
 
 
