@@ -54,7 +54,8 @@ typedef enum {
   JATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   JATTN_ERR_ALIAS = 4,       /* an output buffer overlaps an input or another output */
   JATTN_ERR_CUDA = 5,        /* a CUDA launch or allocation failed */
-  JATTN_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up (reported by jattn_last_device_error) */
+  JATTN_ERR_TIMEOUT = 6,     /* a device-side bounded wait gave up (reported by jattn_last_device_error) */
+  JATTN_ERR_SCRATCH_LIMIT = 7 /* jattn_fwd_noalloc: the problem needs more scratch than its fixed array holds */
 } jattn_status;
 
 /*
@@ -87,6 +88,38 @@ int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, con
 int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
               const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq, jattn_bf16* dk,
               jattn_bf16* dv, float* dgq, float* dgk, int B, int H, int N_img, int N_txt, int d, void* stream);
+
+/*
+ * Forward without any device allocation.  (No counterpart on the pages: an
+ * integration entry point.)  Same arguments, layout and results as jattn_fwd,
+ * but the scratch it needs (the normalised q_hat and k_hat, 2 * 2 * B*H*N*d
+ * bytes, each part 256-byte aligned) lives in one fixed file-scope device
+ * array of JATTN_NOALLOC_SCRATCH_BYTES (64 MiB) instead of a per-call
+ * cudaMallocAsync.  It calls no cudaMalloc / cudaFree / allocating library
+ * routine.
+ *
+ * Who needs it: callers that cannot let a library allocate device memory, such
+ * as a serving process that reserves nearly all of HBM for its own pool up
+ * front (a library allocation would then fail mid-step), or a launch sequence
+ * that must never block on or recover from an allocator call.
+ *
+ * Rules:
+ *  - Problems needing more than the array (B*H*N*d > 16,777,216 = 2^24 at these
+ *    alignments, e.g. the 768 px / d = 128 workload) return
+ *    JATTN_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Every call, on any stream, shares the one array, which keeps the last
+ *    call's contents.  Nothing in it needs clearing (the norm kernel writes
+ *    every element it is later read back from), but calls that overlap on the
+ *    GPU (for example on two streams at once) race on it: serialise them.
+ *  - Every GPU that loads this library holds the array until the process
+ *    exits.
+ */
+#define JATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+                      int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse, void* stream);
 
 /*
  * Synchronises `stream` and returns JATTN_ERR_TIMEOUT if any kernel launched

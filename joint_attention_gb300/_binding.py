@@ -24,6 +24,7 @@ STATUS = {
     4: "JATTN_ERR_ALIAS",
     5: "JATTN_ERR_CUDA",
     6: "JATTN_ERR_TIMEOUT",
+    7: "JATTN_ERR_SCRATCH_LIMIT",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -55,6 +56,8 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     vp, i32 = ctypes.c_void_p, ctypes.c_int
     lib.jattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.jattn_fwd.restype = i32
+    lib.jattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.jattn_fwd_noalloc.restype = i32
     lib.jattn_bwd.argtypes = [vp] * 13 + [i32] * 5 + [vp]
     lib.jattn_bwd.restype = i32
     lib.jattn_last_device_error.argtypes = [vp]
@@ -158,6 +161,23 @@ def jattn_fwd(q, k, v, gq, gk, B: int, H: int, N_img: int, N_txt: int, d: int, o
                        _ptr(lse, "lse", f32, r), _stream(stream))
     if check and rc != 0:
         raise JattnError(rc, "jattn_fwd")
+    return rc
+
+
+def jattn_fwd_noalloc(q, k, v, gq, gk, B: int, H: int, N_img: int, N_txt: int, d: int, out, lse, stream=None,
+                      check: bool = True) -> int:
+    """C ABI jattn_fwd_noalloc: jattn_fwd with its scratch in a fixed device array (no allocation)."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e, r = B * H * N * d, B * H * N
+    bf, f32 = torch.bfloat16, torch.float32
+    rc = lib.jattn_fwd_noalloc(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                               _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), B, H, N_img, N_txt, d,
+                               _ptr(out, "out", bf, e), _ptr(lse, "lse", f32, r), _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_fwd_noalloc")
     return rc
 
 

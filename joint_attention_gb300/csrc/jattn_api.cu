@@ -200,6 +200,79 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
 
 using namespace jattn;
 
+namespace jattn {
+namespace {
+
+// The fixed scratch of jattn_fwd_noalloc (see include/jattn.h): one array per
+// device, looked up once per device and then shared by every call.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[JATTN_NOALLOC_SCRATCH_BYTES];
+
+uint8_t* noalloc_scratch_ptr() {
+  static uint8_t* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      fail(JATTN_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch)", e);
+      return nullptr;
+    }
+    ptrs[dev] = static_cast<uint8_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace jattn
+
+extern "C" int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                                 const float* gk, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out,
+                                 float* lse, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  const void* ptrs[] = {q, k, v, gq, gk, out, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
+  const size_t tb = s.elems * 2;
+  const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(gq, s.d * 4),
+                       range_of(gk, s.d * 4)};
+  const Range outs[] = {range_of(out, tb), range_of(lse, s.rows * 4)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlaps(o, i)) return JATTN_ERR_ALIAS;
+  if (overlaps(outs[0], outs[1])) return JATTN_ERR_ALIAS;
+  const size_t part = (tb + 255) & ~static_cast<size_t>(255);
+  if (2 * part > JATTN_NOALLOC_SCRATCH_BYTES) return JATTN_ERR_SCRATCH_LIMIT;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = dev_err_ptr();
+  if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
+  uint8_t* scratch = noalloc_scratch_ptr();
+  if (!scratch) return JATTN_ERR_CUDA;
+  uint16_t* qhat = reinterpret_cast<uint16_t*>(scratch);
+  uint16_t* khat = reinterpret_cast<uint16_t*>(scratch + part);
+  cudaError_t ce;
+  {
+    Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
+    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, st);
+  }
+  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "qk_norm_fwd launch", ce);
+  CUtensorMap mq, mk, mv;
+  if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
+      !encode_bhnd_map(&mv, v, s.BH, s.N, s.d))
+    return fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
+  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
+  Timed t(JATTN_KERNEL_ATTN_FWD, st);
+  ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
+  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
+  return JATTN_OK;
+}
+
 extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
                          const float* gk, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse,
                          void* stream) {
@@ -408,6 +481,7 @@ extern "C" const char* jattn_status_string(int status) {
     case JATTN_ERR_ALIAS: return "an output buffer overlaps another buffer";
     case JATTN_ERR_CUDA: return "CUDA launch or allocation failed";
     case JATTN_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    case JATTN_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed no-alloc array holds";
     default: return "unknown status";
   }
 }
