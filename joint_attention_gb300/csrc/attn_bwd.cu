@@ -141,13 +141,17 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
   }
 }
 
+// The MMA helpers take base shared-memory descriptors built once by the MMA
+// thread and advance them by (byte offset >> 4) per 16-wide K step.
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t byte_off) { return desc + (byte_off >> 4); }
+
 // D[tmem] = A * B^T with A, B K-major 128 x d tiles (d/16 MMAs of K = 16).
 template <int D>
-__device__ __forceinline__ void mma_kk(uint32_t tmem_d, uint32_t a, uint32_t b, uint32_t idesc) {
+__device__ __forceinline__ void mma_kk(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc) {
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-    umma_bf16_ss(tmem_d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    umma_bf16_ss(tmem_d, dadd(a, off), dadd(b, off), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -155,49 +159,57 @@ __device__ __forceinline__ void mma_kk(uint32_t tmem_d, uint32_t a, uint32_t b, 
 // queries 64-127 in [64,96) of the S^T region), B = dO tile stored
 // query-rows x d (MN-major).
 template <int D>
-__device__ __forceinline__ void mma_dv(uint32_t tmem_d, uint32_t tmem_p, uint32_t b, bool accumulate) {
+__device__ __forceinline__ void mma_dv(uint32_t tmem_d, uint32_t tmem_p, uint64_t b, bool accumulate) {
   using C = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-    umma_bf16_ts(tmem_d, tmem_p + acol, sdesc_sw128(b + kk * 2048, 16384, 1024), C::kIdescKM,
-                 (accumulate || kk > 0) ? 1u : 0u);
+    umma_bf16_ts(tmem_d, tmem_p + acol, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
 // dK (+)= dS^T Q: A = dS^T (K-major over queries), B = Q tile stored
 // query-rows x d (MN-major).
 template <int D>
-__device__ __forceinline__ void mma_dk(uint32_t tmem_d, uint32_t a, uint32_t b, bool accumulate) {
+__device__ __forceinline__ void mma_dk(uint32_t tmem_d, uint64_t a, uint64_t b, bool accumulate) {
   using C = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-    umma_bf16_ss(tmem_d, sdesc_sw128(a + aoff, 16, 1024), sdesc_sw128(b + kk * 2048, 16384, 1024), C::kIdescKM,
-                 (accumulate || kk > 0) ? 1u : 0u);
+    umma_bf16_ss(tmem_d, dadd(a, aoff), dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
 // dQ = dS K: A = dS read from the dS^T tile (MN-major), B = K tile stored
 // key-rows x d (MN-major); K = 128 keys.
 template <int D>
-__device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint32_t a, uint32_t b) {
+__device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) {
   using C = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    umma_bf16_ss(tmem_d, sdesc_sw128(a + kk * 2048, 16384, 1024), sdesc_sw128(b + kk * 2048, 16384, 1024),
-                 C::kIdescMM, kk > 0 ? 1u : 0u);
+    umma_bf16_ss(tmem_d, dadd(a, kk * 2048), dadd(b, kk * 2048), C::kIdescMM, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
 __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
   using C = BwdCfg<D>;
+  // Base descriptors: K-major (LBO unused) for S / dP / dK operands, MN-major
+  // with 64-column blocks 16 KB apart for the B operands of dV, dK, dQ and
+  // the A operand of dQ.
   const uint32_t aK = smem_u32(sm + C::kOffK), aV = smem_u32(sm + C::kOffV);
+  const uint64_t kK = sdesc_sw128(aK, 16, 1024), kV = sdesc_sw128(aV, 16, 1024);
+  const uint64_t mK = sdesc_sw128(aK, 16384, 1024);
   volatile int* ab = &bars.abort;
-  auto aQ = [&](int i) { return smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile); };
-  auto aDO = [&](int i) { return smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile); };
-  auto aDS = [&](int i) { return smem_u32(sm + C::kOffDS + (i % C::kDSBufs) * (128 * 128 * 2)); };
+  auto qaddr = [=](int i) { return smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile); };
+  auto doaddr = [=](int i) { return smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile); };
+  auto dsaddr = [=](int i) { return smem_u32(sm + C::kOffDS + (i % C::kDSBufs) * (128 * 128 * 2)); };
+  auto kQ = [=](int i) { return sdesc_sw128(qaddr(i), 16, 1024); };
+  auto mQ = [=](int i) { return sdesc_sw128(qaddr(i), 16384, 1024); };
+  auto kDO = [=](int i) { return sdesc_sw128(doaddr(i), 16, 1024); };
+  auto mDO = [=](int i) { return sdesc_sw128(doaddr(i), 16384, 1024); };
+  auto kDS = [=](int i) { return sdesc_sw128(dsaddr(i), 16, 1024); };
+  auto mDS = [=](int i) { return sdesc_sw128(dsaddr(i), 16384, 1024); };
   auto q_ph = [](int i) { return static_cast<uint32_t>((i / C::kQStages) & 1); };
   auto do_ph = [](int i) { return static_cast<uint32_t>((i / C::kDOStages) & 1); };
 
@@ -205,56 +217,56 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint3
   if (ok) ok = mbar_wait(&bars.q_full[0], 0, ab, dev_err);
   if (ok) {
     tc_fence_after();
-    mma_kk<D>(tmem + C::kColS, aK, aQ(0), C::kIdescSS);
+    mma_kk<D>(tmem + C::kColS, kK, kQ(0), C::kIdescSS);
     umma_commit(&bars.s_full);
   }
   if (ok) ok = mbar_wait(&bars.do_full[0], 0, ab, dev_err);
   if (ok) {
     tc_fence_after();
-    mma_kk<D>(tmem + C::kColDP, aV, aDO(0), C::kIdescSS);
+    mma_kk<D>(tmem + C::kColDP, kV, kDO(0), C::kIdescSS);
     umma_commit(&bars.dp_full);
   }
   for (int i = 0; ok && i < nq; ++i) {
     // dV(i): needs P^T(i) in TMEM.
     if (!(ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, aDO(i), i > 0);
+    mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(i), i > 0);
     umma_commit(&bars.do_empty[i % C::kDOStages]);
     // S(i+1): overwrites the S^T/P^T columns behind dV(i).
     if (i + 1 < nq) {
       if (!(ok = mbar_wait(&bars.q_full[(i + 1) % C::kQStages], q_ph(i + 1), ab, dev_err))) break;
       tc_fence_after();
-      mma_kk<D>(tmem + C::kColS, aK, aQ(i + 1), C::kIdescSS);
+      mma_kk<D>(tmem + C::kColS, kK, kQ(i + 1), C::kIdescSS);
       umma_commit(&bars.s_full);
     }
     // dK(i): needs dS^T(i) in shared memory (compute is then done with dP(i)).
     if (!(ok = mbar_wait(&bars.ds_ready, i & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_dk<D>(tmem + C::kColDK, aDS(i), aQ(i), i > 0);
+    mma_dk<D>(tmem + C::kColDK, kDS(i), mQ(i), i > 0);
     umma_commit(&bars.q_empty[i % C::kQStages]);
     if (D == 64) {
       if (i + 1 < nq) {
         if (!(ok = mbar_wait(&bars.do_full[(i + 1) % C::kDOStages], do_ph(i + 1), ab, dev_err))) break;
         tc_fence_after();
-        mma_kk<D>(tmem + C::kColDP, aV, aDO(i + 1), C::kIdescSS);
+        mma_kk<D>(tmem + C::kColDP, kV, kDO(i + 1), C::kIdescSS);
         umma_commit(&bars.dp_full);
       }
       if (i > 0 && !(ok = mbar_wait(&bars.dq_free, (i - 1) & 1, ab, dev_err))) break;
       tc_fence_after();
-      mma_dq<D>(tmem + C::kColDQ, aDS(i), aK);
+      mma_dq<D>(tmem + C::kColDQ, mDS(i), mK);
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[i % C::kDSBufs]);
     } else {
       // dQ(i) lands in the dP^T columns (dP(i) already consumed); the drain of
       // dQ(i-1) from those columns finished before dP(i) was issued.
-      mma_dq<D>(tmem + C::kColDQ, aDS(i), aK);
+      mma_dq<D>(tmem + C::kColDQ, mDS(i), mK);
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[i % C::kDSBufs]);
       if (i + 1 < nq) {
         if (!(ok = mbar_wait(&bars.dq_free, i & 1, ab, dev_err))) break;
         if (!(ok = mbar_wait(&bars.do_full[(i + 1) % C::kDOStages], do_ph(i + 1), ab, dev_err))) break;
         tc_fence_after();
-        mma_kk<D>(tmem + C::kColDP, aV, aDO(i + 1), C::kIdescSS);
+        mma_kk<D>(tmem + C::kColDP, kV, kDO(i + 1), C::kIdescSS);
         umma_commit(&bars.dp_full);
       }
     }

@@ -52,6 +52,14 @@ struct FwdCfg {
   static constexpr int kDynSmem = kTileBytes + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+  // d = 64: S_A, S_B, O_A, O_B and two packed-bf16 P buffers fill the 512
+  // TMEM columns exactly, so P gets its own columns and S(j+1) can be issued
+  // ahead of PV(j).  d = 128: P is written over the consumed S columns.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr uint32_t kColS = 0;              // + 128 x
+  static constexpr uint32_t kColO = 256;            // + D x
+  static constexpr uint32_t kColP = kSepP ? 384 : 0;  // + 64 x (d = 64), + 128 x (aliased)
+  static constexpr uint32_t kPStride = kSepP ? 64 : 128;
 };
 
 struct FwdBars {
@@ -61,6 +69,7 @@ struct FwdBars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -106,25 +115,26 @@ __device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k,
   }
 }
 
+// S = Q K^T: both operands K-major 128 x d tiles; base descriptors are built
+// once and advanced by (byte offset >> 4) per 16-wide K step.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
   using C = FwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-    umma_bf16_ss(tmem_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), C::kIdescS,
-                 kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+    umma_bf16_ss(tmem_s, q_desc + off, k_desc + off, C::kIdescS, kk > 0 ? 1u : 0u);
   }
 }
 
 // O (+)= P V with P read from TMEM (16 keys = 8 packed columns per MMA) and
 // V a 128-key x d slot stored key-rows x d (MN-major B operand).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
   using C = FwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < kTileN / 16; ++kk) {
-    umma_bf16_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 2048, 16384, 1024), C::kIdescO,
+    umma_bf16_ts(tmem_o, tmem_p + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), C::kIdescO,
                  (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -132,54 +142,59 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 template <int D>
 __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, int nkv, uint32_t* dev_err) {
   using C = FwdCfg<D>;
-  const uint32_t q_addr[2] = {smem_u32(sm + C::kOffQ), smem_u32(sm + C::kOffQ + C::kQTileBytes)};
+  const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(sm + C::kOffQ), 16, 1024),
+                              sdesc_sw128(smem_u32(sm + C::kOffQ + C::kQTileBytes), 16, 1024)};
   const uint32_t ring = smem_u32(sm + C::kOffRing);
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+  const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + 128};
+  const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + D};
+  const uint32_t tP[2] = {tmem + C::kColP, tmem + C::kColP + C::kPStride};
   auto slot_of = [](int i) { return i % C::kSlots; };
   auto phase_of = [](int i) { return (uint32_t)((i / C::kSlots) & 1); };
-  bool ok = mbar_wait(&bars.q_full, 0, &bars.abort, dev_err);
-  if (ok) ok = mbar_wait(&bars.full[slot_of(0)], phase_of(0), &bars.abort, dev_err);
+  auto k_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16, 1024); };
+  auto v_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16384, 1024); };
+  volatile int* ab = &bars.abort;
+  const int ntiles = hasB ? 2 : 1;
+  bool ok = mbar_wait(&bars.q_full, 0, ab, dev_err);
+  if (ok) ok = mbar_wait(&bars.full[slot_of(0)], phase_of(0), ab, dev_err);
   if (ok) {
     tc_fence_after();
-    const uint32_t k0 = ring + slot_of(0) * C::kSlotBytes;
-    issue_qk<D>(tS[0], q_addr[0], k0);
-    umma_commit(&bars.s_full[0]);
-    if (hasB) {
-      issue_qk<D>(tS[1], q_addr[1], k0);
-      umma_commit(&bars.s_full[1]);
+    for (int x = 0; x < ntiles; ++x) {
+      issue_qk<D>(tS[x], q_desc[x], k_desc(0));
+      umma_commit(&bars.s_full[x]);
     }
     umma_commit(&bars.empty[slot_of(0)]);
   }
   for (int j = 0; ok && j < nkv; ++j) {
     const int iv = 2 * j + 1, ik = 2 * j + 2;
-    const uint32_t v_addr = ring + slot_of(iv) * C::kSlotBytes;
-    const uint32_t kn_addr = ring + slot_of(ik) * C::kSlotBytes;
-    if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), &bars.abort, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.p_full[0], j & 1, &bars.abort, dev_err))) break;
-    tc_fence_after();
-    issue_pv<D>(tO[0], tS[0], v_addr, j > 0);
-    if (j == nkv - 1) umma_commit(&bars.o_done[0]);
-    if (j + 1 < nkv) {
-      if (!(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), &bars.abort, dev_err))) break;
+    const bool more = j + 1 < nkv;
+    if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), ab, dev_err))) break;
+    if (more && !(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), ab, dev_err))) break;
+    for (int x = 0; x < ntiles; ++x) {
+      if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
       tc_fence_after();
-      issue_qk<D>(tS[0], q_addr[0], kn_addr);
-      umma_commit(&bars.s_full[0]);
-    }
-    if (hasB) {
-      if (!(ok = mbar_wait(&bars.p_full[1], j & 1, &bars.abort, dev_err))) break;
-      tc_fence_after();
-      issue_pv<D>(tO[1], tS[1], v_addr, j > 0);
-      if (j == nkv - 1) umma_commit(&bars.o_done[1]);
-    }
-    umma_commit(&bars.empty[slot_of(iv)]);
-    if (j + 1 < nkv) {
-      if (hasB) {
-        issue_qk<D>(tS[1], q_addr[1], kn_addr);
-        umma_commit(&bars.s_full[1]);
+      if (C::kSepP) {
+        // S_X(j+1) first (the softmax has finished reading S_X(j)), then
+        // PV_X(j) from the separate P columns.
+        if (more) {
+          issue_qk<D>(tS[x], q_desc[x], k_desc(ik));
+          umma_commit(&bars.s_full[x]);
+        }
+        issue_pv<D>(tO[x], tP[x], v_desc(iv), j > 0);
+        umma_commit(&bars.pv_done[x]);
+      } else {
+        // P lives in the S columns: PV_X(j) must be issued before S_X(j+1).
+        issue_pv<D>(tO[x], tP[x], v_desc(iv), j > 0);
+        umma_commit(&bars.pv_done[x]);
+        if (more) {
+          issue_qk<D>(tS[x], q_desc[x], k_desc(ik));
+          umma_commit(&bars.s_full[x]);
+        }
       }
-      umma_commit(&bars.empty[slot_of(ik)]);
+      if (j == nkv - 1) umma_commit(&bars.o_done[x]);
     }
+    if (!ok) break;
+    umma_commit(&bars.empty[slot_of(iv)]);
+    if (more) umma_commit(&bars.empty[slot_of(ik)]);
   }
   // Every MMA issued above has completed once this barrier flips.
   umma_commit(&bars.drain);
@@ -197,40 +212,67 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
   const int row = wq * 32 + lane;
   const int n = q0 + x * 128 + row;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t tS = tmem + lane_base + x * 128;
-  const uint32_t tO = tmem + lane_base + 256 + x * D;
+  const uint32_t tS = tmem + lane_base + C::kColS + x * 128;
+  const uint32_t tO = tmem + lane_base + C::kColO + x * D;
+  const uint32_t tP = tmem + lane_base + C::kColP + x * C::kPStride;
+  volatile int* ab = &bars.abort;
 
   float m_ref = -INFINITY;
   float l = 0.f;
   bool ok = true;
   for (int j = 0; j < nkv; ++j) {
-    ok = mbar_wait(&bars.s_full[x], j & 1, &bars.abort, dev_err);
+    ok = mbar_wait(&bars.s_full[x], j & 1, ab, dev_err);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     tc_fence_after();
-    // Pass 1: row max over the tile (scores re-read from TMEM in pass 2, so
-    // only 32 of them are live in registers at a time).  Only the ragged last
-    // key tile needs the column mask.
-    const int nvalid = N - j * kTileN;
-    const bool ragged = nvalid < kTileN;
-    float mt = -INFINITY;
+    // The whole 128-score row in registers: four loads, one wait.
+    uint32_t s[4][32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t s[32];
-      tmem_ld32(tS + c * 32, s);
-      tmem_wait_ld();
-      if (ragged) {
+    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+    tmem_wait_ld();
+    const int nvalid = N - j * kTileN;
+    if (nvalid < kTileN) {  // only the ragged last key tile needs the mask
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (c * 32 + e >= nvalid) s[e] = __float_as_uint(-INFINITY);
-      }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(s[e]));
+          if (c * 32 + e >= nvalid) s[c][e] = __float_as_uint(-INFINITY);
     }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(s[c][e]));
     const float m_tile = mt * scale_log2;
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
     const bool need = (m_new != m_ref) && (j > 0);
     const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+    if (C::kSepP && j > 0) {
+      // PV(j-1) must be done with O (rescale below) and with the P columns.
+      ok = mbar_wait(&bars.pv_done[x], (j - 1) & 1, ab, dev_err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+    }
+    l *= alpha;
+    m_ref = m_new;
+    const float neg_m = -m_ref;
+    // Probabilities and row sum; P (bf16 pairs, 16 packed columns per 32
+    // scores) into TMEM.
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t packed[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h]), scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h + 1]), scale_log2, neg_m));
+        l += p0 + p1;
+        packed[h] = pack_bf16x2(p0, p1);
+      }
+      tmem_st16(tP + c * 16, packed);
+    }
+    // Rescale O (after P, when the score registers are free); PV(j) waits for
+    // this tile's p_full, so O is not being accumulated meanwhile.
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -241,40 +283,13 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
         tmem_st32(tO + c * 32, o);
       }
-      tmem_wait_st();
-    }
-    l *= alpha;
-    m_ref = m_new;
-    const float neg_m = -m_ref;
-    // Pass 2: probabilities and row sum; P (bf16 pairs) goes back into TMEM
-    // over the columns of S already consumed (chunk c of 32 scores becomes 16
-    // packed columns at 16c, behind the reads of chunks <= c).
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t s[32];
-      tmem_ld32(tS + c * 32, s);
-      tmem_wait_ld();
-      if (ragged) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e >= nvalid) s[e] = __float_as_uint(-INFINITY);
-      }
-      uint32_t packed[16];
-#pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * h]), scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * h + 1]), scale_log2, neg_m));
-        l += p0 + p1;
-        packed[h] = pack_bf16x2(p0, p1);
-      }
-      tmem_st16(tS + c * 16, packed);
     }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&bars.p_full[x]);
   }
   if (!ok) return;
-  ok = mbar_wait(&bars.o_done[x], 0, &bars.abort, dev_err);
+  ok = mbar_wait(&bars.o_done[x], 0, ab, dev_err);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return;
   tc_fence_after();
@@ -326,6 +341,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars.s_full[x], 1);
       mbar_init(&bars.p_full[x], 128);
       mbar_init(&bars.o_done[x], 1);
+      mbar_init(&bars.pv_done[x], 1);
     }
     mbar_init(&bars.drain, 1);
     bars.abort = 0;

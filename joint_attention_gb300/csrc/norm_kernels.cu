@@ -223,9 +223,18 @@ __global__ void __launch_bounds__(1024) dg_reduce_kernel(const float* __restrict
   const float* part = blockIdx.y == 0 ? part_q : part_k;
   const int nparts = blockIdx.y == 0 ? nq : nk;
   const int c = blockIdx.x * 32 + threadIdx.x;
-  float s = 0.f;
-  if (c < d)
-    for (int p = threadIdx.y; p < nparts; p += 32) s += part[static_cast<size_t>(p) * d + c];
+  // Eight independent partial sums keep eight loads in flight per thread;
+  // they are combined in a fixed order.
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c < d) {
+    int p = threadIdx.y;
+    for (; p + 7 * 32 < nparts; p += 8 * 32) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] += part[static_cast<size_t>(p + u * 32) * d + c];
+    }
+    for (; p < nparts; p += 32) acc[0] += part[static_cast<size_t>(p) * d + c];
+  }
+  const float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   slice[threadIdx.y][threadIdx.x] = s;
   __syncthreads();
   if (threadIdx.y == 0 && c < d) {
