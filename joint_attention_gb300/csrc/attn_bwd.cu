@@ -46,7 +46,7 @@
 namespace jattn {
 namespace {
 
-constexpr int kBwdThreads = 448;
+constexpr int kBwdThreads = 480;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -54,7 +54,11 @@ struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128 x d bf16 tile
   static constexpr int kQStages = 2;
   static constexpr int kDOStages = (D == 64) ? 2 : 1;
-  static constexpr int kDSBufs = (D == 64) ? 2 : 1;
+  static constexpr int kDSBufs = 1;
+  // d = 64: two MMA issuers (recompute: S, dP; gradients: dV, dK, dQ) and P^T
+  // in its own TMEM columns (S 128 + dP 128 + dV 64 + dK 64 + dQ 64 + P 64 =
+  // 512).  d = 128: one issuer, P^T over the consumed S^T columns.
+  static constexpr bool kTwoIssuers = (D == 64);
   static constexpr int kDQCols = (D == 64) ? 64 : 32;        // dQ columns drained per pass
   static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // padded staging row
   static constexpr int kOffK = 0;
@@ -70,6 +74,7 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
+  static constexpr uint32_t kColP = (D == 64) ? 448 : 0;
   static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
   static constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);      // dQ
@@ -84,8 +89,9 @@ struct BwdBars {
   uint64_t ds_free[2];
   uint64_t dq_full, dq_free;
   uint64_t kv_done;
+  uint64_t dv_done;
   uint64_t epi;
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
   // Per query stage: the tile's LSE in the log2 domain (+inf past N) and D
@@ -163,7 +169,8 @@ __device__ __forceinline__ void mma_dv(uint32_t tmem_d, uint32_t tmem_p, uint64_
   using C = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+    // separate P columns: contiguous; aliased: group 1 starts 64 columns in
+    const uint32_t acol = C::kTwoIssuers ? kk * 8 : ((kk < 4) ? kk * 8 : 64 + (kk - 4) * 8);
     umma_bf16_ts(tmem_d, tmem_p + acol, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -189,6 +196,73 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
   for (int kk = 0; kk < 8; ++kk) {
     umma_bf16_ss(tmem_d, dadd(a, kk * 2048), dadd(b, kk * 2048), C::kIdescMM, kk > 0 ? 1u : 0u);
   }
+}
+
+// Two-issuer backward (d = 64).  Recompute issuer: S(i) and dP(i).
+// Gradient issuer: dV(i), dK(i), dQ(i).  A Q stage is released by both (S
+// reads it, dK reads it), a dO stage likewise (dP, dV).  S(i+1) overwrites
+// S(i) only after the compute groups have read it (p_ready(i)); P^T has its
+// own columns, which the compute groups rewrite only after dV(i-1) is done.
+template <int D>
+__device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
+  using C = BwdCfg<D>;
+  const uint64_t kK = sdesc_sw128(smem_u32(sm + C::kOffK), 16, 1024);
+  const uint64_t kV = sdesc_sw128(smem_u32(sm + C::kOffV), 16, 1024);
+  volatile int* ab = &bars.abort;
+  auto kQ = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile), 16, 1024); };
+  auto kDO = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16, 1024); };
+  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
+  for (int i = 0; ok && i < nq; ++i) {
+    if (i > 0 && !(ok = mbar_wait(&bars.p_ready, (i - 1) & 1, ab, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
+    tc_fence_after();
+    mma_kk<D>(tmem + C::kColS, kK, kQ(i), C::kIdescSS);
+    umma_commit(&bars.s_full);
+    umma_commit(&bars.q_empty[i % C::kQStages]);
+    if (i > 0 && !(ok = mbar_wait(&bars.ds_ready, (i - 1) & 1, ab, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
+    tc_fence_after();
+    mma_kk<D>(tmem + C::kColDP, kV, kDO(i), C::kIdescSS);
+    umma_commit(&bars.dp_full);
+    umma_commit(&bars.do_empty[i % C::kDOStages]);
+  }
+  umma_commit(&bars.drain[0]);
+  mbar_wait_drain(&bars.drain[0], 0);
+}
+
+template <int D>
+__device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
+  using C = BwdCfg<D>;
+  const uint64_t mK = sdesc_sw128(smem_u32(sm + C::kOffK), 16384, 1024);
+  volatile int* ab = &bars.abort;
+  auto mQ = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile), 16384, 1024); };
+  auto mDO = [=](int i) {
+    return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16384, 1024);
+  };
+  const uint32_t ds_addr = smem_u32(sm + C::kOffDS);
+  const uint64_t kDS = sdesc_sw128(ds_addr, 16, 1024), mDS = sdesc_sw128(ds_addr, 16384, 1024);
+  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
+  for (int i = 0; ok && i < nq; ++i) {
+    if (!(ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
+    tc_fence_after();
+    mma_dv<D>(tmem + C::kColDV, tmem + C::kColP, mDO(i), i > 0);
+    umma_commit(&bars.dv_done);
+    umma_commit(&bars.do_empty[i % C::kDOStages]);
+    if (!(ok = mbar_wait(&bars.ds_ready, i & 1, ab, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
+    tc_fence_after();
+    mma_dk<D>(tmem + C::kColDK, kDS, mQ(i), i > 0);
+    umma_commit(&bars.q_empty[i % C::kQStages]);
+    if (i > 0 && !(ok = mbar_wait(&bars.dq_free, (i - 1) & 1, ab, dev_err))) break;
+    tc_fence_after();
+    mma_dq<D>(tmem + C::kColDQ, mDS, mK);
+    umma_commit(&bars.dq_full);
+    umma_commit(&bars.ds_free[0]);
+  }
+  if (ok) umma_commit(&bars.kv_done);
+  umma_commit(&bars.drain[1]);
+  mbar_wait_drain(&bars.drain[1], 0);
 }
 
 template <int D>
@@ -273,8 +347,8 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint3
   }
   if (ok) umma_commit(&bars.kv_done);
   // Every MMA issued above has completed once this barrier flips.
-  umma_commit(&bars.drain);
-  mbar_wait_drain(&bars.drain, 0);
+  umma_commit(&bars.drain[0]);
+  mbar_wait_drain(&bars.drain[0], 0);
 }
 
 // Key-row threads of one compute group (query columns 64g .. 64g+63).
@@ -287,6 +361,8 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
   const bool key_live = kv0 + kr < N;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * g;   // this group's S^T columns
+  // P^T: own columns (32 packed per group) or over the group's S^T columns
+  const uint32_t tP = C::kTwoIssuers ? tmem + lane_base + C::kColP + 32 * g : tS;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * g;
   const uint32_t swz = static_cast<uint32_t>(kr & 7);
   const float scale_log2 = scale * kLog2e;
@@ -317,7 +393,13 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
         pp[(c * 32 + e) / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
         pp[(c * 32 + e) / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
       }
-      tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
+      if (C::kTwoIssuers && c == 0 && i > 0) {
+        // dV(i-1) must be done reading the previous P^T before it is rewritten.
+        ok = mbar_wait(&bars.dv_done, (i - 1) & 1, ab, dev_err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+      }
+      tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
     }
     tmem_wait_st();
     tc_fence_before();
@@ -543,11 +625,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
+    // With two issuers a Q / dO stage is released by a commit from each.
+    const uint32_t n_rel = BwdCfg<D>::kTwoIssuers ? 2u : 1u;
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.q_empty[s], n_rel);
       mbar_init(&bars.do_full[s], 1);
-      mbar_init(&bars.do_empty[s], 1);
+      mbar_init(&bars.do_empty[s], n_rel);
       mbar_init(&bars.ds_free[s], 1);
     }
     mbar_init(&bars.s_full, 1);
@@ -557,8 +641,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.kv_done, 1);
+    mbar_init(&bars.dv_done, 1);
     mbar_init(&bars.epi, 128);
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -575,7 +661,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0)
       bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, bh, kv0, nq, lse2_pad, delta_pad, n_pad, dev_err);
   } else if (warp == 13) {
-    if (lane == 0) bwd_mma<D>(sm, bars, tmem, nq, dev_err);
+    if (lane == 0) {
+      if (BwdCfg<D>::kTwoIssuers) bwd_mma_recompute<D>(sm, bars, tmem, nq, dev_err);
+      else bwd_mma<D>(sm, bars, tmem, nq, dev_err);
+    }
+  } else if (warp == 14) {
+    if (lane == 0 && BwdCfg<D>::kTwoIssuers) bwd_mma_gradients<D>(sm, bars, tmem, nq, dev_err);
   } else if (warp < 8) {
     const int g = warp >> 2;
     bwd_compute<D>(sm, bars, tmem, g, bh, kv0, N, nq, scale, dev_err);

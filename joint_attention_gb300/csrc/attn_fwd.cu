@@ -11,10 +11,12 @@
 //
 //   warp 8      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into
 //               a ring of 128 x d bf16 slots (128-byte swizzle).
-//   warp 9      MMA issuer (one thread): S_X = Q_X K_j^T into TMEM, and
-//               O_X += P_X V_j, ordered S_A(j+1) after PV_A(j) and S_B(j+1)
-//               after PV_B(j) so each tile's softmax overlaps the other
-//               tile's MMAs.
+//   warps 9-10  MMA issuers, one thread per query tile (A: warp 9, B: warp
+//               10): S_X = Q_X K_j^T into TMEM and O_X += P_X V_j.  Two
+//               issuers keep the tensor pipe fed while either one waits on a
+//               barrier (a single issuer's waits and commits between MMA
+//               groups leave the pipe idle).  A ring slot is released once
+//               both issuers have committed their last MMA that reads it.
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread
 //               per query row (TMEM lane), 128 scores per key tile; running
 //               max kept in the log2 domain and O in TMEM rescaled only when
@@ -37,7 +39,7 @@
 namespace jattn {
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -70,7 +72,7 @@ struct FwdBars {
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t pv_done[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -139,29 +141,27 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
   }
 }
 
+// MMA issue for one query tile x.  Both issuers read the same K/V slots; a
+// slot's empty barrier counts one commit per issuer.
 template <int D>
-__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, int nkv, uint32_t* dev_err) {
+__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int nkv, uint32_t* dev_err) {
   using C = FwdCfg<D>;
-  const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(sm + C::kOffQ), 16, 1024),
-                              sdesc_sw128(smem_u32(sm + C::kOffQ + C::kQTileBytes), 16, 1024)};
+  const uint64_t q_desc = sdesc_sw128(smem_u32(sm + C::kOffQ + x * C::kQTileBytes), 16, 1024);
   const uint32_t ring = smem_u32(sm + C::kOffRing);
-  const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + 128};
-  const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + D};
-  const uint32_t tP[2] = {tmem + C::kColP, tmem + C::kColP + C::kPStride};
+  const uint32_t tS = tmem + C::kColS + x * 128;
+  const uint32_t tO = tmem + C::kColO + x * D;
+  const uint32_t tP = tmem + C::kColP + x * C::kPStride;
   auto slot_of = [](int i) { return i % C::kSlots; };
   auto phase_of = [](int i) { return (uint32_t)((i / C::kSlots) & 1); };
   auto k_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16, 1024); };
   auto v_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16384, 1024); };
   volatile int* ab = &bars.abort;
-  const int ntiles = hasB ? 2 : 1;
   bool ok = mbar_wait(&bars.q_full, 0, ab, dev_err);
   if (ok) ok = mbar_wait(&bars.full[slot_of(0)], phase_of(0), ab, dev_err);
   if (ok) {
     tc_fence_after();
-    for (int x = 0; x < ntiles; ++x) {
-      issue_qk<D>(tS[x], q_desc[x], k_desc(0));
-      umma_commit(&bars.s_full[x]);
-    }
+    issue_qk<D>(tS, q_desc, k_desc(0));
+    umma_commit(&bars.s_full[x]);
     umma_commit(&bars.empty[slot_of(0)]);
   }
   for (int j = 0; ok && j < nkv; ++j) {
@@ -169,36 +169,33 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, bool hasB, in
     const bool more = j + 1 < nkv;
     if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), ab, dev_err))) break;
     if (more && !(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), ab, dev_err))) break;
-    for (int x = 0; x < ntiles; ++x) {
-      if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
-      tc_fence_after();
-      if (C::kSepP) {
-        // S_X(j+1) first (the softmax has finished reading S_X(j)), then
-        // PV_X(j) from the separate P columns.
-        if (more) {
-          issue_qk<D>(tS[x], q_desc[x], k_desc(ik));
-          umma_commit(&bars.s_full[x]);
-        }
-        issue_pv<D>(tO[x], tP[x], v_desc(iv), j > 0);
-        umma_commit(&bars.pv_done[x]);
-      } else {
-        // P lives in the S columns: PV_X(j) must be issued before S_X(j+1).
-        issue_pv<D>(tO[x], tP[x], v_desc(iv), j > 0);
-        umma_commit(&bars.pv_done[x]);
-        if (more) {
-          issue_qk<D>(tS[x], q_desc[x], k_desc(ik));
-          umma_commit(&bars.s_full[x]);
-        }
+    if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
+    tc_fence_after();
+    if (C::kSepP) {
+      // S_X(j+1) first (the softmax has finished reading S_X(j)), then PV_X(j)
+      // from the separate P columns.
+      if (more) {
+        issue_qk<D>(tS, q_desc, k_desc(ik));
+        umma_commit(&bars.s_full[x]);
       }
-      if (j == nkv - 1) umma_commit(&bars.o_done[x]);
+      issue_pv<D>(tO, tP, v_desc(iv), j > 0);
+      umma_commit(&bars.pv_done[x]);
+    } else {
+      // P lives in the S columns: PV_X(j) must be issued before S_X(j+1).
+      issue_pv<D>(tO, tP, v_desc(iv), j > 0);
+      umma_commit(&bars.pv_done[x]);
+      if (more) {
+        issue_qk<D>(tS, q_desc, k_desc(ik));
+        umma_commit(&bars.s_full[x]);
+      }
     }
-    if (!ok) break;
+    if (j == nkv - 1) umma_commit(&bars.o_done[x]);
     umma_commit(&bars.empty[slot_of(iv)]);
     if (more) umma_commit(&bars.empty[slot_of(ik)]);
   }
-  // Every MMA issued above has completed once this barrier flips.
-  umma_commit(&bars.drain);
-  mbar_wait_drain(&bars.drain, 0);
+  // Every MMA this thread issued has completed once this barrier flips.
+  umma_commit(&bars.drain[x]);
+  mbar_wait_drain(&bars.drain[x], 0);
 }
 
 // Softmax / epilogue of one 128-row query tile (x = 0: tile A, 1: tile B).
@@ -334,7 +331,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars.full[i], 1);
-      mbar_init(&bars.empty[i], 1);
+      mbar_init(&bars.empty[i], hasB ? 2 : 1);  // one commit per MMA issuer
     }
     mbar_init(&bars.q_full, 1);
     for (int x = 0; x < 2; ++x) {
@@ -342,8 +339,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars.p_full[x], 128);
       mbar_init(&bars.o_done[x], 1);
       mbar_init(&bars.pv_done[x], 1);
+      mbar_init(&bars.drain[x], 1);
     }
-    mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -358,8 +355,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp == 8) {
     if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, bh, q0, hasB, nkv, dev_err);
-  } else if (warp == 9) {
-    if (lane == 0) fwd_mma<D>(sm, bars, tmem, hasB, nkv, dev_err);
+  } else if (warp >= 9) {
+    const int x = warp - 9;
+    if (lane == 0 && (x == 0 || hasB)) fwd_mma<D>(sm, bars, tmem, x, nkv, dev_err);
   } else {
     const int x = warp >> 2;
     if (x == 0 || hasB) fwd_softmax<D>(sm, bars, tmem, x, bh, q0, N, nkv, scale_log2, out, lse, dev_err);
