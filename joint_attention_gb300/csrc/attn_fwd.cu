@@ -33,6 +33,7 @@
 // key columns past N in the last key tile are masked to -inf.
 #include <cuda_bf16.h>
 
+#include "exp2_poly.h"
 #include "jattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -42,6 +43,10 @@ namespace {
 constexpr int kFwdThreads = 352;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Pairs of probabilities (by index within a 32-score chunk, bit h % 8) whose
+// 2^x runs on the FMA pipe (exp2_poly) instead of the MUFU unit: 3 of 8,
+// which balances the two pipes for this kernel's instruction mix.
+constexpr uint32_t kPolyPairMask = (1u << 1) | (1u << 4) | (1u << 6);
 
 template <int D>
 struct FwdCfg {
@@ -255,18 +260,37 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     m_ref = m_new;
     const float neg_m = -m_ref;
     // Probabilities and row sum; P (bf16 pairs, 16 packed columns per 32
-    // scores) into TMEM.
+    // scores) into TMEM.  On full tiles part of the 2^x goes to the FMA pipe;
+    // the ragged last tile keeps exact zeros for masked keys (MUFU only).
+    if (nvalid >= kTileN) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t packed[16];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t packed[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h]), scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h + 1]), scale_log2, neg_m));
-        l += p0 + p1;
-        packed[h] = pack_bf16x2(p0, p1);
+        for (int h = 0; h < 16; ++h) {
+          const float x0 = fmaf(__uint_as_float(s[c][2 * h]), scale_log2, neg_m);
+          const float x1 = fmaf(__uint_as_float(s[c][2 * h + 1]), scale_log2, neg_m);
+          const bool poly = (kPolyPairMask >> (h & 7)) & 1u;
+          const float p0 = poly ? exp2_poly(x0) : ex2_approx(x0);
+          const float p1 = poly ? exp2_poly(x1) : ex2_approx(x1);
+          l += p0 + p1;
+          packed[h] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tP + c * 16, packed);
       }
-      tmem_st16(tP + c * 16, packed);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h]), scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h + 1]), scale_log2, neg_m));
+          l += p0 + p1;
+          packed[h] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tP + c * 16, packed);
+      }
     }
     // Rescale O (after P, when the score registers are free); PV(j) waits for
     // this tile's p_full, so O is not being accumulated meanwhile.
