@@ -44,9 +44,10 @@ constexpr int kFwdThreads = 352;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Pairs of probabilities (by index within a 32-score chunk, bit h % 8) whose
-// 2^x runs on the FMA pipe (exp2_poly) instead of the MUFU unit: 3 of 8,
-// which balances the two pipes for this kernel's instruction mix.
-constexpr uint32_t kPolyPairMask = (1u << 1) | (1u << 4) | (1u << 6);
+// 2^x runs on the FMA pipe (exp2_poly) instead of the MUFU unit.  The
+// polynomial costs about nine issue slots per value against one MUFU slot, so
+// only a small share pays off before instruction issue becomes the limit.
+constexpr uint32_t kPolyPairMask = (1u << 3);
 
 template <int D>
 struct FwdCfg {
