@@ -59,10 +59,10 @@ struct BwdCfg {
   static constexpr int kQStages = 2;
   static constexpr int kDOStages = (D == 64) ? 2 : 1;
   static constexpr int kDSBufs = 1;
-  // d = 64: compute split by role (P group, dS group), two MMA issuers
-  // (recompute: S, dP; gradients: dV, dK, dQ) and P^T in its own TMEM
-  // columns.  d = 128: compute split by query columns, one MMA issuer.
-  static constexpr bool kRoleSplit = (D == 64);
+  // d = 64: two MMA issuers (recompute: S, dP; gradients: dV, dK, dQ), K / V
+  // and dS^T as TMEM A operands.  d = 128: one issuer, operands in shared
+  // memory.
+  static constexpr bool kTwoIssuers = (D == 64);
   static constexpr int kDQCols = (D == 64) ? 64 : 32;        // dQ columns drained per pass
   static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // padded staging row
   static constexpr int kOffK = 0;
@@ -78,7 +78,8 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
-  static constexpr uint32_t kColP = 448;  // d = 64 only: P^T as packed bf16 (64 columns)
+  static constexpr uint32_t kColKA = 448;  // d = 64 only: K as packed bf16 (32 columns)
+  static constexpr uint32_t kColVA = 480;  // d = 64 only: V as packed bf16
   static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
   static constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);      // dQ
@@ -93,7 +94,8 @@ struct BwdBars {
   uint64_t ds_free[2];
   uint64_t dq_full, dq_free;
   uint64_t kv_done;
-  uint64_t s_free, dp_free, p_free;
+  uint64_t kv_tmem;
+  uint64_t dv_done, dk_done;
   uint64_t epi;
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -179,14 +181,27 @@ __device__ __forceinline__ void mma_dv(uint32_t tmem_d, uint32_t tmem_p, uint64_
   }
 }
 
-// dV (+)= P^T dO with P^T in its own 64 TMEM columns (queries 16kk..16kk+15
-// packed at columns 8kk..8kk+7), B = dO tile stored query-rows x d.
+// D = A * B^T with A (K or V, 128 keys x d) packed in TMEM and B a K-major
+// 128 x d tile in shared memory.
 template <int D>
-__device__ __forceinline__ void mma_dv_sep(uint32_t tmem_d, uint32_t tmem_p, uint64_t b, bool accumulate) {
+__device__ __forceinline__ void mma_tk(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+    umma_bf16_ts(tmem_d, tmem_a + kk * 8, dadd(b, off), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// dK (+)= dS^T Q with dS^T packed in TMEM over the dP^T columns (same
+// column pattern as P^T), B = Q tile stored query-rows x d (MN-major).
+template <int D>
+__device__ __forceinline__ void mma_dk_t(uint32_t tmem_d, uint32_t tmem_ds, uint64_t b, bool accumulate) {
   using C = BwdCfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    umma_bf16_ts(tmem_d, tmem_p + kk * 8, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+    umma_bf16_ts(tmem_d, tmem_ds + acol, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 // dK (+)= dS^T Q: A = dS^T (K-major over queries), B = Q tile stored
@@ -212,32 +227,36 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
   }
 }
 
-// Role-split backward (d = 64), two MMA issuers.
-// Recompute issuer: S(i) = K Q_i^T once the P group has read S(i-1) into
-// registers (s_free), dP(i) = V dO_i^T once the dS group has read dP(i-1)
-// (dp_free).  Gradient issuer: dV(i) from P^T in TMEM, then dK(i) and dQ(i)
-// from dS^T in shared memory.  A Q stage is released by both issuers (S and
-// dK read it), a dO stage likewise (dP, dV).
+// Two-issuer backward (d = 64).  Recompute issuer: S(i) = K Q_i^T and
+// dP(i) = V dO_i^T with K, V read from TMEM.  Gradient issuer: dV(i), dK(i)
+// (both with A from TMEM) and dQ(i).  A Q stage is released by both issuers
+// (S and dK read it), a dO stage likewise (dP, dV).  S(i+1) overwrites the
+// P^T(i) columns only after dV(i) completed, dP(i+1) the dS^T(i) columns only
+// after dK(i) completed.
 template <int D>
 __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
   using C = BwdCfg<D>;
-  const uint64_t kK = sdesc_sw128(smem_u32(sm + C::kOffK), 16, 1024);
-  const uint64_t kV = sdesc_sw128(smem_u32(sm + C::kOffV), 16, 1024);
   volatile int* ab = &bars.abort;
   auto kQ = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile), 16, 1024); };
   auto kDO = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16, 1024); };
-  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
+  bool ok = mbar_wait(&bars.kv_tmem, 0, ab, dev_err);
   for (int i = 0; ok && i < nq; ++i) {
-    if (i > 0 && !(ok = mbar_wait(&bars.s_free, (i - 1) & 1, ab, dev_err))) break;
+    if (i > 0) {
+      if (!(ok = mbar_wait(&bars.p_ready, (i - 1) & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.dv_done, (i - 1) & 1, ab, dev_err))) break;
+    }
     if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_kk<D>(tmem + C::kColS, kK, kQ(i), C::kIdescSS);
+    mma_tk<D>(tmem + C::kColS, tmem + C::kColKA, kQ(i), C::kIdescSS);
     umma_commit(&bars.s_full);
     umma_commit(&bars.q_empty[i % C::kQStages]);
-    if (i > 0 && !(ok = mbar_wait(&bars.dp_free, (i - 1) & 1, ab, dev_err))) break;
+    if (i > 0) {
+      if (!(ok = mbar_wait(&bars.ds_ready, (i - 1) & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.dk_done, (i - 1) & 1, ab, dev_err))) break;
+    }
     if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_kk<D>(tmem + C::kColDP, kV, kDO(i), C::kIdescSS);
+    mma_tk<D>(tmem + C::kColDP, tmem + C::kColVA, kDO(i), C::kIdescSS);
     umma_commit(&bars.dp_full);
     umma_commit(&bars.do_empty[i % C::kDOStages]);
   }
@@ -254,20 +273,20 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, int
   auto mDO = [=](int i) {
     return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16384, 1024);
   };
-  const uint32_t ds_addr = smem_u32(sm + C::kOffDS);
-  const uint64_t kDS = sdesc_sw128(ds_addr, 16, 1024), mDS = sdesc_sw128(ds_addr, 16384, 1024);
+  const uint64_t mDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16384, 1024);
   bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
   for (int i = 0; ok && i < nq; ++i) {
     if (!(ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_dv_sep<D>(tmem + C::kColDV, tmem + C::kColP, mDO(i), i > 0);
-    umma_commit(&bars.p_free);
+    mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(i), i > 0);
+    umma_commit(&bars.dv_done);
     umma_commit(&bars.do_empty[i % C::kDOStages]);
     if (!(ok = mbar_wait(&bars.ds_ready, i & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_dk<D>(tmem + C::kColDK, kDS, mQ(i), i > 0);
+    mma_dk_t<D>(tmem + C::kColDK, tmem + C::kColDP, mQ(i), i > 0);
+    umma_commit(&bars.dk_done);
     umma_commit(&bars.q_empty[i % C::kQStages]);
     if (i > 0 && !(ok = mbar_wait(&bars.dq_free, (i - 1) & 1, ab, dev_err))) break;
     tc_fence_after();
@@ -278,136 +297,6 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, int
   if (ok) umma_commit(&bars.kv_done);
   umma_commit(&bars.drain[1]);
   mbar_wait_drain(&bars.drain[1], 0);
-}
-
-// P group (d = 64): one thread per key row computes P^T = exp(s S^T - LSE)
-// for all 128 query columns of each tile.  S^T is read 32 columns at a time
-// (the next load in flight while the current chunk is exponentiated); once
-// the last chunk is in registers the S^T columns are released, so S(i+1) is
-// computed while this tile's exponentials run.  P^T goes to its own TMEM
-// columns, after dV(i-1) and the dS group are done with P^T(i-1).
-template <int D>
-__device__ void bwd_pgroup(BwdBars& bars, uint32_t tmem, int kv0, int N, int nq, float scale, uint32_t* dev_err) {
-  using C = BwdCfg<D>;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kr = (warp & 3) * 32 + lane;
-  const bool key_live = kv0 + kr < N;
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + C::kColS;
-  const uint32_t tP = tmem + lane_base + C::kColP;
-  const float scale_log2 = scale * kLog2e;
-  volatile int* ab = &bars.abort;
-  for (int i = 0; i < nq; ++i) {
-    const int qs = i % C::kQStages;
-    bool ok = mbar_wait(&bars.s_full, i & 1, ab, dev_err);
-    if (ok) ok = mbar_wait(&bars.q_full[qs], (i / C::kQStages) & 1, ab, dev_err);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-    uint32_t sbuf[2][32];
-    tmem_ld32(tS, sbuf[0]);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (c < 3) tmem_ld32(tS + (c + 1) * 32, sbuf[(c + 1) & 1]);  // next chunk in flight
-      uint32_t packed[16];
-      const uint32_t(&sc)[32] = sbuf[c & 1];
-#pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[qs][c * 32 + e]);
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sc[e + 0]), scale_log2, -l4.x));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sc[e + 1]), scale_log2, -l4.y));
-        const float p2 = ex2_approx(fmaf(__uint_as_float(sc[e + 2]), scale_log2, -l4.z));
-        const float p3 = ex2_approx(fmaf(__uint_as_float(sc[e + 3]), scale_log2, -l4.w));
-        packed[e / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
-        packed[e / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
-      }
-      if (c == 0 && i > 0) {
-        // dV(i-1) and the dS group must be done with P^T(i-1) before it is
-        // overwritten.
-        ok = mbar_wait(&bars.p_free, (i - 1) & 1, ab, dev_err);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc_fence_after();
-      }
-      tmem_st16(tP + c * 16, packed);
-      if (c < 3) {
-        tmem_wait_ld();
-        if (c == 2) {  // all of S^T is in registers now
-          tc_fence_before();
-          mbar_arrive(&bars.s_free);
-        }
-      }
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&bars.p_ready);
-  }
-}
-
-// dS group (d = 64): one thread per key row computes dS^T = P^T * (dP^T - D)
-// for all 128 query columns, reading P^T back from TMEM, and writes it as
-// bf16 into shared memory (128-byte-swizzled K-major rows: the A operand of
-// dK, and of dQ read MN-major).
-template <int D>
-__device__ void bwd_dgroup(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
-  using C = BwdCfg<D>;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kr = (warp & 3) * 32 + lane;
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tDP = tmem + lane_base + C::kColDP;
-  const uint32_t tP = tmem + lane_base + C::kColP;
-  const uint32_t swz = static_cast<uint32_t>(kr & 7);
-  const uint32_t ds_row = smem_u32(sm + C::kOffDS) + kr * 128;
-  volatile int* ab = &bars.abort;
-  for (int i = 0; i < nq; ++i) {
-    const int qs = i % C::kQStages;
-    bool ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err);
-    if (ok) ok = mbar_wait(&bars.dp_full, i & 1, ab, dev_err);
-    if (ok) ok = mbar_wait(&bars.q_full[qs], (i / C::kQStages) & 1, ab, dev_err);
-    if (ok && i > 0) ok = mbar_wait(&bars.ds_free[0], (i - 1) & 1, ab, dev_err);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-    // All of P^T (64 packed columns) first, so its columns are released early;
-    // dP^T then 32 columns at a time with the next chunk in flight.
-    uint32_t pall[64], dbuf[2][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld16(tP + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pall[c * 16]));
-    tmem_ld32(tDP, dbuf[0]);
-    tmem_wait_ld();
-    tc_fence_before();
-    mbar_arrive(&bars.p_free);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (c < 3) tmem_ld32(tDP + (c + 1) * 32, dbuf[(c + 1) & 1]);  // next chunk in flight
-      const uint32_t(&dc)[32] = dbuf[c & 1];
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        const int col = c * 32 + e;  // query column of the tile
-        const float4 d0 = *reinterpret_cast<const float4*>(&bars.delta[qs][col]);
-        const float4 d1 = *reinterpret_cast<const float4*>(&bars.delta[qs][col + 4]);
-        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-        uint32_t w[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint32_t pw = pall[col / 2 + h];
-          const float pa = __uint_as_float(pw << 16), pb = __uint_as_float(pw & 0xFFFF0000u);
-          w[h] = pack_bf16x2(pa * (__uint_as_float(dc[e + 2 * h]) - dd[2 * h]),
-                             pb * (__uint_as_float(dc[e + 2 * h + 1]) - dd[2 * h + 1]));
-        }
-        const uint32_t blk = static_cast<uint32_t>(col >> 6);
-        const uint32_t chunk = static_cast<uint32_t>((col & 63) >> 3);
-        st_shared_v4(ds_row + blk * 16384 + ((chunk ^ swz) << 4), w[0], w[1], w[2], w[3]);
-      }
-      if (c < 3) {
-        tmem_wait_ld();
-        if (c == 2) {  // dP^T fully read: release it
-          tc_fence_before();
-          mbar_arrive(&bars.dp_free);
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    mbar_arrive(&bars.ds_ready);
-  }
 }
 
 template <int D>
@@ -496,8 +385,7 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint3
   mbar_wait_drain(&bars.drain[0], 0);
 }
 
-// Key-row threads of one compute group (query columns 64g .. 64g+63); the
-// d = 128 path, where the two groups split the columns of each tile.
+// Key-row threads of one compute group (query columns 64g .. 64g+63).
 template <int D>
 __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, int bh, int kv0, int N, int nq,
                             float scale, uint32_t* dev_err) {
@@ -512,6 +400,27 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
   const float scale_log2 = scale * kLog2e;
   volatile int* ab = &bars.abort;
 
+  if (C::kTwoIssuers) {
+    // Copy this thread's key row of K (group 0) or V (group 1) from the
+    // swizzled shared-memory tile into TMEM as packed bf16 pairs.
+    bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const uint8_t* tile = sm + (g == 0 ? C::kOffK : C::kOffV) + kr * 128;
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + ((static_cast<uint32_t>(c) ^ swz) << 4));
+      w[4 * c] = v.x;
+      w[4 * c + 1] = v.y;
+      w[4 * c + 2] = v.z;
+      w[4 * c + 3] = v.w;
+    }
+    tmem_st32(tmem + lane_base + (g == 0 ? C::kColKA : C::kColVA), w);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bars.kv_tmem);
+  }
+
   for (int i = 0; i < nq; ++i) {
     const int qs = i % C::kQStages;
     bool ok = mbar_wait(&bars.s_full, i & 1, ab, dev_err);
@@ -522,11 +431,15 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
     // P^T = exp2(s log2e S^T - LSE2), packed bf16 pairs, back into TMEM over
     // the S^T columns already read (chunk c -> 16 packed columns at 16c).
     uint32_t pp[32];
+    // Both 32-column chunks of this group's S^T in flight at once: one TMEM
+    // round trip per phase instead of two.
+    uint32_t sall[2][32];
+    tmem_ld32(tS, sall[0]);
+    tmem_ld32(tS + 32, sall[1]);
+    tmem_wait_ld();
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      uint32_t s[32];
-      tmem_ld32(tS + c * 32, s);
-      tmem_wait_ld();
+      const uint32_t(&s)[32] = sall[c];
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[qs][64 * g + c * 32 + e]);
@@ -549,11 +462,13 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
     if (!__all_sync(0xffffffffu, ok)) return;
     tc_fence_after();
     const uint32_t ds_row = smem_u32(sm + C::kOffDS + (i % C::kDSBufs) * (128 * 128 * 2)) + g * 16384 + kr * 128;
+    uint32_t dpall[2][32];
+    tmem_ld32(tDP, dpall[0]);
+    tmem_ld32(tDP + 32, dpall[1]);
+    tmem_wait_ld();
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      uint32_t dpv[32];
-      tmem_ld32(tDP + c * 32, dpv);
-      tmem_wait_ld();
+      const uint32_t(&dpv)[32] = dpall[c];
       uint32_t dsw[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
@@ -571,7 +486,10 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
         st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
                      dsw[e / 2 + 2], dsw[e / 2 + 3]);
       }
+      // dS^T also into TMEM over the dP^T columns just read (A operand of dK).
+      if (C::kTwoIssuers) tmem_st16(tDP + c * 16, dsw);
     }
+    if (C::kTwoIssuers) tmem_wait_st();
     tc_fence_before();
     fence_proxy_async_smem();
     mbar_arrive(&bars.ds_ready);
@@ -765,7 +683,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
     // With two issuers a Q / dO stage is released by a commit from each.
-    const uint32_t n_rel = BwdCfg<D>::kRoleSplit ? 2u : 1u;
+    const uint32_t n_rel = BwdCfg<D>::kTwoIssuers ? 2u : 1u;
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], n_rel);
@@ -775,14 +693,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_ready, BwdCfg<D>::kRoleSplit ? 128 : 256);
-    mbar_init(&bars.ds_ready, BwdCfg<D>::kRoleSplit ? 128 : 256);
+    mbar_init(&bars.p_ready, 256);
+    mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.kv_done, 1);
-    mbar_init(&bars.s_free, 128);
-    mbar_init(&bars.dp_free, 128);
-    mbar_init(&bars.p_free, 129);  // the dV commit plus the 128 dS-group threads
+    mbar_init(&bars.kv_tmem, 256);
+    mbar_init(&bars.dv_done, 1);
+    mbar_init(&bars.dk_done, 1);
     mbar_init(&bars.epi, 128);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
@@ -803,19 +721,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, bh, kv0, nq, lse2_pad, delta_pad, n_pad, dev_err);
   } else if (warp == 13) {
     if (lane == 0) {
-      if (BwdCfg<D>::kRoleSplit) bwd_mma_recompute<D>(sm, bars, tmem, nq, dev_err);
+      if (BwdCfg<D>::kTwoIssuers) bwd_mma_recompute<D>(sm, bars, tmem, nq, dev_err);
       else bwd_mma<D>(sm, bars, tmem, nq, dev_err);
     }
   } else if (warp == 14) {
-    if (lane == 0 && BwdCfg<D>::kRoleSplit) bwd_mma_gradients<D>(sm, bars, tmem, nq, dev_err);
+    if (lane == 0 && BwdCfg<D>::kTwoIssuers) bwd_mma_gradients<D>(sm, bars, tmem, nq, dev_err);
   } else if (warp < 8) {
     const int g = warp >> 2;
-    if (BwdCfg<D>::kRoleSplit) {
-      if (g == 0) bwd_pgroup<D>(bars, tmem, kv0, N, nq, scale, dev_err);
-      else bwd_dgroup<D>(sm, bars, tmem, nq, dev_err);
-    } else {
-      bwd_compute<D>(sm, bars, tmem, g, bh, kv0, N, nq, scale, dev_err);
-    }
+    bwd_compute<D>(sm, bars, tmem, g, bh, kv0, N, nq, scale, dev_err);
     if (g == 0)
       bwd_epilogue_dv<D>(bars, tmem, bh, kv0, N, dv, dev_err);
     else

@@ -47,7 +47,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // 2^x runs on the FMA pipe (exp2_poly) instead of the MUFU unit.  The
 // polynomial costs about nine issue slots per value against one MUFU slot, so
 // only a small share pays off before instruction issue becomes the limit.
-constexpr uint32_t kPolyPairMask = (1u << 3);
+constexpr uint32_t kPolyPairMask = 0u;
 
 template <int D>
 struct FwdCfg {
@@ -245,7 +245,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
 #pragma unroll
     for (int c = 0; c < 4; ++c)
 #pragma unroll
-      for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(s[c][e]));
+      for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
     const float m_tile = mt * scale_log2;
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
     const bool need = (m_new != m_ref) && (j > 0);
@@ -263,35 +263,34 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     // Probabilities and row sum; P (bf16 pairs, 16 packed columns per 32
     // scores) into TMEM.  On full tiles part of the 2^x goes to the FMA pipe;
     // the ragged last tile keeps exact zeros for masked keys (MUFU only).
-    if (nvalid >= kTileN) {
+    // x = s * scale_log2 - m and the row sum in packed f32x2 arithmetic (two
+    // scores per instruction); 2^x on the MUFU unit, except the pairs selected
+    // by kPolyPairMask on full tiles, which use the FMA-pipe polynomial.  The
+    // ragged last tile keeps exact zeros for masked keys (MUFU only).
+    const uint64_t scale2 = f2_make(scale_log2, scale_log2);
+    const uint64_t negm2 = f2_make(neg_m, neg_m);
+    uint64_t l2 = f2_make(0.f, 0.f);
+    const bool full_tile = nvalid >= kTileN;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t packed[16];
+    for (int c = 0; c < 4; ++c) {
+      uint32_t packed[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float x0 = fmaf(__uint_as_float(s[c][2 * h]), scale_log2, neg_m);
-          const float x1 = fmaf(__uint_as_float(s[c][2 * h + 1]), scale_log2, neg_m);
-          const bool poly = (kPolyPairMask >> (h & 7)) & 1u;
-          const float p0 = poly ? exp2_poly(x0) : ex2_approx(x0);
-          const float p1 = poly ? exp2_poly(x1) : ex2_approx(x1);
-          l += p0 + p1;
-          packed[h] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tP + c * 16, packed);
+      for (int h = 0; h < 16; ++h) {
+        float x0, x1;
+        f2_split(f2_fma(f2_make(__uint_as_float(s[c][2 * h]), __uint_as_float(s[c][2 * h + 1])), scale2, negm2), x0,
+                 x1);
+        const bool poly = full_tile && ((kPolyPairMask >> (h & 7)) & 1u);
+        const float p0 = poly ? exp2_poly(x0) : ex2_approx(x0);
+        const float p1 = poly ? exp2_poly(x1) : ex2_approx(x1);
+        l2 = f2_add(l2, f2_make(p0, p1));
+        packed[h] = pack_bf16x2(p0, p1);
       }
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t packed[16];
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h]), scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * h + 1]), scale_log2, neg_m));
-          l += p0 + p1;
-          packed[h] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tP + c * 16, packed);
-      }
+      tmem_st16(tP + c * 16, packed);
+    }
+    {
+      float la, lb;
+      f2_split(l2, la, lb);
+      l += la + lb;
     }
     // Rescale O (after P, when the score registers are free); PV(j) waits for
     // this tile's p_full, so O is not being accumulated meanwhile.
