@@ -78,6 +78,7 @@ struct FwdBars {
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t pv_done[2];
+  uint64_t s_free[2];  // d = 64: the softmax has the scores in registers
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
@@ -175,19 +176,24 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int nk
     const bool more = j + 1 < nkv;
     if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), ab, dev_err))) break;
     if (more && !(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), ab, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
-    tc_fence_after();
     if (C::kSepP) {
-      // S_X(j+1) first (the softmax has finished reading S_X(j)), then PV_X(j)
-      // from the separate P columns.
+      // S_X(j+1) as soon as the softmax holds S_X(j) in registers, so it is
+      // computed during this tile's exponentials; then PV_X(j) from the
+      // separate P columns once P_X(j) is written.
       if (more) {
+        if (!(ok = mbar_wait(&bars.s_free[x], j & 1, ab, dev_err))) break;
+        tc_fence_after();
         issue_qk<D>(tS, q_desc, k_desc(ik));
         umma_commit(&bars.s_full[x]);
       }
+      if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
+      tc_fence_after();
       issue_pv<D>(tO, tP, v_desc(iv), j > 0);
       umma_commit(&bars.pv_done[x]);
     } else {
       // P lives in the S columns: PV_X(j) must be issued before S_X(j+1).
+      if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
+      tc_fence_after();
       issue_pv<D>(tO, tP, v_desc(iv), j > 0);
       umma_commit(&bars.pv_done[x]);
       if (more) {
@@ -233,6 +239,10 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
 #pragma unroll
     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
     tmem_wait_ld();
+    if (C::kSepP) {  // the S columns may be overwritten by S(j+1) now
+      tc_fence_before();
+      mbar_arrive(&bars.s_free[x]);
+    }
     const int nvalid = N - j * kTileN;
     if (nvalid < kTileN) {  // only the ragged last key tile needs the mask
 #pragma unroll
@@ -363,6 +373,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars.p_full[x], 128);
       mbar_init(&bars.o_done[x], 1);
       mbar_init(&bars.pv_done[x], 1);
+      mbar_init(&bars.s_free[x], 128);
       mbar_init(&bars.drain[x], 1);
     }
     bars.abort = 0;

@@ -178,6 +178,8 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
   b += 2 * (static_cast<size_t>(s.BH) * s.n_pad * 4 + 256);       // lse2, delta
   b += s.elems * 4 + 256;                                         // dq accumulator
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
+  b += static_cast<size_t>(dg_reduce_scratch_floats(s.d)) * 4 + 256;  // dg slice partials
+  b += static_cast<size_t>(dg_reduce_tickets(s.d)) * 4 + 256;         // dg tickets
   return b + 256;
 }
 
@@ -364,13 +366,15 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   float* dqacc = cv.take<float>(s.elems);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
   float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
+  float* dg_slices = cv.take<float>(static_cast<size_t>(dg_reduce_scratch_floats(s.d)));
+  unsigned int* dg_tickets = cv.take<unsigned int>(static_cast<size_t>(dg_reduce_tickets(s.d)));
 
   int status = JATTN_OK;
   CUtensorMap mq, mk, mv, mdo;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, lse2, delta, dqacc, s.BH, s.N, s.n_pad,
-                         s.d, st);
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, lse2, delta, dqacc, dg_tickets, s.BH, s.N,
+                         s.n_pad, s.d, st);
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
@@ -392,7 +396,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
     if (ce == cudaSuccess) {
       stage = "dg_reduce launch";
       Timed t(JATTN_KERNEL_DG_REDUCE, st);
-      ce = launch_dg_reduce(dgq_part, nparts_q, dgk_part, nparts_k, s.d, dgq, dgk, st);
+      ce = launch_dg_reduce(dgq_part, nparts_q, dgk_part, nparts_k, s.d, dg_slices, dg_tickets, dgq, dgk, st);
     }
     if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, stage, ce);
   }

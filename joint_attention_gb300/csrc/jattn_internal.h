@@ -32,12 +32,17 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 // rounded up to 128), with +inf / 0 in the pad rows.
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc, int BH,
-                            int N, int n_pad, int d, cudaStream_t st);
+                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc,
+                            unsigned int* tickets, int BH, int N, int n_pad, int d, cudaStream_t st);
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
                               uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, cudaStream_t st);
-cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* dgq, float* dgk,
-                             cudaStream_t st);
+// Gain-gradient reduction: slice_part holds dg_reduce_scratch_floats(d)
+// floats, tickets dg_reduce_tickets(d) counters that the backward
+// preparation kernel zeroes.
+cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* slice_part,
+                             unsigned int* tickets, float* dgq, float* dgk, cudaStream_t st);
+int dg_reduce_scratch_floats(int d);
+int dg_reduce_tickets(int d);
 int q_norm_bwd_parts();
 
 // --- tensor-core attention kernels ------------------------------------------

@@ -19,6 +19,7 @@ namespace {
 
 constexpr float kEps = 1e-6f;
 constexpr int kNormThreads = 256;
+constexpr int kDgSlices = 16;
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -78,20 +79,30 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
     g_k[i] = gk[sub * 8 + i];
   }
   const int64_t total = 2 * rows;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * RPB;
+  constexpr int U = 4;  // rows in flight per thread
   // The loop bound is block-uniform so every lane reaches the row shuffles.
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < total;
-       base += static_cast<int64_t>(gridDim.x) * RPB) {
-    const int64_t rr = base + threadIdx.x / TPR;
-    const bool valid = rr < total;
-    const bool is_k = rr >= rows;
-    const int64_t idx = (is_k ? rr - rows : rr) * TPR + sub;
-    const uint4 w = valid ? (is_k ? k[idx] : q[idx]) : make_uint4(0u, 0u, 0u, 0u);
-    float g[8];
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < total; base += U * step) {
+    uint4 w[U];
+    int64_t idx[U];
+    bool valid[U], is_k[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) g[i] = is_k ? g_k[i] : g_q[i];
-    float r;
-    const uint4 y = norm_chunk<TPR>(w, g, &r);
-    if (valid) (is_k ? khat : qhat)[idx] = y;
+    for (int u = 0; u < U; ++u) {
+      const int64_t rr = base + u * step + threadIdx.x / TPR;
+      valid[u] = rr < total;
+      is_k[u] = rr >= rows;
+      idx[u] = (is_k[u] ? rr - rows : rr) * TPR + sub;
+      w[u] = valid[u] ? (is_k[u] ? k[idx[u]] : q[idx[u]]) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float g[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = is_k[u] ? g_k[i] : g_q[i];
+      float r;
+      const uint4 y = norm_chunk<TPR>(w[u], g, &r);
+      if (valid[u]) (is_k[u] ? khat : qhat)[idx[u]] = y;
+    }
   }
 }
 
@@ -105,7 +116,8 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
     float* __restrict__ rk, float* __restrict__ lse2, float* __restrict__ delta, float4* __restrict__ dqacc,
-    int N, int n_pad, int64_t padded_rows) {
+    unsigned int* __restrict__ tickets, int n_tickets, int N, int n_pad, int64_t padded_rows) {
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < n_tickets) tickets[threadIdx.x] = 0u;
   constexpr int TPR = D / 8;
   constexpr int RPB = kNormThreads / TPR;
   const int sub = threadIdx.x % TPR;
@@ -174,30 +186,46 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
     g[i] = gq[sub * 8 + i];
     acc[i] = 0.f;
   }
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < rows;
-       base += static_cast<int64_t>(gridDim.x) * RPB) {
-    const int64_t row = base + threadIdx.x / TPR;
-    const bool valid = row < rows;
-    const int64_t idx = (valid ? row : 0) * TPR + sub;
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 a = valid ? dqacc[idx * 2] : z4, b = valid ? dqacc[idx * 2 + 1] : z4;
-    const float dh[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
-                         b.x * scale, b.y * scale, b.z * scale, b.w * scale};
-    float x[8];
-    unpack8(valid ? q[idx] : make_uint4(0u, 0u, 0u, 0u), x);
-    const float r = valid ? rq[row] : 0.f;
-    float dot = 0.f;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * RPB;
+  constexpr int U = 2;  // rows in flight per thread
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < rows; base += U * step) {
+    float4 va[U], vb[U];
+    uint4 vq[U];
+    float vr[U];
+    bool valid[U];
+    int64_t idx[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dot = fmaf(g[i] * dh[i], x[i], dot);
-    dot = row_sum<TPR>(dot);
-    const float c = r * r * r * (1.f / D) * dot;
-    float y[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      y[i] = r * g[i] * dh[i] - c * x[i];
-      acc[i] = fmaf(dh[i], x[i] * r, acc[i]);
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = base + u * step + threadIdx.x / TPR;
+      valid[u] = row < rows;
+      idx[u] = (valid[u] ? row : 0) * TPR + sub;
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      va[u] = valid[u] ? dqacc[idx[u] * 2] : z4;
+      vb[u] = valid[u] ? dqacc[idx[u] * 2 + 1] : z4;
+      vq[u] = valid[u] ? q[idx[u]] : make_uint4(0u, 0u, 0u, 0u);
+      vr[u] = valid[u] ? rq[valid[u] ? row : 0] : 0.f;
     }
-    if (valid) dq[idx] = pack8(y);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 a = va[u], b = vb[u];
+      const float dh[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
+                           b.x * scale, b.y * scale, b.z * scale, b.w * scale};
+      float x[8];
+      unpack8(vq[u], x);
+      const float r = vr[u];
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot = fmaf(g[i] * dh[i], x[i], dot);
+      dot = row_sum<TPR>(dot);
+      const float c = r * r * r * (1.f / D) * dot;
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        y[i] = r * g[i] * dh[i] - c * x[i];
+        acc[i] = fmaf(dh[i], x[i] * r, acc[i]);
+      }
+      if (valid[u]) dq[idx[u]] = pack8(y);
+    }
   }
   // Block reduction of acc over the RPB row slots (fixed order).
   __shared__ float red[kNormThreads / TPR][D];
@@ -212,35 +240,54 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
   }
 }
 
-// Fixed-order reduction of the gain-gradient partials.  blockIdx.y selects
-// dgq (0) or dgk (1); each block owns 32 columns: thread (x, y) sums partial
-// rows y, y + 32, y + 64, ... of column x (coalesced 128-byte rows), then the
-// 32 slices are added in index order.  Same grid, same order, every call.
-__global__ void __launch_bounds__(1024) dg_reduce_kernel(const float* __restrict__ part_q, int nq,
-                                                         const float* __restrict__ part_k, int nk, int d,
-                                                         float* __restrict__ dgq, float* __restrict__ dgk) {
-  __shared__ float slice[32][33];
-  const float* part = blockIdx.y == 0 ? part_q : part_k;
-  const int nparts = blockIdx.y == 0 ? nq : nk;
+// Fixed-order reduction of the gain-gradient partials in one launch.
+// blockIdx.z selects dgq (0) or dgk (1), blockIdx.x a group of 32 columns,
+// blockIdx.y one of kDgSlices contiguous slices of the partial rows.  Each
+// block sums its slice (thread (x, y) takes rows y, y + 8, ...; the 8 row
+// lanes are then added in index order) into slice_part; the last block to
+// finish a (array, column group) - found with an atomic ticket - adds the
+// slices in index order.  Same grid, same order, every call; the tickets are
+// zeroed by the backward preparation kernel and reset here.
+__global__ void __launch_bounds__(256) dg_reduce_kernel(const float* __restrict__ part_q, int nq,
+                                                        const float* __restrict__ part_k, int nk, int d,
+                                                        float* __restrict__ slice_part,
+                                                        unsigned int* __restrict__ tickets, float* __restrict__ dgq,
+                                                        float* __restrict__ dgk) {
+  __shared__ float lanes[8][33];
+  __shared__ bool last;
+  const int arr = blockIdx.z;
+  const float* part = arr == 0 ? part_q : part_k;
+  const int nparts = arr == 0 ? nq : nk;
   const int c = blockIdx.x * 32 + threadIdx.x;
-  // Eight independent partial sums keep eight loads in flight per thread;
-  // they are combined in a fixed order.
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (c < d) {
-    int p = threadIdx.y;
-    for (; p + 7 * 32 < nparts; p += 8 * 32) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] += part[static_cast<size_t>(p + u * 32) * d + c];
-    }
-    for (; p < nparts; p += 32) acc[0] += part[static_cast<size_t>(p) * d + c];
-  }
-  const float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-  slice[threadIdx.y][threadIdx.x] = s;
+  const int s = blockIdx.y;
+  const int r0 = static_cast<int>((static_cast<int64_t>(nparts) * s) / kDgSlices);
+  const int r1 = static_cast<int>((static_cast<int64_t>(nparts) * (s + 1)) / kDgSlices);
+  float acc = 0.f;
+  if (c < d)
+    for (int p = r0 + static_cast<int>(threadIdx.y); p < r1; p += 8) acc += part[static_cast<size_t>(p) * d + c];
+  lanes[threadIdx.y][threadIdx.x] = acc;
   __syncthreads();
-  if (threadIdx.y == 0 && c < d) {
+  if (threadIdx.y == 0) {
     float t = 0.f;
-    for (int y = 0; y < 32; ++y) t += slice[y][threadIdx.x];
-    (blockIdx.y == 0 ? dgq : dgk)[c] = t;
+    for (int y = 0; y < 8; ++y) t += lanes[y][threadIdx.x];
+    if (c < d) slice_part[(static_cast<size_t>(arr) * kDgSlices + s) * d + c] = t;
+    __threadfence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && threadIdx.y == 0) {
+    const unsigned int ticket = atomicAdd(&tickets[arr * gridDim.x + blockIdx.x], 1u);
+    last = ticket == kDgSlices - 1;
+  }
+  __syncthreads();
+  if (last && threadIdx.y == 0) {
+    __threadfence();
+    if (c < d) {
+      float t = 0.f;
+      for (int q = 0; q < kDgSlices; ++q)
+        t += __ldcg(&slice_part[(static_cast<size_t>(arr) * kDgSlices + q) * d + c]);
+      (arr == 0 ? dgq : dgk)[c] = t;
+    }
+    if (threadIdx.x == 0) tickets[arr * gridDim.x + blockIdx.x] = 0u;
   }
 }
 
@@ -281,8 +328,8 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc, int BH,
-                            int N, int n_pad, int d, cudaStream_t st) {
+                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc,
+                            unsigned int* tickets, int BH, int N, int n_pad, int d, cudaStream_t st) {
   const int64_t padded_rows = static_cast<int64_t>(BH) * n_pad;
   const int grid = row_grid(padded_rows, d);
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
@@ -290,12 +337,14 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
     bwd_prep_kernel<64><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
                                                         reinterpret_cast<uint4*>(qhat),
                                                         reinterpret_cast<uint4*>(khat), rq, rk, lse2, delta,
-                                                        reinterpret_cast<float4*>(dqacc), N, n_pad, padded_rows);
+                                                        reinterpret_cast<float4*>(dqacc), tickets,
+                                                        dg_reduce_tickets(d), N, n_pad, padded_rows);
   else
     bwd_prep_kernel<128><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
                                                          reinterpret_cast<uint4*>(qhat),
                                                          reinterpret_cast<uint4*>(khat), rq, rk, lse2, delta,
-                                                         reinterpret_cast<float4*>(dqacc), N, n_pad, padded_rows);
+                                                         reinterpret_cast<float4*>(dqacc), tickets,
+                                                         dg_reduce_tickets(d), N, n_pad, padded_rows);
   return cudaGetLastError();
 }
 
@@ -309,9 +358,13 @@ cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float
   return cudaGetLastError();
 }
 
-cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* dgq, float* dgk,
-                             cudaStream_t st) {
-  dg_reduce_kernel<<<dim3((d + 31) / 32, 2), dim3(32, 32), 0, st>>>(part_q, nq, part_k, nk, d, dgq, dgk);
+int dg_reduce_scratch_floats(int d) { return 2 * kDgSlices * d; }
+int dg_reduce_tickets(int d) { return 2 * ((d + 31) / 32); }
+
+cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* slice_part,
+                             unsigned int* tickets, float* dgq, float* dgk, cudaStream_t st) {
+  dg_reduce_kernel<<<dim3((d + 31) / 32, kDgSlices, 2), dim3(32, 8), 0, st>>>(part_q, nq, part_k, nk, d, slice_part,
+                                                                               tickets, dgq, dgk);
   return cudaGetLastError();
 }
 
