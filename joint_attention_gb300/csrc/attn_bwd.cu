@@ -15,13 +15,11 @@
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
-//               row (TMEM lane).  P^T is written back into TMEM as packed
-//               bf16 over the group's consumed S^T columns (A operand of the
-//               dV MMA); dS^T goes to shared memory in the MMA's swizzled
-//               layout (A operand of dQ) and, for d = 64, also into TMEM over
-//               the consumed dP^T columns (A operand of dK).  At the end group
-//               0 writes dv and group 1 applies the K-RMSNorm backward to dK
-//               (dk and this CTA's dgk partial).
+//               row (TMEM lane).  P^T is written into TMEM as packed bf16
+//               (A operand of the dV MMA); dS^T goes to shared memory in the
+//               MMA's swizzled layout (A operand of dK, and of dQ read
+//               MN-major).  At the end group 0 writes dv and group 1 applies
+//               the K-RMSNorm backward to dK (dk and this CTA's dgk partial).
 //   warps 8-11  dQ drain: one thread per query row moves dQ_i from TMEM to a
 //               padded shared-memory row and issues a bulk reduce-add of it.
 //   warp 12     TMA producer: K_j, V_j once; Q_i (+ LSE_i, D_i) and dO_i per
@@ -29,13 +27,12 @@
 //   warps 13-14 MMA issuers (d = 64): recompute (S, dP) and gradients (dV, dK,
 //               dQ); d = 128 uses warp 13 alone.
 //
-// d = 64 keeps the shared-memory traffic per tile low: K and V are copied
-// once into TMEM and are the A operands of S^T = K Q^T and dP^T = V dO^T, and
-// dK reads dS^T from TMEM, so those MMAs stream only their B operand from
-// shared memory.  TMEM (512 columns): S^T/P^T [0,128), dP^T/dS^T [128,256),
-// dV [256,320), dK [320,384), dQ [384,448), K [448,480), V [480,512).  The
-// recompute issuer overwrites S^T only after dV(i-1) and dP^T only after
-// dK(i-1) have completed.
+// d = 64: TMEM (512 columns) S^T [0,128), dP^T [128,256), dV [256,320),
+// dK [320,384), dQ [384,448), P^T [448,512) (packed bf16).  The compute
+// groups release S^T and dP^T as soon as they hold them in registers
+// (s_free, dp_free), so the recompute issuer computes S(i+1) and dP(i+1)
+// while tile i's P and dS are still being formed; P^T(i+1) is written only
+// after dV(i) has read P^T(i).
 //
 // d = 128: TMEM S^T/P^T [0,128), dP^T [128,256), dV [256,384), dK [384,512),
 // dQ over the dP^T columns; one issuer in the order dV(i), S(i+1), dK(i),
@@ -59,9 +56,8 @@ struct BwdCfg {
   static constexpr int kQStages = 2;
   static constexpr int kDOStages = (D == 64) ? 2 : 1;
   static constexpr int kDSBufs = 1;
-  // d = 64: two MMA issuers (recompute: S, dP; gradients: dV, dK, dQ), K / V
-  // and dS^T as TMEM A operands.  d = 128: one issuer, operands in shared
-  // memory.
+  // d = 64: two MMA issuers (recompute: S, dP; gradients: dV, dK, dQ) and
+  // P^T in its own TMEM columns.  d = 128: one issuer, P^T over S^T.
   static constexpr bool kTwoIssuers = (D == 64);
   static constexpr int kDQCols = (D == 64) ? 64 : 32;        // dQ columns drained per pass
   static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // padded staging row
@@ -78,8 +74,7 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
-  static constexpr uint32_t kColKA = 448;  // d = 64 only: K as packed bf16 (32 columns)
-  static constexpr uint32_t kColVA = 480;  // d = 64 only: V as packed bf16
+  static constexpr uint32_t kColP = (D == 64) ? 448 : 0;  // P^T (packed bf16)
   static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
   static constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);      // dQ
@@ -94,8 +89,8 @@ struct BwdBars {
   uint64_t ds_free[2];
   uint64_t dq_full, dq_free;
   uint64_t kv_done;
-  uint64_t kv_tmem;
-  uint64_t dv_done, dk_done;
+  uint64_t s_free, dp_free;
+  uint64_t dv_done;
   uint64_t epi;
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -181,27 +176,14 @@ __device__ __forceinline__ void mma_dv(uint32_t tmem_d, uint32_t tmem_p, uint64_
   }
 }
 
-// D = A * B^T with A (K or V, 128 keys x d) packed in TMEM and B a K-major
-// 128 x d tile in shared memory.
+// dV (+)= P^T dO with P^T in its own 64 TMEM columns (queries 16kk..16kk+15
+// packed at columns 8kk..8kk+7), B = dO tile stored query-rows x d.
 template <int D>
-__device__ __forceinline__ void mma_tk(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-    umma_bf16_ts(tmem_d, tmem_a + kk * 8, dadd(b, off), idesc, kk > 0 ? 1u : 0u);
-  }
-}
-
-// dK (+)= dS^T Q with dS^T packed in TMEM over the dP^T columns (same
-// column pattern as P^T), B = Q tile stored query-rows x d (MN-major).
-template <int D>
-__device__ __forceinline__ void mma_dk_t(uint32_t tmem_d, uint32_t tmem_ds, uint64_t b, bool accumulate) {
+__device__ __forceinline__ void mma_dv_sep(uint32_t tmem_d, uint32_t tmem_p, uint64_t b, bool accumulate) {
   using C = BwdCfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-    umma_bf16_ts(tmem_d, tmem_ds + acol, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16_ts(tmem_d, tmem_p + kk * 8, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // dK (+)= dS^T Q: A = dS^T (K-major over queries), B = Q tile stored
@@ -227,36 +209,31 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
   }
 }
 
-// Two-issuer backward (d = 64).  Recompute issuer: S(i) = K Q_i^T and
-// dP(i) = V dO_i^T with K, V read from TMEM.  Gradient issuer: dV(i), dK(i)
-// (both with A from TMEM) and dQ(i).  A Q stage is released by both issuers
-// (S and dK read it), a dO stage likewise (dP, dV).  S(i+1) overwrites the
-// P^T(i) columns only after dV(i) completed, dP(i+1) the dS^T(i) columns only
-// after dK(i) completed.
+// Two-issuer backward (d = 64).  Recompute issuer: S(i) = K Q_i^T once the
+// compute groups hold S(i-1) in registers, dP(i) = V dO_i^T once they hold
+// dP(i-1).  Gradient issuer: dV(i) from P^T in TMEM, dK(i) and dQ(i) from
+// dS^T in shared memory.  A Q stage is released by both issuers (S and dK
+// read it), a dO stage likewise (dP, dV).
 template <int D>
 __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
   using C = BwdCfg<D>;
+  const uint64_t kK = sdesc_sw128(smem_u32(sm + C::kOffK), 16, 1024);
+  const uint64_t kV = sdesc_sw128(smem_u32(sm + C::kOffV), 16, 1024);
   volatile int* ab = &bars.abort;
   auto kQ = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile), 16, 1024); };
   auto kDO = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16, 1024); };
-  bool ok = mbar_wait(&bars.kv_tmem, 0, ab, dev_err);
+  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
   for (int i = 0; ok && i < nq; ++i) {
-    if (i > 0) {
-      if (!(ok = mbar_wait(&bars.p_ready, (i - 1) & 1, ab, dev_err))) break;
-      if (!(ok = mbar_wait(&bars.dv_done, (i - 1) & 1, ab, dev_err))) break;
-    }
+    if (i > 0 && !(ok = mbar_wait(&bars.s_free, (i - 1) & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_tk<D>(tmem + C::kColS, tmem + C::kColKA, kQ(i), C::kIdescSS);
+    mma_kk<D>(tmem + C::kColS, kK, kQ(i), C::kIdescSS);
     umma_commit(&bars.s_full);
     umma_commit(&bars.q_empty[i % C::kQStages]);
-    if (i > 0) {
-      if (!(ok = mbar_wait(&bars.ds_ready, (i - 1) & 1, ab, dev_err))) break;
-      if (!(ok = mbar_wait(&bars.dk_done, (i - 1) & 1, ab, dev_err))) break;
-    }
+    if (i > 0 && !(ok = mbar_wait(&bars.dp_free, (i - 1) & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_tk<D>(tmem + C::kColDP, tmem + C::kColVA, kDO(i), C::kIdescSS);
+    mma_kk<D>(tmem + C::kColDP, kV, kDO(i), C::kIdescSS);
     umma_commit(&bars.dp_full);
     umma_commit(&bars.do_empty[i % C::kDOStages]);
   }
@@ -273,20 +250,20 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, int
   auto mDO = [=](int i) {
     return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16384, 1024);
   };
-  const uint64_t mDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16384, 1024);
+  const uint32_t ds_addr = smem_u32(sm + C::kOffDS);
+  const uint64_t kDS = sdesc_sw128(ds_addr, 16, 1024), mDS = sdesc_sw128(ds_addr, 16384, 1024);
   bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
   for (int i = 0; ok && i < nq; ++i) {
     if (!(ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(i), i > 0);
+    mma_dv_sep<D>(tmem + C::kColDV, tmem + C::kColP, mDO(i), i > 0);
     umma_commit(&bars.dv_done);
     umma_commit(&bars.do_empty[i % C::kDOStages]);
     if (!(ok = mbar_wait(&bars.ds_ready, i & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
     tc_fence_after();
-    mma_dk_t<D>(tmem + C::kColDK, tmem + C::kColDP, mQ(i), i > 0);
-    umma_commit(&bars.dk_done);
+    mma_dk<D>(tmem + C::kColDK, kDS, mQ(i), i > 0);
     umma_commit(&bars.q_empty[i % C::kQStages]);
     if (i > 0 && !(ok = mbar_wait(&bars.dq_free, (i - 1) & 1, ab, dev_err))) break;
     tc_fence_after();
@@ -395,31 +372,12 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
   const bool key_live = kv0 + kr < N;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * g;   // this group's S^T columns
+  // P^T: own 32 packed columns (d = 64) or over the group's S^T columns
+  const uint32_t tP = C::kTwoIssuers ? tmem + lane_base + C::kColP + 32 * g : tS;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * g;
   const uint32_t swz = static_cast<uint32_t>(kr & 7);
   const float scale_log2 = scale * kLog2e;
   volatile int* ab = &bars.abort;
-
-  if (C::kTwoIssuers) {
-    // Copy this thread's key row of K (group 0) or V (group 1) from the
-    // swizzled shared-memory tile into TMEM as packed bf16 pairs.
-    bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    const uint8_t* tile = sm + (g == 0 ? C::kOffK : C::kOffV) + kr * 128;
-    uint32_t w[32];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + ((static_cast<uint32_t>(c) ^ swz) << 4));
-      w[4 * c] = v.x;
-      w[4 * c + 1] = v.y;
-      w[4 * c + 2] = v.z;
-      w[4 * c + 3] = v.w;
-    }
-    tmem_st32(tmem + lane_base + (g == 0 ? C::kColKA : C::kColVA), w);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&bars.kv_tmem);
-  }
 
   for (int i = 0; i < nq; ++i) {
     const int qs = i % C::kQStages;
@@ -437,6 +395,10 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
     tmem_ld32(tS, sall[0]);
     tmem_ld32(tS + 32, sall[1]);
     tmem_wait_ld();
+    if (C::kTwoIssuers) {  // S^T is in registers: S(i+1) may overwrite it
+      tc_fence_before();
+      mbar_arrive(&bars.s_free);
+    }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const uint32_t(&s)[32] = sall[c];
@@ -450,7 +412,13 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
         pp[(c * 32 + e) / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
         pp[(c * 32 + e) / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
       }
-      tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
+      if (C::kTwoIssuers && c == 0 && i > 0) {
+        // dV(i-1) must be done reading P^T(i-1) before it is overwritten.
+        ok = mbar_wait(&bars.dv_done, (i - 1) & 1, ab, dev_err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+      }
+      tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
     }
     tmem_wait_st();
     tc_fence_before();
@@ -466,6 +434,10 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
     tmem_ld32(tDP, dpall[0]);
     tmem_ld32(tDP + 32, dpall[1]);
     tmem_wait_ld();
+    if (C::kTwoIssuers) {  // dP^T is in registers: dP(i+1) may overwrite it
+      tc_fence_before();
+      mbar_arrive(&bars.dp_free);
+    }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const uint32_t(&dpv)[32] = dpall[c];
@@ -486,10 +458,7 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
         st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
                      dsw[e / 2 + 2], dsw[e / 2 + 3]);
       }
-      // dS^T also into TMEM over the dP^T columns just read (A operand of dK).
-      if (C::kTwoIssuers) tmem_st16(tDP + c * 16, dsw);
     }
-    if (C::kTwoIssuers) tmem_wait_st();
     tc_fence_before();
     fence_proxy_async_smem();
     mbar_arrive(&bars.ds_ready);
@@ -698,9 +667,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.kv_done, 1);
-    mbar_init(&bars.kv_tmem, 256);
+    mbar_init(&bars.s_free, 256);
+    mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.dv_done, 1);
-    mbar_init(&bars.dk_done, 1);
     mbar_init(&bars.epi, 128);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
