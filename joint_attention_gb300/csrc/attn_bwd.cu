@@ -10,20 +10,26 @@
 //   dV_j += P^T dO_i            dK_j += dS^T Q_i              (TMEM accumulators)
 //   dQ_i += dS K_j              (bulk fp32 reduce-add into a global accumulator)
 //
-// One CTA owns one 128-key tile of one (b, h) and streams every query tile
-// of the head.  480 threads:
+// Work unit: one 128-key tile j of one (b, h), streaming every query tile of
+// the head.  The kernel is persistent: one CTA per SM walks the units
+// u = blockIdx.x, blockIdx.x + gridDim.x, ... with every barrier phase
+// running on across units, so the next unit's K/V load and first S / dP
+// products overlap the current unit's last tiles and its epilogue.
+// 480 threads:
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
 //               row (TMEM lane).  P^T is written into TMEM as packed bf16
 //               (A operand of the dV MMA); dS^T goes to shared memory in the
 //               MMA's swizzled layout (A operand of dK, and of dQ read
-//               MN-major).  At the end group 0 writes dv and group 1 applies
-//               the K-RMSNorm backward to dK (dk and this CTA's dgk partial).
+//               MN-major).
 //   warps 8-11  dQ drain: one thread per query row moves dQ_i from TMEM to a
 //               padded shared-memory row and issues a bulk reduce-add of it.
-//   warp 12     TMA producer: K_j, V_j once; Q_i (+ LSE_i, D_i) and dO_i per
-//               query tile through small rings.
+//               At the end of a unit the same threads (now one per key row)
+//               write dv, apply the K-RMSNorm backward to dK (dk and the
+//               unit's dgk partial) and release the accumulators.
+//   warp 12     TMA producer: K_j, V_j per unit (double-buffered for d = 64);
+//               Q_i (+ LSE_i, D_i) and dO_i per query tile through rings.
 //   warps 13-14 MMA issuers (d = 64): recompute (S, dP) and gradients (dV, dK,
 //               dQ); d = 128 uses warp 13 alone.
 //
@@ -56,14 +62,15 @@ struct BwdCfg {
   static constexpr int kQStages = 2;
   static constexpr int kDOStages = (D == 64) ? 2 : 1;
   static constexpr int kDSBufs = 1;
+  // K/V buffers: two let the next unit's keys load during the current unit.
+  static constexpr int kKVBufs = (D == 64) ? 2 : 1;
   // d = 64: two MMA issuers (recompute: S, dP; gradients: dV, dK, dQ) and
   // P^T in its own TMEM columns.  d = 128: one issuer, P^T over S^T.
   static constexpr bool kTwoIssuers = (D == 64);
   static constexpr int kDQCols = (D == 64) ? 64 : 32;        // dQ columns drained per pass
   static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // padded staging row
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kTile;
-  static constexpr int kOffQ = 2 * kTile;                     // + stage * kTile
+  static constexpr int kOffKV = 0;                            // + buf * 2 * kTile: K, then V
+  static constexpr int kOffQ = kKVBufs * 2 * kTile;           // + stage * kTile
   static constexpr int kOffDO = kOffQ + kQStages * kTile;     // + stage * kTile
   static constexpr int kOffDS = kOffDO + kDOStages * kTile;   // + buf * 32 KB (128 x 128 bf16)
   static constexpr int kOffDQ = kOffDS + kDSBufs * 128 * 128 * 2;
@@ -78,17 +85,30 @@ struct BwdCfg {
   static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKM = idesc_bf16_f32(128, D, false, true);     // dV (A in TMEM), dK
   static constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);      // dQ
+  static __device__ __forceinline__ int off_k(int b) { return kOffKV + b * 2 * kTile; }
+  static __device__ __forceinline__ int off_v(int b) { return kOffKV + b * 2 * kTile + kTile; }
+};
+
+// Units: u -> (bh = u / nkt, key tile j = u % nkt); CTA c takes u = c,
+// c + gridDim.x, ...  Query tiles are counted on across units (t = ui * nkt
+// + i for the ui-th unit of this CTA), and every ring / handshake barrier
+// takes its phase from that count.
+struct BwdWork {
+  int N;
+  int nkt;    // key tiles per head == query tiles per head
+  int units;  // BH * nkt
 };
 
 struct BwdBars {
-  uint64_t kv_full;
+  uint64_t kv_full[2], kv_empty[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
   uint64_t s_full, dp_full;
   uint64_t p_ready, ds_ready;
   uint64_t ds_free[2];
   uint64_t dq_full, dq_free;
-  uint64_t kv_done;
+  uint64_t acc_full;                // a unit's dV / dK accumulators are final
+  uint64_t acc_free_v, acc_free_k;  // ... and have been read out of TMEM
   uint64_t s_free, dp_free;
   uint64_t dv_done;
   uint64_t epi;
@@ -107,7 +127,7 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
 
 template <int D>
 __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
-                             const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, int bh, int kv0, int nq,
+                             const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, const BwdWork& w,
                              const float* lse2_pad, const float* delta_pad, int n_pad, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(mq);
@@ -115,32 +135,42 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
   tma_prefetch_desc(mv);
   tma_prefetch_desc(mdo);
   volatile int* ab = &bars.abort;
-  mbar_arrive_expect_tx(&bars.kv_full, 2u * C::kTile);
-  for (int blk = 0; blk < D / 64; ++blk) {
-    tma_load_3d(sm + C::kOffK + blk * 16384, mk, &bars.kv_full, blk * 64, kv0, bh);
-    tma_load_3d(sm + C::kOffV + blk * 16384, mv, &bars.kv_full, blk * 64, kv0, bh);
-  }
-  int nq_issued = 0, ndo_issued = 0;
-  for (int i = 0; i < nq; ++i) {
-    const int qs = i % C::kQStages;
-    if (i >= C::kQStages && !mbar_wait(&bars.q_empty[qs], ((i / C::kQStages) - 1) & 1, ab, dev_err)) break;
-    mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
-    const size_t prow = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
-    bulk_load(bars.lse2[qs], lse2_pad + prow, 512, &bars.q_full[qs]);
-    bulk_load(bars.delta[qs], delta_pad + prow, 512, &bars.q_full[qs]);
-    for (int blk = 0; blk < D / 64; ++blk)
-      tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, i * 128, bh);
-    ++nq_issued;
-    const int ds = i % C::kDOStages;
-    if (i >= C::kDOStages && !mbar_wait(&bars.do_empty[ds], ((i / C::kDOStages) - 1) & 1, ab, dev_err)) break;
-    mbar_arrive_expect_tx(&bars.do_full[ds], C::kTile);
-    for (int blk = 0; blk < D / 64; ++blk)
-      tma_load_3d(sm + C::kOffDO + ds * C::kTile + blk * 16384, mdo, &bars.do_full[ds], blk * 64, i * 128, bh);
-    ++ndo_issued;
+  int nkv_issued = 0, nq_issued = 0, ndo_issued = 0;
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
+    const int b = ui % C::kKVBufs;
+    if (ui >= C::kKVBufs && !(ok = mbar_wait(&bars.kv_empty[b], ((ui / C::kKVBufs) - 1) & 1, ab, dev_err))) break;
+    mbar_arrive_expect_tx(&bars.kv_full[b], 2u * C::kTile);
+    for (int blk = 0; blk < D / 64; ++blk) {
+      tma_load_3d(sm + C::off_k(b) + blk * 16384, mk, &bars.kv_full[b], blk * 64, kv0, bh);
+      tma_load_3d(sm + C::off_v(b) + blk * 16384, mv, &bars.kv_full[b], blk * 64, kv0, bh);
+    }
+    ++nkv_issued;
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = ui * w.nkt + i;
+      const int qs = t % C::kQStages;
+      if (t >= C::kQStages && !(ok = mbar_wait(&bars.q_empty[qs], ((t / C::kQStages) - 1) & 1, ab, dev_err))) break;
+      mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
+      const size_t prow = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
+      bulk_load(bars.lse2[qs], lse2_pad + prow, 512, &bars.q_full[qs]);
+      bulk_load(bars.delta[qs], delta_pad + prow, 512, &bars.q_full[qs]);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, i * 128, bh);
+      ++nq_issued;
+      const int ds = t % C::kDOStages;
+      if (t >= C::kDOStages && !(ok = mbar_wait(&bars.do_empty[ds], ((t / C::kDOStages) - 1) & 1, ab, dev_err)))
+        break;
+      mbar_arrive_expect_tx(&bars.do_full[ds], C::kTile);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d(sm + C::kOffDO + ds * C::kTile + blk * 16384, mdo, &bars.do_full[ds], blk * 64, i * 128, bh);
+      ++ndo_issued;
+    }
   }
   if (*ab) {
     // Aborted: let the copies already in flight land before the CTA exits.
-    mbar_wait_drain(&bars.kv_full, 0);
+    for (int t = (nkv_issued > C::kKVBufs ? nkv_issued - C::kKVBufs : 0); t < nkv_issued; ++t)
+      mbar_wait_drain(&bars.kv_full[t % C::kKVBufs], (t / C::kKVBufs) & 1);
     for (int t = (nq_issued > C::kQStages ? nq_issued - C::kQStages : 0); t < nq_issued; ++t)
       mbar_wait_drain(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1);
     for (int t = (ndo_issued > C::kDOStages ? ndo_issued - C::kDOStages : 0); t < ndo_issued; ++t)
@@ -162,15 +192,14 @@ __device__ __forceinline__ void mma_kk(uint32_t tmem_d, uint64_t a, uint64_t b, 
   }
 }
 
-// dV (+)= P^T dO: A = P^T from TMEM (queries 0-63 packed in columns [0,32),
-// queries 64-127 in [64,96) of the S^T region), B = dO tile stored
+// dV (+)= P^T dO: A = P^T from TMEM over the S^T columns (queries 0-63
+// packed in columns [0,32), queries 64-127 in [64,96)), B = dO tile stored
 // query-rows x d (MN-major).
 template <int D>
 __device__ __forceinline__ void mma_dv(uint32_t tmem_d, uint32_t tmem_p, uint64_t b, bool accumulate) {
   using C = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    // group 0's queries are packed at columns [0,32), group 1's at [64,96)
     const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
     umma_bf16_ts(tmem_d, tmem_p + acol, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
   }
@@ -209,154 +238,169 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
   }
 }
 
-// Two-issuer backward (d = 64).  Recompute issuer: S(i) = K Q_i^T once the
-// compute groups hold S(i-1) in registers, dP(i) = V dO_i^T once they hold
-// dP(i-1).  Gradient issuer: dV(i) from P^T in TMEM, dK(i) and dQ(i) from
+// Two-issuer backward (d = 64).  Recompute issuer: S(t) = K Q_t^T once the
+// compute groups hold S(t-1) in registers, dP(t) = V dO_t^T once they hold
+// dP(t-1).  Gradient issuer: dV(t) from P^T in TMEM, dK(t) and dQ(t) from
 // dS^T in shared memory.  A Q stage is released by both issuers (S and dK
-// read it), a dO stage likewise (dP, dV).
+// read it), a dO stage likewise (dP, dV), and a K/V buffer likewise (the
+// unit's last dP and last dQ).
 template <int D>
-__device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
+__device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w,
+                                  uint32_t* dev_err) {
   using C = BwdCfg<D>;
-  const uint64_t kK = sdesc_sw128(smem_u32(sm + C::kOffK), 16, 1024);
-  const uint64_t kV = sdesc_sw128(smem_u32(sm + C::kOffV), 16, 1024);
   volatile int* ab = &bars.abort;
-  auto kQ = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile), 16, 1024); };
-  auto kDO = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16, 1024); };
-  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
-  for (int i = 0; ok && i < nq; ++i) {
-    if (i > 0 && !(ok = mbar_wait(&bars.s_free, (i - 1) & 1, ab, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_kk<D>(tmem + C::kColS, kK, kQ(i), C::kIdescSS);
-    umma_commit(&bars.s_full);
-    umma_commit(&bars.q_empty[i % C::kQStages]);
-    if (i > 0 && !(ok = mbar_wait(&bars.dp_free, (i - 1) & 1, ab, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_kk<D>(tmem + C::kColDP, kV, kDO(i), C::kIdescSS);
-    umma_commit(&bars.dp_full);
-    umma_commit(&bars.do_empty[i % C::kDOStages]);
+  auto kQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16, 1024); };
+  auto kDO = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16, 1024); };
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int b = ui % C::kKVBufs;
+    if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
+    const uint64_t kK = sdesc_sw128(smem_u32(sm + C::off_k(b)), 16, 1024);
+    const uint64_t kV = sdesc_sw128(smem_u32(sm + C::off_v(b)), 16, 1024);
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = ui * w.nkt + i;
+      if (t > 0 && !(ok = mbar_wait(&bars.s_free, (t - 1) & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
+      tc_fence_after();
+      mma_kk<D>(tmem + C::kColS, kK, kQ(t), C::kIdescSS);
+      umma_commit(&bars.s_full);
+      umma_commit(&bars.q_empty[t % C::kQStages]);
+      if (t > 0 && !(ok = mbar_wait(&bars.dp_free, (t - 1) & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.do_full[t % C::kDOStages], (t / C::kDOStages) & 1, ab, dev_err))) break;
+      tc_fence_after();
+      mma_kk<D>(tmem + C::kColDP, kV, kDO(t), C::kIdescSS);
+      umma_commit(&bars.dp_full);
+      umma_commit(&bars.do_empty[t % C::kDOStages]);
+    }
+    if (ok) umma_commit(&bars.kv_empty[b]);
   }
   umma_commit(&bars.drain[0]);
   mbar_wait_drain(&bars.drain[0], 0);
 }
 
 template <int D>
-__device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
+__device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w,
+                                  uint32_t* dev_err) {
   using C = BwdCfg<D>;
-  const uint64_t mK = sdesc_sw128(smem_u32(sm + C::kOffK), 16384, 1024);
   volatile int* ab = &bars.abort;
-  auto mQ = [=](int i) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile), 16384, 1024); };
-  auto mDO = [=](int i) {
-    return sdesc_sw128(smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile), 16384, 1024);
+  auto mQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16384, 1024); };
+  auto mDO = [=](int t) {
+    return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16384, 1024);
   };
   const uint32_t ds_addr = smem_u32(sm + C::kOffDS);
   const uint64_t kDS = sdesc_sw128(ds_addr, 16, 1024), mDS = sdesc_sw128(ds_addr, 16384, 1024);
-  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
-  for (int i = 0; ok && i < nq; ++i) {
-    if (!(ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_dv_sep<D>(tmem + C::kColDV, tmem + C::kColP, mDO(i), i > 0);
-    umma_commit(&bars.dv_done);
-    umma_commit(&bars.do_empty[i % C::kDOStages]);
-    if (!(ok = mbar_wait(&bars.ds_ready, i & 1, ab, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_dk<D>(tmem + C::kColDK, kDS, mQ(i), i > 0);
-    umma_commit(&bars.q_empty[i % C::kQStages]);
-    if (i > 0 && !(ok = mbar_wait(&bars.dq_free, (i - 1) & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_dq<D>(tmem + C::kColDQ, mDS, mK);
-    umma_commit(&bars.dq_full);
-    umma_commit(&bars.ds_free[0]);
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int b = ui % C::kKVBufs;
+    if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
+    const uint64_t mK = sdesc_sw128(smem_u32(sm + C::off_k(b)), 16384, 1024);
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = ui * w.nkt + i;
+      if (!(ok = mbar_wait(&bars.p_ready, t & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.do_full[t % C::kDOStages], (t / C::kDOStages) & 1, ab, dev_err))) break;
+      // The previous unit's dV has been read out of TMEM.
+      if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_v, (ui - 1) & 1, ab, dev_err))) break;
+      tc_fence_after();
+      mma_dv_sep<D>(tmem + C::kColDV, tmem + C::kColP, mDO(t), i > 0);
+      umma_commit(&bars.dv_done);
+      umma_commit(&bars.do_empty[t % C::kDOStages]);
+      if (!(ok = mbar_wait(&bars.ds_ready, t & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
+      if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_k, (ui - 1) & 1, ab, dev_err))) break;
+      tc_fence_after();
+      mma_dk<D>(tmem + C::kColDK, kDS, mQ(t), i > 0);
+      umma_commit(&bars.q_empty[t % C::kQStages]);
+      if (t > 0 && !(ok = mbar_wait(&bars.dq_free, (t - 1) & 1, ab, dev_err))) break;
+      tc_fence_after();
+      mma_dq<D>(tmem + C::kColDQ, mDS, mK);
+      umma_commit(&bars.dq_full);
+      umma_commit(&bars.ds_free[0]);
+    }
+    if (ok) {
+      umma_commit(&bars.acc_full);
+      umma_commit(&bars.kv_empty[b]);
+    }
   }
-  if (ok) umma_commit(&bars.kv_done);
   umma_commit(&bars.drain[1]);
   mbar_wait_drain(&bars.drain[1], 0);
 }
 
+// Single-issuer backward (d = 128), per unit: S(0), dP(0), then per tile
+// dV(i), S(i+1), dK(i), dQ(i) (into the dP^T columns), dP(i+1) once dQ(i) is
+// drained.
 template <int D>
-__device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint32_t* dev_err) {
+__device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, uint32_t* dev_err) {
   using C = BwdCfg<D>;
-  // Base descriptors: K-major (LBO unused) for S / dP / dK operands, MN-major
-  // with 64-column blocks 16 KB apart for the B operands of dV, dK, dQ and
-  // the A operand of dQ.
-  const uint32_t aK = smem_u32(sm + C::kOffK), aV = smem_u32(sm + C::kOffV);
-  const uint64_t kK = sdesc_sw128(aK, 16, 1024), kV = sdesc_sw128(aV, 16, 1024);
-  const uint64_t mK = sdesc_sw128(aK, 16384, 1024);
   volatile int* ab = &bars.abort;
-  auto qaddr = [=](int i) { return smem_u32(sm + C::kOffQ + (i % C::kQStages) * C::kTile); };
-  auto doaddr = [=](int i) { return smem_u32(sm + C::kOffDO + (i % C::kDOStages) * C::kTile); };
-  auto dsaddr = [=](int i) { return smem_u32(sm + C::kOffDS + (i % C::kDSBufs) * (128 * 128 * 2)); };
-  auto kQ = [=](int i) { return sdesc_sw128(qaddr(i), 16, 1024); };
-  auto mQ = [=](int i) { return sdesc_sw128(qaddr(i), 16384, 1024); };
-  auto kDO = [=](int i) { return sdesc_sw128(doaddr(i), 16, 1024); };
-  auto mDO = [=](int i) { return sdesc_sw128(doaddr(i), 16384, 1024); };
-  auto kDS = [=](int i) { return sdesc_sw128(dsaddr(i), 16, 1024); };
-  auto mDS = [=](int i) { return sdesc_sw128(dsaddr(i), 16384, 1024); };
-  auto q_ph = [](int i) { return static_cast<uint32_t>((i / C::kQStages) & 1); };
-  auto do_ph = [](int i) { return static_cast<uint32_t>((i / C::kDOStages) & 1); };
+  auto qaddr = [=](int t) { return smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile); };
+  auto doaddr = [=](int t) { return smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile); };
+  auto dsaddr = [=](int t) { return smem_u32(sm + C::kOffDS + (t % C::kDSBufs) * (128 * 128 * 2)); };
+  auto kQ = [=](int t) { return sdesc_sw128(qaddr(t), 16, 1024); };
+  auto mQ = [=](int t) { return sdesc_sw128(qaddr(t), 16384, 1024); };
+  auto kDO = [=](int t) { return sdesc_sw128(doaddr(t), 16, 1024); };
+  auto mDO = [=](int t) { return sdesc_sw128(doaddr(t), 16384, 1024); };
+  auto kDS = [=](int t) { return sdesc_sw128(dsaddr(t), 16, 1024); };
+  auto mDS = [=](int t) { return sdesc_sw128(dsaddr(t), 16384, 1024); };
+  auto q_ph = [](int t) { return static_cast<uint32_t>((t / C::kQStages) & 1); };
+  auto do_ph = [](int t) { return static_cast<uint32_t>((t / C::kDOStages) & 1); };
 
-  bool ok = mbar_wait(&bars.kv_full, 0, ab, dev_err);
-  if (ok) ok = mbar_wait(&bars.q_full[0], 0, ab, dev_err);
-  if (ok) {
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int b = ui % C::kKVBufs;
+    const int t0 = ui * w.nkt;
+    if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
+    const uint32_t aK = smem_u32(sm + C::off_k(b)), aV = smem_u32(sm + C::off_v(b));
+    const uint64_t kK = sdesc_sw128(aK, 16, 1024), kV = sdesc_sw128(aV, 16, 1024);
+    const uint64_t mK = sdesc_sw128(aK, 16384, 1024);
+    if (!(ok = mbar_wait(&bars.q_full[t0 % C::kQStages], q_ph(t0), ab, dev_err))) break;
     tc_fence_after();
-    mma_kk<D>(tmem + C::kColS, kK, kQ(0), C::kIdescSS);
+    mma_kk<D>(tmem + C::kColS, kK, kQ(t0), C::kIdescSS);
     umma_commit(&bars.s_full);
-  }
-  if (ok) ok = mbar_wait(&bars.do_full[0], 0, ab, dev_err);
-  if (ok) {
+    // dP(t0) lands where the previous unit's last dQ was drained from.
+    if (t0 > 0 && !(ok = mbar_wait(&bars.dq_free, (t0 - 1) & 1, ab, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.do_full[t0 % C::kDOStages], do_ph(t0), ab, dev_err))) break;
     tc_fence_after();
-    mma_kk<D>(tmem + C::kColDP, kV, kDO(0), C::kIdescSS);
+    mma_kk<D>(tmem + C::kColDP, kV, kDO(t0), C::kIdescSS);
     umma_commit(&bars.dp_full);
-  }
-  for (int i = 0; ok && i < nq; ++i) {
-    // dV(i): needs P^T(i) in TMEM.
-    if (!(ok = mbar_wait(&bars.p_ready, i & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(i), i > 0);
-    umma_commit(&bars.do_empty[i % C::kDOStages]);
-    // S(i+1): overwrites the S^T/P^T columns behind dV(i).
-    if (i + 1 < nq) {
-      if (!(ok = mbar_wait(&bars.q_full[(i + 1) % C::kQStages], q_ph(i + 1), ab, dev_err))) break;
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = t0 + i;
+      // dV(t): needs P^T(t) in TMEM (and the previous unit's dV read out).
+      if (!(ok = mbar_wait(&bars.p_ready, t & 1, ab, dev_err))) break;
+      if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_v, (ui - 1) & 1, ab, dev_err))) break;
       tc_fence_after();
-      mma_kk<D>(tmem + C::kColS, kK, kQ(i + 1), C::kIdescSS);
-      umma_commit(&bars.s_full);
-    }
-    // dK(i): needs dS^T(i) in shared memory (compute is then done with dP(i)).
-    if (!(ok = mbar_wait(&bars.ds_ready, i & 1, ab, dev_err))) break;
-    tc_fence_after();
-    mma_dk<D>(tmem + C::kColDK, kDS(i), mQ(i), i > 0);
-    umma_commit(&bars.q_empty[i % C::kQStages]);
-    if (D == 64) {
-      if (i + 1 < nq) {
-        if (!(ok = mbar_wait(&bars.do_full[(i + 1) % C::kDOStages], do_ph(i + 1), ab, dev_err))) break;
+      mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(t), i > 0);
+      umma_commit(&bars.do_empty[t % C::kDOStages]);
+      // S(t+1): overwrites the S^T/P^T columns behind dV(t).
+      if (i + 1 < w.nkt) {
+        if (!(ok = mbar_wait(&bars.q_full[(t + 1) % C::kQStages], q_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
-        mma_kk<D>(tmem + C::kColDP, kV, kDO(i + 1), C::kIdescSS);
-        umma_commit(&bars.dp_full);
+        mma_kk<D>(tmem + C::kColS, kK, kQ(t + 1), C::kIdescSS);
+        umma_commit(&bars.s_full);
       }
-      if (i > 0 && !(ok = mbar_wait(&bars.dq_free, (i - 1) & 1, ab, dev_err))) break;
+      // dK(t): needs dS^T(t) in shared memory (compute is then done with dP(t)).
+      if (!(ok = mbar_wait(&bars.ds_ready, t & 1, ab, dev_err))) break;
+      if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_k, (ui - 1) & 1, ab, dev_err))) break;
       tc_fence_after();
-      mma_dq<D>(tmem + C::kColDQ, mDS(i), mK);
+      mma_dk<D>(tmem + C::kColDK, kDS(t), mQ(t), i > 0);
+      umma_commit(&bars.q_empty[t % C::kQStages]);
+      // dQ(t) lands in the dP^T columns (dP(t) already consumed); the drain
+      // of dQ(t-1) from those columns finished before dP(t) was issued.
+      mma_dq<D>(tmem + C::kColDQ, mDS(t), mK);
       umma_commit(&bars.dq_full);
-      umma_commit(&bars.ds_free[i % C::kDSBufs]);
-    } else {
-      // dQ(i) lands in the dP^T columns (dP(i) already consumed); the drain of
-      // dQ(i-1) from those columns finished before dP(i) was issued.
-      mma_dq<D>(tmem + C::kColDQ, mDS(i), mK);
-      umma_commit(&bars.dq_full);
-      umma_commit(&bars.ds_free[i % C::kDSBufs]);
-      if (i + 1 < nq) {
-        if (!(ok = mbar_wait(&bars.dq_free, i & 1, ab, dev_err))) break;
-        if (!(ok = mbar_wait(&bars.do_full[(i + 1) % C::kDOStages], do_ph(i + 1), ab, dev_err))) break;
+      umma_commit(&bars.ds_free[t % C::kDSBufs]);
+      if (i + 1 < w.nkt) {
+        if (!(ok = mbar_wait(&bars.dq_free, t & 1, ab, dev_err))) break;
+        if (!(ok = mbar_wait(&bars.do_full[(t + 1) % C::kDOStages], do_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
-        mma_kk<D>(tmem + C::kColDP, kV, kDO(i + 1), C::kIdescSS);
+        mma_kk<D>(tmem + C::kColDP, kV, kDO(t + 1), C::kIdescSS);
         umma_commit(&bars.dp_full);
       }
     }
+    if (ok) {
+      umma_commit(&bars.acc_full);
+      umma_commit(&bars.kv_empty[b]);
+    }
   }
-  if (ok) umma_commit(&bars.kv_done);
   // Every MMA issued above has completed once this barrier flips.
   umma_commit(&bars.drain[0]);
   mbar_wait_drain(&bars.drain[0], 0);
@@ -364,12 +408,11 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, int nq, uint3
 
 // Key-row threads of one compute group (query columns 64g .. 64g+63).
 template <int D>
-__device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, int bh, int kv0, int N, int nq,
-                            float scale, uint32_t* dev_err) {
+__device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, const BwdWork& w, float scale,
+                            uint32_t* dev_err) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kr = (warp & 3) * 32 + lane;  // key row in the tile == TMEM lane
-  const bool key_live = kv0 + kr < N;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * g;   // this group's S^T columns
   // P^T: own 32 packed columns (d = 64) or over the group's S^T columns
@@ -379,255 +422,272 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, in
   const float scale_log2 = scale * kLog2e;
   volatile int* ab = &bars.abort;
 
-  for (int i = 0; i < nq; ++i) {
-    const int qs = i % C::kQStages;
-    bool ok = mbar_wait(&bars.s_full, i & 1, ab, dev_err);
-    // This stage's LSE / D arrived with the query tile (already complete).
-    if (ok) ok = mbar_wait(&bars.q_full[qs], (i / C::kQStages) & 1, ab, dev_err);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-    // P^T = exp2(s log2e S^T - LSE2), packed bf16 pairs, back into TMEM over
-    // the S^T columns already read (chunk c -> 16 packed columns at 16c).
-    uint32_t pp[32];
-    // Both 32-column chunks of this group's S^T in flight at once: one TMEM
-    // round trip per phase instead of two.
-    uint32_t sall[2][32];
-    tmem_ld32(tS, sall[0]);
-    tmem_ld32(tS + 32, sall[1]);
-    tmem_wait_ld();
-    if (C::kTwoIssuers) {  // S^T is in registers: S(i+1) may overwrite it
-      tc_fence_before();
-      mbar_arrive(&bars.s_free);
-    }
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint32_t(&s)[32] = sall[c];
-#pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[qs][64 * g + c * 32 + e]);
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[e + 0]), scale_log2, -l4.x));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), scale_log2, -l4.y));
-        const float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), scale_log2, -l4.z));
-        const float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), scale_log2, -l4.w));
-        pp[(c * 32 + e) / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
-        pp[(c * 32 + e) / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
+  for (int u = blockIdx.x, ui = 0; u < w.units; u += gridDim.x, ++ui) {
+    const bool key_live = (u % w.nkt) * 128 + kr < w.N;
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = ui * w.nkt + i;
+      const int qs = t % C::kQStages;
+      bool ok = mbar_wait(&bars.s_full, t & 1, ab, dev_err);
+      // This stage's LSE / D arrived with the query tile (already complete).
+      if (ok) ok = mbar_wait(&bars.q_full[qs], (t / C::kQStages) & 1, ab, dev_err);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      tc_fence_after();
+      // P^T = exp2(s log2e S^T - LSE2), packed bf16 pairs into TMEM (chunk c
+      // -> 16 packed columns at 16c).
+      uint32_t pp[32];
+      // Both 32-column chunks of this group's S^T in flight at once.
+      uint32_t sall[2][32];
+      tmem_ld32(tS, sall[0]);
+      tmem_ld32(tS + 32, sall[1]);
+      tmem_wait_ld();
+      if (C::kTwoIssuers) {  // S^T is in registers: S(t+1) may overwrite it
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);
       }
-      if (C::kTwoIssuers && c == 0 && i > 0) {
-        // dV(i-1) must be done reading P^T(i-1) before it is overwritten.
-        ok = mbar_wait(&bars.dv_done, (i - 1) & 1, ab, dev_err);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc_fence_after();
-      }
-      tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&bars.p_ready);
-
-    ok = mbar_wait(&bars.dp_full, i & 1, ab, dev_err);
-    if (ok && i >= C::kDSBufs)
-      ok = mbar_wait(&bars.ds_free[i % C::kDSBufs], ((i / C::kDSBufs) - 1) & 1, ab, dev_err);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-    const uint32_t ds_row = smem_u32(sm + C::kOffDS + (i % C::kDSBufs) * (128 * 128 * 2)) + g * 16384 + kr * 128;
-    uint32_t dpall[2][32];
-    tmem_ld32(tDP, dpall[0]);
-    tmem_ld32(tDP + 32, dpall[1]);
-    tmem_wait_ld();
-    if (C::kTwoIssuers) {  // dP^T is in registers: dP(i+1) may overwrite it
-      tc_fence_before();
-      mbar_arrive(&bars.dp_free);
-    }
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint32_t(&dpv)[32] = dpall[c];
-      uint32_t dsw[16];
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t(&s)[32] = sall[c];
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        const int col = c * 32 + e;  // query column within this group's 64
-        const float4 d0 = *reinterpret_cast<const float4*>(&bars.delta[qs][64 * g + col]);
-        const float4 d1 = *reinterpret_cast<const float4*>(&bars.delta[qs][64 * g + col + 4]);
-        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint32_t pw = pp[col / 2 + h];
-          const float pa = __uint_as_float(pw << 16), pb = __uint_as_float(pw & 0xFFFF0000u);
-          dsw[e / 2 + h] = pack_bf16x2(pa * (__uint_as_float(dpv[e + 2 * h]) - dd[2 * h]),
-                                       pb * (__uint_as_float(dpv[e + 2 * h + 1]) - dd[2 * h + 1]));
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[qs][64 * g + c * 32 + e]);
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[e + 0]), scale_log2, -l4.x));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), scale_log2, -l4.y));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), scale_log2, -l4.z));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), scale_log2, -l4.w));
+          pp[(c * 32 + e) / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
+          pp[(c * 32 + e) / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
         }
-        st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
-                     dsw[e / 2 + 2], dsw[e / 2 + 3]);
+        if (C::kTwoIssuers && c == 0 && t > 0) {
+          // dV(t-1) must be done reading P^T(t-1) before it is overwritten.
+          ok = mbar_wait(&bars.dv_done, (t - 1) & 1, ab, dev_err);
+          if (!__all_sync(0xffffffffu, ok)) return;
+          tc_fence_after();
+        }
+        tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars.p_ready);
+
+      ok = mbar_wait(&bars.dp_full, t & 1, ab, dev_err);
+      if (ok && t >= C::kDSBufs)
+        ok = mbar_wait(&bars.ds_free[t % C::kDSBufs], ((t / C::kDSBufs) - 1) & 1, ab, dev_err);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      tc_fence_after();
+      const uint32_t ds_row = smem_u32(sm + C::kOffDS + (t % C::kDSBufs) * (128 * 128 * 2)) + g * 16384 + kr * 128;
+      uint32_t dpall[2][32];
+      tmem_ld32(tDP, dpall[0]);
+      tmem_ld32(tDP + 32, dpall[1]);
+      tmem_wait_ld();
+      if (C::kTwoIssuers) {  // dP^T is in registers: dP(t+1) may overwrite it
+        tc_fence_before();
+        mbar_arrive(&bars.dp_free);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t(&dpv)[32] = dpall[c];
+        uint32_t dsw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          const int col = c * 32 + e;  // query column within this group's 64
+          const float4 d0 = *reinterpret_cast<const float4*>(&bars.delta[qs][64 * g + col]);
+          const float4 d1 = *reinterpret_cast<const float4*>(&bars.delta[qs][64 * g + col + 4]);
+          const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const uint32_t pw = pp[col / 2 + h];
+            const float pa = __uint_as_float(pw << 16), pb = __uint_as_float(pw & 0xFFFF0000u);
+            dsw[e / 2 + h] = pack_bf16x2(pa * (__uint_as_float(dpv[e + 2 * h]) - dd[2 * h]),
+                                         pb * (__uint_as_float(dpv[e + 2 * h + 1]) - dd[2 * h + 1]));
+          }
+          st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
+                       dsw[e / 2 + 2], dsw[e / 2 + 3]);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.ds_ready);
     }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    mbar_arrive(&bars.ds_ready);
   }
 }
 
-// dV epilogue (compute group 0): TMEM row -> bf16 dv row.
+// Warps 8-11.  Per query tile: dQ_t from TMEM into a padded shared-memory
+// row (one thread per query row), then a bulk fp32 reduce-add of the row
+// into the global accumulator.  Per unit, once its accumulators are final
+// (one thread per key row):
+//   dv = bf16(dV acc);
+//   dk_hat = scale * dK acc; u = g * dk_hat; dk = r u - (r^3/d) k sum(u k);
+//   dgk partial = column sums over the tile's rows of dk_hat * k * r, taken
+//   through the staging rows in a fixed order.
 template <int D>
-__device__ void bwd_epilogue_dv(BwdBars& bars, uint32_t tmem, int bh, int kv0, int N, __nv_bfloat16* __restrict__ dv,
-                                uint32_t* dev_err) {
+__device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, float scale,
+                                   float* __restrict__ dqacc, const __nv_bfloat16* __restrict__ k_raw,
+                                   const float* __restrict__ rk, const float* __restrict__ gk,
+                                   __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                   float* __restrict__ dgk_part, uint32_t* dev_err) {
   using C = BwdCfg<D>;
+  constexpr int kRowFloats = C::kDQRowBytes / 4;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kr = (warp & 3) * 32 + lane;
-  const int n = kv0 + kr;
-  const bool key_live = n < N;
+  const int r128 = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQ) or key row (dV, dK)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  bool ok = mbar_wait(&bars.kv_done, 0, &bars.abort, dev_err);
-  if (!__all_sync(0xffffffffu, ok)) return;
-  tc_fence_after();
-  uint4* dvrow = reinterpret_cast<uint4*>(dv + (static_cast<size_t>(bh) * N + (key_live ? n : 0)) * D);
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t a[32];
-    tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
-    tmem_wait_ld();
-    if (key_live) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
-        w.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
-        w.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
-        w.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
-        dvrow[c * 4 + q] = w;
-      }
-    }
-  }
-}
-
-// dK epilogue (compute group 1): dk_hat = scale * acc; u = g * dk_hat;
-// dk = r u - (r^3/d) k sum(u k); dgk partial = sum over the tile's rows of
-// dk_hat * k * r (fixed-order column sum in shared memory).
-template <int D>
-__device__ void bwd_epilogue_dk(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, int kv0, int N, float scale,
-                                const __nv_bfloat16* __restrict__ k_raw, const float* __restrict__ rk,
-                                const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
-                                float* __restrict__ dgk_part, int part_index, uint32_t* dev_err) {
-  using C = BwdCfg<D>;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kr = (warp & 3) * 32 + lane;
-  const int n = kv0 + kr;
-  const bool key_live = n < N;
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  volatile int* ab = &bars.abort;
-  bool ok = mbar_wait(&bars.kv_done, 0, ab, dev_err);
-  if (!__all_sync(0xffffffffu, ok)) return;
-  tc_fence_after();
-  const size_t row_off = (static_cast<size_t>(bh) * N + (key_live ? n : 0)) * D;
-  const float r = key_live ? rk[static_cast<size_t>(bh) * N + n] : 0.f;
-  const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
-  const uint32_t tDK = tmem + lane_base + C::kColDK;
-  float dot = 0.f;
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t a[32];
-    tmem_ld32(tDK + c * 32, a);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-      const uint4 w = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-        dot = fmaf(gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(u[h] << 16), dot);
-        dot = fmaf(gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(u[h] & 0xFFFF0000u), dot);
-      }
-    }
-  }
-  const float coef = r * r * r * (1.f / D) * dot;
-  // Shared memory for the column sum: the query / dO rings, idle now.
-  float* red = reinterpret_cast<float*>(sm + C::kOffQ);
-  constexpr int kRedStride = D + 4;
-  static_assert(128 * kRedStride * 4 <= C::kOffDS - C::kOffQ, "dgk reduction buffer");
-  uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t a[32];
-    tmem_ld32(tDK + c * 32, a);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-      const uint4 w = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-      float y[8], gpart[8];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-        const float x0 = __uint_as_float(u[h] << 16), x1 = __uint_as_float(u[h] & 0xFFFF0000u);
-        const float dk0 = key_live ? __uint_as_float(a[e]) * scale : 0.f;
-        const float dk1 = key_live ? __uint_as_float(a[e + 1]) * scale : 0.f;
-        y[2 * h] = r * gk[col] * dk0 - coef * x0;
-        y[2 * h + 1] = r * gk[col + 1] * dk1 - coef * x1;
-        gpart[2 * h] = dk0 * x0 * r;
-        gpart[2 * h + 1] = dk1 * x1 * r;
-      }
-      if (key_live) {
-        uint4 o;
-        o.x = pack_bf16x2(y[0], y[1]);
-        o.y = pack_bf16x2(y[2], y[3]);
-        o.z = pack_bf16x2(y[4], y[5]);
-        o.w = pack_bf16x2(y[6], y[7]);
-        dkrow[c * 4 + c8] = o;
-      }
-      float4* dst = reinterpret_cast<float4*>(red + kr * kRedStride + c * 32 + c8 * 8);
-      dst[0] = make_float4(gpart[0], gpart[1], gpart[2], gpart[3]);
-      dst[1] = make_float4(gpart[4], gpart[5], gpart[6], gpart[7]);
-    }
-  }
-  // Bounded barrier among the 128 threads of this group.
-  mbar_arrive(&bars.epi);
-  ok = mbar_wait(&bars.epi, 0, ab, dev_err);
-  if (!ok) return;
-  if (kr < D) {
-    float s = 0.f;
-    for (int t = 0; t < 128; ++t) s += red[t * kRedStride + kr];
-    dgk_part[static_cast<size_t>(part_index) * D + kr] = s;
-  }
-}
-
-// Query-row threads: dQ_i from TMEM into a padded shared-memory row, then a
-// bulk fp32 reduce-add of the row into the global accumulator.
-template <int D>
-__device__ void bwd_dq_drain(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, int N, int nq,
-                             float* __restrict__ dqacc, uint32_t* dev_err) {
-  using C = BwdCfg<D>;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qr = (warp & 3) * 32 + lane;
-  const uint32_t tQ = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColDQ;
-  uint8_t* srow = sm + C::kOffDQ + qr * C::kDQRowBytes;
+  const uint32_t tQ = tmem + lane_base + C::kColDQ;
+  uint8_t* srow = sm + C::kOffDQ + r128 * C::kDQRowBytes;
   const uint32_t srow_a = smem_u32(srow);
   volatile int* ab = &bars.abort;
-  for (int i = 0; i < nq; ++i) {
-    bool ok = mbar_wait(&bars.dq_full, i & 1, ab, dev_err);
-    if (!__all_sync(0xffffffffu, ok)) break;
+  uint32_t epi_uses = 0;
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = ui * w.nkt + i;
+      ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      const int qrow = i * 128 + r128;
+      float* grow = dqacc + (static_cast<size_t>(bh) * w.N + (qrow < w.N ? qrow : 0)) * D;
+#pragma unroll
+      for (int pass = 0; pass < D / C::kDQCols; ++pass) {
+        bulk_wait_group_read0();  // the previous reduce has finished reading the row
+#pragma unroll
+        for (int c = 0; c < C::kDQCols / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tQ + pass * C::kDQCols + c * 32, a);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(srow_a + (c * 32 + q * 4) * 4, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+        }
+        if (pass == D / C::kDQCols - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars.dq_free);
+        }
+        fence_proxy_async_smem();
+        if (qrow < w.N) {
+          bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (!ok) break;
+
+    // ---- unit epilogue: this thread owns key row kv0 + r128 ----
+    ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
+    if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
-    const int qrow = i * 128 + qr;
-    float* grow = dqacc + (static_cast<size_t>(bh) * N + (qrow < N ? qrow : 0)) * D;
+    const int n = kv0 + r128;
+    const bool key_live = n < w.N;
+    const size_t row_off = (static_cast<size_t>(bh) * w.N + (key_live ? n : 0)) * D;
+    uint4* dvrow = reinterpret_cast<uint4*>(dv + row_off);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
+      tmem_wait_ld();
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        mbar_arrive(&bars.acc_free_v);
+      }
+      if (key_live) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
+          o.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
+          o.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
+          o.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
+          dvrow[c * 4 + q] = o;
+        }
+      }
+    }
+    const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
+    const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
+    const uint32_t tDK = tmem + lane_base + C::kColDK;
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tDK + c * 32, a);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = c8 * 8 + 2 * h, col = c * 32 + e;
+          dot = fmaf(gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(kx[h] << 16), dot);
+          dot = fmaf(gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(kx[h] & 0xFFFF0000u), dot);
+        }
+      }
+    }
+    const float coef = r * r * r * (1.f / D) * dot;
+    uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
+    const float* red = reinterpret_cast<const float*>(sm + C::kOffDQ);
+    bulk_wait_group_read0();  // the staging row is free for the column sums
 #pragma unroll
     for (int pass = 0; pass < D / C::kDQCols; ++pass) {
-      bulk_wait_group_read0();  // the previous reduce has finished reading the row
 #pragma unroll
-      for (int c = 0; c < C::kDQCols / 32; ++c) {
+      for (int cc = 0; cc < C::kDQCols / 32; ++cc) {
+        const int c = pass * (C::kDQCols / 32) + cc;
         uint32_t a[32];
-        tmem_ld32(tQ + pass * C::kDQCols + c * 32, a);
+        tmem_ld32(tDK + c * 32, a);
         tmem_wait_ld();
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars.acc_free_k);
+        }
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(srow_a + (c * 32 + q * 4) * 4, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+          float y[8], gpart[8];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int e = c8 * 8 + 2 * h, col = c * 32 + e;
+            const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
+            const float dk0 = key_live ? __uint_as_float(a[e]) * scale : 0.f;
+            const float dk1 = key_live ? __uint_as_float(a[e + 1]) * scale : 0.f;
+            y[2 * h] = r * gk[col] * dk0 - coef * x0;
+            y[2 * h + 1] = r * gk[col + 1] * dk1 - coef * x1;
+            gpart[2 * h] = dk0 * x0 * r;
+            gpart[2 * h + 1] = dk1 * x1 * r;
+          }
+          if (key_live) {
+            uint4 o;
+            o.x = pack_bf16x2(y[0], y[1]);
+            o.y = pack_bf16x2(y[2], y[3]);
+            o.z = pack_bf16x2(y[4], y[5]);
+            o.w = pack_bf16x2(y[6], y[7]);
+            dkrow[c * 4 + c8] = o;
+          }
+          const uint32_t soff = static_cast<uint32_t>((cc * 32 + c8 * 8) * 4);
+          st_shared_v4(srow_a + soff, __float_as_uint(gpart[0]), __float_as_uint(gpart[1]),
+                       __float_as_uint(gpart[2]), __float_as_uint(gpart[3]));
+          st_shared_v4(srow_a + soff + 16, __float_as_uint(gpart[4]), __float_as_uint(gpart[5]),
+                       __float_as_uint(gpart[6]), __float_as_uint(gpart[7]));
+        }
       }
-      if (pass == D / C::kDQCols - 1) {
-        tc_fence_before();
-        mbar_arrive(&bars.dq_free);
+      // Bounded barrier among the 128 drain threads: every row is staged.
+      mbar_arrive(&bars.epi);
+      ok = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      if (r128 < C::kDQCols) {
+        // Fixed-order column sum over the tile's 128 key rows.
+        const float* col = red + r128;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 8
+        for (int q = 0; q < 128; q += 4) {
+          s0 += col[(q + 0) * kRowFloats];
+          s1 += col[(q + 1) * kRowFloats];
+          s2 += col[(q + 2) * kRowFloats];
+          s3 += col[(q + 3) * kRowFloats];
+        }
+        dgk_part[static_cast<size_t>(u) * D + pass * C::kDQCols + r128] = (s0 + s1) + (s2 + s3);
       }
-      fence_proxy_async_smem();
-      if (qrow < N) {
-        bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
-        bulk_commit_group();
-      }
+      // ... and every column has been summed before the rows are rewritten.
+      mbar_arrive(&bars.epi);
+      ok = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
     }
   }
   bulk_wait_group0();
@@ -636,24 +696,25 @@ __device__ void bwd_dq_drain(uint8_t* sm, BwdBars& bars, uint32_t tmem, int bh, 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do, int N,
-                    float scale, const float* __restrict__ lse2_pad, const float* __restrict__ delta_pad,
-                    int n_pad, const __nv_bfloat16* __restrict__ k_raw, const float* __restrict__ rk,
-                    const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                    float* __restrict__ dqacc, float* __restrict__ dgk_part, uint32_t* dev_err) {
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const BwdWork w, float scale, const float* __restrict__ lse2_pad,
+                    const float* __restrict__ delta_pad, int n_pad, const __nv_bfloat16* __restrict__ k_raw,
+                    const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
+                    __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, float* __restrict__ dgk_part,
+                    uint32_t* dev_err) {
+  using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(16) BwdBars bars;
   uint8_t* sm = align1024b(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int j = blockIdx.x, bh = blockIdx.y;
-  const int kv0 = j * 128;
-  const int nq = (N + 127) / 128;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars.kv_full, 1);
-    // With two issuers a Q / dO stage is released by a commit from each.
-    const uint32_t n_rel = BwdCfg<D>::kTwoIssuers ? 2u : 1u;
+    // With two issuers a Q / dO stage and a K/V buffer are released by a
+    // commit from each.
+    const uint32_t n_rel = C::kTwoIssuers ? 2u : 1u;
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], n_rel);
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], n_rel);
       mbar_init(&bars.do_full[s], 1);
@@ -666,7 +727,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 128);
-    mbar_init(&bars.kv_done, 1);
+    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_free_v, 128);
+    mbar_init(&bars.acc_free_k, 128);
     mbar_init(&bars.s_free, 256);
     mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.dv_done, 1);
@@ -686,25 +749,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == 12) {
-    if (lane == 0)
-      bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, bh, kv0, nq, lse2_pad, delta_pad, n_pad, dev_err);
+    if (lane == 0) bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, lse2_pad, delta_pad, n_pad, dev_err);
   } else if (warp == 13) {
     if (lane == 0) {
-      if (BwdCfg<D>::kTwoIssuers) bwd_mma_recompute<D>(sm, bars, tmem, nq, dev_err);
-      else bwd_mma<D>(sm, bars, tmem, nq, dev_err);
+      if (C::kTwoIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
+      else bwd_mma<D>(sm, bars, tmem, w, dev_err);
     }
   } else if (warp == 14) {
-    if (lane == 0 && BwdCfg<D>::kTwoIssuers) bwd_mma_gradients<D>(sm, bars, tmem, nq, dev_err);
+    if (lane == 0 && C::kTwoIssuers) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
   } else if (warp < 8) {
-    const int g = warp >> 2;
-    bwd_compute<D>(sm, bars, tmem, g, bh, kv0, N, nq, scale, dev_err);
-    if (g == 0)
-      bwd_epilogue_dv<D>(bars, tmem, bh, kv0, N, dv, dev_err);
-    else
-      bwd_epilogue_dk<D>(sm, bars, tmem, bh, kv0, N, scale, k_raw, rk, gk, dk, dgk_part, bh * gridDim.x + j,
-                         dev_err);
+    bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
-    bwd_dq_drain<D>(sm, bars, tmem, bh, N, nq, dqacc, dev_err);
+    bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, gk, dk, dv, dgk_part, dev_err);
   }
   tc_fence_before();
   __syncthreads();
@@ -723,11 +779,15 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   static_assert(C::kDynSmem + static_cast<int>(sizeof(BwdBars)) <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((s.N + 127) / 128, s.BH);
+  BwdWork w;
+  w.N = s.N;
+  w.nkt = (s.N + 127) / 128;
+  w.units = s.BH * w.nkt;
+  const int sms = device_sm_count();
+  const int grid = w.units < sms ? w.units : sms;
   attn_bwd_kernel<D><<<grid, kBwdThreads, C::kDynSmem, st>>>(
-      mq, mk, mv, mdo, s.N, s.scale, lse2_pad, delta_pad, ((s.N + 127) / 128) * 128,
-      reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk, reinterpret_cast<__nv_bfloat16*>(dk),
-      reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part, dev_err);
+      mq, mk, mv, mdo, w, s.scale, lse2_pad, delta_pad, w.nkt * 128, reinterpret_cast<const __nv_bfloat16*>(k_raw),
+      rk, gk, reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part, dev_err);
   return cudaGetLastError();
 }
 

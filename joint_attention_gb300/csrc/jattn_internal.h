@@ -44,6 +44,8 @@ cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, i
 int dg_reduce_scratch_floats(int d);
 int dg_reduce_tickets(int d);
 int q_norm_bwd_parts();
+// Streaming multiprocessors of the current device (cached after the first call).
+int device_sm_count();
 
 // --- tensor-core attention kernels ------------------------------------------
 struct AttnShape {

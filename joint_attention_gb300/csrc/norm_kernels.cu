@@ -310,6 +310,8 @@ int row_grid(int64_t rows, int d) {
 
 }  // namespace
 
+int device_sm_count() { return sm_count(); }
+
 int q_norm_bwd_parts() { return sm_count() * 4; }
 
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
