@@ -15,7 +15,7 @@
 // u = blockIdx.x, blockIdx.x + gridDim.x, ... with every barrier phase
 // running on across units, so the next unit's K/V load and first S / dP
 // products overlap the current unit's last tiles and its epilogue.
-// 480 threads:
+// 512 threads:
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
@@ -30,8 +30,8 @@
 //               unit's dgk partial) and release the accumulators.
 //   warp 12     TMA producer: K_j, V_j per unit (double-buffered for d = 64);
 //               Q_i (+ LSE_i, D_i) and dO_i per query tile through rings.
-//   warps 13-14 MMA issuers (d = 64): recompute (S, dP) and gradients (dV, dK,
-//               dQ); d = 128 uses warp 13 alone.
+//   warps 13-15 MMA issuers (d = 64): recompute (S, dP), gradients (dV, dK)
+//               and dQ; d = 128 uses warp 13 alone.
 //
 // d = 64: TMEM (512 columns) S^T [0,128), dP^T [128,256), dV [256,320),
 // dK [320,384), dQ [384,448), P^T [448,512) (packed bf16).  The compute
@@ -53,20 +53,20 @@
 namespace jattn {
 namespace {
 
-constexpr int kBwdThreads = 480;
+constexpr int kBwdThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128 x d bf16 tile
-  static constexpr int kQStages = 2;
+  static constexpr int kQStages = (D == 64) ? 3 : 2;
   static constexpr int kDOStages = (D == 64) ? 2 : 1;
   static constexpr int kDSBufs = 1;
   // K/V buffers: two let the next unit's keys load during the current unit.
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
-  // d = 64: two MMA issuers (recompute: S, dP; gradients: dV, dK, dQ) and
+  // d = 64: three MMA issuers (recompute: S, dP; gradients: dV, dK; dQ) and
   // P^T in its own TMEM columns.  d = 128: one issuer, P^T over S^T.
-  static constexpr bool kTwoIssuers = (D == 64);
+  static constexpr bool kSplitIssuers = (D == 64);
   static constexpr int kDQCols = (D == 64) ? 64 : 32;        // dQ columns drained per pass
   static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // padded staging row
   static constexpr int kOffKV = 0;                            // + buf * 2 * kTile: K, then V
@@ -97,11 +97,18 @@ struct BwdWork {
   int N;
   int nkt;    // key tiles per head == query tiles per head
   int units;  // BH * nkt
+  // The i-th query tile visited by unit u: the key tiles of one head (which
+  // run side by side on neighbouring CTAs) start at different query tiles,
+  // so that their dQ reduce-adds go to different rows at any one time.
+  __device__ __forceinline__ int query_tile(int u, int i) const {
+    const int q = i + u % nkt;
+    return q < nkt ? q : q - nkt;
+  }
 };
 
 struct BwdBars {
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[3], q_empty[3];
   uint64_t do_full[2], do_empty[2];
   uint64_t s_full, dp_full;
   uint64_t p_ready, ds_ready;
@@ -112,13 +119,14 @@ struct BwdBars {
   uint64_t s_free, dp_free;
   uint64_t dv_done;
   uint64_t epi;
-  uint64_t drain[2];
+  uint64_t drain[3];
   uint32_t tmem_base;
   int abort;
-  // Per query stage: the tile's LSE in the log2 domain (+inf past N) and D
-  // (0 past N), copied in with the tile from padded scratch rows.
-  __align__(16) float lse2[2][128];
-  __align__(16) float delta[2][128];
+  // Per query stage: minus the tile's LSE in the log2 domain (-inf past N)
+  // and D (0 past N), copied in with the tile from padded scratch rows.
+  __align__(16) float gk[128];  // K-RMSNorm gain (d entries)
+  __align__(16) float nlse2[3][128];
+  __align__(16) float delta[3][128];
 };
 
 __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
@@ -128,7 +136,7 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
 template <int D>
 __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                              const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, const BwdWork& w,
-                             const float* lse2_pad, const float* delta_pad, int n_pad, uint32_t* dev_err) {
+                             const float* nlse2_pad, const float* delta_pad, int n_pad, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(mq);
   tma_prefetch_desc(mk);
@@ -152,18 +160,19 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
       const int qs = t % C::kQStages;
       if (t >= C::kQStages && !(ok = mbar_wait(&bars.q_empty[qs], ((t / C::kQStages) - 1) & 1, ab, dev_err))) break;
       mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
-      const size_t prow = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
-      bulk_load(bars.lse2[qs], lse2_pad + prow, 512, &bars.q_full[qs]);
+      const int qi = w.query_tile(u, i);
+      const size_t prow = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(qi) * 128;
+      bulk_load(bars.nlse2[qs], nlse2_pad + prow, 512, &bars.q_full[qs]);
       bulk_load(bars.delta[qs], delta_pad + prow, 512, &bars.q_full[qs]);
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, i * 128, bh);
+        tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, qi * 128, bh);
       ++nq_issued;
       const int ds = t % C::kDOStages;
       if (t >= C::kDOStages && !(ok = mbar_wait(&bars.do_empty[ds], ((t / C::kDOStages) - 1) & 1, ab, dev_err)))
         break;
       mbar_arrive_expect_tx(&bars.do_full[ds], C::kTile);
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_3d(sm + C::kOffDO + ds * C::kTile + blk * 16384, mdo, &bars.do_full[ds], blk * 64, i * 128, bh);
+        tma_load_3d(sm + C::kOffDO + ds * C::kTile + blk * 16384, mdo, &bars.do_full[ds], blk * 64, qi * 128, bh);
       ++ndo_issued;
     }
   }
@@ -238,12 +247,13 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
   }
 }
 
-// Two-issuer backward (d = 64).  Recompute issuer: S(t) = K Q_t^T once the
-// compute groups hold S(t-1) in registers, dP(t) = V dO_t^T once they hold
-// dP(t-1).  Gradient issuer: dV(t) from P^T in TMEM, dK(t) and dQ(t) from
-// dS^T in shared memory.  A Q stage is released by both issuers (S and dK
-// read it), a dO stage likewise (dP, dV), and a K/V buffer likewise (the
-// unit's last dP and last dQ).
+// Three-issuer backward (d = 64).  Recompute issuer: S(t) = K Q_t^T once
+// the compute groups hold S(t-1) in registers, dP(t) = V dO_t^T once they
+// hold dP(t-1).  Gradient issuer: dV(t) from P^T in TMEM, dK(t) from dS^T in
+// shared memory.  dQ issuer: dQ(t) from dS^T.  Every shared buffer is
+// released by a commit from each of its two readers: a Q stage (S, dK), a dO
+// stage (dP, dV), the dS^T tile (dK, dQ) and a K/V buffer (the unit's last
+// dP and last dQ).
 template <int D>
 __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w,
                                   uint32_t* dev_err) {
@@ -287,13 +297,9 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
   auto mDO = [=](int t) {
     return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16384, 1024);
   };
-  const uint32_t ds_addr = smem_u32(sm + C::kOffDS);
-  const uint64_t kDS = sdesc_sw128(ds_addr, 16, 1024), mDS = sdesc_sw128(ds_addr, 16384, 1024);
+  const uint64_t kDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16, 1024);
   bool ok = true;
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
-    const int b = ui % C::kKVBufs;
-    if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
-    const uint64_t mK = sdesc_sw128(smem_u32(sm + C::off_k(b)), 16384, 1024);
     for (int i = 0; i < w.nkt; ++i) {
       const int t = ui * w.nkt + i;
       if (!(ok = mbar_wait(&bars.p_ready, t & 1, ab, dev_err))) break;
@@ -310,19 +316,39 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       tc_fence_after();
       mma_dk<D>(tmem + C::kColDK, kDS, mQ(t), i > 0);
       umma_commit(&bars.q_empty[t % C::kQStages]);
+      umma_commit(&bars.ds_free[0]);
+    }
+    if (ok) umma_commit(&bars.acc_full);
+  }
+  umma_commit(&bars.drain[1]);
+  mbar_wait_drain(&bars.drain[1], 0);
+}
+
+// dQ issuer (d = 64): dQ(t) = dS(t) K once dS^T(t) is in shared memory and
+// dQ(t-1) has been drained from its TMEM columns.
+template <int D>
+__device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, uint32_t* dev_err) {
+  using C = BwdCfg<D>;
+  volatile int* ab = &bars.abort;
+  const uint64_t mDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16384, 1024);
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int b = ui % C::kKVBufs;
+    if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
+    const uint64_t mK = sdesc_sw128(smem_u32(sm + C::off_k(b)), 16384, 1024);
+    for (int i = 0; i < w.nkt; ++i) {
+      const int t = ui * w.nkt + i;
+      if (!(ok = mbar_wait(&bars.ds_ready, t & 1, ab, dev_err))) break;
       if (t > 0 && !(ok = mbar_wait(&bars.dq_free, (t - 1) & 1, ab, dev_err))) break;
       tc_fence_after();
       mma_dq<D>(tmem + C::kColDQ, mDS, mK);
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[0]);
     }
-    if (ok) {
-      umma_commit(&bars.acc_full);
-      umma_commit(&bars.kv_empty[b]);
-    }
+    if (ok) umma_commit(&bars.kv_empty[b]);
   }
-  umma_commit(&bars.drain[1]);
-  mbar_wait_drain(&bars.drain[1], 0);
+  umma_commit(&bars.drain[2]);
+  mbar_wait_drain(&bars.drain[2], 0);
 }
 
 // Single-issuer backward (d = 128), per unit: S(0), dP(0), then per tile
@@ -416,10 +442,11 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + 64 * g;   // this group's S^T columns
   // P^T: own 32 packed columns (d = 64) or over the group's S^T columns
-  const uint32_t tP = C::kTwoIssuers ? tmem + lane_base + C::kColP + 32 * g : tS;
+  const uint32_t tP = C::kSplitIssuers ? tmem + lane_base + C::kColP + 32 * g : tS;
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * g;
   const uint32_t swz = static_cast<uint32_t>(kr & 7);
-  const float scale_log2 = scale * kLog2e;
+  const uint64_t sc2 = f2_make(scale * kLog2e, scale * kLog2e);
+  const uint64_t minus1 = f2_make(-1.f, -1.f);
   volatile int* ab = &bars.abort;
 
   for (int u = blockIdx.x, ui = 0; u < w.units; u += gridDim.x, ++ui) {
@@ -432,32 +459,38 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
       if (ok) ok = mbar_wait(&bars.q_full[qs], (t / C::kQStages) & 1, ab, dev_err);
       if (!__all_sync(0xffffffffu, ok)) return;
       tc_fence_after();
-      // P^T = exp2(s log2e S^T - LSE2), packed bf16 pairs into TMEM (chunk c
-      // -> 16 packed columns at 16c).
+      // P^T = exp2(s log2e S^T - LSE log2e), packed bf16 pairs into TMEM
+      // (chunk c -> 16 packed columns at 16c).  Key rows past N get P = 0.
       uint32_t pp[32];
       // Both 32-column chunks of this group's S^T in flight at once.
       uint32_t sall[2][32];
       tmem_ld32(tS, sall[0]);
       tmem_ld32(tS + 32, sall[1]);
       tmem_wait_ld();
-      if (C::kTwoIssuers) {  // S^T is in registers: S(t+1) may overwrite it
+      if (C::kSplitIssuers) {  // S^T is in registers: S(t+1) may overwrite it
         tc_fence_before();
         mbar_arrive(&bars.s_free);
       }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint32_t(&s)[32] = sall[c];
+        if (key_live) {  // warp-uniform except in a head's last key tile
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&bars.lse2[qs][64 * g + c * 32 + e]);
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[e + 0]), scale_log2, -l4.x));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[e + 1]), scale_log2, -l4.y));
-          const float p2 = ex2_approx(fmaf(__uint_as_float(s[e + 2]), scale_log2, -l4.z));
-          const float p3 = ex2_approx(fmaf(__uint_as_float(s[e + 3]), scale_log2, -l4.w));
-          pp[(c * 32 + e) / 2] = key_live ? pack_bf16x2(p0, p1) : 0u;
-          pp[(c * 32 + e) / 2 + 1] = key_live ? pack_bf16x2(p2, p3) : 0u;
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(&bars.nlse2[qs][64 * g + c * 32 + e]);
+            float x0, x1, x2, x3;
+            f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, f2_make(l4.x, l4.y)), x0,
+                     x1);
+            f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), sc2, f2_make(l4.z, l4.w)),
+                     x2, x3);
+            pp[(c * 32 + e) / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+            pp[(c * 32 + e) / 2 + 1] = pack_bf16x2(ex2_approx(x2), ex2_approx(x3));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) pp[(c * 32 + e) / 2] = 0u;
         }
-        if (C::kTwoIssuers && c == 0 && t > 0) {
+        if (C::kSplitIssuers && c == 0 && t > 0) {
           // dV(t-1) must be done reading P^T(t-1) before it is overwritten.
           ok = mbar_wait(&bars.dv_done, (t - 1) & 1, ab, dev_err);
           if (!__all_sync(0xffffffffu, ok)) return;
@@ -479,7 +512,7 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
       tmem_ld32(tDP, dpall[0]);
       tmem_ld32(tDP + 32, dpall[1]);
       tmem_wait_ld();
-      if (C::kTwoIssuers) {  // dP^T is in registers: dP(t+1) may overwrite it
+      if (C::kSplitIssuers) {  // dP^T is in registers: dP(t+1) may overwrite it
         tc_fence_before();
         mbar_arrive(&bars.dp_free);
       }
@@ -495,10 +528,12 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
           const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const uint32_t pw = pp[col / 2 + h];
-            const float pa = __uint_as_float(pw << 16), pb = __uint_as_float(pw & 0xFFFF0000u);
-            dsw[e / 2 + h] = pack_bf16x2(pa * (__uint_as_float(dpv[e + 2 * h]) - dd[2 * h]),
-                                         pb * (__uint_as_float(dpv[e + 2 * h + 1]) - dd[2 * h + 1]));
+            // dS = P * bf16(dP - D): one packed fp32 pair, one pack, one bf16x2 product
+            float a, b;
+            f2_split(f2_fma(f2_make(dd[2 * h], dd[2 * h + 1]), minus1,
+                            f2_make(__uint_as_float(dpv[e + 2 * h]), __uint_as_float(dpv[e + 2 * h + 1]))),
+                     a, b);
+            dsw[e / 2 + h] = bf16x2_mul(pp[col / 2 + h], pack_bf16x2(a, b));
           }
           st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
                        dsw[e / 2 + 2], dsw[e / 2 + 3]);
@@ -517,33 +552,69 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 // (one thread per key row):
 //   dv = bf16(dV acc);
 //   dk_hat = scale * dK acc; u = g * dk_hat; dk = r u - (r^3/d) k sum(u k);
-//   dgk partial = column sums over the tile's rows of dk_hat * k * r, taken
-//   through the staging rows in a fixed order.
+//   dgk partial = column sums over the tile's rows of dk_hat * k * r, in a
+//   fixed order.
+// The accumulators are read out of TMEM and released first, so that the next
+// unit's first dV / dK products wait only for that.  d = 64 then runs the
+// rest through the staging rows (free between two dQ drains) as 128-byte-row
+// tiles, so that the k, dk and dv rows move with contiguous 512-byte warp
+// accesses, and sums the dgk terms with a warp butterfly; d = 128 works per
+// row and sums through padded staging rows.
 template <int D>
 __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, float scale,
                                    float* __restrict__ dqacc, const __nv_bfloat16* __restrict__ k_raw,
-                                   const float* __restrict__ rk, const float* __restrict__ gk,
-                                   __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                                   float* __restrict__ dgk_part, uint32_t* dev_err) {
+                                   const float* __restrict__ rk, __nv_bfloat16* __restrict__ dk,
+                                   __nv_bfloat16* __restrict__ dv, float* __restrict__ dgk_part,
+                                   uint32_t* dev_err) {
   using C = BwdCfg<D>;
   constexpr int kRowFloats = C::kDQRowBytes / 4;
+  // d = 64: the epilogue runs through the staging area (free between two dQ
+  // drains) as 128-byte-row tiles, so that every global access is a
+  // contiguous 512-byte warp access.
+  constexpr bool kTiled = (D == 64);
+  static_assert(!kTiled || 2 * 128 * D * 2 + 4 * D * 4 <= 128 * C::kDQRowBytes, "epilogue tiles fit the staging area");
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int r128 = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQ) or key row (dV, dK)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tQ = tmem + lane_base + C::kColDQ;
+  const uint32_t tDK = tmem + lane_base + C::kColDK;
   uint8_t* srow = sm + C::kOffDQ + r128 * C::kDQRowBytes;
   const uint32_t srow_a = smem_u32(srow);
+  const float* red = reinterpret_cast<const float*>(sm + C::kOffDQ);
+  // Tiled epilogue layout: k (then dk) tile, dv tile, 128-byte rows with the
+  // 16-byte chunks XOR-swizzled by (row & 7); then 4 x D floats of per-warp
+  // column sums.
+  const uint32_t tile_k = smem_u32(sm + C::kOffDQ);
+  const uint32_t tile_v = tile_k + 128 * D * 2;
+  float* wsum = reinterpret_cast<float*>(sm + C::kOffDQ + 2 * 128 * D * 2);
+  auto chunk_addr = [](uint32_t tile, int row, int c) {
+    return tile + static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+  };
   volatile int* ab = &bars.abort;
   uint32_t epi_uses = 0;
+  // Bounded barrier among the 128 drain threads.
+  auto epi_sync = [&]() -> bool {
+    mbar_arrive(&bars.epi);
+    const bool okb = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
+    return __all_sync(0xffffffffu, okb);
+  };
   bool ok = true;
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
     const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
+    const int n = kv0 + r128;  // key row of this thread in the epilogue
+    const bool key_live = n < w.N;
+    const int live_rows = w.N - kv0 < 128 ? w.N - kv0 : 128;
+    const size_t tile_off = (static_cast<size_t>(bh) * w.N + kv0) * D;  // first row of the key tile
+    const size_t row_off = (static_cast<size_t>(bh) * w.N + (key_live ? n : 0)) * D;
+
     for (int i = 0; i < w.nkt; ++i) {
       const int t = ui * w.nkt + i;
+      // The raw k tile is pulled into L2 while the last dQ tile is computed.
+      if (kTiled && i == w.nkt - 1 && r128 == 0) bulk_prefetch_l2(k_raw + tile_off, live_rows * D * 2);
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const int qrow = i * 128 + r128;
+      const int qrow = w.query_tile(u, i) * 128 + r128;
       float* grow = dqacc + (static_cast<size_t>(bh) * w.N + (qrow < w.N ? qrow : 0)) * D;
 #pragma unroll
       for (int pass = 0; pass < D / C::kDQCols; ++pass) {
@@ -570,124 +641,225 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     }
     if (!ok) break;
 
-    // ---- unit epilogue: this thread owns key row kv0 + r128 ----
+    // ---- unit epilogue ----
     ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
-    const int n = kv0 + r128;
-    const bool key_live = n < w.N;
-    const size_t row_off = (static_cast<size_t>(bh) * w.N + (key_live ? n : 0)) * D;
-    uint4* dvrow = reinterpret_cast<uint4*>(dv + row_off);
+    const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
+    if constexpr (kTiled) {
+      // Accumulators out of TMEM first: dV packed to bf16 (32 registers),
+      // dK (64 registers); both column ranges released.
+      uint32_t vp[D / 2];
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t a[32];
-      tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
-      tmem_wait_ld();
-      if (c == D / 32 - 1) {
-        tc_fence_before();
-        mbar_arrive(&bars.acc_free_v);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) vp[c * 16 + e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
       }
-      if (key_live) {
+      tc_fence_before();
+      mbar_arrive(&bars.acc_free_v);
+      uint32_t a[D];
+      tmem_ld32(tDK, *reinterpret_cast<uint32_t(*)[32]>(a));
+      tmem_ld32(tDK + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.acc_free_k);
+      bulk_wait_group_read0();        // this thread's staging row has been read
+      if (!(ok = epi_sync())) break;  // ... and every other row too
+      // dv row into the dv tile
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
-          o.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
-          o.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
-          o.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
-          dvrow[c * 4 + q] = o;
+      for (int c = 0; c < D / 8; ++c)
+        st_shared_v4(chunk_addr(tile_v, r128, c), vp[4 * c], vp[4 * c + 1], vp[4 * c + 2], vp[4 * c + 3]);
+      // raw k tile into shared memory: chunk q = it * 128 + r128, 32
+      // consecutive 16-byte chunks per warp access.
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(k_raw + tile_off);
+        uint4 kw[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int q = it * 128 + r128;
+          kw[it] = (q >> 3) < live_rows ? src[q] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int q = it * 128 + r128;
+          st_shared_v4(chunk_addr(tile_k, q >> 3, q & 7), kw[it].x, kw[it].y, kw[it].z, kw[it].w);
         }
       }
-    }
-    const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
-    const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
-    const uint32_t tDK = tmem + lane_base + C::kColDK;
-    float dot = 0.f;
+      if (!(ok = epi_sync())) break;  // the k tile is complete
+      // dot = sum_c g_c dk_hat_c k_c over this thread's row
+      float dot = 0.f;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t a[32];
-      tmem_ld32(tDK + c * 32, a);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < 8; ++c) {
+        const uint4 kw = ld_shared_v4(chunk_addr(tile_k, r128, c));
         const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-          dot = fmaf(gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(kx[h] << 16), dot);
-          dot = fmaf(gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(kx[h] & 0xFFFF0000u), dot);
+          const int col = c * 8 + 2 * h;
+          dot = fmaf(bars.gk[col] * __uint_as_float(a[col]), __uint_as_float(kx[h] << 16), dot);
+          dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[col + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
         }
       }
-    }
-    const float coef = r * r * r * (1.f / D) * dot;
-    uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
-    const float* red = reinterpret_cast<const float*>(sm + C::kOffDQ);
-    bulk_wait_group_read0();  // the staging row is free for the column sums
+      const float coef = r * r * r * (1.f / D) * scale * dot;
+      // dk = r g dk_hat - coef k over the k row (in place); a[] becomes the
+      // row's dgk terms dk_hat k r.
 #pragma unroll
-    for (int pass = 0; pass < D / C::kDQCols; ++pass) {
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = chunk_addr(tile_k, r128, c);
+        const uint4 kw = ld_shared_v4(addr);
+        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int cc = 0; cc < C::kDQCols / 32; ++cc) {
-        const int c = pass * (C::kDQCols / 32) + cc;
+        for (int h = 0; h < 4; ++h) {
+          const int col = c * 8 + 2 * h;
+          const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
+          const float dk0 = __uint_as_float(a[col]) * scale, dk1 = __uint_as_float(a[col + 1]) * scale;
+          o[h] = pack_bf16x2(r * bars.gk[col] * dk0 - coef * x0, r * bars.gk[col + 1] * dk1 - coef * x1);
+          a[col] = __float_as_uint(key_live ? dk0 * x0 * r : 0.f);
+          a[col + 1] = __float_as_uint(key_live ? dk1 * x1 * r : 0.f);
+        }
+        st_shared_v4(addr, o[0], o[1], o[2], o[3]);
+      }
+      // dgk: reduce-scatter over the warp's 32 rows (lane L ends with the
+      // sums of columns 2L, 2L+1), then the 4 warps in order.
+#pragma unroll
+      for (int m = 16, half = 32; m >= 1; m >>= 1, half >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+          const float send = __uint_as_float(upper ? a[j] : a[j + half]);
+          const float keep = __uint_as_float(upper ? a[j + half] : a[j]);
+          a[j] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, m));
+        }
+      }
+      wsum[(warp & 3) * D + 2 * lane] = __uint_as_float(a[0]);
+      wsum[(warp & 3) * D + 2 * lane + 1] = __uint_as_float(a[1]);
+      if (!(ok = epi_sync())) break;  // dk tile, dv tile and warp sums complete
+      if (r128 < D)
+        dgk_part[static_cast<size_t>(u) * D + r128] =
+            ((wsum[r128] + wsum[D + r128]) + wsum[2 * D + r128]) + wsum[3 * D + r128];
+      // dk and dv tiles out, 32 consecutive 16-byte chunks per warp access.
+      uint4* dkdst = reinterpret_cast<uint4*>(dk + tile_off);
+      uint4* dvdst = reinterpret_cast<uint4*>(dv + tile_off);
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int q = it * 128 + r128;
+        if ((q >> 3) < live_rows) {
+          dkdst[q] = ld_shared_v4(chunk_addr(tile_k, q >> 3, q & 7));
+          dvdst[q] = ld_shared_v4(chunk_addr(tile_v, q >> 3, q & 7));
+        }
+      }
+      if (!(ok = epi_sync())) break;  // tiles read: the staging rows are free again
+    } else {
+      // d = 128: per-row accesses; two passes over the TMEM dK accumulator
+      // (dot, then outputs), the dgk rows staged kDQCols columns at a time.
+      const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
+      uint4* dvrow = reinterpret_cast<uint4*>(dv + row_off);
+      uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t a[32];
-        tmem_ld32(tDK + c * 32, a);
+        tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
         tmem_wait_ld();
         if (c == D / 32 - 1) {
           tc_fence_before();
-          mbar_arrive(&bars.acc_free_k);
+          mbar_arrive(&bars.acc_free_v);
         }
+        if (key_live) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
+            o.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
+            o.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
+            o.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
+            dvrow[c * 4 + q] = o;
+          }
+        }
+      }
+      float dot = 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tDK + c * 32, a);
+        tmem_wait_ld();
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
-          float y[8], gpart[8];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-            const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
-            const float dk0 = key_live ? __uint_as_float(a[e]) * scale : 0.f;
-            const float dk1 = key_live ? __uint_as_float(a[e + 1]) * scale : 0.f;
-            y[2 * h] = r * gk[col] * dk0 - coef * x0;
-            y[2 * h + 1] = r * gk[col + 1] * dk1 - coef * x1;
-            gpart[2 * h] = dk0 * x0 * r;
-            gpart[2 * h + 1] = dk1 * x1 * r;
+            dot = fmaf(bars.gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(kx[h] << 16), dot);
+            dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(kx[h] & 0xFFFF0000u),
+                       dot);
           }
-          if (key_live) {
-            uint4 o;
-            o.x = pack_bf16x2(y[0], y[1]);
-            o.y = pack_bf16x2(y[2], y[3]);
-            o.z = pack_bf16x2(y[4], y[5]);
-            o.w = pack_bf16x2(y[6], y[7]);
-            dkrow[c * 4 + c8] = o;
-          }
-          const uint32_t soff = static_cast<uint32_t>((cc * 32 + c8 * 8) * 4);
-          st_shared_v4(srow_a + soff, __float_as_uint(gpart[0]), __float_as_uint(gpart[1]),
-                       __float_as_uint(gpart[2]), __float_as_uint(gpart[3]));
-          st_shared_v4(srow_a + soff + 16, __float_as_uint(gpart[4]), __float_as_uint(gpart[5]),
-                       __float_as_uint(gpart[6]), __float_as_uint(gpart[7]));
         }
       }
-      // Bounded barrier among the 128 drain threads: every row is staged.
-      mbar_arrive(&bars.epi);
-      ok = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
-      if (r128 < C::kDQCols) {
-        // Fixed-order column sum over the tile's 128 key rows.
-        const float* col = red + r128;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      const float coef = r * r * r * (1.f / D) * dot;
+      bulk_wait_group_read0();  // the staging row is free for the column sums
+#pragma unroll
+      for (int pass = 0; pass < D / C::kDQCols; ++pass) {
+#pragma unroll
+        for (int cc = 0; cc < C::kDQCols / 32; ++cc) {
+          const int c = pass * (C::kDQCols / 32) + cc;
+          uint32_t a[32];
+          tmem_ld32(tDK + c * 32, a);
+          tmem_wait_ld();
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars.acc_free_k);
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+            float y[8], gpart[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int col = c * 32 + c8 * 8 + 2 * h;
+              const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
+              const float dk0 = key_live ? __uint_as_float(a[c8 * 8 + 2 * h]) * scale : 0.f;
+              const float dk1 = key_live ? __uint_as_float(a[c8 * 8 + 2 * h + 1]) * scale : 0.f;
+              y[2 * h] = r * bars.gk[col] * dk0 - coef * x0;
+              y[2 * h + 1] = r * bars.gk[col + 1] * dk1 - coef * x1;
+              gpart[2 * h] = dk0 * x0 * r;
+              gpart[2 * h + 1] = dk1 * x1 * r;
+            }
+            if (key_live) {
+              uint4 o;
+              o.x = pack_bf16x2(y[0], y[1]);
+              o.y = pack_bf16x2(y[2], y[3]);
+              o.z = pack_bf16x2(y[4], y[5]);
+              o.w = pack_bf16x2(y[6], y[7]);
+              dkrow[c * 4 + c8] = o;
+            }
+            const uint32_t soff = static_cast<uint32_t>((cc * 32 + c8 * 8) * 4);
+            st_shared_v4(srow_a + soff, __float_as_uint(gpart[0]), __float_as_uint(gpart[1]),
+                         __float_as_uint(gpart[2]), __float_as_uint(gpart[3]));
+            st_shared_v4(srow_a + soff + 16, __float_as_uint(gpart[4]), __float_as_uint(gpart[5]),
+                         __float_as_uint(gpart[6]), __float_as_uint(gpart[7]));
+          }
+        }
+        if (!(ok = epi_sync())) break;  // every row is staged
+        if (r128 < C::kDQCols) {
+          // Fixed-order column sum over the tile's 128 key rows.
+          const float* col = red + r128;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll 8
-        for (int q = 0; q < 128; q += 4) {
-          s0 += col[(q + 0) * kRowFloats];
-          s1 += col[(q + 1) * kRowFloats];
-          s2 += col[(q + 2) * kRowFloats];
-          s3 += col[(q + 3) * kRowFloats];
+          for (int q = 0; q < 128; q += 4) {
+            s0 += col[(q + 0) * kRowFloats];
+            s1 += col[(q + 1) * kRowFloats];
+            s2 += col[(q + 2) * kRowFloats];
+            s3 += col[(q + 3) * kRowFloats];
+          }
+          dgk_part[static_cast<size_t>(u) * D + pass * C::kDQCols + r128] = (s0 + s1) + (s2 + s3);
         }
-        dgk_part[static_cast<size_t>(u) * D + pass * C::kDQCols + r128] = (s0 + s1) + (s2 + s3);
+        if (!(ok = epi_sync())) break;  // every column summed before the rows are rewritten
       }
-      // ... and every column has been summed before the rows are rewritten.
-      mbar_arrive(&bars.epi);
-      ok = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
-      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      if (!ok) break;
     }
   }
   bulk_wait_group0();
@@ -697,7 +869,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                    const BwdWork w, float scale, const float* __restrict__ lse2_pad,
+                    const BwdWork w, float scale, const float* __restrict__ nlse2_pad,
                     const float* __restrict__ delta_pad, int n_pad, const __nv_bfloat16* __restrict__ k_raw,
                     const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, float* __restrict__ dgk_part,
@@ -709,17 +881,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    // With two issuers a Q / dO stage and a K/V buffer are released by a
-    // commit from each.
-    const uint32_t n_rel = C::kTwoIssuers ? 2u : 1u;
+    // With three issuers a Q / dO stage, the dS^T tile and a K/V buffer are
+    // each released by commits from their two readers.
+    const uint32_t n_rel = C::kSplitIssuers ? 2u : 1u;
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], n_rel);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], n_rel);
-      mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], n_rel);
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], n_rel);
-      mbar_init(&bars.ds_free[s], 1);
+      mbar_init(&bars.ds_free[s], n_rel);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
@@ -736,9 +910,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.epi, 128);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
+    mbar_init(&bars.drain[2], 1);
     bars.abort = 0;
     fence_mbar_init();
   }
+  for (int c = threadIdx.x; c < D; c += blockDim.x) bars.gk[c] = gk[c];
   if (warp == 13) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
@@ -749,18 +925,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == 12) {
-    if (lane == 0) bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, lse2_pad, delta_pad, n_pad, dev_err);
+    if (lane == 0) bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, nlse2_pad, delta_pad, n_pad, dev_err);
   } else if (warp == 13) {
     if (lane == 0) {
-      if (C::kTwoIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
+      if (C::kSplitIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
       else bwd_mma<D>(sm, bars, tmem, w, dev_err);
     }
   } else if (warp == 14) {
-    if (lane == 0 && C::kTwoIssuers) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
+    if (lane == 0 && C::kSplitIssuers) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
+  } else if (warp == 15) {
+    if (lane == 0 && C::kSplitIssuers) bwd_mma_dq<D>(sm, bars, tmem, w, dev_err);
   } else if (warp < 8) {
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
-    bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, gk, dk, dv, dgk_part, dev_err);
+    bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, dk, dv, dgk_part, dev_err);
   }
   tc_fence_before();
   __syncthreads();
@@ -772,7 +950,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const AttnShape& s, const float* lse2_pad,
+                         const CUtensorMap& mdo, const AttnShape& s, const float* nlse2_pad,
                          const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk,
                          uint16_t* dv, float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
   using C = BwdCfg<D>;
@@ -786,7 +964,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   const int sms = device_sm_count();
   const int grid = w.units < sms ? w.units : sms;
   attn_bwd_kernel<D><<<grid, kBwdThreads, C::kDynSmem, st>>>(
-      mq, mk, mv, mdo, w, s.scale, lse2_pad, delta_pad, w.nkt * 128, reinterpret_cast<const __nv_bfloat16*>(k_raw),
+      mq, mk, mv, mdo, w, s.scale, nlse2_pad, delta_pad, w.nkt * 128, reinterpret_cast<const __nv_bfloat16*>(k_raw),
       rk, gk, reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part, dev_err);
   return cudaGetLastError();
 }
@@ -796,15 +974,15 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 int attn_bwd_dgk_parts(const AttnShape& s) { return s.BH * ((s.N + 127) / 128); }
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const CUtensorMap& map_do, const AttnShape& s, const float* lse2_pad,
+                            const CUtensorMap& map_do, const AttnShape& s, const float* nlse2_pad,
                             const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk,
                             uint16_t* dk, uint16_t* dv, float* dqacc, float* dgk_part, uint32_t* dev_err,
                             cudaStream_t st) {
   if (s.d == 64)
-    return launch_bwd_d<64>(map_q, map_k, map_v, map_do, s, lse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+    return launch_bwd_d<64>(map_q, map_k, map_v, map_do, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
                             dgk_part, dev_err, st);
   if (s.d == 128)
-    return launch_bwd_d<128>(map_q, map_k, map_v, map_do, s, lse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+    return launch_bwd_d<128>(map_q, map_k, map_v, map_do, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
                              dgk_part, dev_err, st);
   return cudaErrorInvalidValue;
 }

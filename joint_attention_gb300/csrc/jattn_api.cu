@@ -175,7 +175,7 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
   size_t b = 0;
   b += 2 * (s.elems * 2 + 256);                                   // q_hat, k_hat
   b += 2 * (s.rows * 4 + 256);                                    // rq, rk
-  b += 2 * (static_cast<size_t>(s.BH) * s.n_pad * 4 + 256);       // lse2, delta
+  b += 2 * (static_cast<size_t>(s.BH) * s.n_pad * 4 + 256);       // nlse2, delta
   b += s.elems * 4 + 256;                                         // dq accumulator
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
   b += static_cast<size_t>(dg_reduce_scratch_floats(s.d)) * 4 + 256;  // dg slice partials
@@ -361,7 +361,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   uint16_t* khat = cv.take<uint16_t>(s.elems);
   float* rq = cv.take<float>(s.rows);
   float* rk = cv.take<float>(s.rows);
-  float* lse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
+  float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
   float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
   float* dqacc = cv.take<float>(s.elems);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
@@ -373,7 +373,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   CUtensorMap mq, mk, mv, mdo;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, lse2, delta, dqacc, dg_tickets, s.BH, s.N,
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_tickets, s.BH, s.N,
                          s.n_pad, s.d, st);
   }
   if (ce != cudaSuccess) {
@@ -385,7 +385,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
     const char* stage = "attn_bwd launch";
     {
       Timed t(JATTN_KERNEL_ATTN_BWD, st);
-      ce = launch_attn_bwd(mq, mk, mv, mdo, as, lse2, delta, k, rk, gk, dk, dv, dqacc, dgk_part, err, st);
+      ce = launch_attn_bwd(mq, mk, mv, mdo, as, nlse2, delta, k, rk, gk, dk, dv, dqacc, dgk_part, err, st);
     }
     if (ce == cudaSuccess) {
       stage = "q_norm_bwd launch";

@@ -18,7 +18,7 @@ struct Scratch {
   uint16_t* khat = nullptr;  // [BH, N, d] bf16
   float* rq = nullptr;       // [BH*N] 1/rms of q rows
   float* rk = nullptr;       // [BH*N] 1/rms of k rows
-  float* lse2 = nullptr;     // [BH, Npad] LSE * log2(e), +inf in the pad rows
+  float* nlse2 = nullptr;    // [BH, Npad] -LSE * log2(e), -inf in the pad rows
   float* delta = nullptr;    // [BH, Npad] rowsum(dO * O), 0 in the pad rows
   float* dqacc = nullptr;    // [BH, N, d] fp32 accumulator of dS k_hat
   float* dgq_part = nullptr; // [nparts, d]
@@ -28,11 +28,11 @@ struct Scratch {
 // --- norm / elementwise kernels (HBM-bound) ---------------------------------
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                                uint16_t* qhat, uint16_t* khat, int64_t rows, int d, cudaStream_t st);
-// Rows are (bh, n) with n < N; lse2/delta are written for n < n_pad (= N
-// rounded up to 128), with +inf / 0 in the pad rows.
+// Rows are (bh, n) with n < N; nlse2 (= -LSE log2 e) and delta are written
+// for n < n_pad (= N rounded up to 128), with -inf / 0 in the pad rows.
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc,
+                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
                             unsigned int* tickets, int BH, int N, int n_pad, int d, cudaStream_t st);
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
                               uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, cudaStream_t st);
@@ -59,7 +59,7 @@ cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, 
                             const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st);
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const CUtensorMap& map_do, const AttnShape& s, const float* lse2_pad,
+                            const CUtensorMap& map_do, const AttnShape& s, const float* nlse2_pad,
                             const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
                             float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st);
 int attn_bwd_dgk_parts(const AttnShape& s);

@@ -108,14 +108,14 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
 
 // Backward preparation, one pass over the padded rows (bh, n), n < n_pad:
 // for n < N it writes q_hat, k_hat, 1/rms of q and k, D = rowsum(dout * out),
-// LSE in the log2 domain and a zeroed fp32 dq accumulator row; pad rows get
-// LSE = +inf and D = 0 so the attention backward sees zero probabilities.
+// minus LSE in the log2 domain and a zeroed fp32 dq accumulator row; pad rows
+// get -LSE = -inf and D = 0 so the attention backward sees zero probabilities.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
-    float* __restrict__ rk, float* __restrict__ lse2, float* __restrict__ delta, float4* __restrict__ dqacc,
+    float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, float4* __restrict__ dqacc,
     unsigned int* __restrict__ tickets, int n_tickets, int N, int n_pad, int64_t padded_rows) {
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < n_tickets) tickets[threadIdx.x] = 0u;
   constexpr int TPR = D / 8;
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     dot = row_sum<TPR>(dot);
     if (!in_range) continue;
     if (sub == 0) {
-      lse2[prow] = valid ? lse[row] * 1.4426950408889634f : INFINITY;
+      nlse2[prow] = valid ? -lse[row] * 1.4426950408889634f : -INFINITY;
       delta[prow] = valid ? dot : 0.f;
     }
     if (!valid) continue;
@@ -330,7 +330,7 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* lse2, float* delta, float* dqacc,
+                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
                             unsigned int* tickets, int BH, int N, int n_pad, int d, cudaStream_t st) {
   const int64_t padded_rows = static_cast<int64_t>(BH) * n_pad;
   const int grid = row_grid(padded_rows, d);
@@ -338,13 +338,13 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
   if (d == 64)
     bwd_prep_kernel<64><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
                                                         reinterpret_cast<uint4*>(qhat),
-                                                        reinterpret_cast<uint4*>(khat), rq, rk, lse2, delta,
+                                                        reinterpret_cast<uint4*>(khat), rq, rk, nlse2, delta,
                                                         reinterpret_cast<float4*>(dqacc), tickets,
                                                         dg_reduce_tickets(d), N, n_pad, padded_rows);
   else
     bwd_prep_kernel<128><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
                                                          reinterpret_cast<uint4*>(qhat),
-                                                         reinterpret_cast<uint4*>(khat), rq, rk, lse2, delta,
+                                                         reinterpret_cast<uint4*>(khat), rq, rk, nlse2, delta,
                                                          reinterpret_cast<float4*>(dqacc), tickets,
                                                          dg_reduce_tickets(d), N, n_pad, padded_rows);
   return cudaGetLastError();
