@@ -251,11 +251,16 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
         for (int e = 0; e < 32; ++e)
           if (c * 32 + e >= nvalid) s[c][e] = __float_as_uint(-INFINITY);
     }
-    float mt = -INFINITY;
+    // Row max as eight independent partial maxima (short dependency chains).
+    float mp[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int a = 0; a < 8; ++a) mp[a] = fmaxf(__uint_as_float(s[a >> 1][(a & 1) * 16]), __uint_as_float(s[a >> 1][(a & 1) * 16 + 1]));
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int e = 2; e < 16; e += 2)
+        mp[a] = fmax3(mp[a], __uint_as_float(s[a >> 1][(a & 1) * 16 + e]), __uint_as_float(s[a >> 1][(a & 1) * 16 + e + 1]));
+    const float mt = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
     const float m_tile = mt * scale_log2;
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
     const bool need = (m_new != m_ref) && (j > 0);
@@ -279,11 +284,13 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     // ragged last tile keeps exact zeros for masked keys (MUFU only).
     const uint64_t scale2 = f2_make(scale_log2, scale_log2);
     const uint64_t negm2 = f2_make(neg_m, neg_m);
-    uint64_t l2 = f2_make(0.f, 0.f);
+    uint64_t l2[8];  // partial row sums: two per 32-column chunk
     const bool full_tile = nvalid >= kTileN;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t packed[16];
+      l2[2 * c] = f2_make(0.f, 0.f);
+      l2[2 * c + 1] = f2_make(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         float x0, x1;
@@ -292,14 +299,16 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
         const bool poly = full_tile && ((kPolyPairMask >> (h & 7)) & 1u);
         const float p0 = poly ? exp2_poly(x0) : ex2_approx(x0);
         const float p1 = poly ? exp2_poly(x1) : ex2_approx(x1);
-        l2 = f2_add(l2, f2_make(p0, p1));
+        l2[2 * c + (h & 1)] = f2_add(l2[2 * c + (h & 1)], f2_make(p0, p1));
         packed[h] = pack_bf16x2(p0, p1);
       }
       tmem_st16(tP + c * 16, packed);
     }
     {
       float la, lb;
-      f2_split(l2, la, lb);
+      f2_split(f2_add(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])),
+                      f2_add(f2_add(l2[4], l2[5]), f2_add(l2[6], l2[7]))),
+               la, lb);
       l += la + lb;
     }
     // Rescale O (after P, when the score registers are free); PV(j) waits for
