@@ -46,6 +46,29 @@ def flops_bwd(B, H, N, d):
     return 10.0 * B * H * N * N * d
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one ncu capture of the
+# 512 px workload (profiles/attn_kernels_512px.md), keyed to the kernel source they were taken
+# on: a changed source reports null until it is captured again.
+NCU_TRAFFIC = {
+    "attn_bwd": {"bytes": 192.24448e6 + 64.705792e6, "source": "attn_bwd.cu", "sha1": "85bea76bed1b"},
+    "attn_fwd": {"bytes": 81.293568e6 + 6.992896e6, "source": "attn_fwd.cu", "sha1": "fa58f80f27c6"},
+}
+
+
+def ncu_traffic(kernel):
+    import hashlib
+
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec is None:
+        return None
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "joint_attention_gb300", "csrc", rec["source"])
+    try:
+        cur = hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+    except OSError:
+        return None
+    return rec["bytes"] if cur == rec["sha1"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -371,7 +394,7 @@ def main():
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": ncu_traffic(dom),
                 "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
