@@ -291,8 +291,6 @@ def main():
         raise RuntimeError("device-side wait timed out during warm-up")
 
     # ---- timed region (device time, CUDA events on the launching stream) ----
-    ja.jattn_profile_reset()
-    ja.jattn_profile_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         if world > 1:
@@ -305,8 +303,18 @@ def main():
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
-    ja.jattn_profile_enable(False)
     ms_total = ev0.elapsed_time(ev1)
+    # ---- per-kernel breakdown: the same steps again, each launch bracketed by CUDA events
+    # on the launching stream (the library's profiling mode).  A separate pass, because the
+    # per-launch events sit between kernels and would hold back the overlap of one kernel's
+    # launch with the previous one's tail (programmatic dependent launch) in the timed region.
+    torch.cuda.synchronize(dev)
+    ja.jattn_profile_reset()
+    ja.jattn_profile_enable(True)
+    for i in range(args.steps):
+        step(i)
+    torch.cuda.synchronize(dev)
+    ja.jattn_profile_enable(False)
     prof = ja.profile_snapshot()
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the timed region")

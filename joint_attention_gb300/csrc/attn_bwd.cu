@@ -880,6 +880,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sm = align1024b(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     // With three issuers a Q / dO stage, the dS^T tile and a K/V buffer are
     // each released by commits from their two readers.
@@ -914,11 +915,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bars.abort = 0;
     fence_mbar_init();
   }
-  for (int c = threadIdx.x; c < D; c += blockDim.x) bars.gk[c] = gk[c];
   if (warp == 13) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
+  griddep_wait();  // the previous grid's writes (q_hat, k_hat, LSE / D rows, zeroed dQ) are visible
+  for (int c = threadIdx.x; c < D; c += blockDim.x) bars.gk[c] = gk[c];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -963,10 +965,10 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   w.units = s.BH * w.nkt;
   const int sms = device_sm_count();
   const int grid = w.units < sms ? w.units : sms;
-  attn_bwd_kernel<D><<<grid, kBwdThreads, C::kDynSmem, st>>>(
-      mq, mk, mv, mdo, w, s.scale, nlse2_pad, delta_pad, w.nkt * 128, reinterpret_cast<const __nv_bfloat16*>(k_raw),
-      rk, gk, reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part, dev_err);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, w, s.scale,
+                    nlse2_pad, delta_pad, w.nkt * 128, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
+                    reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part,
+                    dev_err);
 }
 
 }  // namespace

@@ -370,6 +370,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int q0 = blockIdx.x * 2 * kTileM;
   const bool hasB = q0 + kTileM < N;
   const int nkv = (N + kTileN - 1) / kTileN;
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
+  griddep_wait();  // the previous grid's writes (q_hat, k_hat) are visible from here on
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -423,9 +425,8 @@ cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   if (e != cudaSuccess) return e;
   dim3 grid((s.N + 2 * kTileM - 1) / (2 * kTileM), s.BH);
   const float scale_log2 = s.scale * 1.4426950408889634f;
-  attn_fwd_kernel<D><<<grid, kFwdThreads, C::kDynSmem, st>>>(mq, mk, mv, s.N, scale_log2,
-                                                             reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
-  return cudaGetLastError();
+  return launch_pdl(attn_fwd_kernel<D>, grid, dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, s.N, scale_log2,
+                    reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
 }
 
 }  // namespace

@@ -7,6 +7,26 @@
 
 namespace jattn {
 
+// Launches kernel<<<grid, block, smem, st>>>(args...) with programmatic
+// stream serialisation, so that its launch and prologue overlap the tail of
+// the previous kernel on the stream (the kernel waits on griddepcontrol.wait
+// before reading its inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Tile sizes of the tensor-core kernels: 128 query rows per tile (the
 // tcgen05 M = 128 accumulator, one row per TMEM lane), 128 keys per tile.
 constexpr int kTileM = 128;

@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "jattn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace jattn {
 namespace {
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
   constexpr int TPR = D / 8;
   constexpr int RPB = kNormThreads / TPR;  // rows per block per iteration
   const int sub = threadIdx.x % TPR;
+  griddep_launch_dependents();
+  griddep_wait();
   float g_q[8], g_k[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -117,6 +120,8 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
     float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, float4* __restrict__ dqacc,
     unsigned int* __restrict__ tickets, int n_tickets, int N, int n_pad, int64_t padded_rows) {
+  griddep_launch_dependents();
+  griddep_wait();
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < n_tickets) tickets[threadIdx.x] = 0u;
   constexpr int TPR = D / 8;
   constexpr int RPB = kNormThreads / TPR;
@@ -180,6 +185,8 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
   constexpr int TPR = D / 8;
   constexpr int RPB = kNormThreads / TPR;
   const int sub = threadIdx.x % TPR;
+  griddep_launch_dependents();
+  griddep_wait();
   float g[8], acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -255,6 +262,8 @@ __global__ void __launch_bounds__(256) dg_reduce_kernel(const float* __restrict_
                                                         float* __restrict__ dgk) {
   __shared__ float lanes[8][33];
   __shared__ bool last;
+  griddep_launch_dependents();
+  griddep_wait();
   const int arr = blockIdx.z;
   const float* part = arr == 0 ? part_q : part_k;
   const int nparts = arr == 0 ? nq : nk;
@@ -319,13 +328,8 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
   const int grid = row_grid(2 * rows, d);
   auto* a = reinterpret_cast<const uint4*>(q);
   auto* b = reinterpret_cast<const uint4*>(k);
-  if (d == 64)
-    qk_norm_fwd_kernel<64><<<grid, kNormThreads, 0, st>>>(a, b, gq, gk, reinterpret_cast<uint4*>(qhat),
-                                                           reinterpret_cast<uint4*>(khat), rows);
-  else
-    qk_norm_fwd_kernel<128><<<grid, kNormThreads, 0, st>>>(a, b, gq, gk, reinterpret_cast<uint4*>(qhat),
-                                                            reinterpret_cast<uint4*>(khat), rows);
-  return cudaGetLastError();
+  return launch_pdl(d == 64 ? qk_norm_fwd_kernel<64> : qk_norm_fwd_kernel<128>, dim3(grid), dim3(kNormThreads), 0,
+                    st, a, b, gq, gk, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rows);
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
@@ -335,19 +339,10 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
   const int64_t padded_rows = static_cast<int64_t>(BH) * n_pad;
   const int grid = row_grid(padded_rows, d);
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
-  if (d == 64)
-    bwd_prep_kernel<64><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
-                                                        reinterpret_cast<uint4*>(qhat),
-                                                        reinterpret_cast<uint4*>(khat), rq, rk, nlse2, delta,
-                                                        reinterpret_cast<float4*>(dqacc), tickets,
-                                                        dg_reduce_tickets(d), N, n_pad, padded_rows);
-  else
-    bwd_prep_kernel<128><<<grid, kNormThreads, 0, st>>>(u4(q), u4(k), gq, gk, u4(out), u4(dout), lse,
-                                                         reinterpret_cast<uint4*>(qhat),
-                                                         reinterpret_cast<uint4*>(khat), rq, rk, nlse2, delta,
-                                                         reinterpret_cast<float4*>(dqacc), tickets,
-                                                         dg_reduce_tickets(d), N, n_pad, padded_rows);
-  return cudaGetLastError();
+  return launch_pdl(d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>, dim3(grid), dim3(kNormThreads), 0, st,
+                    u4(q), u4(k), gq, gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat),
+                    reinterpret_cast<uint4*>(khat), rq, rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets,
+                    dg_reduce_tickets(d), N, n_pad, padded_rows);
 }
 
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
@@ -355,9 +350,8 @@ cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float
   auto* a = reinterpret_cast<const float4*>(dqacc);
   auto* x = reinterpret_cast<const uint4*>(q);
   auto* y = reinterpret_cast<uint4*>(dq);
-  if (d == 64) q_norm_bwd_kernel<64><<<nparts, kNormThreads, 0, st>>>(a, x, rq, gq, scale, y, dgq_part, rows);
-  else q_norm_bwd_kernel<128><<<nparts, kNormThreads, 0, st>>>(a, x, rq, gq, scale, y, dgq_part, rows);
-  return cudaGetLastError();
+  return launch_pdl(d == 64 ? q_norm_bwd_kernel<64> : q_norm_bwd_kernel<128>, dim3(nparts), dim3(kNormThreads), 0,
+                    st, a, x, rq, gq, scale, y, dgq_part, rows);
 }
 
 int dg_reduce_scratch_floats(int d) { return 2 * kDgSlices * d; }
@@ -365,9 +359,8 @@ int dg_reduce_tickets(int d) { return 2 * ((d + 31) / 32); }
 
 cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* slice_part,
                              unsigned int* tickets, float* dgq, float* dgk, cudaStream_t st) {
-  dg_reduce_kernel<<<dim3((d + 31) / 32, kDgSlices, 2), dim3(32, 8), 0, st>>>(part_q, nq, part_k, nk, d, slice_part,
-                                                                               tickets, dgq, dgk);
-  return cudaGetLastError();
+  return launch_pdl(dg_reduce_kernel, dim3((d + 31) / 32, kDgSlices, 2), dim3(32, 8), 0, st, part_q, nq, part_k,
+                    nk, d, slice_part, tickets, dgq, dgk);
 }
 
 }  // namespace jattn

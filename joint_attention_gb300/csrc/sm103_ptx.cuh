@@ -37,6 +37,15 @@ __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation: it lets the next grid of the stream
+// launch as soon as all of its own CTAs are resident (launch_dependents, at
+// the start), and waits for the previous grid to complete and its writes to
+// be visible (wait) before it touches global memory.  Without the launch
+// attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
