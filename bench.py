@@ -94,7 +94,7 @@ def load_peaks():
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,6 +102,10 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.file = None
+        self.window = None  # (t0, t1) wall-clock seconds of the timed loop
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __enter__(self):
         try:
@@ -130,9 +134,21 @@ class ClockSampler:
         with open(self.file.name) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
+                if len(parts) >= 10:
                     rows.append(parts)
         os.unlink(self.file.name)
+        scope = "all samples"
+        if self.window is not None:
+            import datetime
+
+            def stamp(r):
+                try:
+                    return datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    return None
+            inside = [r for r in rows if stamp(r) is not None and self.window[0] <= stamp(r) <= self.window[1]]
+            if inside:
+                rows, scope = inside, "timed loop"
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
@@ -141,13 +157,13 @@ class ClockSampler:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_median": statistics.median([num(r[3]) for r in rows if num(r[3]) is not None] or [0])}
+                "reasons": reasons, "samples": len(rows), "scope": scope,
+                "power_w_median": statistics.median([num(r[4]) for r in rows if num(r[4]) is not None] or [0])}
 
 
 def dist_setup():
@@ -181,35 +197,61 @@ def cpu_oracle_sample(B, H, N, d, seed, budget_s: float, max_heads: int):
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm (rank 0 only)."""
+    """The CPU oracle as the reference arm (rank 0 only).
+
+    A step is one head of the workload run through the oracle's own steps (RMSNorm of q and k,
+    bf16 rounding of q_hat and k_hat, softmax attention with materialised scores, its exact
+    backward, the RMSNorm backward), restricted to R of the head's N query rows against all N
+    keys.  R is the full N when K steps of whole heads fit the time budget, otherwise the largest
+    row count that does; the FLOP per step is 14·R·N·d, the same count per query row as the GPU
+    arm's 14·B·H·N²·d."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    from joint_attention_gb300.inputs import CONFIGS
-
-    c = CONFIGS[WORKLOAD]
     import numpy as np
 
     import oracle
-    from joint_attention_gb300.inputs import make_inputs
+    from joint_attention_gb300.inputs import CONFIGS, make_inputs
 
-    inp = make_inputs(1, 1, c.N, c.d, seed=c.seed)
+    c = CONFIGS[WORKLOAD]
+    N, d = c.N, c.d
+    inp = make_inputs(1, 1, N, d, seed=c.seed)
+    q, k, v, dout = (np.asarray(x[0, 0], dtype=np.float64) for x in (inp.q, inp.k, inp.v, inp.dout))
+    gq, gk = np.asarray(inp.gq, dtype=np.float64), np.asarray(inp.gk, dtype=np.float64)
+    scale = 1.0 / np.sqrt(d)
+
+    def step(R):
+        qh, rq = oracle.rmsnorm_fwd(q[:R], gq)
+        kh, rk = oracle.rmsnorm_fwd(k, gk)
+        qh, kh = oracle.round_to_bf16(qh), oracle.round_to_bf16(kh)
+        O, _, P = oracle.attention_fwd_head(qh, kh, v, scale)
+        dqh, dkh, _ = oracle.attention_bwd_head(qh, kh, v, P, O, dout[:R], scale)
+        oracle.rmsnorm_bwd(q[:R], gq, rq, dqh)
+        oracle.rmsnorm_bwd(k, gk, rk, dkh)
+
+    t0 = time.perf_counter()
+    step(N)
+    t_head = time.perf_counter() - t0
+    budget_s = 120.0
+    R = N
+    if (args.steps + args.warmup) * t_head > budget_s:
+        R = max(16, int(N * budget_s / ((args.steps + args.warmup) * t_head)))
     for _ in range(args.warmup):
-        oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+        step(R)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+        step(R)
     el = time.perf_counter() - t0
-    fl = (flops_fwd(1, 1, c.N, c.d) + flops_bwd(1, 1, c.N, c.d)) * args.steps
+    fl = 14.0 * R * N * d * args.steps
     val = fl / el / 1e12
-    del np
-    sample = (f"each step = one (b, h) head of the {WORKLOAD} workload (N={c.N}, d={c.d}) fwd+bwd in float64 "
-              f"NumPy with materialised scores")
+    sample = (f"each step = {R} of the N={N} query rows of one (b, h) head of the {WORKLOAD} workload "
+              f"(d={d}) against all N keys, fwd+bwd with the RMSNorm steps, float64 NumPy with "
+              f"materialised scores")
     line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": f"{WORKLOAD} B16 H12 N_img1024 N_txt77 d64 (one head per step)",
+            "config": {"workload": f"{WORKLOAD} B16 H12 N_img1024 N_txt77 d64 (a bounded sample per step)",
                        "sample": sample},
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
@@ -218,15 +260,69 @@ def run_reference(args):
     return 0
 
 
+def per_config_throughput(ja, torch, dev, stream, steps=10, warmup=3):
+    """TFLOP/s and images-equivalent/s of every workload of the parity suite (one GPU, eager
+    calls, inputs resident on the device; the fwd+bwd rows are 14·B·H·N²·d per step, the CFG
+    sampling row is its forward, 4·B·H·N²·d per denoising step).  Inputs are seeded device
+    normals of each workload's shape (values do not change the work)."""
+    from joint_attention_gb300.inputs import CONFIGS
+
+    res = {}
+    gen = torch.Generator(device=dev)
+    for name, c in CONFIGS.items():
+        B, H, N, d = c.B, c.H, c.N, c.d
+        gen.manual_seed(1000 + c.seed)
+        shape = (B, H, N, d)
+        t = {key: (torch.randn(shape, generator=gen, device=dev) * c.value_scale).to(torch.bfloat16)
+             for key in ("q", "k", "v", "dout")}
+        gq = torch.rand(d, generator=gen, device=dev) + 0.5
+        gk = torch.rand(d, generator=gen, device=dev) + 0.5
+        out, lse = torch.empty_like(t["q"]), torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
+        fwd_only = c.mode == "cfg_fwd"
+
+        def one():
+            ja.jattn_fwd(t["q"], t["k"], t["v"], gq, gk, B, H, c.N_img, c.N_txt, d, out, lse, stream)
+            if not fwd_only:
+                ja.jattn_bwd(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], dq, dk, dv, dgq, dgk, B, H,
+                             c.N_img, c.N_txt, d, stream)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        fl = flops_fwd(B, H, N, d) + (0.0 if fwd_only else flops_bwd(B, H, N, d))
+        row = {"mode": "fwd (CFG sampling step)" if fwd_only else "fwd+bwd", "B": B, "H": H, "N": N, "d": d,
+               "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+        if fwd_only:
+            row["images_per_s"] = c.n_uncond / (c.steps * 12 * ms * 1e-3)
+        else:
+            row["images_equiv_per_s"] = B / (12 * ms * 1e-3)
+        res[name] = row
+        del t, out, lse, dq, dk, dv
+    if ja.jattn_last_device_error(stream) != 0:
+        raise RuntimeError("device-side wait timed out in the per-config pass")
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    # The default timed loop runs about a second, so that the 200 ms clock samples fall inside it.
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload throughput pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -296,11 +392,13 @@ def main():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        wall0 = time.time()
         ev0.record(stream)
         for i in range(args.steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        clocks.mark(wall0, time.time())
         if world > 1:
             dist.barrier()
     ms_total = ev0.elapsed_time(ev1)
@@ -357,7 +455,7 @@ def main():
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        n_e2e = max(3, args.steps // 3)
+        n_e2e = max(3, min(args.steps, 300))
         for _ in range(n_e2e):
             e2e_step()
         e1.record(stream)
@@ -404,6 +502,9 @@ def main():
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": ncu_traffic(dom),
                 "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
+    per_cfg = None
+    if not args.no_per_config and world == 1:
+        per_cfg = per_config_throughput(ja, torch, dev, stream)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(B, H, N, d, c.seed, args.cpu_budget_s, max_heads=64)
@@ -422,7 +523,7 @@ def main():
         "images_equiv_per_s": B * world / (12 * ms_step * 1e-3),
         "model_tflops": 12.0 * B * H * N * N * d * args.steps * world / (ms_total * 1e-3) / 1e12,
         "roofline": roofline, "kernels": kern, "gpu_launches": launches,
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(), "per_config": per_cfg,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
