@@ -50,8 +50,8 @@ def flops_bwd(B, H, N, d):
 # 512 px workload (profiles/attn_kernels_512px.md), keyed to the kernel source they were taken
 # on: a changed source reports null until it is captured again.
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 192.24448e6 + 64.705792e6, "source": "attn_bwd.cu", "sha1": "85bea76bed1b"},
-    "attn_fwd": {"bytes": 81.293568e6 + 6.992896e6, "source": "attn_fwd.cu", "sha1": "fa58f80f27c6"},
+    "attn_bwd": {"bytes": 192.245248e6 + 64.978432e6, "source": "attn_bwd.cu", "sha1": "4df7189e1c7a"},
+    "attn_fwd": {"bytes": 81.27744e6 + 6.867968e6, "source": "attn_fwd.cu", "sha1": "a63f40942299"},
 }
 
 
