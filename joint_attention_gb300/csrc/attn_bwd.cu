@@ -15,7 +15,8 @@
 // u = blockIdx.x, blockIdx.x + gridDim.x, ... with every barrier phase
 // running on across units, so the next unit's K/V load and first S / dP
 // products overlap the current unit's last tiles and its epilogue.
-// 512 threads:
+// 640 threads (five warpgroups; setmaxnreg gives the two compute
+// warpgroups 128 registers per thread and the other three 72):
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
@@ -24,14 +25,17 @@
 //               MMA's swizzled layout (A operand of dK, and of dQ read
 //               MN-major).
 //   warps 8-11  dQ drain: one thread per query row moves dQ_i from TMEM to a
-//               padded shared-memory row and issues a bulk reduce-add of it.
-//               At the end of a unit the same threads (now one per key row)
-//               write dv, apply the K-RMSNorm backward to dK (dk and the
-//               unit's dgk partial) and release the accumulators.
-//   warp 12     TMA producer: K_j, V_j per unit (double-buffered for d = 64);
+//               padded shared-memory row and issues a bulk reduce-add of it
+//               (d = 128: also the unit epilogue).
+//   warps 12-15 d = 64 unit epilogue, one thread per key row: dv, and the
+//               K-RMSNorm backward of dK (dk and the unit's dgk partial),
+//               built in the unit's own K/V buffer once the MMAs are done
+//               with it; the TMEM accumulators are released as soon as they
+//               are read, so the next unit never waits on this work.
+//   warp 16     TMA producer: K_j, V_j per unit (double-buffered for d = 64);
 //               Q_i (+ LSE_i, D_i) and dO_i per query tile through rings.
-//   warps 13-15 MMA issuers (d = 64): recompute (S, dP), gradients (dV, dK)
-//               and dQ; d = 128 uses warp 13 alone.
+//   warps 17-19 MMA issuers (d = 64): recompute (S, dP), gradients (dV, dK)
+//               and dQ; d = 128 uses warp 17 alone.
 //
 // d = 64: TMEM (512 columns) S^T [0,128), dP^T [128,256), dV [256,320),
 // dK [320,384), dQ [384,448), P^T [448,512) (packed bf16).  The compute
@@ -53,7 +57,16 @@
 namespace jattn {
 namespace {
 
-constexpr int kBwdThreads = 512;
+constexpr int kBwdThreads = 640;  // 5 warpgroups
+// Warp roles: 0-7 compute (two groups), 8-11 dQ drain, 12-15 epilogue
+// (d = 64), 16 TMA, 17-19 MMA issuers.  The compute warpgroups run with 128
+// registers per thread, the others with 72 (setmaxnreg; 256 x 128 + 384 x 72
+// = 60416 of the 640 x 96 registers the block launches with).
+constexpr int kWarpEpi = 12;
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma0 = 17;  // recompute issuer (d = 128: the only one)
+constexpr int kWarpMma1 = 18;  // gradient issuer
+constexpr int kWarpMma2 = 19;  // dQ issuer
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -108,6 +121,7 @@ struct BwdWork {
 
 struct BwdBars {
   uint64_t kv_full[2], kv_empty[2];
+  uint64_t kv_mmadone[2];  // d = 64: the unit's MMAs are done with K/V buffer b
   uint64_t q_full[3], q_empty[3];
   uint64_t do_full[2], do_empty[2];
   uint64_t s_full, dp_full;
@@ -125,6 +139,7 @@ struct BwdBars {
   // Per query stage: minus the tile's LSE in the log2 domain (-inf past N)
   // and D (0 past N), copied in with the tile from padded scratch rows.
   __align__(16) float gk[128];  // K-RMSNorm gain (d entries)
+  __align__(16) float wsum[4][64];  // d = 64 epilogue: per-warp dgk column sums
   __align__(16) float nlse2[3][128];
   __align__(16) float delta[3][128];
 };
@@ -282,7 +297,7 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       umma_commit(&bars.dp_full);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
     }
-    if (ok) umma_commit(&bars.kv_empty[b]);
+    if (ok) umma_commit(&bars.kv_mmadone[b]);
   }
   umma_commit(&bars.drain[0]);
   mbar_wait_drain(&bars.drain[0], 0);
@@ -345,7 +360,7 @@ __device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdW
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[0]);
     }
-    if (ok) umma_commit(&bars.kv_empty[b]);
+    if (ok) umma_commit(&bars.kv_mmadone[b]);
   }
   umma_commit(&bars.drain[2]);
   mbar_wait_drain(&bars.drain[2], 0);
@@ -568,11 +583,8 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
                                    uint32_t* dev_err) {
   using C = BwdCfg<D>;
   constexpr int kRowFloats = C::kDQRowBytes / 4;
-  // d = 64: the epilogue runs through the staging area (free between two dQ
-  // drains) as 128-byte-row tiles, so that every global access is a
-  // contiguous 512-byte warp access.
+  // d = 64: the epilogue warps take the unit epilogue; these warps only drain dQ.
   constexpr bool kTiled = (D == 64);
-  static_assert(!kTiled || 2 * 128 * D * 2 + 4 * D * 4 <= 128 * C::kDQRowBytes, "epilogue tiles fit the staging area");
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int r128 = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQ) or key row (dV, dK)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -581,15 +593,6 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
   uint8_t* srow = sm + C::kOffDQ + r128 * C::kDQRowBytes;
   const uint32_t srow_a = smem_u32(srow);
   const float* red = reinterpret_cast<const float*>(sm + C::kOffDQ);
-  // Tiled epilogue layout: k (then dk) tile, dv tile, 128-byte rows with the
-  // 16-byte chunks XOR-swizzled by (row & 7); then 4 x D floats of per-warp
-  // column sums.
-  const uint32_t tile_k = smem_u32(sm + C::kOffDQ);
-  const uint32_t tile_v = tile_k + 128 * D * 2;
-  float* wsum = reinterpret_cast<float*>(sm + C::kOffDQ + 2 * 128 * D * 2);
-  auto chunk_addr = [](uint32_t tile, int row, int c) {
-    return tile + static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
-  };
   volatile int* ab = &bars.abort;
   uint32_t epi_uses = 0;
   // Bounded barrier among the 128 drain threads.
@@ -603,14 +606,10 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
     const int n = kv0 + r128;  // key row of this thread in the epilogue
     const bool key_live = n < w.N;
-    const int live_rows = w.N - kv0 < 128 ? w.N - kv0 : 128;
-    const size_t tile_off = (static_cast<size_t>(bh) * w.N + kv0) * D;  // first row of the key tile
     const size_t row_off = (static_cast<size_t>(bh) * w.N + (key_live ? n : 0)) * D;
 
     for (int i = 0; i < w.nkt; ++i) {
       const int t = ui * w.nkt + i;
-      // The raw k tile is pulled into L2 while the last dQ tile is computed.
-      if (kTiled && i == w.nkt - 1 && r128 == 0) bulk_prefetch_l2(k_raw + tile_off, live_rows * D * 2);
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -641,118 +640,13 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     }
     if (!ok) break;
 
-    // ---- unit epilogue ----
+    // ---- unit epilogue (d = 128; at d = 64 the epilogue warps take it) ----
+    if constexpr (kTiled) continue;
     ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
     const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
-    if constexpr (kTiled) {
-      // Accumulators out of TMEM first: dV packed to bf16 (32 registers),
-      // dK (64 registers); both column ranges released.
-      uint32_t vp[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) vp[c * 16 + e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-      }
-      tc_fence_before();
-      mbar_arrive(&bars.acc_free_v);
-      uint32_t a[D];
-      tmem_ld32(tDK, *reinterpret_cast<uint32_t(*)[32]>(a));
-      tmem_ld32(tDK + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.acc_free_k);
-      bulk_wait_group_read0();        // this thread's staging row has been read
-      if (!(ok = epi_sync())) break;  // ... and every other row too
-      // dv row into the dv tile
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c)
-        st_shared_v4(chunk_addr(tile_v, r128, c), vp[4 * c], vp[4 * c + 1], vp[4 * c + 2], vp[4 * c + 3]);
-      // raw k tile into shared memory: chunk q = it * 128 + r128, 32
-      // consecutive 16-byte chunks per warp access.
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(k_raw + tile_off);
-        uint4 kw[8];
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int q = it * 128 + r128;
-          kw[it] = (q >> 3) < live_rows ? src[q] : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int q = it * 128 + r128;
-          st_shared_v4(chunk_addr(tile_k, q >> 3, q & 7), kw[it].x, kw[it].y, kw[it].z, kw[it].w);
-        }
-      }
-      if (!(ok = epi_sync())) break;  // the k tile is complete
-      // dot = sum_c g_c dk_hat_c k_c over this thread's row
-      float dot = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 kw = ld_shared_v4(chunk_addr(tile_k, r128, c));
-        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int col = c * 8 + 2 * h;
-          dot = fmaf(bars.gk[col] * __uint_as_float(a[col]), __uint_as_float(kx[h] << 16), dot);
-          dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[col + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
-        }
-      }
-      const float coef = r * r * r * (1.f / D) * scale * dot;
-      // dk = r g dk_hat - coef k over the k row (in place); a[] becomes the
-      // row's dgk terms dk_hat k r.
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = chunk_addr(tile_k, r128, c);
-        const uint4 kw = ld_shared_v4(addr);
-        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int col = c * 8 + 2 * h;
-          const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
-          const float dk0 = __uint_as_float(a[col]) * scale, dk1 = __uint_as_float(a[col + 1]) * scale;
-          o[h] = pack_bf16x2(r * bars.gk[col] * dk0 - coef * x0, r * bars.gk[col + 1] * dk1 - coef * x1);
-          a[col] = __float_as_uint(key_live ? dk0 * x0 * r : 0.f);
-          a[col + 1] = __float_as_uint(key_live ? dk1 * x1 * r : 0.f);
-        }
-        st_shared_v4(addr, o[0], o[1], o[2], o[3]);
-      }
-      // dgk: reduce-scatter over the warp's 32 rows (lane L ends with the
-      // sums of columns 2L, 2L+1), then the 4 warps in order.
-#pragma unroll
-      for (int m = 16, half = 32; m >= 1; m >>= 1, half >>= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int j = 0; j < half; ++j) {
-          const float send = __uint_as_float(upper ? a[j] : a[j + half]);
-          const float keep = __uint_as_float(upper ? a[j + half] : a[j]);
-          a[j] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, m));
-        }
-      }
-      wsum[(warp & 3) * D + 2 * lane] = __uint_as_float(a[0]);
-      wsum[(warp & 3) * D + 2 * lane + 1] = __uint_as_float(a[1]);
-      if (!(ok = epi_sync())) break;  // dk tile, dv tile and warp sums complete
-      if (r128 < D)
-        dgk_part[static_cast<size_t>(u) * D + r128] =
-            ((wsum[r128] + wsum[D + r128]) + wsum[2 * D + r128]) + wsum[3 * D + r128];
-      // dk and dv tiles out, 32 consecutive 16-byte chunks per warp access.
-      uint4* dkdst = reinterpret_cast<uint4*>(dk + tile_off);
-      uint4* dvdst = reinterpret_cast<uint4*>(dv + tile_off);
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int q = it * 128 + r128;
-        if ((q >> 3) < live_rows) {
-          dkdst[q] = ld_shared_v4(chunk_addr(tile_k, q >> 3, q & 7));
-          dvdst[q] = ld_shared_v4(chunk_addr(tile_v, q >> 3, q & 7));
-        }
-      }
-      if (!(ok = epi_sync())) break;  // tiles read: the staging rows are free again
-    } else {
+    if constexpr (!kTiled) {
       // d = 128: per-row accesses; two passes over the TMEM dK accumulator
       // (dot, then outputs), the dgk rows staged kDQCols columns at a time.
       const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
@@ -865,6 +759,178 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
   bulk_wait_group0();
 }
 
+// d = 64 epilogue warps (warps 12-15, one thread per key row): per unit,
+// once its last dK product is done, dv = bf16(dV acc) and the K-RMSNorm
+// backward of dK (dk_hat = scale * acc; u = g * dk_hat; dk = r u - (r^3/d) k
+// sum(u k); the unit's dgk partial = column sums of dk_hat * k * r).  The
+// tiles are built in the unit's own K/V buffer, which the MMAs have finished
+// with (kv_mmadone) and which the producer reloads only after this releases
+// it (kv_empty), so that k, dk and dv move with contiguous 512-byte warp
+// accesses and no other role waits on this work except through the TMEM
+// accumulators, released as soon as they are read.
+template <int D>
+__device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, float scale,
+                                   const __nv_bfloat16* __restrict__ k_raw, const float* __restrict__ rk,
+                                   __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                   float* __restrict__ dgk_part, uint32_t* dev_err) {
+  using C = BwdCfg<D>;
+  static_assert(D == 64, "the epilogue warps serve d = 64");
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r128 = (warp & 3) * 32 + lane;  // key row == TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tDK = tmem + lane_base + C::kColDK;
+  auto chunk_addr = [](uint32_t tile, int row, int c) {
+    return tile + static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+  };
+  volatile int* ab = &bars.abort;
+  uint32_t epi_uses = 0;
+  // Bounded barrier among the 128 epilogue threads.
+  auto epi_sync = [&]() -> bool {
+    mbar_arrive(&bars.epi);
+    const bool okb = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
+    return __all_sync(0xffffffffu, okb);
+  };
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
+    const int b = ui % C::kKVBufs;
+    const int n = kv0 + r128;
+    const bool key_live = n < w.N;
+    const int live_rows = w.N - kv0 < 128 ? w.N - kv0 : 128;
+    const size_t tile_off = (static_cast<size_t>(bh) * w.N + kv0) * D;
+    // The raw k tile is pulled into L2 while the unit runs.
+    if (r128 == 0) bulk_prefetch_l2(k_raw + tile_off, live_rows * D * 2);
+    const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
+    const uint32_t tile_k = smem_u32(sm + C::off_k(b));  // k, then dk
+    const uint32_t tile_v = smem_u32(sm + C::off_v(b));  // dv
+
+    ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
+    // ... and the unit's MMAs are done with its K/V buffer.
+    if (ok) ok = mbar_wait(&bars.kv_mmadone[b], (ui / C::kKVBufs) & 1, ab, dev_err);
+    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+    tc_fence_after();
+    // dV out of TMEM into the dv tile (bf16), its columns released.
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
+      tmem_wait_ld();
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        mbar_arrive(&bars.acc_free_v);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(chunk_addr(tile_v, r128, c * 4 + q),
+                     pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1])),
+                     pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3])),
+                     pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5])),
+                     pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7])));
+    }
+    // raw k tile: chunk q = it * 128 + r128, 32 consecutive 16-byte chunks
+    // per warp access.
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(k_raw + tile_off);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint4 kw[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int q = (half * 4 + it) * 128 + r128;
+          kw[it] = (q >> 3) < live_rows ? src[q] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int q = (half * 4 + it) * 128 + r128;
+          st_shared_v4(chunk_addr(tile_k, q >> 3, q & 7), kw[it].x, kw[it].y, kw[it].z, kw[it].w);
+        }
+      }
+    }
+    if (!(ok = epi_sync())) break;  // the k tile is complete
+    // Pass 1: dot = sum_c g_c dk_hat_c k_c over this thread's row.
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tDK + c * 32, a);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 kw = ld_shared_v4(chunk_addr(tile_k, r128, c * 4 + q));
+        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = q * 8 + 2 * h, col = c * 32 + e;
+          dot = fmaf(bars.gk[col] * __uint_as_float(a[e]), __uint_as_float(kx[h] << 16), dot);
+          dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[e + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
+        }
+      }
+    }
+    const float coef = r * r * r * (1.f / D) * scale * dot;
+    // Pass 2, per 32-column chunk: dk = r g dk_hat - coef k over the k row
+    // (in place), and the chunk's dgk terms dk_hat k r summed over the warp's
+    // 32 rows by a reduce-scatter (lane L ends with column 32c + L).
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tDK + c * 32, a);
+      tmem_wait_ld();
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        mbar_arrive(&bars.acc_free_k);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t addr = chunk_addr(tile_k, r128, c * 4 + q);
+        const uint4 kw = ld_shared_v4(addr);
+        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = q * 8 + 2 * h, col = c * 32 + e;
+          const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
+          const float dk0 = __uint_as_float(a[e]) * scale, dk1 = __uint_as_float(a[e + 1]) * scale;
+          o[h] = pack_bf16x2(r * bars.gk[col] * dk0 - coef * x0, r * bars.gk[col + 1] * dk1 - coef * x1);
+          a[e] = __float_as_uint(key_live ? dk0 * x0 * r : 0.f);
+          a[e + 1] = __float_as_uint(key_live ? dk1 * x1 * r : 0.f);
+        }
+        st_shared_v4(addr, o[0], o[1], o[2], o[3]);
+      }
+#pragma unroll
+      for (int m = 16, half = 16; m >= 1; m >>= 1, half >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+          const float send = __uint_as_float(upper ? a[j] : a[j + half]);
+          const float keep = __uint_as_float(upper ? a[j + half] : a[j]);
+          a[j] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, m));
+        }
+      }
+      bars.wsum[warp & 3][c * 32 + lane] = __uint_as_float(a[0]);
+    }
+    if (!(ok = epi_sync())) break;  // dk tile, dv tile and warp sums complete
+    if (r128 < D)
+      dgk_part[static_cast<size_t>(u) * D + r128] =
+          ((bars.wsum[0][r128] + bars.wsum[1][r128]) + bars.wsum[2][r128]) + bars.wsum[3][r128];
+    // dk and dv tiles out, 32 consecutive 16-byte chunks per warp access.
+    uint4* dkdst = reinterpret_cast<uint4*>(dk + tile_off);
+    uint4* dvdst = reinterpret_cast<uint4*>(dv + tile_off);
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int q = it * 128 + r128;
+      if ((q >> 3) < live_rows) {
+        dkdst[q] = ld_shared_v4(chunk_addr(tile_k, q >> 3, q & 7));
+        dvdst[q] = ld_shared_v4(chunk_addr(tile_v, q >> 3, q & 7));
+      }
+    }
+    // The K/V buffer goes back to the producer: every thread orders its
+    // generic-proxy accesses before the next TMA fill, then one releases it.
+    fence_proxy_async_smem();
+    if (!(ok = epi_sync())) break;  // tiles read (and wsum free)
+    if (r128 == 0) mbar_arrive(&bars.kv_empty[b]);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -891,7 +957,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], n_rel);
+      mbar_init(&bars.kv_empty[s], 1);  // d = 64: the epilogue; d = 128: the issuer
+      mbar_init(&bars.kv_mmadone[s], n_rel);
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], n_rel);
       mbar_init(&bars.ds_free[s], n_rel);
@@ -915,7 +982,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bars.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == kWarpMma0) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
@@ -926,25 +993,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == 12) {
-    if (lane == 0) bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, nlse2_pad, delta_pad, n_pad, dev_err);
-  } else if (warp == 13) {
-    if (lane == 0) {
-      if (C::kSplitIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
-      else bwd_mma<D>(sm, bars, tmem, w, dev_err);
-    }
-  } else if (warp == 14) {
-    if (lane == 0 && C::kSplitIssuers) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
-  } else if (warp == 15) {
-    if (lane == 0 && C::kSplitIssuers) bwd_mma_dq<D>(sm, bars, tmem, w, dev_err);
-  } else if (warp < 8) {
+  if (warp < 8) {
+    setmaxnreg_inc<128>();
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
-    bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, dk, dv, dgk_part, dev_err);
+    setmaxnreg_dec<72>();
+    if (warp < kWarpEpi) {
+      bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, dk, dv, dgk_part, dev_err);
+    } else if (warp < kWarpTma) {
+      if constexpr (D == 64) bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, k_raw, rk, dk, dv, dgk_part, dev_err);
+    } else if (warp == kWarpTma) {
+      if (lane == 0)
+        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, nlse2_pad, delta_pad, n_pad, dev_err);
+    } else if (warp == kWarpMma0) {
+      if (lane == 0) {
+        if (C::kSplitIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
+        else bwd_mma<D>(sm, bars, tmem, w, dev_err);
+      }
+    } else if (warp == kWarpMma1) {
+      if (lane == 0 && C::kSplitIssuers) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
+    } else if (warp == kWarpMma2) {
+      if (lane == 0 && C::kSplitIssuers) bwd_mma_dq<D>(sm, bars, tmem, w, dev_err);
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == kWarpMma0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
