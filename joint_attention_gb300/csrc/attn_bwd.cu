@@ -15,8 +15,8 @@
 // u = blockIdx.x, blockIdx.x + gridDim.x, ... with every barrier phase
 // running on across units, so the next unit's K/V load and first S / dP
 // products overlap the current unit's last tiles and its epilogue.
-// 640 threads (five warpgroups; setmaxnreg gives the two compute
-// warpgroups 128 registers per thread and the other three 72):
+// 640 threads (five warpgroups; setmaxnreg gives the compute warpgroups 128
+// registers per thread, the drain 104, the epilogue 72 and TMA / MMA 40):
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
@@ -59,9 +59,23 @@ namespace {
 
 constexpr int kBwdThreads = 640;  // 5 warpgroups
 // Warp roles: 0-7 compute (two groups), 8-11 dQ drain, 12-15 epilogue
-// (d = 64), 16 TMA, 17-19 MMA issuers.  The compute warpgroups run with 128
-// registers per thread, the others with 72 (setmaxnreg; 256 x 128 + 384 x 72
-// = 60416 of the 640 x 96 registers the block launches with).
+// (d = 64), 16 TMA, 17-19 MMA issuers.  Registers per thread (setmaxnreg):
+// compute 128, drain 104, epilogue 72, TMA / issuers 40 (d = 128: 72 for all
+// but compute); 256 x 128 + 128 x (104 + 72 + 40) = 256 x 128 + 384 x 72 =
+// 60416 of the 640 x 96 the block launches with.
+// setmaxnreg budgets.  An increase must not be below, a decrease not above,
+// the count the kernel launches with, and the sum must fit the launch's
+// registers (640 x that count); the launcher checks both against the
+// compiled kernel before every launch.
+constexpr int kRegCompute = 128, kRegDrain64 = 104, kRegEpi64 = 72, kRegMma64 = 40, kRegOther128 = 72;
+constexpr int kRegLaunchMin = 95, kRegLaunchMax = 104;  // kRegDrain64 and kRegEpi64 / kRegOther128 bounds
+static_assert(256 * kRegCompute + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <= kBwdThreads * kRegLaunchMin,
+              "d = 64 register split exceeds the launch allocation");
+static_assert(256 * kRegCompute + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
+              "d = 128 register split exceeds the launch allocation");
+static_assert(kRegEpi64 <= kRegLaunchMin && kRegMma64 <= kRegLaunchMin && kRegOther128 <= kRegLaunchMin &&
+                  kRegDrain64 >= kRegLaunchMax && kRegCompute >= kRegLaunchMax,
+              "setmaxnreg direction");
 constexpr int kWarpEpi = 12;
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma0 = 17;  // recompute issuer (d = 128: the only one)
@@ -615,26 +629,47 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
       tc_fence_after();
       const int qrow = w.query_tile(u, i) * 128 + r128;
       float* grow = dqacc + (static_cast<size_t>(bh) * w.N + (qrow < w.N ? qrow : 0)) * D;
+      if constexpr (kTiled) {
+        // d = 64: the whole dQ row into registers and the TMEM columns
+        // released first, then the staging row once its previous reduce has
+        // read it.
+        uint32_t a[D];
+        tmem_ld32(tQ, *reinterpret_cast<uint32_t(*)[32]>(a));
+        tmem_ld32(tQ + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars.dq_free);
+        bulk_wait_group_read0();
 #pragma unroll
-      for (int pass = 0; pass < D / C::kDQCols; ++pass) {
-        bulk_wait_group_read0();  // the previous reduce has finished reading the row
-#pragma unroll
-        for (int c = 0; c < C::kDQCols / 32; ++c) {
-          uint32_t a[32];
-          tmem_ld32(tQ + pass * C::kDQCols + c * 32, a);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(srow_a + (c * 32 + q * 4) * 4, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-        }
-        if (pass == D / C::kDQCols - 1) {
-          tc_fence_before();
-          mbar_arrive(&bars.dq_free);
-        }
+        for (int q = 0; q < D / 4; ++q)
+          st_shared_v4(srow_a + q * 16, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
         fence_proxy_async_smem();
         if (qrow < w.N) {
-          bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
+          bulk_reduce_add_f32(grow, srow, D * 4);
           bulk_commit_group();
+        }
+      } else {
+  #pragma unroll
+        for (int pass = 0; pass < D / C::kDQCols; ++pass) {
+          bulk_wait_group_read0();  // the previous reduce has finished reading the row
+  #pragma unroll
+          for (int c = 0; c < C::kDQCols / 32; ++c) {
+            uint32_t a[32];
+            tmem_ld32(tQ + pass * C::kDQCols + c * 32, a);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(srow_a + (c * 32 + q * 4) * 4, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+          }
+          if (pass == D / C::kDQCols - 1) {
+            tc_fence_before();
+            mbar_arrive(&bars.dq_free);
+          }
+          fence_proxy_async_smem();
+          if (qrow < w.N) {
+            bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
+            bulk_commit_group();
+          }
         }
       }
     }
@@ -994,10 +1029,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp < 8) {
-    setmaxnreg_inc<128>();
+    setmaxnreg_inc<kRegCompute>();
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
-    setmaxnreg_dec<72>();
+    if constexpr (D == 64) {
+      if (warp < kWarpEpi) setmaxnreg_inc<kRegDrain64>();  // up from the launch count
+      else if (warp < kWarpTma) setmaxnreg_dec<kRegEpi64>();
+      else setmaxnreg_dec<kRegMma64>();
+    } else {  // d = 128: the drain warps run the epilogue; one issuer
+      setmaxnreg_dec<kRegOther128>();
+    }
     if (warp < kWarpEpi) {
       bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, dk, dv, dgk_part, dev_err);
     } else if (warp < kWarpTma) {
@@ -1033,6 +1074,12 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   static_assert(C::kDynSmem + static_cast<int>(sizeof(BwdBars)) <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
+  // The setmaxnreg split is valid only for the register count it was sized
+  // for; any other build is refused rather than launched.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
   BwdWork w;
   w.N = s.N;
   w.nkt = (s.N + 127) / 128;
