@@ -6,11 +6,15 @@
 // fix" section: the materialised B x 12 x 1101 x 1101 scores were the memory
 // wall; the same [B, H, N, d] Q/K/V layout goes through a fused kernel).
 //
-// One CTA owns 256 query rows of one (b, h) as two 128-row tiles A and B and
-// streams all key/value tiles of that head through a shared-memory ring:
+// Work unit: 256 query rows of one (b, h) as two 128-row tiles A and B,
+// streaming all key/value tiles of that head.  The kernel is persistent: one
+// CTA per SM walks the units u = blockIdx.x, blockIdx.x + gridDim.x, ...
+// with the K/V ring, the Q buffers (two at d = 64) and every barrier phase
+// running on across units, so the next unit's Q load and first score
+// products overlap the current unit's last tiles and its epilogue.  Roles:
 //
-//   warp 8      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into
-//               a ring of 128 x d bf16 slots (128-byte swizzle).
+//   warp 8      TMA producer: per unit its Q tiles, then K_0, V_0, K_1, V_1,
+//               ... into a ring of 128 x d bf16 slots (128-byte swizzle).
 //   warps 9-10  MMA issuers, one thread per query tile (A: warp 9, B: warp
 //               10): S_X = Q_X K_j^T into TMEM and O_X += P_X V_j.  Two
 //               issuers keep the tensor pipe fed while either one waits on a
@@ -54,8 +58,11 @@ struct FwdCfg {
   static constexpr int kQTileBytes = kTileM * D * 2;
   static constexpr int kSlotBytes = kTileN * D * 2;
   static constexpr int kSlots = (D == 64) ? 8 : 5;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = kOffQ + 2 * kQTileBytes;
+  // Q buffers (two query tiles each): two at d = 64, so the next unit's Q
+  // loads while the current unit runs.
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;
+  static constexpr int kOffQ = 0;  // + buf * 2 * kQTileBytes + x * kQTileBytes
+  static constexpr int kOffRing = kOffQ + kQBufs * 2 * kQTileBytes;
   static constexpr int kTileBytes = kOffRing + kSlots * kSlotBytes;
   static constexpr int kDynSmem = kTileBytes + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -73,7 +80,7 @@ struct FwdCfg {
 struct FwdBars {
   uint64_t full[8];
   uint64_t empty[8];  // kSlots <= 8
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -88,39 +95,58 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
+// Units: u -> (bh = u / npairs, query rows q0 = (u % npairs) * 256 ..
+// q0 + 255 as tiles A and B); CTA c takes u = c, c + gridDim.x, ...  Key
+// tiles, ring slots and every per-tile barrier are counted on across units.
+struct FwdWork {
+  int N;
+  int nkv;     // key tiles per head
+  int npairs;  // 256-row query blocks per head
+  int units;   // BH * npairs
+  __device__ __forceinline__ int bh(int u) const { return u / npairs; }
+  __device__ __forceinline__ int q0(int u) const { return (u % npairs) * 2 * kTileM; }
+  __device__ __forceinline__ bool has_b(int u) const { return q0(u) + kTileM < N; }
+};
+
 template <int D>
 __device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k, const CUtensorMap* map_v,
-                             uint8_t* sm, FwdBars& bars, int bh, int q0, bool hasB, int nkv, uint32_t* dev_err) {
+                             uint8_t* sm, FwdBars& bars, const FwdWork& w, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   tma_prefetch_desc(map_q);
   tma_prefetch_desc(map_k);
   tma_prefetch_desc(map_v);
-  mbar_arrive_expect_tx(&bars.q_full, (hasB ? 2u : 1u) * C::kQTileBytes);
-  for (int x = 0; x < (hasB ? 2 : 1); ++x)
-    for (int blk = 0; blk < D / 64; ++blk)
-      tma_load_3d(sm + C::kOffQ + x * C::kQTileBytes + blk * 16384, map_q, &bars.q_full, blk * 64, q0 + x * 128, bh);
-  const int total = 2 * nkv;
-  int issued = 0;
-  for (; issued < total; ++issued) {
-    const int slot = issued % C::kSlots;
-    if (issued >= C::kSlots) {
-      if (!mbar_wait(&bars.empty[slot], ((issued / C::kSlots) - 1) & 1, &bars.abort, dev_err)) break;
+  volatile int* ab = &bars.abort;
+  const int per_unit = 2 * w.nkv;
+  int issued = 0, q_issued = 0;
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int bh = w.bh(u), q0 = w.q0(u);
+    const bool hasB = w.has_b(u);
+    const int b = ui % C::kQBufs;
+    if (ui >= C::kQBufs && !(ok = mbar_wait(&bars.q_empty[b], ((ui / C::kQBufs) - 1) & 1, ab, dev_err))) break;
+    mbar_arrive_expect_tx(&bars.q_full[b], (hasB ? 2u : 1u) * C::kQTileBytes);
+    for (int x = 0; x < (hasB ? 2 : 1); ++x)
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d(sm + C::kOffQ + (b * 2 + x) * C::kQTileBytes + blk * 16384, map_q, &bars.q_full[b], blk * 64,
+                    q0 + x * 128, bh);
+    ++q_issued;
+    for (int i = 0; i < per_unit; ++i, ++issued) {
+      const int slot = issued % C::kSlots;
+      if (issued >= C::kSlots && !(ok = mbar_wait(&bars.empty[slot], ((issued / C::kSlots) - 1) & 1, ab, dev_err)))
+        break;
+      mbar_arrive_expect_tx(&bars.full[slot], C::kSlotBytes);
+      const CUtensorMap* m = (i & 1) ? map_v : map_k;
+      const int kv0 = (i >> 1) * kTileN;
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_3d(sm + C::kOffRing + slot * C::kSlotBytes + blk * 16384, m, &bars.full[slot], blk * 64, kv0, bh);
     }
-    mbar_arrive_expect_tx(&bars.full[slot], C::kSlotBytes);
-    const CUtensorMap* m = (issued & 1) ? map_v : map_k;
-    const int kv0 = (issued >> 1) * kTileN;
-    for (int blk = 0; blk < D / 64; ++blk)
-      tma_load_3d(sm + C::kOffRing + slot * C::kSlotBytes + blk * 16384, m, &bars.full[slot], blk * 64, kv0, bh);
   }
-  if (issued < total) {
+  if (*ab) {
     // Aborted: let the copies already in flight land before the CTA exits.
-    mbar_wait_drain(&bars.q_full, 0);
-    for (int s = 0; s < C::kSlots; ++s) {
-      int last = -1;
-      for (int i = issued - 1; i >= 0 && i >= issued - C::kSlots; --i)
-        if (i % C::kSlots == s) { last = i; break; }
-      if (last >= 0) mbar_wait_drain(&bars.full[s], (last / C::kSlots) & 1);
-    }
+    for (int t = (q_issued > C::kQBufs ? q_issued - C::kQBufs : 0); t < q_issued; ++t)
+      mbar_wait_drain(&bars.q_full[t % C::kQBufs], (t / C::kQBufs) & 1);
+    for (int t = (issued > C::kSlots ? issued - C::kSlots : 0); t < issued; ++t)
+      mbar_wait_drain(&bars.full[t % C::kSlots], (t / C::kSlots) & 1);
   }
 }
 
@@ -148,12 +174,13 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
   }
 }
 
-// MMA issue for one query tile x.  Both issuers read the same K/V slots; a
-// slot's empty barrier counts one commit per issuer.
+// MMA issue for query tile slot x (A: x = 0, B: x = 1).  Both issuers read
+// the same K/V slots; a slot's empty barrier and a Q buffer's empty barrier
+// count one commit per issuer, so the B issuer walks and releases them also
+// for units whose tile B has no rows.
 template <int D>
-__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int nkv, uint32_t* dev_err) {
+__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const FwdWork& w, uint32_t* dev_err) {
   using C = FwdCfg<D>;
-  const uint64_t q_desc = sdesc_sw128(smem_u32(sm + C::kOffQ + x * C::kQTileBytes), 16, 1024);
   const uint32_t ring = smem_u32(sm + C::kOffRing);
   const uint32_t tS = tmem + C::kColS + x * 128;
   const uint32_t tO = tmem + C::kColO + x * D;
@@ -163,47 +190,70 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int nk
   auto k_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16, 1024); };
   auto v_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16384, 1024); };
   volatile int* ab = &bars.abort;
-  bool ok = mbar_wait(&bars.q_full, 0, ab, dev_err);
-  if (ok) ok = mbar_wait(&bars.full[slot_of(0)], phase_of(0), ab, dev_err);
-  if (ok) {
-    tc_fence_after();
-    issue_qk<D>(tS, q_desc, k_desc(0));
-    umma_commit(&bars.s_full[x]);
-    umma_commit(&bars.empty[slot_of(0)]);
-  }
-  for (int j = 0; ok && j < nkv; ++j) {
-    const int iv = 2 * j + 1, ik = 2 * j + 2;
-    const bool more = j + 1 < nkv;
-    if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), ab, dev_err))) break;
-    if (more && !(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), ab, dev_err))) break;
-    if (C::kSepP) {
-      // S_X(j+1) as soon as the softmax holds S_X(j) in registers, so it is
-      // computed during this tile's exponentials; then PV_X(j) from the
-      // separate P columns once P_X(j) is written.
-      if (more) {
-        if (!(ok = mbar_wait(&bars.s_free[x], j & 1, ab, dev_err))) break;
-        tc_fence_after();
-        issue_qk<D>(tS, q_desc, k_desc(ik));
-        umma_commit(&bars.s_full[x]);
+  const int nkv = w.nkv;
+  int jx = 0;  // key tiles this issuer has processed (its barrier phases)
+  bool ok = true;
+  for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int b = ui % C::kQBufs;
+    const int g0 = ui * 2 * nkv;  // first ring item of the unit
+    if (x == 1 && !w.has_b(u)) {
+      // No tile B in this unit: only release the unit's slots and Q buffer.
+      for (int i = 0; ok && i < 2 * nkv; ++i) {
+        if (!(ok = mbar_wait(&bars.full[slot_of(g0 + i)], phase_of(g0 + i), ab, dev_err))) break;
+        umma_commit(&bars.empty[slot_of(g0 + i)]);
       }
-      if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
-      tc_fence_after();
-      issue_pv<D>(tO, tP, v_desc(iv), j > 0);
-      umma_commit(&bars.pv_done[x]);
-    } else {
-      // P lives in the S columns: PV_X(j) must be issued before S_X(j+1).
-      if (!(ok = mbar_wait(&bars.p_full[x], j & 1, ab, dev_err))) break;
-      tc_fence_after();
-      issue_pv<D>(tO, tP, v_desc(iv), j > 0);
-      umma_commit(&bars.pv_done[x]);
-      if (more) {
-        issue_qk<D>(tS, q_desc, k_desc(ik));
-        umma_commit(&bars.s_full[x]);
-      }
+      if (ok) umma_commit(&bars.q_empty[b]);
+      continue;
     }
-    if (j == nkv - 1) umma_commit(&bars.o_done[x]);
-    umma_commit(&bars.empty[slot_of(iv)]);
-    if (more) umma_commit(&bars.empty[slot_of(ik)]);
+    const uint64_t q_desc = sdesc_sw128(smem_u32(sm + C::kOffQ + (b * 2 + x) * C::kQTileBytes), 16, 1024);
+    if (!(ok = mbar_wait(&bars.q_full[b], (ui / C::kQBufs) & 1, ab, dev_err))) break;
+    if (!(ok = mbar_wait(&bars.full[slot_of(g0)], phase_of(g0), ab, dev_err))) break;
+    // S_X of the unit's first key tile once the softmax holds the previous
+    // tile's scores (d = 128: P over S was read by the PV issued before).
+    if (C::kSepP && jx > 0 && !(ok = mbar_wait(&bars.s_free[x], (jx - 1) & 1, ab, dev_err))) break;
+    tc_fence_after();
+    issue_qk<D>(tS, q_desc, k_desc(g0));
+    umma_commit(&bars.s_full[x]);
+    umma_commit(&bars.empty[slot_of(g0)]);
+    for (int j = 0; ok && j < nkv; ++j) {
+      const int jt = jx + j;
+      const int iv = g0 + 2 * j + 1, ik = g0 + 2 * j + 2;
+      const bool more = j + 1 < nkv;
+      if (!(ok = mbar_wait(&bars.full[slot_of(iv)], phase_of(iv), ab, dev_err))) break;
+      if (more && !(ok = mbar_wait(&bars.full[slot_of(ik)], phase_of(ik), ab, dev_err))) break;
+      if (C::kSepP) {
+        // S_X(j+1) as soon as the softmax holds S_X(j) in registers, so it is
+        // computed during this tile's exponentials; then PV_X(j) from the
+        // separate P columns once P_X(j) is written.
+        if (more) {
+          if (!(ok = mbar_wait(&bars.s_free[x], jt & 1, ab, dev_err))) break;
+          tc_fence_after();
+          issue_qk<D>(tS, q_desc, k_desc(ik));
+          umma_commit(&bars.s_full[x]);
+        }
+        if (!(ok = mbar_wait(&bars.p_full[x], jt & 1, ab, dev_err))) break;
+        tc_fence_after();
+        issue_pv<D>(tO, tP, v_desc(iv), j > 0);
+        umma_commit(&bars.pv_done[x]);
+      } else {
+        // P lives in the S columns: PV_X(j) must be issued before S_X(j+1).
+        if (!(ok = mbar_wait(&bars.p_full[x], jt & 1, ab, dev_err))) break;
+        tc_fence_after();
+        issue_pv<D>(tO, tP, v_desc(iv), j > 0);
+        umma_commit(&bars.pv_done[x]);
+        if (more) {
+          issue_qk<D>(tS, q_desc, k_desc(ik));
+          umma_commit(&bars.s_full[x]);
+        }
+      }
+      if (j == nkv - 1) {
+        umma_commit(&bars.o_done[x]);
+        umma_commit(&bars.q_empty[b]);
+      }
+      umma_commit(&bars.empty[slot_of(iv)]);
+      if (more) umma_commit(&bars.empty[slot_of(ik)]);
+    }
+    jx += nkv;
   }
   // Every MMA this thread issued has completed once this barrier flips.
   umma_commit(&bars.drain[x]);
@@ -212,25 +262,30 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int nk
 
 // Softmax / epilogue of one 128-row query tile (x = 0: tile A, 1: tile B).
 template <int D>
-__device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, int bh, int q0, int N, int nkv,
-                            float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                            uint32_t* dev_err) {
+__device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const FwdWork& w, float scale_log2,
+                            __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
   const int row = wq * 32 + lane;
-  const int n = q0 + x * 128 + row;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_base + C::kColS + x * 128;
   const uint32_t tO = tmem + lane_base + C::kColO + x * D;
   const uint32_t tP = tmem + lane_base + C::kColP + x * C::kPStride;
   volatile int* ab = &bars.abort;
-
+  const int N = w.N, nkv = w.nkv;
+  int jx = 0;       // key tiles processed by this query-tile slot (barrier phases)
+  uint32_t uc = 0;  // units processed by this slot (o_done phases)
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < w.units; u += gridDim.x) {
+  if (x == 1 && !w.has_b(u)) continue;
+  const int bh = w.bh(u);
+  const int n = w.q0(u) + x * 128 + row;
   float m_ref = -INFINITY;
   float l = 0.f;
-  bool ok = true;
   for (int j = 0; j < nkv; ++j) {
-    ok = mbar_wait(&bars.s_full[x], j & 1, ab, dev_err);
+    const int jt = jx + j;
+    ok = mbar_wait(&bars.s_full[x], jt & 1, ab, dev_err);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     tc_fence_after();
@@ -265,9 +320,9 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
     const bool need = (m_new != m_ref) && (j > 0);
     const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-    if (C::kSepP && j > 0) {
-      // PV(j-1) must be done with O (rescale below) and with the P columns.
-      ok = mbar_wait(&bars.pv_done[x], (j - 1) & 1, ab, dev_err);
+    if (C::kSepP && jt > 0) {
+      // PV(jt-1) must be done with O (rescale below) and with the P columns.
+      ok = mbar_wait(&bars.pv_done[x], (jt - 1) & 1, ab, dev_err);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -329,7 +384,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     mbar_arrive(&bars.p_full[x]);
   }
   if (!ok) return;
-  ok = mbar_wait(&bars.o_done[x], 0, ab, dev_err);
+  ok = mbar_wait(&bars.o_done[x], uc & 1, ab, dev_err);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return;
   tc_fence_after();
@@ -354,30 +409,32 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, in
     }
   }
   if (live) lse[static_cast<size_t>(bh) * N + n] = (m_ref + log2f(l)) * kLn2;
+  jx += nkv;
+  ++uc;
+  }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, int N, float scale_log2,
+                    const __grid_constant__ CUtensorMap map_v, const FwdWork w, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdBars bars;
   uint8_t* sm = align1024(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * 2 * kTileM;
-  const bool hasB = q0 + kTileM < N;
-  const int nkv = (N + kTileN - 1) / kTileN;
   griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars.full[i], 1);
-      mbar_init(&bars.empty[i], hasB ? 2 : 1);  // one commit per MMA issuer
+      mbar_init(&bars.empty[i], 2);  // one commit per MMA issuer
     }
-    mbar_init(&bars.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.q_full[b], 1);
+      mbar_init(&bars.q_empty[b], 2);
+    }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.s_full[x], 1);
       mbar_init(&bars.p_full[x], 128);
@@ -400,13 +457,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == 8) {
-    if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, bh, q0, hasB, nkv, dev_err);
+    if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, w, dev_err);
   } else if (warp >= 9) {
-    const int x = warp - 9;
-    if (lane == 0 && (x == 0 || hasB)) fwd_mma<D>(sm, bars, tmem, x, nkv, dev_err);
+    if (lane == 0) fwd_mma<D>(sm, bars, tmem, warp - 9, w, dev_err);
   } else {
-    const int x = warp >> 2;
-    if (x == 0 || hasB) fwd_softmax<D>(sm, bars, tmem, x, bh, q0, N, nkv, scale_log2, out, lse, dev_err);
+    fwd_softmax<D>(sm, bars, tmem, warp >> 2, w, scale_log2, out, lse, dev_err);
   }
   tc_fence_before();
   __syncthreads();
@@ -423,9 +478,15 @@ cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   static_assert(C::kDynSmem + static_cast<int>(sizeof(FwdBars)) <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((s.N + 2 * kTileM - 1) / (2 * kTileM), s.BH);
+  FwdWork w;
+  w.N = s.N;
+  w.nkv = (s.N + kTileN - 1) / kTileN;
+  w.npairs = (s.N + 2 * kTileM - 1) / (2 * kTileM);
+  w.units = s.BH * w.npairs;
+  const int sms = device_sm_count();
+  const int grid = w.units < sms ? w.units : sms;
   const float scale_log2 = s.scale * 1.4426950408889634f;
-  return launch_pdl(attn_fwd_kernel<D>, grid, dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, s.N, scale_log2,
+  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, w, scale_log2,
                     reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
 }
 
