@@ -519,14 +519,16 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 #pragma unroll
           for (int e = 0; e < 32; e += 2) pp[(c * 32 + e) / 2] = 0u;
         }
-        if (C::kSplitIssuers && c == 0 && t > 0) {
-          // dV(t-1) must be done reading P^T(t-1) before it is overwritten.
-          ok = mbar_wait(&bars.dv_done, (t - 1) & 1, ab, dev_err);
-          if (!__all_sync(0xffffffffu, ok)) return;
-          tc_fence_after();
-        }
-        tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
       }
+      if (C::kSplitIssuers && t > 0) {
+        // dV(t-1) must be done reading P^T(t-1) before it is overwritten;
+        // waited for after all the exponentials, so that they overlap dV(t-1).
+        ok = mbar_wait(&bars.dv_done, (t - 1) & 1, ab, dev_err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[c * 16]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars.p_ready);

@@ -320,13 +320,6 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
     const float m_new = (m_tile > m_ref + kRescaleThreshold) ? m_tile : m_ref;
     const bool need = (m_new != m_ref) && (j > 0);
     const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-    if (C::kSepP && jt > 0) {
-      // PV(jt-1) must be done with O (rescale below) and with the P columns.
-      ok = mbar_wait(&bars.pv_done[x], (jt - 1) & 1, ab, dev_err);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-    }
     l *= alpha;
     m_ref = m_new;
     const float neg_m = -m_ref;
@@ -341,9 +334,12 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
     const uint64_t negm2 = f2_make(neg_m, neg_m);
     uint64_t l2[8];  // partial row sums: two per 32-column chunk
     const bool full_tile = nvalid >= kTileN;
+    // The whole packed P row is formed in registers before the P columns
+    // are touched, so the wait for PV(j-1) to release them comes after the
+    // exponentials instead of stalling ahead of them.
+    uint32_t packed[4][16];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t packed[16];
       l2[2 * c] = f2_make(0.f, 0.f);
       l2[2 * c + 1] = f2_make(0.f, 0.f);
 #pragma unroll
@@ -355,10 +351,18 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
         const float p0 = poly ? exp2_poly(x0) : ex2_approx(x0);
         const float p1 = poly ? exp2_poly(x1) : ex2_approx(x1);
         l2[2 * c + (h & 1)] = f2_add(l2[2 * c + (h & 1)], f2_make(p0, p1));
-        packed[h] = pack_bf16x2(p0, p1);
+        packed[c][h] = pack_bf16x2(p0, p1);
       }
-      tmem_st16(tP + c * 16, packed);
     }
+    if (C::kSepP && jt > 0) {
+      // PV(jt-1) must be done with the P columns and with O (rescale below).
+      ok = mbar_wait(&bars.pv_done[x], (jt - 1) & 1, ab, dev_err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, packed[c]);
     {
       float la, lb;
       f2_split(f2_add(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])),

@@ -45,7 +45,106 @@ __device__ __forceinline__ float row_sum(float v) {
   return v;
 }
 
-// Normalises one 8-element chunk of a row; returns r through *r_out.
+// --- correctly rounded x_hat ------------------------------------------------
+// x_hat is the bf16 value nearest to the exact real g x r.  The fp32 value
+// y = (g x) r computed with the fp32 sum of squares and rsqrtf is within 12
+// fp32 units in the last place of the exact product: the sum takes at most 11
+// roundings of nonnegative terms (15 at d = 128: 7 within a thread, log2(TPR)
+// across lanes; the squares of bf16 values are exact), the mean and eps add
+// one, rsqrtf is good to 2 ulp and halves the relative error of its argument,
+// and the two products add one each.  Rounding y to bf16 is therefore exact
+// unless y lies within kTieUlps of a bf16 midpoint (low 16 bits 0x8000).
+// Those elements are rounded from a double-float r accurate to about 2^-44:
+// the row's sum of squares by error-free additions, one Newton step from
+// rsqrtf, and an error-free product, with the remainder's sign breaking the
+// midpoint.  A warp takes that path when any of its lanes has such an
+// element (about one element in a thousand).
+constexpr uint32_t kTieUlps = 32;
+constexpr float kEpsLo = static_cast<float>(1e-6 - static_cast<double>(1e-6f));
+
+// Knuth's TwoSum and Dekker's Fast2Sum (|a| >= |b|), with the _rn intrinsics
+// so that nothing is contracted or reassociated.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+struct F8 {
+  float v[8];
+};
+
+// (rh, rl) = (mean of the row's squares + eps)^(-1/2) as a double-float.
+// Every lane of the warp calls it (row reduction by shuffles).
+template <int TPR>
+__device__ __forceinline__ void rsqrt_mean_sq_df(const float (&x)[8], float& rh, float& rl) {
+  float s = 0.f, c = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float t, e;
+    two_sum(s, __fmul_rn(x[i], x[i]), t, e);
+    s = t;
+    c = __fadd_rn(c, e);
+  }
+#pragma unroll
+  for (int o = TPR / 2; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    float t, e;
+    two_sum(s, s2, t, e);
+    fast_two_sum(t, __fadd_rn(__fadd_rn(c, c2), e), s, c);
+  }
+  constexpr float inv_d = 1.f / (TPR * 8);  // a power of two: exact scaling
+  float mh, ml, e1;
+  two_sum(__fmul_rn(s, inv_d), kEps, mh, e1);
+  fast_two_sum(mh, __fadd_rn(__fadd_rn(__fmul_rn(c, inv_d), kEpsLo), e1), mh, ml);
+  // r = r0 (1 - t)^(-1/2) with 1 - t = m r0^2, t of order 2^-22.
+  const float r0 = rsqrtf(mh);
+  const float ph = __fmul_rn(r0, r0), pl = __fmaf_rn(r0, r0, -ph);
+  const float qh = __fmul_rn(mh, ph);
+  const float ql = __fmaf_rn(ml, ph, __fmaf_rn(mh, pl, __fmaf_rn(mh, ph, -qh)));
+  const float t = __fsub_rn(__fsub_rn(1.f, qh), ql);
+  fast_two_sum(r0, __fmul_rn(r0, __fmul_rn(t, __fmaf_rn(0.375f, t, 0.5f))), rh, rl);
+}
+
+// A float whose round-to-nearest-even bf16 conversion is the bf16 value
+// nearest to g x (rh + rl).
+__device__ __forceinline__ float round_bf16_df(float g, float x, float rh, float rl) {
+  const float yh = __fmul_rn(g, x), yl = __fmaf_rn(g, x, -yh);
+  float zh = __fmul_rn(yh, rh);
+  float zl = __fmaf_rn(yl, rh, __fmaf_rn(yh, rl, __fmaf_rn(yh, rh, -zh)));
+  fast_two_sum(zh, zl, zh, zl);
+  const uint32_t b = __float_as_uint(zh);
+  if ((b & 0xFFFFu) == 0x8000u && zl != 0.f) {
+    const bool up = (zl > 0.f) == (zh > 0.f);  // away from zero
+    return __uint_as_float((b & 0xFFFF0000u) + (up ? 0x10000u : 0u));
+  }
+  return zh;  // not a midpoint, or an exact one (ties to even)
+}
+
+__device__ __forceinline__ bool near_bf16_midpoint(float y) {
+  return ((__float_as_uint(y) - (0x8000u - kTieUlps)) & 0xFFFFu) <= 2u * kTieUlps;
+}
+
+// The rare path, kept out of line so that the streaming loops keep their
+// registers: re-rounds the near-midpoint elements of y (all lanes call it).
+template <int TPR>
+__device__ __noinline__ F8 rerround_near_midpoints(const uint4 w, const F8 g, F8 y) {
+  float x[8];
+  unpack8(w, x);
+  float rh, rl;
+  rsqrt_mean_sq_df<TPR>(x, rh, rl);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (near_bf16_midpoint(y.v[i])) y.v[i] = round_bf16_df(g.v[i], x[i], rh, rl);
+  return y;
+}
+
+// Normalises one 8-element chunk of a row; returns r through *r_out.  All
+// lanes of the warp call it together (row shuffles).
 template <int TPR>
 __device__ __forceinline__ uint4 norm_chunk(const uint4 w, const float (&g)[8], float* r_out) {
   float x[8];
@@ -55,11 +154,21 @@ __device__ __forceinline__ uint4 norm_chunk(const uint4 w, const float (&g)[8], 
   for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
   ss = row_sum<TPR>(ss);
   const float r = rsqrtf(ss * (1.f / (TPR * 8)) + kEps);
-  float y[8];
+  F8 y;
+  bool near = false;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = g[i] * x[i] * r;
+  for (int i = 0; i < 8; ++i) {
+    y.v[i] = g[i] * x[i] * r;
+    near |= near_bf16_midpoint(y.v[i]);
+  }
+  if (__any_sync(0xffffffffu, near)) {
+    F8 gg;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) gg.v[i] = g[i];
+    y = rerround_near_midpoints<TPR>(w, gg, y);
+  }
   *r_out = r;
-  return pack8(y);
+  return pack8(y.v);
 }
 
 // q, k -> q_hat, k_hat (bf16).  Rows [0, rows) are q rows, [rows, 2 rows) k rows.

@@ -249,3 +249,48 @@ def test_cfg_sampling_workload(ja):
                                               inp.v[b:b + 1, h:h + 1], inp.gq, inp.gk)
             check_fwd({"O": got["O"][b, h], "LSE": got["LSE"][b, h]}, {"O": o[0, 0], "LSE": l[0, 0]},
                       f"cfg step {step} head {(b, h)}")
+
+
+# ---------------------------------------------------------------------------
+# Work-distribution edge cases of the persistent kernels: fewer units than
+# SMs with long per-unit loops; many one-tile units, so every unit boundary
+# is also a tile boundary (Q buffer hand-off, ring wrap, epilogue hand-off);
+# unit counts just above one and two waves of 152 CTAs.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,N,n_txt", [
+    (1, 1, 4000, 333),    # one head: 16 forward units of 250 key tiles, 32 backward units
+    (64, 12, 24, 7),      # 768 heads of one ragged tile each
+    (8, 20, 129, 77),     # 160 heads of two tiles (one of them a single row)
+    (4, 39, 256, 100),    # 156 heads of exactly two full tiles
+])
+def test_unit_scheduling(ja, B, H, N, n_txt, d):
+    inp = make_inputs(B, H, N, d, seed=7000 + B * H + N + d)
+    got = run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, n_txt)
+    ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    where = f"B={B} H={H} N={N} d={d}"
+    check_fwd(got, ref, where)
+    check_bwd(got, ref, where=where)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_q_hat_k_hat_rounding_at_bf16_midpoints(ja, d):
+    """Rows of equal values +-8 with gains on bf16 midpoints (1 + 3 * 2^-8)
+    put g x r a relative 8e-9 below a midpoint; fp32 arithmetic lands on the
+    midpoint itself and ties to even, the other way.  The kernels must round
+    the exact product, as the oracle does: a wrong q_hat / k_hat shifts these
+    rows' scores by 0.8 % and their LSE far beyond 1e-3."""
+    B, H, N, n_txt = 1, 2, 300, 44
+    inp = make_inputs(B, H, N, d, seed=91 + d)
+    q, k = inp.q.copy(), inp.k.copy()
+    rows = np.arange(0, N, 7)
+    q[:, :, rows, :] = 8.0
+    k[:, :, rows[::2], :] = -8.0
+    gq = inp.gq.copy()
+    gk = inp.gk.copy()
+    gq[::2] = 1.0 + 3 * 2.0 ** -8
+    gk[1::2] = 1.0 + 3 * 2.0 ** -8
+    got = run_gpu(ja, q, k, inp.v, gq, gk, inp.dout, n_txt)
+    ref = oracle.joint_attention_bwd(q, k, inp.v, gq, gk, inp.dout)
+    check_fwd(got, ref, "midpoints")
+    check_bwd(got, ref, where="midpoints")

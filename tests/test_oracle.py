@@ -66,6 +66,28 @@ def test_round_to_bf16_single_rounding_from_float64():
     np.testing.assert_array_equal(got, [1.0 + 2.0 ** -7, 1.0, 1.0 + 2.0 ** -6])
 
 
+def test_q_hat_rounds_the_exact_product_at_a_bf16_midpoint():
+    """A row of equal values 8 gives r = (64 + eps)^(-1/2), just below 1/8, so
+    g x r = g (1 - eps/128 + ...).  With g the midpoint 1 + 3 * 2^-8 between
+    the bf16 values 1 + 2^-7 and 1 + 2^-6 the exact product lies below the
+    midpoint and must round down; with g one float32 step above it, up.  An
+    fp32 r rounds to exactly 1/8 here and would put the product on the
+    midpoint itself, where ties-to-even rounds up (1 + 2^-6 is the even one)."""
+    d = 64
+    x = np.full((1, 1, 1, d), 8.0)
+    mid = 1.0 + 3 * 2.0 ** -8
+    above = float(np.nextafter(np.float32(mid), np.float32(2.0)))
+    for g, want in ((mid, 1.0 + 2.0 ** -7), (above, 1.0 + 2.0 ** -6), (-mid, None)):
+        gv = np.full(d, g)
+        xh, r = jo.rmsnorm_fwd(x, gv)
+        assert r[0, 0, 0, 0] < 0.125
+        got = jo.round_to_bf16(xh)
+        if want is None:  # negative gain: the mirror image
+            np.testing.assert_array_equal(got, -(1.0 + 2.0 ** -7))
+        else:
+            np.testing.assert_array_equal(got, want)
+
+
 # ---------------------------------------------------------------------------
 # Finite differences (no bf16 step, float64)
 # ---------------------------------------------------------------------------
