@@ -261,7 +261,7 @@ extern "C" int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const
   cudaError_t ce;
   {
     Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
-    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, st);
+    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, err, st);
   }
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "qk_norm_fwd launch", ce);
   CUtensorMap mq, mk, mv;
@@ -306,7 +306,7 @@ extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   CUtensorMap mq, mk, mv;
   {
     Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
-    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, st);
+    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, err, st);
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "qk_norm_fwd launch", ce);
@@ -352,7 +352,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   uint32_t* err = dev_err_ptr();
   if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
   AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
-  const int nparts_q = q_norm_bwd_parts();
+  const int nparts_q = q_norm_bwd_parts(s.d);
   const int nparts_k = attn_bwd_dgk_parts(as);
   Carve cv;
   cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k), st);
@@ -374,7 +374,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
     ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_tickets, s.BH, s.N,
-                         s.n_pad, s.d, st);
+                         s.n_pad, s.d, err, st);
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
@@ -391,7 +391,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
       stage = "q_norm_bwd launch";
       Timed t(JATTN_KERNEL_Q_NORM_BWD, st);
       ce = launch_q_norm_bwd(dqacc, q, rq, gq, as.scale, dq, dgq_part, nparts_q, static_cast<int64_t>(s.rows), s.d,
-                             st);
+                             err, st);
     }
     if (ce == cudaSuccess) {
       stage = "dg_reduce launch";

@@ -46,16 +46,22 @@ struct Scratch {
 };
 
 // --- norm / elementwise kernels (HBM-bound) ---------------------------------
+// The streaming norm kernels take the per-launch device error word: their
+// bounded waits on the bulk-copy ring report a timeout through it.
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
-                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, cudaStream_t st);
+                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, uint32_t* dev_err,
+                               cudaStream_t st);
 // Rows are (bh, n) with n < N; nlse2 (= -LSE log2 e) and delta are written
 // for n < n_pad (= N rounded up to 128), with -inf / 0 in the pad rows.
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
-                            unsigned int* tickets, int BH, int N, int n_pad, int d, cudaStream_t st);
+                            unsigned int* tickets, int BH, int N, int n_pad, int d, uint32_t* dev_err,
+                            cudaStream_t st);
+// nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq partials.
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
-                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, cudaStream_t st);
+                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, uint32_t* dev_err,
+                              cudaStream_t st);
 // Gain-gradient reduction: slice_part holds dg_reduce_scratch_floats(d)
 // floats, tickets dg_reduce_tickets(d) counters that the backward
 // preparation kernel zeroes.
@@ -63,7 +69,7 @@ cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, i
                              unsigned int* tickets, float* dgq, float* dgk, cudaStream_t st);
 int dg_reduce_scratch_floats(int d);
 int dg_reduce_tickets(int d);
-int q_norm_bwd_parts();
+int q_norm_bwd_parts(int d);
 // Streaming multiprocessors of the current device (cached after the first call).
 int device_sm_count();
 

@@ -9,7 +9,9 @@
 // Row layout: every row is d contiguous values, d/8 threads per row, each
 // thread holding one 16-byte chunk (8 bf16) so global accesses are fully
 // coalesced 16-byte vectors; the row reduction is a shuffle within the
-// d/8-lane group.  Grids are a multiple of the SM count and stride over rows.
+// d/8-lane group.  The streaming kernels hold no shared memory and meet no
+// block barrier: every thread loads its next rows while it transforms the
+// current ones (register double buffering), and grids fill every SM.
 #include <cuda_bf16.h>
 
 #include "jattn_internal.h"
@@ -19,7 +21,6 @@ namespace jattn {
 namespace {
 
 constexpr float kEps = 1e-6f;
-constexpr int kNormThreads = 256;
 constexpr int kDgSlices = 16;
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
@@ -48,18 +49,19 @@ __device__ __forceinline__ float row_sum(float v) {
 // --- correctly rounded x_hat ------------------------------------------------
 // x_hat is the bf16 value nearest to the exact real g x r.  The fp32 value
 // y = (g x) r computed with the fp32 sum of squares and rsqrtf is within 12
-// fp32 units in the last place of the exact product: the sum takes at most 11
-// roundings of nonnegative terms (15 at d = 128: 7 within a thread, log2(TPR)
-// across lanes; the squares of bf16 values are exact), the mean and eps add
-// one, rsqrtf is good to 2 ulp and halves the relative error of its argument,
-// and the two products add one each.  Rounding y to bf16 is therefore exact
-// unless y lies within kTieUlps of a bf16 midpoint (low 16 bits 0x8000).
-// Those elements are rounded from a double-float r accurate to about 2^-44:
-// the row's sum of squares by error-free additions, one Newton step from
-// rsqrtf, and an error-free product, with the remainder's sign breaking the
-// midpoint.  A warp takes that path when any of its lanes has such an
-// element (about one element in a thousand).
-constexpr uint32_t kTieUlps = 32;
+// fp32 units in the last place of the exact product: the sum takes at most 8
+// roundings of nonnegative terms (3 per packed accumulator, 1 to join them,
+// log2(d/8) across lanes; the squares of bf16 values are exact), the mean and
+// eps add one, rsqrtf is good to 2 ulp and halves the relative error of its
+// argument, and the two products add one each.  Rounding y to bf16 is
+// therefore exact unless y lies within 32 fp32 ulps of a bf16 midpoint (low
+// 16 bits 0x8000): the window test takes the 64 values 0x8000 - 32 ..
+// 0x8000 + 31.  Those elements are rounded from a double-float r accurate to
+// about 2^-44: the row's sum of squares by error-free additions, one Newton
+// step from rsqrtf, and an error-free product, with the remainder's sign
+// breaking the midpoint.  A warp takes that path when any of its lanes has
+// such an element (about one element in a thousand).
+constexpr uint32_t kTieWindow = 64;
 constexpr float kEpsLo = static_cast<float>(1e-6 - static_cast<double>(1e-6f));
 
 // Knuth's TwoSum and Dekker's Fast2Sum (|a| >= |b|), with the _rn intrinsics
@@ -126,7 +128,7 @@ __device__ __forceinline__ float round_bf16_df(float g, float x, float rh, float
 }
 
 __device__ __forceinline__ bool near_bf16_midpoint(float y) {
-  return ((__float_as_uint(y) - (0x8000u - kTieUlps)) & 0xFFFFu) <= 2u * kTieUlps;
+  return ((__float_as_uint(y) + (kTieWindow / 2 - 0x8000u)) & (0xFFFFu & ~(kTieWindow - 1))) == 0u;
 }
 
 // The rare path, kept out of line so that the streaming loops keep their
@@ -149,17 +151,20 @@ template <int TPR>
 __device__ __forceinline__ uint4 norm_chunk(const uint4 w, const float (&g)[8], float* r_out) {
   float x[8];
   unpack8(w, x);
-  float ss = 0.f;
+  uint64_t s2 = f2_mul(f2_make(x[0], x[1]), f2_make(x[0], x[1]));
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-  ss = row_sum<TPR>(ss);
+  for (int i = 2; i < 8; i += 2) s2 = f2_fma(f2_make(x[i], x[i + 1]), f2_make(x[i], x[i + 1]), s2);
+  float sa, sb;
+  f2_split(s2, sa, sb);
+  const float ss = row_sum<TPR>(sa + sb);
   const float r = rsqrtf(ss * (1.f / (TPR * 8)) + kEps);
+  const uint64_t r2 = f2_make(r, r);
   F8 y;
   bool near = false;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    y.v[i] = g[i] * x[i] * r;
-    near |= near_bf16_midpoint(y.v[i]);
+  for (int i = 0; i < 8; i += 2) {
+    f2_split(f2_mul(f2_mul(f2_make(g[i], g[i + 1]), f2_make(x[i], x[i + 1])), r2), y.v[i], y.v[i + 1]);
+    near |= near_bf16_midpoint(y.v[i]) | near_bf16_midpoint(y.v[i + 1]);
   }
   if (__any_sync(0xffffffffu, near)) {
     F8 gg;
@@ -171,7 +176,12 @@ __device__ __forceinline__ uint4 norm_chunk(const uint4 w, const float (&g)[8], 
   return pack8(y.v);
 }
 
-// q, k -> q_hat, k_hat (bf16).  Rows [0, rows) are q rows, [rows, 2 rows) k rows.
+// --- streaming kernels -------------------------------------------------------
+constexpr int kNormThreads = 256;
+
+// q, k -> q_hat, k_hat (bf16).  Rows [0, rows) are q rows, [rows, 2 rows) k
+// rows; each thread takes kU rows per pass and loads the next pass's rows
+// before it transforms the current ones.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* __restrict__ q,
                                                                    const uint4* __restrict__ k,
@@ -180,7 +190,8 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
                                                                    uint4* __restrict__ qhat,
                                                                    uint4* __restrict__ khat, int64_t rows) {
   constexpr int TPR = D / 8;
-  constexpr int RPB = kNormThreads / TPR;  // rows per block per iteration
+  constexpr int RPB = kNormThreads / TPR;  // rows per block and pass slot
+  constexpr int kU = 2;
   const int sub = threadIdx.x % TPR;
   griddep_launch_dependents();
   griddep_wait();
@@ -191,29 +202,30 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
     g_k[i] = gk[sub * 8 + i];
   }
   const int64_t total = 2 * rows;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * RPB;
-  constexpr int U = 4;  // rows in flight per thread
-  // The loop bound is block-uniform so every lane reaches the row shuffles.
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < total; base += U * step) {
-    uint4 w[U];
-    int64_t idx[U];
-    bool valid[U], is_k[U];
+  const int64_t span = static_cast<int64_t>(RPB) * kU;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * span;
+  auto load = [&](int64_t b, uint4 (&w)[kU]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t rr = base + u * step + threadIdx.x / TPR;
-      valid[u] = rr < total;
-      is_k[u] = rr >= rows;
-      idx[u] = (is_k[u] ? rr - rows : rr) * TPR + sub;
-      w[u] = valid[u] ? (is_k[u] ? k[idx[u]] : q[idx[u]]) : make_uint4(0u, 0u, 0u, 0u);
+    for (int u = 0; u < kU; ++u) {
+      const int64_t rr = b + u * RPB + threadIdx.x / TPR;
+      w[u] = rr < total ? (rr >= rows ? k[(rr - rows) * TPR + sub] : q[rr * TPR + sub]) : make_uint4(0u, 0u, 0u, 0u);
     }
+  };
+  int64_t base = static_cast<int64_t>(blockIdx.x) * span;
+  uint4 cur[kU];
+  load(base, cur);
+  // The loop bound is block-uniform so every lane reaches the row shuffles.
+  for (; base < total; base += step) {
+    uint4 nxt[kU];
+    load(base + step, nxt);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float g[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) g[i] = is_k[u] ? g_k[i] : g_q[i];
+    for (int u = 0; u < kU; ++u) {
+      const int64_t rr = base + u * RPB + threadIdx.x / TPR;
+      const bool is_k = rr >= rows;
       float r;
-      const uint4 y = norm_chunk<TPR>(w[u], g, &r);
-      if (valid[u]) (is_k[u] ? khat : qhat)[idx[u]] = y;
+      const uint4 y = norm_chunk<TPR>(cur[u], is_k ? g_k : g_q, &r);
+      if (rr < total) (is_k ? khat[(rr - rows) * TPR + sub] : qhat[rr * TPR + sub]) = y;
+      cur[u] = nxt[u];
     }
   }
 }
@@ -222,6 +234,7 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
 // for n < N it writes q_hat, k_hat, 1/rms of q and k, D = rowsum(dout * out),
 // minus LSE in the log2 domain and a zeroed fp32 dq accumulator row; pad rows
 // get -LSE = -inf and D = 0 so the attention backward sees zero probabilities.
+// Each thread loads its next row while it transforms the current one.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
@@ -241,49 +254,76 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     g_q[i] = gq[sub * 8 + i];
     g_k[i] = gk[sub * 8 + i];
   }
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < padded_rows;
-       base += static_cast<int64_t>(gridDim.x) * RPB) {
-    const int64_t prow = base + threadIdx.x / TPR;
+  struct Row {
+    uint4 q, k, o, d;
+    float lse;
+  };
+  auto locate = [&](int64_t b, int64_t& prow, int64_t& row, bool& in_range, bool& valid) {
+    prow = b + threadIdx.x / TPR;
     const int64_t bh = prow / n_pad;
     const int n = static_cast<int>(prow - bh * n_pad);
-    const bool in_range = prow < padded_rows;
-    const bool valid = in_range && n < N;
-    const int64_t row = bh * N + n;
+    in_range = prow < padded_rows;
+    valid = in_range && n < N;
+    row = bh * N + n;
+  };
+  auto load = [&](int64_t b, Row& w) {
+    int64_t prow, row;
+    bool in_range, valid;
+    locate(b, prow, row, in_range, valid);
     const int64_t idx = (valid ? row : 0) * TPR + sub;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 wq = valid ? q[idx] : zero, wk = valid ? k[idx] : zero;
-    const uint4 wo = valid ? out[idx] : zero, wd = valid ? dout[idx] : zero;
+    w.q = valid ? q[idx] : zero;
+    w.k = valid ? k[idx] : zero;
+    w.o = valid ? out[idx] : zero;
+    w.d = valid ? dout[idx] : zero;
+    w.lse = (valid && sub == 0) ? lse[row] : 0.f;
+  };
+  const int64_t step = static_cast<int64_t>(gridDim.x) * RPB;
+  int64_t base = static_cast<int64_t>(blockIdx.x) * RPB;
+  Row cur;
+  load(base, cur);
+  for (; base < padded_rows; base += step) {
+    Row nxt;
+    load(base + step, nxt);
+    int64_t prow, row;
+    bool in_range, valid;
+    locate(base, prow, row, in_range, valid);
     float r1, r2;
-    const uint4 yq = norm_chunk<TPR>(wq, g_q, &r1);
-    const uint4 yk = norm_chunk<TPR>(wk, g_k, &r2);
+    const uint4 yq = norm_chunk<TPR>(cur.q, g_q, &r1);
+    const uint4 yk = norm_chunk<TPR>(cur.k, g_k, &r2);
     float o[8], dd[8];
-    unpack8(wo, o);
-    unpack8(wd, dd);
+    unpack8(cur.o, o);
+    unpack8(cur.d, dd);
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) dot = fmaf(o[i], dd[i], dot);
     dot = row_sum<TPR>(dot);
-    if (!in_range) continue;
-    if (sub == 0) {
-      nlse2[prow] = valid ? -lse[row] * 1.4426950408889634f : -INFINITY;
-      delta[prow] = valid ? dot : 0.f;
+    if (in_range) {
+      if (sub == 0) {
+        nlse2[prow] = valid ? -cur.lse * 1.4426950408889634f : -INFINITY;
+        delta[prow] = valid ? dot : 0.f;
+      }
+      if (valid) {
+        const int64_t idx = row * TPR + sub;
+        qhat[idx] = yq;
+        khat[idx] = yk;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        dqacc[idx * 2] = z;
+        dqacc[idx * 2 + 1] = z;
+        if (sub == 0) {
+          rq[row] = r1;
+          rk[row] = r2;
+        }
+      }
     }
-    if (!valid) continue;
-    qhat[idx] = yq;
-    khat[idx] = yk;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    dqacc[idx * 2] = z;
-    dqacc[idx * 2 + 1] = z;
-    if (sub == 0) {
-      rq[row] = r1;
-      rk[row] = r2;
-    }
+    cur = nxt;
   }
 }
 
 // dq from the fp32 accumulator of dS k_hat (times `scale`), plus per-block
 // partial sums of dgq.  Each block writes partial[blockIdx.x][d]; the grid
-// size is fixed, so the reduction order is fixed.
+// size is fixed, so the reduction order is fixed.  Each thread loads its next
+// row while it transforms the current one.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* __restrict__ dqacc,
                                                                   const uint4* __restrict__ q,
@@ -302,46 +342,47 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
     g[i] = gq[sub * 8 + i];
     acc[i] = 0.f;
   }
+  struct Row {
+    float4 a, b;
+    uint4 x;
+    float r;
+  };
+  auto load = [&](int64_t b, Row& w) {
+    const int64_t row = b + threadIdx.x / TPR;
+    const bool valid = row < rows;
+    const int64_t idx = (valid ? row : 0) * TPR + sub;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    w.a = valid ? dqacc[idx * 2] : z4;
+    w.b = valid ? dqacc[idx * 2 + 1] : z4;
+    w.x = valid ? q[idx] : make_uint4(0u, 0u, 0u, 0u);
+    w.r = valid ? rq[row] : 0.f;
+  };
   const int64_t step = static_cast<int64_t>(gridDim.x) * RPB;
-  constexpr int U = 2;  // rows in flight per thread
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < rows; base += U * step) {
-    float4 va[U], vb[U];
-    uint4 vq[U];
-    float vr[U];
-    bool valid[U];
-    int64_t idx[U];
+  int64_t base = static_cast<int64_t>(blockIdx.x) * RPB;
+  Row cur;
+  load(base, cur);
+  for (; base < rows; base += step) {
+    Row nxt;
+    load(base + step, nxt);
+    const int64_t row = base + threadIdx.x / TPR;
+    const float dh[8] = {cur.a.x * scale, cur.a.y * scale, cur.a.z * scale, cur.a.w * scale,
+                         cur.b.x * scale, cur.b.y * scale, cur.b.z * scale, cur.b.w * scale};
+    float x[8];
+    unpack8(cur.x, x);
+    const float r = cur.r;
+    float dot = 0.f;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t row = base + u * step + threadIdx.x / TPR;
-      valid[u] = row < rows;
-      idx[u] = (valid[u] ? row : 0) * TPR + sub;
-      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      va[u] = valid[u] ? dqacc[idx[u] * 2] : z4;
-      vb[u] = valid[u] ? dqacc[idx[u] * 2 + 1] : z4;
-      vq[u] = valid[u] ? q[idx[u]] : make_uint4(0u, 0u, 0u, 0u);
-      vr[u] = valid[u] ? rq[valid[u] ? row : 0] : 0.f;
+    for (int i = 0; i < 8; ++i) dot = fmaf(g[i] * dh[i], x[i], dot);
+    dot = row_sum<TPR>(dot);
+    const float c = r * r * r * (1.f / D) * dot;
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[i] = r * g[i] * dh[i] - c * x[i];
+      acc[i] = fmaf(dh[i], x[i] * r, acc[i]);  // rows past the end are zero
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float4 a = va[u], b = vb[u];
-      const float dh[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
-                           b.x * scale, b.y * scale, b.z * scale, b.w * scale};
-      float x[8];
-      unpack8(vq[u], x);
-      const float r = vr[u];
-      float dot = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dot = fmaf(g[i] * dh[i], x[i], dot);
-      dot = row_sum<TPR>(dot);
-      const float c = r * r * r * (1.f / D) * dot;
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        y[i] = r * g[i] * dh[i] - c * x[i];
-        acc[i] = fmaf(dh[i], x[i] * r, acc[i]);
-      }
-      if (valid[u]) dq[idx[u]] = pack8(y);
-    }
+    if (row < rows) dq[row * TPR + sub] = pack8(y);
+    cur = nxt;
   }
   // Block reduction of acc over the RPB row slots (fixed order).
   __shared__ float red[kNormThreads / TPR][D];
@@ -350,9 +391,9 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
   for (int i = 0; i < 8; ++i) red[slot][sub * 8 + i] = acc[i];
   __syncthreads();
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float s = 0.f;
-    for (int t = 0; t < RPB; ++t) s += red[t][c];
-    partial[static_cast<size_t>(blockIdx.x) * D + c] = s;
+    float t = 0.f;
+    for (int w = 0; w < RPB; ++w) t += red[w][c];
+    partial[static_cast<size_t>(blockIdx.x) * D + c] = t;
   }
 }
 
@@ -419,10 +460,16 @@ int sm_count() {
   return n;
 }
 
-int row_grid(int64_t rows, int d) {
+// As many 256-thread blocks as fit on every SM (from the kernel's
+// registers), no more than the rows need.
+template <class Kernel>
+int row_grid(Kernel kernel, int64_t rows, int d) {
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kNormThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
   const int64_t rpb = kNormThreads / (d / 8);
   const int64_t need = (rows + rpb - 1) / rpb;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
   return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
@@ -430,35 +477,45 @@ int row_grid(int64_t rows, int d) {
 
 int device_sm_count() { return sm_count(); }
 
-int q_norm_bwd_parts() { return sm_count() * 4; }
+int q_norm_bwd_parts(int d) {
+  return d == 128 ? row_grid(q_norm_bwd_kernel<128>, int64_t{1} << 40, 128)
+                  : row_grid(q_norm_bwd_kernel<64>, int64_t{1} << 40, 64);
+}
 
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
-                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, cudaStream_t st) {
-  const int grid = row_grid(2 * rows, d);
+                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, uint32_t* dev_err,
+                               cudaStream_t st) {
+  (void)dev_err;
   auto* a = reinterpret_cast<const uint4*>(q);
   auto* b = reinterpret_cast<const uint4*>(k);
-  return launch_pdl(d == 64 ? qk_norm_fwd_kernel<64> : qk_norm_fwd_kernel<128>, dim3(grid), dim3(kNormThreads), 0,
-                    st, a, b, gq, gk, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rows);
+  auto kernel = d == 64 ? qk_norm_fwd_kernel<64> : qk_norm_fwd_kernel<128>;
+  return launch_pdl(kernel, dim3(row_grid(kernel, 2 * rows, d)), dim3(kNormThreads), 0, st, a, b, gq, gk,
+                    reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rows);
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
-                            unsigned int* tickets, int BH, int N, int n_pad, int d, cudaStream_t st) {
+                            unsigned int* tickets, int BH, int N, int n_pad, int d, uint32_t* dev_err,
+                            cudaStream_t st) {
+  (void)dev_err;
   const int64_t padded_rows = static_cast<int64_t>(BH) * n_pad;
-  const int grid = row_grid(padded_rows, d);
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
-  return launch_pdl(d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>, dim3(grid), dim3(kNormThreads), 0, st,
-                    u4(q), u4(k), gq, gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat),
-                    reinterpret_cast<uint4*>(khat), rq, rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets,
-                    dg_reduce_tickets(d), N, n_pad, padded_rows);
+  auto kernel = d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>;
+  return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
+                    gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
+                    rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets, dg_reduce_tickets(d), N, n_pad,
+                    padded_rows);
 }
 
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
-                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, cudaStream_t st) {
+                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, uint32_t* dev_err,
+                              cudaStream_t st) {
+  (void)dev_err;
   auto* a = reinterpret_cast<const float4*>(dqacc);
   auto* x = reinterpret_cast<const uint4*>(q);
   auto* y = reinterpret_cast<uint4*>(dq);
+  // Every one of the nparts blocks writes its partial (zeros if it has no row).
   return launch_pdl(d == 64 ? q_norm_bwd_kernel<64> : q_norm_bwd_kernel<128>, dim3(nparts), dim3(kNormThreads), 0,
                     st, a, x, rq, gq, scale, y, dgq_part, rows);
 }
