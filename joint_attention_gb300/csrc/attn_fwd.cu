@@ -63,7 +63,11 @@ struct FwdCfg {
   static constexpr int kQBufs = (D == 64) ? 2 : 1;
   static constexpr int kOffQ = 0;  // + buf * 2 * kQTileBytes + x * kQTileBytes
   static constexpr int kOffRing = kOffQ + kQBufs * 2 * kQTileBytes;
-  static constexpr int kTileBytes = kOffRing + kSlots * kSlotBytes;
+  // d = 64: the normalised O tiles are staged (128-byte swizzle) and leave
+  // with one TMA store per query tile; d = 128 has no room and stores rows.
+  static constexpr bool kStageO = (D == 64);
+  static constexpr int kOffStage = kOffRing + kSlots * kSlotBytes;  // + x * kQTileBytes
+  static constexpr int kTileBytes = kOffStage + (kStageO ? 2 * kQTileBytes : 0);
   static constexpr int kDynSmem = kTileBytes + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
@@ -87,6 +91,7 @@ struct FwdBars {
   uint64_t pv_done[2];
   uint64_t s_free[2];  // d = 64: the softmax has the scores in registers
   uint64_t drain[2];
+  uint64_t epi[2];  // d = 64: the query tile's O rows are staged (one arrival per warp)
   uint32_t tmem_base;
   int abort;
 };
@@ -192,6 +197,10 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
   volatile int* ab = &bars.abort;
   const int nkv = w.nkv;
   int jx = 0;  // key tiles this issuer has processed (its barrier phases)
+  // d = 64: the next unit's first score product is issued in place of the
+  // last tile's S(j+1), so that it is ready when the softmax finishes the
+  // unit's epilogue.
+  bool s0_issued = false;
   bool ok = true;
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
     const int b = ui % C::kQBufs;
@@ -206,15 +215,23 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
       continue;
     }
     const uint64_t q_desc = sdesc_sw128(smem_u32(sm + C::kOffQ + (b * 2 + x) * C::kQTileBytes), 16, 1024);
-    if (!(ok = mbar_wait(&bars.q_full[b], (ui / C::kQBufs) & 1, ab, dev_err))) break;
-    if (!(ok = mbar_wait(&bars.full[slot_of(g0)], phase_of(g0), ab, dev_err))) break;
-    // S_X of the unit's first key tile once the softmax holds the previous
-    // tile's scores (d = 128: P over S was read by the PV issued before).
-    if (C::kSepP && jx > 0 && !(ok = mbar_wait(&bars.s_free[x], (jx - 1) & 1, ab, dev_err))) break;
-    tc_fence_after();
-    issue_qk<D>(tS, q_desc, k_desc(g0));
-    umma_commit(&bars.s_full[x]);
-    umma_commit(&bars.empty[slot_of(g0)]);
+    if (!s0_issued) {
+      if (!(ok = mbar_wait(&bars.q_full[b], (ui / C::kQBufs) & 1, ab, dev_err))) break;
+      if (!(ok = mbar_wait(&bars.full[slot_of(g0)], phase_of(g0), ab, dev_err))) break;
+      // S_X of the unit's first key tile once the softmax holds the previous
+      // tile's scores (d = 128: P over S was read by the PV issued before).
+      if (C::kSepP && jx > 0 && !(ok = mbar_wait(&bars.s_free[x], (jx - 1) & 1, ab, dev_err))) break;
+      tc_fence_after();
+      issue_qk<D>(tS, q_desc, k_desc(g0));
+      umma_commit(&bars.s_full[x]);
+      umma_commit(&bars.empty[slot_of(g0)]);
+    }
+    s0_issued = false;
+    // The next unit, if this issuer computes a tile of it (tile B may be
+    // absent): its first score product goes out early (d = 64).
+    const int un = u + static_cast<int>(gridDim.x);
+    const bool early_next = C::kSepP && un < w.units && (x == 0 || w.has_b(un));
+    const int bn = (ui + 1) % C::kQBufs, g0n = (ui + 1) * 2 * nkv;
     for (int j = 0; ok && j < nkv; ++j) {
       const int jt = jx + j;
       const int iv = g0 + 2 * j + 1, ik = g0 + 2 * j + 2;
@@ -230,6 +247,17 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
           tc_fence_after();
           issue_qk<D>(tS, q_desc, k_desc(ik));
           umma_commit(&bars.s_full[x]);
+        } else if (early_next) {
+          if (!(ok = mbar_wait(&bars.q_full[bn], ((ui + 1) / C::kQBufs) & 1, ab, dev_err))) break;
+          if (!(ok = mbar_wait(&bars.full[slot_of(g0n)], phase_of(g0n), ab, dev_err))) break;
+          if (!(ok = mbar_wait(&bars.s_free[x], jt & 1, ab, dev_err))) break;
+          tc_fence_after();
+          const uint64_t q_desc_n =
+              sdesc_sw128(smem_u32(sm + C::kOffQ + (bn * 2 + x) * C::kQTileBytes), 16, 1024);
+          issue_qk<D>(tS, q_desc_n, k_desc(g0n));
+          umma_commit(&bars.s_full[x]);
+          umma_commit(&bars.empty[slot_of(g0n)]);
+          s0_issued = true;
         }
         if (!(ok = mbar_wait(&bars.p_full[x], jt & 1, ab, dev_err))) break;
         tc_fence_after();
@@ -263,7 +291,8 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
 // Softmax / epilogue of one 128-row query tile (x = 0: tile A, 1: tile B).
 template <int D>
 __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const FwdWork& w, float scale_log2,
-                            __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
+                            const CUtensorMap* map_o, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                            uint32_t* dev_err) {
   using C = FwdCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
@@ -394,34 +423,71 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
   tc_fence_after();
   const float inv_l = 1.f / l;
   const bool live = n < N;
-  uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + (live ? n : 0)) * D);
+  if constexpr (C::kStageO) {
+    // O rows into the query tile's staging tile (128-byte swizzle: 16-byte
+    // chunk c of row r at c ^ (r & 7)), then one TMA store of the tile; rows
+    // past N fall outside the tensor and are not written.
+    const uint32_t stage = smem_u32(sm + C::kOffStage + x * C::kQTileBytes);
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(tO + c * 32, o);
-    tmem_wait_ld();
-    if (live) {
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32, o);
+      tmem_wait_ld();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l);
-        w.y = pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l);
-        w.z = pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l);
-        w.w = pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l);
-        orow[c * 4 + g] = w;
+        const uint32_t chunk = static_cast<uint32_t>(c * 4 + g) ^ static_cast<uint32_t>(row & 7);
+        st_shared_v4(stage + row * 128 + (chunk << 4),
+                     pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l),
+                     pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l),
+                     pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l),
+                     pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.epi[x]);
+    if (row == 0) {
+      // Every row is staged; the store has read the tile before this thread
+      // goes on (the next unit's rows reuse it only after this tile's
+      // p_full, which counts this thread).
+      if (mbar_wait(&bars.epi[x], uc & 1, ab, dev_err)) {
+        tma_store_3d(map_o, sm + C::kOffStage + x * C::kQTileBytes, 0, w.q0(u) + x * 128, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+    }
+  } else {
+    uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + (live ? n : 0)) * D);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32, o);
+      tmem_wait_ld();
+      if (live) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 w4;
+          w4.x = pack_bf16x2(__uint_as_float(o[g * 8 + 0]) * inv_l, __uint_as_float(o[g * 8 + 1]) * inv_l);
+          w4.y = pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l);
+          w4.z = pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l);
+          w4.w = pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l);
+          orow[c * 4 + g] = w4;
+        }
       }
     }
   }
-  if (live) lse[static_cast<size_t>(bh) * N + n] = (m_ref + log2f(l)) * kLn2;
+  if (live) lse[static_cast<size_t>(bh) * N + n] = (m_ref + lg2_approx(l)) * kLn2;
   jx += nkv;
   ++uc;
   }
+  if (C::kStageO && row == 0) bulk_wait_group0();
 }
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, const FwdWork w, float scale_log2,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                    const FwdWork w, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -446,6 +512,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars.pv_done[x], 1);
       mbar_init(&bars.s_free[x], 128);
       mbar_init(&bars.drain[x], 1);
+      mbar_init(&bars.epi[x], 4);
     }
     bars.abort = 0;
     fence_mbar_init();
@@ -465,7 +532,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp >= 9) {
     if (lane == 0) fwd_mma<D>(sm, bars, tmem, warp - 9, w, dev_err);
   } else {
-    fwd_softmax<D>(sm, bars, tmem, warp >> 2, w, scale_log2, out, lse, dev_err);
+    fwd_softmax<D>(sm, bars, tmem, warp >> 2, w, scale_log2, &map_o, out, lse, dev_err);
   }
   tc_fence_before();
   __syncthreads();
@@ -490,8 +557,10 @@ cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   const int sms = device_sm_count();
   const int grid = w.units < sms ? w.units : sms;
   const float scale_log2 = s.scale * 1.4426950408889634f;
-  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, w, scale_log2,
-                    reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
+  CUtensorMap mo;  // the output, for the staged tile stores (d = 64)
+  if (!encode_bhnd_map(&mo, out, s.BH, s.N, D)) return cudaErrorInvalidValue;
+  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, mo, w,
+                    scale_log2, reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
 }
 
 }  // namespace
