@@ -50,8 +50,8 @@ def flops_bwd(B, H, N, d):
 # 512 px workload (profiles/attn_kernels_512px.md), keyed to the kernel source they were taken
 # on: a changed source reports null until it is captured again.
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 192.49792e6 + 64.714752e6, "source": "attn_bwd.cu", "sha1": "78a4853b9ea8"},
-    "attn_fwd": {"bytes": 81.262592e6 + 4.880128e6, "source": "attn_fwd.cu", "sha1": "566828784a06"},
+    "attn_bwd": {"bytes": 192.504832e6 + 65.088768e6, "source": "attn_bwd.cu", "sha1": "78a4853b9ea8"},
+    "attn_fwd": {"bytes": 81.28256e6 + 7.352832e6, "source": "attn_fwd.cu", "sha1": "a8e747cd0eb4"},
 }
 
 

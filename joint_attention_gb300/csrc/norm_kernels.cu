@@ -48,20 +48,21 @@ __device__ __forceinline__ float row_sum(float v) {
 
 // --- correctly rounded x_hat ------------------------------------------------
 // x_hat is the bf16 value nearest to the exact real g x r.  The fp32 value
-// y = (g x) r computed with the fp32 sum of squares and rsqrtf is within 12
-// fp32 units in the last place of the exact product: the sum takes at most 8
-// roundings of nonnegative terms (3 per packed accumulator, 1 to join them,
-// log2(d/8) across lanes; the squares of bf16 values are exact), the mean and
-// eps add one, rsqrtf is good to 2 ulp and halves the relative error of its
-// argument, and the two products add one each.  Rounding y to bf16 is
-// therefore exact unless y lies within 32 fp32 ulps of a bf16 midpoint (low
-// 16 bits 0x8000): the window test takes the 64 values 0x8000 - 32 ..
-// 0x8000 + 31.  Those elements are rounded from a double-float r accurate to
-// about 2^-44: the row's sum of squares by error-free additions, one Newton
-// step from rsqrtf, and an error-free product, with the remainder's sign
-// breaking the midpoint.  A warp takes that path when any of its lanes has
-// such an element (about one element in a thousand).
-constexpr uint32_t kTieWindow = 64;
+// y = (g x) r computed with the fp32 sum of squares and rsqrtf is within 10.5
+// fp32 units in the last place of the exact product (first order in
+// u = 2^-24): the squares of bf16 values are exact and the sum takes at most
+// 8 roundings of nonnegative terms (3 per packed accumulator, 1 to join them,
+// log2(d/8) <= 4 across lanes): 8u; the mean and eps add u; rsqrtf is good
+// to 2 ulp (4u) and halves the relative error of its argument (4.5u); the
+// two products add u each.  Rounding y to bf16 is therefore exact unless y
+// lies within 16 fp32 ulps of a bf16 midpoint (low 16 bits 0x8000): the
+// window test takes the 32 values 0x8000 - 16 .. 0x8000 + 15.  Those elements
+// are rounded from a double-float r accurate to about 2^-44: the row's sum
+// of squares by error-free additions, one Newton step from rsqrtf, and an
+// error-free product, with the remainder's sign breaking the midpoint.  A
+// warp takes that path when any of its lanes has such an element (about one
+// element in two thousand).
+constexpr uint32_t kTieWindow = 32;
 constexpr float kEpsLo = static_cast<float>(1e-6 - static_cast<double>(1e-6f));
 
 // Knuth's TwoSum and Dekker's Fast2Sum (|a| >= |b|), with the _rn intrinsics

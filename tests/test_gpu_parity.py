@@ -119,13 +119,9 @@ def test_sharp_softmax_exercises_rescaling(ja):
     bound = 2.0 ** -9 * vmax + 2.0 ** -9 * float(np.max(np.abs(ref["O"]))) + 1e-3
     assert float(np.max(np.abs(got["O"] - ref["O"]))) <= bound
     assert relF(got["O"], ref["O"]) <= O_RELF
-    # LSE: the bf16 rounding of q_hat / k_hat is decided in fp32 on the GPU
-    # and in fp64 by the oracle, so a few elements land one ulp apart.  With
-    # gains of 2-4 the normalised vectors are large (ulp up to 2^-5) and a
-    # near one-hot LSE follows the single largest score, so one flip moves it
-    # by up to s * ulp(q_hat) * |k_hat| ~ 2^-10 of |LSE|; the bound is that.
-    lse_bound = 2.0 ** -10 * float(np.max(np.abs(ref["LSE"]))) + LSE_MAXABS
-    assert float(np.max(np.abs(got["LSE"] - ref["LSE"]))) <= lse_bound
+    # LSE: q_hat and k_hat round the same exact products on both sides, so
+    # the standard bound holds even for these large logits.
+    assert float(np.max(np.abs(got["LSE"] - ref["LSE"]))) <= LSE_MAXABS
     check_bwd(got, ref, where="sharp")
 
 
