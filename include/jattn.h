@@ -90,6 +90,36 @@ int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, con
               jattn_bf16* dv, float* dgq, float* dgk, int B, int H, int N_img, int N_txt, int d, void* stream);
 
 /*
+ * Packed variable-length forward and backward: one call over sequences of
+ * different lengths, each attending only within itself.  This is for batches
+ * that mix resolutions, for example images from different aspect-ratio buckets
+ * with their captions.  The re-diffusion README's training-data paragraph
+ * describes the aspect-bucketed export, and its roadmap lists multi-resolution
+ * training.
+ *   Layout: [H, T, d] bf16 with T = cu_seqlens[n_seqs].  Head h holds T rows,
+ *           and sequence s is rows cu_seqlens[s] .. cu_seqlens[s+1]-1 of every
+ *           head.  This is the [B, H, N, d] layout with B = 1 and the
+ *           sequences concatenated along N; each sequence lists its caption
+ *           rows and image rows in any order.
+ *   cu_seqlens: HOST array of n_seqs + 1 ints, cu_seqlens[0] = 0, strictly
+ *           increasing (every sequence has at least one row); read during
+ *           the call only.
+ *   n_seqs: 1 .. JATTN_MAX_SEQS.
+ *   lse   : [H, T] float32.
+ *   The other arguments and every status are those of jattn_fwd / jattn_bwd.
+ *   An invalid cu_seqlens gives JATTN_ERR_INVALID_ARG; n_seqs above
+ *   JATTN_MAX_SEQS gives JATTN_ERR_UNSUPPORTED.  H*T*d < 2^31.
+ * dgq and dgk sum over every sequence, head and row.
+ */
+#define JATTN_MAX_SEQS 256
+int jattn_fwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+                     const int* cu_seqlens, int n_seqs, int H, int d, jattn_bf16* out, float* lse, void* stream);
+int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+                     const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq, jattn_bf16* dk,
+                     jattn_bf16* dv, float* dgq, float* dgk, const int* cu_seqlens, int n_seqs, int H, int d,
+                     void* stream);
+
+/*
  * Forward without any device allocation.  (No counterpart on the pages: an
  * integration entry point.)  Same arguments, layout and results as jattn_fwd,
  * but the scratch it needs (the normalised q_hat and k_hat, 2 * 2 * B*H*N*d

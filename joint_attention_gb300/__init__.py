@@ -7,14 +7,15 @@ plus small conveniences that allocate the output tensors with torch.
 from __future__ import annotations
 
 from ._binding import (KERNEL_KINDS, STATUS, STATUS_CODE, JattnError, declared_symbols, jattn_bwd, jattn_fwd,
-                       jattn_fwd_noalloc,
+                       jattn_fwd_noalloc, jattn_fwd_varlen, jattn_bwd_varlen,
                        jattn_kernel_name, jattn_last_device_error, jattn_last_error_message, jattn_profile_enable, jattn_profile_read,
                        jattn_profile_reset, jattn_status_string, jattn_version, load_library, profile_snapshot)
 
 __all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd", "jattn_fwd",
            "jattn_last_device_error", "jattn_status_string", "jattn_version", "load_library", "forward",
            "backward", "KERNEL_KINDS", "jattn_kernel_name", "jattn_profile_enable", "jattn_profile_read",
-           "jattn_profile_reset", "profile_snapshot", "jattn_last_error_message", "jattn_fwd_noalloc"]
+           "jattn_profile_reset", "profile_snapshot", "jattn_last_error_message", "jattn_fwd_noalloc",
+           "jattn_fwd_varlen", "jattn_bwd_varlen", "forward_varlen", "backward_varlen"]
 
 
 def forward(q, k, v, gq, gk, n_txt: int, stream=None):
@@ -37,4 +38,28 @@ def backward(q, k, v, gq, gk, out, lse, dout, n_txt: int, stream=None):
     dgq = torch.empty_like(gq)
     dgk = torch.empty_like(gk)
     jattn_bwd(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, B, H, N - n_txt, n_txt, d, stream)
+    return dq, dk, dv, dgq, dgk
+
+
+def forward_varlen(q, k, v, gq, gk, cu_seqlens, stream=None):
+    """out, lse for packed sequences: q, k, v [H, T, d] bf16 CUDA tensors, sequence s in rows
+    cu_seqlens[s] .. cu_seqlens[s+1]-1 of every head (cu_seqlens: host ints)."""
+    import torch
+
+    H, T, d = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    jattn_fwd_varlen(q, k, v, gq, gk, cu_seqlens, H, d, out, lse, stream)
+    return out, lse
+
+
+def backward_varlen(q, k, v, gq, gk, out, lse, dout, cu_seqlens, stream=None):
+    """dq, dk, dv, dgq, dgk for packed sequences (layouts as forward_varlen)."""
+    import torch
+
+    H, T, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dgq = torch.empty_like(gq)
+    dgk = torch.empty_like(gk)
+    jattn_bwd_varlen(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, cu_seqlens, H, d, stream)
     return dq, dk, dv, dgq, dgk

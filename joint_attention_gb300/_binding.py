@@ -60,6 +60,11 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     lib.jattn_fwd_noalloc.restype = i32
     lib.jattn_bwd.argtypes = [vp] * 13 + [i32] * 5 + [vp]
     lib.jattn_bwd.restype = i32
+    i32p = ctypes.POINTER(ctypes.c_int)
+    lib.jattn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i32p, i32, i32, i32, vp, vp, vp]
+    lib.jattn_fwd_varlen.restype = i32
+    lib.jattn_bwd_varlen.argtypes = [vp] * 13 + [i32p, i32, i32, i32, vp]
+    lib.jattn_bwd_varlen.restype = i32
     lib.jattn_last_device_error.argtypes = [vp]
     lib.jattn_last_device_error.restype = i32
     lib.jattn_status_string.argtypes = [i32]
@@ -197,6 +202,50 @@ def jattn_bwd(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, B: int, H: 
                        N_txt, d, _stream(stream))
     if check and rc != 0:
         raise JattnError(rc, "jattn_bwd")
+    return rc
+
+
+def _cu_array(cu_seqlens):
+    """Host int array (ctypes) of the sequence offsets, and T and the count."""
+    vals = [int(x) for x in cu_seqlens]
+    arr = (ctypes.c_int * len(vals))(*vals)
+    return arr, vals[-1] if vals else 0, len(vals) - 1
+
+
+def jattn_fwd_varlen(q, k, v, gq, gk, cu_seqlens, H: int, d: int, out, lse, stream=None,
+                     check: bool = True) -> int:
+    """C ABI jattn_fwd_varlen.  q/k/v/out [H, T, d] bf16 (sequence s = rows cu[s]..cu[s+1]-1 of every
+    head), gq/gk [d] fp32, lse [H, T] fp32; cu_seqlens a host sequence of n + 1 ints."""
+    import torch
+
+    lib = load_library()
+    arr, T, n = _cu_array(cu_seqlens)
+    e, r = H * T * d, H * T
+    bf, f32 = torch.bfloat16, torch.float32
+    rc = lib.jattn_fwd_varlen(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                              _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), arr, n, H, d,
+                              _ptr(out, "out", bf, e), _ptr(lse, "lse", f32, r), _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_fwd_varlen")
+    return rc
+
+
+def jattn_bwd_varlen(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, cu_seqlens, H: int, d: int,
+                     stream=None, check: bool = True) -> int:
+    """C ABI jattn_bwd_varlen (layouts as jattn_fwd_varlen)."""
+    import torch
+
+    lib = load_library()
+    arr, T, n = _cu_array(cu_seqlens)
+    e, r = H * T * d, H * T
+    bf, f32 = torch.bfloat16, torch.float32
+    rc = lib.jattn_bwd_varlen(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                              _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), _ptr(out, "out", bf, e),
+                              _ptr(lse, "lse", f32, r), _ptr(dout, "dout", bf, e), _ptr(dq, "dq", bf, e),
+                              _ptr(dk, "dk", bf, e), _ptr(dv, "dv", bf, e), _ptr(dgq, "dgq", f32, d),
+                              _ptr(dgk, "dgk", f32, d), arr, n, H, d, _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_bwd_varlen")
     return rc
 
 

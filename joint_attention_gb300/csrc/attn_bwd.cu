@@ -10,11 +10,13 @@
 //   dV_j += P^T dO_i            dK_j += dS^T Q_i              (TMEM accumulators)
 //   dQ_i += dS K_j              (bulk fp32 reduce-add into a global accumulator)
 //
-// Work unit: one 128-key tile j of one (b, h), streaming every query tile of
-// the head.  The kernel is persistent: one CTA per SM walks the units
-// u = blockIdx.x, blockIdx.x + gridDim.x, ... with every barrier phase
-// running on across units, so the next unit's K/V load and first S / dP
-// products overlap the current unit's last tiles and its epilogue.
+// Work unit: one 128-key tile j of one segment of one head (a (b, h) of the
+// [B, H, N, d] layout, or one sequence of a packed variable-length call),
+// streaming every query tile of that segment.  The kernel is persistent: one
+// CTA per SM walks the units u = blockIdx.x, blockIdx.x + gridDim.x, ...
+// with every barrier phase running on across units, so the next unit's K/V
+// load and first S / dP products overlap the current unit's last tiles and
+// its epilogue.
 // 640 threads (five warpgroups; setmaxnreg gives the compute warpgroups 128
 // registers per thread, the drain 104, the epilogue 72 and TMA / MMA 40):
 //
@@ -116,20 +118,50 @@ struct BwdCfg {
   static __device__ __forceinline__ int off_v(int b) { return kOffKV + b * 2 * kTile + kTile; }
 };
 
-// Units: u -> (bh = u / nkt, key tile j = u % nkt); CTA c takes u = c,
-// c + gridDim.x, ...  Query tiles are counted on across units (t = ui * nkt
-// + i for the ui-th unit of this CTA), and every ring / handshake barrier
-// takes its phase from that count.
-struct BwdWork {
-  int N;
-  int nkt;    // key tiles per head == query tiles per head
-  int units;  // BH * nkt
-  // The i-th query tile visited by unit u: the key tiles of one head (which
-  // run side by side on neighbouring CTAs) start at different query tiles,
-  // so that their dQ reduce-adds go to different rows at any one time.
-  __device__ __forceinline__ int query_tile(int u, int i) const {
-    const int q = i + u % nkt;
+// Units: one 128-key tile of one segment of one head.  Per head the units
+// run over the segments' 128-row tiles in order (unit index k within the
+// head is the segment's first padded row / 128 plus the key tile j); CTA c
+// takes u = c, c + gridDim.x, ...  Each unit visits every query tile of its
+// own segment.  Query tiles are counted on across units (t runs over all
+// query tiles of the CTA's units), and every ring / handshake barrier takes
+// its phase from that count.
+struct BwdUnit {
+  int bh;     // head
+  int j;      // key tile within the segment
+  int nkt;    // 128-row tiles of the segment (key tiles == query tiles)
+  int row0;   // the segment's first row in the head
+  int end;    // one past its last row
+  int prow0;  // its first row in the padded per-head scratch
+  // The i-th query tile visited: the key tiles of one segment (which run
+  // side by side on neighbouring CTAs) start at different query tiles, so
+  // that their dQ reduce-adds go to different rows at any one time.
+  __device__ __forceinline__ int query_tile(int i) const {
+    const int q = i + j;
     return q < nkt ? q : q - nkt;
+  }
+  __device__ __forceinline__ int kv0() const { return row0 + 128 * j; }  // first key row
+};
+
+struct BwdWork {
+  int upc;    // units per head (padded rows per head / 128)
+  int units;  // heads * upc
+  SegTable seg;
+  __device__ __forceinline__ BwdUnit unit(int u) const {
+    BwdUnit r;
+    r.bh = u / upc;
+    const int k = u - r.bh * upc;
+    int lo = 0, hi = seg.n;  // seg.pcu[lo] <= 128 k < seg.pcu[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seg.pcu[mid] <= 128 * k) lo = mid;
+      else hi = mid;
+    }
+    r.j = k - seg.pcu[lo] / 128;
+    r.nkt = (seg.pcu[lo + 1] - seg.pcu[lo]) / 128;
+    r.row0 = seg.cu[lo];
+    r.end = seg.cu[lo + 1];
+    r.prow0 = seg.pcu[lo];
+    return r;
   }
 };
 
@@ -165,7 +197,7 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
 template <int D>
 __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                              const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, const BwdWork& w,
-                             const float* nlse2_pad, const float* delta_pad, int n_pad, uint32_t* dev_err) {
+                             const float* nlse2_pad, const float* delta_pad, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(mq);
   tma_prefetch_desc(mk);
@@ -174,8 +206,10 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
   volatile int* ab = &bars.abort;
   int nkv_issued = 0, nq_issued = 0, ndo_issued = 0;
   bool ok = true;
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
-    const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
+    const BwdUnit un = w.unit(u);
+    const int bh = un.bh, kv0 = un.kv0();
     const int b = ui % C::kKVBufs;
     if (ui >= C::kKVBufs && !(ok = mbar_wait(&bars.kv_empty[b], ((ui / C::kKVBufs) - 1) & 1, ab, dev_err))) break;
     mbar_arrive_expect_tx(&bars.kv_full[b], 2u * C::kTile);
@@ -184,26 +218,29 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
       tma_load_3d(sm + C::off_v(b) + blk * 16384, mv, &bars.kv_full[b], blk * 64, kv0, bh);
     }
     ++nkv_issued;
-    for (int i = 0; i < w.nkt; ++i) {
-      const int t = ui * w.nkt + i;
+    for (int i = 0; i < un.nkt; ++i) {
+      const int t = tb + i;
       const int qs = t % C::kQStages;
       if (t >= C::kQStages && !(ok = mbar_wait(&bars.q_empty[qs], ((t / C::kQStages) - 1) & 1, ab, dev_err))) break;
       mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
-      const int qi = w.query_tile(u, i);
-      const size_t prow = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(qi) * 128;
+      const int qi = un.query_tile(i);
+      const size_t prow = static_cast<size_t>(bh) * w.seg.prows + un.prow0 + static_cast<size_t>(qi) * 128;
       bulk_load(bars.nlse2[qs], nlse2_pad + prow, 512, &bars.q_full[qs]);
       bulk_load(bars.delta[qs], delta_pad + prow, 512, &bars.q_full[qs]);
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, qi * 128, bh);
+        tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, un.row0 + qi * 128,
+                    bh);
       ++nq_issued;
       const int ds = t % C::kDOStages;
       if (t >= C::kDOStages && !(ok = mbar_wait(&bars.do_empty[ds], ((t / C::kDOStages) - 1) & 1, ab, dev_err)))
         break;
       mbar_arrive_expect_tx(&bars.do_full[ds], C::kTile);
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_3d(sm + C::kOffDO + ds * C::kTile + blk * 16384, mdo, &bars.do_full[ds], blk * 64, qi * 128, bh);
+        tma_load_3d(sm + C::kOffDO + ds * C::kTile + blk * 16384, mdo, &bars.do_full[ds], blk * 64,
+                    un.row0 + qi * 128, bh);
       ++ndo_issued;
     }
+    tb += un.nkt;
   }
   if (*ab) {
     // Aborted: let the copies already in flight land before the CTA exits.
@@ -291,13 +328,15 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
   auto kQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16, 1024); };
   auto kDO = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16, 1024); };
   bool ok = true;
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int nkt = w.unit(u).nkt;
     const int b = ui % C::kKVBufs;
     if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
     const uint64_t kK = sdesc_sw128(smem_u32(sm + C::off_k(b)), 16, 1024);
     const uint64_t kV = sdesc_sw128(smem_u32(sm + C::off_v(b)), 16, 1024);
-    for (int i = 0; i < w.nkt; ++i) {
-      const int t = ui * w.nkt + i;
+    for (int i = 0; i < nkt; ++i) {
+      const int t = tb + i;
       if (t > 0 && !(ok = mbar_wait(&bars.s_free, (t - 1) & 1, ab, dev_err))) break;
       if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
       tc_fence_after();
@@ -311,6 +350,7 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       umma_commit(&bars.dp_full);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
     }
+    tb += nkt;
     if (ok) umma_commit(&bars.kv_mmadone[b]);
   }
   umma_commit(&bars.drain[0]);
@@ -328,9 +368,11 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
   };
   const uint64_t kDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16, 1024);
   bool ok = true;
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
-    for (int i = 0; i < w.nkt; ++i) {
-      const int t = ui * w.nkt + i;
+    const int nkt = w.unit(u).nkt;
+    for (int i = 0; i < nkt; ++i) {
+      const int t = tb + i;
       if (!(ok = mbar_wait(&bars.p_ready, t & 1, ab, dev_err))) break;
       if (!(ok = mbar_wait(&bars.do_full[t % C::kDOStages], (t / C::kDOStages) & 1, ab, dev_err))) break;
       // The previous unit's dV has been read out of TMEM.
@@ -347,6 +389,7 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       umma_commit(&bars.q_empty[t % C::kQStages]);
       umma_commit(&bars.ds_free[0]);
     }
+    tb += nkt;
     if (ok) umma_commit(&bars.acc_full);
   }
   umma_commit(&bars.drain[1]);
@@ -361,12 +404,14 @@ __device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdW
   volatile int* ab = &bars.abort;
   const uint64_t mDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16384, 1024);
   bool ok = true;
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int nkt = w.unit(u).nkt;
     const int b = ui % C::kKVBufs;
     if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
     const uint64_t mK = sdesc_sw128(smem_u32(sm + C::off_k(b)), 16384, 1024);
-    for (int i = 0; i < w.nkt; ++i) {
-      const int t = ui * w.nkt + i;
+    for (int i = 0; i < nkt; ++i) {
+      const int t = tb + i;
       if (!(ok = mbar_wait(&bars.ds_ready, t & 1, ab, dev_err))) break;
       if (t > 0 && !(ok = mbar_wait(&bars.dq_free, (t - 1) & 1, ab, dev_err))) break;
       tc_fence_after();
@@ -374,6 +419,7 @@ __device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdW
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[0]);
     }
+    tb += nkt;
     if (ok) umma_commit(&bars.kv_mmadone[b]);
   }
   umma_commit(&bars.drain[2]);
@@ -400,9 +446,12 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork
   auto do_ph = [](int t) { return static_cast<uint32_t>((t / C::kDOStages) & 1); };
 
   bool ok = true;
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
+    const int nkt = w.unit(u).nkt;
     const int b = ui % C::kKVBufs;
-    const int t0 = ui * w.nkt;
+    const int t0 = tb;
+    tb += nkt;
     if (!(ok = mbar_wait(&bars.kv_full[b], (ui / C::kKVBufs) & 1, ab, dev_err))) break;
     const uint32_t aK = smem_u32(sm + C::off_k(b)), aV = smem_u32(sm + C::off_v(b));
     const uint64_t kK = sdesc_sw128(aK, 16, 1024), kV = sdesc_sw128(aV, 16, 1024);
@@ -417,7 +466,7 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork
     tc_fence_after();
     mma_kk<D>(tmem + C::kColDP, kV, kDO(t0), C::kIdescSS);
     umma_commit(&bars.dp_full);
-    for (int i = 0; i < w.nkt; ++i) {
+    for (int i = 0; i < nkt; ++i) {
       const int t = t0 + i;
       // dV(t): needs P^T(t) in TMEM (and the previous unit's dV read out).
       if (!(ok = mbar_wait(&bars.p_ready, t & 1, ab, dev_err))) break;
@@ -426,7 +475,7 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork
       mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(t), i > 0);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
       // S(t+1): overwrites the S^T/P^T columns behind dV(t).
-      if (i + 1 < w.nkt) {
+      if (i + 1 < nkt) {
         if (!(ok = mbar_wait(&bars.q_full[(t + 1) % C::kQStages], q_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
         mma_kk<D>(tmem + C::kColS, kK, kQ(t + 1), C::kIdescSS);
@@ -443,7 +492,7 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork
       mma_dq<D>(tmem + C::kColDQ, mDS(t), mK);
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[t % C::kDSBufs]);
-      if (i + 1 < w.nkt) {
+      if (i + 1 < nkt) {
         if (!(ok = mbar_wait(&bars.dq_free, t & 1, ab, dev_err))) break;
         if (!(ok = mbar_wait(&bars.do_full[(t + 1) % C::kDOStages], do_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
@@ -478,10 +527,14 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
   const uint64_t minus1 = f2_make(-1.f, -1.f);
   volatile int* ab = &bars.abort;
 
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; u < w.units; u += gridDim.x, ++ui) {
-    const bool key_live = (u % w.nkt) * 128 + kr < w.N;
-    for (int i = 0; i < w.nkt; ++i) {
-      const int t = ui * w.nkt + i;
+    const BwdUnit un = w.unit(u);
+    const bool key_live = un.kv0() + kr < un.end;
+    const int t0 = tb;
+    tb += un.nkt;
+    for (int i = 0; i < un.nkt; ++i) {
+      const int t = t0 + i;
       const int qs = t % C::kQStages;
       bool ok = mbar_wait(&bars.s_full, t & 1, ab, dev_err);
       // This stage's LSE / D arrived with the query tile (already complete).
@@ -618,19 +671,25 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     return __all_sync(0xffffffffu, okb);
   };
   bool ok = true;
+  const size_t rows = static_cast<size_t>(w.seg.rows);
+  int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
-    const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
-    const int n = kv0 + r128;  // key row of this thread in the epilogue
-    const bool key_live = n < w.N;
-    const size_t row_off = (static_cast<size_t>(bh) * w.N + (key_live ? n : 0)) * D;
+    const BwdUnit un = w.unit(u);
+    const int bh = un.bh;
+    const int n = un.kv0() + r128;  // key row of this thread in the epilogue
+    const bool key_live = n < un.end;
+    const size_t row_off = (static_cast<size_t>(bh) * rows + (key_live ? n : 0)) * D;
+    const int t0 = tb;
+    tb += un.nkt;
 
-    for (int i = 0; i < w.nkt; ++i) {
-      const int t = ui * w.nkt + i;
+    for (int i = 0; i < un.nkt; ++i) {
+      const int t = t0 + i;
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const int qrow = w.query_tile(u, i) * 128 + r128;
-      float* grow = dqacc + (static_cast<size_t>(bh) * w.N + (qrow < w.N ? qrow : 0)) * D;
+      const int qrow = un.row0 + un.query_tile(i) * 128 + r128;
+      const bool q_live = qrow < un.end;
+      float* grow = dqacc + (static_cast<size_t>(bh) * rows + (q_live ? qrow : 0)) * D;
       if constexpr (kTiled) {
         // d = 64: the whole dQ row into registers and the TMEM columns
         // released first, then the staging row once its previous reduce has
@@ -646,7 +705,7 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
         for (int q = 0; q < D / 4; ++q)
           st_shared_v4(srow_a + q * 16, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
         fence_proxy_async_smem();
-        if (qrow < w.N) {
+        if (q_live) {
           bulk_reduce_add_f32(grow, srow, D * 4);
           bulk_commit_group();
         }
@@ -668,7 +727,7 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
             mbar_arrive(&bars.dq_free);
           }
           fence_proxy_async_smem();
-          if (qrow < w.N) {
+          if (q_live) {
             bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
             bulk_commit_group();
           }
@@ -682,7 +741,7 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
-    const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
+    const float r = key_live ? rk[static_cast<size_t>(bh) * rows + n] : 0.f;
     if constexpr (!kTiled) {
       // d = 128: per-row accesses; two passes over the TMEM dK accumulator
       // (dot, then outputs), the dgk rows staged kDQCols columns at a time.
@@ -828,16 +887,18 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     return __all_sync(0xffffffffu, okb);
   };
   bool ok = true;
+  const size_t rows = static_cast<size_t>(w.seg.rows);
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
-    const int bh = u / w.nkt, kv0 = (u % w.nkt) * 128;
+    const BwdUnit un = w.unit(u);
+    const int bh = un.bh, kv0 = un.kv0();
     const int b = ui % C::kKVBufs;
     const int n = kv0 + r128;
-    const bool key_live = n < w.N;
-    const int live_rows = w.N - kv0 < 128 ? w.N - kv0 : 128;
-    const size_t tile_off = (static_cast<size_t>(bh) * w.N + kv0) * D;
+    const bool key_live = n < un.end;
+    const int live_rows = un.end - kv0 < 128 ? un.end - kv0 : 128;
+    const size_t tile_off = (static_cast<size_t>(bh) * rows + kv0) * D;
     // The raw k tile is pulled into L2 while the unit runs.
     if (r128 == 0) bulk_prefetch_l2(k_raw + tile_off, live_rows * D * 2);
-    const float r = key_live ? rk[static_cast<size_t>(bh) * w.N + n] : 0.f;
+    const float r = key_live ? rk[static_cast<size_t>(bh) * rows + n] : 0.f;
     const uint32_t tile_k = smem_u32(sm + C::off_k(b));  // k, then dk
     const uint32_t tile_v = smem_u32(sm + C::off_v(b));  // dv
 
@@ -972,8 +1033,8 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                    const BwdWork w, float scale, const float* __restrict__ nlse2_pad,
-                    const float* __restrict__ delta_pad, int n_pad, const __nv_bfloat16* __restrict__ k_raw,
+                    const __grid_constant__ BwdWork w, float scale, const float* __restrict__ nlse2_pad,
+                    const float* __restrict__ delta_pad, const __nv_bfloat16* __restrict__ k_raw,
                     const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, float* __restrict__ dgk_part,
                     uint32_t* dev_err) {
@@ -1047,7 +1108,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if constexpr (D == 64) bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, k_raw, rk, dk, dv, dgk_part, dev_err);
     } else if (warp == kWarpTma) {
       if (lane == 0)
-        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, nlse2_pad, delta_pad, n_pad, dev_err);
+        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, nlse2_pad, delta_pad, dev_err);
     } else if (warp == kWarpMma0) {
       if (lane == 0) {
         if (C::kSplitIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
@@ -1083,20 +1144,20 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
   BwdWork w;
-  w.N = s.N;
-  w.nkt = (s.N + 127) / 128;
-  w.units = s.BH * w.nkt;
+  w.seg = s.seg;
+  w.upc = s.seg.prows / 128;
+  w.units = s.BH * w.upc;
   const int sms = device_sm_count();
   const int grid = w.units < sms ? w.units : sms;
   return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, w, s.scale,
-                    nlse2_pad, delta_pad, w.nkt * 128, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
+                    nlse2_pad, delta_pad, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
                     reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part,
                     dev_err);
 }
 
 }  // namespace
 
-int attn_bwd_dgk_parts(const AttnShape& s) { return s.BH * ((s.N + 127) / 128); }
+int attn_bwd_dgk_parts(const AttnShape& s) { return s.BH * (s.seg.prows / 128); }
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, const AttnShape& s, const float* nlse2_pad,

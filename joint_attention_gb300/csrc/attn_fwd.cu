@@ -100,17 +100,41 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-// Units: u -> (bh = u / npairs, query rows q0 = (u % npairs) * 256 ..
-// q0 + 255 as tiles A and B); CTA c takes u = c, c + gridDim.x, ...  Key
+// Units: 256 query rows (tiles A and B) of one segment of one head.  Per
+// head the units run over the segments' 256-row blocks in order; CTA c takes
+// u = c, c + gridDim.x, ...  A unit streams its segment's key tiles.  Key
 // tiles, ring slots and every per-tile barrier are counted on across units.
+struct FwdUnit {
+  int bh;      // head
+  int q0;      // first query row (tile A) in the head
+  int kvb;     // the segment's first row
+  int end;     // one past its last row
+  int nkv;     // its 128-key tiles
+  bool has_b;  // tile B has rows
+};
+
 struct FwdWork {
-  int N;
-  int nkv;     // key tiles per head
-  int npairs;  // 256-row query blocks per head
-  int units;   // BH * npairs
-  __device__ __forceinline__ int bh(int u) const { return u / npairs; }
-  __device__ __forceinline__ int q0(int u) const { return (u % npairs) * 2 * kTileM; }
-  __device__ __forceinline__ bool has_b(int u) const { return q0(u) + kTileM < N; }
+  int upc;    // units per head
+  int units;  // heads * upc
+  SegTable seg;
+  int uf[kMaxSegments + 1];  // units before each segment (256-row blocks)
+  __device__ __forceinline__ FwdUnit unit(int u) const {
+    FwdUnit r;
+    r.bh = u / upc;
+    const int k = u - r.bh * upc;
+    int lo = 0, hi = seg.n;  // uf[lo] <= k < uf[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (uf[mid] <= k) lo = mid;
+      else hi = mid;
+    }
+    r.kvb = seg.cu[lo];
+    r.end = seg.cu[lo + 1];
+    r.q0 = r.kvb + (k - uf[lo]) * 2 * kTileM;
+    r.nkv = (r.end - r.kvb + kTileN - 1) / kTileN;
+    r.has_b = r.q0 + kTileM < r.end;
+    return r;
+  }
 };
 
 template <int D>
@@ -121,12 +145,13 @@ __device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k,
   tma_prefetch_desc(map_k);
   tma_prefetch_desc(map_v);
   volatile int* ab = &bars.abort;
-  const int per_unit = 2 * w.nkv;
   int issued = 0, q_issued = 0;
   bool ok = true;
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
-    const int bh = w.bh(u), q0 = w.q0(u);
-    const bool hasB = w.has_b(u);
+    const FwdUnit un = w.unit(u);
+    const int bh = un.bh, q0 = un.q0;
+    const bool hasB = un.has_b;
+    const int per_unit = 2 * un.nkv;
     const int b = ui % C::kQBufs;
     if (ui >= C::kQBufs && !(ok = mbar_wait(&bars.q_empty[b], ((ui / C::kQBufs) - 1) & 1, ab, dev_err))) break;
     mbar_arrive_expect_tx(&bars.q_full[b], (hasB ? 2u : 1u) * C::kQTileBytes);
@@ -141,7 +166,7 @@ __device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k,
         break;
       mbar_arrive_expect_tx(&bars.full[slot], C::kSlotBytes);
       const CUtensorMap* m = (i & 1) ? map_v : map_k;
-      const int kv0 = (i >> 1) * kTileN;
+      const int kv0 = un.kvb + (i >> 1) * kTileN;
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_3d(sm + C::kOffRing + slot * C::kSlotBytes + blk * 16384, m, &bars.full[slot], blk * 64, kv0, bh);
     }
@@ -195,8 +220,8 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
   auto k_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16, 1024); };
   auto v_desc = [=](int i) { return sdesc_sw128(ring + slot_of(i) * C::kSlotBytes, 16384, 1024); };
   volatile int* ab = &bars.abort;
-  const int nkv = w.nkv;
   int jx = 0;  // key tiles this issuer has processed (its barrier phases)
+  int gb = 0;  // ring items of the previous units
   // d = 64: the next unit's first score product is issued in place of the
   // last tile's S(j+1), so that it is ready when the softmax finishes the
   // unit's epilogue.
@@ -204,8 +229,11 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
   bool ok = true;
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
     const int b = ui % C::kQBufs;
-    const int g0 = ui * 2 * nkv;  // first ring item of the unit
-    if (x == 1 && !w.has_b(u)) {
+    const FwdUnit uo = w.unit(u);
+    const int nkv = uo.nkv;
+    const int g0 = gb;  // first ring item of the unit
+    gb += 2 * nkv;
+    if (x == 1 && !uo.has_b) {
       // No tile B in this unit: only release the unit's slots and Q buffer.
       for (int i = 0; ok && i < 2 * nkv; ++i) {
         if (!(ok = mbar_wait(&bars.full[slot_of(g0 + i)], phase_of(g0 + i), ab, dev_err))) break;
@@ -230,8 +258,8 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
     // The next unit, if this issuer computes a tile of it (tile B may be
     // absent): its first score product goes out early (d = 64).
     const int un = u + static_cast<int>(gridDim.x);
-    const bool early_next = C::kSepP && un < w.units && (x == 0 || w.has_b(un));
-    const int bn = (ui + 1) % C::kQBufs, g0n = (ui + 1) * 2 * nkv;
+    const bool early_next = C::kSepP && un < w.units && (x == 0 || w.unit(un).has_b);
+    const int bn = (ui + 1) % C::kQBufs, g0n = g0 + 2 * nkv;
     for (int j = 0; ok && j < nkv; ++j) {
       const int jt = jx + j;
       const int iv = g0 + 2 * j + 1, ik = g0 + 2 * j + 2;
@@ -302,14 +330,17 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
   const uint32_t tO = tmem + lane_base + C::kColO + x * D;
   const uint32_t tP = tmem + lane_base + C::kColP + x * C::kPStride;
   volatile int* ab = &bars.abort;
-  const int N = w.N, nkv = w.nkv;
+  const size_t rows = static_cast<size_t>(w.seg.rows);
   int jx = 0;       // key tiles processed by this query-tile slot (barrier phases)
   uint32_t uc = 0;  // units processed by this slot (o_done phases)
+  uint32_t us = 0;  // tiles stored through the staging buffer (epi phases)
   bool ok = true;
   for (int u = blockIdx.x; ok && u < w.units; u += gridDim.x) {
-  if (x == 1 && !w.has_b(u)) continue;
-  const int bh = w.bh(u);
-  const int n = w.q0(u) + x * 128 + row;
+  const FwdUnit un = w.unit(u);
+  if (x == 1 && !un.has_b) continue;
+  const int bh = un.bh, nkv = un.nkv;
+  const int qt0 = un.q0 + x * 128;  // the tile's first row
+  const int n = qt0 + row;
   float m_ref = -INFINITY;
   float l = 0.f;
   for (int j = 0; j < nkv; ++j) {
@@ -327,7 +358,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
       tc_fence_before();
       mbar_arrive(&bars.s_free[x]);
     }
-    const int nvalid = N - j * kTileN;
+    const int nvalid = un.end - (un.kvb + j * kTileN);
     if (nvalid < kTileN) {  // only the ragged last key tile needs the mask
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -422,8 +453,11 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
   if (!ok) return;
   tc_fence_after();
   const float inv_l = 1.f / l;
-  const bool live = n < N;
-  if constexpr (C::kStageO) {
+  const bool live = n < un.end;
+  // The staged tile store writes whole 128-row tiles, clipped only at the
+  // head's last row: a tile that runs past its segment into the next one
+  // stores rows instead.
+  if (C::kStageO && (qt0 + 128 <= un.end || un.end == w.seg.rows)) {
     // O rows into the query tile's staging tile (128-byte swizzle: 16-byte
     // chunk c of row r at c ^ (r & 7)), then one TMA store of the tile; rows
     // past N fall outside the tensor and are not written.
@@ -450,14 +484,15 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
       // Every row is staged; the store has read the tile before this thread
       // goes on (the next unit's rows reuse it only after this tile's
       // p_full, which counts this thread).
-      if (mbar_wait(&bars.epi[x], uc & 1, ab, dev_err)) {
-        tma_store_3d(map_o, sm + C::kOffStage + x * C::kQTileBytes, 0, w.q0(u) + x * 128, bh);
+      if (mbar_wait(&bars.epi[x], us & 1, ab, dev_err)) {
+        tma_store_3d(map_o, sm + C::kOffStage + x * C::kQTileBytes, 0, qt0, bh);
         bulk_commit_group();
         bulk_wait_group_read0();
       }
     }
+    ++us;
   } else {
-    uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + (live ? n : 0)) * D);
+    uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * rows + (live ? n : 0)) * D);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -476,7 +511,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
       }
     }
   }
-  if (live) lse[static_cast<size_t>(bh) * N + n] = (m_ref + lg2_approx(l)) * kLn2;
+  if (live) lse[static_cast<size_t>(bh) * rows + n] = (m_ref + lg2_approx(l)) * kLn2;
   jx += nkv;
   ++uc;
   }
@@ -487,7 +522,7 @@ template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
-                    const FwdWork w, float scale_log2,
+                    const __grid_constant__ FwdWork w, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -550,10 +585,12 @@ cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   FwdWork w;
-  w.N = s.N;
-  w.nkv = (s.N + kTileN - 1) / kTileN;
-  w.npairs = (s.N + 2 * kTileM - 1) / (2 * kTileM);
-  w.units = s.BH * w.npairs;
+  w.seg = s.seg;
+  w.uf[0] = 0;
+  for (int i = 0; i < s.seg.n; ++i)
+    w.uf[i + 1] = w.uf[i] + (s.seg.cu[i + 1] - s.seg.cu[i] + 2 * kTileM - 1) / (2 * kTileM);
+  w.upc = w.uf[s.seg.n];
+  w.units = s.BH * w.upc;
   const int sms = device_sm_count();
   const int grid = w.units < sms ? w.units : sms;
   const float scale_log2 = s.scale * 1.4426950408889634f;

@@ -131,9 +131,10 @@ Range range_of(const void* p, size_t bytes) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Shape {
-  int B, H, N, d, BH, n_pad;
-  size_t rows;   // BH * N
-  size_t elems;  // BH * N * d
+  int B, H, N, d, BH;  // BH heads of N rows each (packed variable-length: H heads of T rows)
+  size_t rows;         // BH * N
+  size_t elems;        // BH * N * d
+  SegTable seg;        // the heads' segments
 };
 
 int check_shape(int B, int H, int N_img, int N_txt, int d, Shape* s) {
@@ -150,8 +151,30 @@ int check_shape(int B, int H, int N_img, int N_txt, int d, Shape* s) {
   s->N = static_cast<int>(N);
   s->d = d;
   s->BH = static_cast<int>(BH);
-  s->n_pad = static_cast<int>((N + 127) / 128 * 128);
   s->rows = static_cast<size_t>(BH * N);
+  s->elems = static_cast<size_t>(elems);
+  make_uniform_seg_table(&s->seg, s->N);
+  return JATTN_OK;
+}
+
+// Packed variable-length layout: H heads of T = cu[n] rows, one segment per
+// sequence.  cu is a host array of n + 1 row offsets.
+int check_shape_varlen(const int* cu, int n, int H, int d, Shape* s) {
+  if (!cu || n < 1 || H <= 0 || d <= 0) return JATTN_ERR_INVALID_ARG;
+  if (n > kMaxSegments) return JATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return JATTN_ERR_UNSUPPORTED;
+  if (H > 65535) return JATTN_ERR_INVALID_ARG;
+  if (!make_seg_table(&s->seg, cu, n)) return JATTN_ERR_INVALID_ARG;
+  const int64_t T = s->seg.rows;
+  const int64_t elems = static_cast<int64_t>(H) * T * d;
+  if (elems >= (int64_t{1} << 31) || static_cast<int64_t>(H) * s->seg.prows >= (int64_t{1} << 31))
+    return JATTN_ERR_INVALID_ARG;
+  s->B = 1;
+  s->H = H;
+  s->N = static_cast<int>(T);
+  s->d = d;
+  s->BH = H;
+  s->rows = static_cast<size_t>(H) * T;
   s->elems = static_cast<size_t>(elems);
   return JATTN_OK;
 }
@@ -175,7 +198,7 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
   size_t b = 0;
   b += 2 * (s.elems * 2 + 256);                                   // q_hat, k_hat
   b += 2 * (s.rows * 4 + 256);                                    // rq, rk
-  b += 2 * (static_cast<size_t>(s.BH) * s.n_pad * 4 + 256);       // nlse2, delta
+  b += 2 * (static_cast<size_t>(s.BH) * s.seg.prows * 4 + 256);   // nlse2, delta
   b += s.elems * 4 + 256;                                         // dq accumulator
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
   b += static_cast<size_t>(dg_reduce_scratch_floats(s.d)) * 4 + 256;  // dg slice partials
@@ -184,6 +207,28 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
 }
 
 }  // namespace
+
+bool make_seg_table(SegTable* t, const int* cu, int n) {
+  if (!t || !cu || n < 1 || n > kMaxSegments || cu[0] != 0) return false;
+  t->n = n;
+  t->cu[0] = 0;
+  t->pcu[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    if (cu[i + 1] <= cu[i]) return false;  // every segment has a row
+    const int64_t padded = t->pcu[i] + (static_cast<int64_t>(cu[i + 1] - cu[i]) + 127) / 128 * 128;
+    if (padded >= (int64_t{1} << 31)) return false;
+    t->cu[i + 1] = cu[i + 1];
+    t->pcu[i + 1] = static_cast<int>(padded);
+  }
+  t->rows = cu[n];
+  t->prows = t->pcu[n];
+  return true;
+}
+
+void make_uniform_seg_table(SegTable* t, int N) {
+  const int cu[2] = {0, N};
+  make_seg_table(t, cu, 1);
+}
 
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
   auto fn = encode_fn();
@@ -268,20 +313,18 @@ extern "C" int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const
   if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
       !encode_bhnd_map(&mv, v, s.BH, s.N, s.d))
     return fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
-  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
+  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d)), s.seg};
   Timed t(JATTN_KERNEL_ATTN_FWD, st);
   ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
   return JATTN_OK;
 }
 
-extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
-                         const float* gk, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse,
-                         void* stream) {
-  if (!q || !k || !v || !gq || !gk || !out || !lse) return JATTN_ERR_INVALID_ARG;
-  Shape s;
-  int rc = check_shape(B, H, N_img, N_txt, d, &s);
-  if (rc != JATTN_OK) return rc;
+namespace {
+
+// The forward for a validated shape (either layout).
+int fwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+             const float* gk, jattn_bf16* out, float* lse, void* stream) {
   const void* ptrs[] = {q, k, v, gq, gk, out, lse};
   for (const void* p : ptrs)
     if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
@@ -314,7 +357,7 @@ extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
              !encode_bhnd_map(&mv, v, s.BH, s.N, s.d)) {
     status = fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   } else {
-    AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
+    AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d)), s.seg};
     Timed t(JATTN_KERNEL_ATTN_FWD, st);
     ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
     if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
@@ -324,15 +367,34 @@ extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   return status;
 }
 
-extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
-                         const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
-                         jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, int B, int H,
-                         int N_img, int N_txt, int d, void* stream) {
-  if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !dq || !dk || !dv || !dgq || !dgk)
-    return JATTN_ERR_INVALID_ARG;
+}  // namespace
+
+extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                         const float* gk, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse,
+                         void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse) return JATTN_ERR_INVALID_ARG;
   Shape s;
   int rc = check_shape(B, H, N_img, N_txt, d, &s);
   if (rc != JATTN_OK) return rc;
+  return fwd_body(s, q, k, v, gq, gk, out, lse, stream);
+}
+
+extern "C" int jattn_fwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                                const float* gk, const int* cu_seqlens, int n_seqs, int H, int d, jattn_bf16* out,
+                                float* lse, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape_varlen(cu_seqlens, n_seqs, H, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return fwd_body(s, q, k, v, gq, gk, out, lse, stream);
+}
+
+namespace {
+
+// The backward for a validated shape (either layout).
+int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+             const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq,
+             jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, void* stream) {
   const void* ptrs[] = {q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk};
   for (const void* p : ptrs)
     if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
@@ -351,7 +413,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = dev_err_ptr();
   if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
-  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d))};
+  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d)), s.seg};
   const int nparts_q = q_norm_bwd_parts(s.d);
   const int nparts_k = attn_bwd_dgk_parts(as);
   Carve cv;
@@ -361,8 +423,8 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   uint16_t* khat = cv.take<uint16_t>(s.elems);
   float* rq = cv.take<float>(s.rows);
   float* rk = cv.take<float>(s.rows);
-  float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
-  float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.n_pad);
+  float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
+  float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
   float* dqacc = cv.take<float>(s.elems);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
   float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
@@ -373,8 +435,8 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   CUtensorMap mq, mk, mv, mdo;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_tickets, s.BH, s.N,
-                         s.n_pad, s.d, err, st);
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_tickets, s.BH,
+                         s.seg, s.d, err, st);
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
@@ -403,6 +465,32 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   ce = cudaFreeAsync(cv.base, st);
   if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "cudaFreeAsync", ce);
   return status;
+}
+
+}  // namespace
+
+extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                         const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
+                         jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, int B, int H,
+                         int N_img, int N_txt, int d, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !dq || !dk || !dv || !dgq || !dgk)
+    return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, stream);
+}
+
+extern "C" int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                                const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
+                                jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk,
+                                const int* cu_seqlens, int n_seqs, int H, int d, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !dq || !dk || !dv || !dgq || !dgk)
+    return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape_varlen(cu_seqlens, n_seqs, H, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, stream);
 }
 
 extern "C" int jattn_last_device_error(void* stream) {

@@ -32,6 +32,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 
+// Rows of every head split into segments that attend only within
+// themselves.  A [B, H, N, d] call is B*H heads of one segment [0, N); a
+// packed variable-length call is H heads of T = sum of the sequence lengths
+// rows with one segment per sequence.  Segment s holds the head's rows
+// [cu[s], cu[s+1]); in the 128-row-padded per-head scratch (-LSE log2 e and
+// D for the attention backward) it starts at pcu[s], so pcu[s+1] - pcu[s] is
+// 128 times the segment's number of 128-row tiles.
+constexpr int kMaxSegments = 256;
+struct SegTable {
+  int n;      // segments per head (1 .. kMaxSegments)
+  int rows;   // rows per head
+  int prows;  // padded rows per head (pcu[n])
+  int cu[kMaxSegments + 1];
+  int pcu[kMaxSegments + 1];
+};
+// Fills t from n + 1 row offsets (cu[0] = 0, strictly increasing); false if
+// they are not valid or n is out of range.
+bool make_seg_table(SegTable* t, const int* cu, int n);
+// One segment of N rows (the [B, H, N, d] layout).
+void make_uniform_seg_table(SegTable* t, int N);
+
 // Scratch of one call, carved from one stream-ordered allocation.
 struct Scratch {
   uint16_t* qhat = nullptr;  // [BH, N, d] bf16
@@ -51,12 +72,13 @@ struct Scratch {
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                                uint16_t* qhat, uint16_t* khat, int64_t rows, int d, uint32_t* dev_err,
                                cudaStream_t st);
-// Rows are (bh, n) with n < N; nlse2 (= -LSE log2 e) and delta are written
-// for n < n_pad (= N rounded up to 128), with -inf / 0 in the pad rows.
+// Rows are the BH heads' seg.rows rows; nlse2 (= -LSE log2 e) and delta are
+// written in the per-head padded layout (segment s from seg.pcu[s], 128-row
+// multiples), with -inf / 0 in the pad rows.
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
-                            unsigned int* tickets, int BH, int N, int n_pad, int d, uint32_t* dev_err,
+                            unsigned int* tickets, int BH, const SegTable& seg, int d, uint32_t* dev_err,
                             cudaStream_t st);
 // nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq partials.
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
@@ -75,10 +97,11 @@ int device_sm_count();
 
 // --- tensor-core attention kernels ------------------------------------------
 struct AttnShape {
-  int BH;
-  int N;
+  int BH;        // heads (B*H, or H for a packed variable-length call)
+  int N;         // rows per head
   int d;
-  float scale;  // 1/sqrt(d)
+  float scale;   // 1/sqrt(d)
+  SegTable seg;  // the heads' segments (one segment [0, N) for the [B, H, N, d] layout)
 };
 
 cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,

@@ -231,18 +231,20 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
   }
 }
 
-// Backward preparation, one pass over the padded rows (bh, n), n < n_pad:
-// for n < N it writes q_hat, k_hat, 1/rms of q and k, D = rowsum(dout * out),
-// minus LSE in the log2 domain and a zeroed fp32 dq accumulator row; pad rows
-// get -LSE = -inf and D = 0 so the attention backward sees zero probabilities.
-// Each thread loads its next row while it transforms the current one.
+// Backward preparation, one pass over the padded rows (bh, p) of the heads'
+// segment-padded layout: a padded row of a segment's first len rows is the
+// segment's row t, for which it writes q_hat, k_hat, 1/rms of q and k,
+// D = rowsum(dout * out), minus LSE in the log2 domain and a zeroed fp32 dq
+// accumulator row; pad rows get -LSE = -inf and D = 0 so the attention
+// backward sees zero probabilities.  Each thread loads its next row while it
+// transforms the current one.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
     float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, float4* __restrict__ dqacc,
-    unsigned int* __restrict__ tickets, int n_tickets, int N, int n_pad, int64_t padded_rows) {
+    unsigned int* __restrict__ tickets, int n_tickets, const __grid_constant__ SegTable seg, int64_t padded_rows) {
   griddep_launch_dependents();
   griddep_wait();
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < n_tickets) tickets[threadIdx.x] = 0u;
@@ -261,11 +263,18 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
   };
   auto locate = [&](int64_t b, int64_t& prow, int64_t& row, bool& in_range, bool& valid) {
     prow = b + threadIdx.x / TPR;
-    const int64_t bh = prow / n_pad;
-    const int n = static_cast<int>(prow - bh * n_pad);
+    const int64_t bh = prow / seg.prows;
+    const int p = static_cast<int>(prow - bh * seg.prows);
+    int lo = 0, hi = seg.n;  // seg.pcu[lo] <= p < seg.pcu[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seg.pcu[mid] <= p) lo = mid;
+      else hi = mid;
+    }
+    const int t = seg.cu[lo] + (p - seg.pcu[lo]);
     in_range = prow < padded_rows;
-    valid = in_range && n < N;
-    row = bh * N + n;
+    valid = in_range && t < seg.cu[lo + 1];
+    row = bh * seg.rows + t;
   };
   auto load = [&](int64_t b, Row& w) {
     int64_t prow, row;
@@ -497,15 +506,15 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
-                            unsigned int* tickets, int BH, int N, int n_pad, int d, uint32_t* dev_err,
+                            unsigned int* tickets, int BH, const SegTable& seg, int d, uint32_t* dev_err,
                             cudaStream_t st) {
   (void)dev_err;
-  const int64_t padded_rows = static_cast<int64_t>(BH) * n_pad;
+  const int64_t padded_rows = static_cast<int64_t>(BH) * seg.prows;
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
   auto kernel = d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>;
   return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
                     gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
-                    rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets, dg_reduce_tickets(d), N, n_pad,
+                    rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets, dg_reduce_tickets(d), seg,
                     padded_rows);
 }
 

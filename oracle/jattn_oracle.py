@@ -202,6 +202,34 @@ def joint_attention_streams(q_txt, k_txt, v_txt, q_img, k_img, v_img, gq, gk, ep
     return O[:, :, :n_txt], O[:, :, n_txt:], lse
 
 
+def joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu_seqlens, eps: float = EPS, round_qk: bool = True):
+    """Packed sequences of different lengths (re-diffusion README: the
+    aspect-bucketed training data, and multi-resolution training on its
+    roadmap): every sequence is its own joint-attention problem.
+
+    Inputs are [H, T, d]; sequence s is rows cu_seqlens[s] .. cu_seqlens[s+1]-1
+    of every head.  Each sequence goes through ``joint_attention_bwd`` as a
+    batch of one; the gain gradients sum over the sequences.  Returns the same
+    keys with O, dq, dk, dv [H, T, d] and LSE [H, T].
+    """
+    q, k, v, dout = _as64(q), _as64(k), _as64(v), _as64(dout)
+    H, T, d = q.shape
+    cu = [int(c) for c in cu_seqlens]
+    if cu[0] != 0 or cu[-1] != T or any(b <= a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0, end at T and increase strictly")
+    out = {"O": np.zeros_like(v), "LSE": np.zeros((H, T)), "dq": np.zeros_like(q), "dk": np.zeros_like(k),
+           "dv": np.zeros_like(v), "dgq": np.zeros(d), "dgk": np.zeros(d)}
+    for a, b in zip(cu, cu[1:]):
+        r = joint_attention_bwd(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], gq, gk, dout[None, :, a:b],
+                                eps=eps, round_qk=round_qk)
+        for key in ("O", "dq", "dk", "dv"):
+            out[key][:, a:b] = r[key][0]
+        out["LSE"][:, a:b] = r["LSE"][0]
+        out["dgq"] += r["dgq"]
+        out["dgk"] += r["dgk"]
+    return out
+
+
 def attention_one_row(q_row, K, V, gq, gk, eps: float = EPS, round_qk: bool = True):
     """O and LSE of a single query row against the full key/value set of its head.
 

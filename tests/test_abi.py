@@ -1,6 +1,8 @@
 """The C ABI library: builds, loads, exports every declared symbol, and rejects
 bad arguments before touching the GPU (these calls never reach CUDA, so they
 run on a machine without one)."""
+import ctypes
+
 import pytest
 
 import joint_attention_gb300 as ja
@@ -93,6 +95,52 @@ def test_fwd_validation(lib, kw, expect):
 ])
 def test_bwd_validation(lib, kw, expect):
     assert bwd(lib, **kw) == STATUS_CODE[expect]
+
+
+def fwd_varlen(lib, cu=(0, 24, 40), H=2, d=64, **kw):
+    p = dict(q=A, k=A + 0x1000000, v=A + 0x2000000, gq=A + 0x3000000, gk=A + 0x3001000, out=A + 0x4000000,
+             lse=A + 0x5000000)
+    p.update(kw)
+    arr = (ctypes.c_int * len(cu))(*cu)
+    return lib.jattn_fwd_varlen(p["q"], p["k"], p["v"], p["gq"], p["gk"], arr, len(cu) - 1, H, d, p["out"],
+                                p["lse"], None)
+
+
+def bwd_varlen(lib, cu=(0, 24, 40), H=2, d=64, **kw):
+    p = dict(q=A, k=A + 0x1000000, v=A + 0x2000000, gq=A + 0x3000000, gk=A + 0x3001000, out=A + 0x4000000,
+             lse=A + 0x5000000, dout=A + 0x6000000, dq=A + 0x7000000, dk=A + 0x8000000, dv=A + 0x9000000,
+             dgq=A + 0xA000000, dgk=A + 0xA001000)
+    p.update(kw)
+    arr = (ctypes.c_int * len(cu))(*cu)
+    return lib.jattn_bwd_varlen(p["q"], p["k"], p["v"], p["gq"], p["gk"], p["out"], p["lse"], p["dout"], p["dq"],
+                                p["dk"], p["dv"], p["dgq"], p["dgk"], arr, len(cu) - 1, H, d, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), "JATTN_ERR_INVALID_ARG"),
+    (dict(cu=(0,)), "JATTN_ERR_INVALID_ARG"),                # no sequence
+    (dict(cu=(1, 24)), "JATTN_ERR_INVALID_ARG"),             # does not start at 0
+    (dict(cu=(0, 24, 24, 40)), "JATTN_ERR_INVALID_ARG"),     # an empty sequence
+    (dict(cu=(0, 30, 20)), "JATTN_ERR_INVALID_ARG"),         # decreasing
+    (dict(cu=tuple(range(258))), "JATTN_ERR_UNSUPPORTED"),   # 257 sequences
+    (dict(H=0), "JATTN_ERR_INVALID_ARG"),
+    (dict(d=96), "JATTN_ERR_UNSUPPORTED"),
+    (dict(cu=(0, 1 << 30), H=4), "JATTN_ERR_INVALID_ARG"),   # H*T*d overflows
+    (dict(v=A + 0x2000004), "JATTN_ERR_MISALIGNED"),
+    (dict(out=A + 0x1000000), "JATTN_ERR_ALIAS"),            # out == k
+])
+def test_fwd_varlen_validation(lib, kw, expect):
+    assert fwd_varlen(lib, **kw) == STATUS_CODE[expect]
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dout=None), "JATTN_ERR_INVALID_ARG"),
+    (dict(cu=(0, 5, 3)), "JATTN_ERR_INVALID_ARG"),
+    (dict(d=32), "JATTN_ERR_UNSUPPORTED"),
+    (dict(dq=A), "JATTN_ERR_ALIAS"),                         # dq == q
+])
+def test_bwd_varlen_validation(lib, kw, expect):
+    assert bwd_varlen(lib, **kw) == STATUS_CODE[expect]
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):

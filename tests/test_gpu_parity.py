@@ -290,3 +290,59 @@ def test_q_hat_k_hat_rounding_at_bf16_midpoints(ja, d):
     ref = oracle.joint_attention_bwd(q, k, inp.v, gq, gk, inp.dout)
     check_fwd(got, ref, "midpoints")
     check_bwd(got, ref, where="midpoints")
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length sequences ([H, T, d], sequence s = rows cu[s] ..
+# cu[s+1]-1 of every head)
+# ---------------------------------------------------------------------------
+def run_gpu_varlen(ja, q, k, v, gq, gk, dout, cu):
+    tq, tk, tv, tgq, tgk = dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_f32(gq), dev_f32(gk)
+    out, lse = ja.forward_varlen(tq, tk, tv, tgq, tgk, cu)
+    dq, dk, dv, dgq, dgk = ja.backward_varlen(tq, tk, tv, tgq, tgk, out, lse, dev_bf16(dout), cu)
+    torch.cuda.synchronize()
+    assert ja.jattn_last_device_error() == 0
+    return {key: np64(t) for key, t in dict(O=out, LSE=lse, dq=dq, dk=dk, dv=dv, dgq=dgq, dgk=dgk).items()}
+
+
+def packed_inputs(lens, H, d, seed):
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    inp = make_inputs(1, H, cu[-1], d, seed=seed)
+    return cu, inp.q[0], inp.k[0], inp.v[0], inp.dout[0], inp.gq, inp.gk
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("lens", [
+    (1101, 333, 24),               # the d = 64 workloads' joint lengths in one call
+    (1, 129, 256, 77, 1, 300),     # single rows, ragged and tile-exact lengths
+    (2381,),                       # one sequence (the 768 px length)
+])
+def test_varlen_matches_oracle(ja, lens, d):
+    cu, q, k, v, dout, gq, gk = packed_inputs(lens, 2, d, seed=500 + len(lens) + d)
+    got = run_gpu_varlen(ja, q, k, v, gq, gk, dout, cu)
+    ref = oracle.joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu)
+    where = f"varlen {lens} d={d}"
+    check_fwd(got, ref, where)
+    check_bwd(got, ref, where=where)
+
+
+def test_varlen_of_equal_lengths_equals_the_batched_layout(ja):
+    """B sequences of one length L packed as [H, B*L, d] and the same data as
+    [B, H, L, d]: the kernels walk the same tiles in the same order, so O, LSE,
+    dk and dv agree bit for bit; dq (fp32 reduce-adds in arrival order) and
+    the gain gradients (partials summed in another grouping) agree to
+    rounding."""
+    B, H, L, d = 3, 2, 333, 64
+    inp = make_inputs(B, H, L, d, seed=601)
+    batched = run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, 77)
+    pack = lambda a: np.ascontiguousarray(np.transpose(a, (1, 0, 2, 3)).reshape(H, B * L, d))  # noqa: E731
+    cu = [i * L for i in range(B + 1)]
+    packed = run_gpu_varlen(ja, pack(inp.q), pack(inp.k), pack(inp.v), inp.gq, inp.gk, pack(inp.dout), cu)
+    for name in ("O", "dk", "dv"):
+        assert np.array_equal(packed[name], pack(batched[name])), name
+    assert np.array_equal(packed["LSE"], np.transpose(batched["LSE"], (1, 0, 2)).reshape(H, B * L))
+    assert relF(packed["dq"], pack(batched["dq"])) < 1e-2
+    for name in ("dgq", "dgk"):
+        assert relF(packed[name], batched[name]) < 1e-5, name

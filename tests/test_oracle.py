@@ -220,6 +220,51 @@ def test_oracle_matches_torch_float64(B, H, N, d, seed, round_qk):
         assert relF(ours[key], ref[key]) < 1e-12, key
 
 
+def torch_reference_block_diagonal(q, k, v, gq, gk, dout, cu, eps=jo.EPS):
+    """Packed sequences as one attention over all T rows with a block-diagonal
+    boolean mask (torch float64, SDPA math path, autograd): an independent
+    formulation of the per-sequence split."""
+    t = lambda a: torch.tensor(np.asarray(a, np.float64)[None], requires_grad=True)  # noqa: E731
+    tq, tk, tv = t(q), t(k), t(v)
+    tgq = torch.tensor(np.asarray(gq, np.float64), requires_grad=True)
+    tgk = torch.tensor(np.asarray(gk, np.float64), requires_grad=True)
+    d, T = q.shape[-1], q.shape[1]
+    seg = np.zeros(T, dtype=np.int64)
+    for s_, (a, b) in enumerate(zip(cu, cu[1:])):
+        seg[a:b] = s_
+    mask = torch.tensor(seg[:, None] == seg[None, :])
+    # No bf16 step: the rounding is pinned on its own; this pins the split.
+    qh = F.rms_norm(tq, (d,), weight=tgq, eps=eps)
+    kh = F.rms_norm(tk, (d,), weight=tgk, eps=eps)
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    with sdpa_kernel(SDPBackend.MATH):
+        O = F.scaled_dot_product_attention(qh, kh, tv, attn_mask=mask, scale=1.0 / math.sqrt(d))
+    S = (qh @ kh.transpose(-1, -2)) / math.sqrt(d)
+    lse = torch.logsumexp(S.masked_fill(~mask, float("-inf")), dim=-1)
+    (O * torch.tensor(np.asarray(dout, np.float64)[None])).sum().backward()
+    return {"O": O.detach().numpy()[0], "LSE": lse.detach().numpy()[0], "dq": tq.grad.numpy()[0],
+            "dk": tk.grad.numpy()[0], "dv": tv.grad.numpy()[0], "dgq": tgq.grad.numpy(), "dgk": tgk.grad.numpy()}
+
+
+@pytest.mark.parametrize("cu,d", [([0, 24, 25, 70, 203], 64), ([0, 7, 140], 128), ([0, 1], 64)])
+def test_varlen_oracle_matches_block_diagonal_masked_attention(cu, d):
+    rng = np.random.default_rng(len(cu) * 100 + d)
+    H, T = 2, cu[-1]
+    q, k, v, dout = (rng.standard_normal((H, T, d)) for _ in range(4))
+    gq, gk = rng.uniform(0.5, 1.5, d), rng.uniform(0.5, 1.5, d)
+    ours = oracle.joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu, round_qk=False)
+    ref = torch_reference_block_diagonal(q, k, v, gq, gk, dout, cu)
+    for key in ("O", "LSE", "dq", "dk", "dv", "dgq", "dgk"):
+        assert relF(ours[key], ref[key]) < 1e-12, key
+
+
+def test_varlen_oracle_rejects_bad_offsets():
+    q = np.zeros((1, 5, 4))
+    for cu in ([1, 5], [0, 3, 3, 5], [0, 4]):
+        with pytest.raises(ValueError):
+            oracle.joint_attention_varlen_bwd(q, q, q, np.ones(4), np.ones(4), q, cu)
+
+
 @pytest.mark.parametrize("name", ["tiny", "256px"])
 def test_oracle_matches_torch_on_workloads(name):
     inp = make_config_inputs(CONFIGS[name])
