@@ -307,6 +307,42 @@ def per_config_throughput(ja, torch, dev, stream, steps=10, warmup=3):
             row["images_equiv_per_s"] = B / (12 * ms * 1e-3)
         res[name] = row
         del t, out, lse, dq, dk, dv
+    # Packed variable-length call (jattn_fwd_varlen / jattn_bwd_varlen): the 512 px and 256 px joint
+    # lengths mixed in one call, 8 x 1101 + 16 x 333 rows per head, H = 12, d = 64.
+    lens = [1101] * 8 + [333] * 16
+    H, d = 12, 64
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    T = cu[-1]
+    gen.manual_seed(2000)
+    t = {key: torch.randn((H, T, d), generator=gen, device=dev).to(torch.bfloat16) for key in ("q", "k", "v", "dout")}
+    gq = torch.rand(d, generator=gen, device=dev) + 0.5
+    gk = torch.rand(d, generator=gen, device=dev) + 0.5
+    out, lse = torch.empty_like(t["q"]), torch.empty((H, T), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
+
+    def one_varlen():
+        ja.jattn_fwd_varlen(t["q"], t["k"], t["v"], gq, gk, cu, H, d, out, lse, stream)
+        ja.jattn_bwd_varlen(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], dq, dk, dv, dgq, dgk, cu, H, d,
+                            stream)
+
+    for _ in range(warmup):
+        one_varlen()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one_varlen()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    fl = sum(flops_fwd(1, H, n, d) + flops_bwd(1, H, n, d) for n in lens)
+    res["varlen_mix"] = {"mode": "fwd+bwd, packed sequences", "sequences": "8 x 1101 + 16 x 333", "H": H, "T": T,
+                         "d": d, "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                         "images_equiv_per_s": len(lens) / (12 * ms * 1e-3)}
+    del t, out, lse, dq, dk, dv
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the per-config pass")
     return res
