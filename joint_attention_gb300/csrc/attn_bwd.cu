@@ -142,6 +142,27 @@ struct BwdUnit {
   __device__ __forceinline__ int kv0() const { return row0 + 128 * j; }  // first key row
 };
 
+// The [B, H, N, d] layout: one segment [0, N) per head, decoded without the
+// segment table.
+struct BwdWorkUniform {
+  int upc;    // 128-row tiles per head
+  int units;  // heads * upc
+  struct {
+    int rows, prows;
+  } seg;
+  __device__ __forceinline__ BwdUnit unit(int u) const {
+    BwdUnit r;
+    r.bh = u / upc;
+    r.j = u - r.bh * upc;
+    r.nkt = upc;
+    r.row0 = 0;
+    r.end = seg.rows;
+    r.prow0 = 0;
+    return r;
+  }
+};
+
+// Packed variable-length layout: segments from the table.
 struct BwdWork {
   int upc;    // units per head (padded rows per head / 128)
   int units;  // heads * upc
@@ -194,9 +215,9 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-template <int D>
+template <int D, class W>
 __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
-                             const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, const BwdWork& w,
+                             const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, const W& w,
                              const float* nlse2_pad, const float* delta_pad, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(mq);
@@ -320,8 +341,8 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
 // released by a commit from each of its two readers: a Q stage (S, dK), a dO
 // stage (dP, dV), the dS^T tile (dK, dQ) and a K/V buffer (the unit's last
 // dP and last dQ).
-template <int D>
-__device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w,
+template <int D, class W>
+__device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w,
                                   uint32_t* dev_err) {
   using C = BwdCfg<D>;
   volatile int* ab = &bars.abort;
@@ -357,8 +378,8 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
   mbar_wait_drain(&bars.drain[0], 0);
 }
 
-template <int D>
-__device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w,
+template <int D, class W>
+__device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w,
                                   uint32_t* dev_err) {
   using C = BwdCfg<D>;
   volatile int* ab = &bars.abort;
@@ -398,8 +419,8 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
 
 // dQ issuer (d = 64): dQ(t) = dS(t) K once dS^T(t) is in shared memory and
 // dQ(t-1) has been drained from its TMEM columns.
-template <int D>
-__device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, uint32_t* dev_err) {
+template <int D, class W>
+__device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   volatile int* ab = &bars.abort;
   const uint64_t mDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16384, 1024);
@@ -429,8 +450,8 @@ __device__ void bwd_mma_dq(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdW
 // Single-issuer backward (d = 128), per unit: S(0), dP(0), then per tile
 // dV(i), S(i+1), dK(i), dQ(i) (into the dP^T columns), dP(i+1) once dQ(i) is
 // drained.
-template <int D>
-__device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, uint32_t* dev_err) {
+template <int D, class W>
+__device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   volatile int* ab = &bars.abort;
   auto qaddr = [=](int t) { return smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile); };
@@ -511,8 +532,8 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork
 }
 
 // Key-row threads of one compute group (query columns 64g .. 64g+63).
-template <int D>
-__device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, const BwdWork& w, float scale,
+template <int D, class W>
+__device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, const W& w, float scale,
                             uint32_t* dev_err) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -644,8 +665,8 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 // tiles, so that the k, dk and dv rows move with contiguous 512-byte warp
 // accesses, and sums the dgk terms with a warp butterfly; d = 128 works per
 // row and sums through padded staging rows.
-template <int D>
-__device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, float scale,
+template <int D, class W>
+__device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, float scale,
                                    float* __restrict__ dqacc, const __nv_bfloat16* __restrict__ k_raw,
                                    const float* __restrict__ rk, __nv_bfloat16* __restrict__ dk,
                                    __nv_bfloat16* __restrict__ dv, float* __restrict__ dgk_part,
@@ -864,8 +885,8 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
 // it (kv_empty), so that k, dk and dv move with contiguous 512-byte warp
 // accesses and no other role waits on this work except through the TMEM
 // accumulators, released as soon as they are read.
-template <int D>
-__device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, const BwdWork& w, float scale,
+template <int D, class W>
+__device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, float scale,
                                    const __nv_bfloat16* __restrict__ k_raw, const float* __restrict__ rk,
                                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
                                    float* __restrict__ dgk_part, uint32_t* dev_err) {
@@ -1029,11 +1050,11 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
   }
 }
 
-template <int D>
+template <int D, class W>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                    const __grid_constant__ BwdWork w, float scale, const float* __restrict__ nlse2_pad,
+                    const __grid_constant__ W w, float scale, const float* __restrict__ nlse2_pad,
                     const float* __restrict__ delta_pad, const __nv_bfloat16* __restrict__ k_raw,
                     const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, float* __restrict__ dgk_part,
@@ -1128,31 +1149,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+template <int D, class W>
+cudaError_t launch_bwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, const AttnShape& s, const float* nlse2_pad, const float* delta_pad,
+                         const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
+                         float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  static_assert(C::kDynSmem + static_cast<int>(sizeof(BwdBars)) <= 232448, "shared memory budget");
+  auto kernel = attn_bwd_kernel<D, W>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+  if (e != cudaSuccess) return e;
+  // The setmaxnreg split is valid only for the register count it was sized
+  // for; any other build is refused rather than launched.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
+  const int sms = device_sm_count();
+  const int grid = w.units < sms ? w.units : sms;
+  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, w, s.scale, nlse2_pad,
+                    delta_pad, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
+                    reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part,
+                    dev_err);
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const AttnShape& s, const float* nlse2_pad,
                          const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk,
                          uint16_t* dv, float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
-  using C = BwdCfg<D>;
-  static_assert(C::kDynSmem + static_cast<int>(sizeof(BwdBars)) <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
-  if (e != cudaSuccess) return e;
-  // The setmaxnreg split is valid only for the register count it was sized
-  // for; any other build is refused rather than launched.
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<D>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
+  if (s.seg.n == 1) {
+    BwdWorkUniform w;
+    w.seg.rows = s.seg.rows;
+    w.seg.prows = s.seg.prows;
+    w.upc = s.seg.prows / 128;
+    w.units = s.BH * w.upc;
+    return launch_bwd_w<D>(w, mq, mk, mv, mdo, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc, dgk_part,
+                           dev_err, st);
+  }
   BwdWork w;
   w.seg = s.seg;
   w.upc = s.seg.prows / 128;
   w.units = s.BH * w.upc;
-  const int sms = device_sm_count();
-  const int grid = w.units < sms ? w.units : sms;
-  return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, w, s.scale,
-                    nlse2_pad, delta_pad, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
-                    reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part,
-                    dev_err);
+  return launch_bwd_w<D>(w, mq, mk, mv, mdo, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc, dgk_part,
+                         dev_err, st);
 }
 
 }  // namespace

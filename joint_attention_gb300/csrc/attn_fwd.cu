@@ -113,6 +113,28 @@ struct FwdUnit {
   bool has_b;  // tile B has rows
 };
 
+// The [B, H, N, d] layout: one segment [0, N) per head, decoded without the
+// segment table.
+struct FwdWorkUniform {
+  int upc;    // 256-row blocks per head
+  int units;  // heads * upc
+  int nkv;    // 128-key tiles per head
+  struct {
+    int rows;
+  } seg;
+  __device__ __forceinline__ FwdUnit unit(int u) const {
+    FwdUnit r;
+    r.bh = u / upc;
+    r.q0 = (u - r.bh * upc) * 2 * kTileM;
+    r.kvb = 0;
+    r.end = seg.rows;
+    r.nkv = nkv;
+    r.has_b = r.q0 + kTileM < r.end;
+    return r;
+  }
+};
+
+// Packed variable-length layout: segments from the table.
 struct FwdWork {
   int upc;    // units per head
   int units;  // heads * upc
@@ -137,9 +159,9 @@ struct FwdWork {
   }
 };
 
-template <int D>
+template <int D, class W>
 __device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k, const CUtensorMap* map_v,
-                             uint8_t* sm, FwdBars& bars, const FwdWork& w, uint32_t* dev_err) {
+                             uint8_t* sm, FwdBars& bars, const W& w, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   tma_prefetch_desc(map_q);
   tma_prefetch_desc(map_k);
@@ -208,8 +230,8 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 // the same K/V slots; a slot's empty barrier and a Q buffer's empty barrier
 // count one commit per issuer, so the B issuer walks and releases them also
 // for units whose tile B has no rows.
-template <int D>
-__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const FwdWork& w, uint32_t* dev_err) {
+template <int D, class W>
+__device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const W& w, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   const uint32_t ring = smem_u32(sm + C::kOffRing);
   const uint32_t tS = tmem + C::kColS + x * 128;
@@ -317,8 +339,8 @@ __device__ void fwd_mma(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const 
 }
 
 // Softmax / epilogue of one 128-row query tile (x = 0: tile A, 1: tile B).
-template <int D>
-__device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const FwdWork& w, float scale_log2,
+template <int D, class W>
+__device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, const W& w, float scale_log2,
                             const CUtensorMap* map_o, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                             uint32_t* dev_err) {
   using C = FwdCfg<D>;
@@ -338,9 +360,18 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
   for (int u = blockIdx.x; ok && u < w.units; u += gridDim.x) {
   const FwdUnit un = w.unit(u);
   if (x == 1 && !un.has_b) continue;
-  const int bh = un.bh, nkv = un.nkv;
+  // Per-unit values, so that the tile loop keeps few of them live.
+  const int nkv = un.nkv;
   const int qt0 = un.q0 + x * 128;  // the tile's first row
   const int n = qt0 + row;
+  const int nvalid_last = un.end - (un.kvb + (nkv - 1) * kTileN);  // keys of the last key tile
+  const bool live = n < un.end;
+  // The staged tile store writes whole 128-row tiles, clipped only at the
+  // head's last row: a tile that runs past its segment into the next one
+  // stores rows instead.
+  const bool tile_store = C::kStageO && (qt0 + 128 <= un.end || un.end == w.seg.rows);
+  const size_t orow = static_cast<size_t>(un.bh) * rows + (live ? n : 0);  // the row's index in O / LSE
+  const int bh = un.bh;
   float m_ref = -INFINITY;
   float l = 0.f;
   for (int j = 0; j < nkv; ++j) {
@@ -358,7 +389,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
       tc_fence_before();
       mbar_arrive(&bars.s_free[x]);
     }
-    const int nvalid = un.end - (un.kvb + j * kTileN);
+    const int nvalid = j + 1 < nkv ? kTileN : nvalid_last;
     if (nvalid < kTileN) {  // only the ragged last key tile needs the mask
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -453,11 +484,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
   if (!ok) return;
   tc_fence_after();
   const float inv_l = 1.f / l;
-  const bool live = n < un.end;
-  // The staged tile store writes whole 128-row tiles, clipped only at the
-  // head's last row: a tile that runs past its segment into the next one
-  // stores rows instead.
-  if (C::kStageO && (qt0 + 128 <= un.end || un.end == w.seg.rows)) {
+  if (tile_store) {
     // O rows into the query tile's staging tile (128-byte swizzle: 16-byte
     // chunk c of row r at c ^ (r & 7)), then one TMA store of the tile; rows
     // past N fall outside the tensor and are not written.
@@ -492,7 +519,7 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
     }
     ++us;
   } else {
-    uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * rows + (live ? n : 0)) * D);
+    uint4* orow_p = reinterpret_cast<uint4*>(out + orow * D);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -506,23 +533,23 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
           w4.y = pack_bf16x2(__uint_as_float(o[g * 8 + 2]) * inv_l, __uint_as_float(o[g * 8 + 3]) * inv_l);
           w4.z = pack_bf16x2(__uint_as_float(o[g * 8 + 4]) * inv_l, __uint_as_float(o[g * 8 + 5]) * inv_l);
           w4.w = pack_bf16x2(__uint_as_float(o[g * 8 + 6]) * inv_l, __uint_as_float(o[g * 8 + 7]) * inv_l);
-          orow[c * 4 + g] = w4;
+          orow_p[c * 4 + g] = w4;
         }
       }
     }
   }
-  if (live) lse[static_cast<size_t>(bh) * rows + n] = (m_ref + lg2_approx(l)) * kLn2;
+  if (live) lse[orow] = (m_ref + lg2_approx(l)) * kLn2;
   jx += nkv;
   ++uc;
   }
   if (C::kStageO && row == 0) bulk_wait_group0();
 }
 
-template <int D>
+template <int D, class W>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
-                    const __grid_constant__ FwdWork w, float scale_log2,
+                    const __grid_constant__ W w, float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -577,13 +604,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+template <int D, class W>
+cudaError_t launch_fwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  static_assert(C::kDynSmem + static_cast<int>(sizeof(FwdBars)) <= 232448, "shared memory budget");
+  auto kernel = attn_fwd_kernel<D, W>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
+  const int grid = w.units < sms ? w.units : sms;
+  const float scale_log2 = s.scale * 1.4426950408889634f;
+  CUtensorMap mo;  // the output, for the staged tile stores (d = 64)
+  if (!encode_bhnd_map(&mo, out, s.BH, s.N, D)) return cudaErrorInvalidValue;
+  return launch_pdl(kernel, dim3(grid), dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, mo, w, scale_log2,
+                    reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnShape& s,
                          uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
-  using C = FwdCfg<D>;
-  static_assert(C::kDynSmem + static_cast<int>(sizeof(FwdBars)) <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
-  if (e != cudaSuccess) return e;
+  if (s.seg.n == 1) {
+    FwdWorkUniform w;
+    w.seg.rows = s.seg.rows;
+    w.upc = (s.seg.rows + 2 * kTileM - 1) / (2 * kTileM);
+    w.nkv = (s.seg.rows + kTileN - 1) / kTileN;
+    w.units = s.BH * w.upc;
+    return launch_fwd_w<D>(w, mq, mk, mv, s, out, lse, dev_err, st);
+  }
   FwdWork w;
   w.seg = s.seg;
   w.uf[0] = 0;
@@ -591,13 +639,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     w.uf[i + 1] = w.uf[i] + (s.seg.cu[i + 1] - s.seg.cu[i] + 2 * kTileM - 1) / (2 * kTileM);
   w.upc = w.uf[s.seg.n];
   w.units = s.BH * w.upc;
-  const int sms = device_sm_count();
-  const int grid = w.units < sms ? w.units : sms;
-  const float scale_log2 = s.scale * 1.4426950408889634f;
-  CUtensorMap mo;  // the output, for the staged tile stores (d = 64)
-  if (!encode_bhnd_map(&mo, out, s.BH, s.N, D)) return cudaErrorInvalidValue;
-  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, mo, w,
-                    scale_log2, reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
+  return launch_fwd_w<D>(w, mq, mk, mv, s, out, lse, dev_err, st);
 }
 
 }  // namespace
