@@ -173,6 +173,18 @@ def dist_setup():
     return world, rank, local
 
 
+def aggregate_over_ranks(ms_total, steps, fl_step, world, dist=None, device="cpu"):
+    """The job's timed-loop duration (the slowest rank's) and whole-job throughput in TFLOP/s:
+    every rank ran `steps` steps of `fl_step` FLOP on its own replica."""
+    if world > 1:
+        import torch
+
+        t = torch.tensor([ms_total], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    return ms_total, fl_step * steps * world / (ms_total * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(B, H, N, d, seed, budget_s: float, max_heads: int):
     """Times the float64 oracle on whole heads of the workload until budget_s."""
     import numpy as np
@@ -452,13 +464,9 @@ def main():
     prof = ja.profile_snapshot()
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the timed region")
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-    ms_step = ms_total / args.steps
     fl_step = flops_fwd(B, H, N, d) + flops_bwd(B, H, N, d)
-    value = fl_step * args.steps * world / (ms_total * 1e-3) / 1e12
+    ms_total, value = aggregate_over_ranks(ms_total, args.steps, fl_step, world, dist, dev)
+    ms_step = ms_total / args.steps
 
     # ---- end to end: pinned host buffers, copies inside the timed region ----
     # Each step copies its inputs host -> device, runs fwd + bwd through the C ABI and copies
