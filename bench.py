@@ -553,7 +553,6 @@ def main():
         "qk_norm_fwd": ("hbm", 4.0 * B * H * N * d * 2),
         "bwd_prep": ("hbm", B * H * N * d * 2 * 4 + B * H * N * d * 2 * 2 + B * H * N * d * 4 + B * H * N * 4 * 5),
         "q_norm_bwd": ("hbm", B * H * N * d * (4 + 2 + 2) + B * H * N * 4),
-        "dg_reduce": ("hbm", 0.0),
     }
     bound, work = algo[dom]
     avg_s = kern[dom]["avg_us"] * 1e-6

@@ -172,9 +172,8 @@ typedef enum {
   JATTN_KERNEL_ATTN_FWD = 1,     /* tensor-core attention forward */
   JATTN_KERNEL_BWD_PREP = 2,     /* norm recompute + rowsum(dO*O) + dq accumulator clear */
   JATTN_KERNEL_ATTN_BWD = 3,     /* tensor-core attention backward (+ K-norm backward) */
-  JATTN_KERNEL_Q_NORM_BWD = 4,   /* Q-norm backward from the dq accumulator */
-  JATTN_KERNEL_DG_REDUCE = 5,    /* fixed-order reduction of the gain gradients */
-  JATTN_KERNEL_COUNT = 6
+  JATTN_KERNEL_Q_NORM_BWD = 4,   /* Q-norm backward from the dq accumulator, and the gain gradients */
+  JATTN_KERNEL_COUNT = 5
 } jattn_kernel_kind;
 
 int jattn_profile_enable(int on);

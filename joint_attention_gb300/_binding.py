@@ -86,7 +86,7 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     return lib
 
 
-KERNEL_KINDS = 6
+KERNEL_KINDS = 5
 
 
 def jattn_profile_enable(on: bool = True) -> int:

@@ -207,6 +207,7 @@ struct BwdBars {
   // and D (0 past N), copied in with the tile from padded scratch rows.
   __align__(16) float gk[128];  // K-RMSNorm gain (d entries)
   __align__(16) float wsum[4][64];  // d = 64 epilogue: per-warp dgk column sums
+  float dgk_cta[128];               // this CTA's dgk partial, summed over its units in unit order
   __align__(16) float nlse2[3][128];
   __align__(16) float delta[3][128];
 };
@@ -866,12 +867,17 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
             s2 += col[(q + 2) * kRowFloats];
             s3 += col[(q + 3) * kRowFloats];
           }
-          dgk_part[static_cast<size_t>(u) * D + pass * C::kDQCols + r128] = (s0 + s1) + (s2 + s3);
+          bars.dgk_cta[pass * C::kDQCols + r128] += (s0 + s1) + (s2 + s3);
         }
         if (!(ok = epi_sync())) break;  // every column summed before the rows are rewritten
       }
       if (!ok) break;
     }
+  }
+  if (!kTiled && r128 < C::kDQCols) {
+#pragma unroll
+    for (int pass = 0; pass < D / C::kDQCols; ++pass)
+      dgk_part[static_cast<size_t>(blockIdx.x) * D + pass * C::kDQCols + r128] = bars.dgk_cta[pass * C::kDQCols + r128];
   }
   bulk_wait_group0();
 }
@@ -1029,8 +1035,7 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     }
     if (!(ok = epi_sync())) break;  // dk tile, dv tile and warp sums complete
     if (r128 < D)
-      dgk_part[static_cast<size_t>(u) * D + r128] =
-          ((bars.wsum[0][r128] + bars.wsum[1][r128]) + bars.wsum[2][r128]) + bars.wsum[3][r128];
+      bars.dgk_cta[r128] += ((bars.wsum[0][r128] + bars.wsum[1][r128]) + bars.wsum[2][r128]) + bars.wsum[3][r128];
     // dk and dv tiles out, 32 consecutive 16-byte chunks per warp access.
     uint4* dkdst = reinterpret_cast<uint4*>(dk + tile_off);
     uint4* dvdst = reinterpret_cast<uint4*>(dv + tile_off);
@@ -1048,6 +1053,7 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     if (!(ok = epi_sync())) break;  // tiles read (and wsum free)
     if (r128 == 0) mbar_arrive(&bars.kv_empty[b]);
   }
+  if (r128 < D) dgk_part[static_cast<size_t>(blockIdx.x) * D + r128] = bars.dgk_cta[r128];
 }
 
 template <int D, class W>
@@ -1106,7 +1112,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_relinquish();
   }
   griddep_wait();  // the previous grid's writes (q_hat, k_hat, LSE / D rows, zeroed dQ) are visible
-  for (int c = threadIdx.x; c < D; c += blockDim.x) bars.gk[c] = gk[c];
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    bars.gk[c] = gk[c];
+    bars.dgk_cta[c] = 0.f;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1197,7 +1206,12 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 
 }  // namespace
 
-int attn_bwd_dgk_parts(const AttnShape& s) { return s.BH * (s.seg.prows / 128); }
+// One dgk partial per CTA (the grid: one CTA per SM, no more than units).
+int attn_bwd_dgk_parts(const AttnShape& s) {
+  const int units = s.BH * (s.seg.prows / 128);
+  const int sms = device_sm_count();
+  return units < sms ? units : sms;
+}
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, const AttnShape& s, const float* nlse2_pad,

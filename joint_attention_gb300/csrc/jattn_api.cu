@@ -201,8 +201,7 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
   b += 2 * (static_cast<size_t>(s.BH) * s.seg.prows * 4 + 256);   // nlse2, delta
   b += s.elems * 4 + 256;                                         // dq accumulator
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
-  b += static_cast<size_t>(dg_reduce_scratch_floats(s.d)) * 4 + 256;  // dg slice partials
-  b += static_cast<size_t>(dg_reduce_tickets(s.d)) * 4 + 256;         // dg tickets
+  b += 4 + 256;                                                   // dg ticket
   return b + 256;
 }
 
@@ -428,14 +427,13 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   float* dqacc = cv.take<float>(s.elems);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
   float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
-  float* dg_slices = cv.take<float>(static_cast<size_t>(dg_reduce_scratch_floats(s.d)));
-  unsigned int* dg_tickets = cv.take<unsigned int>(static_cast<size_t>(dg_reduce_tickets(s.d)));
+  unsigned int* dg_ticket = cv.take<unsigned int>(1);
 
   int status = JATTN_OK;
   CUtensorMap mq, mk, mv, mdo;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_tickets, s.BH,
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_ticket, s.BH,
                          s.seg, s.d, err, st);
   }
   if (ce != cudaSuccess) {
@@ -452,13 +450,8 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
     if (ce == cudaSuccess) {
       stage = "q_norm_bwd launch";
       Timed t(JATTN_KERNEL_Q_NORM_BWD, st);
-      ce = launch_q_norm_bwd(dqacc, q, rq, gq, as.scale, dq, dgq_part, nparts_q, static_cast<int64_t>(s.rows), s.d,
-                             err, st);
-    }
-    if (ce == cudaSuccess) {
-      stage = "dg_reduce launch";
-      Timed t(JATTN_KERNEL_DG_REDUCE, st);
-      ce = launch_dg_reduce(dgq_part, nparts_q, dgk_part, nparts_k, s.d, dg_slices, dg_tickets, dgq, dgk, st);
+      ce = launch_q_norm_bwd(dqacc, q, rq, gq, as.scale, dq, dgq_part, nparts_q, static_cast<int64_t>(s.rows),
+                             dgk_part, nparts_k, dg_ticket, dgq, dgk, s.d, err, st);
     }
     if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, stage, ce);
   }
@@ -559,7 +552,6 @@ extern "C" const char* jattn_kernel_name(int kind) {
     case JATTN_KERNEL_BWD_PREP: return "bwd_prep";
     case JATTN_KERNEL_ATTN_BWD: return "attn_bwd";
     case JATTN_KERNEL_Q_NORM_BWD: return "q_norm_bwd";
-    case JATTN_KERNEL_DG_REDUCE: return "dg_reduce";
     default: return "unknown";
   }
 }

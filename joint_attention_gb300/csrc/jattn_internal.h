@@ -80,17 +80,13 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
                             unsigned int* tickets, int BH, const SegTable& seg, int d, uint32_t* dev_err,
                             cudaStream_t st);
-// nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq partials.
+// nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq
+// partials; the last one (by *ticket, zeroed by the backward preparation)
+// sums them and the nk dgk partials into dgq and dgk.
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
-                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, uint32_t* dev_err,
+                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, const float* dgk_part, int nk,
+                              unsigned int* ticket, float* dgq, float* dgk, int d, uint32_t* dev_err,
                               cudaStream_t st);
-// Gain-gradient reduction: slice_part holds dg_reduce_scratch_floats(d)
-// floats, tickets dg_reduce_tickets(d) counters that the backward
-// preparation kernel zeroes.
-cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* slice_part,
-                             unsigned int* tickets, float* dgq, float* dgk, cudaStream_t st);
-int dg_reduce_scratch_floats(int d);
-int dg_reduce_tickets(int d);
 int q_norm_bwd_parts(int d);
 // Streaming multiprocessors of the current device (cached after the first call).
 int device_sm_count();

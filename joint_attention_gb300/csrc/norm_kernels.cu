@@ -21,7 +21,6 @@ namespace jattn {
 namespace {
 
 constexpr float kEps = 1e-6f;
-constexpr int kDgSlices = 16;
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -179,6 +178,9 @@ __device__ __forceinline__ uint4 norm_chunk(const uint4 w, const float (&g)[8], 
 
 // --- streaming kernels -------------------------------------------------------
 constexpr int kNormThreads = 256;
+// The dq kernel runs one 1024-thread block per SM: few dgq partials, and
+// 1024 / d threads per column for their final sum.
+constexpr int kQBwdThreads = 1024;
 
 // q, k -> q_hat, k_hat (bf16).  Rows [0, rows) are q rows, [rows, 2 rows) k
 // rows; each thread takes kU rows per pass and loads the next pass's rows
@@ -330,19 +332,25 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
   }
 }
 
-// dq from the fp32 accumulator of dS k_hat (times `scale`), plus per-block
-// partial sums of dgq.  Each block writes partial[blockIdx.x][d]; the grid
-// size is fixed, so the reduction order is fixed.  Each thread loads its next
-// row while it transforms the current one.
+// dq from the fp32 accumulator of dS k_hat (times `scale`), and the gain
+// gradients.  Each block writes its dgq partial to partial[blockIdx.x][d];
+// the last block to finish (an atomic ticket, zeroed by the backward
+// preparation) then sums every block's dgq partial and the attention
+// backward's nk dgk partials, each in index order, into dgq and dgk.  The
+// grid size is fixed, so the reduction order is fixed.  Each thread loads its
+// next row while it transforms the current one.
 template <int D>
-__global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* __restrict__ dqacc,
+__global__ void __launch_bounds__(kQBwdThreads) q_norm_bwd_kernel(const float4* __restrict__ dqacc,
                                                                   const uint4* __restrict__ q,
                                                                   const float* __restrict__ rq,
                                                                   const float* __restrict__ gq, float scale,
                                                                   uint4* __restrict__ dq,
-                                                                  float* __restrict__ partial, int64_t rows) {
+                                                                  float* __restrict__ partial, int64_t rows,
+                                                                  const float* __restrict__ part_k, int nk,
+                                                                  unsigned int* __restrict__ ticket,
+                                                                  float* __restrict__ dgq, float* __restrict__ dgk) {
   constexpr int TPR = D / 8;
-  constexpr int RPB = kNormThreads / TPR;
+  constexpr int RPB = kQBwdThreads / TPR;
   const int sub = threadIdx.x % TPR;
   griddep_launch_dependents();
   griddep_wait();
@@ -395,7 +403,7 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
     cur = nxt;
   }
   // Block reduction of acc over the RPB row slots (fixed order).
-  __shared__ float red[kNormThreads / TPR][D];
+  __shared__ float red[kQBwdThreads / TPR][D];
   const int slot = threadIdx.x / TPR;
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[slot][sub * 8 + i] = acc[i];
@@ -405,58 +413,47 @@ __global__ void __launch_bounds__(kNormThreads) q_norm_bwd_kernel(const float4* 
     for (int w = 0; w < RPB; ++w) t += red[w][c];
     partial[static_cast<size_t>(blockIdx.x) * D + c] = t;
   }
-}
-
-// Fixed-order reduction of the gain-gradient partials in one launch.
-// blockIdx.z selects dgq (0) or dgk (1), blockIdx.x a group of 32 columns,
-// blockIdx.y one of kDgSlices contiguous slices of the partial rows.  Each
-// block sums its slice (thread (x, y) takes rows y, y + 8, ...; the 8 row
-// lanes are then added in index order) into slice_part; the last block to
-// finish a (array, column group) - found with an atomic ticket - adds the
-// slices in index order.  Same grid, same order, every call; the tickets are
-// zeroed by the backward preparation kernel and reset here.
-__global__ void __launch_bounds__(256) dg_reduce_kernel(const float* __restrict__ part_q, int nq,
-                                                        const float* __restrict__ part_k, int nk, int d,
-                                                        float* __restrict__ slice_part,
-                                                        unsigned int* __restrict__ tickets, float* __restrict__ dgq,
-                                                        float* __restrict__ dgk) {
-  __shared__ float lanes[8][33];
   __shared__ bool last;
-  griddep_launch_dependents();
-  griddep_wait();
-  const int arr = blockIdx.z;
-  const float* part = arr == 0 ? part_q : part_k;
-  const int nparts = arr == 0 ? nq : nk;
-  const int c = blockIdx.x * 32 + threadIdx.x;
-  const int s = blockIdx.y;
-  const int r0 = static_cast<int>((static_cast<int64_t>(nparts) * s) / kDgSlices);
-  const int r1 = static_cast<int>((static_cast<int64_t>(nparts) * (s + 1)) / kDgSlices);
-  float acc = 0.f;
-  if (c < d)
-    for (int p = r0 + static_cast<int>(threadIdx.y); p < r1; p += 8) acc += part[static_cast<size_t>(p) * d + c];
-  lanes[threadIdx.y][threadIdx.x] = acc;
+  __threadfence();
   __syncthreads();
-  if (threadIdx.y == 0) {
-    float t = 0.f;
-    for (int y = 0; y < 8; ++y) t += lanes[y][threadIdx.x];
-    if (c < d) slice_part[(static_cast<size_t>(arr) * kDgSlices + s) * d + c] = t;
-    __threadfence();
-  }
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
   __syncthreads();
-  if (threadIdx.x == 0 && threadIdx.y == 0) {
-    const unsigned int ticket = atomicAdd(&tickets[arr * gridDim.x + blockIdx.x], 1u);
-    last = ticket == kDgSlices - 1;
-  }
-  __syncthreads();
-  if (last && threadIdx.y == 0) {
-    __threadfence();
-    if (c < d) {
-      float t = 0.f;
-      for (int q = 0; q < kDgSlices; ++q)
-        t += __ldcg(&slice_part[(static_cast<size_t>(arr) * kDgSlices + q) * d + c]);
-      (arr == 0 ? dgq : dgk)[c] = t;
+  if (!last) return;
+  __threadfence();
+  // kSplit threads per column, each summing the partial rows p = sl (mod
+  // kSplit) in order; the slices are then added in slice order.
+  constexpr int kSplit = kQBwdThreads / D;
+  __shared__ float comb[2][kSplit][D];
+  const int c = threadIdx.x % D, sl = threadIdx.x / D;
+  float sq = 0.f, sk = 0.f;
+  auto strided_sum = [&](const float* src, int n) {
+    // rows sl, sl + kSplit, ... in order, four loads in flight
+    float acc = 0.f;
+    int p = sl;
+    for (; p + 3 * kSplit < n; p += 4 * kSplit) {
+      const float v0 = __ldcg(&src[static_cast<size_t>(p) * D + c]);
+      const float v1 = __ldcg(&src[static_cast<size_t>(p + kSplit) * D + c]);
+      const float v2 = __ldcg(&src[static_cast<size_t>(p + 2 * kSplit) * D + c]);
+      const float v3 = __ldcg(&src[static_cast<size_t>(p + 3 * kSplit) * D + c]);
+      acc = (((acc + v0) + v1) + v2) + v3;
     }
-    if (threadIdx.x == 0) tickets[arr * gridDim.x + blockIdx.x] = 0u;
+    for (; p < n; p += kSplit) acc += __ldcg(&src[static_cast<size_t>(p) * D + c]);
+    return acc;
+  };
+  sq = strided_sum(partial, static_cast<int>(gridDim.x));
+  sk = strided_sum(part_k, nk);
+  comb[0][sl][c] = sq;
+  comb[1][sl][c] = sk;
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSplit; ++i) {
+      a += comb[0][i][c];
+      b += comb[1][i][c];
+    }
+    dgq[c] = a;
+    dgk[c] = b;
   }
 }
 
@@ -488,8 +485,13 @@ int row_grid(Kernel kernel, int64_t rows, int d) {
 int device_sm_count() { return sm_count(); }
 
 int q_norm_bwd_parts(int d) {
-  return d == 128 ? row_grid(q_norm_bwd_kernel<128>, int64_t{1} << 40, 128)
-                  : row_grid(q_norm_bwd_kernel<64>, int64_t{1} << 40, 64);
+  int per_sm = 1;
+  const cudaError_t e = d == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q_norm_bwd_kernel<128>,
+                                                                                   kQBwdThreads, 0)
+                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q_norm_bwd_kernel<64>,
+                                                                                   kQBwdThreads, 0);
+  if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+  return sm_count() * per_sm;
 }
 
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
@@ -514,29 +516,21 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
   auto kernel = d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>;
   return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
                     gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
-                    rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets, dg_reduce_tickets(d), seg,
+                    rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets, 1, seg,
                     padded_rows);
 }
 
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
-                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, int d, uint32_t* dev_err,
+                              uint16_t* dq, float* dgq_part, int nparts, int64_t rows, const float* dgk_part, int nk,
+                              unsigned int* ticket, float* dgq, float* dgk, int d, uint32_t* dev_err,
                               cudaStream_t st) {
   (void)dev_err;
   auto* a = reinterpret_cast<const float4*>(dqacc);
   auto* x = reinterpret_cast<const uint4*>(q);
   auto* y = reinterpret_cast<uint4*>(dq);
   // Every one of the nparts blocks writes its partial (zeros if it has no row).
-  return launch_pdl(d == 64 ? q_norm_bwd_kernel<64> : q_norm_bwd_kernel<128>, dim3(nparts), dim3(kNormThreads), 0,
-                    st, a, x, rq, gq, scale, y, dgq_part, rows);
-}
-
-int dg_reduce_scratch_floats(int d) { return 2 * kDgSlices * d; }
-int dg_reduce_tickets(int d) { return 2 * ((d + 31) / 32); }
-
-cudaError_t launch_dg_reduce(const float* part_q, int nq, const float* part_k, int nk, int d, float* slice_part,
-                             unsigned int* tickets, float* dgq, float* dgk, cudaStream_t st) {
-  return launch_pdl(dg_reduce_kernel, dim3((d + 31) / 32, kDgSlices, 2), dim3(32, 8), 0, st, part_q, nq, part_k,
-                    nk, d, slice_part, tickets, dgq, dgk);
+  return launch_pdl(d == 64 ? q_norm_bwd_kernel<64> : q_norm_bwd_kernel<128>, dim3(nparts), dim3(kQBwdThreads), 0,
+                    st, a, x, rq, gq, scale, y, dgq_part, rows, dgk_part, nk, ticket, dgq, dgk);
 }
 
 }  // namespace jattn

@@ -26,7 +26,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_kernel_names_and_profile_argument_checks(lib):
     names = [ja.jattn_kernel_name(k) for k in range(ja.KERNEL_KINDS)]
-    assert names == ["qk_norm_fwd", "attn_fwd", "bwd_prep", "attn_bwd", "q_norm_bwd", "dg_reduce"]
+    assert names == ["qk_norm_fwd", "attn_fwd", "bwd_prep", "attn_bwd", "q_norm_bwd"]
     assert ja.jattn_kernel_name(ja.KERNEL_KINDS) == "unknown"
     import ctypes
     n, ms = ctypes.c_int(0), ctypes.c_double(0)
