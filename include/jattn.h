@@ -81,9 +81,10 @@ int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, con
  *   dgq, dgk   : [d] float32, overwritten (summed over all b, h, n).
  * The bf16 rounding of q_hat/k_hat is treated as the identity.  The
  * normalised q_hat/k_hat are recomputed from q, k (nothing is cached from
- * the forward call).  dq is accumulated in float32 with atomics across key
- * tiles, so it may differ in the last bits between runs; dk, dv, dgq and dgk
- * are computed in a fixed order and are bitwise reproducible.
+ * the forward call).  dq is accumulated in float32 with reduce-adds across
+ * key tiles in arrival order, so dq and dgq (a sum over dq's accumulator)
+ * may differ in the last bits between runs; dk, dv and dgk are computed in a
+ * fixed order and are bitwise reproducible.
  */
 int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
               const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq, jattn_bf16* dk,

@@ -148,7 +148,10 @@ def test_token_permutation_equivariance(ja):
 
 
 def test_output_margins_untouched_and_dg_deterministic(ja):
-    B, H, N, d = 1, 2, 200, 128
+    # Four key tiles: dq's fp32 reduce-adds land in arrival order, so dq and
+    # dgq (summed from dq's accumulator) agree to rounding only; dk, dv and
+    # dgk are summed in a fixed order and repeat bit for bit.
+    B, H, N, d = 1, 2, 500, 128
     inp = make_inputs(B, H, N, d, seed=9)
     e, r, pad = B * H * N * d, B * H * N, 4096
     q, k, v, dout = (dev_bf16(a) for a in (inp.q, inp.k, inp.v, inp.dout))
@@ -167,14 +170,17 @@ def test_output_margins_untouched_and_dg_deterministic(ja):
     ja.jattn_fwd(q, k, v, gq, gk, B, H, N - 77, 77, d, o, l)
     ja.jattn_bwd(q, k, v, gq, gk, o, l, dout, dq, dk, dv, dgq, dgk, B, H, N - 77, 77, d)
     torch.cuda.synchronize()
-    first = {n: bufs[n][1].clone() for n in ("dk", "dv", "dgq", "dgk")}
+    first = {n: bufs[n][1].clone() for n in ("dq", "dk", "dv", "dgq", "dgk")}
     for name, (buf, view) in bufs.items():
         assert torch.isnan(buf[:pad].float()).all() and torch.isnan(buf[pad + view.numel():].float()).all(), name
         assert torch.isfinite(view.float()).all(), name
     ja.jattn_bwd(q, k, v, gq, gk, o, l, dout, dq, dk, dv, dgq, dgk, B, H, N - 77, 77, d)
     torch.cuda.synchronize()
-    for n in ("dk", "dv", "dgq", "dgk"):
+    for n in ("dk", "dv", "dgk"):
         assert torch.equal(first[n], bufs[n][1]), n
+    for n in ("dq", "dgq"):
+        a, b = first[n].double(), bufs[n][1].double()
+        assert float((a - b).norm() / b.norm()) < 1e-3, n
     assert ja.jattn_last_device_error() == 0
 
 
