@@ -50,8 +50,8 @@ def flops_bwd(B, H, N, d):
 # 512 px workload (profiles/attn_kernels_512px.md), keyed to the kernel source they were taken
 # on: a changed source reports null until it is captured again.
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 192.674048e6 + 65.379072e6, "source": "attn_bwd.cu", "sha1": "9968b78a99be"},
-    "attn_fwd": {"bytes": 81.272832e6 + 6.930688e6, "source": "attn_fwd.cu", "sha1": "ae7f9713a8e1"},
+    "attn_bwd": {"bytes": 192.615936e6 + 65.480960e6, "source": "attn_bwd.cu", "sha1": "6d3229987f6a"},
+    "attn_fwd": {"bytes": 81.278976e6 + 6.556672e6, "source": "attn_fwd.cu", "sha1": "ae7f9713a8e1"},
 }
 
 
