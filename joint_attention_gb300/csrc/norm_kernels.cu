@@ -402,15 +402,29 @@ __global__ void __launch_bounds__(kQBwdThreads) q_norm_bwd_kernel(const float4* 
     if (row < rows) dq[row * TPR + sub] = pack8(y);
     cur = nxt;
   }
-  // Block reduction of acc over the RPB row slots (fixed order).
-  __shared__ float red[kQBwdThreads / TPR][D];
+  // Block reduction of acc over the RPB row slots, in a fixed order: kSplit
+  // threads per column each add the slots w = sl (mod kSplit) in slot order,
+  // then one thread per column adds the kSplit slices in slice order.
+  constexpr int kSplit = kQBwdThreads / D;
+  static_assert(RPB % kSplit == 0, "slots per slice");
+  __shared__ float red[RPB][D];
+  __shared__ float comb[2][kSplit][D];
   const int slot = threadIdx.x / TPR;
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[slot][sub * 8 + i] = acc[i];
   __syncthreads();
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+  const int c = threadIdx.x % D, sl = threadIdx.x / D;
+  {
     float t = 0.f;
-    for (int w = 0; w < RPB; ++w) t += red[w][c];
+#pragma unroll
+    for (int w = sl; w < RPB; w += kSplit) t += red[w][c];
+    comb[0][sl][c] = t;
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSplit; ++i) t += comb[0][i][c];
     partial[static_cast<size_t>(blockIdx.x) * D + c] = t;
   }
   __shared__ bool last;
@@ -421,27 +435,26 @@ __global__ void __launch_bounds__(kQBwdThreads) q_norm_bwd_kernel(const float4* 
   if (!last) return;
   __threadfence();
   // kSplit threads per column, each summing the partial rows p = sl (mod
-  // kSplit) in order; the slices are then added in slice order.
-  constexpr int kSplit = kQBwdThreads / D;
-  __shared__ float comb[2][kSplit][D];
-  const int c = threadIdx.x % D, sl = threadIdx.x / D;
+  // kSplit) in order, the dgq and dgk rows of a chunk loaded together; the
+  // slices are then added in slice order.
+  constexpr int kChunk = 12;
+  const int nq = static_cast<int>(gridDim.x);
+  const int n = nq > nk ? nq : nk;
   float sq = 0.f, sk = 0.f;
-  auto strided_sum = [&](const float* src, int n) {
-    // rows sl, sl + kSplit, ... in order, four loads in flight
-    float acc = 0.f;
-    int p = sl;
-    for (; p + 3 * kSplit < n; p += 4 * kSplit) {
-      const float v0 = __ldcg(&src[static_cast<size_t>(p) * D + c]);
-      const float v1 = __ldcg(&src[static_cast<size_t>(p + kSplit) * D + c]);
-      const float v2 = __ldcg(&src[static_cast<size_t>(p + 2 * kSplit) * D + c]);
-      const float v3 = __ldcg(&src[static_cast<size_t>(p + 3 * kSplit) * D + c]);
-      acc = (((acc + v0) + v1) + v2) + v3;
+  for (int p0 = sl; p0 < n; p0 += kChunk * kSplit) {
+    float vq[kChunk], vk[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int p = p0 + i * kSplit;
+      vq[i] = p < nq ? __ldcg(&partial[static_cast<size_t>(p) * D + c]) : 0.f;
+      vk[i] = p < nk ? __ldcg(&part_k[static_cast<size_t>(p) * D + c]) : 0.f;
     }
-    for (; p < n; p += kSplit) acc += __ldcg(&src[static_cast<size_t>(p) * D + c]);
-    return acc;
-  };
-  sq = strided_sum(partial, static_cast<int>(gridDim.x));
-  sk = strided_sum(part_k, nk);
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      sq += vq[i];
+      sk += vk[i];
+    }
+  }
   comb[0][sl][c] = sq;
   comb[1][sl][c] = sk;
   __syncthreads();
