@@ -161,6 +161,17 @@ int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16
 int jattn_last_device_error(void* stream);
 
 /*
+ * Self-test of the bounded-wait path (no counterpart on the pages: failure
+ * detection).  Enqueues on `stream` a one-thread kernel that waits on an
+ * mbarrier nothing ever arrives at.  The wait is the one every attention
+ * kernel uses: it gives up after its limit (about 1 s), records the device
+ * error and returns, so the context stays usable.  The next
+ * jattn_last_device_error(stream) then returns JATTN_ERR_TIMEOUT.  Returns
+ * JATTN_OK, or JATTN_ERR_CUDA if the launch failed.
+ */
+int jattn_selftest_wait_timeout(void* stream);
+
+/*
  * Kernel timing (off by default; no counterpart on the pages: measurement
  * support).  While enabled, every kernel launch made by jattn_fwd / jattn_bwd
  * on the calling thread's device is bracketed by two CUDA events recorded on

@@ -67,6 +67,8 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     lib.jattn_bwd_varlen.restype = i32
     lib.jattn_last_device_error.argtypes = [vp]
     lib.jattn_last_device_error.restype = i32
+    lib.jattn_selftest_wait_timeout.argtypes = [vp]
+    lib.jattn_selftest_wait_timeout.restype = i32
     lib.jattn_status_string.argtypes = [i32]
     lib.jattn_status_string.restype = ctypes.c_char_p
     lib.jattn_version.argtypes = []
@@ -251,6 +253,14 @@ def jattn_bwd_varlen(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, cu_s
 
 def jattn_last_device_error(stream=None) -> int:
     return load_library().jattn_last_device_error(_stream(stream))
+
+
+def jattn_selftest_wait_timeout(stream=None) -> int:
+    """Runs the bounded-wait self-test kernel; the next jattn_last_device_error reports the timeout."""
+    rc = load_library().jattn_selftest_wait_timeout(_stream(stream))
+    if rc != 0:
+        raise JattnError(rc, "jattn_selftest_wait_timeout")
+    return rc
 
 
 def jattn_status_string(status: int) -> str:

@@ -486,6 +486,33 @@ extern "C" int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const 
   return bwd_body(s, q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, stream);
 }
 
+namespace jattn {
+
+// One thread waits on an mbarrier that nothing arrives at, through the same
+// bounded wait the attention kernels use: it gives up after kWaitLimitNs and
+// records DEV_ERR_WAIT_TIMEOUT, and the kernel returns.
+__global__ void selftest_wait_kernel(uint32_t* dev_err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0u, &abort_flag, dev_err);
+}
+
+}  // namespace jattn
+
+extern "C" int jattn_selftest_wait_timeout(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = dev_err_ptr();
+  if (!err) return fail(JATTN_ERR_CUDA, "device error word");
+  jattn::selftest_wait_kernel<<<1, 32, 0, st>>>(err);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(JATTN_ERR_CUDA, "selftest_wait_kernel launch", e);
+  return JATTN_OK;
+}
+
 extern "C" int jattn_last_device_error(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return JATTN_ERR_CUDA;

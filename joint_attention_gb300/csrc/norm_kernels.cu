@@ -239,10 +239,9 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
 // D = rowsum(dout * out), minus LSE in the log2 domain and a zeroed fp32 dq
 // accumulator row; pad rows get -LSE = -inf and D = 0 so the attention
 // backward sees zero probabilities.  Each thread loads its next row while it
-// transforms the current one.  Bounded to three CTAs per SM (80 registers):
-// more rows in flight than the two CTAs its natural register count allows.
+// transforms the current one.
 template <int D>
-__global__ void __launch_bounds__(kNormThreads, 3) bwd_prep_kernel(
+__global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
