@@ -334,6 +334,61 @@ def test_varlen_matches_oracle(ja, lens, d):
     check_bwd(got, ref, where=where)
 
 
+def _random_lengths(rng, count, hi):
+    return tuple(int(x) for x in rng.integers(1, hi + 1, size=count))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_varlen_random_length_mixes(ja, seed, d):
+    """Seeded mixes of 3 to 12 sequences of 1 to 400 rows each."""
+    rng = np.random.default_rng(900 + seed)
+    lens = _random_lengths(rng, int(rng.integers(3, 13)), 400)
+    cu, q, k, v, dout, gq, gk = packed_inputs(lens, 2, d, seed=910 + seed + d)
+    got = run_gpu_varlen(ja, q, k, v, gq, gk, dout, cu)
+    ref = oracle.joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu)
+    where = f"varlen {lens} d={d}"
+    check_fwd(got, ref, where)
+    check_bwd(got, ref, where=where)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_maximum_sequence_count(ja, d):
+    """JATTN_MAX_SEQS (256) sequences of 1 to 40 rows: the segment tables at
+    their full size, and every unit shorter than one tile, so that the O rows
+    of every sequence but the last leave by row stores, not tile stores."""
+    rng = np.random.default_rng(950 + d)
+    lens = _random_lengths(rng, 256, 40)
+    cu, q, k, v, dout, gq, gk = packed_inputs(lens, 2, d, seed=960 + d)
+    got = run_gpu_varlen(ja, q, k, v, gq, gk, dout, cu)
+    ref = oracle.joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu)
+    where = f"varlen 256 sequences d={d}"
+    check_fwd(got, ref, where)
+    check_bwd(got, ref, where=where)
+
+
+def test_maximum_head_count(ja):
+    """B*H = 65535, the largest head count the ABI accepts, with N = 2 (one
+    caption row, one image row): every head compared with the oracle.
+
+    With two keys, O is a mix of two v rows and |O| reaches the largest |v| of
+    8.4 M draws (about 5), where the workloads' long rows average |O| down.
+    The kernel rounds P and O to bf16 (relative 2^-9 each) and normalises by a
+    row sum of the unrounded P, so |O - O_exact| <= 3 * 2^-9 * max_j |v_j,c|
+    per head and column.  The test holds O to 2^-7 * max_j |v_j,c| there, in
+    place of the fixed 1e-2, and keeps every other bound."""
+    B, H, N, d = 5, 13107, 2, 64
+    inp = make_inputs(B, H, N, d, seed=970)
+    got = run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, 1)
+    ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    bound = 2.0 ** -7 * np.max(np.abs(inp.v.astype(np.float64)), axis=2, keepdims=True)
+    excess = np.abs(got["O"] - ref["O"]) - bound
+    assert float(np.max(excess)) <= 0.0, ("65535 heads", "O above the bf16 bound", float(np.max(excess)))
+    assert relF(got["O"], ref["O"]) <= O_RELF
+    assert float(np.max(np.abs(got["LSE"] - ref["LSE"]))) <= LSE_MAXABS
+    check_bwd(got, ref, where="65535 heads")
+
+
 def test_varlen_of_equal_lengths_equals_the_batched_layout(ja):
     """B sequences of one length L packed as [H, B*L, d] and the same data as
     [B, H, L, d]: the kernels walk the same tiles in the same order, so O, LSE,
