@@ -273,12 +273,27 @@ def run_reference(args):
     return 0
 
 
-def per_config_throughput(ja, torch, dev, stream, steps=10, warmup=3):
+def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
     """TFLOP/s and images-equivalent/s of every workload of the parity suite (one GPU, eager
     calls, inputs resident on the device; the fwd+bwd rows are 14·B·H·N²·d per step, the CFG
     sampling row is its forward, 4·B·H·N²·d per denoising step).  Inputs are seeded device
-    normals of each workload's shape (values do not change the work)."""
+    normals of each workload's shape (values do not change the work), in N_SETS rotating sets
+    whose combined size exceeds L2 for every workload but the tiny one.  Each row is the median
+    of `reps` steps, each timed alone with CUDA events on the launching stream, after `warmup`
+    untimed steps."""
     from joint_attention_gb300.inputs import CONFIGS
+
+    def median_ms(one):
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            one(i)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
 
     res = {}
     gen = torch.Generator(device=dev)
@@ -286,31 +301,23 @@ def per_config_throughput(ja, torch, dev, stream, steps=10, warmup=3):
         B, H, N, d = c.B, c.H, c.N, c.d
         gen.manual_seed(1000 + c.seed)
         shape = (B, H, N, d)
-        t = {key: (torch.randn(shape, generator=gen, device=dev) * c.value_scale).to(torch.bfloat16)
-             for key in ("q", "k", "v", "dout")}
+        sets = [{key: (torch.randn(shape, generator=gen, device=dev) * c.value_scale).to(torch.bfloat16)
+                 for key in ("q", "k", "v", "dout")} for _ in range(N_SETS)]
         gq = torch.rand(d, generator=gen, device=dev) + 0.5
         gk = torch.rand(d, generator=gen, device=dev) + 0.5
-        out, lse = torch.empty_like(t["q"]), torch.empty((B, H, N), device=dev, dtype=torch.float32)
-        dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        out, lse = torch.empty_like(sets[0]["q"]), torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        dq, dk, dv = torch.empty_like(out), torch.empty_like(out), torch.empty_like(out)
         dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
         fwd_only = c.mode == "cfg_fwd"
 
-        def one():
+        def one(i):
+            t = sets[i % N_SETS]
             ja.jattn_fwd(t["q"], t["k"], t["v"], gq, gk, B, H, c.N_img, c.N_txt, d, out, lse, stream)
             if not fwd_only:
                 ja.jattn_bwd(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], dq, dk, dv, dgq, dgk, B, H,
                              c.N_img, c.N_txt, d, stream)
 
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            one()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = e0.elapsed_time(e1) / steps
+        ms = median_ms(one)
         fl = flops_fwd(B, H, N, d) + (0.0 if fwd_only else flops_bwd(B, H, N, d))
         row = {"mode": "fwd (CFG sampling step)" if fwd_only else "fwd+bwd", "B": B, "H": H, "N": N, "d": d,
                "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
@@ -319,7 +326,7 @@ def per_config_throughput(ja, torch, dev, stream, steps=10, warmup=3):
         else:
             row["images_equiv_per_s"] = B / (12 * ms * 1e-3)
         res[name] = row
-        del t, out, lse, dq, dk, dv
+        del sets, out, lse, dq, dk, dv
     # Packed variable-length call (jattn_fwd_varlen / jattn_bwd_varlen): the 512 px and 256 px joint
     # lengths mixed in one call, 8 x 1101 + 16 x 333 rows per head, H = 12, d = 64.
     lens = [1101] * 8 + [333] * 16
@@ -329,33 +336,26 @@ def per_config_throughput(ja, torch, dev, stream, steps=10, warmup=3):
         cu.append(cu[-1] + n)
     T = cu[-1]
     gen.manual_seed(2000)
-    t = {key: torch.randn((H, T, d), generator=gen, device=dev).to(torch.bfloat16) for key in ("q", "k", "v", "dout")}
+    sets = [{key: torch.randn((H, T, d), generator=gen, device=dev).to(torch.bfloat16)
+             for key in ("q", "k", "v", "dout")} for _ in range(N_SETS)]
     gq = torch.rand(d, generator=gen, device=dev) + 0.5
     gk = torch.rand(d, generator=gen, device=dev) + 0.5
-    out, lse = torch.empty_like(t["q"]), torch.empty((H, T), device=dev, dtype=torch.float32)
-    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    out, lse = torch.empty_like(sets[0]["q"]), torch.empty((H, T), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(out), torch.empty_like(out), torch.empty_like(out)
     dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
 
-    def one_varlen():
+    def one_varlen(i):
+        t = sets[i % N_SETS]
         ja.jattn_fwd_varlen(t["q"], t["k"], t["v"], gq, gk, cu, H, d, out, lse, stream)
         ja.jattn_bwd_varlen(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], dq, dk, dv, dgq, dgk, cu, H, d,
                             stream)
 
-    for _ in range(warmup):
-        one_varlen()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one_varlen()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / steps
+    ms = median_ms(one_varlen)
     fl = sum(flops_fwd(1, H, n, d) + flops_bwd(1, H, n, d) for n in lens)
     res["varlen_mix"] = {"mode": "fwd+bwd, packed sequences", "sequences": "8 x 1101 + 16 x 333", "H": H, "T": T,
                          "d": d, "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                          "images_equiv_per_s": len(lens) / (12 * ms * 1e-3)}
-    del t, out, lse, dq, dk, dv
+    del sets, out, lse, dq, dk, dv
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the per-config pass")
     return res
