@@ -458,3 +458,28 @@ def test_cfg_stream_uncond_text_rows_are_shared():
         assert not np.all(arr[:8, :, :77, :] == arr[:1, :, :1, :])
     assert not np.array_equal(s0.q, s1.q)
     np.testing.assert_array_equal(s0.gq, s1.gq)
+
+
+def test_oracle_reproduces_its_stored_tiny_values():
+    """tests/golden/tiny_oracle.json was written by tests/golden/make_oracle_golden.py, which calls
+    only the oracle (the pages print no worked example).  A change to the oracle's arithmetic shows
+    here first."""
+    import json
+    import os
+    import sys
+
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    try:
+        from make_oracle_golden import golden
+    finally:
+        sys.path.remove(here)
+    stored = json.load(open(os.path.join(here, "tiny_oracle.json")))
+    now = golden()
+    assert stored["workload"] == now["workload"] and stored["rows"] == now["rows"]
+    for key in ("LSE", "dgq", "dgk", "O_rows", "dq_rows", "dk_rows", "dv_rows"):
+        a, b = np.asarray(now[key]), np.asarray(stored[key])
+        assert a.shape == b.shape, key
+        assert np.max(np.abs(a - b)) <= 1e-12 * max(1.0, np.max(np.abs(b))), key
+    for key, v in stored["norms"].items():
+        assert abs(now["norms"][key] - v) <= 1e-12 * v, key
