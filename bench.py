@@ -47,12 +47,16 @@ def flops_bwd(B, H, N, d):
     return 10.0 * B * H * N * N * d
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one ncu capture of the
-# 512 px workload (profiles/attn_kernels_512px.md), keyed to the kernel source they were taken
-# on: a changed source reports null until it is captured again.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, stored from one ncu capture
+# of the 512 px workload and keyed to the kernel source they were taken on: a changed source
+# reports null until it is captured again.  The line labels the figure as stored, with its capture.
+_CAPTURE = ("ncu --set full --clock-control none -k regex:attn_ -s 2 -c 2, "
+            "python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-per-config")
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 192.615936e6 + 65.480960e6, "source": "attn_bwd.cu", "sha1": "6d3229987f6a"},
-    "attn_fwd": {"bytes": 81.278976e6 + 6.556672e6, "source": "attn_fwd.cu", "sha1": "e5fa777ef2e8"},
+    "attn_bwd": {"bytes": 192.615936e6 + 65.480960e6, "source": "attn_bwd.cu", "sha1": "6d3229987f6a",
+                 "capture": _CAPTURE},
+    "attn_fwd": {"bytes": 81.278976e6 + 6.556672e6, "source": "attn_fwd.cu", "sha1": "e5fa777ef2e8",
+                 "capture": _CAPTURE},
 }
 
 
@@ -86,6 +90,9 @@ def load_peaks():
             walk(data)
             if "bf16_tflops" in flat and "hbm_gbs" in flat:
                 flat.setdefault("bf16_tflops_sustained", flat["bf16_tflops"])
+                cl = data.get("clocks_under_load") if isinstance(data, dict) else None
+                if isinstance(cl, dict) and isinstance(cl.get("sm_mhz_median"), (int, float)):
+                    flat["sustained_sm_mhz"] = float(cl["sm_mhz_median"])
                 return flat, "measured"
         except (OSError, ValueError):
             pass
@@ -207,6 +214,42 @@ def cpu_oracle_sample(B, H, N, d, seed, budget_s: float, max_heads: int):
     return {"value": fl / el / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{heads} head(s) of the {WORKLOAD} workload (N={N}, d={d}) fwd+bwd in float64 NumPy, "
                       f"materialised N x N scores, {el:.2f} s; BLAS threads = all host cores"}
+
+
+def cpu_oracle_per_config(budget_s: float):
+    """The float64 oracle timed on each workload of the parity suite, on the host cores.
+
+    A sample of whole (b, h) heads of each workload runs through the oracle (fwd+bwd for the
+    training workloads; the forward for the CFG sampling workload) until budget_s has passed or
+    every head is done; the time of the full workload is the per-head time times its heads (times
+    its denoising steps for CFG sampling), stated as extrapolated unless every head ran."""
+    import oracle
+    from joint_attention_gb300.inputs import CONFIGS, make_inputs
+
+    res = {}
+    for name, c in CONFIGS.items():
+        fwd_only = c.mode == "cfg_fwd"
+        inp = make_inputs(1, 1, c.N, c.d, seed=c.seed, value_scale=c.value_scale, with_dout=not fwd_only)
+        heads_total = c.B * c.H
+        heads = 0
+        t0 = time.perf_counter()
+        while heads < heads_total:
+            if fwd_only:
+                oracle.joint_attention_fwd(inp.q, inp.k, inp.v, inp.gq, inp.gk)
+            else:
+                oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+            heads += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        el = time.perf_counter() - t0
+        fl_head = flops_fwd(1, 1, c.N, c.d) + (0.0 if fwd_only else flops_bwd(1, 1, c.N, c.d))
+        steps = c.steps if fwd_only else 1
+        full_s = el / heads * heads_total * steps
+        res[name] = {"value": fl_head * heads / el / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                     "full_workload_s": full_s, "extrapolated": heads < heads_total or steps > 1,
+                     "sample": f"{heads} of {heads_total} heads ({'forward' if fwd_only else 'fwd+bwd'}, N={c.N}, "
+                               f"d={c.d}) in {el:.2f} s" + (f"; x{steps} denoising steps" if steps > 1 else "")}
+    return res
 
 
 def run_reference(args):
@@ -371,6 +414,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--cpu-config-budget-s", type=float, default=3.0,
+                    help="host seconds of oracle time per workload in the per-config pass")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload throughput pass")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -567,23 +612,44 @@ def main():
     }
     bound, work = algo[dom]
     avg_s = kern[dom]["avg_us"] * 1e-6
+    clk = clocks.summary()
+    extra = {}
     if bound == "tensor":
         achieved = work / avg_s / 1e12
-        peak = peaks["bf16_tflops_sustained"]
         unit = "TFLOP/s"
+        # The burst bf16 peak is a GEMM timed alone at full clock; the sustained one is a
+        # seconds-long GEMM loop at the clock the power cap settles it to.  The peak taken is the
+        # one whose clock the timed loop ran at: burst when its median SM clock is within 10 % of
+        # the maximum.
+        sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+        full_clock = sm is None or mx is None or sm >= 0.9 * mx
+        peak = peaks["bf16_tflops"] if full_clock else peaks["bf16_tflops_sustained"]
+        which = "burst bf16" if full_clock else "sustained bf16"
+        extra = {"frac_vs_sustained": achieved / peaks["bf16_tflops_sustained"],
+                 "sustained_peak": peaks["bf16_tflops_sustained"],
+                 "sustained_peak_clock_mhz": peaks.get("sustained_sm_mhz")}
     else:
         achieved = work / avg_s / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
+        which = "HBM copy"
+    traffic = ncu_traffic(dom)
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": ncu_traffic(dom),
-                "peak_source": f"{peak_src} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})"}
+                "frac": achieved / peak, "traffic": traffic,
+                "traffic_source": (f"stored: dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture "
+                                   f"of {dom} on this workload, keyed to its source file "
+                                   f"({NCU_TRAFFIC[dom]['capture']})") if traffic is not None else None,
+                "peak_source": f"{peak_src} ({which})", **extra}
     per_cfg = None
     if not args.no_per_config and world == 1:
         per_cfg = per_config_throughput(ja, torch, dev, stream)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(B, H, N, d, c.seed, args.cpu_budget_s, max_heads=64)
+        if per_cfg is not None:
+            for name, row in cpu_oracle_per_config(args.cpu_config_budget_s).items():
+                if name in per_cfg:
+                    per_cfg[name]["cpu_baseline"] = row
     launches = sum(v["launches"] for v in kern.values())
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -599,7 +665,7 @@ def main():
         "images_equiv_per_s": B * world / (12 * ms_step * 1e-3),
         "model_tflops": 12.0 * B * H * N * N * d * args.steps * world / (ms_total * 1e-3) / 1e12,
         "roofline": roofline, "kernels": kern, "gpu_launches": launches,
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(), "per_config": per_cfg,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "per_config": per_cfg,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

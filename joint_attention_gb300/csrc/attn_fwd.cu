@@ -37,7 +37,6 @@
 // key columns past N in the last key tile are masked to -inf.
 #include <cuda_bf16.h>
 
-#include "exp2_poly.h"
 #include "jattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -47,13 +46,6 @@ namespace {
 constexpr int kFwdThreads = 352;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// Pairs of probabilities (by index within a 32-score chunk, bit h % 8) whose
-// 2^x runs on the FMA pipe (exp2_poly) instead of the MUFU unit.  The
-// polynomial costs about nine issue slots per value against one MUFU slot.
-// The softmax here is bound by instruction issue, not by MUFU, and every
-// non-empty mask measured slower, so none is used; the mask is 0 and the
-// polynomial is compiled out.
-constexpr uint32_t kPolyPairMask = 0u;
 
 template <int D>
 struct FwdCfg {
@@ -417,16 +409,12 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
     m_ref = m_new;
     const float neg_m = -m_ref;
     // Probabilities and row sum; P (bf16 pairs, 16 packed columns per 32
-    // scores) into TMEM.  On full tiles part of the 2^x goes to the FMA pipe;
-    // the ragged last tile keeps exact zeros for masked keys (MUFU only).
-    // x = s * scale_log2 - m and the row sum in packed f32x2 arithmetic (two
-    // scores per instruction); 2^x on the MUFU unit, except the pairs selected
-    // by kPolyPairMask on full tiles, which use the FMA-pipe polynomial.  The
-    // ragged last tile keeps exact zeros for masked keys (MUFU only).
+    // scores) into TMEM.  x = s * scale_log2 - m and the row sum in packed
+    // f32x2 arithmetic (two scores per instruction), 2^x on the MUFU unit;
+    // masked keys of the ragged last tile give exact zeros.
     const uint64_t scale2 = f2_make(scale_log2, scale_log2);
     const uint64_t negm2 = f2_make(neg_m, neg_m);
     uint64_t l2[8];  // partial row sums: two per 32-column chunk
-    const bool full_tile = nvalid >= kTileN;
     // The whole packed P row is formed in registers before the P columns
     // are touched, so the wait for PV(j-1) to release them comes after the
     // exponentials instead of stalling ahead of them.
@@ -440,9 +428,8 @@ __device__ void fwd_softmax(uint8_t* sm, FwdBars& bars, uint32_t tmem, int x, co
         float x0, x1;
         f2_split(f2_fma(f2_make(__uint_as_float(s[c][2 * h]), __uint_as_float(s[c][2 * h + 1])), scale2, negm2), x0,
                  x1);
-        const bool poly = full_tile && ((kPolyPairMask >> (h & 7)) & 1u);
-        const float p0 = poly ? exp2_poly(x0) : ex2_approx(x0);
-        const float p1 = poly ? exp2_poly(x1) : ex2_approx(x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
         l2[2 * c + (h & 1)] = f2_add(l2[2 * c + (h & 1)], f2_make(p0, p1));
         packed[c][h] = pack_bf16x2(p0, p1);
       }

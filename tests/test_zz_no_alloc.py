@@ -36,6 +36,10 @@ def test_noalloc_rejects_problems_beyond_its_array():
 
 @pytest.mark.gpu
 def test_noalloc_matches_jattn_fwd_on_two_calls_in_a_row():
+    """Two no-allocation calls back to back on one stream, on different inputs, with no
+    synchronisation between them: the second call's normalisation pass reuses the shared array
+    while the first call's attention may still read it, so the outputs show whether the launch
+    order keeps them apart.  Each is compared with jattn_fwd on the same inputs."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     build()
@@ -43,23 +47,29 @@ def test_noalloc_matches_jattn_fwd_on_two_calls_in_a_row():
     dev = torch.device("cuda:0")
     bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16).contiguous()  # noqa: E731
     f32 = lambda a: torch.from_numpy(a).to(dev).float().contiguous()  # noqa: E731
-    cases = [make_config_inputs(CONFIGS["512px"]), make_inputs(2, 3, 333, 128, seed=21)]
-    n_txts = [CONFIGS["512px"].N_txt, 77]
-    for inp, n_txt in zip(cases, n_txts):  # two calls in a row, different shapes
+    cases = [(make_config_inputs(CONFIGS["512px"]), CONFIGS["512px"].N_txt),
+             (make_inputs(2, 3, 333, 128, seed=21), 77),
+             (make_inputs(16, 12, 1101, 64, seed=22), 77)]
+    runs = []
+    for inp, n_txt in cases:
         B, H, N, d = inp.q.shape
-        q, k, v = bf(inp.q), bf(inp.k), bf(inp.v)
-        gq, gk = f32(inp.gq), f32(inp.gk)
-        out_a, lse_a = torch.empty_like(q), torch.empty((B, H, N), device=dev, dtype=torch.float32)
-        out_b = torch.full_like(q, float("nan"))
-        lse_b = torch.full((B, H, N), float("nan"), device=dev, dtype=torch.float32)
-        ja.jattn_fwd(q, k, v, gq, gk, B, H, N - n_txt, n_txt, d, out_a, lse_a)
-        rc = ja.jattn_fwd_noalloc(q, k, v, gq, gk, B, H, N - n_txt, n_txt, d, out_b, lse_b)
+        t = dict(q=bf(inp.q), k=bf(inp.k), v=bf(inp.v), gq=f32(inp.gq), gk=f32(inp.gk))
+        t["out_a"], t["lse_a"] = torch.empty_like(t["q"]), torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        t["out_b"] = torch.full_like(t["q"], float("nan"))
+        t["lse_b"] = torch.full((B, H, N), float("nan"), device=dev, dtype=torch.float32)
+        ja.jattn_fwd(t["q"], t["k"], t["v"], t["gq"], t["gk"], B, H, N - n_txt, n_txt, d, t["out_a"], t["lse_a"])
+        runs.append((t, (B, H, N, d, n_txt)))
+    torch.cuda.synchronize()
+    for t, (B, H, N, d, n_txt) in runs:  # back to back, same stream, no synchronisation
+        rc = ja.jattn_fwd_noalloc(t["q"], t["k"], t["v"], t["gq"], t["gk"], B, H, N - n_txt, n_txt, d, t["out_b"],
+                                  t["lse_b"])
         assert rc == 0
-        torch.cuda.synchronize()
-        assert ja.jattn_last_device_error() == 0
-        a = out_a.float().cpu().numpy().astype(np.float64)
-        b = out_b.float().cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    assert ja.jattn_last_device_error() == 0
+    for t, _ in runs:
+        a = t["out_a"].float().cpu().numpy().astype(np.float64)
+        b = t["out_b"].float().cpu().numpy().astype(np.float64)
         assert np.all(np.isfinite(b))
         assert float(np.max(np.abs(a - b))) <= O_MAXABS
         assert float(np.linalg.norm(a - b) / np.linalg.norm(a)) <= O_RELF
-        assert float((lse_a - lse_b).abs().max()) <= LSE_MAXABS
+        assert float((t["lse_a"] - t["lse_b"]).abs().max()) <= LSE_MAXABS
