@@ -81,10 +81,12 @@ int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, con
  *   dgq, dgk   : [d] float32, overwritten (summed over all b, h, n).
  * The bf16 rounding of q_hat/k_hat is treated as the identity.  The
  * normalised q_hat/k_hat are recomputed from q, k (nothing is cached from
- * the forward call).  dq is accumulated in float32 with reduce-adds across
- * key tiles in arrival order, so dq and dgq (a sum over dq's accumulator)
- * may differ in the last bits between runs; dk, dv and dgk are computed in a
- * fixed order and are bitwise reproducible.
+ * the forward call).  dk, dv and dgk are always summed in a fixed order and
+ * repeat bit for bit.  dq is accumulated in float32 across key tiles: by
+ * default with reduce-adds in arrival order, so that dq and dgq (a sum over
+ * dq's accumulator) may differ in the last bits between runs; with
+ * jattn_set_deterministic(1), in a fixed order, so that all five gradients
+ * repeat bit for bit (on the same GPU model and CTA cap).
  */
 int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
               const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq, jattn_bf16* dk,
@@ -192,6 +194,32 @@ int jattn_profile_enable(int on);
 int jattn_profile_reset(void);
 int jattn_profile_read(int kind, int* launches, double* total_ms);
 const char* jattn_kernel_name(int kind);
+
+/*
+ * Deterministic backward (off by default; no counterpart on the pages).
+ * With on != 0, later jattn_bwd / jattn_bwd_varlen calls from any thread add
+ * the key tiles' contributions to each query tile's float32 dq accumulator in
+ * a fixed order (the first is stored, each later one is added only after the
+ * one before it has completed), so that dq and dgq repeat bit for bit.  The
+ * order costs time: contributions wait on one another across CTAs (bounded
+ * waits: a stalled wait ends the kernel and jattn_last_device_error reports
+ * JATTN_ERR_TIMEOUT).  Every CTA of the launch must be able to run at the
+ * same time as the others (see jattn_set_sm_limit).  Returns JATTN_OK.
+ */
+int jattn_set_deterministic(int on);
+
+/*
+ * Caps the number of CTAs the persistent attention kernels launch, and so the
+ * SMs they occupy, at max_sms (0 = every SM of the device, the default); for
+ * sharing the GPU with concurrent work, and for exercising the kernels' work
+ * schedules on small problems.  It applies to later calls from any thread.
+ * In the deterministic mode the backward picks its dQ order from it.  A cap
+ * above the SMs the process may use (for example under an MPS thread limit)
+ * can make the deterministic backward's cross-CTA waits give up
+ * (JATTN_ERR_TIMEOUT).  Returns JATTN_ERR_INVALID_ARG for a negative cap.
+ * (No counterpart on the pages.)
+ */
+int jattn_set_sm_limit(int max_sms);
 
 /* Static description of a status code (never NULL). */
 const char* jattn_status_string(int status);

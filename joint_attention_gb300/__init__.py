@@ -7,8 +7,8 @@ plus small conveniences that allocate the output tensors with torch.
 from __future__ import annotations
 
 from ._binding import (KERNEL_KINDS, STATUS, STATUS_CODE, JattnError, declared_symbols, jattn_bwd, jattn_fwd,
-                       jattn_fwd_noalloc, jattn_fwd_varlen, jattn_bwd_varlen, jattn_selftest_wait_timeout,
-                       jattn_kernel_name, jattn_last_device_error, jattn_last_error_message, jattn_profile_enable, jattn_profile_read,
+                       jattn_fwd_noalloc, jattn_fwd_varlen, jattn_bwd_varlen, jattn_selftest_wait_timeout, jattn_set_sm_limit,
+                       jattn_set_deterministic, jattn_kernel_name, jattn_last_device_error, jattn_last_error_message, jattn_profile_enable, jattn_profile_read,
                        jattn_profile_reset, jattn_status_string, jattn_version, load_library, profile_snapshot)
 
 __all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd", "jattn_fwd",
@@ -16,7 +16,7 @@ __all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd
            "backward", "KERNEL_KINDS", "jattn_kernel_name", "jattn_profile_enable", "jattn_profile_read",
            "jattn_profile_reset", "profile_snapshot", "jattn_last_error_message", "jattn_fwd_noalloc",
            "jattn_fwd_varlen", "jattn_bwd_varlen", "forward_varlen", "backward_varlen",
-           "jattn_selftest_wait_timeout"]
+           "jattn_selftest_wait_timeout", "jattn_set_sm_limit", "jattn_set_deterministic"]
 
 
 def forward(q, k, v, gq, gk, n_txt: int, stream=None):

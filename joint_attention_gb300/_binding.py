@@ -81,6 +81,10 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     lib.jattn_profile_reset.restype = i32
     lib.jattn_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
     lib.jattn_profile_read.restype = i32
+    lib.jattn_set_sm_limit.argtypes = [i32]
+    lib.jattn_set_sm_limit.restype = i32
+    lib.jattn_set_deterministic.argtypes = [i32]
+    lib.jattn_set_deterministic.restype = i32
     lib.jattn_kernel_name.argtypes = [i32]
     lib.jattn_kernel_name.restype = ctypes.c_char_p
     if path is None:
@@ -260,6 +264,22 @@ def jattn_selftest_wait_timeout(stream=None) -> int:
     rc = load_library().jattn_selftest_wait_timeout(_stream(stream))
     if rc != 0:
         raise JattnError(rc, "jattn_selftest_wait_timeout")
+    return rc
+
+
+def jattn_set_sm_limit(max_sms: int) -> int:
+    """C ABI jattn_set_sm_limit: cap the persistent kernels' CTAs (0 = every SM)."""
+    rc = load_library().jattn_set_sm_limit(int(max_sms))
+    if rc != 0:
+        raise JattnError(rc, "jattn_set_sm_limit")
+    return rc
+
+
+def jattn_set_deterministic(on: bool) -> int:
+    """C ABI jattn_set_deterministic: bitwise-reproducible backward (fixed dQ accumulation order) or not."""
+    rc = load_library().jattn_set_deterministic(1 if on else 0)
+    if rc != 0:
+        raise JattnError(rc, "jattn_set_deterministic")
     return rc
 
 

@@ -18,39 +18,43 @@
 // load and first S / dP products overlap the current unit's last tiles and
 // its epilogue.
 // 640 threads (five warpgroups; setmaxnreg gives the compute warpgroups 128
-// registers per thread, the drain 104, the epilogue 72 and TMA / MMA 40):
+// registers per thread, the drain 96, the epilogue 72 and TMA / MMA 48):
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
 //               row (TMEM lane).  P^T is written into TMEM as packed bf16
-//               (A operand of the dV MMA); dS^T goes to shared memory in the
-//               MMA's swizzled layout (A operand of dK, and of dQ read
-//               MN-major).
-//   warps 8-11  dQ drain: one thread per query row moves dQ_i from TMEM to a
-//               padded shared-memory row and issues a bulk reduce-add of it
-//               (d = 128: also the unit epilogue).
+//               (A operand of the dV MMA).  dS^T goes to shared memory in
+//               the MMA's swizzled layout (read MN-major as the A operand of
+//               dQ) and, d = 64, into TMEM over the group's own dP^T columns
+//               as the A operand of dK (d = 128: dK reads the shared tile).
+//   warps 8-11  dQ drain, one thread per query row: d = 64, dQ_i from TMEM
+//               into two swizzled 128 x 32 fp32 staging halves, each added
+//               into the global accumulator by one TMA tensor reduce;
+//               d = 128, padded rows and one bulk reduce-add per row, and
+//               the unit epilogue.
 //   warps 12-15 d = 64 unit epilogue, one thread per key row: dv, and the
 //               K-RMSNorm backward of dK (dk and the unit's dgk partial),
 //               built in the unit's own K/V buffer once the MMAs are done
 //               with it; the TMEM accumulators are released as soon as they
-//               are read, so the next unit never waits on this work.
+//               are read.
 //   warp 16     TMA producer: K_j, V_j per unit (double-buffered for d = 64);
-//               Q_i (+ LSE_i, D_i) and dO_i per query tile through rings.
+//               per query tile Q_i and dO_i through rings, with the tile's
+//               softmax statistics (d = 64: a bf16 chunk for the MMAs;
+//               d = 128: fp32 LSE_i and D_i rows).
 //   warps 17-19 MMA issuers (d = 64): recompute (S, dP), gradients (dV, dK)
 //               and dQ; d = 128 uses warp 17 alone.
 //
-// d = 64: TMEM (512 columns) S^T [0,128), dP^T [128,256), dV [256,320),
-// dK [320,384), dQ [384,448), P^T [448,512) (packed bf16).  The compute
-// groups release S^T and dP^T as soon as they hold them in registers
-// (s_free, dp_free), so the recompute issuer computes S(i+1) and dP(i+1)
-// while tile i's P and dS are still being formed; P^T(i+1) is written only
-// after dV(i) has read P^T(i).
+// d = 64: TMEM (512 columns) S^T [0,128), dP^T [128,256) (then dS^T),
+// dV [256,320), dK [320,384), dQ [384,448), P^T [448,512) (packed bf16).
+// S(i+1) is computed as soon as the compute groups hold S^T(i) in registers
+// (s_free); dP(i+1) once dK(i) has read dS^T(i) out of the dP^T columns;
+// P^T(i+1) is written only after dV(i) has read P^T(i).  The statistics
+// enter as one more K = 16 step of the S^T and dP^T products, so TMEM holds
+// S^T - LSE / scale and dP^T - D.
 //
 // d = 128: TMEM S^T/P^T [0,128), dP^T [128,256), dV [256,384), dK [384,512),
 // dQ over the dP^T columns; one issuer in the order dV(i), S(i+1), dK(i),
 // dQ(i), dP(i+1), with dP(i+1) waiting for dQ(i) to be drained.
-//
-// The dS^T tile in shared memory serves dQ = dS K as an MN-major A operand.
 #include <cuda_bf16.h>
 
 #include "jattn_internal.h"
@@ -62,21 +66,27 @@ namespace {
 constexpr int kBwdThreads = 640;  // 5 warpgroups
 // Warp roles: 0-7 compute (two groups), 8-11 dQ drain, 12-15 epilogue
 // (d = 64), 16 TMA, 17-19 MMA issuers.  Registers per thread (setmaxnreg):
-// compute 128, drain 104, epilogue 72, TMA / issuers 40 (d = 128: 72 for all
-// but compute); 256 x 128 + 128 x (104 + 72 + 40) = 256 x 128 + 384 x 72 =
+// compute 128, drain 96, epilogue 72, TMA / issuers 48 (d = 128: 72 for all
+// but compute); 256 x 128 + 128 x (96 + 72 + 48) = 256 x 128 + 384 x 72 =
 // 60416 of the 640 x 96 the block launches with.
 // setmaxnreg budgets.  An increase must not be below, a decrease not above,
 // the count the kernel launches with, and the sum must fit the launch's
 // registers (640 x that count); the launcher checks both against the
 // compiled kernel before every launch.
-constexpr int kRegCompute = 128, kRegDrain64 = 104, kRegEpi64 = 72, kRegMma64 = 40, kRegOther128 = 72;
-constexpr int kRegLaunchMin = 95, kRegLaunchMax = 104;  // kRegDrain64 and kRegEpi64 / kRegOther128 bounds
+constexpr int kRegCompute = 128, kRegDrain64 = 96, kRegEpi64 = 72, kRegMma64 = 48, kRegOther128 = 72;
+// The d = 64 drain warps keep the count the kernel launches with.
+constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
+// Each SM sub-partition holds one warp of every warpgroup (warp w on w % 4)
+// and 16384 registers, so one warp of each role must fit there too.
+static_assert(32 * (2 * kRegCompute + kRegDrain64 + kRegEpi64 + kRegMma64) <= 16384,
+              "d = 64 register split exceeds a sub-partition");
+static_assert(32 * (2 * kRegCompute + 3 * kRegOther128) <= 16384, "d = 128 register split exceeds a sub-partition");
 static_assert(256 * kRegCompute + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <= kBwdThreads * kRegLaunchMin,
               "d = 64 register split exceeds the launch allocation");
 static_assert(256 * kRegCompute + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
               "d = 128 register split exceeds the launch allocation");
 static_assert(kRegEpi64 <= kRegLaunchMin && kRegMma64 <= kRegLaunchMin && kRegOther128 <= kRegLaunchMin &&
-                  kRegDrain64 >= kRegLaunchMax && kRegCompute >= kRegLaunchMax,
+                  kRegDrain64 == kRegLaunchMax && kRegCompute >= kRegLaunchMax,
               "setmaxnreg direction");
 constexpr int kWarpEpi = 12;
 constexpr int kWarpTma = 16;
@@ -96,14 +106,43 @@ struct BwdCfg {
   // d = 64: three MMA issuers (recompute: S, dP; gradients: dV, dK; dQ) and
   // P^T in its own TMEM columns.  d = 128: one issuer, P^T over S^T.
   static constexpr bool kSplitIssuers = (D == 64);
-  static constexpr int kDQCols = (D == 64) ? 64 : 32;        // dQ columns drained per pass
-  static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // padded staging row
+  // d = 64: the softmax statistics enter through the tensor cores.  Each
+  // query tile brings a 16-column bf16 chunk B of its rows' -LSE / scale and
+  // -D, each split into three bf16 terms (columns 0-2 and 3-5), and one more
+  // K = 16 step of the S^T and dP^T products with a constant A chunk (ones in
+  // columns 0-2, resp. 3-5, of every key row) gives S^T - LSE / scale and
+  // dP^T - D directly in TMEM.  The compute warps then read no per-query
+  // values from shared memory.
+  static constexpr bool kStatsFold = (D == 64);
+  static constexpr int kStatsChunk = 128 * 16 * 2;             // 128 rows x 16 bf16, 32-byte swizzle
+  // The constant A chunks repeat one 8-row atom (256 bytes) with a zero atom
+  // stride, so each takes 256 bytes.
+  static constexpr int kConstAtom = 256;
+  // dQ: d = 64 stages the tile in two 128 x 32 fp32 halves (128-byte rows,
+  // 128-byte swizzle), each reduced into the accumulator by one TMA tensor
+  // reduce; d = 128 stages 32 columns per pass in padded rows, reduced row
+  // by row.
+  static constexpr int kDQCols = 32;                          // dQ columns staged per pass
+  static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // d = 128 padded staging row
+  static constexpr int kDQStageBytes = (D == 64) ? 2 * 128 * 128 : 128 * kDQRowBytes;
   static constexpr int kOffKV = 0;                            // + buf * 2 * kTile: K, then V
   static constexpr int kOffQ = kKVBufs * 2 * kTile;           // + stage * kTile
   static constexpr int kOffDO = kOffQ + kQStages * kTile;     // + stage * kTile
   static constexpr int kOffDS = kOffDO + kDOStages * kTile;   // + buf * 32 KB (128 x 128 bf16)
-  static constexpr int kOffDQ = kOffDS + kDSBufs * 128 * 128 * 2;
-  static constexpr int kTileBytes = kOffDQ + 128 * kDQRowBytes;
+  static constexpr int kOffStats = kOffDS + kDSBufs * 128 * 128 * 2;          // + stage * kStatsChunk
+  static constexpr int kOffConst = kOffStats + (kStatsFold ? kQStages * kStatsChunk : 0);  // S, then dP
+  static constexpr int kOffDQ = kOffConst + (kStatsFold ? 1024 : 0);
+  // d = 128: per query stage, minus the tile's LSE in the log2 domain (-inf
+  // past N) and D (0 past N), copied in with the tile from padded scratch rows.
+  static constexpr int kOffNlse = kOffDQ + kDQStageBytes;                 // + stage * 512
+  static constexpr int kOffDelta = kOffNlse + (kStatsFold ? 0 : kQStages * 512);
+  static constexpr int kTileBytes = kOffDelta + (kStatsFold ? 0 : kQStages * 512);
+  static __device__ __forceinline__ float* nlse2(uint8_t* sm, int qs) {
+    return reinterpret_cast<float*>(sm + kOffNlse + qs * 512);
+  }
+  static __device__ __forceinline__ float* delta(uint8_t* sm, int qs) {
+    return reinterpret_cast<float*>(sm + kOffDelta + qs * 512);
+  }
   static constexpr int kDynSmem = kTileBytes + 1024;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;
@@ -125,6 +164,12 @@ struct BwdCfg {
 // own segment.  Query tiles are counted on across units (t runs over all
 // query tiles of the CTA's units), and every ring / handshake barrier takes
 // its phase from that count.
+// dQ accumulation order.  kDqArrival: every key tile's contribution is a
+// bulk reduce-add into a zeroed accumulator, in whatever order they land (the
+// default; dq and dgq repeat to rounding).  kDqRotated / kDqAscending: the
+// deterministic mode, a fixed order per query tile (see bwd_drain_epilogue).
+enum : int { kDqArrival = 0, kDqRotated = 1, kDqAscending = 2 };
+
 struct BwdUnit {
   int bh;     // head
   int j;      // key tile within the segment
@@ -132,13 +177,19 @@ struct BwdUnit {
   int row0;   // the segment's first row in the head
   int end;    // one past its last row
   int prow0;  // its first row in the padded per-head scratch
-  // The i-th query tile visited: the key tiles of one segment (which run
-  // side by side on neighbouring CTAs) start at different query tiles, so
-  // that their dQ reduce-adds go to different rows at any one time.
+  int ord;    // dQ order: kDqArrival, kDqRotated or kDqAscending
+  // The i-th query tile visited: except in the ascending order, the key tiles
+  // of one segment (which run side by side on neighbouring CTAs) start at
+  // different query tiles, so that their dQ contributions go to different
+  // rows at any one time.
   __device__ __forceinline__ int query_tile(int i) const {
+    if (ord == kDqAscending) return i;
     const int q = i + j;
     return q < nkt ? q : q - nkt;
   }
+  // Ordered modes: contributions to that query tile's accumulator made before
+  // this one.
+  __device__ __forceinline__ int rank(int i) const { return ord == kDqAscending ? j : i; }
   __device__ __forceinline__ int kv0() const { return row0 + 128 * j; }  // first key row
 };
 
@@ -147,6 +198,7 @@ struct BwdUnit {
 struct BwdWorkUniform {
   int upc;    // 128-row tiles per head
   int units;  // heads * upc
+  int ord;    // dQ order
   struct {
     int rows, prows;
   } seg;
@@ -158,6 +210,7 @@ struct BwdWorkUniform {
     r.row0 = 0;
     r.end = seg.rows;
     r.prow0 = 0;
+    r.ord = ord;
     return r;
   }
 };
@@ -166,6 +219,7 @@ struct BwdWorkUniform {
 struct BwdWork {
   int upc;    // units per head (padded rows per head / 128)
   int units;  // heads * upc
+  int ord;    // dQ order
   SegTable seg;
   __device__ __forceinline__ BwdUnit unit(int u) const {
     BwdUnit r;
@@ -182,6 +236,7 @@ struct BwdWork {
     r.row0 = seg.cu[lo];
     r.end = seg.cu[lo + 1];
     r.prow0 = seg.pcu[lo];
+    r.ord = ord;
     return r;
   }
 };
@@ -197,19 +252,18 @@ struct BwdBars {
   uint64_t dq_full, dq_free;
   uint64_t acc_full;                // a unit's dV / dK accumulators are final
   uint64_t acc_free_v, acc_free_k;  // ... and have been read out of TMEM
-  uint64_t s_free, dp_free;
+  uint64_t s_free;
   uint64_t dv_done;
+  uint64_t dk_done;     // d = 64: dK(t) has read dS^T(t) from the dP^T columns
   uint64_t epi;
+  uint64_t drain_sync;  // d = 64: the dQ drain threads' staging handshakes
   uint64_t drain[3];
   uint32_t tmem_base;
   int abort;
-  // Per query stage: minus the tile's LSE in the log2 domain (-inf past N)
-  // and D (0 past N), copied in with the tile from padded scratch rows.
+  uint32_t dq_join[2];  // ordered dQ: drain threads whose contribution is complete (by parity)
   __align__(16) float gk[128];  // K-RMSNorm gain (d entries)
   __align__(16) float wsum[4][64];  // d = 64 epilogue: per-warp dgk column sums
   float dgk_cta[128];               // this CTA's dgk partial, summed over its units in unit order
-  __align__(16) float nlse2[3][128];
-  __align__(16) float delta[3][128];
 };
 
 __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
@@ -218,13 +272,14 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
 
 template <int D, class W>
 __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
-                             const CUtensorMap* mdo, uint8_t* sm, BwdBars& bars, const W& w,
-                             const float* nlse2_pad, const float* delta_pad, uint32_t* dev_err) {
+                             const CUtensorMap* mdo, const CUtensorMap* mstats, uint8_t* sm, BwdBars& bars,
+                             const W& w, const float* nlse2_pad, const float* delta_pad, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(mq);
   tma_prefetch_desc(mk);
   tma_prefetch_desc(mv);
   tma_prefetch_desc(mdo);
+  if constexpr (C::kStatsFold) tma_prefetch_desc(mstats);
   volatile int* ab = &bars.abort;
   int nkv_issued = 0, nq_issued = 0, ndo_issued = 0;
   bool ok = true;
@@ -244,11 +299,16 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
       const int t = tb + i;
       const int qs = t % C::kQStages;
       if (t >= C::kQStages && !(ok = mbar_wait(&bars.q_empty[qs], ((t / C::kQStages) - 1) & 1, ab, dev_err))) break;
-      mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
       const int qi = un.query_tile(i);
-      const size_t prow = static_cast<size_t>(bh) * w.seg.prows + un.prow0 + static_cast<size_t>(qi) * 128;
-      bulk_load(bars.nlse2[qs], nlse2_pad + prow, 512, &bars.q_full[qs]);
-      bulk_load(bars.delta[qs], delta_pad + prow, 512, &bars.q_full[qs]);
+      if constexpr (C::kStatsFold) {
+        mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + C::kStatsChunk);
+        tma_load_3d(sm + C::kOffStats + qs * C::kStatsChunk, mstats, &bars.q_full[qs], 0, un.prow0 + qi * 128, bh);
+      } else {
+        mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
+        const size_t prow = static_cast<size_t>(bh) * w.seg.prows + un.prow0 + static_cast<size_t>(qi) * 128;
+        bulk_load(C::nlse2(sm, qs), nlse2_pad + prow, 512, &bars.q_full[qs]);
+        bulk_load(C::delta(sm, qs), delta_pad + prow, 512, &bars.q_full[qs]);
+      }
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, un.row0 + qi * 128,
                     bh);
@@ -324,6 +384,19 @@ __device__ __forceinline__ void mma_dk(uint32_t tmem_d, uint64_t a, uint64_t b, 
   }
 }
 
+// dK (+)= dS^T Q with dS^T in TMEM over the dP^T columns (queries 0-63
+// packed in columns [0,32), queries 64-127 in [64,96)), B = Q tile stored
+// query-rows x d (MN-major).
+template <int D>
+__device__ __forceinline__ void mma_dk_ts(uint32_t tmem_d, uint32_t tmem_ds, uint64_t b, bool accumulate) {
+  using C = BwdCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+    umma_bf16_ts(tmem_d, tmem_ds + acol, dadd(b, kk * 2048), C::kIdescKM, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 // dQ = dS K: A = dS read from the dS^T tile (MN-major), B = K tile stored
 // key-rows x d (MN-major); K = 128 keys.
 template <int D>
@@ -335,9 +408,10 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
   }
 }
 
-// Three-issuer backward (d = 64).  Recompute issuer: S(t) = K Q_t^T once
-// the compute groups hold S(t-1) in registers, dP(t) = V dO_t^T once they
-// hold dP(t-1).  Gradient issuer: dV(t) from P^T in TMEM, dK(t) from dS^T in
+// Three-issuer backward (d = 64).  Recompute issuer: S(t) = K Q_t^T - LSE /
+// scale once the compute groups hold S(t-1) in registers, dP(t) = V dO_t^T -
+// D once they hold dP(t-1) (the statistics by one more K step each, from the
+// query stage's statistics chunk).  Gradient issuer: dV(t) from P^T in TMEM, dK(t) from dS^T in
 // shared memory.  dQ issuer: dQ(t) from dS^T.  Every shared buffer is
 // released by a commit from each of its two readers: a Q stage (S, dK), a dO
 // stage (dP, dV), the dS^T tile (dK, dQ) and a K/V buffer (the unit's last
@@ -349,6 +423,11 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
   volatile int* ab = &bars.abort;
   auto kQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16, 1024); };
   auto kDO = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16, 1024); };
+  auto kSt = [=](int t) {
+    return sdesc_sw32_kmajor(smem_u32(sm + C::kOffStats + (t % C::kQStages) * C::kStatsChunk), 256u);
+  };
+  const uint64_t kOnesS = sdesc_sw32_kmajor(smem_u32(sm + C::kOffConst), 0u);
+  const uint64_t kOnesD = sdesc_sw32_kmajor(smem_u32(sm + C::kOffConst + C::kConstAtom), 0u);
   bool ok = true;
   int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
@@ -363,14 +442,19 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
       tc_fence_after();
       mma_kk<D>(tmem + C::kColS, kK, kQ(t), C::kIdescSS);
+      if constexpr (C::kStatsFold) umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t), C::kIdescSS, 1u);
       umma_commit(&bars.s_full);
-      umma_commit(&bars.q_empty[t % C::kQStages]);
-      if (t > 0 && !(ok = mbar_wait(&bars.dp_free, (t - 1) & 1, ab, dev_err))) break;
+      // dK(t-1) has read dS^T(t-1) from the dP^T columns (so the compute
+      // groups are done with dP^T(t-1) too).
+      if (t > 0 && !(ok = mbar_wait(&bars.dk_done, (t - 1) & 1, ab, dev_err))) break;
       if (!(ok = mbar_wait(&bars.do_full[t % C::kDOStages], (t / C::kDOStages) & 1, ab, dev_err))) break;
       tc_fence_after();
       mma_kk<D>(tmem + C::kColDP, kV, kDO(t), C::kIdescSS);
+      if constexpr (C::kStatsFold) umma_bf16_ss(tmem + C::kColDP, kOnesD, kSt(t), C::kIdescSS, 1u);
       umma_commit(&bars.dp_full);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
+      // The query stage (and its statistics chunk) is done with here.
+      umma_commit(&bars.q_empty[t % C::kQStages]);
     }
     tb += nkt;
     if (ok) umma_commit(&bars.kv_mmadone[b]);
@@ -388,7 +472,6 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
   auto mDO = [=](int t) {
     return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16384, 1024);
   };
-  const uint64_t kDS = sdesc_sw128(smem_u32(sm + C::kOffDS), 16, 1024);
   bool ok = true;
   int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
@@ -407,9 +490,9 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
       if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_k, (ui - 1) & 1, ab, dev_err))) break;
       tc_fence_after();
-      mma_dk<D>(tmem + C::kColDK, kDS, mQ(t), i > 0);
+      mma_dk_ts<D>(tmem + C::kColDK, tmem + C::kColDP, mQ(t), i > 0);
       umma_commit(&bars.q_empty[t % C::kQStages]);
-      umma_commit(&bars.ds_free[0]);
+      umma_commit(&bars.dk_done);
     }
     tb += nkt;
     if (ok) umma_commit(&bars.acc_full);
@@ -559,12 +642,14 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
       const int t = t0 + i;
       const int qs = t % C::kQStages;
       bool ok = mbar_wait(&bars.s_full, t & 1, ab, dev_err);
-      // This stage's LSE / D arrived with the query tile (already complete).
-      if (ok) ok = mbar_wait(&bars.q_full[qs], (t / C::kQStages) & 1, ab, dev_err);
+      // d = 128: this stage's LSE / D arrived with the query tile (already complete).
+      if (!C::kStatsFold && ok) ok = mbar_wait(&bars.q_full[qs], (t / C::kQStages) & 1, ab, dev_err);
       if (!__all_sync(0xffffffffu, ok)) return;
       tc_fence_after();
       // P^T = exp2(s log2e S^T - LSE log2e), packed bf16 pairs into TMEM
       // (chunk c -> 16 packed columns at 16c).  Key rows past N get P = 0.
+      // d = 64: TMEM holds S^T - LSE / scale, so only the product by
+      // s log2e remains.
       uint32_t pp[32];
       // Both 32-column chunks of this group's S^T in flight at once.
       uint32_t sall[2][32];
@@ -578,10 +663,20 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint32_t(&s)[32] = sall[c];
-        if (key_live) {  // warp-uniform except in a head's last key tile
+        if (key_live && C::kStatsFold) {  // warp-uniform except in a head's last key tile
+          const uint64_t zero2 = f2_make(0.f, 0.f);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(&bars.nlse2[qs][64 * g + c * 32 + e]);
+            float x0, x1, x2, x3;
+            f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, zero2), x0, x1);
+            f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), sc2, zero2), x2, x3);
+            pp[(c * 32 + e) / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+            pp[(c * 32 + e) / 2 + 1] = pack_bf16x2(ex2_approx(x2), ex2_approx(x3));
+          }
+        } else if (key_live) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(C::nlse2(sm, qs) + 64 * g + c * 32 + e);
             float x0, x1, x2, x3;
             f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, f2_make(l4.x, l4.y)), x0,
                      x1);
@@ -618,10 +713,8 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
       tmem_ld32(tDP, dpall[0]);
       tmem_ld32(tDP + 32, dpall[1]);
       tmem_wait_ld();
-      if (C::kSplitIssuers) {  // dP^T is in registers: dP(t+1) may overwrite it
-        tc_fence_before();
-        mbar_arrive(&bars.dp_free);
-      }
+      // d = 64: dS^T(t) goes over this group's dP^T(t) columns (packed like
+      // P^T), where dK(t) reads it; dP(t+1) is issued once dK(t) is done.
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint32_t(&dpv)[32] = dpall[c];
@@ -629,8 +722,19 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           const int col = c * 32 + e;  // query column within this group's 64
-          const float4 d0 = *reinterpret_cast<const float4*>(&bars.delta[qs][64 * g + col]);
-          const float4 d1 = *reinterpret_cast<const float4*>(&bars.delta[qs][64 * g + col + 4]);
+          if constexpr (C::kStatsFold) {
+            // dS = P * bf16(dP - D), dP - D from TMEM: one pack, one bf16x2 product
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              dsw[e / 2 + h] = bf16x2_mul(pp[col / 2 + h], pack_bf16x2(__uint_as_float(dpv[e + 2 * h]),
+                                                                         __uint_as_float(dpv[e + 2 * h + 1])));
+            st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
+                         dsw[e / 2 + 2], dsw[e / 2 + 3]);
+            if (e == 24) tmem_st16(tDP + c * 16, dsw);  // dS^T for dK
+            continue;
+          }
+          const float4 d0 = *reinterpret_cast<const float4*>(C::delta(sm, qs) + 64 * g + col);
+          const float4 d1 = *reinterpret_cast<const float4*>(C::delta(sm, qs) + 64 * g + col + 4);
           const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -645,6 +749,7 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
                        dsw[e / 2 + 2], dsw[e / 2 + 3]);
         }
       }
+      if (C::kSplitIssuers) tmem_wait_st();
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&bars.ds_ready);
@@ -652,30 +757,135 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
   }
 }
 
-// Warps 8-11.  Per query tile: dQ_t from TMEM into a padded shared-memory
-// row (one thread per query row), then a bulk fp32 reduce-add of the row
-// into the global accumulator.  Per unit, once its accumulators are final
-// (one thread per key row):
+// Shared-memory fetch-and-add with acquire-release semantics at CTA scope.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta_shared(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+  return old;
+}
+
+// d = 64, warps 8-11 (one thread per query row): per query tile, dQ_t out of
+// TMEM into registers and its columns released, then into the two staging
+// halves (columns 0-31 and 32-63, 128-byte rows with 16-byte chunks XOR-ed
+// by row % 8, so that the row-per-thread writes are free of bank conflicts),
+// each added into the fp32 accumulator by one TMA tensor reduce issued by
+// thread 0.  Rows past the tensor's end are clipped by the TMA unit; rows of
+// the tile that belong to the next segment receive exact zeros (their
+// probabilities are 0).  Thread 0 waits for the previous tile's reduces to
+// have read the staging before the halves are rewritten.  Ordered modes:
+// thread 0 also waits, before the tile's reduces, until the contributions of
+// lower rank to the query tile are complete (its counter), and announces its
+// own once they are complete (at the next tile, or at once for a unit's
+// last).
+template <int D, bool kOrd, class W>
+__device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, const CUtensorMap* mdq,
+                            uint32_t* __restrict__ counters, uint32_t* dev_err) {
+  using C = BwdCfg<D>;
+  static_assert(D == 64, "tiled dQ drain serves d = 64");
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r128 = (warp & 3) * 32 + lane;  // query row == TMEM lane
+  const bool leader = r128 == 0;
+  const uint32_t tQ = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColDQ;
+  uint8_t* stage = sm + C::kOffDQ;
+  const uint32_t srow = smem_u32(stage) + static_cast<uint32_t>(r128 * 128);
+  const uint32_t swz = static_cast<uint32_t>(r128 & 7);
+  volatile int* ab = &bars.abort;
+  if (leader) tma_prefetch_desc(mdq);
+  uint32_t uses = 0;
+  // Bounded barrier among the 128 drain threads.
+  auto drain_sync = [&]() -> bool {
+    mbar_arrive(&bars.drain_sync);
+    const bool okb = mbar_wait(&bars.drain_sync, (uses++) & 1, ab, dev_err);
+    return __all_sync(0xffffffffu, okb) && !*ab;
+  };
+  uint32_t* pend = nullptr;  // thread 0, ordered modes: the counter to announce
+  auto complete_previous = [&]() {
+    if (!pend) return;
+    bulk_wait_group0();
+    fence_proxy_async_global();
+    red_release_gpu_add(pend, 1u);
+    pend = nullptr;
+  };
+  bool ok = true;
+  const int tiles_per_head = w.seg.prows / 128;
+  int tb = 0;  // query tiles of the previous units
+  for (int u = blockIdx.x; ok && u < w.units; u += gridDim.x) {
+    const BwdUnit un = w.unit(u);
+    const int t0 = tb;
+    tb += un.nkt;
+    for (int i = 0; i < un.nkt; ++i) {
+      const int t = t0 + i;
+      const int qt = un.query_tile(i), rank = un.rank(i);
+      uint32_t* cnt = counters + static_cast<size_t>(un.bh) * tiles_per_head + un.prow0 / 128 + qt;
+      // Ordered modes: the counter read ahead (its latency overlaps the wait for dQ).
+      const uint32_t seen = kOrd && leader && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
+      ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      uint32_t a[D];
+      tmem_ld32(tQ, *reinterpret_cast<uint32_t(*)[32]>(a));
+      tmem_ld32(tQ + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.dq_free);
+      if (leader) {
+        if constexpr (kOrd) {
+          complete_previous();
+          if (rank > 0 && seen < static_cast<uint32_t>(rank)) gwait_geq(cnt, static_cast<uint32_t>(rank), ab, dev_err);
+          fence_proxy_async_global();  // the lower ranks' sums before this tile's reduces
+        }
+        bulk_wait_group_read0();  // the previous tile's reduces have read the staging
+      }
+      if (!(ok = drain_sync())) break;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int e = h * 32 + 4 * c;
+          st_shared_v4(srow + h * 16384 + ((static_cast<uint32_t>(c) ^ swz) << 4), a[e], a[e + 1], a[e + 2], a[e + 3]);
+        }
+      fence_proxy_async_smem();
+      if (!(ok = drain_sync())) break;
+      if (leader) {
+        const int row = un.row0 + qt * 128;
+        tma_reduce_add_3d(mdq, stage, 0, row, un.bh);
+        tma_reduce_add_3d(mdq, stage + 16384, 32, row, un.bh);
+        bulk_commit_group();
+        if constexpr (kOrd) {
+          if (rank != un.nkt - 1) {
+            pend = cnt;
+            if (i == un.nkt - 1) complete_previous();
+          }
+        }
+      }
+    }
+  }
+  if (leader) {
+    if constexpr (kOrd)
+      if (ok) complete_previous();
+    bulk_wait_group0();
+  }
+}
+
+// d = 128, warps 8-11.  Per query tile: dQ_t from TMEM into a padded
+// shared-memory row (one thread per query row), 32 columns per pass, then a
+// bulk fp32 reduce-add (ordered modes: the first contribution a bulk store)
+// of the row into the global accumulator.  Per unit, once its accumulators
+// are final (one thread per key row):
 //   dv = bf16(dV acc);
 //   dk_hat = scale * dK acc; u = g * dk_hat; dk = r u - (r^3/d) k sum(u k);
 //   dgk partial = column sums over the tile's rows of dk_hat * k * r, in a
-//   fixed order.
-// The accumulators are read out of TMEM and released first, so that the next
-// unit's first dV / dK products wait only for that.  d = 64 then runs the
-// rest through the staging rows (free between two dQ drains) as 128-byte-row
-// tiles, so that the k, dk and dv rows move with contiguous 512-byte warp
-// accesses, and sums the dgk terms with a warp butterfly; d = 128 works per
-// row and sums through padded staging rows.
-template <int D, class W>
+//   fixed order, summed through the staging rows.
+template <int D, bool kOrd, class W>
 __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, float scale,
-                                   float* __restrict__ dqacc, const __nv_bfloat16* __restrict__ k_raw,
+                                   float* __restrict__ dqacc, uint32_t* __restrict__ counters,
+                                   const __nv_bfloat16* __restrict__ k_raw,
                                    const float* __restrict__ rk, __nv_bfloat16* __restrict__ dk,
                                    __nv_bfloat16* __restrict__ dv, float* __restrict__ dgk_part,
                                    uint32_t* dev_err) {
   using C = BwdCfg<D>;
+  static_assert(D == 128, "the d = 64 drain is bwd_drain64");
   constexpr int kRowFloats = C::kDQRowBytes / 4;
-  // d = 64: the epilogue warps take the unit epilogue; these warps only drain dQ.
-  constexpr bool kTiled = (D == 64);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int r128 = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQ) or key row (dV, dK)
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -692,8 +902,23 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     const bool okb = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
     return __all_sync(0xffffffffu, okb);
   };
+  // Ordered modes: the previous contribution, once this thread's row of it
+  // is complete; the last of the 128 threads announces it (release increment
+  // of its query tile's counter).
+  uint32_t* pend = nullptr;
+  uint32_t joins = 0;  // contributions joined so far (selects the parity counter)
+  auto complete_previous = [&]() {
+    if (!pend) return;
+    bulk_wait_group0();
+    fence_proxy_async_global();
+    const uint32_t old = atom_add_acq_rel_cta_shared(&bars.dq_join[joins & 1], 1u);
+    if ((old & 127u) == 127u) red_release_gpu_add(pend, 1u);
+    ++joins;
+    pend = nullptr;
+  };
   bool ok = true;
   const size_t rows = static_cast<size_t>(w.seg.rows);
+  const int tiles_per_head = w.seg.prows / 128;
   int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
     const BwdUnit un = w.unit(u);
@@ -703,44 +928,44 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     const size_t row_off = (static_cast<size_t>(bh) * rows + (key_live ? n : 0)) * D;
     const int t0 = tb;
     tb += un.nkt;
+    constexpr bool ordered = kOrd;
 
     for (int i = 0; i < un.nkt; ++i) {
       const int t = t0 + i;
+      const int qt = un.query_tile(i), rank = un.rank(i);
+      uint32_t* cnt = counters + static_cast<size_t>(bh) * tiles_per_head + un.prow0 / 128 + qt;
+      // Ordered modes: the counter is read ahead (its latency overlaps the
+      // wait for dQ); the first contribution is a plain store.
+      const uint32_t seen = ordered && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
+      const bool store = ordered && rank == 0;
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const int qrow = un.row0 + un.query_tile(i) * 128 + r128;
+      const int qrow = un.row0 + qt * 128 + r128;
       const bool q_live = qrow < un.end;
       float* grow = dqacc + (static_cast<size_t>(bh) * rows + (q_live ? qrow : 0)) * D;
-      if constexpr (kTiled) {
-        // d = 64: the whole dQ row into registers and the TMEM columns
-        // released first, then the staging row once its previous reduce has
-        // read it.
-        uint32_t a[D];
-        tmem_ld32(tQ, *reinterpret_cast<uint32_t(*)[32]>(a));
-        tmem_ld32(tQ + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars.dq_free);
-        bulk_wait_group_read0();
+      // Ordered modes: every row of the previous contribution complete and
+      // announced, then this query tile's lower ranks awaited.
+      auto in_order = [&]() -> bool {
+        if constexpr (!ordered) return true;
+        complete_previous();
+        bool oko = true;
+        if (rank > 0 && seen < static_cast<uint32_t>(rank)) oko = gwait_geq(cnt, static_cast<uint32_t>(rank), ab, dev_err);
+        fence_proxy_async_global();
+        return __all_sync(0xffffffffu, oko);
+      };
+      {
+        ok = in_order();
+        if (!ok) break;
 #pragma unroll
-        for (int q = 0; q < D / 4; ++q)
-          st_shared_v4(srow_a + q * 16, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-        fence_proxy_async_smem();
-        if (q_live) {
-          bulk_reduce_add_f32(grow, srow, D * 4);
-          bulk_commit_group();
-        }
-      } else {
-  #pragma unroll
         for (int pass = 0; pass < D / C::kDQCols; ++pass) {
           bulk_wait_group_read0();  // the previous reduce has finished reading the row
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < C::kDQCols / 32; ++c) {
             uint32_t a[32];
             tmem_ld32(tQ + pass * C::kDQCols + c * 32, a);
             tmem_wait_ld();
-  #pragma unroll
+#pragma unroll
             for (int q = 0; q < 8; ++q)
               st_shared_v4(srow_a + (c * 32 + q * 4) * 4, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
           }
@@ -750,23 +975,31 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
           }
           fence_proxy_async_smem();
           if (q_live) {
-            bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
+            if (store) bulk_store(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
+            else bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
             bulk_commit_group();
           }
+        }
+      }
+      // A contribution after which others wait is announced at the next
+      // query tile, or at once if it is the unit's last (ascending order).
+      if constexpr (ordered) {
+        if (rank != un.nkt - 1) {
+          pend = cnt;
+          if (i == un.nkt - 1) complete_previous();
         }
       }
     }
     if (!ok) break;
 
-    // ---- unit epilogue (d = 128; at d = 64 the epilogue warps take it) ----
-    if constexpr (kTiled) continue;
+    // ---- unit epilogue ----
     ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
     const float r = key_live ? rk[static_cast<size_t>(bh) * rows + n] : 0.f;
-    if constexpr (!kTiled) {
-      // d = 128: per-row accesses; two passes over the TMEM dK accumulator
-      // (dot, then outputs), the dgk rows staged kDQCols columns at a time.
+    {
+      // Per-row accesses; two passes over the TMEM dK accumulator (dot, then
+      // outputs), the dgk rows staged kDQCols columns at a time.
       const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
       uint4* dvrow = reinterpret_cast<uint4*>(dv + row_off);
       uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
@@ -874,7 +1107,9 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
       if (!ok) break;
     }
   }
-  if (!kTiled && r128 < C::kDQCols) {
+  if constexpr (kOrd)
+    if (ok) complete_previous();
+  if (r128 < C::kDQCols) {
 #pragma unroll
     for (int pass = 0; pass < D / C::kDQCols; ++pass)
       dgk_part[static_cast<size_t>(blockIdx.x) * D + pass * C::kDQCols + r128] = bars.dgk_cta[pass * C::kDQCols + r128];
@@ -1056,15 +1291,17 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
   if (r128 < D) dgk_part[static_cast<size_t>(blockIdx.x) * D + r128] = bars.dgk_cta[r128];
 }
 
-template <int D, class W>
+template <int D, class W, bool kOrd>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                    const __grid_constant__ W w, float scale, const float* __restrict__ nlse2_pad,
+                    const __grid_constant__ CUtensorMap map_stats, const __grid_constant__ CUtensorMap map_dq,
+                    const __grid_constant__ W w, float scale,
+                    const float* __restrict__ nlse2_pad,
                     const float* __restrict__ delta_pad, const __nv_bfloat16* __restrict__ k_raw,
                     const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
-                    __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, float* __restrict__ dgk_part,
-                    uint32_t* dev_err) {
+                    __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, uint32_t* __restrict__ counters,
+                    float* __restrict__ dgk_part, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(16) BwdBars bars;
@@ -1086,7 +1323,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars.kv_mmadone[s], n_rel);
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], n_rel);
-      mbar_init(&bars.ds_free[s], n_rel);
+      mbar_init(&bars.ds_free[s], 1);  // the dQ product (d = 64: dK reads dS^T from TMEM)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
@@ -1098,18 +1335,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.acc_free_v, 128);
     mbar_init(&bars.acc_free_k, 128);
     mbar_init(&bars.s_free, 256);
-    mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.dv_done, 1);
+    mbar_init(&bars.dk_done, 1);
     mbar_init(&bars.epi, 128);
+    mbar_init(&bars.drain_sync, 128);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
     mbar_init(&bars.drain[2], 1);
     bars.abort = 0;
+    bars.dq_join[0] = 0u;
+    bars.dq_join[1] = 0u;
     fence_mbar_init();
   }
   if (warp == kWarpMma0) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
+  }
+  if constexpr (C::kStatsFold) {
+    // The constant A chunks of the statistics K step: key rows of ones in
+    // columns 0-2 (S^T) and 3-5 (dP^T), zeros elsewhere, in the 32-byte
+    // swizzled K-major layout (16-byte half h of row r at r * 32 + 16 (h ^ bit
+    // 2 of r)); one 8-row atom each, which the descriptor repeats.
+    for (int i = threadIdx.x; i < 2 * 8 * 2; i += blockDim.x) {
+      const int which = i >> 4, r = (i >> 1) & 7, h = i & 1;
+      const uint32_t one = 0x3F80u;  // bf16 1.0
+      uint32_t w0 = 0u, w1 = 0u, w2 = 0u;
+      if (h == 0) {
+        if (which == 0) {
+          w0 = one | (one << 16);
+          w1 = one;
+        } else {
+          w1 = one << 16;
+          w2 = one | (one << 16);
+        }
+      }
+      st_shared_v4(smem_u32(sm + C::kOffConst + which * C::kConstAtom + r * 32 + ((h ^ ((r >> 2) & 1)) << 4)), w0, w1,
+                   w2, 0u);
+    }
+    fence_proxy_async_smem();  // visible to the tensor cores
   }
   griddep_wait();  // the previous grid's writes (q_hat, k_hat, LSE / D rows, zeroed dQ) are visible
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
@@ -1126,19 +1389,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
     if constexpr (D == 64) {
-      if (warp < kWarpEpi) setmaxnreg_inc<kRegDrain64>();  // up from the launch count
-      else if (warp < kWarpTma) setmaxnreg_dec<kRegEpi64>();
-      else setmaxnreg_dec<kRegMma64>();
+      if (warp >= kWarpEpi && warp < kWarpTma) setmaxnreg_dec<kRegEpi64>();
+      else if (warp >= kWarpTma) setmaxnreg_dec<kRegMma64>();
     } else {  // d = 128: the drain warps run the epilogue; one issuer
       setmaxnreg_dec<kRegOther128>();
     }
     if (warp < kWarpEpi) {
-      bwd_drain_epilogue<D>(sm, bars, tmem, w, scale, dqacc, k_raw, rk, dk, dv, dgk_part, dev_err);
+      if constexpr (D == 64) bwd_drain64<D, kOrd>(sm, bars, tmem, w, &map_dq, counters, dev_err);
+      else bwd_drain_epilogue<D, kOrd>(sm, bars, tmem, w, scale, dqacc, counters, k_raw, rk, dk, dv, dgk_part, dev_err);
     } else if (warp < kWarpTma) {
       if constexpr (D == 64) bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, k_raw, rk, dk, dv, dgk_part, dev_err);
     } else if (warp == kWarpTma) {
       if (lane == 0)
-        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, sm, bars, w, nlse2_pad, delta_pad, dev_err);
+        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, nlse2_pad, delta_pad, dev_err);
     } else if (warp == kWarpMma0) {
       if (lane == 0) {
         if (C::kSplitIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
@@ -1158,14 +1421,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, class W>
-cudaError_t launch_bwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const AttnShape& s, const float* nlse2_pad, const float* delta_pad,
+template <int D, bool kOrd, class W>
+cudaError_t launch_bwd_w(const W& w, int grid, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, const CUtensorMap& mstats, const CUtensorMap& mdq, const AttnShape& s,
+                         const float* nlse2_pad, const float* delta_pad,
                          const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
-                         float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
+                         float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
   using C = BwdCfg<D>;
   static_assert(C::kDynSmem + static_cast<int>(sizeof(BwdBars)) <= 232448, "shared memory budget");
-  auto kernel = attn_bwd_kernel<D, W>;
+  auto kernel = attn_bwd_kernel<D, W, kOrd>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   // The setmaxnreg split is valid only for the register count it was sized
@@ -1174,56 +1438,96 @@ cudaError_t launch_bwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& m
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
-  const int sms = device_sm_count();
-  const int grid = w.units < sms ? w.units : sms;
-  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, w, s.scale, nlse2_pad,
+  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, mstats, mdq, w, s.scale, nlse2_pad,
                     delta_pad, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
-                    reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, dgk_part,
-                    dev_err);
+                    reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, counters,
+                    dgk_part, dev_err);
+}
+
+// The dQ order and grid of a launch.  Arrival order unless the deterministic
+// mode is on; then the rotated order when every segment's key tiles fit on
+// the grid at once (the waits between CTAs cannot then form a cycle), else
+// the ascending order, which no wait can deadlock.  For the [B, H, N, d]
+// layout in rotated order the grid is cut to a multiple of the key tiles per
+// head when that takes no more rounds, so that no head's units straddle two
+// rounds.
+struct BwdPlan {
+  int ord;
+  int grid;
+};
+BwdPlan bwd_plan(const AttnShape& s) {
+  const int sms = device_sm_count();
+  const int units = s.BH * (s.seg.prows / 128);
+  BwdPlan p;
+  p.grid = units < sms ? units : sms;
+  p.ord = kDqArrival;
+  if (!s.deterministic) return p;
+  int max_nkt = 0;
+  for (int i = 0; i < s.seg.n; ++i) {
+    const int nkt = (s.seg.pcu[i + 1] - s.seg.pcu[i]) / 128;
+    max_nkt = nkt > max_nkt ? nkt : max_nkt;
+  }
+  p.ord = max_nkt <= p.grid ? kDqRotated : kDqAscending;
+  if (p.ord == kDqRotated && s.seg.n == 1) {
+    const int g2 = (p.grid / max_nkt) * max_nkt;
+    const int rounds = (units + p.grid - 1) / p.grid, rounds2 = (units + g2 - 1) / g2;
+    if (g2 > 0 && rounds2 == rounds) p.grid = g2;
+  }
+  return p;
 }
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const AttnShape& s, const float* nlse2_pad,
+                         const CUtensorMap& mdo, const CUtensorMap& mstats, const CUtensorMap& mdq, const AttnShape& s,
+                         const float* nlse2_pad,
                          const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk,
-                         uint16_t* dv, float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
+                         uint16_t* dv, float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err,
+                         cudaStream_t st) {
+  const BwdPlan plan = bwd_plan(s);
   if (s.seg.n == 1) {
     BwdWorkUniform w;
     w.seg.rows = s.seg.rows;
     w.seg.prows = s.seg.prows;
     w.upc = s.seg.prows / 128;
     w.units = s.BH * w.upc;
-    return launch_bwd_w<D>(w, mq, mk, mv, mdo, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc, dgk_part,
-                           dev_err, st);
+    w.ord = plan.ord;
+    if (plan.ord == kDqArrival)
+      return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+                                    dqacc, counters, dgk_part, dev_err, st);
+    return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+                                 dqacc, counters, dgk_part, dev_err, st);
   }
   BwdWork w;
   w.seg = s.seg;
   w.upc = s.seg.prows / 128;
   w.units = s.BH * w.upc;
-  return launch_bwd_w<D>(w, mq, mk, mv, mdo, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc, dgk_part,
-                         dev_err, st);
+  w.ord = plan.ord;
+  if (plan.ord == kDqArrival)
+    return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+                                  dqacc, counters, dgk_part, dev_err, st);
+  return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+                               counters, dgk_part, dev_err, st);
 }
 
 }  // namespace
 
-// One dgk partial per CTA (the grid: one CTA per SM, no more than units).
-int attn_bwd_dgk_parts(const AttnShape& s) {
-  const int units = s.BH * (s.seg.prows / 128);
-  const int sms = device_sm_count();
-  return units < sms ? units : sms;
-}
+// One dgk partial per CTA.
+int attn_bwd_dgk_parts(const AttnShape& s) { return bwd_plan(s).grid; }
+
+int attn_bwd_counter_words(const AttnShape& s) { return s.BH * (s.seg.prows / 128); }
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const CUtensorMap& map_do, const AttnShape& s, const float* nlse2_pad,
+                            const CUtensorMap& map_do, const CUtensorMap& map_stats, const CUtensorMap& map_dq,
+                            const AttnShape& s, const float* nlse2_pad,
                             const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk,
-                            uint16_t* dk, uint16_t* dv, float* dqacc, float* dgk_part, uint32_t* dev_err,
-                            cudaStream_t st) {
+                            uint16_t* dk, uint16_t* dv, float* dqacc, uint32_t* counters, float* dgk_part,
+                            uint32_t* dev_err, cudaStream_t st) {
   if (s.d == 64)
-    return launch_bwd_d<64>(map_q, map_k, map_v, map_do, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
-                            dgk_part, dev_err, st);
+    return launch_bwd_d<64>(map_q, map_k, map_v, map_do, map_stats, map_dq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+                            counters, dgk_part, dev_err, st);
   if (s.d == 128)
-    return launch_bwd_d<128>(map_q, map_k, map_v, map_do, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
-                             dgk_part, dev_err, st);
+    return launch_bwd_d<128>(map_q, map_k, map_v, map_do, map_stats, map_dq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+                             counters, dgk_part, dev_err, st);
   return cudaErrorInvalidValue;
 }
 

@@ -1,6 +1,7 @@
 // jattn_api.cu — the C ABI of libjattn (declared in include/jattn.h):
 // argument validation, per-call scratch, TMA tensor maps and the launch
 // sequence of the forward and backward passes.
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cstdio>
@@ -24,6 +25,9 @@ constexpr int kMaxDevices = 64;
 
 // Device error word written by the kernels' bounded waits (one per device).
 __device__ uint32_t g_dev_err;
+
+// Backward mode set by jattn_set_deterministic (applies to later calls).
+std::atomic<int> g_deterministic{0};
 
 // Text of the last failure seen by an entry point on this thread.
 thread_local char g_last_msg[256] = "no error";
@@ -194,14 +198,15 @@ struct Carve {
 
 size_t fwd_scratch_bytes(const Shape& s) { return 2 * (s.elems * 2 + 256) + 256; }
 
-size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k) {
+size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k, int counter_words) {
   size_t b = 0;
   b += 2 * (s.elems * 2 + 256);                                   // q_hat, k_hat
   b += 2 * (s.rows * 4 + 256);                                    // rq, rk
   b += 2 * (static_cast<size_t>(s.BH) * s.seg.prows * 4 + 256);   // nlse2, delta
+  if (attn_bwd_stats_chunks(s.d)) b += static_cast<size_t>(s.BH) * s.seg.prows * 32 + 256;  // statistics chunks
   b += s.elems * 4 + 256;                                         // dq accumulator
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
-  b += 4 + 256;                                                   // dg ticket
+  b += 4 * (1 + static_cast<size_t>(counter_words)) + 256;      // dg ticket, dQ order counters
   return b + 256;
 }
 
@@ -238,6 +243,32 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(rows) * 256};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_stats_map(CUtensorMap* map, const void* base, int BH, int prows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(prows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {32, static_cast<cuuint64_t>(prows) * 32};
+  cuuint32_t box[3] = {16, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -414,9 +445,11 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
   AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d)), s.seg};
   const int nparts_q = q_norm_bwd_parts(s.d);
+  as.deterministic = g_deterministic.load(std::memory_order_relaxed) != 0;
   const int nparts_k = attn_bwd_dgk_parts(as);
+  const int counter_words = as.deterministic ? attn_bwd_counter_words(as) : 0;
   Carve cv;
-  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k), st);
+  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k, counter_words), st);
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
   uint16_t* qhat = cv.take<uint16_t>(s.elems);
   uint16_t* khat = cv.take<uint16_t>(s.elems);
@@ -424,28 +457,36 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   float* rk = cv.take<float>(s.rows);
   float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
   float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
+  const bool chunks = attn_bwd_stats_chunks(s.d);
+  uint16_t* stats = chunks ? cv.take<uint16_t>(static_cast<size_t>(s.BH) * s.seg.prows * 16) : nullptr;
   float* dqacc = cv.take<float>(s.elems);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
   float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
-  unsigned int* dg_ticket = cv.take<unsigned int>(1);
+  // The gain-gradient ticket, then (deterministic mode) one dQ order counter
+  // per query tile; the preparation zeroes them all.
+  unsigned int* dg_ticket = cv.take<unsigned int>(1 + static_cast<size_t>(counter_words));
 
   int status = JATTN_OK;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mstats, mdqacc;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, dqacc, dg_ticket, s.BH,
-                         s.seg, s.d, err, st);
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, stats,
+                         sqrtf(static_cast<float>(s.d)), attn_bwd_dq_stores_first(as) ? nullptr : dqacc, dg_ticket,
+                         1 + counter_words, s.BH, s.seg, s.d, err, st);
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
   } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
-             !encode_bhnd_map(&mv, v, s.BH, s.N, s.d) || !encode_bhnd_map(&mdo, dout, s.BH, s.N, s.d)) {
+             !encode_bhnd_map(&mv, v, s.BH, s.N, s.d) || !encode_bhnd_map(&mdo, dout, s.BH, s.N, s.d) ||
+             !(chunks ? encode_stats_map(&mstats, stats, s.BH, s.seg.prows) : (mstats = mq, true)) ||
+             !(chunks ? encode_dq_map(&mdqacc, dqacc, s.BH, s.seg.rows) : (mdqacc = mq, true))) {
     status = fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   } else {
     const char* stage = "attn_bwd launch";
     {
       Timed t(JATTN_KERNEL_ATTN_BWD, st);
-      ce = launch_attn_bwd(mq, mk, mv, mdo, as, nlse2, delta, k, rk, gk, dk, dv, dqacc, dgk_part, err, st);
+      ce = launch_attn_bwd(mq, mk, mv, mdo, mstats, mdqacc, as, nlse2, delta, k, rk, gk, dk, dv, dqacc, dg_ticket + 1, dgk_part, err,
+                           st);
     }
     if (ce == cudaSuccess) {
       stage = "q_norm_bwd launch";
@@ -570,6 +611,17 @@ extern "C" int jattn_profile_read(int kind, int* launches, double* total_ms) {
   *launches = static_cast<int>(p.launches[kind]);
   *total_ms = p.ms[kind];
   return status;
+}
+
+extern "C" int jattn_set_deterministic(int on) {
+  g_deterministic.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
+  return JATTN_OK;
+}
+
+extern "C" int jattn_set_sm_limit(int max_sms) {
+  if (max_sms < 0) return JATTN_ERR_INVALID_ARG;
+  set_sm_limit(max_sms);
+  return JATTN_OK;
 }
 
 extern "C" const char* jattn_kernel_name(int kind) {

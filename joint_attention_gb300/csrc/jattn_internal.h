@@ -72,14 +72,23 @@ struct Scratch {
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                                uint16_t* qhat, uint16_t* khat, int64_t rows, int d, uint32_t* dev_err,
                                cudaStream_t st);
-// Rows are the BH heads' seg.rows rows; nlse2 (= -LSE log2 e) and delta are
-// written in the per-head padded layout (segment s from seg.pcu[s], 128-row
-// multiples), with -inf / 0 in the pad rows.
+// Rows are the BH heads' seg.rows rows.  The softmax statistics are written
+// in the per-head padded layout (segment s from seg.pcu[s], 128-row
+// multiples): with `stats` null, nlse2 (= -LSE log2 e, -inf in pad rows) and
+// delta (D, 0 in pad rows) as fp32; otherwise `stats` gets 16 bf16 per row,
+// -LSE * inv_scale and -D each as three bf16 terms whose sum rounds to the
+// fp32 value (columns 0-2 and 3-5; pad rows -1e30 and 0), zeros after.  The
+// dq accumulator rows are zeroed unless dqacc is null (the deterministic
+// backward stores its first contribution); the first n_tickets words of
+// `tickets` are zeroed.
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
-                            unsigned int* tickets, int BH, const SegTable& seg, int d, uint32_t* dev_err,
-                            cudaStream_t st);
+                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,
+                            float inv_scale, float* dqacc, unsigned int* tickets, int n_tickets, int BH,
+                            const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st);
+// Whether the attention backward takes the statistics as the bf16 chunks
+// above (and a TMA map over them) rather than as fp32 rows.
+inline bool attn_bwd_stats_chunks(int d) { return d == 64; }
 // nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq
 // partials; the last one (by *ticket, zeroed by the backward preparation)
 // sums them and the nk dgk partials into dgq and dgk.
@@ -88,8 +97,11 @@ cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float
                               unsigned int* ticket, float* dgq, float* dgk, int d, uint32_t* dev_err,
                               cudaStream_t st);
 int q_norm_bwd_parts(int d);
-// Streaming multiprocessors of the current device (cached after the first call).
+// Streaming multiprocessors of the current device (cached after the first
+// call), or the limit set by set_sm_limit if that is lower: the number of
+// CTAs the persistent kernels launch.
 int device_sm_count();
+void set_sm_limit(int n);  // n <= 0: no limit
 
 // --- tensor-core attention kernels ------------------------------------------
 struct AttnShape {
@@ -98,19 +110,38 @@ struct AttnShape {
   int d;
   float scale;   // 1/sqrt(d)
   SegTable seg;  // the heads' segments (one segment [0, N) for the [B, H, N, d] layout)
+  bool deterministic = false;  // backward: fixed dQ accumulation order
 };
 
 cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st);
 
+// map_stats: a TMA map over the bf16 statistics chunks (encode_stats_map) and
+// map_dq one over the fp32 dQ accumulator (encode_dq_map) when
+// attn_bwd_stats_chunks(d), else unused.  The accumulator must be zeroed
+// unless attn_bwd_dq_stores_first(s).
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const CUtensorMap& map_do, const AttnShape& s, const float* nlse2_pad,
+                            const CUtensorMap& map_do, const CUtensorMap& map_stats, const CUtensorMap& map_dq,
+                            const AttnShape& s, const float* nlse2_pad,
                             const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
-                            float* dqacc, float* dgk_part, uint32_t* dev_err, cudaStream_t st);
+                            float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st);
+// CTAs of the backward launch (one dgk partial each) and, for the
+// deterministic mode, the counter words it needs zeroed (one per query tile).
 int attn_bwd_dgk_parts(const AttnShape& s);
+int attn_bwd_counter_words(const AttnShape& s);
+// Whether the first dQ contribution to each query tile is stored rather than
+// added (the deterministic mode at d = 128), so that the accumulator needs no
+// zeroing.
+inline bool attn_bwd_dq_stores_first(const AttnShape& s) { return s.deterministic && s.d == 128; }
 
 // Encodes a 3-D TMA map over a [BH, N, d] bf16 tensor with a (64, 128, 1)
 // box and 128-byte swizzle.  Returns false if the driver rejects it.
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+// A 3-D TMA map over [BH, prows, 16] bf16 statistics chunks with a
+// (16, 128, 1) box and 32-byte swizzle.
+bool encode_stats_map(CUtensorMap* map, const void* base, int BH, int prows);
+// A 3-D TMA map over a [BH, rows, 64] fp32 accumulator with a (32, 128, 1)
+// box and 128-byte swizzle.
+bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows);
 
 }  // namespace jattn

@@ -12,6 +12,8 @@
 // d/8-lane group.  The streaming kernels hold no shared memory and meet no
 // block barrier: every thread loads its next rows while it transforms the
 // current ones (register double buffering), and grids fill every SM.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "jattn_internal.h"
@@ -240,16 +242,30 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
 // accumulator row; pad rows get -LSE = -inf and D = 0 so the attention
 // backward sees zero probabilities.  Each thread loads its next row while it
 // transforms the current one.
+// x as three bf16 terms (bit patterns), each the round-to-nearest of what
+// the previous ones leave (each remainder is exact in fp32): their sum is
+// within 2^-24 |x| of x.
+__device__ __forceinline__ void split3_bf16(float x, uint32_t (&h)[3]) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    h[i] = __bfloat16_as_ushort(b);
+    x -= __bfloat162float(b);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
-    float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, float4* __restrict__ dqacc,
-    unsigned int* __restrict__ tickets, int n_tickets, const __grid_constant__ SegTable seg, int64_t padded_rows) {
+    float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, uint4* __restrict__ stats,
+    float inv_scale, float4* __restrict__ dqacc, unsigned int* __restrict__ tickets, int n_tickets,
+    const __grid_constant__ SegTable seg, int64_t padded_rows) {
   griddep_launch_dependents();
   griddep_wait();
-  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < n_tickets) tickets[threadIdx.x] = 0u;
+  for (int i = blockIdx.x * kNormThreads + threadIdx.x; i < n_tickets; i += gridDim.x * kNormThreads)
+    tickets[i] = 0u;
   constexpr int TPR = D / 8;
   constexpr int RPB = kNormThreads / TPR;
   const int sub = threadIdx.x % TPR;
@@ -311,7 +327,17 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     for (int i = 0; i < 8; ++i) dot = fmaf(o[i], dd[i], dot);
     dot = row_sum<TPR>(dot);
     if (in_range) {
-      if (sub == 0) {
+      if (stats) {
+        // Two 16-byte halves per row: the split statistics, then zeros.
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (sub == 0) {
+          uint32_t l[3], dd3[3];
+          split3_bf16(valid ? -cur.lse * inv_scale : -1e30f, l);
+          split3_bf16(valid ? -dot : 0.f, dd3);
+          v = make_uint4(l[0] | (l[1] << 16), l[2] | (dd3[0] << 16), dd3[1] | (dd3[2] << 16), 0u);
+        }
+        if (sub < 2) stats[prow * 2 + sub] = v;
+      } else if (sub == 0) {
         nlse2[prow] = valid ? -cur.lse * 1.4426950408889634f : -INFINITY;
         delta[prow] = valid ? dot : 0.f;
       }
@@ -319,9 +345,11 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
         const int64_t idx = row * TPR + sub;
         qhat[idx] = yq;
         khat[idx] = yk;
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        dqacc[idx * 2] = z;
-        dqacc[idx * 2 + 1] = z;
+        if (dqacc) {
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          dqacc[idx * 2] = z;
+          dqacc[idx * 2 + 1] = z;
+        }
         if (sub == 0) {
           rq[row] = r1;
           rk[row] = r2;
@@ -470,6 +498,8 @@ __global__ void __launch_bounds__(kQBwdThreads) q_norm_bwd_kernel(const float4* 
   }
 }
 
+std::atomic<int> g_sm_limit{0};
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -477,7 +507,8 @@ int sm_count() {
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
   }
-  return n;
+  const int lim = g_sm_limit.load(std::memory_order_relaxed);
+  return lim > 0 && lim < n ? lim : n;
 }
 
 // As many 256-thread blocks as fit on every SM (from the kernel's
@@ -496,6 +527,8 @@ int row_grid(Kernel kernel, int64_t rows, int d) {
 }  // namespace
 
 int device_sm_count() { return sm_count(); }
+
+void set_sm_limit(int n) { g_sm_limit.store(n > 0 ? n : 0, std::memory_order_relaxed); }
 
 int q_norm_bwd_parts(int d) {
   int per_sm = 1;
@@ -520,17 +553,17 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, float* dqacc,
-                            unsigned int* tickets, int BH, const SegTable& seg, int d, uint32_t* dev_err,
-                            cudaStream_t st) {
+                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,
+                            float inv_scale, float* dqacc, unsigned int* tickets, int n_tickets, int BH,
+                            const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st) {
   (void)dev_err;
   const int64_t padded_rows = static_cast<int64_t>(BH) * seg.prows;
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
   auto kernel = d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>;
   return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
                     gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
-                    rk, nlse2, delta, reinterpret_cast<float4*>(dqacc), tickets, 1, seg,
-                    padded_rows);
+                    rk, nlse2, delta, reinterpret_cast<uint4*>(stats), inv_scale, reinterpret_cast<float4*>(dqacc),
+                    tickets, n_tickets, seg, padded_rows);
 }
 
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,

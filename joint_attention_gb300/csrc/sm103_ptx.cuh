@@ -111,6 +111,49 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
+// Cross-CTA ordering through a global counter: a release increment by the
+// producer of some data, and a bounded acquire poll by its consumer.  Like
+// mbar_wait, the poll gives up after kWaitLimitNs (raising the CTA's abort
+// flag and the device error word) or as soon as another role of the CTA has
+// aborted.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool gwait_geq(const uint32_t* p, uint32_t target, volatile int* cta_abort,
+                                          uint32_t* dev_err) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 15u) == 0u) {
+      if (*cta_abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *cta_abort = 1;
+        if (dev_err) atomicOr(dev_err, DEV_ERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// Orders this thread's async-proxy accesses of global memory (completed bulk
+// copies and reductions) with its generic-proxy accesses, in both directions.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Asynchronous 16-byte global -> shared copies (L2 only), completed by this
+// thread's cp.async.wait_group; the data is then visible to this thread.
+__device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sdst), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Shared-memory 16-byte store.
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -151,6 +194,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
                : "memory");
+}
+// TMA tiled fp32 add-reduction shared -> global (bulk-group completion):
+// the box is added element-wise into the tensor; box rows past the tensor's
+// extent are not written.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
 }
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
@@ -307,6 +361,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1u) << 46;
   d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor, 32-byte swizzle, K-major: one 16-element
+// bf16 K slice per 32-byte row, 8-row atoms sbo_bytes apart (256: the layout a
+// TMA load with CU_TENSOR_MAP_SWIZZLE_32B and a 32-byte inner box writes; 0:
+// every 8-row group reads the same atom).
+__device__ __forceinline__ uint64_t sdesc_sw32_kmajor(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;           // leading offset: unused within one swizzle row
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(6u) << 61;           // SWIZZLE_32B
   return d;
 }
 

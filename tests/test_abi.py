@@ -146,3 +146,14 @@ def test_bwd_varlen_validation(lib, kw, expect):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(FileNotFoundError):
         ja.load_library(str(tmp_path / "missing.so"))
+
+
+def test_mode_switches_validate_and_apply_to_later_calls(lib):
+    # The CTA cap and the deterministic-backward switch take effect on later
+    # calls; only a negative cap is rejected.  Nothing runs on a device here.
+    assert ja.jattn_set_sm_limit(0) == 0
+    assert ja.jattn_set_sm_limit(7) == 0
+    assert ja.jattn_set_sm_limit(0) == 0
+    assert lib.jattn_set_sm_limit(-1) == ja.STATUS_CODE["JATTN_ERR_INVALID_ARG"]
+    assert ja.jattn_set_deterministic(True) == 0
+    assert ja.jattn_set_deterministic(False) == 0

@@ -148,9 +148,10 @@ def test_token_permutation_equivariance(ja):
 
 
 def test_output_margins_untouched_and_dg_deterministic(ja):
-    # Four key tiles: dq's fp32 reduce-adds land in arrival order, so dq and
-    # dgq (summed from dq's accumulator) agree to rounding only; dk, dv and
-    # dgk are summed in a fixed order and repeat bit for bit.
+    # Four key tiles: in the default mode dq's fp32 reduce-adds land in
+    # arrival order, so dq and dgq (summed from dq's accumulator) agree to
+    # rounding only; dk, dv and dgk are summed in a fixed order and repeat
+    # bit for bit.
     B, H, N, d = 1, 2, 500, 128
     inp = make_inputs(B, H, N, d, seed=9)
     e, r, pad = B * H * N * d, B * H * N, 4096
@@ -182,6 +183,34 @@ def test_output_margins_untouched_and_dg_deterministic(ja):
         a, b = first[n].double(), bufs[n][1].double()
         assert float((a - b).norm() / b.norm()) < 1e-3, n
     assert ja.jattn_last_device_error() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_deterministic_mode_repeats_bit_for_bit(ja, d):
+    """jattn_set_deterministic(1): dq's accumulator takes the key tiles'
+    contributions in a fixed order, so every gradient repeats bit for bit over
+    repeated calls (the full 512 px launch at d = 64; four key tiles at
+    d = 128), and still matches the oracle."""
+    if d == 64:
+        cfg = CONFIGS["512px"]
+        inp, n_txt = make_config_inputs(cfg), cfg.N_txt
+    else:
+        inp, n_txt = make_inputs(2, 3, 500, 128, seed=19), 77
+    try:
+        ja.jattn_set_deterministic(True)
+        runs = [run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, n_txt) for _ in range(3)]
+    finally:
+        ja.jattn_set_deterministic(False)
+    for key in ("dq", "dk", "dv", "dgq", "dgk", "O", "LSE"):
+        assert np.array_equal(runs[0][key], runs[1][key]) and np.array_equal(runs[0][key], runs[2][key]), key
+    B, H = inp.q.shape[:2]
+    heads = _sampled_heads(B, H)
+    ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, heads=heads)
+    for b, h in heads:
+        g = {key: runs[0][key][b, h] for key in ("O", "LSE", "dq", "dk", "dv")}
+        rr = {key: ref[key][b, h] for key in ("O", "LSE", "dq", "dk", "dv")}
+        check_fwd(g, rr, f"deterministic d={d} head {(b, h)}")
+        check_bwd(g, rr, keys=("dq", "dk", "dv"), where=f"deterministic d={d} head {(b, h)}")
 
 
 # ---------------------------------------------------------------------------
@@ -265,6 +294,10 @@ def test_cfg_sampling_workload(ja):
     (64, 12, 24, 7),      # 768 heads of one ragged tile each
     (8, 20, 129, 77),     # 160 heads of two tiles (one of them a single row)
     (4, 39, 256, 100),    # 156 heads of exactly two full tiles
+    # 104 heads of three forward units, the last without a second query
+    # tile: with 152 CTAs (152 mod 3 = 2) some CTAs' first unit has one query
+    # tile and their second has two; backward: five key tiles per head
+    (8, 13, 600, 77),
 ])
 def test_unit_scheduling(ja, B, H, N, n_txt, d):
     inp = make_inputs(B, H, N, d, seed=7000 + B * H + N + d)
@@ -273,6 +306,36 @@ def test_unit_scheduling(ja, B, H, N, n_txt, d):
     where = f"B={B} H={H} N={N} d={d}"
     check_fwd(got, ref, where)
     check_bwd(got, ref, where=where)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("sm_limit,B,H,N", [
+    (2, 2, 3, 333),     # 3 key tiles per head on 2 CTAs: ascending dQ order
+    (8, 1, 3, 1101),    # 9 key tiles on 8 CTAs: ascending
+    (9, 2, 3, 1101),    # 9 key tiles on 9 CTAs: rotated, one head per round
+    (7, 3, 5, 333),     # rotated on 7 CTAs, heads straddling rounds (45 units)
+    (5, 1, 2, 2381),    # 19 key tiles on 5 CTAs: ascending, several rounds per head
+])
+def test_dq_orders_under_a_cta_cap(ja, sm_limit, B, H, N, d):
+    """The deterministic backward's two dQ accumulation orders (rotated when
+    every key tile of a head fits on the grid at once, ascending otherwise),
+    forced on small problems by capping the CTAs: parity with the oracle, and
+    every output repeats bit for bit."""
+    inp = make_inputs(B, H, N, d, seed=9100 + sm_limit + N + d)
+    try:
+        ja.jattn_set_sm_limit(sm_limit)
+        ja.jattn_set_deterministic(True)
+        got = run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, 77)
+        again = run_gpu(ja, inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout, 77)
+    finally:
+        ja.jattn_set_sm_limit(0)
+        ja.jattn_set_deterministic(False)
+    ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    where = f"cap={sm_limit} B={B} H={H} N={N} d={d}"
+    check_fwd(got, ref, where)
+    check_bwd(got, ref, where=where)
+    for key in got:
+        assert np.array_equal(got[key], again[key]), (where, key)
 
 
 @pytest.mark.parametrize("d", [64, 128])
