@@ -18,7 +18,7 @@
 // load and first S / dP products overlap the current unit's last tiles and
 // its epilogue.
 // 640 threads (five warpgroups; setmaxnreg gives the compute warpgroups 128
-// registers per thread, the drain 96, the epilogue 72 and TMA / MMA 48):
+// registers per thread, the drain 88, the epilogue 88 and TMA / MMA 48):
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
@@ -66,15 +66,16 @@ namespace {
 constexpr int kBwdThreads = 640;  // 5 warpgroups
 // Warp roles: 0-7 compute (two groups), 8-11 dQ drain, 12-15 epilogue
 // (d = 64), 16 TMA, 17-19 MMA issuers.  Registers per thread (setmaxnreg):
-// compute 128, drain 96, epilogue 72, TMA / issuers 48 (d = 128: 72 for all
-// but compute); 256 x 128 + 128 x (96 + 72 + 48) = 256 x 128 + 384 x 72 =
-// 60416 of the 640 x 96 the block launches with.
+// compute 128, drain 88, epilogue 88, TMA / issuers 48 (d = 128: 72 for all
+// but compute); 256 x 128 + 128 x (88 + 88 + 48) = 61440, the 640 x 96 the
+// block launches with (d = 128: 256 x 128 + 384 x 72 = 60416).
 // setmaxnreg budgets.  An increase must not be below, a decrease not above,
 // the count the kernel launches with, and the sum must fit the launch's
 // registers (640 x that count); the launcher checks both against the
 // compiled kernel before every launch.
-constexpr int kRegCompute = 128, kRegDrain64 = 96, kRegEpi64 = 72, kRegMma64 = 48, kRegOther128 = 72;
-// The d = 64 drain warps keep the count the kernel launches with.
+constexpr int kRegCompute = 128, kRegDrain64 = 88, kRegEpi64 = 88, kRegMma64 = 48, kRegOther128 = 72;
+// The split uses the whole launch allocation (640 x 96): the kernel must launch
+// with exactly 96 registers per thread.
 constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
 // Each SM sub-partition holds one warp of every warpgroup (warp w on w % 4)
 // and 16384 registers, so one warp of each role must fit there too.
@@ -86,7 +87,7 @@ static_assert(256 * kRegCompute + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <=
 static_assert(256 * kRegCompute + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
               "d = 128 register split exceeds the launch allocation");
 static_assert(kRegEpi64 <= kRegLaunchMin && kRegMma64 <= kRegLaunchMin && kRegOther128 <= kRegLaunchMin &&
-                  kRegDrain64 == kRegLaunchMax && kRegCompute >= kRegLaunchMax,
+                  kRegDrain64 <= kRegLaunchMin && kRegCompute >= kRegLaunchMax,
               "setmaxnreg direction");
 constexpr int kWarpEpi = 12;
 constexpr int kWarpTma = 16;
@@ -1187,6 +1188,15 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
                      pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5])),
                      pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7])));
     }
+    // dK out of TMEM into registers and its columns released at once: the
+    // next unit's first dK product (and through it the next dP product)
+    // waits for this read only.
+    uint32_t dkr[D];
+    tmem_ld32(tDK, *reinterpret_cast<uint32_t(*)[32]>(dkr));
+    tmem_ld32(tDK + 32, *reinterpret_cast<uint32_t(*)[32]>(dkr + 32));
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars.acc_free_k);
     // raw k tile: chunk q = it * 128 + r128, 32 consecutive 16-byte chunks
     // per warp access.
     {
@@ -1211,18 +1221,15 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     float dot = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      uint32_t a[32];
-      tmem_ld32(tDK + c * 32, a);
-      tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 kw = ld_shared_v4(chunk_addr(tile_k, r128, c * 4 + q));
         const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const int e = q * 8 + 2 * h, col = c * 32 + e;
-          dot = fmaf(bars.gk[col] * __uint_as_float(a[e]), __uint_as_float(kx[h] << 16), dot);
-          dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[e + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
+          const int e = c * 32 + q * 8 + 2 * h;
+          dot = fmaf(bars.gk[e] * __uint_as_float(dkr[e]), __uint_as_float(kx[h] << 16), dot);
+          dot = fmaf(bars.gk[e + 1] * __uint_as_float(dkr[e + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
         }
       }
     }
@@ -1232,13 +1239,8 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     // 32 rows by a reduce-scatter (lane L ends with column 32c + L).
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      uint32_t a[32];
-      tmem_ld32(tDK + c * 32, a);
-      tmem_wait_ld();
-      if (c == D / 32 - 1) {
-        tc_fence_before();
-        mbar_arrive(&bars.acc_free_k);
-      }
+      // The chunk's dK values are dead once read: the dgk terms replace them.
+      uint32_t(&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(dkr + c * 32);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t addr = chunk_addr(tile_k, r128, c * 4 + q);
@@ -1389,7 +1391,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
     if constexpr (D == 64) {
-      if (warp >= kWarpEpi && warp < kWarpTma) setmaxnreg_dec<kRegEpi64>();
+      if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain64>();
+      else if (warp < kWarpTma) setmaxnreg_dec<kRegEpi64>();
       else if (warp >= kWarpTma) setmaxnreg_dec<kRegMma64>();
     } else {  // d = 128: the drain warps run the epilogue; one issuer
       setmaxnreg_dec<kRegOther128>();
