@@ -18,7 +18,8 @@
 // load and first S / dP products overlap the current unit's last tiles and
 // its epilogue.
 // 640 threads (five warpgroups; setmaxnreg gives the compute warpgroups 128
-// registers per thread, the drain 88, the epilogue 88 and TMA / MMA 48):
+// registers per thread (d = 64: 120), the drain 88, the epilogue 104 and
+// TMA / MMA 48):
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
@@ -41,8 +42,8 @@
 //               per query tile Q_i and dO_i through rings, with the tile's
 //               softmax statistics (d = 64: a bf16 chunk for the MMAs;
 //               d = 128: fp32 LSE_i and D_i rows).
-//   warps 17-19 MMA issuers (d = 64): recompute (S, dP), gradients (dV, dK)
-//               and dQ; d = 128 uses warp 17 alone.
+//   warps 17-19 MMA issuers (d = 64): recompute (S, dK, dP), dV, and dQ;
+//               d = 128 uses warp 17 alone.
 //
 // d = 64: TMEM (512 columns) S^T [0,128), dP^T [128,256) (then dS^T),
 // dV [256,320), dK [320,384), dQ [384,448), P^T [448,512) (packed bf16).
@@ -66,33 +67,34 @@ namespace {
 constexpr int kBwdThreads = 640;  // 5 warpgroups
 // Warp roles: 0-7 compute (two groups), 8-11 dQ drain, 12-15 epilogue
 // (d = 64), 16 TMA, 17-19 MMA issuers.  Registers per thread (setmaxnreg):
-// compute 128, drain 88, epilogue 88, TMA / issuers 48 (d = 128: 72 for all
-// but compute); 256 x 128 + 128 x (88 + 88 + 48) = 61440, the 640 x 96 the
-// block launches with (d = 128: 256 x 128 + 384 x 72 = 60416).
+// compute 120, drain 88, epilogue 104, TMA / issuers 48 (d = 128: compute 128
+// and 72 for all others); 256 x 120 + 128 x (88 + 104 + 48) = 61440, the
+// 640 x 96 the block launches with (d = 128: 256 x 128 + 384 x 72 = 60416).
 // setmaxnreg budgets.  An increase must not be below, a decrease not above,
 // the count the kernel launches with, and the sum must fit the launch's
 // registers (640 x that count); the launcher checks both against the
 // compiled kernel before every launch.
-constexpr int kRegCompute = 128, kRegDrain64 = 88, kRegEpi64 = 88, kRegMma64 = 48, kRegOther128 = 72;
+constexpr int kRegCompute64 = 120, kRegDrain64 = 88, kRegEpi64 = 104, kRegMma64 = 48;
+constexpr int kRegCompute128 = 128, kRegOther128 = 72;
 // The split uses the whole launch allocation (640 x 96): the kernel must launch
 // with exactly 96 registers per thread.
 constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
 // Each SM sub-partition holds one warp of every warpgroup (warp w on w % 4)
 // and 16384 registers, so one warp of each role must fit there too.
-static_assert(32 * (2 * kRegCompute + kRegDrain64 + kRegEpi64 + kRegMma64) <= 16384,
+static_assert(32 * (2 * kRegCompute64 + kRegDrain64 + kRegEpi64 + kRegMma64) <= 16384,
               "d = 64 register split exceeds a sub-partition");
-static_assert(32 * (2 * kRegCompute + 3 * kRegOther128) <= 16384, "d = 128 register split exceeds a sub-partition");
-static_assert(256 * kRegCompute + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <= kBwdThreads * kRegLaunchMin,
+static_assert(32 * (2 * kRegCompute128 + 3 * kRegOther128) <= 16384, "d = 128 register split exceeds a sub-partition");
+static_assert(256 * kRegCompute64 + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <= kBwdThreads * kRegLaunchMin,
               "d = 64 register split exceeds the launch allocation");
-static_assert(256 * kRegCompute + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
+static_assert(256 * kRegCompute128 + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
               "d = 128 register split exceeds the launch allocation");
-static_assert(kRegEpi64 <= kRegLaunchMin && kRegMma64 <= kRegLaunchMin && kRegOther128 <= kRegLaunchMin &&
-                  kRegDrain64 <= kRegLaunchMin && kRegCompute >= kRegLaunchMax,
+static_assert(kRegEpi64 >= kRegLaunchMax && kRegMma64 <= kRegLaunchMin && kRegOther128 <= kRegLaunchMin &&
+                  kRegDrain64 <= kRegLaunchMin && kRegCompute64 >= kRegLaunchMax && kRegCompute128 >= kRegLaunchMax,
               "setmaxnreg direction");
 constexpr int kWarpEpi = 12;
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma0 = 17;  // recompute issuer (d = 128: the only one)
-constexpr int kWarpMma1 = 18;  // gradient issuer
+constexpr int kWarpMma1 = 18;  // dV issuer
 constexpr int kWarpMma2 = 19;  // dQ issuer
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -104,7 +106,7 @@ struct BwdCfg {
   static constexpr int kDSBufs = 1;
   // K/V buffers: two let the next unit's keys load during the current unit.
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
-  // d = 64: three MMA issuers (recompute: S, dP; gradients: dV, dK; dQ) and
+  // d = 64: three MMA issuers (S, dK, dP; dV; dQ) and
   // P^T in its own TMEM columns.  d = 128: one issuer, P^T over S^T.
   static constexpr bool kSplitIssuers = (D == 64);
   // d = 64: the softmax statistics enter through the tensor cores.  Each
@@ -255,9 +257,9 @@ struct BwdBars {
   uint64_t acc_free_v, acc_free_k;  // ... and have been read out of TMEM
   uint64_t s_free;
   uint64_t dv_done;
-  uint64_t dk_done;     // d = 64: dK(t) has read dS^T(t) from the dP^T columns
   uint64_t epi;
   uint64_t drain_sync;  // d = 64: the dQ drain threads' staging handshakes
+  uint64_t kraw_full;   // d = 64: the unit's raw k tile has landed (epilogue)
   uint64_t drain[3];
   uint32_t tmem_base;
   int abort;
@@ -410,25 +412,42 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint64_t a, uint64_t b) 
 }
 
 // Three-issuer backward (d = 64).  Recompute issuer: S(t) = K Q_t^T - LSE /
-// scale once the compute groups hold S(t-1) in registers, dP(t) = V dO_t^T -
-// D once they hold dP(t-1) (the statistics by one more K step each, from the
-// query stage's statistics chunk).  Gradient issuer: dV(t) from P^T in TMEM, dK(t) from dS^T in
-// shared memory.  dQ issuer: dQ(t) from dS^T.  Every shared buffer is
-// released by a commit from each of its two readers: a Q stage (S, dK), a dO
-// stage (dP, dV), the dS^T tile (dK, dQ) and a K/V buffer (the unit's last
-// dP and last dQ).
+// scale once the compute groups hold S(t-1) in registers, then dK(t-1) once
+// dS^T(t-1) is in TMEM, then dP(t) = V dO_t^T - D (the statistics by one
+// more K step of S and dP, from the query stage's statistics chunk).
+// Gradient issuer: dV(t) from P^T in TMEM.  dQ issuer: dQ(t) from the dS^T
+// tile in shared memory.  A dO stage is released by commits from its two
+// readers (dP, dV), a K/V buffer by the unit's last dP and last dQ, a Q stage
+// by its last reader (dK), the dS^T tile by dQ, and a unit's accumulators are
+// final once both the dV and the dK issuer have committed.
 template <int D, class W>
 __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w,
                                   uint32_t* dev_err) {
   using C = BwdCfg<D>;
   volatile int* ab = &bars.abort;
   auto kQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16, 1024); };
+  auto mQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16384, 1024); };
   auto kDO = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16, 1024); };
   auto kSt = [=](int t) {
     return sdesc_sw32_kmajor(smem_u32(sm + C::kOffStats + (t % C::kQStages) * C::kStatsChunk), 256u);
   };
   const uint64_t kOnesS = sdesc_sw32_kmajor(smem_u32(sm + C::kOffConst), 0u);
   const uint64_t kOnesD = sdesc_sw32_kmajor(smem_u32(sm + C::kOffConst + C::kConstAtom), 0u);
+  // dK(t) is issued one tile late, between S(t+1) and dP(t+1): it reads
+  // dS^T(t) out of the dP^T columns, which dP(t+1) then overwrites, and MMAs
+  // issued by one thread execute in issue order.
+  int pend_t = -1, pend_ui = 0;
+  bool pend_first = false, pend_last = false;
+  auto issue_dk = [&]() -> bool {
+    if (!mbar_wait(&bars.ds_ready, pend_t & 1, ab, dev_err)) return false;
+    // The previous unit's dK has been read out of TMEM.
+    if (pend_first && pend_ui > 0 && !mbar_wait(&bars.acc_free_k, (pend_ui - 1) & 1, ab, dev_err)) return false;
+    tc_fence_after();
+    mma_dk_ts<D>(tmem + C::kColDK, tmem + C::kColDP, mQ(pend_t), !pend_first);
+    umma_commit(&bars.q_empty[pend_t % C::kQStages]);  // the stage's last reader
+    if (pend_last) umma_commit(&bars.acc_full);
+    return true;
+  };
   bool ok = true;
   int tb = 0;  // query tiles of the previous units
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
@@ -445,31 +464,32 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       mma_kk<D>(tmem + C::kColS, kK, kQ(t), C::kIdescSS);
       if constexpr (C::kStatsFold) umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t), C::kIdescSS, 1u);
       umma_commit(&bars.s_full);
-      // dK(t-1) has read dS^T(t-1) from the dP^T columns (so the compute
-      // groups are done with dP^T(t-1) too).
-      if (t > 0 && !(ok = mbar_wait(&bars.dk_done, (t - 1) & 1, ab, dev_err))) break;
+      if (pend_t >= 0 && !(ok = issue_dk())) break;
       if (!(ok = mbar_wait(&bars.do_full[t % C::kDOStages], (t / C::kDOStages) & 1, ab, dev_err))) break;
       tc_fence_after();
       mma_kk<D>(tmem + C::kColDP, kV, kDO(t), C::kIdescSS);
       if constexpr (C::kStatsFold) umma_bf16_ss(tmem + C::kColDP, kOnesD, kSt(t), C::kIdescSS, 1u);
       umma_commit(&bars.dp_full);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
-      // The query stage (and its statistics chunk) is done with here.
-      umma_commit(&bars.q_empty[t % C::kQStages]);
+      pend_t = t;
+      pend_ui = ui;
+      pend_first = (i == 0);
+      pend_last = (i == nkt - 1);
     }
     tb += nkt;
     if (ok) umma_commit(&bars.kv_mmadone[b]);
   }
+  if (ok && pend_t >= 0) issue_dk();
   umma_commit(&bars.drain[0]);
   mbar_wait_drain(&bars.drain[0], 0);
 }
 
+// Gradient issuer (d = 64): dV(t) += P^T(t) dO_t once P^T(t) is in TMEM.
 template <int D, class W>
 __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w,
                                   uint32_t* dev_err) {
   using C = BwdCfg<D>;
   volatile int* ab = &bars.abort;
-  auto mQ = [=](int t) { return sdesc_sw128(smem_u32(sm + C::kOffQ + (t % C::kQStages) * C::kTile), 16384, 1024); };
   auto mDO = [=](int t) {
     return sdesc_sw128(smem_u32(sm + C::kOffDO + (t % C::kDOStages) * C::kTile), 16384, 1024);
   };
@@ -487,13 +507,6 @@ __device__ void bwd_mma_gradients(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       mma_dv_sep<D>(tmem + C::kColDV, tmem + C::kColP, mDO(t), i > 0);
       umma_commit(&bars.dv_done);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
-      if (!(ok = mbar_wait(&bars.ds_ready, t & 1, ab, dev_err))) break;
-      if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
-      if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_k, (ui - 1) & 1, ab, dev_err))) break;
-      tc_fence_after();
-      mma_dk_ts<D>(tmem + C::kColDK, tmem + C::kColDP, mQ(t), i > 0);
-      umma_commit(&bars.q_empty[t % C::kQStages]);
-      umma_commit(&bars.dk_done);
     }
     tb += nkt;
     if (ok) umma_commit(&bars.acc_full);
@@ -1129,7 +1142,8 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
 // accumulators, released as soon as they are read.
 template <int D, class W>
 __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, float scale,
-                                   const __nv_bfloat16* __restrict__ k_raw, const float* __restrict__ rk,
+                                   const CUtensorMap* mkraw, const CUtensorMap* mdk, const CUtensorMap* mdv,
+                                   const float* __restrict__ rk,
                                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
                                    float* __restrict__ dgk_part, uint32_t* dev_err) {
   using C = BwdCfg<D>;
@@ -1143,6 +1157,12 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
   };
   volatile int* ab = &bars.abort;
   uint32_t epi_uses = 0;
+  uint32_t kraw_issued = 0, kraw_done = 0;  // thread 0 issues the raw k tile loads
+  if (r128 == 0) {
+    tma_prefetch_desc(mkraw);
+    tma_prefetch_desc(mdk);
+    tma_prefetch_desc(mdv);
+  }
   // Bounded barrier among the 128 epilogue threads.
   auto epi_sync = [&]() -> bool {
     mbar_arrive(&bars.epi);
@@ -1159,8 +1179,6 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     const bool key_live = n < un.end;
     const int live_rows = un.end - kv0 < 128 ? un.end - kv0 : 128;
     const size_t tile_off = (static_cast<size_t>(bh) * rows + kv0) * D;
-    // The raw k tile is pulled into L2 while the unit runs.
-    if (r128 == 0) bulk_prefetch_l2(k_raw + tile_off, live_rows * D * 2);
     const float r = key_live ? rk[static_cast<size_t>(bh) * rows + n] : 0.f;
     const uint32_t tile_k = smem_u32(sm + C::off_k(b));  // k, then dk
     const uint32_t tile_v = smem_u32(sm + C::off_v(b));  // dv
@@ -1170,6 +1188,15 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     if (ok) ok = mbar_wait(&bars.kv_mmadone[b], (ui / C::kKVBufs) & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
+    // The raw k tile into the unit's K buffer by TMA (the MMAs are done with
+    // it), in the same 128-byte swizzled layout the tile had.  Rows past the
+    // segment (zero-filled past the tensor's end, the next sequence's rows in
+    // a packed call) have r = 0 and zero dK, so they contribute nothing.
+    if (r128 == 0) {
+      mbar_arrive_expect_tx(&bars.kraw_full, C::kTile);
+      tma_load_3d(sm + C::off_k(b), mkraw, &bars.kraw_full, 0, kv0, bh);
+      ++kraw_issued;
+    }
     // dV out of TMEM into the dv tile (bf16), its columns released.
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -1197,27 +1224,17 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars.acc_free_k);
-    // raw k tile: chunk q = it * 128 + r128, 32 consecutive 16-byte chunks
-    // per warp access.
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(k_raw + tile_off);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 kw[4];
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int q = (half * 4 + it) * 128 + r128;
-          kw[it] = (q >> 3) < live_rows ? src[q] : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int q = (half * 4 + it) * 128 + r128;
-          st_shared_v4(chunk_addr(tile_k, q >> 3, q & 7), kw[it].x, kw[it].y, kw[it].z, kw[it].w);
-        }
-      }
-    }
-    if (!(ok = epi_sync())) break;  // the k tile is complete
+    ok = mbar_wait(&bars.kraw_full, ui & 1, ab, dev_err);
+    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+    ++kraw_done;
     // Pass 1: dot = sum_c g_c dk_hat_c k_c over this thread's row.
+    // The gain is read 8 columns at a time (two 16-byte broadcasts).
+    auto gain8 = [&](int col, float (&g)[8]) {
+      const float4 g0 = *reinterpret_cast<const float4*>(&bars.gk[col]);
+      const float4 g1 = *reinterpret_cast<const float4*>(&bars.gk[col + 4]);
+      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+      g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+    };
     float dot = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -1225,15 +1242,19 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
       for (int q = 0; q < 4; ++q) {
         const uint4 kw = ld_shared_v4(chunk_addr(tile_k, r128, c * 4 + q));
         const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+        float g[8];
+        gain8(c * 32 + q * 8, g);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int e = c * 32 + q * 8 + 2 * h;
-          dot = fmaf(bars.gk[e] * __uint_as_float(dkr[e]), __uint_as_float(kx[h] << 16), dot);
-          dot = fmaf(bars.gk[e + 1] * __uint_as_float(dkr[e + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
+          dot = fmaf(g[2 * h] * __uint_as_float(dkr[e]), __uint_as_float(kx[h] << 16), dot);
+          dot = fmaf(g[2 * h + 1] * __uint_as_float(dkr[e + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
         }
       }
     }
     const float coef = r * r * r * (1.f / D) * scale * dot;
+    // Key rows past the segment have r = 0 and k = 0, so their terms vanish.
+    const float rs = r * scale;
     // Pass 2, per 32-column chunk: dk = r g dk_hat - coef k over the k row
     // (in place), and the chunk's dgk terms dk_hat k r summed over the warp's
     // 32 rows by a reduce-scatter (lane L ends with column 32c + L).
@@ -1247,14 +1268,16 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
         const uint4 kw = ld_shared_v4(addr);
         const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
         uint32_t o[4];
+        float g[8];
+        gain8(c * 32 + q * 8, g);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const int e = q * 8 + 2 * h, col = c * 32 + e;
+          const int e = q * 8 + 2 * h;
           const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
-          const float dk0 = __uint_as_float(a[e]) * scale, dk1 = __uint_as_float(a[e + 1]) * scale;
-          o[h] = pack_bf16x2(r * bars.gk[col] * dk0 - coef * x0, r * bars.gk[col + 1] * dk1 - coef * x1);
-          a[e] = __float_as_uint(key_live ? dk0 * x0 * r : 0.f);
-          a[e + 1] = __float_as_uint(key_live ? dk1 * x1 * r : 0.f);
+          const float a0 = __uint_as_float(a[e]), a1 = __uint_as_float(a[e + 1]);
+          o[h] = pack_bf16x2(fmaf(rs * g[2 * h], a0, -coef * x0), fmaf(rs * g[2 * h + 1], a1, -coef * x1));
+          a[e] = __float_as_uint(a0 * x0 * rs);
+          a[e + 1] = __float_as_uint(a1 * x1 * rs);
         }
         st_shared_v4(addr, o[0], o[1], o[2], o[3]);
       }
@@ -1270,18 +1293,30 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
       }
       bars.wsum[warp & 3][c * 32 + lane] = __uint_as_float(a[0]);
     }
+    fence_proxy_async_smem();  // the dk / dv tiles, for the TMA stores
     if (!(ok = epi_sync())) break;  // dk tile, dv tile and warp sums complete
     if (r128 < D)
       bars.dgk_cta[r128] += ((bars.wsum[0][r128] + bars.wsum[1][r128]) + bars.wsum[2][r128]) + bars.wsum[3][r128];
-    // dk and dv tiles out, 32 consecutive 16-byte chunks per warp access.
-    uint4* dkdst = reinterpret_cast<uint4*>(dk + tile_off);
-    uint4* dvdst = reinterpret_cast<uint4*>(dv + tile_off);
+    if (live_rows == 128 || un.end == w.seg.rows) {
+      // The tiles out by TMA (rows past the tensor's end are clipped).
+      if (r128 == 0) {
+        tma_store_3d(mdk, sm + C::off_k(b), 0, kv0, bh);
+        tma_store_3d(mdv, sm + C::off_v(b), 0, kv0, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // read out of the K/V buffer
+      }
+    } else {
+      // A segment's last tile in a packed call: the live rows only, 32
+      // consecutive 16-byte chunks per warp access.
+      uint4* dkdst = reinterpret_cast<uint4*>(dk + tile_off);
+      uint4* dvdst = reinterpret_cast<uint4*>(dv + tile_off);
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int q = it * 128 + r128;
-      if ((q >> 3) < live_rows) {
-        dkdst[q] = ld_shared_v4(chunk_addr(tile_k, q >> 3, q & 7));
-        dvdst[q] = ld_shared_v4(chunk_addr(tile_v, q >> 3, q & 7));
+      for (int it = 0; it < 8; ++it) {
+        const int q = it * 128 + r128;
+        if ((q >> 3) < live_rows) {
+          dkdst[q] = ld_shared_v4(chunk_addr(tile_k, q >> 3, q & 7));
+          dvdst[q] = ld_shared_v4(chunk_addr(tile_v, q >> 3, q & 7));
+        }
       }
     }
     // The K/V buffer goes back to the producer: every thread orders its
@@ -1289,6 +1324,11 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     fence_proxy_async_smem();
     if (!(ok = epi_sync())) break;  // tiles read (and wsum free)
     if (r128 == 0) mbar_arrive(&bars.kv_empty[b]);
+  }
+  if (r128 == 0) {
+    // Aborted: a raw k tile load still in flight lands before the CTA exits.
+    if (kraw_issued > kraw_done) mbar_wait_drain(&bars.kraw_full, kraw_done & 1);
+    bulk_wait_group0();  // the dk / dv stores are complete
   }
   if (r128 < D) dgk_part[static_cast<size_t>(blockIdx.x) * D + r128] = bars.dgk_cta[r128];
 }
@@ -1298,7 +1338,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                     const __grid_constant__ CUtensorMap map_stats, const __grid_constant__ CUtensorMap map_dq,
-                    const __grid_constant__ W w, float scale,
+                    const __grid_constant__ CUtensorMap map_kraw, const __grid_constant__ CUtensorMap map_dk,
+                    const __grid_constant__ CUtensorMap map_dv, const __grid_constant__ W w, float scale,
                     const float* __restrict__ nlse2_pad,
                     const float* __restrict__ delta_pad, const __nv_bfloat16* __restrict__ k_raw,
                     const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
@@ -1317,12 +1358,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t n_rel = C::kSplitIssuers ? 2u : 1u;
     for (int s = 0; s < 3; ++s) {
       mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], n_rel);
+      mbar_init(&bars.q_empty[s], 1);  // released after its last product (dK)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);  // d = 64: the epilogue; d = 128: the issuer
-      mbar_init(&bars.kv_mmadone[s], n_rel);
+      mbar_init(&bars.kv_mmadone[s], n_rel);  // d = 64: the recompute and the dQ issuers
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], n_rel);
       mbar_init(&bars.ds_free[s], 1);  // the dQ product (d = 64: dK reads dS^T from TMEM)
@@ -1333,14 +1374,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 128);
-    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_full, n_rel);  // d = 64: the dV and the dK issuers
     mbar_init(&bars.acc_free_v, 128);
     mbar_init(&bars.acc_free_k, 128);
     mbar_init(&bars.s_free, 256);
     mbar_init(&bars.dv_done, 1);
-    mbar_init(&bars.dk_done, 1);
     mbar_init(&bars.epi, 128);
     mbar_init(&bars.drain_sync, 128);
+    mbar_init(&bars.kraw_full, 1);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
     mbar_init(&bars.drain[2], 1);
@@ -1387,12 +1428,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp < 8) {
-    setmaxnreg_inc<kRegCompute>();
+    setmaxnreg_inc<D == 64 ? kRegCompute64 : kRegCompute128>();
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
   } else {
     if constexpr (D == 64) {
       if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain64>();
-      else if (warp < kWarpTma) setmaxnreg_dec<kRegEpi64>();
+      else if (warp < kWarpTma) setmaxnreg_inc<kRegEpi64>();
       else if (warp >= kWarpTma) setmaxnreg_dec<kRegMma64>();
     } else {  // d = 128: the drain warps run the epilogue; one issuer
       setmaxnreg_dec<kRegOther128>();
@@ -1401,7 +1442,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if constexpr (D == 64) bwd_drain64<D, kOrd>(sm, bars, tmem, w, &map_dq, counters, dev_err);
       else bwd_drain_epilogue<D, kOrd>(sm, bars, tmem, w, scale, dqacc, counters, k_raw, rk, dk, dv, dgk_part, dev_err);
     } else if (warp < kWarpTma) {
-      if constexpr (D == 64) bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, k_raw, rk, dk, dv, dgk_part, dev_err);
+      if constexpr (D == 64) bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, &map_kraw, &map_dk, &map_dv, rk, dk, dv, dgk_part,
+                                                    dev_err);
     } else if (warp == kWarpTma) {
       if (lane == 0)
         bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, nlse2_pad, delta_pad, dev_err);
@@ -1426,7 +1468,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool kOrd, class W>
 cudaError_t launch_bwd_w(const W& w, int grid, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const CUtensorMap& mstats, const CUtensorMap& mdq, const AttnShape& s,
+                         const CUtensorMap& mdo, const CUtensorMap& mstats, const CUtensorMap& mdq,
+                         const CUtensorMap& mkraw, const CUtensorMap& mdk, const CUtensorMap& mdv, const AttnShape& s,
                          const float* nlse2_pad, const float* delta_pad,
                          const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
                          float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
@@ -1441,7 +1484,7 @@ cudaError_t launch_bwd_w(const W& w, int grid, const CUtensorMap& mq, const CUte
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
-  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, mstats, mdq, w, s.scale, nlse2_pad,
+  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, w, s.scale, nlse2_pad,
                     delta_pad, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
                     reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, counters,
                     dgk_part, dev_err);
@@ -1486,6 +1529,11 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
                          const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk,
                          uint16_t* dv, float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err,
                          cudaStream_t st) {
+  // d = 64: the epilogue loads raw k tiles and stores dk / dv tiles by TMA.
+  CUtensorMap mkraw = mq, mdk = mq, mdv = mq;
+  if (D == 64 && (!encode_bhnd_map(&mkraw, k_raw, s.BH, s.N, s.d) || !encode_bhnd_map(&mdk, dk, s.BH, s.N, s.d) ||
+                  !encode_bhnd_map(&mdv, dv, s.BH, s.N, s.d)))
+    return cudaErrorInvalidValue;
   const BwdPlan plan = bwd_plan(s);
   if (s.seg.n == 1) {
     BwdWorkUniform w;
@@ -1495,9 +1543,9 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     w.units = s.BH * w.upc;
     w.ord = plan.ord;
     if (plan.ord == kDqArrival)
-      return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+      return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
                                     dqacc, counters, dgk_part, dev_err, st);
-    return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+    return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
                                  dqacc, counters, dgk_part, dev_err, st);
   }
   BwdWork w;
@@ -1506,9 +1554,9 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   w.units = s.BH * w.upc;
   w.ord = plan.ord;
   if (plan.ord == kDqArrival)
-    return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+    return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
                                   dqacc, counters, dgk_part, dev_err, st);
-  return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+  return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
                                counters, dgk_part, dev_err, st);
 }
 
