@@ -1,7 +1,9 @@
 """Benchmark: MM-DiT joint attention (QK-RMSNorm + softmax attention) fwd+bwd on GB300.
 
-One step = jattn_fwd + jattn_bwd over one batch of the 512 px workload
-(B=16, H=12, N = 1024 image + 77 text tokens, d=64), inputs resident in HBM.
+One step = jattn_fwd_train + jattn_bwd_train over one batch of the 512 px
+workload (B=16, H=12, N = 1024 image + 77 text tokens, d=64), inputs resident
+in HBM: a training step's attention, whose forward keeps the normalised q / k
+and the rows' 1/rms for its backward.
 The metric is TFLOP/s of the fwd+bwd pair at 14*B*H*N^2*d FLOP per step
 (forward 4 B H N^2 d; backward 10 B H N^2 d, the five N x N x d products
 including the recomputed scores), with the true N, so tile padding counts
@@ -352,13 +354,17 @@ def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
         dq, dk, dv = torch.empty_like(out), torch.empty_like(out), torch.empty_like(out)
         dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
         fwd_only = c.mode == "cfg_fwd"
+        saved = torch.empty(ja.jattn_saved_bytes(B, H, c.N_img, c.N_txt, d), dtype=torch.uint8, device=dev)
 
         def one(i):
             t = sets[i % N_SETS]
-            ja.jattn_fwd(t["q"], t["k"], t["v"], gq, gk, B, H, c.N_img, c.N_txt, d, out, lse, stream)
-            if not fwd_only:
-                ja.jattn_bwd(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], dq, dk, dv, dgq, dgk, B, H,
-                             c.N_img, c.N_txt, d, stream)
+            if fwd_only:
+                ja.jattn_fwd(t["q"], t["k"], t["v"], gq, gk, B, H, c.N_img, c.N_txt, d, out, lse, stream)
+            else:
+                ja.jattn_fwd_train(t["q"], t["k"], t["v"], gq, gk, B, H, c.N_img, c.N_txt, d, out, lse, saved,
+                                   stream)
+                ja.jattn_bwd_train(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], saved, dq, dk, dv, dgq,
+                                   dgk, B, H, c.N_img, c.N_txt, d, stream)
 
         ms = median_ms(one)
         fl = flops_fwd(B, H, N, d) + (0.0 if fwd_only else flops_bwd(B, H, N, d))
@@ -369,8 +375,8 @@ def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
         else:
             row["images_equiv_per_s"] = B / (12 * ms * 1e-3)
         res[name] = row
-        del sets, out, lse, dq, dk, dv
-    # Packed variable-length call (jattn_fwd_varlen / jattn_bwd_varlen): the 512 px and 256 px joint
+        del sets, out, lse, dq, dk, dv, saved
+    # Packed variable-length call (the training pair's varlen form): the 512 px and 256 px joint
     # lengths mixed in one call, 8 x 1101 + 16 x 333 rows per head, H = 12, d = 64.
     lens = [1101] * 8 + [333] * 16
     H, d = 12, 64
@@ -386,19 +392,20 @@ def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
     out, lse = torch.empty_like(sets[0]["q"]), torch.empty((H, T), device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(out), torch.empty_like(out), torch.empty_like(out)
     dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
+    saved = torch.empty(ja.jattn_saved_bytes_varlen(cu, H, d), dtype=torch.uint8, device=dev)
 
     def one_varlen(i):
         t = sets[i % N_SETS]
-        ja.jattn_fwd_varlen(t["q"], t["k"], t["v"], gq, gk, cu, H, d, out, lse, stream)
-        ja.jattn_bwd_varlen(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], dq, dk, dv, dgq, dgk, cu, H, d,
-                            stream)
+        ja.jattn_fwd_train_varlen(t["q"], t["k"], t["v"], gq, gk, cu, H, d, out, lse, saved, stream)
+        ja.jattn_bwd_train_varlen(t["q"], t["k"], t["v"], gq, gk, out, lse, t["dout"], saved, dq, dk, dv, dgq,
+                                  dgk, cu, H, d, stream)
 
     ms = median_ms(one_varlen)
     fl = sum(flops_fwd(1, H, n, d) + flops_bwd(1, H, n, d) for n in lens)
     res["varlen_mix"] = {"mode": "fwd+bwd, packed sequences", "sequences": "8 x 1101 + 16 x 333", "H": H, "T": T,
                          "d": d, "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                          "images_equiv_per_s": len(lens) / (12 * ms * 1e-3)}
-    del sets, out, lse, dq, dk, dv
+    del sets, out, lse, dq, dk, dv, saved
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the per-config pass")
     return res
@@ -464,15 +471,18 @@ def main():
         sets.append(dict(q=q, k=k, v=v, dout=do, out=torch.empty_like(q),
                          lse=torch.empty((B, H, N), device=dev, dtype=torch.float32),
                          dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
-                         dgq=torch.empty_like(gq), dgk=torch.empty_like(gk)))
+                         dgq=torch.empty_like(gq), dgk=torch.empty_like(gk),
+                         saved=torch.empty(ja.jattn_saved_bytes(B, H, c.N_img, c.N_txt, d), dtype=torch.uint8,
+                                           device=dev)))
     stream = torch.cuda.current_stream(dev)
     n_img, n_txt = c.N_img, c.N_txt
 
     def step(i):
         t = sets[i % N_SETS]
-        ja.jattn_fwd(t["q"], t["k"], t["v"], gq, gk, B, H, n_img, n_txt, d, t["out"], t["lse"], stream)
-        ja.jattn_bwd(t["q"], t["k"], t["v"], gq, gk, t["out"], t["lse"], t["dout"], t["dq"], t["dk"], t["dv"],
-                     t["dgq"], t["dgk"], B, H, n_img, n_txt, d, stream)
+        ja.jattn_fwd_train(t["q"], t["k"], t["v"], gq, gk, B, H, n_img, n_txt, d, t["out"], t["lse"], t["saved"],
+                           stream)
+        ja.jattn_bwd_train(t["q"], t["k"], t["v"], gq, gk, t["out"], t["lse"], t["dout"], t["saved"], t["dq"],
+                           t["dk"], t["dv"], t["dgq"], t["dgk"], B, H, n_img, n_txt, d, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -552,10 +562,11 @@ def main():
                     g[n].copy_(x, non_blocking=True)
                 ev_in[kb].record(s_in)
             stream.wait_event(ev_in[kb])
-            ja.jattn_fwd(t["q"], t["k"], t["v"], g["gq"], g["gk"], B, H, n_img, n_txt, d, t["out"], t["lse"], stream)
+            ja.jattn_fwd_train(t["q"], t["k"], t["v"], g["gq"], g["gk"], B, H, n_img, n_txt, d, t["out"], t["lse"],
+                               t["saved"], stream)
             ev_fwd[kb].record(stream)
-            ja.jattn_bwd(t["q"], t["k"], t["v"], g["gq"], g["gk"], t["out"], t["lse"], t["dout"], t["dq"], t["dk"],
-                         t["dv"], t["dgq"], t["dgk"], B, H, n_img, n_txt, d, stream)
+            ja.jattn_bwd_train(t["q"], t["k"], t["v"], g["gq"], g["gk"], t["out"], t["lse"], t["dout"], t["saved"],
+                               t["dq"], t["dk"], t["dv"], t["dgq"], t["dgk"], B, H, n_img, n_txt, d, stream)
             ev_comp[kb].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_fwd[kb])
@@ -606,8 +617,13 @@ def main():
     algo = {  # algorithmic work per launch (FLOP for contractions, bytes for HBM-bound kernels)
         "attn_fwd": ("tensor", flops_fwd(B, H, N, d)),
         "attn_bwd": ("tensor", flops_bwd(B, H, N, d)),
-        "qk_norm_fwd": ("hbm", 4.0 * B * H * N * d * 2),
-        "bwd_prep": ("hbm", B * H * N * d * 2 * 4 + B * H * N * d * 2 * 2 + B * H * N * d * 4 + B * H * N * 4 * 5),
+        # read q, k; write q_hat, k_hat and the rows' 1/rms (kept for the backward)
+        "qk_norm_fwd": ("hbm", 4.0 * B * H * N * d * 2 + 2 * B * H * N * 4),
+        # read out, dout, lse; write the zeroed dq accumulator and the statistics chunks
+        # (16 bf16 per row of the 128-row-padded layout)
+        "bwd_prep": ("hbm", B * H * N * d * 2 * 2 + B * H * N * 4 + B * H * N * d * 4
+                     + B * H * (-(-N // 128) * 128) * 32),
+        # read the dq accumulator, q and rq; write dq
         "q_norm_bwd": ("hbm", B * H * N * d * (4 + 2 + 2) + B * H * N * 4),
     }
     bound, work = algo[dom]

@@ -39,6 +39,7 @@
 #ifndef JATTN_H
 #define JATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -81,7 +82,7 @@ int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, con
  *   dgq, dgk   : [d] float32, overwritten (summed over all b, h, n).
  * The bf16 rounding of q_hat/k_hat is treated as the identity.  The
  * normalised q_hat/k_hat are recomputed from q, k (nothing is cached from
- * the forward call).  dk, dv and dgk are always summed in a fixed order and
+ * the forward call; jattn_fwd_train / jattn_bwd_train below keep them).  dk, dv and dgk are always summed in a fixed order and
  * repeat bit for bit.  dq is accumulated in float32 across key tiles: by
  * default with reduce-adds in arrival order, so that dq and dgq (a sum over
  * dq's accumulator) may differ in the last bits between runs; with
@@ -121,6 +122,38 @@ int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16*
                      const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq, jattn_bf16* dk,
                      jattn_bf16* dv, float* dgq, float* dgk, const int* cu_seqlens, int n_seqs, int H, int d,
                      void* stream);
+
+/*
+ * Training pair: a forward that keeps the normalised q_hat, k_hat and the
+ * rows' 1/rms r(q), r(k) in a caller buffer `saved`, and a backward that
+ * reads them there instead of recomputing them (the autograd practice of
+ * saving an op's activations for its backward).  Results are those of
+ * jattn_fwd / jattn_bwd with the same arguments, bit for bit where those
+ * repeat bit for bit.
+ *   saved : DEVICE buffer of jattn_saved_bytes(...) bytes (16-byte aligned),
+ *           written by the forward and read by the backward, which must be
+ *           given the same q, k, gq, gk and shape; its layout is private.
+ *           It may not overlap any other argument.
+ * jattn_saved_bytes returns 0 for a shape the calls would reject.  The other
+ * arguments and every status are those of jattn_fwd / jattn_bwd (and of
+ * their varlen forms); a null `saved` gives JATTN_ERR_INVALID_ARG.
+ */
+size_t jattn_saved_bytes(int B, int H, int N_img, int N_txt, int d);
+size_t jattn_saved_bytes_varlen(const int* cu_seqlens, int n_seqs, int H, int d);
+int jattn_fwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+                    int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse, void* saved,
+                    void* stream);
+int jattn_bwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
+                    const jattn_bf16* out, const float* lse, const jattn_bf16* dout, const void* saved,
+                    jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, int B, int H, int N_img,
+                    int N_txt, int d, void* stream);
+int jattn_fwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                           const float* gk, const int* cu_seqlens, int n_seqs, int H, int d, jattn_bf16* out,
+                           float* lse, void* saved, void* stream);
+int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                           const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
+                           const void* saved, jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk,
+                           const int* cu_seqlens, int n_seqs, int H, int d, void* stream);
 
 /*
  * Forward without any device allocation.  (No counterpart on the pages: an

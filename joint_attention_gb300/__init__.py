@@ -9,14 +9,18 @@ from __future__ import annotations
 from ._binding import (KERNEL_KINDS, STATUS, STATUS_CODE, JattnError, declared_symbols, jattn_bwd, jattn_fwd,
                        jattn_fwd_noalloc, jattn_fwd_varlen, jattn_bwd_varlen, jattn_selftest_wait_timeout, jattn_set_sm_limit,
                        jattn_set_deterministic, jattn_kernel_name, jattn_last_device_error, jattn_last_error_message, jattn_profile_enable, jattn_profile_read,
-                       jattn_profile_reset, jattn_status_string, jattn_version, load_library, profile_snapshot)
+                       jattn_profile_reset, jattn_status_string, jattn_version, load_library, profile_snapshot,
+                       jattn_saved_bytes, jattn_saved_bytes_varlen, jattn_fwd_train, jattn_bwd_train,
+                       jattn_fwd_train_varlen, jattn_bwd_train_varlen)
 
 __all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd", "jattn_fwd",
            "jattn_last_device_error", "jattn_status_string", "jattn_version", "load_library", "forward",
            "backward", "KERNEL_KINDS", "jattn_kernel_name", "jattn_profile_enable", "jattn_profile_read",
            "jattn_profile_reset", "profile_snapshot", "jattn_last_error_message", "jattn_fwd_noalloc",
            "jattn_fwd_varlen", "jattn_bwd_varlen", "forward_varlen", "backward_varlen",
-           "jattn_selftest_wait_timeout", "jattn_set_sm_limit", "jattn_set_deterministic"]
+           "jattn_selftest_wait_timeout", "jattn_set_sm_limit", "jattn_set_deterministic", "jattn_saved_bytes",
+           "jattn_saved_bytes_varlen", "jattn_fwd_train", "jattn_bwd_train", "jattn_fwd_train_varlen",
+           "jattn_bwd_train_varlen", "forward_train", "backward_train"]
 
 
 def forward(q, k, v, gq, gk, n_txt: int, stream=None):
@@ -63,4 +67,29 @@ def backward_varlen(q, k, v, gq, gk, out, lse, dout, cu_seqlens, stream=None):
     dgq = torch.empty_like(gq)
     dgk = torch.empty_like(gk)
     jattn_bwd_varlen(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, cu_seqlens, H, d, stream)
+    return dq, dk, dv, dgq, dgk
+
+
+def forward_train(q, k, v, gq, gk, n_txt: int, stream=None):
+    """out, lse, saved: a training forward of [B, H, N, d] bf16 CUDA tensors that keeps the
+    normalised q / k in `saved` (a uint8 CUDA tensor) for backward_train."""
+    import torch
+
+    B, H, N, d = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    saved = torch.empty(jattn_saved_bytes(B, H, N - n_txt, n_txt, d), dtype=torch.uint8, device=q.device)
+    jattn_fwd_train(q, k, v, gq, gk, B, H, N - n_txt, n_txt, d, out, lse, saved, stream)
+    return out, lse, saved
+
+
+def backward_train(q, k, v, gq, gk, out, lse, dout, saved, n_txt: int, stream=None):
+    """dq, dk, dv, dgq, dgk from forward_train's outputs and `saved`."""
+    import torch
+
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dgq = torch.empty_like(gq)
+    dgk = torch.empty_like(gk)
+    jattn_bwd_train(q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, B, H, N - n_txt, n_txt, d, stream)
     return dq, dk, dv, dgq, dgk

@@ -87,6 +87,19 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     lib.jattn_set_deterministic.restype = i32
     lib.jattn_kernel_name.argtypes = [i32]
     lib.jattn_kernel_name.restype = ctypes.c_char_p
+    sz = ctypes.c_size_t
+    lib.jattn_saved_bytes.argtypes = [i32] * 5
+    lib.jattn_saved_bytes.restype = sz
+    lib.jattn_saved_bytes_varlen.argtypes = [i32p, i32, i32, i32]
+    lib.jattn_saved_bytes_varlen.restype = sz
+    lib.jattn_fwd_train.argtypes = [vp] * 5 + [i32] * 5 + [vp] * 4
+    lib.jattn_fwd_train.restype = i32
+    lib.jattn_bwd_train.argtypes = [vp] * 14 + [i32] * 5 + [vp]
+    lib.jattn_bwd_train.restype = i32
+    lib.jattn_fwd_train_varlen.argtypes = [vp] * 5 + [i32p, i32, i32, i32] + [vp] * 4
+    lib.jattn_fwd_train_varlen.restype = i32
+    lib.jattn_bwd_train_varlen.argtypes = [vp] * 14 + [i32p, i32, i32, i32, vp]
+    lib.jattn_bwd_train_varlen.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -124,7 +137,7 @@ def profile_snapshot() -> dict:
 def declared_symbols(header: str = HEADER) -> list[str]:
     """Names of the functions include/jattn.h declares."""
     text = open(header).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(jattn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(jattn_\w+)\s*\(", text, flags=re.M)))
 
 
 def _ptr(x, name: str, dtype=None, numel: int | None = None):
@@ -252,6 +265,109 @@ def jattn_bwd_varlen(q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, cu_s
                               _ptr(dgk, "dgk", f32, d), arr, n, H, d, _stream(stream))
     if check and rc != 0:
         raise JattnError(rc, "jattn_bwd_varlen")
+    return rc
+
+
+def jattn_saved_bytes(B: int, H: int, N_img: int, N_txt: int, d: int) -> int:
+    """C ABI jattn_saved_bytes: size of the activation buffer of jattn_fwd_train / jattn_bwd_train."""
+    return int(load_library().jattn_saved_bytes(B, H, N_img, N_txt, d))
+
+
+def jattn_saved_bytes_varlen(cu_seqlens, H: int, d: int) -> int:
+    """C ABI jattn_saved_bytes_varlen."""
+    arr, _, n = _cu_array(cu_seqlens)
+    return int(load_library().jattn_saved_bytes_varlen(arr, n, H, d))
+
+
+def _saved_ptr(saved, nbytes: int):
+    import torch
+
+    if isinstance(saved, int) or saved is None:
+        return saved
+    if not isinstance(saved, torch.Tensor) or not saved.is_cuda or not saved.is_contiguous():
+        raise ValueError("saved: expected a contiguous CUDA tensor")
+    if saved.numel() * saved.element_size() < nbytes:
+        raise ValueError(f"saved: needs {nbytes} bytes, got {saved.numel() * saved.element_size()}")
+    return saved.data_ptr()
+
+
+def jattn_fwd_train(q, k, v, gq, gk, B: int, H: int, N_img: int, N_txt: int, d: int, out, lse, saved,
+                    stream=None, check: bool = True) -> int:
+    """C ABI jattn_fwd_train: jattn_fwd that also fills `saved` (jattn_saved_bytes bytes) for jattn_bwd_train."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e, r = B * H * N * d, B * H * N
+    bf, f32 = torch.bfloat16, torch.float32
+    nb = jattn_saved_bytes(B, H, N_img, N_txt, d)
+    rc = lib.jattn_fwd_train(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                             _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), B, H, N_img, N_txt, d,
+                             _ptr(out, "out", bf, e), _ptr(lse, "lse", f32, r), _saved_ptr(saved, nb),
+                             _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_fwd_train")
+    return rc
+
+
+def jattn_bwd_train(q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, B: int, H: int, N_img: int,
+                    N_txt: int, d: int, stream=None, check: bool = True) -> int:
+    """C ABI jattn_bwd_train: jattn_bwd reading q_hat, k_hat and 1/rms from the forward's `saved`."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e, r = B * H * N * d, B * H * N
+    bf, f32 = torch.bfloat16, torch.float32
+    nb = jattn_saved_bytes(B, H, N_img, N_txt, d)
+    rc = lib.jattn_bwd_train(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                             _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), _ptr(out, "out", bf, e),
+                             _ptr(lse, "lse", f32, r), _ptr(dout, "dout", bf, e), _saved_ptr(saved, nb),
+                             _ptr(dq, "dq", bf, e), _ptr(dk, "dk", bf, e), _ptr(dv, "dv", bf, e),
+                             _ptr(dgq, "dgq", f32, d), _ptr(dgk, "dgk", f32, d), B, H, N_img, N_txt, d,
+                             _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_bwd_train")
+    return rc
+
+
+def jattn_fwd_train_varlen(q, k, v, gq, gk, cu_seqlens, H: int, d: int, out, lse, saved, stream=None,
+                           check: bool = True) -> int:
+    """C ABI jattn_fwd_train_varlen (layouts as jattn_fwd_varlen)."""
+    import torch
+
+    lib = load_library()
+    arr, T, n = _cu_array(cu_seqlens)
+    e, r = H * T * d, H * T
+    bf, f32 = torch.bfloat16, torch.float32
+    nb = jattn_saved_bytes_varlen(cu_seqlens, H, d)
+    rc = lib.jattn_fwd_train_varlen(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                                    _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), arr, n, H, d,
+                                    _ptr(out, "out", bf, e), _ptr(lse, "lse", f32, r), _saved_ptr(saved, nb),
+                                    _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_fwd_train_varlen")
+    return rc
+
+
+def jattn_bwd_train_varlen(q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, cu_seqlens, H: int,
+                           d: int, stream=None, check: bool = True) -> int:
+    """C ABI jattn_bwd_train_varlen (layouts as jattn_fwd_varlen)."""
+    import torch
+
+    lib = load_library()
+    arr, T, n = _cu_array(cu_seqlens)
+    e, r = H * T * d, H * T
+    bf, f32 = torch.bfloat16, torch.float32
+    nb = jattn_saved_bytes_varlen(cu_seqlens, H, d)
+    rc = lib.jattn_bwd_train_varlen(_ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e),
+                                    _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), _ptr(out, "out", bf, e),
+                                    _ptr(lse, "lse", f32, r), _ptr(dout, "dout", bf, e), _saved_ptr(saved, nb),
+                                    _ptr(dq, "dq", bf, e), _ptr(dk, "dk", bf, e), _ptr(dv, "dv", bf, e),
+                                    _ptr(dgq, "dgq", f32, d), _ptr(dgk, "dgk", f32, d), arr, n, H, d,
+                                    _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_bwd_train_varlen")
     return rc
 
 

@@ -198,10 +198,29 @@ struct Carve {
 
 size_t fwd_scratch_bytes(const Shape& s) { return 2 * (s.elems * 2 + 256) + 256; }
 
-size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k, int counter_words) {
+// The activations a training forward keeps for its backward, at 256-byte
+// aligned offsets of one caller buffer: q_hat, k_hat (bf16, q's shape), then
+// 1/rms of every q and k row (fp32).
+struct SavedLayout {
+  size_t qhat, khat, rq, rk, total;
+};
+SavedLayout saved_layout(const Shape& s) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  SavedLayout l;
+  l.qhat = 0;
+  l.khat = up(s.elems * 2);
+  l.rq = l.khat + up(s.elems * 2);
+  l.rk = l.rq + up(s.rows * 4);
+  l.total = l.rk + up(s.rows * 4);
+  return l;
+}
+
+size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k, int counter_words, bool saved) {
   size_t b = 0;
-  b += 2 * (s.elems * 2 + 256);                                   // q_hat, k_hat
-  b += 2 * (s.rows * 4 + 256);                                    // rq, rk
+  if (!saved) {
+    b += 2 * (s.elems * 2 + 256);  // q_hat, k_hat
+    b += 2 * (s.rows * 4 + 256);   // rq, rk
+  }
   b += 2 * (static_cast<size_t>(s.BH) * s.seg.prows * 4 + 256);   // nlse2, delta
   if (attn_bwd_stats_chunks(s.d)) b += static_cast<size_t>(s.BH) * s.seg.prows * 32 + 256;  // statistics chunks
   b += s.elems * 4 + 256;                                         // dq accumulator
@@ -336,7 +355,7 @@ extern "C" int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const
   cudaError_t ce;
   {
     Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
-    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, err, st);
+    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, nullptr, nullptr, static_cast<int64_t>(s.rows), s.d, err, st);
   }
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "qk_norm_fwd launch", ce);
   CUtensorMap mq, mk, mv;
@@ -352,34 +371,50 @@ extern "C" int jattn_fwd_noalloc(const jattn_bf16* q, const jattn_bf16* k, const
 
 namespace {
 
-// The forward for a validated shape (either layout).
+// The forward for a validated shape (either layout); with `saved` non-null
+// (a training forward) q_hat, k_hat and the rows' 1/rms go there instead of
+// into scratch.
 int fwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
-             const float* gk, jattn_bf16* out, float* lse, void* stream) {
-  const void* ptrs[] = {q, k, v, gq, gk, out, lse};
+             const float* gk, jattn_bf16* out, float* lse, void* saved, void* stream) {
+  const void* ptrs[] = {q, k, v, gq, gk, out, lse, saved};
   for (const void* p : ptrs)
     if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
   const size_t tb = s.elems * 2;
+  const SavedLayout sl = saved_layout(s);
   const Range ins[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(gq, s.d * 4),
                        range_of(gk, s.d * 4)};
-  const Range outs[] = {range_of(out, tb), range_of(lse, s.rows * 4)};
-  for (const Range& o : outs)
+  const Range outs[] = {range_of(out, tb), range_of(lse, s.rows * 4), range_of(saved, saved ? sl.total : 0)};
+  for (size_t a = 0; a < sizeof(outs) / sizeof(outs[0]); ++a) {
     for (const Range& i : ins)
-      if (overlaps(o, i)) return JATTN_ERR_ALIAS;
-  if (overlaps(outs[0], outs[1])) return JATTN_ERR_ALIAS;
+      if (overlaps(outs[a], i)) return JATTN_ERR_ALIAS;
+    for (size_t b = a + 1; b < sizeof(outs) / sizeof(outs[0]); ++b)
+      if (overlaps(outs[a], outs[b])) return JATTN_ERR_ALIAS;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = dev_err_ptr();
   if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
   Carve cv;
-  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), fwd_scratch_bytes(s), st);
-  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
-  uint16_t* qhat = cv.take<uint16_t>(s.elems);
-  uint16_t* khat = cv.take<uint16_t>(s.elems);
+  uint16_t *qhat, *khat;
+  float *rq = nullptr, *rk = nullptr;
+  cudaError_t ce;
+  if (saved) {
+    uint8_t* base = static_cast<uint8_t*>(saved);
+    qhat = reinterpret_cast<uint16_t*>(base + sl.qhat);
+    khat = reinterpret_cast<uint16_t*>(base + sl.khat);
+    rq = reinterpret_cast<float*>(base + sl.rq);
+    rk = reinterpret_cast<float*>(base + sl.rk);
+  } else {
+    ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), fwd_scratch_bytes(s), st);
+    if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
+    qhat = cv.take<uint16_t>(s.elems);
+    khat = cv.take<uint16_t>(s.elems);
+  }
   int status = JATTN_OK;
   CUtensorMap mq, mk, mv;
   {
     Timed t(JATTN_KERNEL_QK_NORM_FWD, st);
-    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, static_cast<int64_t>(s.rows), s.d, err, st);
+    ce = launch_qk_norm_fwd(q, k, gq, gk, qhat, khat, rq, rk, static_cast<int64_t>(s.rows), s.d, err, st);
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "qk_norm_fwd launch", ce);
@@ -392,8 +427,10 @@ int fwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
     ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
     if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
   }
-  ce = cudaFreeAsync(cv.base, st);
-  if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "cudaFreeAsync", ce);
+  if (cv.base) {
+    ce = cudaFreeAsync(cv.base, st);
+    if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "cudaFreeAsync", ce);
+  }
   return status;
 }
 
@@ -406,7 +443,7 @@ extern "C" int jattn_fwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   Shape s;
   int rc = check_shape(B, H, N_img, N_txt, d, &s);
   if (rc != JATTN_OK) return rc;
-  return fwd_body(s, q, k, v, gq, gk, out, lse, stream);
+  return fwd_body(s, q, k, v, gq, gk, out, lse, nullptr, stream);
 }
 
 extern "C" int jattn_fwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
@@ -416,22 +453,26 @@ extern "C" int jattn_fwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const 
   Shape s;
   int rc = check_shape_varlen(cu_seqlens, n_seqs, H, d, &s);
   if (rc != JATTN_OK) return rc;
-  return fwd_body(s, q, k, v, gq, gk, out, lse, stream);
+  return fwd_body(s, q, k, v, gq, gk, out, lse, nullptr, stream);
 }
 
 namespace {
 
-// The backward for a validated shape (either layout).
+// The backward for a validated shape (either layout); with `saved` non-null
+// q_hat, k_hat and the rows' 1/rms come from a training forward instead of
+// being recomputed.
 int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
-             const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout, jattn_bf16* dq,
-             jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, void* stream) {
-  const void* ptrs[] = {q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk};
+             const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout, const void* saved,
+             jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, void* stream) {
+  const void* ptrs[] = {q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk};
   for (const void* p : ptrs)
     if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
   const size_t tb = s.elems * 2;
   const size_t gb = static_cast<size_t>(s.d) * 4;
+  const SavedLayout sl = saved_layout(s);
   const Range ins[] = {range_of(q, tb),  range_of(k, tb),   range_of(v, tb),           range_of(gq, gb),
-                       range_of(gk, gb), range_of(out, tb), range_of(lse, s.rows * 4), range_of(dout, tb)};
+                       range_of(gk, gb), range_of(out, tb), range_of(lse, s.rows * 4), range_of(dout, tb),
+                       range_of(saved, saved ? sl.total : 0)};
   const Range outs[] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb), range_of(dgq, gb), range_of(dgk, gb)};
   for (size_t a = 0; a < sizeof(outs) / sizeof(outs[0]); ++a) {
     for (const Range& i : ins)
@@ -449,12 +490,23 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   const int nparts_k = attn_bwd_dgk_parts(as);
   const int counter_words = as.deterministic ? attn_bwd_counter_words(as) : 0;
   Carve cv;
-  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base), bwd_scratch_bytes(s, nparts_q, nparts_k, counter_words), st);
+  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base),
+                                   bwd_scratch_bytes(s, nparts_q, nparts_k, counter_words, saved != nullptr), st);
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
-  uint16_t* qhat = cv.take<uint16_t>(s.elems);
-  uint16_t* khat = cv.take<uint16_t>(s.elems);
-  float* rq = cv.take<float>(s.rows);
-  float* rk = cv.take<float>(s.rows);
+  uint16_t *qhat, *khat;
+  float *rq, *rk;
+  if (saved) {
+    const uint8_t* base = static_cast<const uint8_t*>(saved);
+    qhat = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(base + sl.qhat));
+    khat = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(base + sl.khat));
+    rq = reinterpret_cast<float*>(const_cast<uint8_t*>(base + sl.rq));
+    rk = reinterpret_cast<float*>(const_cast<uint8_t*>(base + sl.rk));
+  } else {
+    qhat = cv.take<uint16_t>(s.elems);
+    khat = cv.take<uint16_t>(s.elems);
+    rq = cv.take<float>(s.rows);
+    rk = cv.take<float>(s.rows);
+  }
   float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
   float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
   const bool chunks = attn_bwd_stats_chunks(s.d);
@@ -470,7 +522,8 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   CUtensorMap mq, mk, mv, mdo, mstats, mdqacc;
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, qhat, khat, rq, rk, nlse2, delta, stats,
+    // Saved activations: the preparation computes only the statistics.
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, saved ? nullptr : qhat, khat, rq, rk, nlse2, delta, stats,
                          sqrtf(static_cast<float>(s.d)), attn_bwd_dq_stores_first(as) ? nullptr : dqacc, dg_ticket,
                          1 + counter_words, s.BH, s.seg, s.d, err, st);
   }
@@ -512,7 +565,7 @@ extern "C" int jattn_bwd(const jattn_bf16* q, const jattn_bf16* k, const jattn_b
   Shape s;
   int rc = check_shape(B, H, N_img, N_txt, d, &s);
   if (rc != JATTN_OK) return rc;
-  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, stream);
+  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, nullptr, dq, dk, dv, dgq, dgk, stream);
 }
 
 extern "C" int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
@@ -524,7 +577,64 @@ extern "C" int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const 
   Shape s;
   int rc = check_shape_varlen(cu_seqlens, n_seqs, H, d, &s);
   if (rc != JATTN_OK) return rc;
-  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, dq, dk, dv, dgq, dgk, stream);
+  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, nullptr, dq, dk, dv, dgq, dgk, stream);
+}
+
+extern "C" size_t jattn_saved_bytes(int B, int H, int N_img, int N_txt, int d) {
+  Shape s;
+  if (check_shape(B, H, N_img, N_txt, d, &s) != JATTN_OK) return 0;
+  return saved_layout(s).total;
+}
+
+extern "C" size_t jattn_saved_bytes_varlen(const int* cu_seqlens, int n_seqs, int H, int d) {
+  Shape s;
+  if (check_shape_varlen(cu_seqlens, n_seqs, H, d, &s) != JATTN_OK) return 0;
+  return saved_layout(s).total;
+}
+
+extern "C" int jattn_fwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                               const float* gk, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out,
+                               float* lse, void* saved, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !saved) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return fwd_body(s, q, k, v, gq, gk, out, lse, saved, stream);
+}
+
+extern "C" int jattn_fwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                                      const float* gk, const int* cu_seqlens, int n_seqs, int H, int d,
+                                      jattn_bf16* out, float* lse, void* saved, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !saved) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape_varlen(cu_seqlens, n_seqs, H, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return fwd_body(s, q, k, v, gq, gk, out, lse, saved, stream);
+}
+
+extern "C" int jattn_bwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
+                               const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
+                               const void* saved, jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq,
+                               float* dgk, int B, int H, int N_img, int N_txt, int d, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !saved || !dq || !dk || !dv || !dgq || !dgk)
+    return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, stream);
+}
+
+extern "C" int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v,
+                                      const float* gq, const float* gk, const jattn_bf16* out, const float* lse,
+                                      const jattn_bf16* dout, const void* saved, jattn_bf16* dq, jattn_bf16* dk,
+                                      jattn_bf16* dv, float* dgq, float* dgk, const int* cu_seqlens, int n_seqs,
+                                      int H, int d, void* stream) {
+  if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !saved || !dq || !dk || !dv || !dgq || !dgk)
+    return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape_varlen(cu_seqlens, n_seqs, H, d, &s);
+  if (rc != JATTN_OK) return rc;
+  return bwd_body(s, q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, stream);
 }
 
 namespace jattn {

@@ -69,9 +69,10 @@ struct Scratch {
 // --- norm / elementwise kernels (HBM-bound) ---------------------------------
 // The streaming norm kernels take the per-launch device error word: their
 // bounded waits on the bulk-copy ring report a timeout through it.
+// rq / rk (1/rms of every q / k row) are written unless null.
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
-                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, uint32_t* dev_err,
-                               cudaStream_t st);
+                               uint16_t* qhat, uint16_t* khat, float* rq, float* rk, int64_t rows, int d,
+                               uint32_t* dev_err, cudaStream_t st);
 // Rows are the BH heads' seg.rows rows.  The softmax statistics are written
 // in the per-head padded layout (segment s from seg.pcu[s], 128-row
 // multiples): with `stats` null, nlse2 (= -LSE log2 e, -inf in pad rows) and
@@ -80,7 +81,9 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 // fp32 value (columns 0-2 and 3-5; pad rows -1e30 and 0), zeros after.  The
 // dq accumulator rows are zeroed unless dqacc is null (the deterministic
 // backward stores its first contribution); the first n_tickets words of
-// `tickets` are zeroed.
+// `tickets` are zeroed.  With qhat null (q_hat, k_hat, rq and rk saved by a
+// training forward) only the statistics, the zeroing and the tickets are
+// done, and q, k, qhat, khat, rq, rk are not accessed.
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,

@@ -184,16 +184,18 @@ constexpr int kNormThreads = 256;
 // 1024 / d threads per column for their final sum.
 constexpr int kQBwdThreads = 1024;
 
-// q, k -> q_hat, k_hat (bf16).  Rows [0, rows) are q rows, [rows, 2 rows) k
-// rows; each thread takes kU rows per pass and loads the next pass's rows
-// before it transforms the current ones.
+// q, k -> q_hat, k_hat (bf16), and 1/rms of every row into rq, rk unless
+// they are null.  Rows [0, rows) are q rows, [rows, 2 rows) k rows; each
+// thread takes kU rows per pass and loads the next pass's rows before it
+// transforms the current ones.
 template <int D>
 __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* __restrict__ q,
                                                                    const uint4* __restrict__ k,
                                                                    const float* __restrict__ gq,
                                                                    const float* __restrict__ gk,
                                                                    uint4* __restrict__ qhat,
-                                                                   uint4* __restrict__ khat, int64_t rows) {
+                                                                   uint4* __restrict__ khat, float* __restrict__ rq,
+                                                                   float* __restrict__ rk, int64_t rows) {
   constexpr int TPR = D / 8;
   constexpr int RPB = kNormThreads / TPR;  // rows per block and pass slot
   constexpr int kU = 2;
@@ -229,7 +231,10 @@ __global__ void __launch_bounds__(kNormThreads) qk_norm_fwd_kernel(const uint4* 
       const bool is_k = rr >= rows;
       float r;
       const uint4 y = norm_chunk<TPR>(cur[u], is_k ? g_k : g_q, &r);
-      if (rr < total) (is_k ? khat[(rr - rows) * TPR + sub] : qhat[rr * TPR + sub]) = y;
+      if (rr < total) {
+        (is_k ? khat[(rr - rows) * TPR + sub] : qhat[rr * TPR + sub]) = y;
+        if (rq && sub == 0) (is_k ? rk[rr - rows] : rq[rr]) = r;
+      }
       cur[u] = nxt[u];
     }
   }
@@ -254,7 +259,7 @@ __device__ __forceinline__ void split3_bf16(float x, uint32_t (&h)[3]) {
   }
 }
 
-template <int D>
+template <int D, bool kNorm>
 __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
@@ -300,8 +305,8 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     locate(b, prow, row, in_range, valid);
     const int64_t idx = (valid ? row : 0) * TPR + sub;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    w.q = valid ? q[idx] : zero;
-    w.k = valid ? k[idx] : zero;
+    w.q = kNorm && valid ? q[idx] : zero;
+    w.k = kNorm && valid ? k[idx] : zero;
     w.o = valid ? out[idx] : zero;
     w.d = valid ? dout[idx] : zero;
     w.lse = (valid && sub == 0) ? lse[row] : 0.f;
@@ -316,9 +321,12 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     int64_t prow, row;
     bool in_range, valid;
     locate(base, prow, row, in_range, valid);
-    float r1, r2;
-    const uint4 yq = norm_chunk<TPR>(cur.q, g_q, &r1);
-    const uint4 yk = norm_chunk<TPR>(cur.k, g_k, &r2);
+    float r1 = 0.f, r2 = 0.f;
+    uint4 yq = make_uint4(0u, 0u, 0u, 0u), yk = yq;
+    if constexpr (kNorm) {
+      yq = norm_chunk<TPR>(cur.q, g_q, &r1);
+      yk = norm_chunk<TPR>(cur.k, g_k, &r2);
+    }
     float o[8], dd[8];
     unpack8(cur.o, o);
     unpack8(cur.d, dd);
@@ -343,14 +351,16 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
       }
       if (valid) {
         const int64_t idx = row * TPR + sub;
-        qhat[idx] = yq;
-        khat[idx] = yk;
+        if constexpr (kNorm) {
+          qhat[idx] = yq;
+          khat[idx] = yk;
+        }
         if (dqacc) {
           const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
           dqacc[idx * 2] = z;
           dqacc[idx * 2 + 1] = z;
         }
-        if (sub == 0) {
+        if (kNorm && sub == 0) {
           rq[row] = r1;
           rk[row] = r2;
         }
@@ -541,14 +551,14 @@ int q_norm_bwd_parts(int d) {
 }
 
 cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
-                               uint16_t* qhat, uint16_t* khat, int64_t rows, int d, uint32_t* dev_err,
-                               cudaStream_t st) {
+                               uint16_t* qhat, uint16_t* khat, float* rq, float* rk, int64_t rows, int d,
+                               uint32_t* dev_err, cudaStream_t st) {
   (void)dev_err;
   auto* a = reinterpret_cast<const uint4*>(q);
   auto* b = reinterpret_cast<const uint4*>(k);
   auto kernel = d == 64 ? qk_norm_fwd_kernel<64> : qk_norm_fwd_kernel<128>;
   return launch_pdl(kernel, dim3(row_grid(kernel, 2 * rows, d)), dim3(kNormThreads), 0, st, a, b, gq, gk,
-                    reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rows);
+                    reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq, rk, rows);
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
@@ -559,7 +569,10 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
   (void)dev_err;
   const int64_t padded_rows = static_cast<int64_t>(BH) * seg.prows;
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
-  auto kernel = d == 64 ? bwd_prep_kernel<64> : bwd_prep_kernel<128>;
+  // q_hat / k_hat / rq / rk saved by a training forward: only the statistics.
+  const bool norm = qhat != nullptr;
+  auto kernel = d == 64 ? (norm ? bwd_prep_kernel<64, true> : bwd_prep_kernel<64, false>)
+                        : (norm ? bwd_prep_kernel<128, true> : bwd_prep_kernel<128, false>);
   return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
                     gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
                     rk, nlse2, delta, reinterpret_cast<uint4*>(stats), inv_scale, reinterpret_cast<float4*>(dqacc),

@@ -157,3 +157,35 @@ def test_mode_switches_validate_and_apply_to_later_calls(lib):
     assert lib.jattn_set_sm_limit(-1) == ja.STATUS_CODE["JATTN_ERR_INVALID_ARG"]
     assert ja.jattn_set_deterministic(True) == 0
     assert ja.jattn_set_deterministic(False) == 0
+
+
+def test_training_pair_sizes_and_validation(lib):
+    """jattn_saved_bytes covers q_hat, k_hat and two fp32 values per row (0
+    for a shape the calls reject), and the training pair validates like
+    jattn_fwd / jattn_bwd plus its `saved` argument, before any CUDA call."""
+    B, H, N_img, N_txt, d = 1, 2, 16, 8, 64
+    rows, elems = B * H * (N_img + N_txt), B * H * (N_img + N_txt) * d
+    nb = ja.jattn_saved_bytes(B, H, N_img, N_txt, d)
+    assert nb >= 2 * elems * 2 + 2 * rows * 4 and nb % 256 == 0
+    assert ja.jattn_saved_bytes(B, H, N_img, N_txt, 96) == 0
+    assert ja.jattn_saved_bytes(0, H, N_img, N_txt, d) == 0
+    assert ja.jattn_saved_bytes_varlen([0, 24, 40], 2, 64) >= 2 * 2 * 40 * 64 * 2
+    assert ja.jattn_saved_bytes_varlen([0, 24, 24], 2, 64) == 0
+    S = A + 0xB000000
+    f = lambda **kw: lib.jattn_fwd_train(*[kw.get(n, v) for n, v in (  # noqa: E731
+        ("q", A), ("k", A + 0x1000000), ("v", A + 0x2000000), ("gq", A + 0x3000000), ("gk", A + 0x3001000),
+        ("B", B), ("H", H), ("N_img", N_img), ("N_txt", N_txt), ("d", d), ("out", A + 0x4000000),
+        ("lse", A + 0x5000000), ("saved", S))], None)
+    assert f(saved=None) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]
+    assert f(saved=S + 8) == STATUS_CODE["JATTN_ERR_MISALIGNED"]
+    assert f(saved=A + 0x4000000) == STATUS_CODE["JATTN_ERR_ALIAS"]       # saved == out
+    assert f(saved=A + 0x2000000 - 0x100) == STATUS_CODE["JATTN_ERR_ALIAS"]  # saved runs into v
+    assert f(d=32) == STATUS_CODE["JATTN_ERR_UNSUPPORTED"]
+    g = lambda **kw: lib.jattn_bwd_train(*[kw.get(n, v) for n, v in (  # noqa: E731
+        ("q", A), ("k", A + 0x1000000), ("v", A + 0x2000000), ("gq", A + 0x3000000), ("gk", A + 0x3001000),
+        ("out", A + 0x4000000), ("lse", A + 0x5000000), ("dout", A + 0x6000000), ("saved", S),
+        ("dq", A + 0x7000000), ("dk", A + 0x8000000), ("dv", A + 0x9000000), ("dgq", A + 0xA000000),
+        ("dgk", A + 0xA001000), ("B", B), ("H", H), ("N_img", N_img), ("N_txt", N_txt), ("d", d))], None)
+    assert g(saved=None) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]
+    assert g(saved=A + 0x7000000) == STATUS_CODE["JATTN_ERR_ALIAS"]       # saved == dq
+    assert g(dq=None) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]

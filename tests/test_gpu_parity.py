@@ -470,3 +470,87 @@ def test_varlen_of_equal_lengths_equals_the_batched_layout(ja):
     assert relF(packed["dq"], pack(batched["dq"])) < 1e-2
     for name in ("dgq", "dgk"):
         assert relF(packed[name], batched[name]) < 1e-5, name
+
+
+# ---------------------------------------------------------------------------
+# Training pair: jattn_fwd_train keeps q_hat, k_hat and 1/rms for
+# jattn_bwd_train, which must then match jattn_fwd / jattn_bwd exactly.
+# ---------------------------------------------------------------------------
+def _bitwise_equal(a, b):
+    return torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                       b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,N,n_txt", [(2, 3, 333, 77), (1, 2, 1101, 77), (3, 1, 129, 0)])
+def test_training_pair_matches_plain_calls(ja, B, H, N, n_txt, d):
+    """In the deterministic mode every output of the training pair equals the
+    plain calls' bit for bit (the same kernels, fed the same q_hat / k_hat /
+    1/rms, in the same order); the plain calls are held to the oracle on the
+    same inputs."""
+    inp = make_inputs(B, H, N, d, seed=1200 + N + d)
+    tq, tk, tv, tgq, tgk, tdo = (dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_f32(inp.gq),
+                                 dev_f32(inp.gk), dev_bf16(inp.dout))
+    ja.jattn_set_deterministic(True)
+    try:
+        out0, lse0 = ja.forward(tq, tk, tv, tgq, tgk, n_txt)
+        g0 = ja.backward(tq, tk, tv, tgq, tgk, out0, lse0, tdo, n_txt)
+        out1, lse1, saved = ja.forward_train(tq, tk, tv, tgq, tgk, n_txt)
+        g1 = ja.backward_train(tq, tk, tv, tgq, tgk, out1, lse1, tdo, saved, n_txt)
+        torch.cuda.synchronize()
+        assert ja.jattn_last_device_error() == 0
+    finally:
+        ja.jattn_set_deterministic(False)
+    assert _bitwise_equal(out0, out1) and _bitwise_equal(lse0, lse1)
+    for name, a, b in zip(("dq", "dk", "dv", "dgq", "dgk"), g0, g1):
+        assert _bitwise_equal(a, b), name
+    ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    got = {"O": np64(out1), "LSE": np64(lse1)}
+    got.update({n: np64(t) for n, t in zip(("dq", "dk", "dv", "dgq", "dgk"), g1)})
+    check_fwd(got, ref, f"train {B, H, N, d}")
+    check_bwd(got, ref, where=f"train {B, H, N, d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_training_pair_varlen_matches_plain_calls(ja, d):
+    lens = (1101, 1, 300, 128)
+    cu, q, k, v, dout, gq, gk = packed_inputs(lens, 2, d, seed=1300 + d)
+    tq, tk, tv, tgq, tgk, tdo = dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_f32(gq), dev_f32(gk), dev_bf16(dout)
+    H, T = 2, cu[-1]
+    ja.jattn_set_deterministic(True)
+    try:
+        out0, lse0 = ja.forward_varlen(tq, tk, tv, tgq, tgk, cu)
+        g0 = ja.backward_varlen(tq, tk, tv, tgq, tgk, out0, lse0, tdo, cu)
+        saved = torch.empty(ja.jattn_saved_bytes_varlen(cu, H, d), dtype=torch.uint8, device="cuda")
+        out1, lse1 = torch.empty_like(tq), torch.empty((H, T), dtype=torch.float32, device="cuda")
+        ja.jattn_fwd_train_varlen(tq, tk, tv, tgq, tgk, cu, H, d, out1, lse1, saved)
+        g1 = [torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv), torch.empty_like(tgq),
+              torch.empty_like(tgk)]
+        ja.jattn_bwd_train_varlen(tq, tk, tv, tgq, tgk, out1, lse1, tdo, saved, *g1, cu, H, d)
+        torch.cuda.synchronize()
+        assert ja.jattn_last_device_error() == 0
+    finally:
+        ja.jattn_set_deterministic(False)
+    assert _bitwise_equal(out0, out1) and _bitwise_equal(lse0, lse1)
+    for name, a, b in zip(("dq", "dk", "dv", "dgq", "dgk"), g0, g1):
+        assert _bitwise_equal(a, b), name
+
+
+def test_training_pair_argument_checks(ja):
+    B, H, N, d = 1, 2, 200, 64
+    inp = make_inputs(B, H, N, d, seed=1400)
+    tq, tk, tv, tgq, tgk = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_f32(inp.gq), dev_f32(inp.gk)
+    out, lse = torch.empty_like(tq), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    nb = ja.jattn_saved_bytes(B, H, N - 10, 10, d)
+    assert nb >= 2 * tq.numel() * 2 + 2 * B * H * N * 4
+    saved = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    code = ja.STATUS_CODE
+    assert ja.jattn_fwd_train(tq, tk, tv, tgq, tgk, B, H, N - 10, 10, d, out, lse, 0, check=False) == \
+        code["JATTN_ERR_INVALID_ARG"]
+    # `saved` overlapping an output is refused before anything runs.
+    assert ja.jattn_fwd_train(tq, tk, tv, tgq, tgk, B, H, N - 10, 10, d, out, lse, out.data_ptr(),
+                              check=False) == code["JATTN_ERR_ALIAS"]
+    assert ja.jattn_fwd_train(tq, tk, tv, tgq, tgk, B, H, N - 10, 10, d, out, lse, saved.data_ptr() + 4,
+                              check=False) == code["JATTN_ERR_MISALIGNED"]
+    assert ja.jattn_fwd_train(tq, tk, tv, tgq, tgk, B, H, N - 10, 10, d, out, lse, saved) == 0
+    torch.cuda.synchronize()
