@@ -58,6 +58,8 @@
 // dQ(i), dP(i+1), with dP(i+1) waiting for dQ(i) to be drained.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "jattn_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -786,16 +788,22 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_cta_shared(uint32_t* p, uin
 // thread 0.  Rows past the tensor's end are clipped by the TMA unit; rows of
 // the tile that belong to the next segment receive exact zeros (their
 // probabilities are 0).  Thread 0 waits for the previous tile's reduces to
-// have read the staging before the halves are rewritten.  Ordered modes:
-// thread 0 also waits, before the tile's reduces, until the contributions of
-// lower rank to the query tile are complete (its counter), and announces its
-// own once they are complete (at the next tile, or at once for a unit's
-// last).
+// have read the staging before the halves are rewritten.
+// Ordered modes: thread 0 also waits, before the tile's reduces, until the
+// contributions of lower rank to the query tile are complete (its counter),
+// and announces its own once they are complete (at the next tile, or at once
+// for a unit's last).  In the [B, H, N, d] layout (whose tiles end at the
+// tensor's end) the rank-0 contribution is a TMA store, so that the
+// accumulator needs no zeroing beforehand.  (Arrival order keeps the zeroed
+// accumulator: a first-store there would make later contributions wait for
+// the store's completion, which queues behind the reduces already in flight
+// and stalled the drain by microseconds.)
 template <int D, bool kOrd, class W>
 __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, const CUtensorMap* mdq,
                             uint32_t* __restrict__ counters, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   static_assert(D == 64, "tiled dQ drain serves d = 64");
+  constexpr bool kFirstStore = kOrd && std::is_same<W, BwdWorkUniform>::value;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int r128 = (warp & 3) * 32 + lane;  // query row == TMEM lane
   const bool leader = r128 == 0;
@@ -812,7 +820,9 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
     const bool okb = mbar_wait(&bars.drain_sync, (uses++) & 1, ab, dev_err);
     return __all_sync(0xffffffffu, okb) && !*ab;
   };
-  uint32_t* pend = nullptr;  // thread 0, ordered modes: the counter to announce
+  // Thread 0, ordered modes: the counter to announce on once its
+  // contribution is complete.
+  uint32_t* pend = nullptr;
   auto complete_previous = [&]() {
     if (!pend) return;
     bulk_wait_group0();
@@ -833,6 +843,7 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
       uint32_t* cnt = counters + static_cast<size_t>(un.bh) * tiles_per_head + un.prow0 / 128 + qt;
       // Ordered modes: the counter read ahead (its latency overlaps the wait for dQ).
       const uint32_t seen = kOrd && leader && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
+      const bool store = kFirstStore && rank == 0;
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
@@ -862,8 +873,13 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
       if (!(ok = drain_sync())) break;
       if (leader) {
         const int row = un.row0 + qt * 128;
-        tma_reduce_add_3d(mdq, stage, 0, row, un.bh);
-        tma_reduce_add_3d(mdq, stage + 16384, 32, row, un.bh);
+        if (store) {
+          tma_store_3d(mdq, stage, 0, row, un.bh);
+          tma_store_3d(mdq, stage + 16384, 32, row, un.bh);
+        } else {
+          tma_reduce_add_3d(mdq, stage, 0, row, un.bh);
+          tma_reduce_add_3d(mdq, stage + 16384, 32, row, un.bh);
+        }
         bulk_commit_group();
         if constexpr (kOrd) {
           if (rank != un.nkt - 1) {
@@ -875,8 +891,7 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
     }
   }
   if (leader) {
-    if constexpr (kOrd)
-      if (ok) complete_previous();
+    if (ok) complete_previous();
     bulk_wait_group0();
   }
 }
@@ -1565,7 +1580,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 // One dgk partial per CTA.
 int attn_bwd_dgk_parts(const AttnShape& s) { return bwd_plan(s).grid; }
 
-int attn_bwd_counter_words(const AttnShape& s) { return s.BH * (s.seg.prows / 128); }
+int attn_bwd_counter_words(const AttnShape& s) { return s.deterministic ? s.BH * (s.seg.prows / 128) : 0; }
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, const CUtensorMap& map_stats, const CUtensorMap& map_dq,

@@ -488,7 +488,7 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   const int nparts_q = q_norm_bwd_parts(s.d);
   as.deterministic = g_deterministic.load(std::memory_order_relaxed) != 0;
   const int nparts_k = attn_bwd_dgk_parts(as);
-  const int counter_words = as.deterministic ? attn_bwd_counter_words(as) : 0;
+  const int counter_words = attn_bwd_counter_words(as);
   Carve cv;
   cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&cv.base),
                                    bwd_scratch_bytes(s, nparts_q, nparts_k, counter_words, saved != nullptr), st);

@@ -128,14 +128,16 @@ cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, 
                             const AttnShape& s, const float* nlse2_pad,
                             const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
                             float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st);
-// CTAs of the backward launch (one dgk partial each) and, for the
-// deterministic mode, the counter words it needs zeroed (one per query tile).
+// Whether the first dQ contribution to each query tile is stored rather than
+// added, so that the accumulator needs no zeroing: the deterministic mode at
+// d = 128, and at d = 64 in the [B, H, N, d] layout (one segment).
+inline bool attn_bwd_dq_stores_first(const AttnShape& s) {
+  return s.deterministic && (s.d == 128 || s.seg.n == 1);
+}
+// CTAs of the backward launch (one dgk partial each), and the counter words
+// it needs zeroed (deterministic mode: one per query tile; else 0).
 int attn_bwd_dgk_parts(const AttnShape& s);
 int attn_bwd_counter_words(const AttnShape& s);
-// Whether the first dQ contribution to each query tile is stored rather than
-// added (the deterministic mode at d = 128), so that the accumulator needs no
-// zeroing.
-inline bool attn_bwd_dq_stores_first(const AttnShape& s) { return s.deterministic && s.d == 128; }
 
 // Encodes a 3-D TMA map over a [BH, N, d] bf16 tensor with a (64, 128, 1)
 // box and 128-byte swizzle.  Returns false if the driver rejects it.
