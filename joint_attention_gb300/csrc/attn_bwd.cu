@@ -81,11 +81,16 @@ constexpr int kRegCompute128 = 128, kRegOther128 = 72;
 // The split uses the whole launch allocation (640 x 96): the kernel must launch
 // with exactly 96 registers per thread.
 constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
-// Each SM sub-partition holds one warp of every warpgroup (warp w on w % 4)
-// and 16384 registers, so one warp of each role must fit there too.
-static_assert(32 * (2 * kRegCompute64 + kRegDrain64 + kRegEpi64 + kRegMma64) <= 16384,
-              "d = 64 register split exceeds a sub-partition");
-static_assert(32 * (2 * kRegCompute128 + 3 * kRegOther128) <= 16384, "d = 128 register split exceeds a sub-partition");
+// Each SM sub-partition holds one warp of every warpgroup (warp w on w % 4),
+// and setmaxnreg.inc draws only on the registers its five warps were launched
+// with (5 x 32 x 96): a warp's increase that the decreases on its own
+// sub-partition do not cover waits forever.  So the five warps of every
+// sub-partition must fit the launch allocation of five warps.
+constexpr int kSubPartRegs = 5 * 32 * kRegLaunchMin;
+static_assert(32 * (2 * kRegCompute64 + kRegDrain64 + kRegEpi64 + kRegMma64) <= kSubPartRegs,
+              "d = 64 register split exceeds a sub-partition's launch allocation");
+static_assert(32 * (2 * kRegCompute128 + 3 * kRegOther128) <= kSubPartRegs,
+              "d = 128 register split exceeds a sub-partition's launch allocation");
 static_assert(256 * kRegCompute64 + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <= kBwdThreads * kRegLaunchMin,
               "d = 64 register split exceeds the launch allocation");
 static_assert(256 * kRegCompute128 + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
