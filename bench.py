@@ -375,6 +375,17 @@ def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
         else:
             row["images_equiv_per_s"] = B / (12 * ms * 1e-3)
         res[name] = row
+        if name == WORKLOAD:
+            # The same workload with dQ added in a fixed order (jattn_set_deterministic): the
+            # cost of bit-for-bit repeatable gradients.
+            ja.jattn_set_deterministic(True)
+            try:
+                ms_det = median_ms(one)
+            finally:
+                ja.jattn_set_deterministic(False)
+            res[name + "_deterministic"] = dict(row, mode="fwd+bwd, deterministic dQ order", ms=ms_det,
+                                                tflops=fl / (ms_det * 1e-3) / 1e12,
+                                                images_equiv_per_s=B / (12 * ms_det * 1e-3))
         del sets, out, lse, dq, dk, dv, saved
     # Packed variable-length call (the training pair's varlen form): the 512 px and 256 px joint
     # lengths mixed in one call, 8 x 1101 + 16 x 333 rows per head, H = 12, d = 64.
