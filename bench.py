@@ -318,7 +318,7 @@ def run_reference(args):
     return 0
 
 
-def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
+def per_config_throughput(ja, torch, dev, stream, peaks, reps=50, warmup=10):
     """TFLOP/s and images-equivalent/s of every workload of the parity suite (one GPU, eager
     calls, inputs resident on the device; the fwd+bwd rows are 14·B·H·N²·d per step, the CFG
     sampling row is its forward, 4·B·H·N²·d per denoising step).  Inputs are seeded device
@@ -417,9 +417,85 @@ def per_config_throughput(ja, torch, dev, stream, reps=50, warmup=10):
                          "d": d, "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                          "images_equiv_per_s": len(lens) / (12 * ms * 1e-3)}
     del sets, out, lse, dq, dk, dv, saved
+    res[WORKLOAD + "_projected"] = projected_step_throughput(ja, torch, dev, stream, median_ms, peaks)
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the per-config pass")
     return res
+
+
+def projected_step_throughput(ja, torch, dev, stream, median_ms, peaks):
+    """The 512 px training step from the tokens: both streams' QKV projections (width C = 768,
+    W [3 H d, C] per stream) with QK-RMSNorm in the projection's epilogue (jattn_qkv_norm), then
+    the attention forward from the saved q_hat / k_hat (jattn_fwd_saved) and the training
+    backward.  Beside it the same step with the projection as two cuBLAS GEMMs (torch F.linear,
+    bf16), the heads copied into the joint layout, and the training pair normalising q / k
+    itself.  Reports both step times, the fused kernel's own time (CUDA events around each
+    launch) and its TFLOP/s against the measured bf16 peak."""
+    from joint_attention_gb300.inputs import CONFIGS
+
+    c = CONFIGS[WORKLOAD]
+    B, H, N_img, N_txt, d, N = c.B, c.H, c.N_img, c.N_txt, c.d, c.N
+    C = H * d
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000)
+    sets = [{"x_img": torch.randn((B, N_img, C), generator=gen, device=dev).to(torch.bfloat16),
+             "x_txt": torch.randn((B, N_txt, C), generator=gen, device=dev).to(torch.bfloat16),
+             "dout": torch.randn((B, H, N, d), generator=gen, device=dev).to(torch.bfloat16)}
+            for _ in range(N_SETS)]
+    w = {s: (torch.randn((3 * H * d, C), generator=gen, device=dev) * C ** -0.5).to(torch.bfloat16)
+         for s in ("img", "txt")}
+    b = {s: torch.randn(3 * H * d, generator=gen, device=dev) * 0.1 for s in ("img", "txt")}
+    b16 = {s: b[s].to(torch.bfloat16) for s in b}
+    gq = torch.rand(d, generator=gen, device=dev) + 0.5
+    gk = torch.rand(d, generator=gen, device=dev) + 0.5
+    q = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    k, v, out = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dgq, dgk = torch.empty_like(gq), torch.empty_like(gk)
+    saved = torch.empty(ja.jattn_saved_bytes(B, H, N_img, N_txt, d), dtype=torch.uint8, device=dev)
+
+    def fused(i):
+        t = sets[i % N_SETS]
+        ja.jattn_qkv_norm(t["x_img"], w["img"], b["img"], t["x_txt"], w["txt"], b["txt"], gq, gk, B, H, N_img,
+                          N_txt, d, C, q, k, v, saved, stream)
+        ja.jattn_fwd_saved(v, B, H, N_img, N_txt, d, out, lse, saved, stream)
+        ja.jattn_bwd_train(q, k, v, gq, gk, out, lse, t["dout"], saved, dq, dk, dv, dgq, dgk, B, H, N_img, N_txt,
+                           d, stream)
+
+    def unfused(i):
+        t = sets[i % N_SETS]
+        # torch's current stream is `stream` (the bench launches everything on it)
+        for s, x, rows in (("txt", t["x_txt"], slice(0, N_txt)), ("img", t["x_img"], slice(N_txt, N))):
+            y = torch.nn.functional.linear(x, w[s], b16[s]).view(B, -1, 3, H, d).permute(2, 0, 3, 1, 4)
+            q[:, :, rows], k[:, :, rows], v[:, :, rows] = y[0], y[1], y[2]
+        ja.jattn_fwd_train(q, k, v, gq, gk, B, H, N_img, N_txt, d, out, lse, saved, stream)
+        ja.jattn_bwd_train(q, k, v, gq, gk, out, lse, t["dout"], saved, dq, dk, dv, dgq, dgk, B, H, N_img, N_txt,
+                           d, stream)
+
+    ms_fused = median_ms(fused)
+    ms_unfused = median_ms(unfused)
+    ja.jattn_profile_reset()
+    ja.jattn_profile_enable(True)
+    for i in range(20):
+        fused(i)
+    torch.cuda.synchronize(dev)
+    ja.jattn_profile_enable(False)
+    kinds = {ja.jattn_kernel_name(kk): ja.jattn_profile_read(kk) for kk in range(ja.KERNEL_KINDS)}
+    n, tot = kinds["qkv_norm"]
+    qkv_us = tot / max(n, 1) * 1e3
+    proj_fl = 2.0 * B * N * (3 * H * d) * C
+    qkv_tf = proj_fl / (qkv_us * 1e-6) / 1e12
+    fl = proj_fl + flops_fwd(B, H, N, d) + flops_bwd(B, H, N, d)
+    row = {"mode": "QKV projection + QK-RMSNorm epilogue, attention fwd from saved, training bwd",
+           "B": B, "H": H, "N": N, "d": d, "C": C, "ms": ms_fused, "tflops": fl / (ms_fused * 1e-3) / 1e12,
+           "ms_projection_by_cublas_and_norm_pass": ms_unfused,
+           "qkv_norm_us": qkv_us, "qkv_norm_tflops": qkv_tf,
+           "qkv_norm_frac_of_measured_bf16": qkv_tf / peaks["bf16_tflops"],
+           "kernel_us": {name: tot_ms / max(cnt, 1) * 1e3 for name, (cnt, tot_ms) in kinds.items() if cnt},
+           "images_equiv_per_s": B / (12 * ms_fused * 1e-3)}
+    del sets, q, k, v, out, lse, dq, dk, dv, saved
+    return row
 
 
 def main():
@@ -669,7 +745,7 @@ def main():
                 "peak_source": f"{peak_src} ({which})", **extra}
     per_cfg = None
     if not args.no_per_config and world == 1:
-        per_cfg = per_config_throughput(ja, torch, dev, stream)
+        per_cfg = per_config_throughput(ja, torch, dev, stream, peaks)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(B, H, N, d, c.seed, args.cpu_budget_s, max_heads=64)

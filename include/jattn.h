@@ -51,7 +51,7 @@ typedef uint16_t jattn_bf16; /* bfloat16 bit pattern */
 typedef enum {
   JATTN_OK = 0,
   JATTN_ERR_INVALID_ARG = 1, /* null pointer, B/H/d <= 0, N_img/N_txt < 0, N < 1, size overflow */
-  JATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128} */
+  JATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}; jattn_qkv_norm: C not a multiple of 8 */
   JATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   JATTN_ERR_ALIAS = 4,       /* an output buffer overlaps an input or another output */
   JATTN_ERR_CUDA = 5,        /* a CUDA launch or allocation failed */
@@ -156,6 +156,51 @@ int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn
                            const int* cu_seqlens, int n_seqs, int H, int d, void* stream);
 
 /*
+ * QKV projection with QK-RMSNorm in its epilogue (re-diffusion README,
+ * "architecture flowchart": each stream's tokens are projected to Q, K, V
+ * with that stream's own weights, the streams are concatenated along the
+ * token axis and Q, K are RMS-normalised before the attention; "design notes"
+ * table, row "QK norm").  One call computes, for both streams,
+ *
+ *   Y = bf16(X W^T + b)           fp32 accumulation, bias added in fp32,
+ *                                 then one rounding to bf16
+ *   q, k, v = the Y columns of each head, written into the joint layout
+ *   q_hat, k_hat, 1/rms of every q and k row, as jattn_fwd_train keeps them
+ *
+ * so that jattn_fwd_saved can start the attention from q_hat / k_hat and
+ * jattn_bwd_train can run the backward, with no normalisation pass of their
+ * own.  Results are those of projecting, then calling jattn_fwd_train on the
+ * projected q, k, v: q_hat, k_hat bit for bit (both correctly rounded), the
+ * 1/rms values to fp32 rounding.
+ *   x_img  : [B, N_img, C] bf16 image-stream tokens (rows N_txt .. N - 1)
+ *   w_img  : [3 H d, C] bf16 image-stream weight, row-major like a linear
+ *            layer's weight: rows h d .. h d + d - 1 give head h of q, rows
+ *            H d + h d .. of k, rows 2 H d + h d .. of v
+ *   b_img  : [3 H d] float32 bias, or NULL for none
+ *   x_txt, w_txt, b_txt : the caption stream's, likewise (rows 0 .. N_txt - 1);
+ *            a stream with no rows may pass NULL tokens and weight
+ *   gq, gk : [d] float32 gains
+ *   C      : model width, a multiple of 8 (else JATTN_ERR_UNSUPPORTED)
+ *   q, k, v: [B, H, N, d] outputs (the layout above)
+ *   saved  : jattn_saved_bytes(B, H, N_img, N_txt, d) bytes, written as a
+ *            training forward writes it
+ * Every pointer is a 16-byte aligned DEVICE pointer; outputs may not overlap
+ * inputs or each other (JATTN_ERR_ALIAS).  The [B, H, N, d] layout only (no
+ * varlen form).  Sizes: 3 H d C, B N_img C and B N_txt C below 2^31.
+ *
+ * jattn_fwd_saved is the attention forward of a training pair whose q_hat /
+ * k_hat are already in `saved` (from jattn_qkv_norm, or from jattn_fwd_train
+ * with the same shape): out and lse as jattn_fwd computes them from the q, k
+ * that gave those q_hat / k_hat.  It launches the attention kernel only.
+ */
+int jattn_qkv_norm(const jattn_bf16* x_img, const jattn_bf16* w_img, const float* b_img, const jattn_bf16* x_txt,
+                   const jattn_bf16* w_txt, const float* b_txt, const float* gq, const float* gk, int B, int H,
+                   int N_img, int N_txt, int d, int C, jattn_bf16* q, jattn_bf16* k, jattn_bf16* v, void* saved,
+                   void* stream);
+int jattn_fwd_saved(const jattn_bf16* v, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse,
+                    const void* saved, void* stream);
+
+/*
  * Forward without any device allocation.  (No counterpart on the pages: an
  * integration entry point.)  Same arguments, layout and results as jattn_fwd,
  * but the scratch it needs (the normalised q_hat and k_hat, 2 * 2 * B*H*N*d
@@ -208,7 +253,7 @@ int jattn_selftest_wait_timeout(void* stream);
 
 /*
  * Kernel timing (off by default; no counterpart on the pages: measurement
- * support).  While enabled, every kernel launch made by jattn_fwd / jattn_bwd
+ * support).  While enabled, every kernel launch made by the library
  * on the calling thread's device is bracketed by two CUDA events recorded on
  * the caller's stream.  jattn_profile_read synchronises on those events and
  * adds, for one kernel kind, the number of launches and their summed
@@ -220,7 +265,8 @@ typedef enum {
   JATTN_KERNEL_BWD_PREP = 2,     /* norm recompute + rowsum(dO*O) + dq accumulator clear */
   JATTN_KERNEL_ATTN_BWD = 3,     /* tensor-core attention backward (+ K-norm backward) */
   JATTN_KERNEL_Q_NORM_BWD = 4,   /* Q-norm backward from the dq accumulator, and the gain gradients */
-  JATTN_KERNEL_COUNT = 5
+  JATTN_KERNEL_QKV_NORM = 5,     /* QKV projection of both streams with the QK-RMSNorm epilogue */
+  JATTN_KERNEL_COUNT = 6
 } jattn_kernel_kind;
 
 int jattn_profile_enable(int on);

@@ -11,7 +11,7 @@ from ._binding import (KERNEL_KINDS, STATUS, STATUS_CODE, JattnError, declared_s
                        jattn_set_deterministic, jattn_kernel_name, jattn_last_device_error, jattn_last_error_message, jattn_profile_enable, jattn_profile_read,
                        jattn_profile_reset, jattn_status_string, jattn_version, load_library, profile_snapshot,
                        jattn_saved_bytes, jattn_saved_bytes_varlen, jattn_fwd_train, jattn_bwd_train,
-                       jattn_fwd_train_varlen, jattn_bwd_train_varlen)
+                       jattn_fwd_train_varlen, jattn_bwd_train_varlen, jattn_qkv_norm, jattn_fwd_saved)
 
 __all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd", "jattn_fwd",
            "jattn_last_device_error", "jattn_status_string", "jattn_version", "load_library", "forward",
@@ -20,7 +20,8 @@ __all__ = ["STATUS", "STATUS_CODE", "JattnError", "declared_symbols", "jattn_bwd
            "jattn_fwd_varlen", "jattn_bwd_varlen", "forward_varlen", "backward_varlen",
            "jattn_selftest_wait_timeout", "jattn_set_sm_limit", "jattn_set_deterministic", "jattn_saved_bytes",
            "jattn_saved_bytes_varlen", "jattn_fwd_train", "jattn_bwd_train", "jattn_fwd_train_varlen",
-           "jattn_bwd_train_varlen", "forward_train", "backward_train"]
+           "jattn_bwd_train_varlen", "forward_train", "backward_train", "jattn_qkv_norm", "jattn_fwd_saved",
+           "qkv_norm"]
 
 
 def forward(q, k, v, gq, gk, n_txt: int, stream=None):
@@ -93,3 +94,23 @@ def backward_train(q, k, v, gq, gk, out, lse, dout, saved, n_txt: int, stream=No
     dgk = torch.empty_like(gk)
     jattn_bwd_train(q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, B, H, N - n_txt, n_txt, d, stream)
     return dq, dk, dv, dgq, dgk
+
+
+def qkv_norm(x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk, H: int, stream=None):
+    """q, k, v, saved: the QKV projections of the image tokens x_img [B, N_img, C] and the caption
+    tokens x_txt [B, N_txt, C] (bf16 CUDA tensors; weights [3 H d, C] bf16, biases [3 H d] fp32 or
+    None) into the joint [B, H, N, d] layout, with q_hat, k_hat and 1/rms in `saved` for
+    jattn_fwd_saved / backward_train."""
+    import torch
+
+    B, N_img, C = x_img.shape
+    N_txt = x_txt.shape[1]
+    d = gq.shape[0]
+    N = N_img + N_txt
+    dev = x_img.device
+    q = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    saved = torch.empty(jattn_saved_bytes(B, H, N_img, N_txt, d), dtype=torch.uint8, device=dev)
+    jattn_qkv_norm(x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk, B, H, N_img, N_txt, d, C, q, k, v, saved,
+                   stream)
+    return q, k, v, saved

@@ -100,12 +100,16 @@ def load_library(path: str | None = None, build_if_missing: bool = False) -> cty
     lib.jattn_fwd_train_varlen.restype = i32
     lib.jattn_bwd_train_varlen.argtypes = [vp] * 14 + [i32p, i32, i32, i32, vp]
     lib.jattn_bwd_train_varlen.restype = i32
+    lib.jattn_qkv_norm.argtypes = [vp] * 8 + [i32] * 6 + [vp] * 5
+    lib.jattn_qkv_norm.restype = i32
+    lib.jattn_fwd_saved.argtypes = [vp] + [i32] * 5 + [vp] * 4
+    lib.jattn_fwd_saved.restype = i32
     if path is None:
         _lib = lib
     return lib
 
 
-KERNEL_KINDS = 5
+KERNEL_KINDS = 6
 
 
 def jattn_profile_enable(on: bool = True) -> int:
@@ -368,6 +372,47 @@ def jattn_bwd_train_varlen(q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, d
                                     _stream(stream))
     if check and rc != 0:
         raise JattnError(rc, "jattn_bwd_train_varlen")
+    return rc
+
+
+def jattn_qkv_norm(x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk, B: int, H: int, N_img: int, N_txt: int,
+                   d: int, C: int, q, k, v, saved, stream=None, check: bool = True) -> int:
+    """C ABI jattn_qkv_norm.  x_img [B, N_img, C] / x_txt [B, N_txt, C] bf16 tokens, w_* [3 H d, C] bf16,
+    b_* [3 H d] fp32 or None, gq/gk [d] fp32; writes q/k/v [B, H, N, d] bf16 and `saved`."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e = B * H * N * d
+    bf, f32 = torch.bfloat16, torch.float32
+    yc = 3 * H * d
+    nb = jattn_saved_bytes(B, H, N_img, N_txt, d)
+    rc = lib.jattn_qkv_norm(_ptr(x_img, "x_img", bf, B * N_img * C if N_img else None),
+                            _ptr(w_img, "w_img", bf, yc * C if N_img else None), _ptr(b_img, "b_img", f32, yc),
+                            _ptr(x_txt, "x_txt", bf, B * N_txt * C if N_txt else None),
+                            _ptr(w_txt, "w_txt", bf, yc * C if N_txt else None), _ptr(b_txt, "b_txt", f32, yc),
+                            _ptr(gq, "gq", f32, d), _ptr(gk, "gk", f32, d), B, H, N_img, N_txt, d, C,
+                            _ptr(q, "q", bf, e), _ptr(k, "k", bf, e), _ptr(v, "v", bf, e), _saved_ptr(saved, nb),
+                            _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_qkv_norm")
+    return rc
+
+
+def jattn_fwd_saved(v, B: int, H: int, N_img: int, N_txt: int, d: int, out, lse, saved, stream=None,
+                    check: bool = True) -> int:
+    """C ABI jattn_fwd_saved: the attention forward from the q_hat / k_hat already in `saved`."""
+    import torch
+
+    lib = load_library()
+    N = N_img + N_txt
+    e, r = B * H * N * d, B * H * N
+    bf, f32 = torch.bfloat16, torch.float32
+    nb = jattn_saved_bytes(B, H, N_img, N_txt, d)
+    rc = lib.jattn_fwd_saved(_ptr(v, "v", bf, e), B, H, N_img, N_txt, d, _ptr(out, "out", bf, e),
+                             _ptr(lse, "lse", f32, r), _saved_ptr(saved, nb), _stream(stream))
+    if check and rc != 0:
+        raise JattnError(rc, "jattn_fwd_saved")
     return rc
 
 

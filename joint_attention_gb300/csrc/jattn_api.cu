@@ -266,6 +266,19 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS;
 }
 
+bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -637,6 +650,120 @@ extern "C" int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, 
   return bwd_body(s, q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk, stream);
 }
 
+extern "C" int jattn_qkv_norm(const jattn_bf16* x_img, const jattn_bf16* w_img, const float* b_img,
+                              const jattn_bf16* x_txt, const jattn_bf16* w_txt, const float* b_txt, const float* gq,
+                              const float* gk, int B, int H, int N_img, int N_txt, int d, int C, jattn_bf16* q,
+                              jattn_bf16* k, jattn_bf16* v, void* saved, void* stream) {
+  if (!gq || !gk || !q || !k || !v || !saved) return JATTN_ERR_INVALID_ARG;
+  if ((N_img > 0 && (!x_img || !w_img)) || (N_txt > 0 && (!x_txt || !w_txt))) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  if (C <= 0) return JATTN_ERR_INVALID_ARG;
+  if (C % 8 != 0) return JATTN_ERR_UNSUPPORTED;  // TMA row stride: a multiple of 16 bytes
+  const int64_t ycols = 3 * static_cast<int64_t>(H) * d;
+  if (ycols * C >= (int64_t{1} << 31) || static_cast<int64_t>(B) * N_img * C >= (int64_t{1} << 31) ||
+      static_cast<int64_t>(B) * N_txt * C >= (int64_t{1} << 31))
+    return JATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk, q, k, v, saved};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
+  const size_t tb = s.elems * 2;
+  const SavedLayout sl = saved_layout(s);
+  const size_t xb_img = static_cast<size_t>(B) * N_img * C * 2, xb_txt = static_cast<size_t>(B) * N_txt * C * 2;
+  const size_t wb = static_cast<size_t>(ycols) * C * 2, bb = static_cast<size_t>(ycols) * 4;
+  const Range ins[] = {range_of(x_img, N_img ? xb_img : 0), range_of(w_img, N_img ? wb : 0),
+                       range_of(b_img, N_img && b_img ? bb : 0), range_of(x_txt, N_txt ? xb_txt : 0),
+                       range_of(w_txt, N_txt ? wb : 0), range_of(b_txt, N_txt && b_txt ? bb : 0),
+                       range_of(gq, d * 4), range_of(gk, d * 4)};
+  const Range outs[] = {range_of(q, tb), range_of(k, tb), range_of(v, tb), range_of(saved, sl.total)};
+  for (size_t a = 0; a < sizeof(outs) / sizeof(outs[0]); ++a) {
+    for (const Range& i : ins)
+      if (overlaps(outs[a], i)) return JATTN_ERR_ALIAS;
+    for (size_t b = a + 1; b < sizeof(outs) / sizeof(outs[0]); ++b)
+      if (overlaps(outs[a], outs[b])) return JATTN_ERR_ALIAS;
+  }
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = dev_err_ptr();
+  if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
+  uint8_t* base = static_cast<uint8_t*>(saved);
+  QkvLaunch a;
+  a.H = H;
+  a.C = C;
+  a.N = s.N;
+  a.d = d;
+  // Stream 0: the image rows (after the caption rows); stream 1: the caption rows.
+  a.M[0] = B * N_img;
+  a.N_s[0] = N_img;
+  a.row0[0] = N_txt;
+  a.bias[0] = b_img;
+  a.M[1] = B * N_txt;
+  a.N_s[1] = N_txt;
+  a.row0[1] = 0;
+  a.bias[1] = b_txt;
+  a.gq = gq;
+  a.gk = gk;
+  a.out[0] = q;
+  a.out[1] = k;
+  a.out[2] = v;
+  a.hat[0] = reinterpret_cast<uint16_t*>(base + sl.qhat);
+  a.hat[1] = reinterpret_cast<uint16_t*>(base + sl.khat);
+  a.r[0] = reinterpret_cast<float*>(base + sl.rq);
+  a.r[1] = reinterpret_cast<float*>(base + sl.rk);
+  CUtensorMap maps[4];
+  const jattn_bf16* xs[2] = {N_img ? x_img : x_txt, N_txt ? x_txt : x_img};
+  const jattn_bf16* ws[2] = {N_img ? w_img : w_txt, N_txt ? w_txt : w_img};
+  const int64_t ms[2] = {N_img ? a.M[0] : a.M[1], N_txt ? a.M[1] : a.M[0]};
+  for (int i = 0; i < 2; ++i)
+    if (!encode_rows_map(&maps[2 * i], xs[i], ms[i], C, 128) || !encode_rows_map(&maps[2 * i + 1], ws[i], ycols, C, 256))
+      return fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
+  cudaError_t ce;
+  {
+    Timed t(JATTN_KERNEL_QKV_NORM, st);
+    ce = launch_qkv_norm(maps, a, err, st);
+  }
+  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "qkv_norm launch", ce);
+  return JATTN_OK;
+}
+
+extern "C" int jattn_fwd_saved(const jattn_bf16* v, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out,
+                               float* lse, const void* saved, void* stream) {
+  if (!v || !out || !lse || !saved) return JATTN_ERR_INVALID_ARG;
+  Shape s;
+  int rc = check_shape(B, H, N_img, N_txt, d, &s);
+  if (rc != JATTN_OK) return rc;
+  const void* ptrs[] = {v, out, lse, saved};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return JATTN_ERR_MISALIGNED;
+  const size_t tb = s.elems * 2;
+  const SavedLayout sl = saved_layout(s);
+  const Range ins[] = {range_of(v, tb), range_of(saved, sl.total)};
+  const Range outs[] = {range_of(out, tb), range_of(lse, s.rows * 4)};
+  for (size_t a = 0; a < sizeof(outs) / sizeof(outs[0]); ++a) {
+    for (const Range& i : ins)
+      if (overlaps(outs[a], i)) return JATTN_ERR_ALIAS;
+    for (size_t b = a + 1; b < sizeof(outs) / sizeof(outs[0]); ++b)
+      if (overlaps(outs[a], outs[b])) return JATTN_ERR_ALIAS;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = dev_err_ptr();
+  if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
+  const uint8_t* base = static_cast<const uint8_t*>(saved);
+  CUtensorMap mq, mk, mv;
+  if (!encode_bhnd_map(&mq, base + sl.qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, base + sl.khat, s.BH, s.N, s.d) ||
+      !encode_bhnd_map(&mv, v, s.BH, s.N, s.d))
+    return fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
+  AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d)), s.seg};
+  cudaError_t ce;
+  {
+    Timed t(JATTN_KERNEL_ATTN_FWD, st);
+    ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
+  }
+  if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
+  return JATTN_OK;
+}
+
 namespace jattn {
 
 // One thread waits on an mbarrier that nothing arrives at, through the same
@@ -741,6 +868,7 @@ extern "C" const char* jattn_kernel_name(int kind) {
     case JATTN_KERNEL_BWD_PREP: return "bwd_prep";
     case JATTN_KERNEL_ATTN_BWD: return "attn_bwd";
     case JATTN_KERNEL_Q_NORM_BWD: return "q_norm_bwd";
+    case JATTN_KERNEL_QKV_NORM: return "qkv_norm";
     default: return "unknown";
   }
 }
@@ -749,7 +877,8 @@ extern "C" const char* jattn_status_string(int status) {
   switch (status) {
     case JATTN_OK: return "ok";
     case JATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive or overflowing size)";
-    case JATTN_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 64 or 128)";
+    case JATTN_ERR_UNSUPPORTED:
+      return "unsupported size (d must be 64 or 128; jattn_qkv_norm: C a multiple of 8)";
     case JATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case JATTN_ERR_ALIAS: return "an output buffer overlaps another buffer";
     case JATTN_ERR_CUDA: return "CUDA launch or allocation failed";

@@ -139,6 +139,27 @@ inline bool attn_bwd_dq_stores_first(const AttnShape& s) {
 int attn_bwd_dgk_parts(const AttnShape& s);
 int attn_bwd_counter_words(const AttnShape& s);
 
+// --- QKV projection with the QK-RMSNorm epilogue ---------------------------
+// Stream 0 is the image stream, stream 1 the caption stream; maps holds the
+// TMA maps of x0, w0, x1, w1 (encode_rows_map: x with 128-row boxes, w with
+// 256-row boxes).  A stream with M = 0 rows launches no tiles (its maps are
+// then any valid map).
+struct QkvLaunch {
+  int H, C, N, d;
+  int M[2];     // token rows B * N_s
+  int N_s[2];   // tokens per batch item
+  int row0[2];  // first row in the joint sequence
+  const float* bias[2];  // [3 H d] fp32 or null
+  const float *gq, *gk;
+  uint16_t* out[3];  // q, k, v
+  uint16_t* hat[2];  // q_hat, k_hat
+  float* r[2];       // rq, rk
+};
+cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const QkvLaunch& a, uint32_t* dev_err, cudaStream_t st);
+// A 2-D TMA map over a row-major [rows, cols] bf16 matrix with a
+// (64, box_rows) box and 128-byte swizzle (cols * 2 a multiple of 16).
+bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+
 // Encodes a 3-D TMA map over a [BH, N, d] bf16 tensor with a (64, 128, 1)
 // box and 128-byte swizzle.  Returns false if the driver rejects it.
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d);

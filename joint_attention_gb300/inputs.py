@@ -146,3 +146,45 @@ class CfgStream:
                           {"name": c.name, "step": self.step_index, "N_img": c.N_img, "N_txt": c.N_txt})
         self.step_index += 1
         return out
+
+
+@dataclass
+class QkvInputs:
+    """Tokens and weights of the two streams' QKV projections."""
+
+    x_img: np.ndarray  # [B, N_img, C]
+    w_img: np.ndarray  # [3 H d, C]
+    b_img: np.ndarray | None  # [3 H d]
+    x_txt: np.ndarray  # [B, N_txt, C]
+    w_txt: np.ndarray
+    b_txt: np.ndarray | None
+    gq: np.ndarray
+    gk: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+
+def make_qkv_inputs(B: int, H: int, N_img: int, N_txt: int, d: int, C: int, seed: int,
+                    bias: bool = True) -> QkvInputs:
+    """Draw the projection inputs of both streams.
+
+    Tokens ~ N(0, 1) (the adaLN-modulated hidden states feeding the
+    projection are of unit scale), weights ~ N(0, 1/C) (a linear layer's usual
+    initial scale, so each projected value is of unit scale), all
+    bf16-rounded; biases ~ N(0, 0.1^2) float32 (not rounded); gains
+    ~ U(0.5, 1.5) bf16-rounded.  Draw order (PCG64, float32): x_img, x_txt,
+    w_img, w_txt, then (if bias) b_img, b_txt, then gq, gk.
+    """
+    rng = np.random.default_rng(seed)
+    x_img = _normal(rng, (B, N_img, C), 1.0)
+    x_txt = _normal(rng, (B, N_txt, C), 1.0)
+    ws = float(1.0 / np.sqrt(C))
+    w_img = _normal(rng, (3 * H * d, C), ws)
+    w_txt = _normal(rng, (3 * H * d, C), ws)
+    b_img = b_txt = None
+    if bias:
+        b_img = rng.standard_normal(3 * H * d, dtype=np.float32) * np.float32(0.1)
+        b_txt = rng.standard_normal(3 * H * d, dtype=np.float32) * np.float32(0.1)
+    gq = _gain(rng, d)
+    gk = _gain(rng, d)
+    return QkvInputs(x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk,
+                     {"B": B, "H": H, "N_img": N_img, "N_txt": N_txt, "d": d, "C": C, "seed": seed})

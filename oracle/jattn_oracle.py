@@ -202,6 +202,47 @@ def joint_attention_streams(q_txt, k_txt, v_txt, q_img, k_img, v_img, gq, gk, ep
     return O[:, :, :n_txt], O[:, :, n_txt:], lse
 
 
+# ---------------------------------------------------------------------------
+# QKV projection per stream, then QK-RMSNorm ("architecture flowchart":
+# adaLN -> QKV per stream -> concat [c; x] -> QK-RMSNorm -> SDPA)
+# ---------------------------------------------------------------------------
+def qkv_projection(x, w, b, H: int):
+    """One stream's QKV projection with that stream's weights.
+
+    x: [B, N_s, C] tokens; w: [3 H d, C], laid out like a linear layer's
+    weight (output row j = x . w[j]): rows h d .. h d + d - 1 are head h of q,
+    rows H d + h d .. of k, rows 2 H d + h d .. of v; b: [3 H d] or None.
+    Returns (Y, Y_bf16), both [3, B, H, N_s, d] (q, k, v stacked): Y = x w^T + b
+    exactly in float64, and its single rounding to bf16 (the projection's
+    bf16 output in bf16 training).
+    """
+    x, w = _as64(x), _as64(w)
+    B, N_s, _ = x.shape
+    d = w.shape[0] // (3 * H)
+    Y = x @ w.T
+    if b is not None:
+        Y = Y + _as64(b)
+    Y = Y.reshape(B, N_s, 3, H, d).transpose(2, 0, 3, 1, 4)
+    return Y, round_to_bf16(Y)
+
+
+def qkv_norm_streams(x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk, H: int, eps: float = EPS):
+    """Both streams projected, joined caption-first along the token axis, and
+    Q, K normalised: what the fused projection call produces.
+
+    Returns a dict: y_exact [3, B, H, N, d] (before rounding), q, k, v
+    [B, H, N, d] (bf16 values), qhat, khat (bf16-rounded RMSNorm of q, k) and
+    rq, rk [B, H, N] (each row's 1/rms).
+    """
+    parts = [qkv_projection(x_txt, w_txt, b_txt, H), qkv_projection(x_img, w_img, b_img, H)]
+    y_exact = np.concatenate([p[0] for p in parts], axis=3)
+    q, k, v = np.concatenate([p[1] for p in parts], axis=3)
+    qh, rq = rmsnorm_fwd(q, gq, eps)
+    kh, rk = rmsnorm_fwd(k, gk, eps)
+    return {"y_exact": y_exact, "q": q, "k": k, "v": v, "qhat": round_to_bf16(qh), "khat": round_to_bf16(kh),
+            "rq": rq[..., 0], "rk": rk[..., 0]}
+
+
 def joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu_seqlens, eps: float = EPS, round_qk: bool = True):
     """Packed sequences of different lengths (re-diffusion README: the
     aspect-bucketed training data, and multi-resolution training on its

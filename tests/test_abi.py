@@ -26,7 +26,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_kernel_names_and_profile_argument_checks(lib):
     names = [ja.jattn_kernel_name(k) for k in range(ja.KERNEL_KINDS)]
-    assert names == ["qk_norm_fwd", "attn_fwd", "bwd_prep", "attn_bwd", "q_norm_bwd"]
+    assert names == ["qk_norm_fwd", "attn_fwd", "bwd_prep", "attn_bwd", "q_norm_bwd", "qkv_norm"]
     assert ja.jattn_kernel_name(ja.KERNEL_KINDS) == "unknown"
     import ctypes
     n, ms = ctypes.c_int(0), ctypes.c_double(0)
@@ -189,3 +189,39 @@ def test_training_pair_sizes_and_validation(lib):
     assert g(saved=None) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]
     assert g(saved=A + 0x7000000) == STATUS_CODE["JATTN_ERR_ALIAS"]       # saved == dq
     assert g(dq=None) == STATUS_CODE["JATTN_ERR_INVALID_ARG"]
+
+
+def test_qkv_norm_and_fwd_saved_validation(lib):
+    """jattn_qkv_norm / jattn_fwd_saved refuse bad arguments before any CUDA call."""
+    B, H, N_img, N_txt, d, C = 2, 3, 40, 8, 64, 96
+    S = A + 0xB000000
+    f = lambda **kw: lib.jattn_qkv_norm(*[kw.get(n, v) for n, v in (  # noqa: E731
+        ("x_img", A), ("w_img", A + 0x1000000), ("b_img", None), ("x_txt", A + 0x2000000),
+        ("w_txt", A + 0x3000000), ("b_txt", A + 0x3100000), ("gq", A + 0x3200000), ("gk", A + 0x3201000),
+        ("B", B), ("H", H), ("N_img", N_img), ("N_txt", N_txt), ("d", d), ("C", C), ("q", A + 0x4000000),
+        ("k", A + 0x5000000), ("v", A + 0x6000000), ("saved", S))], None)
+    code = STATUS_CODE
+    assert f(saved=None) == code["JATTN_ERR_INVALID_ARG"]
+    assert f(q=None) == code["JATTN_ERR_INVALID_ARG"]
+    assert f(x_img=None) == code["JATTN_ERR_INVALID_ARG"]          # image rows need tokens
+    assert f(w_txt=None) == code["JATTN_ERR_INVALID_ARG"]          # caption rows need a weight
+    assert f(B=0) == code["JATTN_ERR_INVALID_ARG"]
+    assert f(C=0) == code["JATTN_ERR_INVALID_ARG"]
+    assert f(C=100) == code["JATTN_ERR_UNSUPPORTED"]               # row stride not a multiple of 16 bytes
+    assert f(d=32) == code["JATTN_ERR_UNSUPPORTED"]
+    assert f(C=1 << 24, H=64) == code["JATTN_ERR_INVALID_ARG"]     # 3 H d C beyond 2^31
+    assert f(x_img=A + 2) == code["JATTN_ERR_MISALIGNED"]
+    assert f(b_img=A + 0x3300008) == code["JATTN_ERR_MISALIGNED"]
+    assert f(q=A + 0x5000000) == code["JATTN_ERR_ALIAS"]           # q == k
+    assert f(saved=A + 0x1000000) == code["JATTN_ERR_ALIAS"]       # saved over w_img
+    assert f(v=A + 0x3200000 - 0x100) == code["JATTN_ERR_ALIAS"]   # v runs into gq
+    # A stream without rows needs no tokens or weight.
+    assert f(N_txt=0, x_txt=None, w_txt=None, b_txt=None, d=32) == code["JATTN_ERR_UNSUPPORTED"]
+    g = lambda **kw: lib.jattn_fwd_saved(*[kw.get(n, v) for n, v in (  # noqa: E731
+        ("v", A), ("B", B), ("H", H), ("N_img", N_img), ("N_txt", N_txt), ("d", d), ("out", A + 0x1000000),
+        ("lse", A + 0x2000000), ("saved", S))], None)
+    assert g(saved=None) == code["JATTN_ERR_INVALID_ARG"]
+    assert g(d=96) == code["JATTN_ERR_UNSUPPORTED"]
+    assert g(out=A + 0x1000004) == code["JATTN_ERR_MISALIGNED"]
+    assert g(out=S) == code["JATTN_ERR_ALIAS"]
+    assert g(lse=A + 0x10) == code["JATTN_ERR_ALIAS"]

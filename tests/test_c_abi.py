@@ -25,7 +25,7 @@ int main(void) {
   EXPECT(jattn_version() >= 100);
   EXPECT(strcmp(jattn_status_string(JATTN_OK), jattn_status_string(JATTN_ERR_TIMEOUT)) != 0);
   EXPECT(strcmp(jattn_kernel_name(JATTN_KERNEL_ATTN_BWD), "attn_bwd") == 0);
-  EXPECT(JATTN_KERNEL_COUNT == 5);
+  EXPECT(JATTN_KERNEL_COUNT == 6);
   /* null pointers and bad shapes are rejected before anything is enqueued */
   EXPECT(jattn_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 16, 8, 64, NULL, NULL, NULL) == JATTN_ERR_INVALID_ARG);
   EXPECT(jattn_bwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,

@@ -483,3 +483,129 @@ def test_oracle_reproduces_its_stored_tiny_values():
         assert np.max(np.abs(a - b)) <= 1e-12 * max(1.0, np.max(np.abs(b))), key
     for key, v in stored["norms"].items():
         assert abs(now["norms"][key] - v) <= 1e-12 * v, key
+
+
+# ---------------------------------------------------------------------------
+# QKV projection per stream, then QK-RMSNorm ("architecture flowchart")
+# ---------------------------------------------------------------------------
+def _one_hot_layout_errors(fn, B=2, H=3, d=4, N_img=5, N_txt=3, C=16, seed=3):
+    """Tokens that are unit vectors turn the projection into a lookup: the
+    token (b, n) of a stream with x = e_c gives, for head h and element e,
+    q = w[h d + e, c] + b[h d + e], k = w[H d + h d + e, c] + ..., v = w[2 H d
+    + h d + e, c] + ..., at joint row n (caption stream) or N_txt + n (image
+    stream).  Returns the number of elements of q, k, v that differ from that
+    lookup (with the bf16 rounding of each looked-up value)."""
+    rng = np.random.default_rng(seed)
+    ws = {s: to_bf16_values(rng.standard_normal((3 * H * d, C)).astype(np.float32)) for s in ("img", "txt")}
+    bs = {s: rng.standard_normal(3 * H * d) for s in ("img", "txt")}
+    cs = {"img": rng.integers(0, C, (B, N_img)), "txt": rng.integers(0, C, (B, N_txt))}
+    xs = {}
+    for s, n_s in (("img", N_img), ("txt", N_txt)):
+        x = np.zeros((B, n_s, C))
+        for b in range(B):
+            for n in range(n_s):
+                x[b, n, cs[s][b, n]] = 1.0
+        xs[s] = x
+    gq = rng.uniform(0.5, 1.5, d)
+    gk = rng.uniform(0.5, 1.5, d)
+    out = fn(xs["img"], ws["img"], bs["img"], xs["txt"], ws["txt"], bs["txt"], gq, gk, H)
+    wrong = 0
+    for s, n_s, row0 in (("img", N_img, N_txt), ("txt", N_txt, 0)):
+        for b in range(B):
+            for n in range(n_s):
+                c = cs[s][b, n]
+                for which, key in enumerate(("q", "k", "v")):
+                    for h in range(H):
+                        for e in range(d):
+                            j = which * H * d + h * d + e
+                            want = oracle.round_to_bf16(np.array([ws[s][j, c] + bs[s][j]]))[0]
+                            wrong += int(out[key][b, h, row0 + n, e] != want)
+    return wrong
+
+
+def test_qkv_projection_one_hot_tokens_look_up_weight_columns():
+    assert _one_hot_layout_errors(oracle.qkv_norm_streams) == 0
+
+
+def test_qkv_projection_of_all_ones_tokens_is_the_weight_row_sum():
+    rng = np.random.default_rng(4)
+    B, N_s, C, H, d = 2, 3, 24, 2, 8
+    w = rng.standard_normal((3 * H * d, C))
+    b = rng.standard_normal(3 * H * d)
+    Y, _ = oracle.qkv_projection(np.ones((B, N_s, C)), w, b, H)
+    rowsum = w.sum(axis=1) + b
+    for which in range(3):
+        for h in range(H):
+            want = rowsum[which * H * d + h * d:which * H * d + (h + 1) * d]
+            np.testing.assert_allclose(Y[which, :, h], np.broadcast_to(want, (B, N_s, d)), rtol=1e-13, atol=1e-13)
+
+
+def test_qkv_projection_rounds_the_exact_sum_once():
+    """bf16 keeps 8 significant bits: at 1 its spacing is 2^-7.  An exact sum
+    of 1 + 2^-8 is a tie and goes to the even neighbour 1; 1 + 3 2^-8 goes to
+    1 + 2^-6; a bias of 2^-30 on the first tie moves the exact value above the
+    midpoint, so one rounding gives 1 + 2^-7 (rounding through fp32 first
+    would lose the 2^-30 and give 1)."""
+    H, d = 1, 1
+    w = np.zeros((3, 2))
+    w[:, 0] = 1.0
+    w[:, 1] = 2.0 ** -8
+    x = np.array([[[1.0, 1.0], [1.0, 3.0]]])
+    _, Yr = oracle.qkv_projection(x, w, None, H)
+    assert Yr[0, 0, 0, 0, 0] == 1.0 and Yr[0, 0, 0, 1, 0] == 1.0 + 2.0 ** -6
+    _, Yr = oracle.qkv_projection(x[:, :1], w, np.full(3, 2.0 ** -30), H)
+    assert Yr[0, 0, 0, 0, 0] == 1.0 + 2.0 ** -7
+
+
+def test_qkv_norm_streams_matches_torch_float64():
+    """The float64 torch route (F.linear, view / permute into heads, cat along
+    the tokens caption first, F.rms_norm) gives the same values."""
+    B, H, N_img, N_txt, d, C = 2, 3, 7, 4, 8, 16
+    from joint_attention_gb300.inputs import make_qkv_inputs
+
+    inp = make_qkv_inputs(B, H, N_img, N_txt, d, C, seed=9)
+    ref = oracle.qkv_norm_streams(inp.x_img, inp.w_img, inp.b_img, inp.x_txt, inp.w_txt, inp.b_txt, inp.gq,
+                                  inp.gk, H)
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))  # noqa: E731
+
+    def proj(x, w, b):
+        y = F.linear(t(x), t(w), t(b))                      # [B, N_s, 3 H d]
+        return y.view(B, -1, 3, H, d).permute(2, 0, 3, 1, 4)  # [3, B, H, N_s, d]
+
+    y = torch.cat([proj(inp.x_txt, inp.w_txt, inp.b_txt), proj(inp.x_img, inp.w_img, inp.b_img)], dim=3)
+    np.testing.assert_allclose(ref["y_exact"], y.numpy(), rtol=1e-12, atol=1e-12)
+    for key, i, g in (("qhat", 0, inp.gq), ("khat", 1, inp.gk)):
+        xr = t(ref["qkv"[i]])
+        want = F.rms_norm(xr, (d,), weight=t(g), eps=jo.EPS)
+        np.testing.assert_allclose(ref[key], oracle.round_to_bf16(want.numpy()), rtol=0, atol=0)
+        rr = torch.rsqrt(xr.pow(2).mean(-1) + jo.EPS)
+        np.testing.assert_allclose(ref["r" + "qk"[i]], rr.numpy(), rtol=1e-14)
+
+
+def _mutant_streams(kind):
+    def proj(x, w, b, H):
+        x, w = np.asarray(x, np.float64), np.asarray(w, np.float64)
+        B, N_s, _ = x.shape
+        d = w.shape[0] // (3 * H)
+        Y = x @ w.T + (0.0 if kind == "no_bias" or b is None else b)
+        if kind == "heads_outer":       # q / k / v interleaved per head
+            Y = Y.reshape(B, N_s, H, 3, d).transpose(3, 0, 2, 1, 4)
+        elif kind == "dim_outer":       # head index and element index swapped
+            Y = Y.reshape(B, N_s, 3, d, H).transpose(2, 0, 4, 1, 3)
+        else:
+            Y = Y.reshape(B, N_s, 3, H, d).transpose(2, 0, 3, 1, 4)
+        return Y, oracle.round_to_bf16(Y)
+
+    def streams(x_img, w_img, b_img, x_txt, w_txt, b_txt, gq, gk, H):
+        parts = [proj(x_txt, w_txt, b_txt, H), proj(x_img, w_img, b_img, H)]
+        if kind == "image_first":
+            parts = parts[::-1]
+        q, k, v = np.concatenate([p[1] for p in parts], axis=3)
+        return {"q": q, "k": k, "v": v}
+
+    return streams
+
+
+@pytest.mark.parametrize("kind", ["no_bias", "heads_outer", "dim_outer", "image_first"])
+def test_planted_projection_mistakes_are_caught(kind):
+    assert _one_hot_layout_errors(_mutant_streams(kind)) > 0
