@@ -22,18 +22,19 @@
 // 64; persistent, one CTA per SM, the image stream's tiles then the caption
 // stream's.
 //   warp 8      TMA producer: the X tile (128 x 64) and the W tile (256 x 64)
-//               of each K step, 128-byte swizzle, through a 4-stage ring.
+//               of each K step, 128-byte swizzle, through a 3-stage ring.
 //   warp 9      MMA issuer: 4 MMAs (M 128, N 256, K 16) per K step into one of
 //               two TMEM accumulators (256 columns each), so that a tile's
 //               epilogue overlaps the next tile's products.
 //   warps 0-7   epilogue, one thread per token row (TMEM lane): warps w and
 //               w + 4 share the lanes of warp w % 4 and take columns 0-127 and
 //               128-255 of the tile (two heads of d = 64, or one of d = 128).
-//               Per head: d fp32 values out of TMEM, + bias, rounded to bf16
-//               (the projection's output) and stored to q / k / v; for q and
-//               k the row's RMSNorm from those bf16 values, and q_hat / k_hat
-//               and r stored too.  Each thread writes whole head rows with
-//               16-byte stores.
+//               Per head: d fp32 values out of TMEM, + bias (the warp's
+//               slice, copied to shared memory while the products run),
+//               rounded to bf16 (the projection's output) for q / k / v; for
+//               q and k the row's RMSNorm from those bf16 values, q_hat /
+//               k_hat and r.  Rows are staged in shared memory and written
+//               out as whole 128-byte lines, four rows per store instruction.
 // Heads past 3 H in the last column tile, and token rows past the stream's
 // end in its last row tile, read the TMA's zero fill and are not stored.
 //
@@ -50,15 +51,33 @@
 namespace jattn {
 namespace {
 
-constexpr int kQkvThreads = 320;
-constexpr int kQkvStages = 4;
+constexpr int kQkvStages = 3;
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kATile = kBM * kBK * 2;  // 16 KB
 constexpr int kBTile = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kATile + kBTile;
-constexpr int kQkvDynSmem = kQkvStages * kStageBytes + 1024;
-constexpr int kWarpProd = 8, kWarpIssue = 9;
-constexpr int kEpiThreads = 256;
+constexpr int kStageRowBytes = 128;                 // 64 bf16 columns of one token row
+constexpr int kStagingBytes = 32 * kStageRowBytes;  // per epilogue warp: its 32 rows of 64 columns
+constexpr uint32_t kDeadRow = 0xFFFFFFFFu;
+
+// Eight epilogue warps (warps w and w + 4 take the TMEM lanes of warp w % 4
+// and columns 0-127 / 128-255 of the tile: two heads of d = 64, or one of
+// d = 128), then the TMA producer and the MMA issuer.  Each epilogue warp
+// stages its rows in shared memory: at d = 64 raw rows and q_hat / k_hat rows
+// in two buffers, at d = 128 one buffer used for each 64-column half.
+template <int D>
+struct QkvCfg {
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kWarpProd = kEpiWarps, kWarpIssue = kEpiWarps + 1;
+  static constexpr int kThreads = 32 * (kEpiWarps + 2);
+  static constexpr int kBuffers = D == 64 ? 2 : 1;
+  static constexpr int kStaging = kBuffers * kStagingBytes;
+  static constexpr int kBiasBytes = 128 * 4;  // per epilogue warp: the bias of its 128 columns
+  static constexpr int kOffStaging = kQkvStages * kStageBytes;
+  static constexpr int kOffBias = kOffStaging + kEpiWarps * kStaging;
+  static constexpr int kDynSmem = kOffBias + kEpiWarps * kBiasBytes + 1024;
+};
 
 struct QkvBars {
   uint64_t full[kQkvStages], empty[kQkvStages];
@@ -76,53 +95,131 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) { return desc + (byte_off >> 4); }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  const uint4 v = ld_shared_v4(addr);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
 
-// The rare path, taken by the whole warp for each of its rows that has an
-// element near a bf16 midpoint (owner: the lane holding the row): each lane
-// takes D / 32 of the row's values (words lane, lane + 32, ... of the owner's
-// packed yb), their squares (exact) summed by error-free additions and a
-// butterfly over the warp (every lane ends with the same double-float sum),
-// then re-rounds its elements that the owner's fp32 path put near a
-// midpoint, storing them again over the owner's hat row.
-template <int D>
-__device__ __forceinline__ void fix_hat_rows(unsigned todo, const uint32_t (&yb)[D / 2], float r, size_t hrow,
-                                             uint16_t* hat_base, const float* g, int lane) {
-  constexpr int kW = D / 64;  // packed words per lane
-  while (todo) {
-    const int owner = __ffs(todo) - 1;
-    todo &= todo - 1;
-    uint32_t mine[kW];
+// Staging of a warp's 32 token rows of 64 bf16 columns (128 bytes each) in
+// shared memory: row i at i * 128, its 16-byte chunk c at slot c ^ (i % 8),
+// so that a row written by one lane and a chunk column read across 8 lanes
+// both touch every bank once.
+__device__ __forceinline__ uint32_t staged(uint32_t buf, int row, int chunk) {
+  return buf + row * kStageRowBytes + ((chunk ^ (row & 7)) << 4);
+}
+// This lane's row: w[0..31] (packed pairs).
+__device__ __forceinline__ void stage_row(uint32_t buf, const uint32_t* w, int lane) {
 #pragma unroll
-    for (int i = 0; i < D / 2; ++i) {
-      const uint32_t t = __shfl_sync(0xffffffffu, yb[i], owner);
+  for (int c = 0; c < 8; ++c) st_shared_v4(staged(buf, lane, c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+// Writes the 32 staged rows out, four whole rows (four 128-byte lines) per
+// store instruction: lanes 8 j' .. 8 j' + 7 take row 4 j + j', one chunk
+// each.  rows[j]: the global row index (b H + h) N + n of staged row
+// 4 j + lane / 8 for head 0 (kDeadRow: past the stream's end); head_rows =
+// h N; col: the first column (0, or 64 within a d = 128 head row).
+template <int D>
+__device__ __forceinline__ void store_rows(uint32_t buf, uint16_t* base, const uint32_t (&rows)[8],
+                                           uint32_t head_rows, int col, int lane) {
+  const int ch = lane & 7;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 val = ld_shared_v4(staged(buf, 4 * j + (lane >> 3), ch));
+    if (rows[j] != kDeadRow)
+      *reinterpret_cast<uint4*>(base + (static_cast<size_t>(rows[j]) + head_rows) * D + col + ch * 8) = val;
+  }
+}
+
+// The double-float sum of squares of a row spread over the warp, the same
+// on every lane: each lane's own error-free sum (s, c), then a butterfly of
+// error-free additions (symmetric, so every lane forms the same values).
+__device__ __forceinline__ void warp_sum_df(float& s, float& c) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off), c2 = __shfl_xor_sync(0xffffffffu, c, off);
+    float t, e;
+    two_sum(s, s2, t, e);
+    s = t;
+    c = __fadd_rn(__fadd_rn(c, c2), e);
+  }
+  fast_two_sum(s, c, s, c);
+}
+__device__ __forceinline__ void add_sq_df(uint32_t w, float& s, float& c) {
+  float t, e;
+  two_sum(s, __fmul_rn(bf_lo(w), bf_lo(w)), t, e);
+  c = __fadd_rn(c, e);
+  two_sum(t, __fmul_rn(bf_hi(w), bf_hi(w)), s, e);
+  c = __fadd_rn(c, e);
+}
+
+// The rare path.  The warp takes each of its rows that has an element near
+// a bf16 midpoint (owner: the lane holding the row) together: each lane
+// takes D / 32 of the row's values, their squares (exact) are summed by
+// error-free additions over the warp, and each lane re-rounds its elements
+// that the owner's fp32 path put near a midpoint, from the double-float r.
+//
+// d = 64 (fix_staged_rows): the row's raw values come from the raw staging
+// buffer and each lane writes its word of the row (two elements, re-rounded
+// where needed) over the staged q_hat / k_hat row, before that is written
+// out.
+__device__ __forceinline__ void fix_staged_rows(unsigned todo, uint32_t raw, uint32_t hat, float r, const float* g,
+                                                int lane) {
+  while (todo) {
+    const int o = __ffs(todo) - 1;
+    todo &= todo - 1;
+    // Word `lane` of row o: elements 2 lane, 2 lane + 1 (chunk lane / 4).
+    const uint32_t off = (lane & 3) * 4;
+    const uint32_t w = ld_shared_u32(staged(raw, o, lane >> 2) + off);
+    const float ro = __shfl_sync(0xffffffffu, r, o);
+    float s = 0.f, c = 0.f;
+    add_sq_df(w, s, c);
+    warp_sum_df(s, c);
+    float rh, rl;
+    rsqrt_mean_eps_df(s, c, 1.f / 64, rh, rl);
+    float f[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = 2 * lane + j;
+      const float x = j ? bf_hi(w) : bf_lo(w);
+      const float z = __fmul_rn(__fmul_rn(g[e], x), ro);
+      f[j] = near_bf16_midpoint(z) ? round_bf16_df(g[e], x, rh, rl) : z;
+    }
+    st_shared_u32(staged(hat, o, lane >> 2) + off, pack_bf16x2(f[0], f[1]));
+  }
+}
+// d = 128 (fix_stored_rows): the row's raw values come from the owner's
+// registers (yb, by shuffles) and the corrected elements are stored again
+// over the owner's q_hat / k_hat row, which is already written.
+__device__ __forceinline__ void fix_stored_rows(unsigned todo, const uint32_t (&yb)[64], float r, size_t hrow,
+                                                uint16_t* hat_base, const float* g, int lane) {
+  while (todo) {
+    const int o = __ffs(todo) - 1;
+    todo &= todo - 1;
+    uint32_t mine[2];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const uint32_t t = __shfl_sync(0xffffffffu, yb[i], o);
       if ((i & 31) == lane) mine[i >> 5] = t;
     }
-    const float ro = __shfl_sync(0xffffffffu, r, owner);
-    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(hrow), owner);
-    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(hrow >> 32), owner);
-    uint16_t* hat = hat_base + ((static_cast<size_t>(hi) << 32) | lo) * D;
+    const float ro = __shfl_sync(0xffffffffu, r, o);
+    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(hrow), o);
+    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(hrow >> 32), o);
+    uint16_t* hat = hat_base + ((static_cast<size_t>(hi) << 32) | lo) * 128;
     float s = 0.f, c = 0.f;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) {
-      float t, e;
-      two_sum(s, __fmul_rn(bf_lo(mine[w]), bf_lo(mine[w])), t, e);
-      c = __fadd_rn(c, e);
-      two_sum(t, __fmul_rn(bf_hi(mine[w]), bf_hi(mine[w])), s, e);
-      c = __fadd_rn(c, e);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, off), c2 = __shfl_xor_sync(0xffffffffu, c, off);
-      float t, e;
-      two_sum(s, s2, t, e);
-      s = t;
-      c = __fadd_rn(__fadd_rn(c, c2), e);
-    }
-    fast_two_sum(s, c, s, c);
+    add_sq_df(mine[0], s, c);
+    add_sq_df(mine[1], s, c);
+    warp_sum_df(s, c);
     float rh, rl;
-    rsqrt_mean_eps_df(s, c, 1.f / D, rh, rl);
+    rsqrt_mean_eps_df(s, c, 1.f / 128, rh, rl);
 #pragma unroll
-    for (int w = 0; w < kW; ++w) {
+    for (int w = 0; w < 2; ++w) {
       const int e0 = 2 * (lane + 32 * w);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -154,75 +251,156 @@ struct QkvParams {
   float* r[2];        // rq, rk: [B, H, N]
 };
 
-// One head of one token row: D accumulator columns at taddr.  row is head
-// 0's row index (b H N + n); the head's is row + h N.
+// Field selection by a runtime index through selects: indexing the kernel's
+// parameter arrays with a runtime value would copy them to local memory.
+__device__ __forceinline__ uint16_t* out_of(const QkvParams& p, int which) {
+  return which == 0 ? p.out[0] : which == 1 ? p.out[1] : p.out[2];
+}
+__device__ __forceinline__ uint16_t* hat_of(const QkvParams& p, int which) { return which == 0 ? p.hat[0] : p.hat[1]; }
+__device__ __forceinline__ float* r_of(const QkvParams& p, int which) { return which == 0 ? p.r[0] : p.r[1]; }
+__device__ __forceinline__ QkvStream stream_of(const QkvParams& p, int si) {
+  QkvStream s;
+  s.M = si ? p.s[1].M : p.s[0].M;
+  s.N_s = si ? p.s[1].N_s : p.s[0].N_s;
+  s.row0 = si ? p.s[1].row0 : p.s[0].row0;
+  s.tile0 = si ? p.s[1].tile0 : p.s[0].tile0;
+  s.bias = si ? p.s[1].bias : p.s[0].bias;
+  return s;
+}
+
+// r of one row from its bf16 values (packed pairs; exact squares): a
+// balanced tree, built block by block (16 values, then across the D / 16
+// blocks) so that few partial sums are live at once.
 template <int D>
-__device__ __forceinline__ void qkv_emit_head(uint32_t taddr, int ocol, bool live, size_t row, const QkvParams& p,
-                                              const float* bias, const QkvBars& bars) {
+__device__ __forceinline__ float row_rsqrt(const uint32_t (&yb)[D / 2]) {
+  float blk[D / 16];
+#pragma unroll
+  for (int b = 0; b < D / 16; ++b) {
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t u = yb[b * 8 + i];
+      t[i] = __fadd_rn(__fmul_rn(bf_lo(u), bf_lo(u)), __fmul_rn(bf_hi(u), bf_hi(u)));
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = __fadd_rn(t[i], t[i + w]);
+    blk[b] = t[0];
+  }
+#pragma unroll
+  for (int w = D / 32; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) blk[i] = __fadd_rn(blk[i], blk[i + w]);
+  return rsqrtf(__fadd_rn(__fmul_rn(blk[0], 1.f / D), kEps));
+}
+
+// 64 columns of this lane's q_hat / k_hat row, (g x) r per element, staged
+// 16 bytes at a time into its row of the staging buffer; `near` collects the
+// elements within the midpoint window.
+__device__ __forceinline__ void stage_hat_row(uint32_t buf, const uint32_t* y, uint32_t g, float r, bool& near,
+                                              int lane) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    // The gains through ordered shared loads: loaded chunk by chunk, not all
+    // at once ahead of the loop.
+    const float4 ga = ld_shared_f4(g + c * 32), gb = ld_shared_f4(g + c * 32 + 16);
+    const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t yv = y[4 * c + i];
+      const float z0 = __fmul_rn(__fmul_rn(gv[2 * i], bf_lo(yv)), r);
+      const float z1 = __fmul_rn(__fmul_rn(gv[2 * i + 1], bf_hi(yv)), r);
+      near |= near_bf16_midpoint(z0) | near_bf16_midpoint(z1);
+      w[i] = pack_bf16x2(z0, z1);
+    }
+    st_shared_v4(staged(buf, lane, c), w[0], w[1], w[2], w[3]);
+  }
+}
+
+// One head of the warp's 32 token rows: D accumulator columns at taddr
+// (this lane's row).  row: head 0's row index (b H N + n) of this lane; the
+// head's is row + h N.  bias: this head's D bias values in shared memory.
+template <int D>
+__device__ __forceinline__ void qkv_emit_head(uint32_t taddr, int ocol, bool live, size_t row,
+                                              const uint32_t (&rows)[8], uint32_t stg, uint32_t bias,
+                                              const QkvParams& p, const QkvBars& bars, int lane) {
   const int hd = p.H * D;
   const int which = ocol / hd;  // 0 q, 1 k, 2 v
-  const size_t hrow = row + static_cast<size_t>((ocol - which * hd) / D) * p.N;
-  // Y = bf16(acc + bias), 64 columns at a time (packed pairs).
+  const uint32_t head_rows = static_cast<uint32_t>((ocol - which * hd) / D) * static_cast<uint32_t>(p.N);
+  const size_t hrow = row + head_rows;
+  const uint32_t raw = stg;
+  // Y = bf16(acc + bias), 32 columns at a time (packed pairs).
   uint32_t yb[D / 2];
 #pragma unroll
-  for (int h64 = 0; h64 < D / 64; ++h64) {
-    uint32_t acc[2][32];
-    tmem_ld32(taddr + h64 * 64, acc[0]);
-    tmem_ld32(taddr + h64 * 64 + 32, acc[1]);
+  for (int c32 = 0; c32 < D / 32; ++c32) {
+    uint32_t acc[32];
+    tmem_ld32(taddr + c32 * 32, acc);
     tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 64; e += 4) {
-      float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (bias) bv = *reinterpret_cast<const float4*>(bias + ocol + h64 * 64 + e);
-      const uint32_t* a = &acc[e / 32][e % 32];
-      yb[h64 * 32 + e / 2] = pack_bf16x2(__uint_as_float(a[0]) + bv.x, __uint_as_float(a[1]) + bv.y);
-      yb[h64 * 32 + e / 2 + 1] = pack_bf16x2(__uint_as_float(a[2]) + bv.z, __uint_as_float(a[3]) + bv.w);
+    for (int e = 0; e < 32; e += 4) {
+      const float4 bv = ld_shared_f4(bias + (c32 * 32 + e) * 4);
+      yb[c32 * 16 + e / 2] = pack_bf16x2(__uint_as_float(acc[e]) + bv.x, __uint_as_float(acc[e + 1]) + bv.y);
+      yb[c32 * 16 + e / 2 + 1] = pack_bf16x2(__uint_as_float(acc[e + 2]) + bv.z, __uint_as_float(acc[e + 3]) + bv.w);
     }
   }
-  if (live) {
-    uint4* dst = reinterpret_cast<uint4*>(p.out[which] + hrow * D);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(yb[4 * c], yb[4 * c + 1], yb[4 * c + 2], yb[4 * c + 3]);
-  }
-  if (which == 2) return;
-
   const float* g = which == 0 ? bars.gq : bars.gk;
-  bool near = false;
-  float r = 0.f;
-  if (live) {
-    // Sum of the squares of the bf16 values: a balanced tree over exact squares.
-    float sq[D / 2];
-#pragma unroll
-    for (int i = 0; i < D / 2; ++i)
-      sq[i] = __fadd_rn(__fmul_rn(bf_lo(yb[i]), bf_lo(yb[i])), __fmul_rn(bf_hi(yb[i]), bf_hi(yb[i])));
-#pragma unroll
-    for (int w = D / 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int i = 0; i < w; ++i) sq[i] = __fadd_rn(sq[i], sq[i + w]);
-    r = rsqrtf(__fadd_rn(__fmul_rn(sq[0], 1.f / D), kEps));
-    uint32_t hb[D / 2];
-#pragma unroll
-    for (int e = 0; e < D; e += 2) {
-      const float z0 = __fmul_rn(__fmul_rn(g[e], bf_lo(yb[e / 2])), r);
-      const float z1 = __fmul_rn(__fmul_rn(g[e + 1], bf_hi(yb[e / 2])), r);
-      near |= near_bf16_midpoint(z0) | near_bf16_midpoint(z1);
-      hb[e / 2] = pack_bf16x2(z0, z1);
+  if constexpr (D == 64) {
+    const uint32_t hat = raw + kStagingBytes;
+    stage_row(raw, yb, lane);
+    if (which == 2) {
+      __syncwarp();
+      store_rows<D>(raw, out_of(p, which), rows, head_rows, 0, lane);
+      __syncwarp();
+      return;
     }
-    uint4* hdst = reinterpret_cast<uint4*>(p.hat[which] + hrow * D);
+    const float r = row_rsqrt<D>(yb);
+    bool near = false;
+    stage_hat_row(hat, yb, smem_u32(g), r, near, lane);
+    const unsigned todo = __ballot_sync(0xffffffffu, near && live);
+    __syncwarp();
+    if (todo) {
+      fix_staged_rows(todo, raw, hat, r, g, lane);
+      __syncwarp();
+    }
+    store_rows<D>(raw, out_of(p, which), rows, head_rows, 0, lane);
+    store_rows<D>(hat, hat_of(p, which), rows, head_rows, 0, lane);
+    if (live) r_of(p, which)[hrow] = r;
+    __syncwarp();
+  } else {
+    // d = 128: each 64-column half through the raw staging buffer.
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) hdst[c] = make_uint4(hb[4 * c], hb[4 * c + 1], hb[4 * c + 2], hb[4 * c + 3]);
-    p.r[which][hrow] = r;
+    for (int h64 = 0; h64 < 2; ++h64) {
+      stage_row(raw, yb + h64 * 32, lane);
+      __syncwarp();
+      store_rows<D>(raw, out_of(p, which), rows, head_rows, h64 * 64, lane);
+      __syncwarp();
+    }
+    if (which == 2) return;
+    const float r = row_rsqrt<D>(yb);
+    bool near = false;
+#pragma unroll
+    for (int h64 = 0; h64 < 2; ++h64) {
+      stage_hat_row(raw, yb + h64 * 32, smem_u32(g + h64 * 64), r, near, lane);
+      __syncwarp();
+      store_rows<D>(raw, hat_of(p, which), rows, head_rows, h64 * 64, lane);
+      __syncwarp();
+    }
+    if (live) r_of(p, which)[hrow] = r;
+    const unsigned todo = __ballot_sync(0xffffffffu, near && live);
+    if (todo) fix_stored_rows(todo, *reinterpret_cast<const uint32_t(*)[64]>(yb), r, hrow, hat_of(p, which), g, lane);
   }
-  const unsigned todo = __ballot_sync(0xffffffffu, near);
-  if (todo) fix_hat_rows<D>(todo, yb, r, hrow, p.hat[which], g, threadIdx.x % 32);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kQkvThreads, 1)
+__global__ void __launch_bounds__(QkvCfg<D>::kThreads, 1)
     qkv_norm_kernel(const __grid_constant__ CUtensorMap map_x0, const __grid_constant__ CUtensorMap map_w0,
                     const __grid_constant__ CUtensorMap map_x1, const __grid_constant__ CUtensorMap map_w1,
                     const __grid_constant__ QkvParams p, const float* __restrict__ gq, const float* __restrict__ gk,
                     uint32_t* dev_err) {
+  using Cfg = QkvCfg<D>;
+  constexpr int kWarpProd = Cfg::kWarpProd, kWarpIssue = Cfg::kWarpIssue;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(16) QkvBars bars;
   uint8_t* sm = align1024(smem_raw);
@@ -237,7 +415,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.acc_full[b], 1);
-      mbar_init(&bars.acc_empty[b], kEpiThreads);
+      mbar_init(&bars.acc_empty[b], Cfg::kEpiThreads);
     }
     mbar_init(&bars.mma_done, 1);
     bars.abort = 0;
@@ -268,7 +446,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
         const int si = t >= p.s[1].tile0 ? 1 : 0;
-        const int tl = t - p.s[si].tile0;
+        const int tl = t - (si ? p.s[1].tile0 : p.s[0].tile0);
         const int mt = tl / p.n_tiles, nt = tl - mt * p.n_tiles;
         const CUtensorMap* mx = si ? &map_x1 : &map_x0;
         const CUtensorMap* mw = si ? &map_w1 : &map_w0;
@@ -316,30 +494,46 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       mbar_wait_drain(&bars.mma_done, 0);
     }
   } else {
-    const int lg = warp & 3, half = warp >> 2;
+    // Warp w: the TMEM lanes of warp w % 4, and columns 128 (w / 4) .. + 127 of the tile.
+    const int lg = warp & 3, wcol = (warp >> 2) * 128;
+    const uint32_t stg = smem_u32(sm + Cfg::kOffStaging + warp * Cfg::kStaging);
+    const uint32_t bias_w = smem_u32(sm + Cfg::kOffBias + warp * Cfg::kBiasBytes);
     const uint32_t lane_base = static_cast<uint32_t>(lg * 32) << 16;
     const int hd3 = 3 * p.H * D;
     int lt = 0;
     for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++lt) {
       const int abuf = lt & 1;
-      const bool ok = mbar_wait(&bars.acc_full[abuf], (lt >> 1) & 1, ab, dev_err);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
       const int si = t >= p.s[1].tile0 ? 1 : 0;
-      const QkvStream& S = p.s[si];
+      const QkvStream S = stream_of(p, si);
       const int tl = t - S.tile0;
       const int mt = tl / p.n_tiles, nt = tl - mt * p.n_tiles;
+      const int col0 = nt * kBN + wcol;  // the warp's first column in Y
+      // The bias of the warp's 128 columns (zero past 3 H d, or without a
+      // bias) into its shared slice, while the products are still running.
+      float4 bq = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (S.bias && col0 + lane * 4 < hd3) bq = __ldg(reinterpret_cast<const float4*>(S.bias + col0) + lane);
+      __syncwarp();  // the previous tile's reads of the slice are done
+      st_shared_v4(bias_w + lane * 16, __float_as_uint(bq.x), __float_as_uint(bq.y), __float_as_uint(bq.z),
+                   __float_as_uint(bq.w));
+      const bool ok = mbar_wait(&bars.acc_full[abuf], (lt >> 1) & 1, ab, dev_err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      __syncwarp();
+      tc_fence_after();
       const int m = mt * kBM + lg * 32 + lane;
       const bool live = m < S.M;
       const int bi = live ? m / S.N_s : 0;
       const int n = live ? S.row0 + (m - bi * S.N_s) : 0;
-      const size_t row = static_cast<size_t>(bi) * p.H * p.N + n;
+      const size_t row = static_cast<size_t>(bi) * p.H * p.N + n;  // < B H N < 2^31 / d
+      const uint32_t row32 = live ? static_cast<uint32_t>(row) : kDeadRow;
+      uint32_t rows[8];  // the rows this lane writes out in store_rows
+#pragma unroll
+      for (int j = 0; j < 8; ++j) rows[j] = __shfl_sync(0xffffffffu, row32, 4 * j + (lane >> 3));
 #pragma unroll
       for (int j = 0; j < 128 / D; ++j) {
-        const int tcol = half * 128 + j * D;  // the head's first column in the tile
-        const int ocol = nt * kBN + tcol;     // ... in Y
+        const int ocol = col0 + j * D;  // the head's first column in Y
         if (ocol < hd3)
-          qkv_emit_head<D>(tmem + lane_base + abuf * kBN + tcol, ocol, live, row, p, S.bias, bars);
+          qkv_emit_head<D>(tmem + lane_base + abuf * kBN + wcol + j * D, ocol, live, row, rows, stg,
+                           bias_w + j * D * 4, p, bars, lane);
       }
       tc_fence_before();
       mbar_arrive(&bars.acc_empty[abuf]);
@@ -377,13 +571,16 @@ cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const QkvLaunch& a, ui
     p.r[i] = a.r[i];
   }
   if (p.tiles == 0) return cudaSuccess;
-  auto kernel = a.d == 64 ? qkv_norm_kernel<64> : qkv_norm_kernel<128>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvDynSmem);
-  if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   const int grid = p.tiles < sms ? p.tiles : sms;
-  return launch_pdl(kernel, dim3(grid), dim3(kQkvThreads), kQkvDynSmem, st, maps[0], maps[1], maps[2], maps[3], p,
-                    a.gq, a.gk, dev_err);
+  auto go = [&](auto kernel, int threads, int smem) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kernel, dim3(grid), dim3(threads), smem, st, maps[0], maps[1], maps[2], maps[3], p, a.gq,
+                      a.gk, dev_err);
+  };
+  if (a.d == 64) return go(qkv_norm_kernel<64>, QkvCfg<64>::kThreads, QkvCfg<64>::kDynSmem);
+  return go(qkv_norm_kernel<128>, QkvCfg<128>::kThreads, QkvCfg<128>::kDynSmem);
 }
 
 }  // namespace jattn
