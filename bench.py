@@ -318,7 +318,7 @@ def run_reference(args):
     return 0
 
 
-def per_config_throughput(ja, torch, dev, stream, peaks, reps=50, warmup=10):
+def per_config_throughput(ja, torch, dev, stream, peaks, reps=50, warmup=10, only=None):
     """TFLOP/s and images-equivalent/s of every workload of the parity suite (one GPU, eager
     calls, inputs resident on the device; the fwd+bwd rows are 14·B·H·N²·d per step, the CFG
     sampling row is its forward, 4·B·H·N²·d per denoising step).  Inputs are seeded device
@@ -343,6 +343,8 @@ def per_config_throughput(ja, torch, dev, stream, peaks, reps=50, warmup=10):
     res = {}
     gen = torch.Generator(device=dev)
     for name, c in CONFIGS.items():
+        if only and name not in only:
+            continue
         B, H, N, d = c.B, c.H, c.N, c.d
         gen.manual_seed(1000 + c.seed)
         shape = (B, H, N, d)
@@ -387,6 +389,8 @@ def per_config_throughput(ja, torch, dev, stream, peaks, reps=50, warmup=10):
                                                 tflops=fl / (ms_det * 1e-3) / 1e12,
                                                 images_equiv_per_s=B / (12 * ms_det * 1e-3))
         del sets, out, lse, dq, dk, dv, saved
+    if only and "varlen_mix" not in only:
+        return _per_config_tail(ja, torch, dev, stream, median_ms, peaks, res, only)
     # Packed variable-length call (the training pair's varlen form): the 512 px and 256 px joint
     # lengths mixed in one call, 8 x 1101 + 16 x 333 rows per head, H = 12, d = 64.
     lens = [1101] * 8 + [333] * 16
@@ -417,7 +421,12 @@ def per_config_throughput(ja, torch, dev, stream, peaks, reps=50, warmup=10):
                          "d": d, "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                          "images_equiv_per_s": len(lens) / (12 * ms * 1e-3)}
     del sets, out, lse, dq, dk, dv, saved
-    res[WORKLOAD + "_projected"] = projected_step_throughput(ja, torch, dev, stream, median_ms, peaks)
+    return _per_config_tail(ja, torch, dev, stream, median_ms, peaks, res, only)
+
+
+def _per_config_tail(ja, torch, dev, stream, median_ms, peaks, res, only):
+    if not only or WORKLOAD + "_projected" in only:
+        res[WORKLOAD + "_projected"] = projected_step_throughput(ja, torch, dev, stream, median_ms, peaks)
     if ja.jattn_last_device_error(stream) != 0:
         raise RuntimeError("device-side wait timed out in the per-config pass")
     return res
@@ -511,6 +520,8 @@ def main():
     ap.add_argument("--cpu-config-budget-s", type=float, default=3.0,
                     help="host seconds of oracle time per workload in the per-config pass")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload throughput pass")
+    ap.add_argument("--per-config", default="",
+                    help="comma-separated rows of the per-workload pass to run (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -745,7 +756,8 @@ def main():
                 "peak_source": f"{peak_src} ({which})", **extra}
     per_cfg = None
     if not args.no_per_config and world == 1:
-        per_cfg = per_config_throughput(ja, torch, dev, stream, peaks)
+        only = {x for x in args.per_config.split(",") if x}
+        per_cfg = per_config_throughput(ja, torch, dev, stream, peaks, only=only)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_sample(B, H, N, d, c.seed, args.cpu_budget_s, max_heads=64)
