@@ -131,9 +131,16 @@ int jattn_bwd_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16*
  * jattn_fwd / jattn_bwd with the same arguments, bit for bit where those
  * repeat bit for bit.
  *   saved : DEVICE buffer of jattn_saved_bytes(...) bytes (16-byte aligned),
- *           written by the forward and read by the backward, which must be
+ *           written by the forward and used by the backward, which must be
  *           given the same q, k, gq, gk and shape; its layout is private.
- *           It may not overlap any other argument.
+ *           It may not overlap any other argument.  It also holds the
+ *           backward's fp32 dQ accumulator, which the forward zeroes while it
+ *           runs (with HBM bandwidth its attention kernel leaves idle) so
+ *           that the backward need not; a backward that finds it not zeroed
+ *           by a forward since the last backward (a second backward on the
+ *           same buffer, or a buffer no forward has filled) zeroes it itself,
+ *           so any number of backward calls per forward stay correct.
+ *           Size: 2 B*H*N*d*2 + B*H*N*d*4 + 2 B*H*N*4 bytes plus alignment.
  * jattn_saved_bytes returns 0 for a shape the calls would reject.  The other
  * arguments and every status are those of jattn_fwd / jattn_bwd (and of
  * their varlen forms); a null `saved` gives JATTN_ERR_INVALID_ARG.
@@ -144,7 +151,7 @@ int jattn_fwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* 
                     int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse, void* saved,
                     void* stream);
 int jattn_bwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq, const float* gk,
-                    const jattn_bf16* out, const float* lse, const jattn_bf16* dout, const void* saved,
+                    const jattn_bf16* out, const float* lse, const jattn_bf16* dout, void* saved,
                     jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, int B, int H, int N_img,
                     int N_txt, int d, void* stream);
 int jattn_fwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
@@ -152,7 +159,7 @@ int jattn_fwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn
                            float* lse, void* saved, void* stream);
 int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
                            const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
-                           const void* saved, jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk,
+                           void* saved, jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk,
                            const int* cu_seqlens, int n_seqs, int H, int d, void* stream);
 
 /*
@@ -191,14 +198,15 @@ int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn
  * jattn_fwd_saved is the attention forward of a training pair whose q_hat /
  * k_hat are already in `saved` (from jattn_qkv_norm, or from jattn_fwd_train
  * with the same shape): out and lse as jattn_fwd computes them from the q, k
- * that gave those q_hat / k_hat.  It launches the attention kernel only.
+ * that gave those q_hat / k_hat.  It launches the attention kernel only (which
+ * also zeroes the buffer's dQ accumulator, as jattn_fwd_train does).
  */
 int jattn_qkv_norm(const jattn_bf16* x_img, const jattn_bf16* w_img, const float* b_img, const jattn_bf16* x_txt,
                    const jattn_bf16* w_txt, const float* b_txt, const float* gq, const float* gk, int B, int H,
                    int N_img, int N_txt, int d, int C, jattn_bf16* q, jattn_bf16* k, jattn_bf16* v, void* saved,
                    void* stream);
 int jattn_fwd_saved(const jattn_bf16* v, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out, float* lse,
-                    const void* saved, void* stream);
+                    void* saved, void* stream);
 
 /*
  * Forward without any device allocation.  (No counterpart on the pages: an

@@ -43,7 +43,7 @@
 namespace jattn {
 namespace {
 
-constexpr int kFwdThreads = 352;
+constexpr int kFwdThreads = 384;  // 8 softmax warps, producer, 2 MMA issuers, accumulator zeroing
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -152,6 +152,28 @@ struct FwdWork {
     return r;
   }
 };
+
+// Warp 11 (training pair): zeroes the backward's fp32 dQ accumulator rows of
+// this CTA's units, with HBM bandwidth the forward leaves idle, then counts
+// the CTA as done (release increment).  The backward's preparation skips its
+// own zeroing when the count equals this launch's grid size, and the
+// norm backward resets the count.
+template <int D, class W>
+__device__ void fwd_zero_dq(const W& w, float* dq, uint32_t* count, int lane) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int u = blockIdx.x; u < w.units; u += gridDim.x) {
+    const FwdUnit un = w.unit(u);
+    const int r1 = min(un.q0 + 2 * kTileM, un.end);
+    uint4* base = reinterpret_cast<uint4*>(dq + (static_cast<size_t>(un.bh) * w.seg.rows + un.q0) * D);
+    const int n = (r1 - un.q0) * (D / 4);
+    for (int i = lane; i < n; i += 32) base[i] = z;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(count, 1u);
+  }
+}
 
 template <int D, class W>
 __device__ void fwd_producer(const CUtensorMap* map_q, const CUtensorMap* map_k, const CUtensorMap* map_v,
@@ -539,7 +561,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                     const __grid_constant__ W w, float scale_log2,
-                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* dev_err) {
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* dq_zero, uint32_t* zero_count,
+                    uint32_t* dev_err) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdBars bars;
@@ -580,6 +603,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp == 8) {
     if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, w, dev_err);
+  } else if (warp == 11) {
+    if (dq_zero) fwd_zero_dq<D>(w, dq_zero, zero_count, lane);
   } else if (warp >= 9) {
     if (lane == 0) fwd_mma<D>(sm, bars, tmem, warp - 9, w, dev_err);
   } else {
@@ -595,7 +620,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 template <int D, class W>
 cudaError_t launch_fwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
+                         const AttnShape& s, uint16_t* out, float* lse, float* dq_zero, uint32_t* zero_count,
+                         uint32_t* dev_err, cudaStream_t st) {
   using C = FwdCfg<D>;
   static_assert(C::kDynSmem + static_cast<int>(sizeof(FwdBars)) <= 232448, "shared memory budget");
   auto kernel = attn_fwd_kernel<D, W>;
@@ -607,19 +633,27 @@ cudaError_t launch_fwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& m
   CUtensorMap mo;  // the output, for the staged tile stores (d = 64)
   if (!encode_bhnd_map(&mo, out, s.BH, s.N, D)) return cudaErrorInvalidValue;
   return launch_pdl(kernel, dim3(grid), dim3(kFwdThreads), C::kDynSmem, st, mq, mk, mv, mo, w, scale_log2,
-                    reinterpret_cast<__nv_bfloat16*>(out), lse, dev_err);
+                    reinterpret_cast<__nv_bfloat16*>(out), lse, dq_zero, zero_count, dev_err);
+}
+
+// Work units (256 query rows of one head's segment) of a launch.
+int fwd_units(const AttnShape& s) {
+  int upc = 0;
+  for (int i = 0; i < s.seg.n; ++i) upc += (s.seg.cu[i + 1] - s.seg.cu[i] + 2 * kTileM - 1) / (2 * kTileM);
+  return s.BH * upc;
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const AttnShape& s,
-                         uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
+                         uint16_t* out, float* lse, float* dq_zero, uint32_t* zero_count, uint32_t* dev_err,
+                         cudaStream_t st) {
   if (s.seg.n == 1) {
     FwdWorkUniform w;
     w.seg.rows = s.seg.rows;
     w.upc = (s.seg.rows + 2 * kTileM - 1) / (2 * kTileM);
     w.nkv = (s.seg.rows + kTileN - 1) / kTileN;
     w.units = s.BH * w.upc;
-    return launch_fwd_w<D>(w, mq, mk, mv, s, out, lse, dev_err, st);
+    return launch_fwd_w<D>(w, mq, mk, mv, s, out, lse, dq_zero, zero_count, dev_err, st);
   }
   FwdWork w;
   w.seg = s.seg;
@@ -628,16 +662,23 @@ cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     w.uf[i + 1] = w.uf[i] + (s.seg.cu[i + 1] - s.seg.cu[i] + 2 * kTileM - 1) / (2 * kTileM);
   w.upc = w.uf[s.seg.n];
   w.units = s.BH * w.upc;
-  return launch_fwd_w<D>(w, mq, mk, mv, s, out, lse, dev_err, st);
+  return launch_fwd_w<D>(w, mq, mk, mv, s, out, lse, dq_zero, zero_count, dev_err, st);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st) {
-  if (s.d == 64) return launch_fwd_d<64>(map_q, map_k, map_v, s, out, lse, dev_err, st);
-  if (s.d == 128) return launch_fwd_d<128>(map_q, map_k, map_v, s, out, lse, dev_err, st);
+                            const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st,
+                            float* dq_zero, uint32_t* zero_count) {
+  if (s.d == 64) return launch_fwd_d<64>(map_q, map_k, map_v, s, out, lse, dq_zero, zero_count, dev_err, st);
+  if (s.d == 128) return launch_fwd_d<128>(map_q, map_k, map_v, s, out, lse, dq_zero, zero_count, dev_err, st);
   return cudaErrorInvalidValue;
+}
+
+int attn_fwd_grid(const AttnShape& s) {
+  const int units = fwd_units(s);
+  const int sms = device_sm_count();
+  return units < sms ? units : sms;
 }
 
 }  // namespace jattn

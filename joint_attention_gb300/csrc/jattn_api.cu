@@ -200,9 +200,11 @@ size_t fwd_scratch_bytes(const Shape& s) { return 2 * (s.elems * 2 + 256) + 256;
 
 // The activations a training forward keeps for its backward, at 256-byte
 // aligned offsets of one caller buffer: q_hat, k_hat (bf16, q's shape), then
-// 1/rms of every q and k row (fp32).
+// 1/rms of every q and k row (fp32); then the backward's fp32 dQ accumulator
+// (q's shape), which the forward zeroes with bandwidth it leaves idle, and the
+// word that counts the forward CTAs that have zeroed their share.
 struct SavedLayout {
-  size_t qhat, khat, rq, rk, total;
+  size_t qhat, khat, rq, rk, dq, zero_count, total;
 };
 SavedLayout saved_layout(const Shape& s) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
@@ -211,7 +213,9 @@ SavedLayout saved_layout(const Shape& s) {
   l.khat = up(s.elems * 2);
   l.rq = l.khat + up(s.elems * 2);
   l.rk = l.rq + up(s.rows * 4);
-  l.total = l.rk + up(s.rows * 4);
+  l.dq = l.rk + up(s.rows * 4);
+  l.zero_count = l.dq + up(s.elems * 4);
+  l.total = l.zero_count + 256;
   return l;
 }
 
@@ -220,10 +224,10 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k, int counter
   if (!saved) {
     b += 2 * (s.elems * 2 + 256);  // q_hat, k_hat
     b += 2 * (s.rows * 4 + 256);   // rq, rk
+    b += s.elems * 4 + 256;        // dq accumulator
   }
   b += 2 * (static_cast<size_t>(s.BH) * s.seg.prows * 4 + 256);   // nlse2, delta
   if (attn_bwd_stats_chunks(s.d)) b += static_cast<size_t>(s.BH) * s.seg.prows * 32 + 256;  // statistics chunks
-  b += s.elems * 4 + 256;                                         // dq accumulator
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
   b += 4 * (1 + static_cast<size_t>(counter_words)) + 256;      // dg ticket, dQ order counters
   return b + 256;
@@ -437,7 +441,9 @@ int fwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   } else {
     AttnShape as{s.BH, s.N, s.d, 1.0f / sqrtf(static_cast<float>(s.d)), s.seg};
     Timed t(JATTN_KERNEL_ATTN_FWD, st);
-    ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
+    uint8_t* base = static_cast<uint8_t*>(saved);
+    ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st, saved ? reinterpret_cast<float*>(base + sl.dq) : nullptr,
+                         saved ? reinterpret_cast<uint32_t*>(base + sl.zero_count) : nullptr);
     if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
   }
   if (cv.base) {
@@ -475,7 +481,7 @@ namespace {
 // q_hat, k_hat and the rows' 1/rms come from a training forward instead of
 // being recomputed.
 int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
-             const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout, const void* saved,
+             const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout, void* saved,
              jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq, float* dgk, void* stream) {
   const void* ptrs[] = {q, k, v, gq, gk, out, lse, dout, saved, dq, dk, dv, dgq, dgk};
   for (const void* p : ptrs)
@@ -507,24 +513,27 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
                                    bwd_scratch_bytes(s, nparts_q, nparts_k, counter_words, saved != nullptr), st);
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "cudaMallocAsync", ce);
   uint16_t *qhat, *khat;
-  float *rq, *rk;
+  float *rq, *rk, *dqacc;
+  uint32_t* zero_count = nullptr;
   if (saved) {
-    const uint8_t* base = static_cast<const uint8_t*>(saved);
-    qhat = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(base + sl.qhat));
-    khat = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(base + sl.khat));
-    rq = reinterpret_cast<float*>(const_cast<uint8_t*>(base + sl.rq));
-    rk = reinterpret_cast<float*>(const_cast<uint8_t*>(base + sl.rk));
+    uint8_t* base = static_cast<uint8_t*>(saved);
+    qhat = reinterpret_cast<uint16_t*>(base + sl.qhat);
+    khat = reinterpret_cast<uint16_t*>(base + sl.khat);
+    rq = reinterpret_cast<float*>(base + sl.rq);
+    rk = reinterpret_cast<float*>(base + sl.rk);
+    dqacc = reinterpret_cast<float*>(base + sl.dq);
+    zero_count = reinterpret_cast<uint32_t*>(base + sl.zero_count);
   } else {
     qhat = cv.take<uint16_t>(s.elems);
     khat = cv.take<uint16_t>(s.elems);
     rq = cv.take<float>(s.rows);
     rk = cv.take<float>(s.rows);
+    dqacc = cv.take<float>(s.elems);
   }
   float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
   float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
   const bool chunks = attn_bwd_stats_chunks(s.d);
   uint16_t* stats = chunks ? cv.take<uint16_t>(static_cast<size_t>(s.BH) * s.seg.prows * 16) : nullptr;
-  float* dqacc = cv.take<float>(s.elems);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
   float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
   // The gain-gradient ticket, then (deterministic mode) one dQ order counter
@@ -538,7 +547,8 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
     // Saved activations: the preparation computes only the statistics.
     ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, saved ? nullptr : qhat, khat, rq, rk, nlse2, delta, stats,
                          sqrtf(static_cast<float>(s.d)), attn_bwd_dq_stores_first(as) ? nullptr : dqacc, dg_ticket,
-                         1 + counter_words, s.BH, s.seg, s.d, err, st);
+                         1 + counter_words, s.BH, s.seg, s.d, err, st, zero_count,
+                         static_cast<uint32_t>(attn_fwd_grid(as)));
   }
   if (ce != cudaSuccess) {
     status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
@@ -558,7 +568,7 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
       stage = "q_norm_bwd launch";
       Timed t(JATTN_KERNEL_Q_NORM_BWD, st);
       ce = launch_q_norm_bwd(dqacc, q, rq, gq, as.scale, dq, dgq_part, nparts_q, static_cast<int64_t>(s.rows),
-                             dgk_part, nparts_k, dg_ticket, dgq, dgk, s.d, err, st);
+                             dgk_part, nparts_k, dg_ticket, dgq, dgk, s.d, err, st, zero_count);
     }
     if (ce != cudaSuccess) status = fail(JATTN_ERR_CUDA, stage, ce);
   }
@@ -627,7 +637,7 @@ extern "C" int jattn_fwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, 
 
 extern "C" int jattn_bwd_train(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v, const float* gq,
                                const float* gk, const jattn_bf16* out, const float* lse, const jattn_bf16* dout,
-                               const void* saved, jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq,
+                               void* saved, jattn_bf16* dq, jattn_bf16* dk, jattn_bf16* dv, float* dgq,
                                float* dgk, int B, int H, int N_img, int N_txt, int d, void* stream) {
   if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !saved || !dq || !dk || !dv || !dgq || !dgk)
     return JATTN_ERR_INVALID_ARG;
@@ -639,7 +649,7 @@ extern "C" int jattn_bwd_train(const jattn_bf16* q, const jattn_bf16* k, const j
 
 extern "C" int jattn_bwd_train_varlen(const jattn_bf16* q, const jattn_bf16* k, const jattn_bf16* v,
                                       const float* gq, const float* gk, const jattn_bf16* out, const float* lse,
-                                      const jattn_bf16* dout, const void* saved, jattn_bf16* dq, jattn_bf16* dk,
+                                      const jattn_bf16* dout, void* saved, jattn_bf16* dq, jattn_bf16* dk,
                                       jattn_bf16* dv, float* dgq, float* dgk, const int* cu_seqlens, int n_seqs,
                                       int H, int d, void* stream) {
   if (!q || !k || !v || !gq || !gk || !out || !lse || !dout || !saved || !dq || !dk || !dv || !dgq || !dgk)
@@ -728,7 +738,7 @@ extern "C" int jattn_qkv_norm(const jattn_bf16* x_img, const jattn_bf16* w_img, 
 }
 
 extern "C" int jattn_fwd_saved(const jattn_bf16* v, int B, int H, int N_img, int N_txt, int d, jattn_bf16* out,
-                               float* lse, const void* saved, void* stream) {
+                               float* lse, void* saved, void* stream) {
   if (!v || !out || !lse || !saved) return JATTN_ERR_INVALID_ARG;
   Shape s;
   int rc = check_shape(B, H, N_img, N_txt, d, &s);
@@ -749,7 +759,7 @@ extern "C" int jattn_fwd_saved(const jattn_bf16* v, int B, int H, int N_img, int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = dev_err_ptr();
   if (!err) return fail(JATTN_ERR_CUDA, "device error word", cudaGetLastError());
-  const uint8_t* base = static_cast<const uint8_t*>(saved);
+  uint8_t* base = static_cast<uint8_t*>(saved);
   CUtensorMap mq, mk, mv;
   if (!encode_bhnd_map(&mq, base + sl.qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, base + sl.khat, s.BH, s.N, s.d) ||
       !encode_bhnd_map(&mv, v, s.BH, s.N, s.d))
@@ -758,7 +768,8 @@ extern "C" int jattn_fwd_saved(const jattn_bf16* v, int B, int H, int N_img, int
   cudaError_t ce;
   {
     Timed t(JATTN_KERNEL_ATTN_FWD, st);
-    ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st);
+    ce = launch_attn_fwd(mq, mk, mv, as, out, lse, err, st, reinterpret_cast<float*>(base + sl.dq),
+                         reinterpret_cast<uint32_t*>(base + sl.zero_count));
   }
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "attn_fwd launch", ce);
   return JATTN_OK;

@@ -83,22 +83,26 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 // backward stores its first contribution); the first n_tickets words of
 // `tickets` are zeroed.  With qhat null (q_hat, k_hat, rq and rk saved by a
 // training forward) only the statistics, the zeroing and the tickets are
-// done, and q, k, qhat, khat, rq, rk are not accessed.
+// done, and q, k, qhat, khat, rq, rk are not accessed.  With zero_count
+// non-null, the zeroing is skipped when *zero_count == zeroed_by (a training
+// forward's CTAs zeroed the accumulator and counted themselves there).
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,
                             float inv_scale, float* dqacc, unsigned int* tickets, int n_tickets, int BH,
-                            const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st);
+                            const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st,
+                            const uint32_t* zero_count = nullptr, uint32_t zeroed_by = 0);
 // Whether the attention backward takes the statistics as the bf16 chunks
 // above (and a TMA map over them) rather than as fp32 rows.
 inline bool attn_bwd_stats_chunks(int d) { return d == 64; }
 // nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq
 // partials; the last one (by *ticket, zeroed by the backward preparation)
-// sums them and the nk dgk partials into dgq and dgk.
+// sums them and the nk dgk partials into dgq and dgk.  zero_count (or null)
+// is reset to 0: the accumulator it vouched for is no longer zero.
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
                               uint16_t* dq, float* dgq_part, int nparts, int64_t rows, const float* dgk_part, int nk,
                               unsigned int* ticket, float* dgq, float* dgk, int d, uint32_t* dev_err,
-                              cudaStream_t st);
+                              cudaStream_t st, uint32_t* zero_count = nullptr);
 int q_norm_bwd_parts(int d);
 // Streaming multiprocessors of the current device (cached after the first
 // call), or the limit set by set_sm_limit if that is lower: the number of
@@ -116,8 +120,13 @@ struct AttnShape {
   bool deterministic = false;  // backward: fixed dQ accumulation order
 };
 
+// dq_zero / zero_count (training pair, else null): the backward's fp32 dQ
+// accumulator ([BH, rows, d]) to zero, and the word each CTA increments once
+// its share is zeroed (attn_fwd_grid(s) increments in all).
 cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                            const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st);
+                            const AttnShape& s, uint16_t* out, float* lse, uint32_t* dev_err, cudaStream_t st,
+                            float* dq_zero = nullptr, uint32_t* zero_count = nullptr);
+int attn_fwd_grid(const AttnShape& s);
 
 // map_stats: a TMA map over the bf16 statistics chunks (encode_stats_map) and
 // map_dq one over the fp32 dQ accumulator (encode_dq_map) when

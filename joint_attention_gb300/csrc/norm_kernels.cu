@@ -199,6 +199,23 @@ __device__ __forceinline__ void split3_bf16(float x, uint32_t (&h)[3]) {
   }
 }
 
+// Division of n < 2^31 by a fixed d >= 1 through a multiply-high: with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, n / d =
+// (mulhi(n, m) + n) >> l (the round-up method for invariant divisors, as in
+// Hacker's Delight, ch. 10); mulhi(n, m) + n < 2^32 for n < 2^31.
+struct DivU31 {
+  uint32_t m, l;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> l; }
+};
+DivU31 make_div_u31(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t{1} << l) < d) ++l;
+  DivU31 r;
+  r.l = l;
+  r.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
+  return r;
+}
+
 template <int D, bool kNorm>
 __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
@@ -206,9 +223,13 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
     float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, uint4* __restrict__ stats,
     float inv_scale, float4* __restrict__ dqacc, unsigned int* __restrict__ tickets, int n_tickets,
-    const __grid_constant__ SegTable seg, int64_t padded_rows) {
+    const __grid_constant__ SegTable seg, int64_t padded_rows, DivU31 div_prows, const uint32_t* zero_count,
+    uint32_t zeroed_by) {
   griddep_launch_dependents();
   griddep_wait();
+  // The accumulator is already zero when every CTA of the training forward
+  // counted its share.
+  if (dqacc && zero_count && *zero_count == zeroed_by) dqacc = nullptr;
   for (int i = blockIdx.x * kNormThreads + threadIdx.x; i < n_tickets; i += gridDim.x * kNormThreads)
     tickets[i] = 0u;
   constexpr int TPR = D / 8;
@@ -224,10 +245,14 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     uint4 q, k, o, d;
     float lse;
   };
+  // Padded rows number below 2^31 (B H N d < 2^31), so the head index comes
+  // from a 32-bit multiply-high division.
   auto locate = [&](int64_t b, int64_t& prow, int64_t& row, bool& in_range, bool& valid) {
     prow = b + threadIdx.x / TPR;
-    const int64_t bh = prow / seg.prows;
-    const int p = static_cast<int>(prow - bh * seg.prows);
+    in_range = prow < padded_rows;
+    const uint32_t p32 = in_range ? static_cast<uint32_t>(prow) : 0u;
+    const uint32_t bh = div_prows.div(p32);
+    const int p = static_cast<int>(p32 - bh * static_cast<uint32_t>(seg.prows));
     int lo = 0, hi = seg.n;  // seg.pcu[lo] <= p < seg.pcu[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -235,9 +260,8 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
       else hi = mid;
     }
     const int t = seg.cu[lo] + (p - seg.pcu[lo]);
-    in_range = prow < padded_rows;
     valid = in_range && t < seg.cu[lo + 1];
-    row = bh * seg.rows + t;
+    row = static_cast<int64_t>(bh) * seg.rows + t;
   };
   auto load = [&](int64_t b, Row& w) {
     int64_t prow, row;
@@ -326,12 +350,14 @@ __global__ void __launch_bounds__(kQBwdThreads) q_norm_bwd_kernel(const float4* 
                                                                   float* __restrict__ partial, int64_t rows,
                                                                   const float* __restrict__ part_k, int nk,
                                                                   unsigned int* __restrict__ ticket,
-                                                                  float* __restrict__ dgq, float* __restrict__ dgk) {
+                                                                  float* __restrict__ dgq, float* __restrict__ dgk,
+                                                                  uint32_t* zero_count) {
   constexpr int TPR = D / 8;
   constexpr int RPB = kQBwdThreads / TPR;
   const int sub = threadIdx.x % TPR;
   griddep_launch_dependents();
   griddep_wait();
+  if (zero_count && blockIdx.x == 0 && threadIdx.x == 0) *zero_count = 0u;
   float g[8], acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -505,7 +531,8 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
                             uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,
                             float inv_scale, float* dqacc, unsigned int* tickets, int n_tickets, int BH,
-                            const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st) {
+                            const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st,
+                            const uint32_t* zero_count, uint32_t zeroed_by) {
   (void)dev_err;
   const int64_t padded_rows = static_cast<int64_t>(BH) * seg.prows;
   auto u4 = [](const uint16_t* p) { return reinterpret_cast<const uint4*>(p); };
@@ -516,20 +543,21 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
   return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
                     gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
                     rk, nlse2, delta, reinterpret_cast<uint4*>(stats), inv_scale, reinterpret_cast<float4*>(dqacc),
-                    tickets, n_tickets, seg, padded_rows);
+                    tickets, n_tickets, seg, padded_rows, make_div_u31(static_cast<uint32_t>(seg.prows)), zero_count,
+                    zeroed_by);
 }
 
 cudaError_t launch_q_norm_bwd(const float* dqacc, const uint16_t* q, const float* rq, const float* gq, float scale,
                               uint16_t* dq, float* dgq_part, int nparts, int64_t rows, const float* dgk_part, int nk,
                               unsigned int* ticket, float* dgq, float* dgk, int d, uint32_t* dev_err,
-                              cudaStream_t st) {
+                              cudaStream_t st, uint32_t* zero_count) {
   (void)dev_err;
   auto* a = reinterpret_cast<const float4*>(dqacc);
   auto* x = reinterpret_cast<const uint4*>(q);
   auto* y = reinterpret_cast<uint4*>(dq);
   // Every one of the nparts blocks writes its partial (zeros if it has no row).
   return launch_pdl(d == 64 ? q_norm_bwd_kernel<64> : q_norm_bwd_kernel<128>, dim3(nparts), dim3(kQBwdThreads), 0,
-                    st, a, x, rq, gq, scale, y, dgq_part, rows, dgk_part, nk, ticket, dgq, dgk);
+                    st, a, x, rq, gq, scale, y, dgq_part, rows, dgk_part, nk, ticket, dgq, dgk, zero_count);
 }
 
 }  // namespace jattn

@@ -536,6 +536,53 @@ def test_training_pair_varlen_matches_plain_calls(ja, d):
         assert _bitwise_equal(a, b), name
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_training_pair_backward_twice_and_from_a_dirty_buffer(ja, d):
+    """The training forward zeroes the backward's dQ accumulator inside `saved`
+    and counts itself there; a backward that finds no such count (a buffer of
+    stale bytes, or a second backward on the same buffer) zeroes it itself.
+    In the default mode (the accumulator is added into) every backward of the
+    sequence below must match the oracle; a skipped zeroing would add dq̂
+    twice.  The deterministic mode (stores the first contribution) repeats
+    the plain backward bit for bit on the same sequence."""
+    B, H, N, n_txt = 2, 3, 333, 77
+    inp = make_inputs(B, H, N, d, seed=1500 + d)
+    tq, tk, tv, tgq, tgk, tdo = (dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_f32(inp.gq),
+                                 dev_f32(inp.gk), dev_bf16(inp.dout))
+    ref = oracle.joint_attention_bwd(inp.q, inp.k, inp.v, inp.gq, inp.gk, inp.dout)
+    nb = ja.jattn_saved_bytes(B, H, N - n_txt, n_txt, d)
+    names = ("dq", "dk", "dv", "dgq", "dgk")
+
+    def sequence():
+        saved = torch.full((nb,), 0x7F, dtype=torch.uint8, device="cuda")  # stale bytes everywhere
+        out, lse = torch.empty_like(tq), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        runs = []
+        ja.jattn_fwd_train(tq, tk, tv, tgq, tgk, B, H, N - n_txt, n_txt, d, out, lse, saved)
+        runs.append(ja.backward_train(tq, tk, tv, tgq, tgk, out, lse, tdo, saved, n_txt))  # stale count
+        runs.append(ja.backward_train(tq, tk, tv, tgq, tgk, out, lse, tdo, saved, n_txt))  # second backward
+        ja.jattn_fwd_train(tq, tk, tv, tgq, tgk, B, H, N - n_txt, n_txt, d, out, lse, saved)
+        runs.append(ja.backward_train(tq, tk, tv, tgq, tgk, out, lse, tdo, saved, n_txt))  # trusts the forward
+        runs.append(ja.backward_train(tq, tk, tv, tgq, tgk, out, lse, tdo, saved, n_txt))
+        torch.cuda.synchronize()
+        assert ja.jattn_last_device_error() == 0
+        return out, lse, runs
+
+    _, _, runs = sequence()
+    for i, r in enumerate(runs):
+        check_bwd({n: np64(t) for n, t in zip(names, r)}, ref, where=f"default mode, backward {i}, d={d}")
+    ja.jattn_set_deterministic(True)
+    try:
+        out0, lse0 = ja.forward(tq, tk, tv, tgq, tgk, n_txt)
+        g0 = ja.backward(tq, tk, tv, tgq, tgk, out0, lse0, tdo, n_txt)
+        out1, lse1, runs = sequence()
+    finally:
+        ja.jattn_set_deterministic(False)
+    assert _bitwise_equal(out0, out1) and _bitwise_equal(lse0, lse1)
+    for r in runs:
+        for name, a, b in zip(names, g0, r):
+            assert _bitwise_equal(a, b), name
+
+
 def test_training_pair_argument_checks(ja):
     B, H, N, d = 1, 2, 200, 64
     inp = make_inputs(B, H, N, d, seed=1400)
