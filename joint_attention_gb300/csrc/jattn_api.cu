@@ -258,11 +258,15 @@ void make_uniform_seg_table(SegTable* t, int N) {
 }
 
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  return encode_bhnd_map_rows(map, base, BH, N, d, 128);
+}
+
+bool encode_bhnd_map_rows(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -728,10 +732,14 @@ extern "C" int jattn_qkv_norm(const jattn_bf16* x_img, const jattn_bf16* w_img, 
   for (int i = 0; i < 2; ++i)
     if (!encode_rows_map(&maps[2 * i], xs[i], ms[i], C, 128) || !encode_rows_map(&maps[2 * i + 1], ws[i], ycols, C, 256))
       return fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
+  CUtensorMap out_maps[5];
+  const void* outs_p[5] = {q, k, v, a.hat[0], a.hat[1]};
+  for (int i = 0; i < 5; ++i)
+    if (!encode_bhnd_map_rows(&out_maps[i], outs_p[i], s.BH, s.N, d, 32)) return fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   cudaError_t ce;
   {
     Timed t(JATTN_KERNEL_QKV_NORM, st);
-    ce = launch_qkv_norm(maps, a, err, st);
+    ce = launch_qkv_norm(maps, out_maps, a, err, st);
   }
   if (ce != cudaSuccess) return fail(JATTN_ERR_CUDA, "qkv_norm launch", ce);
   return JATTN_OK;

@@ -164,7 +164,9 @@ struct QkvLaunch {
   uint16_t* hat[2];  // q_hat, k_hat
   float* r[2];       // rq, rk
 };
-cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const QkvLaunch& a, uint32_t* dev_err, cudaStream_t st);
+// out_maps: q, k, v, q_hat, k_hat as encode_bhnd_map_rows(..., 32) maps.
+cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const CUtensorMap (&out_maps)[5], const QkvLaunch& a,
+                            uint32_t* dev_err, cudaStream_t st);
 // A 2-D TMA map over a row-major [rows, cols] bf16 matrix with a
 // (64, box_rows) box and 128-byte swizzle (cols * 2 a multiple of 16).
 bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
@@ -172,6 +174,8 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 // Encodes a 3-D TMA map over a [BH, N, d] bf16 tensor with a (64, 128, 1)
 // box and 128-byte swizzle.  Returns false if the driver rejects it.
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+// The same with a (64, box_rows, 1) box.
+bool encode_bhnd_map_rows(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 // A 3-D TMA map over [BH, prows, 16] bf16 statistics chunks with a
 // (16, 128, 1) box and 32-byte swizzle.
 bool encode_stats_map(CUtensorMap* map, const void* base, int BH, int prows);

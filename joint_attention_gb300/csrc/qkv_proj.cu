@@ -251,6 +251,20 @@ struct QkvParams {
   float* r[2];        // rq, rk: [B, H, N]
 };
 
+// TMA maps over the five outputs ([B H, N, d] bf16, box 64 columns x 32 rows,
+// 128-byte swizzle: the staging buffers' layout), for warps whose 32 rows lie
+// in one batch item.
+struct QkvOutMaps {
+  CUtensorMap out[3];  // q, k, v
+  CUtensorMap hat[2];  // q_hat, k_hat
+};
+__device__ __forceinline__ void tma_store_3d_s(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Field selection by a runtime index through selects: indexing the kernel's
 // parameter arrays with a runtime value would copy them to local memory.
 __device__ __forceinline__ uint16_t* out_of(const QkvParams& p, int which) {
@@ -258,6 +272,40 @@ __device__ __forceinline__ uint16_t* out_of(const QkvParams& p, int which) {
 }
 __device__ __forceinline__ uint16_t* hat_of(const QkvParams& p, int which) { return which == 0 ? p.hat[0] : p.hat[1]; }
 __device__ __forceinline__ float* r_of(const QkvParams& p, int which) { return which == 0 ? p.r[0] : p.r[1]; }
+__device__ __forceinline__ const CUtensorMap* out_map(const QkvOutMaps& m, int which) {
+  return which == 0 ? &m.out[0] : which == 1 ? &m.out[1] : &m.out[2];
+}
+__device__ __forceinline__ const CUtensorMap* hat_map(const QkvOutMaps& m, int which) {
+  return which == 0 ? &m.hat[0] : &m.hat[1];
+}
+
+// Where a warp's 32 staged rows go: one TMA tile store when they are 32
+// consecutive rows of one head (contig; n0 and bh0 = b H of the first row),
+// else the row-by-row stores of store_rows.
+struct RowsOut {
+  bool contig;
+  int n0, bh0;
+};
+template <int D>
+__device__ __forceinline__ void emit_rows(uint32_t buf, const CUtensorMap* map, uint16_t* base, const RowsOut& ro,
+                                          const uint32_t (&rows)[8], uint32_t head_rows, int h, int col, int lane) {
+  if (ro.contig) {
+    fence_proxy_async_smem();  // this lane's staged writes, to the TMA unit
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d_s(map, buf, col, ro.n0, ro.bh0 + h);
+      bulk_commit_group();
+    }
+  } else {
+    __syncwarp();
+    store_rows<D>(buf, base, rows, head_rows, col, lane);
+  }
+}
+// Before a staging buffer is written again: the TMA stores have read it.
+__device__ __forceinline__ void staging_free(int lane) {
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
+}
 __device__ __forceinline__ QkvStream stream_of(const QkvParams& p, int si) {
   QkvStream s;
   s.M = si ? p.s[1].M : p.s[0].M;
@@ -324,11 +372,13 @@ __device__ __forceinline__ void stage_hat_row(uint32_t buf, const uint32_t* y, u
 // head's is row + h N.  bias: this head's D bias values in shared memory.
 template <int D>
 __device__ __forceinline__ void qkv_emit_head(uint32_t taddr, int ocol, bool live, size_t row,
-                                              const uint32_t (&rows)[8], uint32_t stg, uint32_t bias,
-                                              const QkvParams& p, const QkvBars& bars, int lane) {
+                                              const uint32_t (&rows)[8], const RowsOut& ro, uint32_t stg,
+                                              uint32_t bias, const QkvParams& p, const QkvOutMaps& om,
+                                              const QkvBars& bars, int lane) {
   const int hd = p.H * D;
   const int which = ocol / hd;  // 0 q, 1 k, 2 v
-  const uint32_t head_rows = static_cast<uint32_t>((ocol - which * hd) / D) * static_cast<uint32_t>(p.N);
+  const int h = (ocol - which * hd) / D;
+  const uint32_t head_rows = static_cast<uint32_t>(h) * static_cast<uint32_t>(p.N);
   const size_t hrow = row + head_rows;
   const uint32_t raw = stg;
   // Y = bf16(acc + bias), 32 columns at a time (packed pairs).
@@ -348,10 +398,10 @@ __device__ __forceinline__ void qkv_emit_head(uint32_t taddr, int ocol, bool liv
   const float* g = which == 0 ? bars.gq : bars.gk;
   if constexpr (D == 64) {
     const uint32_t hat = raw + kStagingBytes;
+    staging_free(lane);
     stage_row(raw, yb, lane);
     if (which == 2) {
-      __syncwarp();
-      store_rows<D>(raw, out_of(p, which), rows, head_rows, 0, lane);
+      emit_rows<D>(raw, out_map(om, which), out_of(p, which), ro, rows, head_rows, h, 0, lane);
       __syncwarp();
       return;
     }
@@ -364,17 +414,17 @@ __device__ __forceinline__ void qkv_emit_head(uint32_t taddr, int ocol, bool liv
       fix_staged_rows(todo, raw, hat, r, g, lane);
       __syncwarp();
     }
-    store_rows<D>(raw, out_of(p, which), rows, head_rows, 0, lane);
-    store_rows<D>(hat, hat_of(p, which), rows, head_rows, 0, lane);
+    emit_rows<D>(raw, out_map(om, which), out_of(p, which), ro, rows, head_rows, h, 0, lane);
+    emit_rows<D>(hat, hat_map(om, which), hat_of(p, which), ro, rows, head_rows, h, 0, lane);
     if (live) r_of(p, which)[hrow] = r;
     __syncwarp();
   } else {
     // d = 128: each 64-column half through the raw staging buffer.
 #pragma unroll
     for (int h64 = 0; h64 < 2; ++h64) {
+      staging_free(lane);
       stage_row(raw, yb + h64 * 32, lane);
-      __syncwarp();
-      store_rows<D>(raw, out_of(p, which), rows, head_rows, h64 * 64, lane);
+      emit_rows<D>(raw, out_map(om, which), out_of(p, which), ro, rows, head_rows, h, h64 * 64, lane);
       __syncwarp();
     }
     if (which == 2) return;
@@ -382,11 +432,14 @@ __device__ __forceinline__ void qkv_emit_head(uint32_t taddr, int ocol, bool liv
     bool near = false;
 #pragma unroll
     for (int h64 = 0; h64 < 2; ++h64) {
+      staging_free(lane);
       stage_hat_row(raw, yb + h64 * 32, smem_u32(g + h64 * 64), r, near, lane);
-      __syncwarp();
-      store_rows<D>(raw, hat_of(p, which), rows, head_rows, h64 * 64, lane);
+      emit_rows<D>(raw, hat_map(om, which), hat_of(p, which), ro, rows, head_rows, h, h64 * 64, lane);
       __syncwarp();
     }
+    // The row re-rounding below stores over these rows: the tile stores first.
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
     if (live) r_of(p, which)[hrow] = r;
     const unsigned todo = __ballot_sync(0xffffffffu, near && live);
     if (todo) fix_stored_rows(todo, *reinterpret_cast<const uint32_t(*)[64]>(yb), r, hrow, hat_of(p, which), g, lane);
@@ -397,8 +450,8 @@ template <int D>
 __global__ void __launch_bounds__(QkvCfg<D>::kThreads, 1)
     qkv_norm_kernel(const __grid_constant__ CUtensorMap map_x0, const __grid_constant__ CUtensorMap map_w0,
                     const __grid_constant__ CUtensorMap map_x1, const __grid_constant__ CUtensorMap map_w1,
-                    const __grid_constant__ QkvParams p, const float* __restrict__ gq, const float* __restrict__ gk,
-                    uint32_t* dev_err) {
+                    const __grid_constant__ QkvOutMaps om, const __grid_constant__ QkvParams p,
+                    const float* __restrict__ gq, const float* __restrict__ gk, uint32_t* dev_err) {
   using Cfg = QkvCfg<D>;
   constexpr int kWarpProd = Cfg::kWarpProd, kWarpIssue = Cfg::kWarpIssue;
   extern __shared__ uint8_t smem_raw[];
@@ -528,16 +581,24 @@ __global__ void __launch_bounds__(QkvCfg<D>::kThreads, 1)
       uint32_t rows[8];  // the rows this lane writes out in store_rows
 #pragma unroll
       for (int j = 0; j < 8; ++j) rows[j] = __shfl_sync(0xffffffffu, row32, 4 * j + (lane >> 3));
+      RowsOut ro;
+      {
+        const uint32_t first = __shfl_sync(0xffffffffu, row32, 0), last = __shfl_sync(0xffffffffu, row32, 31);
+        ro.contig = first != kDeadRow && last != kDeadRow && last - first == 31u;
+        ro.n0 = __shfl_sync(0xffffffffu, n, 0);
+        ro.bh0 = __shfl_sync(0xffffffffu, bi, 0) * p.H;
+      }
 #pragma unroll
       for (int j = 0; j < 128 / D; ++j) {
         const int ocol = col0 + j * D;  // the head's first column in Y
         if (ocol < hd3)
-          qkv_emit_head<D>(tmem + lane_base + abuf * kBN + wcol + j * D, ocol, live, row, rows, stg,
-                           bias_w + j * D * 4, p, bars, lane);
+          qkv_emit_head<D>(tmem + lane_base + abuf * kBN + wcol + j * D, ocol, live, row, rows, ro, stg,
+                           bias_w + j * D * 4, p, om, bars, lane);
       }
       tc_fence_before();
       mbar_arrive(&bars.acc_empty[abuf]);
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's tile stores are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -549,7 +610,11 @@ __global__ void __launch_bounds__(QkvCfg<D>::kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const QkvLaunch& a, uint32_t* dev_err, cudaStream_t st) {
+cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const CUtensorMap (&out_maps)[5], const QkvLaunch& a,
+                            uint32_t* dev_err, cudaStream_t st) {
+  QkvOutMaps om;
+  for (int i = 0; i < 3; ++i) om.out[i] = out_maps[i];
+  for (int i = 0; i < 2; ++i) om.hat[i] = out_maps[3 + i];
   QkvParams p;
   p.H = a.H;
   p.C = a.C;
@@ -576,7 +641,7 @@ cudaError_t launch_qkv_norm(const CUtensorMap (&maps)[4], const QkvLaunch& a, ui
   auto go = [&](auto kernel, int threads, int smem) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kernel, dim3(grid), dim3(threads), smem, st, maps[0], maps[1], maps[2], maps[3], p, a.gq,
+    return launch_pdl(kernel, dim3(grid), dim3(threads), smem, st, maps[0], maps[1], maps[2], maps[3], om, p, a.gq,
                       a.gk, dev_err);
   };
   if (a.d == 64) return go(qkv_norm_kernel<64>, QkvCfg<64>::kThreads, QkvCfg<64>::kDynSmem);
