@@ -69,15 +69,20 @@ namespace {
 constexpr int kBwdThreads = 640;  // 5 warpgroups
 // Warp roles: 0-7 compute (two groups), 8-11 dQ drain, 12-15 epilogue
 // (d = 64), 16 TMA, 17-19 MMA issuers.  Registers per thread (setmaxnreg):
-// compute 120, drain 88, epilogue 104, TMA / issuers 48 (d = 128: compute 128
-// and 72 for all others); 256 x 120 + 128 x (88 + 104 + 48) = 61440, the
-// 640 x 96 the block launches with (d = 128: 256 x 128 + 384 x 72 = 60416).
+// d = 64: compute 120, drain 88, epilogue 104, TMA / issuers 48;
+// 256 x 120 + 128 x (88 + 104 + 48) = 61440, the 640 x 96 the block launches
+// with (112 / 88 / 112 / 56 spills nothing but runs slower: the compute
+// warps want the registers).  d = 128: compute 128, drain + epilogue 88, the
+// idle warps 12-15 24, TMA / issuer 96 (their launch count, no setmaxnreg);
+// 256 x 128 + 128 x (88 + 24 + 96) = 59392.  The d = 128 kernel spills
+// nothing at these counts (at 72 for every other role it spilled 52-76
+// bytes, the issuers' share of it).
 // setmaxnreg budgets.  An increase must not be below, a decrease not above,
 // the count the kernel launches with, and the sum must fit the launch's
 // registers (640 x that count); the launcher checks both against the
 // compiled kernel before every launch.
 constexpr int kRegCompute64 = 120, kRegDrain64 = 88, kRegEpi64 = 104, kRegMma64 = 48;
-constexpr int kRegCompute128 = 128, kRegOther128 = 72;
+constexpr int kRegCompute128 = 128, kRegDrain128 = 88, kRegIdle128 = 24, kRegMma128 = 96;
 // The split uses the whole launch allocation (640 x 96): the kernel must launch
 // with exactly 96 registers per thread.
 constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
@@ -89,13 +94,14 @@ constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
 constexpr int kSubPartRegs = 5 * 32 * kRegLaunchMin;
 static_assert(32 * (2 * kRegCompute64 + kRegDrain64 + kRegEpi64 + kRegMma64) <= kSubPartRegs,
               "d = 64 register split exceeds a sub-partition's launch allocation");
-static_assert(32 * (2 * kRegCompute128 + 3 * kRegOther128) <= kSubPartRegs,
+static_assert(32 * (2 * kRegCompute128 + kRegDrain128 + kRegIdle128 + kRegMma128) <= kSubPartRegs,
               "d = 128 register split exceeds a sub-partition's launch allocation");
 static_assert(256 * kRegCompute64 + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) <= kBwdThreads * kRegLaunchMin,
               "d = 64 register split exceeds the launch allocation");
-static_assert(256 * kRegCompute128 + 384 * kRegOther128 <= kBwdThreads * kRegLaunchMin,
+static_assert(256 * kRegCompute128 + 128 * (kRegDrain128 + kRegIdle128 + kRegMma128) <= kBwdThreads * kRegLaunchMin,
               "d = 128 register split exceeds the launch allocation");
-static_assert(kRegEpi64 >= kRegLaunchMax && kRegMma64 <= kRegLaunchMin && kRegOther128 <= kRegLaunchMin &&
+static_assert(kRegEpi64 >= kRegLaunchMax && kRegMma64 <= kRegLaunchMin && kRegDrain128 <= kRegLaunchMin && kRegIdle128 <= kRegLaunchMin &&
+                  kRegMma128 <= kRegLaunchMin &&
                   kRegDrain64 <= kRegLaunchMin && kRegCompute64 >= kRegLaunchMax && kRegCompute128 >= kRegLaunchMax,
               "setmaxnreg direction");
 constexpr int kWarpEpi = 12;
@@ -1454,9 +1460,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if constexpr (D == 64) {
       if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain64>();
       else if (warp < kWarpTma) setmaxnreg_inc<kRegEpi64>();
-      else if (warp >= kWarpTma) setmaxnreg_dec<kRegMma64>();
-    } else {  // d = 128: the drain warps run the epilogue; one issuer
-      setmaxnreg_dec<kRegOther128>();
+      else setmaxnreg_dec<kRegMma64>();
+    } else {  // the TMA / issuer warps keep their launch count
+      static_assert(kRegMma128 == kRegLaunchMin, "d = 128: the TMA / issuer warps keep their launch count");
+      if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain128>();
+      else if (warp < kWarpTma) setmaxnreg_dec<kRegIdle128>();
     }
     if (warp < kWarpEpi) {
       if constexpr (D == 64) bwd_drain64<D, kOrd>(sm, bars, tmem, w, &map_dq, counters, dev_err);
