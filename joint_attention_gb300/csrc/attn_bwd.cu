@@ -72,17 +72,16 @@ constexpr int kBwdThreads = 640;  // 5 warpgroups
 // d = 64: compute 120, drain 88, epilogue 104, TMA / issuers 48;
 // 256 x 120 + 128 x (88 + 104 + 48) = 61440, the 640 x 96 the block launches
 // with (112 / 88 / 112 / 56 spills nothing but runs slower: the compute
-// warps want the registers).  d = 128: compute 128, drain + epilogue 88, the
-// idle warps 12-15 24, TMA / issuer 96 (their launch count, no setmaxnreg);
-// 256 x 128 + 128 x (88 + 24 + 96) = 59392.  The d = 128 kernel spills
-// nothing at these counts (at 72 for every other role it spilled 52-76
-// bytes, the issuers' share of it).
+// warps want the registers).  d = 128: compute 128, drain + epilogue 104,
+// the idle warps 12-15 24, TMA / issuer 96 (their launch count, no
+// setmaxnreg); 256 x 128 + 128 x (104 + 24 + 96) = 61440.  The issuers spill
+// below 96.
 // setmaxnreg budgets.  An increase must not be below, a decrease not above,
 // the count the kernel launches with, and the sum must fit the launch's
 // registers (640 x that count); the launcher checks both against the
 // compiled kernel before every launch.
 constexpr int kRegCompute64 = 120, kRegDrain64 = 88, kRegEpi64 = 104, kRegMma64 = 48;
-constexpr int kRegCompute128 = 128, kRegDrain128 = 88, kRegIdle128 = 24, kRegMma128 = 96;
+constexpr int kRegCompute128 = 128, kRegDrain128 = 104, kRegIdle128 = 24, kRegMma128 = 96;
 // The split uses the whole launch allocation (640 x 96): the kernel must launch
 // with exactly 96 registers per thread.
 constexpr int kRegLaunchMin = 96, kRegLaunchMax = 96;
@@ -100,7 +99,7 @@ static_assert(256 * kRegCompute64 + 128 * (kRegDrain64 + kRegEpi64 + kRegMma64) 
               "d = 64 register split exceeds the launch allocation");
 static_assert(256 * kRegCompute128 + 128 * (kRegDrain128 + kRegIdle128 + kRegMma128) <= kBwdThreads * kRegLaunchMin,
               "d = 128 register split exceeds the launch allocation");
-static_assert(kRegEpi64 >= kRegLaunchMax && kRegMma64 <= kRegLaunchMin && kRegDrain128 <= kRegLaunchMin && kRegIdle128 <= kRegLaunchMin &&
+static_assert(kRegEpi64 >= kRegLaunchMax && kRegMma64 <= kRegLaunchMin && kRegDrain128 >= kRegLaunchMax && kRegIdle128 <= kRegLaunchMin &&
                   kRegMma128 <= kRegLaunchMin &&
                   kRegDrain64 <= kRegLaunchMin && kRegCompute64 >= kRegLaunchMax && kRegCompute128 >= kRegLaunchMax,
               "setmaxnreg direction");
@@ -134,13 +133,10 @@ struct BwdCfg {
   // The constant A chunks repeat one 8-row atom (256 bytes) with a zero atom
   // stride, so each takes 256 bytes.
   static constexpr int kConstAtom = 256;
-  // dQ: d = 64 stages the tile in two 128 x 32 fp32 halves (128-byte rows,
-  // 128-byte swizzle), each reduced into the accumulator by one TMA tensor
-  // reduce; d = 128 stages 32 columns per pass in padded rows, reduced row
-  // by row.
-  static constexpr int kDQCols = 32;                          // dQ columns staged per pass
-  static constexpr int kDQRowBytes = kDQCols * 4 + 16;        // d = 128 padded staging row
-  static constexpr int kDQStageBytes = (D == 64) ? 2 * 128 * 128 : 128 * kDQRowBytes;
+  // dQ staging: 128 x 32 fp32 tiles (128-byte rows, 128-byte swizzle), each
+  // reduced into the accumulator by one TMA tensor reduce; d = 64 has two of
+  // its own, d = 128 one (two more lie over the dS^T tile).
+  static constexpr int kDQStageBytes = (D == 64) ? 2 * 128 * 128 : 128 * 128;
   static constexpr int kOffKV = 0;                            // + buf * 2 * kTile: K, then V
   static constexpr int kOffQ = kKVBufs * 2 * kTile;           // + stage * kTile
   static constexpr int kOffDO = kOffQ + kQStages * kTile;     // + stage * kTile
@@ -271,14 +267,13 @@ struct BwdBars {
   uint64_t s_free;
   uint64_t dv_done;
   uint64_t epi;
-  uint64_t drain_sync;  // d = 64: the dQ drain threads' staging handshakes
+  uint64_t drain_sync;  // the dQ drain threads' staging handshakes
   uint64_t kraw_full;   // d = 64: the unit's raw k tile has landed (epilogue)
   uint64_t drain[3];
   uint32_t tmem_base;
   int abort;
-  uint32_t dq_join[2];  // ordered dQ: drain threads whose contribution is complete (by parity)
   __align__(16) float gk[128];  // K-RMSNorm gain (d entries)
-  __align__(16) float wsum[4][64];  // d = 64 epilogue: per-warp dgk column sums
+  __align__(16) float wsum[4][128];  // unit epilogue: per-warp dgk column sums
   float dgk_cta[128];               // this CTA's dgk partial, summed over its units in unit order
 };
 
@@ -784,13 +779,6 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
   }
 }
 
-// Shared-memory fetch-and-add with acquire-release semantics at CTA scope.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_cta_shared(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
-  return old;
-}
-
 // d = 64, warps 8-11 (one thread per query row): per query tile, dQ_t out of
 // TMEM into registers and its columns released, then into the two staging
 // halves (columns 0-31 and 32-63, 128-byte rows with 16-byte chunks XOR-ed
@@ -907,53 +895,80 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
   }
 }
 
-// d = 128, warps 8-11.  Per query tile: dQ_t from TMEM into a padded
-// shared-memory row (one thread per query row), 32 columns per pass, then a
-// bulk fp32 reduce-add (ordered modes: the first contribution a bulk store)
-// of the row into the global accumulator.  Per unit, once its accumulators
-// are final (one thread per key row):
+// d = 128, warps 8-11 (one thread per query row, then per key row).
+// Per query tile: dQ_t out of TMEM in four 32-column quarters, staged as
+// 128 x 32 fp32 tiles with the 128-byte swizzle (16-byte chunk c of row r at
+// c ^ (r % 8), so that the row-per-thread writes are free of bank conflicts)
+// and added into the fp32 accumulator by TMA tensor reduces issued by
+// thread 0.  One staging tile (H0) is the drain's own; two more (H1, H2) lie
+// over the dS^T tile, which dK(t) and dQ(t) are done with once dQ(t) is
+// complete and which the compute groups rewrite only after the reduces have
+// read it (their ds_free wait also counts thread 0's arrival); the fourth
+// quarter waits in registers until H0 has been read again.  All four quarters are
+// out of TMEM before dq_free, so that dP(t+1), which lands in those columns,
+// never waits for the reduces.  Rows past the tensor's end are clipped by
+// the TMA unit; rows of the tile that belong to the next segment receive
+// exact zeros (their probabilities are 0).
+// Ordered modes, as in bwd_drain64: thread 0 waits, before the tile's first
+// reduce, until the contributions of lower rank to the query tile are
+// complete (its counter), and announces its own once it is complete (at the
+// next tile, or at once for a unit's last); in the [B, H, N, d] layout the
+// rank-0 contribution is a TMA store.
+// Per unit, once its accumulators are final (one thread per key row):
 //   dv = bf16(dV acc);
 //   dk_hat = scale * dK acc; u = g * dk_hat; dk = r u - (r^3/d) k sum(u k);
-//   dgk partial = column sums over the tile's rows of dk_hat * k * r, in a
-//   fixed order, summed through the staging rows.
+//   dgk partial = column sums over the tile's rows of dk_hat * k * r: a
+//   fixed-order reduce-scatter within each warp, then a fixed-order sum of
+//   the four warps.
 template <int D, bool kOrd, class W>
-__device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, float scale,
-                                   float* __restrict__ dqacc, uint32_t* __restrict__ counters,
-                                   const __nv_bfloat16* __restrict__ k_raw,
-                                   const float* __restrict__ rk, __nv_bfloat16* __restrict__ dk,
-                                   __nv_bfloat16* __restrict__ dv, float* __restrict__ dgk_part,
-                                   uint32_t* dev_err) {
+__device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, float scale,
+                             const CUtensorMap* mdq, uint32_t* __restrict__ counters,
+                             const __nv_bfloat16* __restrict__ k_raw, const float* __restrict__ rk,
+                             __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                             float* __restrict__ dgk_part, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   static_assert(D == 128, "the d = 64 drain is bwd_drain64");
-  constexpr int kRowFloats = C::kDQRowBytes / 4;
+  constexpr bool kFirstStore = kOrd && std::is_same<W, BwdWorkUniform>::value;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int r128 = (warp & 3) * 32 + lane;  // TMEM lane: query row (dQ) or key row (dV, dK)
+  const bool leader = r128 == 0;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tQ = tmem + lane_base + C::kColDQ;
   const uint32_t tDK = tmem + lane_base + C::kColDK;
-  uint8_t* srow = sm + C::kOffDQ + r128 * C::kDQRowBytes;
-  const uint32_t srow_a = smem_u32(srow);
-  const float* red = reinterpret_cast<const float*>(sm + C::kOffDQ);
+  uint8_t* h0 = sm + C::kOffDQ;
+  uint8_t* h1 = sm + C::kOffDS;
+  uint8_t* h2 = sm + C::kOffDS + 16384;
+  const uint32_t rowoff = static_cast<uint32_t>(r128 * 128);
+  const uint32_t swz = static_cast<uint32_t>(r128 & 7);
+  auto stage32 = [&](uint8_t* tile, const uint32_t (&a)[32]) {
+    const uint32_t base = smem_u32(tile) + rowoff;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      st_shared_v4(base + ((static_cast<uint32_t>(c) ^ swz) << 4), a[4 * c], a[4 * c + 1], a[4 * c + 2],
+                   a[4 * c + 3]);
+  };
   volatile int* ab = &bars.abort;
-  uint32_t epi_uses = 0;
-  // Bounded barrier among the 128 drain threads.
+  if (leader) tma_prefetch_desc(mdq);
+  uint32_t uses = 0, epi_uses = 0;
+  // Bounded barriers among the 128 drain threads.
+  auto drain_sync = [&]() -> bool {
+    mbar_arrive(&bars.drain_sync);
+    const bool okb = mbar_wait(&bars.drain_sync, (uses++) & 1, ab, dev_err);
+    return __all_sync(0xffffffffu, okb) && !*ab;
+  };
   auto epi_sync = [&]() -> bool {
     mbar_arrive(&bars.epi);
     const bool okb = mbar_wait(&bars.epi, (epi_uses++) & 1, ab, dev_err);
     return __all_sync(0xffffffffu, okb);
   };
-  // Ordered modes: the previous contribution, once this thread's row of it
-  // is complete; the last of the 128 threads announces it (release increment
-  // of its query tile's counter).
+  // Thread 0, ordered modes: the counter to announce on once its
+  // contribution is complete.
   uint32_t* pend = nullptr;
-  uint32_t joins = 0;  // contributions joined so far (selects the parity counter)
   auto complete_previous = [&]() {
     if (!pend) return;
     bulk_wait_group0();
     fence_proxy_async_global();
-    const uint32_t old = atom_add_acq_rel_cta_shared(&bars.dq_join[joins & 1], 1u);
-    if ((old & 127u) == 127u) red_release_gpu_add(pend, 1u);
-    ++joins;
+    red_release_gpu_add(pend, 1u);
     pend = nullptr;
   };
   bool ok = true;
@@ -963,70 +978,75 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
   for (int u = blockIdx.x, ui = 0; ok && u < w.units; u += gridDim.x, ++ui) {
     const BwdUnit un = w.unit(u);
     const int bh = un.bh;
-    const int n = un.kv0() + r128;  // key row of this thread in the epilogue
-    const bool key_live = n < un.end;
-    const size_t row_off = (static_cast<size_t>(bh) * rows + (key_live ? n : 0)) * D;
     const int t0 = tb;
     tb += un.nkt;
-    constexpr bool ordered = kOrd;
-
     for (int i = 0; i < un.nkt; ++i) {
       const int t = t0 + i;
       const int qt = un.query_tile(i), rank = un.rank(i);
       uint32_t* cnt = counters + static_cast<size_t>(bh) * tiles_per_head + un.prow0 / 128 + qt;
-      // Ordered modes: the counter is read ahead (its latency overlaps the
-      // wait for dQ); the first contribution is a plain store.
-      const uint32_t seen = ordered && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
-      const bool store = ordered && rank == 0;
+      // Ordered modes: the counter read ahead (its latency overlaps the wait for dQ).
+      const uint32_t seen = kOrd && leader && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
+      const bool store = kFirstStore && rank == 0;
+      const int row = un.row0 + qt * 128;
+      // H0 is free once the previous tile's last reduce has read it.
+      if (leader) bulk_wait_group_read0();
+      if (!(ok = drain_sync())) break;
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      const int qrow = un.row0 + qt * 128 + r128;
-      const bool q_live = qrow < un.end;
-      float* grow = dqacc + (static_cast<size_t>(bh) * rows + (q_live ? qrow : 0)) * D;
-      // Ordered modes: every row of the previous contribution complete and
-      // announced, then this query tile's lower ranks awaited.
-      auto in_order = [&]() -> bool {
-        if constexpr (!ordered) return true;
-        complete_previous();
-        bool oko = true;
-        if (rank > 0 && seen < static_cast<uint32_t>(rank)) oko = gwait_geq(cnt, static_cast<uint32_t>(rank), ab, dev_err);
-        fence_proxy_async_global();
-        return __all_sync(0xffffffffu, oko);
-      };
-      {
-        ok = in_order();
-        if (!ok) break;
-#pragma unroll
-        for (int pass = 0; pass < D / C::kDQCols; ++pass) {
-          bulk_wait_group_read0();  // the previous reduce has finished reading the row
-#pragma unroll
-          for (int c = 0; c < C::kDQCols / 32; ++c) {
-            uint32_t a[32];
-            tmem_ld32(tQ + pass * C::kDQCols + c * 32, a);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              st_shared_v4(srow_a + (c * 32 + q * 4) * 4, a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-          }
-          if (pass == D / C::kDQCols - 1) {
-            tc_fence_before();
-            mbar_arrive(&bars.dq_free);
-          }
-          fence_proxy_async_smem();
-          if (q_live) {
-            if (store) bulk_store(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
-            else bulk_reduce_add_f32(grow + pass * C::kDQCols, srow, C::kDQCols * 4);
-            bulk_commit_group();
-          }
+      // Columns 0-31 into H0, 32-95 into H1 / H2 (the dS^T tile, free once
+      // dQ(t) is done), 96-127 into registers; then dQ's columns are free.
+      uint32_t a[32];
+      tmem_ld32(tQ, a);
+      tmem_wait_ld();
+      stage32(h0, a);
+      tmem_ld32(tQ + 32, a);
+      tmem_wait_ld();
+      stage32(h1, a);
+      tmem_ld32(tQ + 64, a);
+      tmem_wait_ld();
+      stage32(h2, a);
+      uint32_t b[32];
+      tmem_ld32(tQ + 96, b);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.dq_free);
+      fence_proxy_async_smem();
+      if constexpr (kOrd) {
+        if (leader) {
+          complete_previous();
+          if (rank > 0 && seen < static_cast<uint32_t>(rank)) gwait_geq(cnt, static_cast<uint32_t>(rank), ab, dev_err);
+          fence_proxy_async_global();  // the lower ranks' sums before this tile's reduces
         }
       }
-      // A contribution after which others wait is announced at the next
-      // query tile, or at once if it is the unit's last (ascending order).
-      if constexpr (ordered) {
-        if (rank != un.nkt - 1) {
-          pend = cnt;
-          if (i == un.nkt - 1) complete_previous();
+      if (!(ok = drain_sync())) break;
+      if (leader) {
+        if (store) {
+          tma_store_3d(mdq, h0, 0, row, bh);
+          tma_store_3d(mdq, h1, 32, row, bh);
+          tma_store_3d(mdq, h2, 64, row, bh);
+        } else {
+          tma_reduce_add_3d(mdq, h0, 0, row, bh);
+          tma_reduce_add_3d(mdq, h1, 32, row, bh);
+          tma_reduce_add_3d(mdq, h2, 64, row, bh);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();        // H0, H1 and H2 have been read
+        mbar_arrive(&bars.ds_free[0]);  // the compute groups may rewrite the dS^T tile
+      }
+      if (!(ok = drain_sync())) break;
+      stage32(h0, b);
+      fence_proxy_async_smem();
+      if (!(ok = drain_sync())) break;
+      if (leader) {
+        if (store) tma_store_3d(mdq, h0, 96, row, bh);
+        else tma_reduce_add_3d(mdq, h0, 96, row, bh);
+        bulk_commit_group();
+        if constexpr (kOrd) {
+          if (rank != un.nkt - 1) {
+            pend = cnt;
+            if (i == un.nkt - 1) complete_previous();
+          }
         }
       }
     }
@@ -1036,125 +1056,113 @@ __device__ void bwd_drain_epilogue(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
     ok = mbar_wait(&bars.acc_full, ui & 1, ab, dev_err);
     if (!(ok = __all_sync(0xffffffffu, ok))) break;
     tc_fence_after();
+    const int n = un.kv0() + r128;  // key row of this thread
+    const bool key_live = n < un.end;
+    const size_t row_off = (static_cast<size_t>(bh) * rows + (key_live ? n : 0)) * D;
     const float r = key_live ? rk[static_cast<size_t>(bh) * rows + n] : 0.f;
-    {
-      // Per-row accesses; two passes over the TMEM dK accumulator (dot, then
-      // outputs), the dgk rows staged kDQCols columns at a time.
-      const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
-      uint4* dvrow = reinterpret_cast<uint4*>(dv + row_off);
-      uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
+    const uint4* krow = reinterpret_cast<const uint4*>(k_raw + row_off);
+    uint4* dvrow = reinterpret_cast<uint4*>(dv + row_off);
+    uint4* dkrow = reinterpret_cast<uint4*>(dk + row_off);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
-        tmem_wait_ld();
-        if (c == D / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(&bars.acc_free_v);
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tmem + lane_base + C::kColDV + c * 32, a);
+      tmem_wait_ld();
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        mbar_arrive(&bars.acc_free_v);
+      }
+      if (key_live) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
+          o.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
+          o.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
+          o.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
+          dvrow[c * 4 + q] = o;
+        }
+      }
+    }
+    // Pass 1 over the dK accumulator: dot = sum_c g_c dk_hat_c k_c.
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tDK + c * 32, a);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = c8 * 8 + 2 * h, col = c * 32 + e;
+          dot = fmaf(bars.gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(kx[h] << 16), dot);
+          dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(kx[h] & 0xFFFF0000u),
+                     dot);
+        }
+      }
+    }
+    const float coef = r * r * r * (1.f / D) * dot;
+    // Pass 2, per 32-column chunk: dk = r g dk_hat - coef k, and the chunk's
+    // dgk terms dk_hat k r summed over the warp's 32 rows by a reduce-scatter
+    // (lane L ends with column 32 c + L).
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tDK + c * 32, a);
+      tmem_wait_ld();
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        mbar_arrive(&bars.acc_free_k);
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+        float y[8];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = c8 * 8 + 2 * h, col = c * 32 + e;
+          const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
+          const float dk0 = key_live ? __uint_as_float(a[e]) * scale : 0.f;
+          const float dk1 = key_live ? __uint_as_float(a[e + 1]) * scale : 0.f;
+          y[2 * h] = r * bars.gk[col] * dk0 - coef * x0;
+          y[2 * h + 1] = r * bars.gk[col + 1] * dk1 - coef * x1;
+          a[e] = __float_as_uint(dk0 * x0 * r);
+          a[e + 1] = __float_as_uint(dk1 * x1 * r);
         }
         if (key_live) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(a[q * 8 + 0]), __uint_as_float(a[q * 8 + 1]));
-            o.y = pack_bf16x2(__uint_as_float(a[q * 8 + 2]), __uint_as_float(a[q * 8 + 3]));
-            o.z = pack_bf16x2(__uint_as_float(a[q * 8 + 4]), __uint_as_float(a[q * 8 + 5]));
-            o.w = pack_bf16x2(__uint_as_float(a[q * 8 + 6]), __uint_as_float(a[q * 8 + 7]));
-            dvrow[c * 4 + q] = o;
-          }
+          uint4 o;
+          o.x = pack_bf16x2(y[0], y[1]);
+          o.y = pack_bf16x2(y[2], y[3]);
+          o.z = pack_bf16x2(y[4], y[5]);
+          o.w = pack_bf16x2(y[6], y[7]);
+          dkrow[c * 4 + c8] = o;
         }
       }
-      float dot = 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tDK + c * 32, a);
-        tmem_wait_ld();
+      for (int m = 16, half = 16; m >= 1; m >>= 1, half >>= 1) {
+        const bool upper = (lane & m) != 0;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-            dot = fmaf(bars.gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(kx[h] << 16), dot);
-            dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(kx[h] & 0xFFFF0000u),
-                       dot);
-          }
+        for (int j = 0; j < half; ++j) {
+          const float send = __uint_as_float(upper ? a[j] : a[j + half]);
+          const float keep = __uint_as_float(upper ? a[j + half] : a[j]);
+          a[j] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, m));
         }
       }
-      const float coef = r * r * r * (1.f / D) * dot;
-      bulk_wait_group_read0();  // the staging row is free for the column sums
-#pragma unroll
-      for (int pass = 0; pass < D / C::kDQCols; ++pass) {
-#pragma unroll
-        for (int cc = 0; cc < C::kDQCols / 32; ++cc) {
-          const int c = pass * (C::kDQCols / 32) + cc;
-          uint32_t a[32];
-          tmem_ld32(tDK + c * 32, a);
-          tmem_wait_ld();
-          if (c == D / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(&bars.acc_free_k);
-          }
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
-            float y[8], gpart[8];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int col = c * 32 + c8 * 8 + 2 * h;
-              const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
-              const float dk0 = key_live ? __uint_as_float(a[c8 * 8 + 2 * h]) * scale : 0.f;
-              const float dk1 = key_live ? __uint_as_float(a[c8 * 8 + 2 * h + 1]) * scale : 0.f;
-              y[2 * h] = r * bars.gk[col] * dk0 - coef * x0;
-              y[2 * h + 1] = r * bars.gk[col + 1] * dk1 - coef * x1;
-              gpart[2 * h] = dk0 * x0 * r;
-              gpart[2 * h + 1] = dk1 * x1 * r;
-            }
-            if (key_live) {
-              uint4 o;
-              o.x = pack_bf16x2(y[0], y[1]);
-              o.y = pack_bf16x2(y[2], y[3]);
-              o.z = pack_bf16x2(y[4], y[5]);
-              o.w = pack_bf16x2(y[6], y[7]);
-              dkrow[c * 4 + c8] = o;
-            }
-            const uint32_t soff = static_cast<uint32_t>((cc * 32 + c8 * 8) * 4);
-            st_shared_v4(srow_a + soff, __float_as_uint(gpart[0]), __float_as_uint(gpart[1]),
-                         __float_as_uint(gpart[2]), __float_as_uint(gpart[3]));
-            st_shared_v4(srow_a + soff + 16, __float_as_uint(gpart[4]), __float_as_uint(gpart[5]),
-                         __float_as_uint(gpart[6]), __float_as_uint(gpart[7]));
-          }
-        }
-        if (!(ok = epi_sync())) break;  // every row is staged
-        if (r128 < C::kDQCols) {
-          // Fixed-order column sum over the tile's 128 key rows.
-          const float* col = red + r128;
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll 8
-          for (int q = 0; q < 128; q += 4) {
-            s0 += col[(q + 0) * kRowFloats];
-            s1 += col[(q + 1) * kRowFloats];
-            s2 += col[(q + 2) * kRowFloats];
-            s3 += col[(q + 3) * kRowFloats];
-          }
-          bars.dgk_cta[pass * C::kDQCols + r128] += (s0 + s1) + (s2 + s3);
-        }
-        if (!(ok = epi_sync())) break;  // every column summed before the rows are rewritten
-      }
-      if (!ok) break;
+      bars.wsum[warp & 3][c * 32 + lane] = __uint_as_float(a[0]);
     }
+    if (!(ok = epi_sync())) break;  // the warp sums are complete
+    bars.dgk_cta[r128] += ((bars.wsum[0][r128] + bars.wsum[1][r128]) + bars.wsum[2][r128]) + bars.wsum[3][r128];
+    if (!(ok = epi_sync())) break;  // ... and read before the next unit rewrites them
   }
-  if constexpr (kOrd)
+  if (leader) {
     if (ok) complete_previous();
-  if (r128 < C::kDQCols) {
-#pragma unroll
-    for (int pass = 0; pass < D / C::kDQCols; ++pass)
-      dgk_part[static_cast<size_t>(blockIdx.x) * D + pass * C::kDQCols + r128] = bars.dgk_cta[pass * C::kDQCols + r128];
+    bulk_wait_group0();
   }
-  bulk_wait_group0();
+  dgk_part[static_cast<size_t>(blockIdx.x) * D + r128] = bars.dgk_cta[r128];
 }
 
 // d = 64 epilogue warps (warps 12-15, one thread per key row): per unit,
@@ -1392,7 +1400,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars.kv_mmadone[s], n_rel);  // d = 64: the recompute and the dQ issuers
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], n_rel);
-      mbar_init(&bars.ds_free[s], 1);  // the dQ product (d = 64: dK reads dS^T from TMEM)
+      // The dQ product (d = 64: dK reads dS^T from TMEM); d = 128 also the
+      // drain, whose reduces read two staging tiles over the dS^T tile.
+      mbar_init(&bars.ds_free[s], D == 128 ? 2 : 1);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
@@ -1412,8 +1422,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.drain[1], 1);
     mbar_init(&bars.drain[2], 1);
     bars.abort = 0;
-    bars.dq_join[0] = 0u;
-    bars.dq_join[1] = 0u;
     fence_mbar_init();
   }
   if (warp == kWarpMma0) {
@@ -1456,34 +1464,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp < 8) {
     setmaxnreg_inc<D == 64 ? kRegCompute64 : kRegCompute128>();
     bwd_compute<D>(sm, bars, tmem, warp >> 2, w, scale, dev_err);
-  } else {
-    if constexpr (D == 64) {
-      if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain64>();
-      else if (warp < kWarpTma) setmaxnreg_inc<kRegEpi64>();
-      else setmaxnreg_dec<kRegMma64>();
-    } else {  // the TMA / issuer warps keep their launch count
-      static_assert(kRegMma128 == kRegLaunchMin, "d = 128: the TMA / issuer warps keep their launch count");
-      if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain128>();
-      else if (warp < kWarpTma) setmaxnreg_dec<kRegIdle128>();
-    }
+  } else if constexpr (D == 64) {
+    if (warp < kWarpEpi) setmaxnreg_dec<kRegDrain64>();
+    else if (warp < kWarpTma) setmaxnreg_inc<kRegEpi64>();
+    else setmaxnreg_dec<kRegMma64>();
     if (warp < kWarpEpi) {
-      if constexpr (D == 64) bwd_drain64<D, kOrd>(sm, bars, tmem, w, &map_dq, counters, dev_err);
-      else bwd_drain_epilogue<D, kOrd>(sm, bars, tmem, w, scale, dqacc, counters, k_raw, rk, dk, dv, dgk_part, dev_err);
+      bwd_drain64<D, kOrd>(sm, bars, tmem, w, &map_dq, counters, dev_err);
     } else if (warp < kWarpTma) {
-      if constexpr (D == 64) bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, &map_kraw, &map_dk, &map_dv, rk, dk, dv, dgk_part,
-                                                    dev_err);
+      bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, &map_kraw, &map_dk, &map_dv, rk, dk, dv, dgk_part, dev_err);
     } else if (warp == kWarpTma) {
       if (lane == 0)
         bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, nlse2_pad, delta_pad, dev_err);
     } else if (warp == kWarpMma0) {
-      if (lane == 0) {
-        if (C::kSplitIssuers) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
-        else bwd_mma<D>(sm, bars, tmem, w, dev_err);
-      }
+      if (lane == 0) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
     } else if (warp == kWarpMma1) {
-      if (lane == 0 && C::kSplitIssuers) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
+      if (lane == 0) bwd_mma_gradients<D>(sm, bars, tmem, w, dev_err);
     } else if (warp == kWarpMma2) {
-      if (lane == 0 && C::kSplitIssuers) bwd_mma_dq<D>(sm, bars, tmem, w, dev_err);
+      if (lane == 0) bwd_mma_dq<D>(sm, bars, tmem, w, dev_err);
+    }
+  } else {
+    // d = 128: each role's setmaxnreg heads its own branch, so that the
+    // compiler sizes the role's code for the count it sets; the TMA / issuer
+    // warps keep their launch count.
+    static_assert(kRegMma128 == kRegLaunchMin, "d = 128: the TMA / issuer warps keep their launch count");
+    if (warp < kWarpEpi) {
+      setmaxnreg_inc<kRegDrain128>();
+      bwd_drain128<D, kOrd>(sm, bars, tmem, w, scale, &map_dq, counters, k_raw, rk, dk, dv, dgk_part, dev_err);
+    } else if (warp < kWarpTma) {
+      setmaxnreg_dec<kRegIdle128>();
+    } else if (warp == kWarpTma) {
+      if (lane == 0)
+        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, nlse2_pad, delta_pad, dev_err);
+    } else if (warp == kWarpMma0) {
+      if (lane == 0) bwd_mma<D>(sm, bars, tmem, w, dev_err);
     }
   }
   tc_fence_before();

@@ -287,11 +287,11 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
   return r == CUDA_SUCCESS;
 }
 
-bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows) {
+bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows, int d) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(rows) * 256};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(rows) * d * 4};
   cuuint32_t box[3] = {32, 128, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -559,7 +559,7 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
              !encode_bhnd_map(&mv, v, s.BH, s.N, s.d) || !encode_bhnd_map(&mdo, dout, s.BH, s.N, s.d) ||
              !(chunks ? encode_stats_map(&mstats, stats, s.BH, s.seg.prows) : (mstats = mq, true)) ||
-             !(chunks ? encode_dq_map(&mdqacc, dqacc, s.BH, s.seg.rows) : (mdqacc = mq, true))) {
+             !encode_dq_map(&mdqacc, dqacc, s.BH, s.seg.rows, s.d)) {
     status = fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   } else {
     const char* stage = "attn_bwd launch";

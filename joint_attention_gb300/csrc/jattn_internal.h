@@ -128,21 +128,20 @@ cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, 
                             float* dq_zero = nullptr, uint32_t* zero_count = nullptr);
 int attn_fwd_grid(const AttnShape& s);
 
-// map_stats: a TMA map over the bf16 statistics chunks (encode_stats_map) and
-// map_dq one over the fp32 dQ accumulator (encode_dq_map) when
-// attn_bwd_stats_chunks(d), else unused.  The accumulator must be zeroed
-// unless attn_bwd_dq_stores_first(s).
+// map_stats: a TMA map over the bf16 statistics chunks (encode_stats_map)
+// when attn_bwd_stats_chunks(d), else unused; map_dq one over the fp32 dQ
+// accumulator (encode_dq_map).  The accumulator must be zeroed unless
+// attn_bwd_dq_stores_first(s).
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, const CUtensorMap& map_stats, const CUtensorMap& map_dq,
                             const AttnShape& s, const float* nlse2_pad,
                             const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
                             float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st);
 // Whether the first dQ contribution to each query tile is stored rather than
-// added, so that the accumulator needs no zeroing: the deterministic mode at
-// d = 128, and at d = 64 in the [B, H, N, d] layout (one segment).
-inline bool attn_bwd_dq_stores_first(const AttnShape& s) {
-  return s.deterministic && (s.d == 128 || s.seg.n == 1);
-}
+// added, so that the accumulator needs no zeroing: the deterministic mode in
+// the [B, H, N, d] layout (one segment), whose 128-row tiles end at the
+// tensor's end.
+inline bool attn_bwd_dq_stores_first(const AttnShape& s) { return s.deterministic && s.seg.n == 1; }
 // CTAs of the backward launch (one dgk partial each), and the counter words
 // it needs zeroed (deterministic mode: one per query tile; else 0).
 int attn_bwd_dgk_parts(const AttnShape& s);
@@ -181,6 +180,6 @@ bool encode_bhnd_map_rows(CUtensorMap* map, const void* base, int BH, int N, int
 bool encode_stats_map(CUtensorMap* map, const void* base, int BH, int prows);
 // A 3-D TMA map over a [BH, rows, 64] fp32 accumulator with a (32, 128, 1)
 // box and 128-byte swizzle.
-bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows);
+bool encode_dq_map(CUtensorMap* map, const void* base, int BH, int rows, int d);
 
 }  // namespace jattn
