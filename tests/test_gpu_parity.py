@@ -397,6 +397,29 @@ def test_varlen_matches_oracle(ja, lens, d):
     check_bwd(got, ref, where=where)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_deterministic_repeats_and_matches_oracle(ja, d):
+    """Packed sequences in the deterministic mode: the dQ tiles of a segment's
+    last query tile run into the next segment's rows, so every contribution
+    is a reduce into the zeroed accumulator (the next segment's rows get exact
+    zeros from it), in a fixed order.  Every output repeats bit for bit and
+    matches the oracle."""
+    lens = (300, 77, 1101, 5, 129)
+    cu, q, k, v, dout, gq, gk = packed_inputs(lens, 2, d, seed=1400 + d)
+    try:
+        ja.jattn_set_deterministic(True)
+        got = run_gpu_varlen(ja, q, k, v, gq, gk, dout, cu)
+        again = run_gpu_varlen(ja, q, k, v, gq, gk, dout, cu)
+    finally:
+        ja.jattn_set_deterministic(False)
+    for key in got:
+        assert np.array_equal(got[key], again[key]), key
+    ref = oracle.joint_attention_varlen_bwd(q, k, v, gq, gk, dout, cu)
+    where = f"deterministic varlen {lens} d={d}"
+    check_fwd(got, ref, where)
+    check_bwd(got, ref, where=where)
+
+
 def _random_lengths(rng, count, hi):
     return tuple(int(x) for x in rng.integers(1, hi + 1, size=count))
 
