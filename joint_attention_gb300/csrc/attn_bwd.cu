@@ -128,7 +128,7 @@ struct BwdCfg {
   // columns 0-2, resp. 3-5, of every key row) gives S^T - LSE / scale and
   // dP^T - D directly in TMEM.  The compute warps then read no per-query
   // values from shared memory.
-  static constexpr bool kStatsFold = (D == 64);
+  static constexpr bool kStatsFold = true;
   static constexpr int kStatsChunk = 128 * 16 * 2;             // 128 rows x 16 bf16, 32-byte swizzle
   // The constant A chunks repeat one 8-row atom (256 bytes) with a zero atom
   // stride, so each takes 256 bytes.
@@ -571,6 +571,11 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, u
   auto mDS = [=](int t) { return sdesc_sw128(dsaddr(t), 16384, 1024); };
   auto q_ph = [](int t) { return static_cast<uint32_t>((t / C::kQStages) & 1); };
   auto do_ph = [](int t) { return static_cast<uint32_t>((t / C::kDOStages) & 1); };
+  auto kSt = [=](int t) {
+    return sdesc_sw32_kmajor(smem_u32(sm + C::kOffStats + (t % C::kQStages) * C::kStatsChunk), 256u);
+  };
+  const uint64_t kOnesS = sdesc_sw32_kmajor(smem_u32(sm + C::kOffConst), 0u);
+  const uint64_t kOnesD = sdesc_sw32_kmajor(smem_u32(sm + C::kOffConst + C::kConstAtom), 0u);
 
   bool ok = true;
   int tb = 0;  // query tiles of the previous units
@@ -586,12 +591,14 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, u
     if (!(ok = mbar_wait(&bars.q_full[t0 % C::kQStages], q_ph(t0), ab, dev_err))) break;
     tc_fence_after();
     mma_kk<D>(tmem + C::kColS, kK, kQ(t0), C::kIdescSS);
+    umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t0), C::kIdescSS, 1u);
     umma_commit(&bars.s_full);
     // dP(t0) lands where the previous unit's last dQ was drained from.
     if (t0 > 0 && !(ok = mbar_wait(&bars.dq_free, (t0 - 1) & 1, ab, dev_err))) break;
     if (!(ok = mbar_wait(&bars.do_full[t0 % C::kDOStages], do_ph(t0), ab, dev_err))) break;
     tc_fence_after();
     mma_kk<D>(tmem + C::kColDP, kV, kDO(t0), C::kIdescSS);
+    umma_bf16_ss(tmem + C::kColDP, kOnesD, kSt(t0), C::kIdescSS, 1u);
     umma_commit(&bars.dp_full);
     for (int i = 0; i < nkt; ++i) {
       const int t = t0 + i;
@@ -606,6 +613,7 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, u
         if (!(ok = mbar_wait(&bars.q_full[(t + 1) % C::kQStages], q_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
         mma_kk<D>(tmem + C::kColS, kK, kQ(t + 1), C::kIdescSS);
+        umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t + 1), C::kIdescSS, 1u);
         umma_commit(&bars.s_full);
       }
       // dK(t): needs dS^T(t) in shared memory (compute is then done with dP(t)).
@@ -624,6 +632,7 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, u
         if (!(ok = mbar_wait(&bars.do_full[(t + 1) % C::kDOStages], do_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
         mma_kk<D>(tmem + C::kColDP, kV, kDO(t + 1), C::kIdescSS);
+        umma_bf16_ss(tmem + C::kColDP, kOnesD, kSt(t + 1), C::kIdescSS, 1u);
         umma_commit(&bars.dp_full);
       }
     }
@@ -752,7 +761,7 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
                                                                          __uint_as_float(dpv[e + 2 * h + 1])));
             st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
                          dsw[e / 2 + 2], dsw[e / 2 + 3]);
-            if (e == 24) tmem_st16(tDP + c * 16, dsw);  // dS^T for dK
+            if (C::kSplitIssuers && e == 24) tmem_st16(tDP + c * 16, dsw);  // dS^T for dK (d = 64)
             continue;
           }
           const float4 d0 = *reinterpret_cast<const float4*>(C::delta(sm, qs) + 64 * g + col);

@@ -94,7 +94,7 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
                             const uint32_t* zero_count = nullptr, uint32_t zeroed_by = 0);
 // Whether the attention backward takes the statistics as the bf16 chunks
 // above (and a TMA map over them) rather than as fp32 rows.
-inline bool attn_bwd_stats_chunks(int d) { return d == 64; }
+inline bool attn_bwd_stats_chunks(int d) { return d == 64 || d == 128; }
 // nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq
 // partials; the last one (by *ticket, zeroed by the backward preparation)
 // sums them and the nk dgk partials into dgq and dgk.  zero_count (or null)
