@@ -40,8 +40,7 @@
 //               are read.
 //   warp 16     TMA producer: K_j, V_j per unit (double-buffered for d = 64);
 //               per query tile Q_i and dO_i through rings, with the tile's
-//               softmax statistics (d = 64: a bf16 chunk for the MMAs;
-//               d = 128: fp32 LSE_i and D_i rows).
+//               softmax statistics (a bf16 chunk for the MMAs).
 //   warps 17-19 MMA issuers (d = 64): recompute (S, dK, dP), dV, and dQ;
 //               d = 128 uses warp 17 alone.
 //
@@ -121,14 +120,13 @@ struct BwdCfg {
   // d = 64: three MMA issuers (S, dK, dP; dV; dQ) and
   // P^T in its own TMEM columns.  d = 128: one issuer, P^T over S^T.
   static constexpr bool kSplitIssuers = (D == 64);
-  // d = 64: the softmax statistics enter through the tensor cores.  Each
-  // query tile brings a 16-column bf16 chunk B of its rows' -LSE / scale and
-  // -D, each split into three bf16 terms (columns 0-2 and 3-5), and one more
-  // K = 16 step of the S^T and dP^T products with a constant A chunk (ones in
+  // The softmax statistics enter through the tensor cores.  Each query tile
+  // brings a 16-column bf16 chunk B of its rows' -LSE / scale and -D, each
+  // split into three bf16 terms (columns 0-2 and 3-5), and one more K = 16
+  // step of the S^T and dP^T products with a constant A chunk (ones in
   // columns 0-2, resp. 3-5, of every key row) gives S^T - LSE / scale and
   // dP^T - D directly in TMEM.  The compute warps then read no per-query
   // values from shared memory.
-  static constexpr bool kStatsFold = true;
   static constexpr int kStatsChunk = 128 * 16 * 2;             // 128 rows x 16 bf16, 32-byte swizzle
   // The constant A chunks repeat one 8-row atom (256 bytes) with a zero atom
   // stride, so each takes 256 bytes.
@@ -142,19 +140,9 @@ struct BwdCfg {
   static constexpr int kOffDO = kOffQ + kQStages * kTile;     // + stage * kTile
   static constexpr int kOffDS = kOffDO + kDOStages * kTile;   // + buf * 32 KB (128 x 128 bf16)
   static constexpr int kOffStats = kOffDS + kDSBufs * 128 * 128 * 2;          // + stage * kStatsChunk
-  static constexpr int kOffConst = kOffStats + (kStatsFold ? kQStages * kStatsChunk : 0);  // S, then dP
-  static constexpr int kOffDQ = kOffConst + (kStatsFold ? 1024 : 0);
-  // d = 128: per query stage, minus the tile's LSE in the log2 domain (-inf
-  // past N) and D (0 past N), copied in with the tile from padded scratch rows.
-  static constexpr int kOffNlse = kOffDQ + kDQStageBytes;                 // + stage * 512
-  static constexpr int kOffDelta = kOffNlse + (kStatsFold ? 0 : kQStages * 512);
-  static constexpr int kTileBytes = kOffDelta + (kStatsFold ? 0 : kQStages * 512);
-  static __device__ __forceinline__ float* nlse2(uint8_t* sm, int qs) {
-    return reinterpret_cast<float*>(sm + kOffNlse + qs * 512);
-  }
-  static __device__ __forceinline__ float* delta(uint8_t* sm, int qs) {
-    return reinterpret_cast<float*>(sm + kOffDelta + qs * 512);
-  }
+  static constexpr int kOffConst = kOffStats + kQStages * kStatsChunk;  // S, then dP
+  static constexpr int kOffDQ = kOffConst + 1024;
+  static constexpr int kTileBytes = kOffDQ + kDQStageBytes;
   static constexpr int kDynSmem = kTileBytes + 1024;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;
@@ -284,13 +272,13 @@ __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
 template <int D, class W>
 __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                              const CUtensorMap* mdo, const CUtensorMap* mstats, uint8_t* sm, BwdBars& bars,
-                             const W& w, const float* nlse2_pad, const float* delta_pad, uint32_t* dev_err) {
+                             const W& w, uint32_t* dev_err) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(mq);
   tma_prefetch_desc(mk);
   tma_prefetch_desc(mv);
   tma_prefetch_desc(mdo);
-  if constexpr (C::kStatsFold) tma_prefetch_desc(mstats);
+  tma_prefetch_desc(mstats);
   volatile int* ab = &bars.abort;
   int nkv_issued = 0, nq_issued = 0, ndo_issued = 0;
   bool ok = true;
@@ -311,15 +299,8 @@ __device__ void bwd_producer(const CUtensorMap* mq, const CUtensorMap* mk, const
       const int qs = t % C::kQStages;
       if (t >= C::kQStages && !(ok = mbar_wait(&bars.q_empty[qs], ((t / C::kQStages) - 1) & 1, ab, dev_err))) break;
       const int qi = un.query_tile(i);
-      if constexpr (C::kStatsFold) {
-        mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + C::kStatsChunk);
-        tma_load_3d(sm + C::kOffStats + qs * C::kStatsChunk, mstats, &bars.q_full[qs], 0, un.prow0 + qi * 128, bh);
-      } else {
-        mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + 1024u);
-        const size_t prow = static_cast<size_t>(bh) * w.seg.prows + un.prow0 + static_cast<size_t>(qi) * 128;
-        bulk_load(C::nlse2(sm, qs), nlse2_pad + prow, 512, &bars.q_full[qs]);
-        bulk_load(C::delta(sm, qs), delta_pad + prow, 512, &bars.q_full[qs]);
-      }
+      mbar_arrive_expect_tx(&bars.q_full[qs], C::kTile + C::kStatsChunk);
+      tma_load_3d(sm + C::kOffStats + qs * C::kStatsChunk, mstats, &bars.q_full[qs], 0, un.prow0 + qi * 128, bh);
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_3d(sm + C::kOffQ + qs * C::kTile + blk * 16384, mq, &bars.q_full[qs], blk * 64, un.row0 + qi * 128,
                     bh);
@@ -470,13 +451,13 @@ __device__ void bwd_mma_recompute(uint8_t* sm, BwdBars& bars, uint32_t tmem, con
       if (!(ok = mbar_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, ab, dev_err))) break;
       tc_fence_after();
       mma_kk<D>(tmem + C::kColS, kK, kQ(t), C::kIdescSS);
-      if constexpr (C::kStatsFold) umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t), C::kIdescSS, 1u);
+      umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t), C::kIdescSS, 1u);
       umma_commit(&bars.s_full);
       if (pend_t >= 0 && !(ok = issue_dk())) break;
       if (!(ok = mbar_wait(&bars.do_full[t % C::kDOStages], (t / C::kDOStages) & 1, ab, dev_err))) break;
       tc_fence_after();
       mma_kk<D>(tmem + C::kColDP, kV, kDO(t), C::kIdescSS);
-      if constexpr (C::kStatsFold) umma_bf16_ss(tmem + C::kColDP, kOnesD, kSt(t), C::kIdescSS, 1u);
+      umma_bf16_ss(tmem + C::kColDP, kOnesD, kSt(t), C::kIdescSS, 1u);
       umma_commit(&bars.dp_full);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
       pend_t = t;
@@ -660,7 +641,6 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
   const uint32_t tDP = tmem + lane_base + C::kColDP + 64 * g;
   const uint32_t swz = static_cast<uint32_t>(kr & 7);
   const uint64_t sc2 = f2_make(scale * kLog2e, scale * kLog2e);
-  const uint64_t minus1 = f2_make(-1.f, -1.f);
   volatile int* ab = &bars.abort;
 
   int tb = 0;  // query tiles of the previous units
@@ -671,16 +651,13 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
     tb += un.nkt;
     for (int i = 0; i < un.nkt; ++i) {
       const int t = t0 + i;
-      const int qs = t % C::kQStages;
       bool ok = mbar_wait(&bars.s_full, t & 1, ab, dev_err);
-      // d = 128: this stage's LSE / D arrived with the query tile (already complete).
-      if (!C::kStatsFold && ok) ok = mbar_wait(&bars.q_full[qs], (t / C::kQStages) & 1, ab, dev_err);
       if (!__all_sync(0xffffffffu, ok)) return;
       tc_fence_after();
       // P^T = exp2(s log2e S^T - LSE log2e), packed bf16 pairs into TMEM
       // (chunk c -> 16 packed columns at 16c).  Key rows past N get P = 0.
-      // d = 64: TMEM holds S^T - LSE / scale, so only the product by
-      // s log2e remains.
+      // TMEM holds S^T - LSE / scale (the statistics step), so only the
+      // product by s log2e remains.
       uint32_t pp[32];
       // Both 32-column chunks of this group's S^T in flight at once.
       uint32_t sall[2][32];
@@ -694,25 +671,13 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint32_t(&s)[32] = sall[c];
-        if (key_live && C::kStatsFold) {  // warp-uniform except in a head's last key tile
+        if (key_live) {  // warp-uniform except in a head's last key tile
           const uint64_t zero2 = f2_make(0.f, 0.f);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             float x0, x1, x2, x3;
             f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, zero2), x0, x1);
             f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), sc2, zero2), x2, x3);
-            pp[(c * 32 + e) / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-            pp[(c * 32 + e) / 2 + 1] = pack_bf16x2(ex2_approx(x2), ex2_approx(x3));
-          }
-        } else if (key_live) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(C::nlse2(sm, qs) + 64 * g + c * 32 + e);
-            float x0, x1, x2, x3;
-            f2_split(f2_fma(f2_make(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sc2, f2_make(l4.x, l4.y)), x0,
-                     x1);
-            f2_split(f2_fma(f2_make(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), sc2, f2_make(l4.z, l4.w)),
-                     x2, x3);
             pp[(c * 32 + e) / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
             pp[(c * 32 + e) / 2 + 1] = pack_bf16x2(ex2_approx(x2), ex2_approx(x3));
           }
@@ -753,31 +718,14 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           const int col = c * 32 + e;  // query column within this group's 64
-          if constexpr (C::kStatsFold) {
-            // dS = P * bf16(dP - D), dP - D from TMEM: one pack, one bf16x2 product
+          // dS = P * bf16(dP - D), dP - D from TMEM: one pack, one bf16x2 product
 #pragma unroll
-            for (int h = 0; h < 4; ++h)
-              dsw[e / 2 + h] = bf16x2_mul(pp[col / 2 + h], pack_bf16x2(__uint_as_float(dpv[e + 2 * h]),
-                                                                         __uint_as_float(dpv[e + 2 * h + 1])));
-            st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
-                         dsw[e / 2 + 2], dsw[e / 2 + 3]);
-            if (C::kSplitIssuers && e == 24) tmem_st16(tDP + c * 16, dsw);  // dS^T for dK (d = 64)
-            continue;
-          }
-          const float4 d0 = *reinterpret_cast<const float4*>(C::delta(sm, qs) + 64 * g + col);
-          const float4 d1 = *reinterpret_cast<const float4*>(C::delta(sm, qs) + 64 * g + col + 4);
-          const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            // dS = P * bf16(dP - D): one packed fp32 pair, one pack, one bf16x2 product
-            float a, b;
-            f2_split(f2_fma(f2_make(dd[2 * h], dd[2 * h + 1]), minus1,
-                            f2_make(__uint_as_float(dpv[e + 2 * h]), __uint_as_float(dpv[e + 2 * h + 1]))),
-                     a, b);
-            dsw[e / 2 + h] = bf16x2_mul(pp[col / 2 + h], pack_bf16x2(a, b));
-          }
+          for (int h = 0; h < 4; ++h)
+            dsw[e / 2 + h] = bf16x2_mul(pp[col / 2 + h], pack_bf16x2(__uint_as_float(dpv[e + 2 * h]),
+                                                                       __uint_as_float(dpv[e + 2 * h + 1])));
           st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
                        dsw[e / 2 + 2], dsw[e / 2 + 3]);
+          if (C::kSplitIssuers && e == 24) tmem_st16(tDP + c * 16, dsw);  // dS^T for dK (d = 64)
         }
       }
       if (C::kSplitIssuers) tmem_wait_st();
@@ -1383,8 +1331,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap map_stats, const __grid_constant__ CUtensorMap map_dq,
                     const __grid_constant__ CUtensorMap map_kraw, const __grid_constant__ CUtensorMap map_dk,
                     const __grid_constant__ CUtensorMap map_dv, const __grid_constant__ W w, float scale,
-                    const float* __restrict__ nlse2_pad,
-                    const float* __restrict__ delta_pad, const __nv_bfloat16* __restrict__ k_raw,
+                    const __nv_bfloat16* __restrict__ k_raw,
                     const float* __restrict__ rk, const float* __restrict__ gk, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, float* __restrict__ dqacc, uint32_t* __restrict__ counters,
                     float* __restrict__ dgk_part, uint32_t* dev_err) {
@@ -1437,7 +1384,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
-  if constexpr (C::kStatsFold) {
+  {
     // The constant A chunks of the statistics K step: key rows of ones in
     // columns 0-2 (S^T) and 3-5 (dP^T), zeros elsewhere, in the 32-byte
     // swizzled K-major layout (16-byte half h of row r at r * 32 + 16 (h ^ bit
@@ -1460,7 +1407,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_proxy_async_smem();  // visible to the tensor cores
   }
-  griddep_wait();  // the previous grid's writes (q_hat, k_hat, LSE / D rows, zeroed dQ) are visible
+
+  griddep_wait();  // the previous grid's writes (q_hat, k_hat, statistics chunks, zeroed dQ) are visible
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     bars.gk[c] = gk[c];
     bars.dgk_cta[c] = 0.f;
@@ -1483,7 +1431,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bwd_epilogue_warps<D>(sm, bars, tmem, w, scale, &map_kraw, &map_dk, &map_dv, rk, dk, dv, dgk_part, dev_err);
     } else if (warp == kWarpTma) {
       if (lane == 0)
-        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, nlse2_pad, delta_pad, dev_err);
+        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, dev_err);
     } else if (warp == kWarpMma0) {
       if (lane == 0) bwd_mma_recompute<D>(sm, bars, tmem, w, dev_err);
     } else if (warp == kWarpMma1) {
@@ -1503,7 +1451,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       setmaxnreg_dec<kRegIdle128>();
     } else if (warp == kWarpTma) {
       if (lane == 0)
-        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, nlse2_pad, delta_pad, dev_err);
+        bwd_producer<D>(&map_q, &map_k, &map_v, &map_do, &map_stats, sm, bars, w, dev_err);
     } else if (warp == kWarpMma0) {
       if (lane == 0) bwd_mma<D>(sm, bars, tmem, w, dev_err);
     }
@@ -1520,7 +1468,6 @@ template <int D, bool kOrd, class W>
 cudaError_t launch_bwd_w(const W& w, int grid, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const CUtensorMap& mstats, const CUtensorMap& mdq,
                          const CUtensorMap& mkraw, const CUtensorMap& mdk, const CUtensorMap& mdv, const AttnShape& s,
-                         const float* nlse2_pad, const float* delta_pad,
                          const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
                          float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st) {
   using C = BwdCfg<D>;
@@ -1534,8 +1481,8 @@ cudaError_t launch_bwd_w(const W& w, int grid, const CUtensorMap& mq, const CUte
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kRegLaunchMin || fa.numRegs > kRegLaunchMax) return cudaErrorInvalidConfiguration;
-  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, w, s.scale, nlse2_pad,
-                    delta_pad, reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
+  return launch_pdl(kernel, dim3(grid), dim3(kBwdThreads), C::kDynSmem, st, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, w, s.scale,
+                    reinterpret_cast<const __nv_bfloat16*>(k_raw), rk, gk,
                     reinterpret_cast<__nv_bfloat16*>(dk), reinterpret_cast<__nv_bfloat16*>(dv), dqacc, counters,
                     dgk_part, dev_err);
 }
@@ -1575,8 +1522,7 @@ BwdPlan bwd_plan(const AttnShape& s) {
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const CUtensorMap& mstats, const CUtensorMap& mdq, const AttnShape& s,
-                         const float* nlse2_pad,
-                         const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk,
+                         const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk,
                          uint16_t* dv, float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err,
                          cudaStream_t st) {
   // d = 64: the epilogue loads raw k tiles and stores dk / dv tiles by TMA.
@@ -1593,9 +1539,9 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     w.units = s.BH * w.upc;
     w.ord = plan.ord;
     if (plan.ord == kDqArrival)
-      return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+      return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, k_raw, rk, gk, dk, dv,
                                     dqacc, counters, dgk_part, dev_err, st);
-    return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+    return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, k_raw, rk, gk, dk, dv,
                                  dqacc, counters, dgk_part, dev_err, st);
   }
   BwdWork w;
@@ -1604,9 +1550,9 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   w.units = s.BH * w.upc;
   w.ord = plan.ord;
   if (plan.ord == kDqArrival)
-    return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv,
+    return launch_bwd_w<D, false>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, k_raw, rk, gk, dk, dv,
                                   dqacc, counters, dgk_part, dev_err, st);
-  return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+  return launch_bwd_w<D, true>(w, plan.grid, mq, mk, mv, mdo, mstats, mdq, mkraw, mdk, mdv, s, k_raw, rk, gk, dk, dv, dqacc,
                                counters, dgk_part, dev_err, st);
 }
 
@@ -1619,15 +1565,14 @@ int attn_bwd_counter_words(const AttnShape& s) { return s.deterministic ? s.BH *
 
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, const CUtensorMap& map_stats, const CUtensorMap& map_dq,
-                            const AttnShape& s, const float* nlse2_pad,
-                            const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk,
+                            const AttnShape& s, const uint16_t* k_raw, const float* rk, const float* gk,
                             uint16_t* dk, uint16_t* dv, float* dqacc, uint32_t* counters, float* dgk_part,
                             uint32_t* dev_err, cudaStream_t st) {
   if (s.d == 64)
-    return launch_bwd_d<64>(map_q, map_k, map_v, map_do, map_stats, map_dq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+    return launch_bwd_d<64>(map_q, map_k, map_v, map_do, map_stats, map_dq, s, k_raw, rk, gk, dk, dv, dqacc,
                             counters, dgk_part, dev_err, st);
   if (s.d == 128)
-    return launch_bwd_d<128>(map_q, map_k, map_v, map_do, map_stats, map_dq, s, nlse2_pad, delta_pad, k_raw, rk, gk, dk, dv, dqacc,
+    return launch_bwd_d<128>(map_q, map_k, map_v, map_do, map_stats, map_dq, s, k_raw, rk, gk, dk, dv, dqacc,
                              counters, dgk_part, dev_err, st);
   return cudaErrorInvalidValue;
 }

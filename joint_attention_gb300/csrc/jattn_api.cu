@@ -226,8 +226,7 @@ size_t bwd_scratch_bytes(const Shape& s, int nparts_q, int nparts_k, int counter
     b += 2 * (s.rows * 4 + 256);   // rq, rk
     b += s.elems * 4 + 256;        // dq accumulator
   }
-  b += 2 * (static_cast<size_t>(s.BH) * s.seg.prows * 4 + 256);   // nlse2, delta
-  if (attn_bwd_stats_chunks(s.d)) b += static_cast<size_t>(s.BH) * s.seg.prows * 32 + 256;  // statistics chunks
+  b += static_cast<size_t>(s.BH) * s.seg.prows * 32 + 256;  // statistics chunks
   b += (static_cast<size_t>(nparts_q) + nparts_k) * s.d * 4 + 512; // dg partials
   b += 4 * (1 + static_cast<size_t>(counter_words)) + 256;      // dg ticket, dQ order counters
   return b + 256;
@@ -534,10 +533,7 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
     rk = cv.take<float>(s.rows);
     dqacc = cv.take<float>(s.elems);
   }
-  float* nlse2 = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
-  float* delta = cv.take<float>(static_cast<size_t>(s.BH) * s.seg.prows);
-  const bool chunks = attn_bwd_stats_chunks(s.d);
-  uint16_t* stats = chunks ? cv.take<uint16_t>(static_cast<size_t>(s.BH) * s.seg.prows * 16) : nullptr;
+  uint16_t* stats = cv.take<uint16_t>(static_cast<size_t>(s.BH) * s.seg.prows * 16);
   float* dgq_part = cv.take<float>(static_cast<size_t>(nparts_q) * s.d);
   float* dgk_part = cv.take<float>(static_cast<size_t>(nparts_k) * s.d);
   // The gain-gradient ticket, then (deterministic mode) one dQ order counter
@@ -549,7 +545,7 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
   {
     Timed t(JATTN_KERNEL_BWD_PREP, st);
     // Saved activations: the preparation computes only the statistics.
-    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, saved ? nullptr : qhat, khat, rq, rk, nlse2, delta, stats,
+    ce = launch_bwd_prep(q, k, gq, gk, out, dout, lse, saved ? nullptr : qhat, khat, rq, rk, stats,
                          sqrtf(static_cast<float>(s.d)), attn_bwd_dq_stores_first(as) ? nullptr : dqacc, dg_ticket,
                          1 + counter_words, s.BH, s.seg, s.d, err, st, zero_count,
                          static_cast<uint32_t>(attn_fwd_grid(as)));
@@ -558,14 +554,14 @@ int bwd_body(const Shape& s, const jattn_bf16* q, const jattn_bf16* k, const jat
     status = fail(JATTN_ERR_CUDA, "bwd_prep launch", ce);
   } else if (!encode_bhnd_map(&mq, qhat, s.BH, s.N, s.d) || !encode_bhnd_map(&mk, khat, s.BH, s.N, s.d) ||
              !encode_bhnd_map(&mv, v, s.BH, s.N, s.d) || !encode_bhnd_map(&mdo, dout, s.BH, s.N, s.d) ||
-             !(chunks ? encode_stats_map(&mstats, stats, s.BH, s.seg.prows) : (mstats = mq, true)) ||
+             !encode_stats_map(&mstats, stats, s.BH, s.seg.prows) ||
              !encode_dq_map(&mdqacc, dqacc, s.BH, s.seg.rows, s.d)) {
     status = fail(JATTN_ERR_CUDA, "cuTensorMapEncodeTiled");
   } else {
     const char* stage = "attn_bwd launch";
     {
       Timed t(JATTN_KERNEL_ATTN_BWD, st);
-      ce = launch_attn_bwd(mq, mk, mv, mdo, mstats, mdqacc, as, nlse2, delta, k, rk, gk, dk, dv, dqacc, dg_ticket + 1, dgk_part, err,
+      ce = launch_attn_bwd(mq, mk, mv, mdo, mstats, mdqacc, as, k, rk, gk, dk, dv, dqacc, dg_ticket + 1, dgk_part, err,
                            st);
     }
     if (ce == cudaSuccess) {

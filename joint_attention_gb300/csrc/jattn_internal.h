@@ -53,19 +53,6 @@ bool make_seg_table(SegTable* t, const int* cu, int n);
 // One segment of N rows (the [B, H, N, d] layout).
 void make_uniform_seg_table(SegTable* t, int N);
 
-// Scratch of one call, carved from one stream-ordered allocation.
-struct Scratch {
-  uint16_t* qhat = nullptr;  // [BH, N, d] bf16
-  uint16_t* khat = nullptr;  // [BH, N, d] bf16
-  float* rq = nullptr;       // [BH*N] 1/rms of q rows
-  float* rk = nullptr;       // [BH*N] 1/rms of k rows
-  float* nlse2 = nullptr;    // [BH, Npad] -LSE * log2(e), -inf in the pad rows
-  float* delta = nullptr;    // [BH, Npad] rowsum(dO * O), 0 in the pad rows
-  float* dqacc = nullptr;    // [BH, N, d] fp32 accumulator of dS k_hat
-  float* dgq_part = nullptr; // [nparts, d]
-  float* dgk_part = nullptr; // [nparts, d]
-};
-
 // --- norm / elementwise kernels (HBM-bound) ---------------------------------
 // The streaming norm kernels take the per-launch device error word: their
 // bounded waits on the bulk-copy ring report a timeout through it.
@@ -75,10 +62,9 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
                                uint32_t* dev_err, cudaStream_t st);
 // Rows are the BH heads' seg.rows rows.  The softmax statistics are written
 // in the per-head padded layout (segment s from seg.pcu[s], 128-row
-// multiples): with `stats` null, nlse2 (= -LSE log2 e, -inf in pad rows) and
-// delta (D, 0 in pad rows) as fp32; otherwise `stats` gets 16 bf16 per row,
-// -LSE * inv_scale and -D each as three bf16 terms whose sum rounds to the
-// fp32 value (columns 0-2 and 3-5; pad rows -1e30 and 0), zeros after.  The
+// multiples): `stats` gets 16 bf16 per row, -LSE * inv_scale and -D each as
+// three bf16 terms whose sum rounds to the fp32 value (columns 0-2 and 3-5;
+// pad rows -1e30 and 0), zeros after.  The
 // dq accumulator rows are zeroed unless dqacc is null (the deterministic
 // backward stores its first contribution); the first n_tickets words of
 // `tickets` are zeroed.  With qhat null (q_hat, k_hat, rq and rk saved by a
@@ -88,13 +74,10 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 // forward's CTAs zeroed the accumulator and counted themselves there).
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,
+                            uint16_t* khat, float* rq, float* rk, uint16_t* stats,
                             float inv_scale, float* dqacc, unsigned int* tickets, int n_tickets, int BH,
                             const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st,
                             const uint32_t* zero_count = nullptr, uint32_t zeroed_by = 0);
-// Whether the attention backward takes the statistics as the bf16 chunks
-// above (and a TMA map over them) rather than as fp32 rows.
-inline bool attn_bwd_stats_chunks(int d) { return d == 64 || d == 128; }
 // nparts = q_norm_bwd_parts() CTAs, each writing one d-vector of dgq
 // partials; the last one (by *ticket, zeroed by the backward preparation)
 // sums them and the nk dgk partials into dgq and dgk.  zero_count (or null)
@@ -128,14 +111,12 @@ cudaError_t launch_attn_fwd(const CUtensorMap& map_q, const CUtensorMap& map_k, 
                             float* dq_zero = nullptr, uint32_t* zero_count = nullptr);
 int attn_fwd_grid(const AttnShape& s);
 
-// map_stats: a TMA map over the bf16 statistics chunks (encode_stats_map)
-// when attn_bwd_stats_chunks(d), else unused; map_dq one over the fp32 dQ
-// accumulator (encode_dq_map).  The accumulator must be zeroed unless
+// map_stats: a TMA map over the bf16 statistics chunks (encode_stats_map);
+// map_dq one over the fp32 dQ accumulator (encode_dq_map).  The accumulator must be zeroed unless
 // attn_bwd_dq_stores_first(s).
 cudaError_t launch_attn_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                             const CUtensorMap& map_do, const CUtensorMap& map_stats, const CUtensorMap& map_dq,
-                            const AttnShape& s, const float* nlse2_pad,
-                            const float* delta_pad, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
+                            const AttnShape& s, const uint16_t* k_raw, const float* rk, const float* gk, uint16_t* dk, uint16_t* dv,
                             float* dqacc, uint32_t* counters, float* dgk_part, uint32_t* dev_err, cudaStream_t st);
 // Whether the first dQ contribution to each query tile is stored rather than
 // added, so that the accumulator needs no zeroing: the deterministic mode in

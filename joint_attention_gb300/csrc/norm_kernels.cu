@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const float* __restrict__ gq,
     const float* __restrict__ gk, const uint4* __restrict__ out, const uint4* __restrict__ dout,
     const float* __restrict__ lse, uint4* __restrict__ qhat, uint4* __restrict__ khat, float* __restrict__ rq,
-    float* __restrict__ rk, float* __restrict__ nlse2, float* __restrict__ delta, uint4* __restrict__ stats,
+    float* __restrict__ rk, uint4* __restrict__ stats,
     float inv_scale, float4* __restrict__ dqacc, unsigned int* __restrict__ tickets, int n_tickets,
     const __grid_constant__ SegTable seg, int64_t padded_rows, DivU31 div_prows, const uint32_t* zero_count,
     uint32_t zeroed_by) {
@@ -299,20 +299,15 @@ __global__ void __launch_bounds__(kNormThreads) bwd_prep_kernel(
     for (int i = 0; i < 8; ++i) dot = fmaf(o[i], dd[i], dot);
     dot = row_sum<TPR>(dot);
     if (in_range) {
-      if (stats) {
-        // Two 16-byte halves per row: the split statistics, then zeros.
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (sub == 0) {
-          uint32_t l[3], dd3[3];
-          split3_bf16(valid ? -cur.lse * inv_scale : -1e30f, l);
-          split3_bf16(valid ? -dot : 0.f, dd3);
-          v = make_uint4(l[0] | (l[1] << 16), l[2] | (dd3[0] << 16), dd3[1] | (dd3[2] << 16), 0u);
-        }
-        if (sub < 2) stats[prow * 2 + sub] = v;
-      } else if (sub == 0) {
-        nlse2[prow] = valid ? -cur.lse * 1.4426950408889634f : -INFINITY;
-        delta[prow] = valid ? dot : 0.f;
+      // Two 16-byte halves per row: the split statistics, then zeros.
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (sub == 0) {
+        uint32_t l[3], dd3[3];
+        split3_bf16(valid ? -cur.lse * inv_scale : -1e30f, l);
+        split3_bf16(valid ? -dot : 0.f, dd3);
+        v = make_uint4(l[0] | (l[1] << 16), l[2] | (dd3[0] << 16), dd3[1] | (dd3[2] << 16), 0u);
       }
+      if (sub < 2) stats[prow * 2 + sub] = v;
       if (valid) {
         const int64_t idx = row * TPR + sub;
         if constexpr (kNorm) {
@@ -529,7 +524,7 @@ cudaError_t launch_qk_norm_fwd(const uint16_t* q, const uint16_t* k, const float
 
 cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* gq, const float* gk,
                             const uint16_t* out, const uint16_t* dout, const float* lse, uint16_t* qhat,
-                            uint16_t* khat, float* rq, float* rk, float* nlse2, float* delta, uint16_t* stats,
+                            uint16_t* khat, float* rq, float* rk, uint16_t* stats,
                             float inv_scale, float* dqacc, unsigned int* tickets, int n_tickets, int BH,
                             const SegTable& seg, int d, uint32_t* dev_err, cudaStream_t st,
                             const uint32_t* zero_count, uint32_t zeroed_by) {
@@ -542,7 +537,7 @@ cudaError_t launch_bwd_prep(const uint16_t* q, const uint16_t* k, const float* g
                         : (norm ? bwd_prep_kernel<128, true> : bwd_prep_kernel<128, false>);
   return launch_pdl(kernel, dim3(row_grid(kernel, padded_rows, d)), dim3(kNormThreads), 0, st, u4(q), u4(k), gq,
                     gk, u4(out), u4(dout), lse, reinterpret_cast<uint4*>(qhat), reinterpret_cast<uint4*>(khat), rq,
-                    rk, nlse2, delta, reinterpret_cast<uint4*>(stats), inv_scale, reinterpret_cast<float4*>(dqacc),
+                    rk, reinterpret_cast<uint4*>(stats), inv_scale, reinterpret_cast<float4*>(dqacc),
                     tickets, n_tickets, seg, padded_rows, make_div_u31(static_cast<uint32_t>(seg.prows)), zero_count,
                     zeroed_by);
 }
