@@ -55,7 +55,7 @@ def flops_bwd(B, H, N, d):
 _CAPTURE = ("ncu --set full --clock-control none -k regex:attn_ -s 2 -c 2, "
             "python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-per-config")
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 197.590272e6 + 64.896256e6, "source": "attn_bwd.cu", "sha1": "600485ee26df",
+    "attn_bwd": {"bytes": 197.590272e6 + 64.896256e6, "source": "attn_bwd.cu", "sha1": "55b39b376a1b",
                  "capture": _CAPTURE},
     "attn_fwd": {"bytes": 81.32864e6 + 56.33664e6, "source": "attn_fwd.cu", "sha1": "d52b848c736f",
                  "capture": _CAPTURE},

@@ -8,7 +8,7 @@
 //   S^T  = K_j Q_i^T            P^T  = exp(s S^T - LSE_i)      (per column)
 //   dP^T = V_j dO_i^T           dS^T = P^T * (dP^T - D_i),  D = rowsum(dO*O)
 //   dV_j += P^T dO_i            dK_j += dS^T Q_i              (TMEM accumulators)
-//   dQ_i += dS K_j              (bulk fp32 reduce-add into a global accumulator)
+//   dQ_i += dS K_j              (TMA fp32 reduce-add into a global accumulator)
 //
 // Work unit: one 128-key tile j of one segment of one head (a (b, h) of the
 // [B, H, N, d] layout, or one sequence of a packed variable-length call),
@@ -17,9 +17,8 @@
 // with every barrier phase running on across units, so the next unit's K/V
 // load and first S / dP products overlap the current unit's last tiles and
 // its epilogue.
-// 640 threads (five warpgroups; setmaxnreg gives the compute warpgroups 128
-// registers per thread (d = 64: 120), the drain 88, the epilogue 104 and
-// TMA / MMA 48):
+// 640 threads (five warpgroups; setmaxnreg splits the registers per role,
+// see the budgets below):
 //
 //   warps 0-3   compute group 0: query columns 0-63 of each tile;
 //   warps 4-7   compute group 1: query columns 64-127.  One thread per key
@@ -28,11 +27,11 @@
 //               the MMA's swizzled layout (read MN-major as the A operand of
 //               dQ) and, d = 64, into TMEM over the group's own dP^T columns
 //               as the A operand of dK (d = 128: dK reads the shared tile).
-//   warps 8-11  dQ drain, one thread per query row: d = 64, dQ_i from TMEM
-//               into two swizzled 128 x 32 fp32 staging halves, each added
-//               into the global accumulator by one TMA tensor reduce;
-//               d = 128, padded rows and one bulk reduce-add per row, and
-//               the unit epilogue.
+//   warps 8-11  dQ drain, one thread per query row: dQ_i from TMEM into
+//               swizzled 128 x 32 fp32 staging tiles, each added into the
+//               global accumulator by one TMA tensor reduce (d = 128: two of
+//               the four tiles over the dS^T tile); d = 128, also the unit
+//               epilogue.
 //   warps 12-15 d = 64 unit epilogue, one thread per key row: dv, and the
 //               K-RMSNorm backward of dK (dk and the unit's dgk partial),
 //               built in the unit's own K/V buffer once the MMAs are done
@@ -54,7 +53,7 @@
 //
 // d = 128: TMEM S^T/P^T [0,128), dP^T [128,256), dV [256,384), dK [384,512),
 // dQ over the dP^T columns; one issuer in the order dV(i), S(i+1), dK(i),
-// dQ(i), dP(i+1), with dP(i+1) waiting for dQ(i) to be drained.
+// dQ(i), dP(i+1), with dP(i+1) waiting for dQ(i) to be out of TMEM.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -167,7 +166,7 @@ struct BwdCfg {
 // dQ accumulation order.  kDqArrival: every key tile's contribution is a
 // bulk reduce-add into a zeroed accumulator, in whatever order they land (the
 // default; dq and dgq repeat to rounding).  kDqRotated / kDqAscending: the
-// deterministic mode, a fixed order per query tile (see bwd_drain_epilogue).
+// deterministic mode, a fixed order per query tile (see bwd_drain64).
 enum : int { kDqArrival = 0, kDqRotated = 1, kDqAscending = 2 };
 
 struct BwdUnit {
