@@ -699,34 +699,40 @@ __device__ void bwd_compute(uint8_t* sm, BwdBars& bars, uint32_t tmem, int g, co
       mbar_arrive(&bars.p_ready);
 
       ok = mbar_wait(&bars.dp_full, t & 1, ab, dev_err);
-      if (ok && t >= C::kDSBufs)
-        ok = mbar_wait(&bars.ds_free[t % C::kDSBufs], ((t / C::kDSBufs) - 1) & 1, ab, dev_err);
       if (!__all_sync(0xffffffffu, ok)) return;
       tc_fence_after();
       const uint32_t ds_row = smem_u32(sm + C::kOffDS + (t % C::kDSBufs) * (128 * 128 * 2)) + g * 16384 + kr * 128;
-      uint32_t dpall[2][32];
-      tmem_ld32(tDP, dpall[0]);
-      tmem_ld32(tDP + 32, dpall[1]);
-      tmem_wait_ld();
-      // d = 64: dS^T(t) goes over this group's dP^T(t) columns (packed like
-      // P^T), where dK(t) reads it; dP(t+1) is issued once dK(t) is done.
+      uint32_t dsw[2][16];
+      {
+        uint32_t dpall[2][32];
+        tmem_ld32(tDP, dpall[0]);
+        tmem_ld32(tDP + 32, dpall[1]);
+        tmem_wait_ld();
+        // dS = P * bf16(dP - D), dP - D from TMEM: one pack, one bf16x2 product
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t(&dpv)[32] = dpall[c];
-        uint32_t dsw[16];
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          const int col = c * 32 + e;  // query column within this group's 64
-          // dS = P * bf16(dP - D), dP - D from TMEM: one pack, one bf16x2 product
-#pragma unroll
-          for (int h = 0; h < 4; ++h)
-            dsw[e / 2 + h] = bf16x2_mul(pp[col / 2 + h], pack_bf16x2(__uint_as_float(dpv[e + 2 * h]),
-                                                                       __uint_as_float(dpv[e + 2 * h + 1])));
-          st_shared_v4(ds_row + ((static_cast<uint32_t>(col >> 3) ^ swz) << 4), dsw[e / 2], dsw[e / 2 + 1],
-                       dsw[e / 2 + 2], dsw[e / 2 + 3]);
-          if (C::kSplitIssuers && e == 24) tmem_st16(tDP + c * 16, dsw);  // dS^T for dK (d = 64)
+          for (int e = 0; e < 32; e += 2)
+            dsw[c][e / 2] = bf16x2_mul(pp[(c * 32 + e) / 2], pack_bf16x2(__uint_as_float(dpall[c][e]),
+                                                                          __uint_as_float(dpall[c][e + 1])));
+          // d = 64: dS^T(t) also goes over this group's dP^T(t) columns
+          // (packed like P^T), where dK(t) reads it; dP(t+1) is issued once
+          // dK(t) is done.
+          if (C::kSplitIssuers) tmem_st16(tDP + c * 16, dsw[c]);
         }
       }
+      // The shared dS^T tile is free once the previous tile's readers are
+      // done with it: waited for after the arithmetic, which overlaps them.
+      if (t >= C::kDSBufs) {
+        ok = mbar_wait(&bars.ds_free[t % C::kDSBufs], ((t / C::kDSBufs) - 1) & 1, ab, dev_err);
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 8)
+          st_shared_v4(ds_row + ((static_cast<uint32_t>((c * 32 + e) >> 3) ^ swz) << 4), dsw[c][e / 2],
+                       dsw[c][e / 2 + 1], dsw[c][e / 2 + 2], dsw[c][e / 2 + 3]);
       if (C::kSplitIssuers) tmem_wait_st();
       tc_fence_before();
       fence_proxy_async_smem();
