@@ -865,10 +865,11 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
 // thread 0.  One staging tile (H0) is the drain's own; two more (H1, H2) lie
 // over the dS^T tile, which dK(t) and dQ(t) are done with once dQ(t) is
 // complete and which the compute groups rewrite only after the reduces have
-// read it (their ds_free wait also counts thread 0's arrival); the fourth
-// quarter waits in registers until H0 has been read again.  All four quarters are
-// out of TMEM before dq_free, so that dP(t+1), which lands in those columns,
-// never waits for the reduces.  Rows past the tensor's end are clipped by
+// read it (their ds_free wait also counts thread 0's arrival, so their
+// reduces are issued first); the first and fourth quarters wait in
+// registers until H0 is free.  All four quarters are out of TMEM before
+// dq_free, so that dP(t+1), which lands in those columns, never waits for
+// the reduces.  Rows past the tensor's end are clipped by
 // the TMA unit; rows of the tile that belong to the next segment receive
 // exact zeros (their probabilities are 0).
 // Ordered modes, as in bwd_drain64: thread 0 waits, before the tile's first
@@ -950,29 +951,18 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
       const uint32_t seen = kOrd && leader && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
       const bool store = kFirstStore && rank == 0;
       const int row = un.row0 + qt * 128;
-      // H0 is free once the previous tile's last reduce has read it.
-      if (leader) bulk_wait_group_read0();
-      if (!(ok = drain_sync())) break;
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // Columns 0-31 into H0, 32-95 into H1 / H2 (the dS^T tile, free once
-      // dQ(t) is done), 96-127 into registers; then dQ's columns are free.
+      // Columns 32-95 into H1 / H2 (the dS^T tile, free once dQ(t) is done),
+      // whose reduces go first: the compute groups wait for them to be read.
       uint32_t a[32];
-      tmem_ld32(tQ, a);
-      tmem_wait_ld();
-      stage32(h0, a);
       tmem_ld32(tQ + 32, a);
       tmem_wait_ld();
       stage32(h1, a);
       tmem_ld32(tQ + 64, a);
       tmem_wait_ld();
       stage32(h2, a);
-      uint32_t b[32];
-      tmem_ld32(tQ + 96, b);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.dq_free);
       fence_proxy_async_smem();
       if constexpr (kOrd) {
         if (leader) {
@@ -984,17 +974,35 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
       if (!(ok = drain_sync())) break;
       if (leader) {
         if (store) {
-          tma_store_3d(mdq, h0, 0, row, bh);
           tma_store_3d(mdq, h1, 32, row, bh);
           tma_store_3d(mdq, h2, 64, row, bh);
         } else {
-          tma_reduce_add_3d(mdq, h0, 0, row, bh);
           tma_reduce_add_3d(mdq, h1, 32, row, bh);
           tma_reduce_add_3d(mdq, h2, 64, row, bh);
         }
         bulk_commit_group();
-        bulk_wait_group_read0();        // H0, H1 and H2 have been read
+      }
+      // Columns 0-31 and 96-127 into registers; then dQ's columns are free.
+      uint32_t b[32];
+      tmem_ld32(tQ, a);
+      tmem_ld32(tQ + 96, b);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.dq_free);
+      // H0 is free once the previous tile's reduces from it have read it
+      // (every group but this tile's first).
+      if (leader) bulk_wait_group_read<1>();
+      if (!(ok = drain_sync())) break;
+      stage32(h0, a);
+      fence_proxy_async_smem();
+      if (!(ok = drain_sync())) break;
+      if (leader) {
+        if (store) tma_store_3d(mdq, h0, 0, row, bh);
+        else tma_reduce_add_3d(mdq, h0, 0, row, bh);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();      // H1 and H2 have been read
         mbar_arrive(&bars.ds_free[0]);  // the compute groups may rewrite the dS^T tile
+        bulk_wait_group_read0();        // ... and H0
       }
       if (!(ok = drain_sync())) break;
       stage32(h0, b);
