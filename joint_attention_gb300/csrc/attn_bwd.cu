@@ -52,8 +52,8 @@
 // S^T - LSE / scale and dP^T - D.
 //
 // d = 128: TMEM S^T/P^T [0,128), dP^T [128,256), dV [256,384), dK [384,512),
-// dQ over the dP^T columns; one issuer in the order dV(i), S(i+1), dK(i),
-// dQ(i), dP(i+1), with dP(i+1) waiting for dQ(i) to be out of TMEM.
+// dQ over the dP^T columns; one issuer in the order dV(i), dK(i), dQ(i),
+// S(i+1), dP(i+1), with dP(i+1) waiting for dQ(i) to be out of TMEM.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -588,14 +588,6 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, u
       tc_fence_after();
       mma_dv<D>(tmem + C::kColDV, tmem + C::kColS, mDO(t), i > 0);
       umma_commit(&bars.do_empty[t % C::kDOStages]);
-      // S(t+1): overwrites the S^T/P^T columns behind dV(t).
-      if (i + 1 < nkt) {
-        if (!(ok = mbar_wait(&bars.q_full[(t + 1) % C::kQStages], q_ph(t + 1), ab, dev_err))) break;
-        tc_fence_after();
-        mma_kk<D>(tmem + C::kColS, kK, kQ(t + 1), C::kIdescSS);
-        umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t + 1), C::kIdescSS, 1u);
-        umma_commit(&bars.s_full);
-      }
       // dK(t): needs dS^T(t) in shared memory (compute is then done with dP(t)).
       if (!(ok = mbar_wait(&bars.ds_ready, t & 1, ab, dev_err))) break;
       if (i == 0 && ui > 0 && !(ok = mbar_wait(&bars.acc_free_k, (ui - 1) & 1, ab, dev_err))) break;
@@ -608,6 +600,14 @@ __device__ void bwd_mma(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& w, u
       umma_commit(&bars.dq_full);
       umma_commit(&bars.ds_free[t % C::kDSBufs]);
       if (i + 1 < nkt) {
+        // S(t+1): overwrites the S^T/P^T columns behind dV(t); issued after
+        // dK(t) and dQ(t), which lead to dP(t+1) through the dQ drain (the
+        // compute groups need S(t+1) no sooner than dP(t+1)).
+        if (!(ok = mbar_wait(&bars.q_full[(t + 1) % C::kQStages], q_ph(t + 1), ab, dev_err))) break;
+        tc_fence_after();
+        mma_kk<D>(tmem + C::kColS, kK, kQ(t + 1), C::kIdescSS);
+        umma_bf16_ss(tmem + C::kColS, kOnesS, kSt(t + 1), C::kIdescSS, 1u);
+        umma_commit(&bars.s_full);
         if (!(ok = mbar_wait(&bars.dq_free, t & 1, ab, dev_err))) break;
         if (!(ok = mbar_wait(&bars.do_full[(t + 1) % C::kDOStages], do_ph(t + 1), ab, dev_err))) break;
         tc_fence_after();
