@@ -1239,7 +1239,8 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
       g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
       g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
     };
-    float dot = 0.f;
+    // (packed f32x2 arithmetic: even and odd columns in two partial sums)
+    uint64_t dot2 = f2_make(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
@@ -1251,14 +1252,18 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int e = c * 32 + q * 8 + 2 * h;
-          dot = fmaf(g[2 * h] * __uint_as_float(dkr[e]), __uint_as_float(kx[h] << 16), dot);
-          dot = fmaf(g[2 * h + 1] * __uint_as_float(dkr[e + 1]), __uint_as_float(kx[h] & 0xFFFF0000u), dot);
+          const uint64_t ga = f2_mul(f2_make(g[2 * h], g[2 * h + 1]),
+                                     f2_make(__uint_as_float(dkr[e]), __uint_as_float(dkr[e + 1])));
+          dot2 = f2_fma(ga, f2_make(__uint_as_float(kx[h] << 16), __uint_as_float(kx[h] & 0xFFFF0000u)), dot2);
         }
       }
     }
-    const float coef = r * r * r * (1.f / D) * scale * dot;
+    float dot0, dot1;
+    f2_split(dot2, dot0, dot1);
+    const float coef = r * r * r * (1.f / D) * scale * (dot0 + dot1);
     // Key rows past the segment have r = 0 and k = 0, so their terms vanish.
     const float rs = r * scale;
+    const uint64_t rs2 = f2_make(rs, rs), ncoef2 = f2_make(-coef, -coef);
     // Pass 2, per 32-column chunk: dk = r g dk_hat - coef k over the k row
     // (in place), and the chunk's dgk terms dk_hat k r summed over the warp's
     // 32 rows by a reduce-scatter (lane L ends with column 32c + L).
@@ -1277,11 +1282,14 @@ __device__ void bwd_epilogue_warps(uint8_t* sm, BwdBars& bars, uint32_t tmem, co
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int e = q * 8 + 2 * h;
-          const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
-          const float a0 = __uint_as_float(a[e]), a1 = __uint_as_float(a[e + 1]);
-          o[h] = pack_bf16x2(fmaf(rs * g[2 * h], a0, -coef * x0), fmaf(rs * g[2 * h + 1], a1, -coef * x1));
-          a[e] = __float_as_uint(a0 * x0 * rs);
-          a[e + 1] = __float_as_uint(a1 * x1 * rs);
+          const uint64_t x2 = f2_make(__uint_as_float(kx[h] << 16), __uint_as_float(kx[h] & 0xFFFF0000u));
+          const uint64_t a2 = f2_make(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+          float y0, y1, p0, p1;
+          f2_split(f2_fma(f2_mul(rs2, f2_make(g[2 * h], g[2 * h + 1])), a2, f2_mul(ncoef2, x2)), y0, y1);
+          o[h] = pack_bf16x2(y0, y1);
+          f2_split(f2_mul(f2_mul(a2, x2), rs2), p0, p1);
+          a[e] = __float_as_uint(p0);
+          a[e + 1] = __float_as_uint(p1);
         }
         st_shared_v4(addr, o[0], o[1], o[2], o[3]);
       }
