@@ -1054,8 +1054,16 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
         }
       }
     }
-    // Pass 1 over the dK accumulator: dot = sum_c g_c dk_hat_c k_c.
-    float dot = 0.f;
+    // The gain, 8 columns at a time (two 16-byte broadcasts).
+    auto gain8 = [&](int col, float (&g)[8]) {
+      const float4 g0 = *reinterpret_cast<const float4*>(&bars.gk[col]);
+      const float4 g1 = *reinterpret_cast<const float4*>(&bars.gk[col + 4]);
+      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+      g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+    };
+    // Pass 1 over the dK accumulator: dot = sum_c g_c dk_hat_c k_c (packed
+    // f32x2 arithmetic: even and odd columns in two partial sums).
+    uint64_t dot2 = f2_make(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t a[32];
@@ -1065,16 +1073,22 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
       for (int c8 = 0; c8 < 4; ++c8) {
         const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
+        float g[8];
+        gain8(c * 32 + c8 * 8, g);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-          dot = fmaf(bars.gk[col] * __uint_as_float(a[e]) * scale, __uint_as_float(kx[h] << 16), dot);
-          dot = fmaf(bars.gk[col + 1] * __uint_as_float(a[e + 1]) * scale, __uint_as_float(kx[h] & 0xFFFF0000u),
-                     dot);
+          const int e = c8 * 8 + 2 * h;
+          const uint64_t ga = f2_mul(f2_make(g[2 * h], g[2 * h + 1]),
+                                     f2_make(__uint_as_float(a[e]), __uint_as_float(a[e + 1])));
+          dot2 = f2_fma(ga, f2_make(__uint_as_float(kx[h] << 16), __uint_as_float(kx[h] & 0xFFFF0000u)), dot2);
         }
       }
     }
-    const float coef = r * r * r * (1.f / D) * dot;
+    float dot0, dot1;
+    f2_split(dot2, dot0, dot1);
+    const float coef = r * r * r * (1.f / D) * scale * (dot0 + dot1);
+    const float rs = r * scale;
+    const uint64_t rs2 = f2_make(rs, rs), ncoef2 = f2_make(-coef, -coef);
     // Pass 2, per 32-column chunk: dk = r g dk_hat - coef k, and the chunk's
     // dgk terms dk_hat k r summed over the warp's 32 rows by a reduce-scatter
     // (lane L ends with column 32 c + L).
@@ -1091,17 +1105,19 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
       for (int c8 = 0; c8 < 4; ++c8) {
         const uint4 kw = key_live ? krow[c * 4 + c8] : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t kx[4] = {kw.x, kw.y, kw.z, kw.w};
-        float y[8];
+        float y[8], g[8];
+        gain8(c * 32 + c8 * 8, g);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const int e = c8 * 8 + 2 * h, col = c * 32 + e;
-          const float x0 = __uint_as_float(kx[h] << 16), x1 = __uint_as_float(kx[h] & 0xFFFF0000u);
-          const float dk0 = key_live ? __uint_as_float(a[e]) * scale : 0.f;
-          const float dk1 = key_live ? __uint_as_float(a[e + 1]) * scale : 0.f;
-          y[2 * h] = r * bars.gk[col] * dk0 - coef * x0;
-          y[2 * h + 1] = r * bars.gk[col + 1] * dk1 - coef * x1;
-          a[e] = __float_as_uint(dk0 * x0 * r);
-          a[e + 1] = __float_as_uint(dk1 * x1 * r);
+          const int e = c8 * 8 + 2 * h;
+          // Key rows past the segment have r = 0 and k = 0, so their terms vanish.
+          const uint64_t x2 = f2_make(__uint_as_float(kx[h] << 16), __uint_as_float(kx[h] & 0xFFFF0000u));
+          const uint64_t a2 = key_live ? f2_make(__uint_as_float(a[e]), __uint_as_float(a[e + 1])) : f2_make(0.f, 0.f);
+          float p0, p1;
+          f2_split(f2_fma(f2_mul(rs2, f2_make(g[2 * h], g[2 * h + 1])), a2, f2_mul(ncoef2, x2)), y[2 * h], y[2 * h + 1]);
+          f2_split(f2_mul(f2_mul(a2, x2), rs2), p0, p1);
+          a[e] = __float_as_uint(p0);
+          a[e + 1] = __float_as_uint(p1);
         }
         if (key_live) {
           uint4 o;
