@@ -55,9 +55,9 @@ def flops_bwd(B, H, N, d):
 _CAPTURE = ("ncu --set full --clock-control none -k regex:attn_ -s 2 -c 2, "
             "python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-per-config")
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 197.568768e6 + 64.572672e6, "source": "attn_bwd.cu", "sha1": "fe15a5daea6a",
+    "attn_bwd": {"bytes": 197.590784e6 + 64.651264e6, "source": "attn_bwd.cu", "sha1": "aff0a1037281",
                  "capture": _CAPTURE},
-    "attn_fwd": {"bytes": 81.348096e6 + 57.467392e6, "source": "attn_fwd.cu", "sha1": "d52b848c736f",
+    "attn_fwd": {"bytes": 81.400064e6 + 56.985088e6, "source": "attn_fwd.cu", "sha1": "d52b848c736f",
                  "capture": _CAPTURE},
 }
 
