@@ -30,8 +30,8 @@
 //   warps 8-11  dQ drain, one thread per query row: dQ_i from TMEM into
 //               swizzled 128 x 32 fp32 staging tiles, each added into the
 //               global accumulator by one TMA tensor reduce (d = 128: two of
-//               the four tiles over the dS^T tile); d = 128, also the unit
-//               epilogue.
+//               the four tiles over the query tile's finished Q stage);
+//               d = 128, also the unit epilogue.
 //   warps 12-15 d = 64 unit epilogue, one thread per key row: dv, and the
 //               K-RMSNorm backward of dK (dk and the unit's dgk partial),
 //               built in the unit's own K/V buffer once the MMAs are done
@@ -132,7 +132,7 @@ struct BwdCfg {
   static constexpr int kConstAtom = 256;
   // dQ staging: 128 x 32 fp32 tiles (128-byte rows, 128-byte swizzle), each
   // reduced into the accumulator by one TMA tensor reduce; d = 64 has two of
-  // its own, d = 128 one (two more lie over the dS^T tile).
+  // its own, d = 128 one (two more lie over the query tile's Q stage).
   static constexpr int kDQStageBytes = (D == 64) ? 2 * 128 * 128 : 128 * 128;
   static constexpr int kOffKV = 0;                            // + buf * 2 * kTile: K, then V
   static constexpr int kOffQ = kKVBufs * 2 * kTile;           // + stage * kTile
@@ -863,15 +863,15 @@ __device__ void bwd_drain64(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W& 
 // c ^ (r % 8), so that the row-per-thread writes are free of bank conflicts)
 // and added into the fp32 accumulator by TMA tensor reduces issued by
 // thread 0.  One staging tile (H0) is the drain's own; two more (H1, H2) lie
-// over the dS^T tile, which dK(t) and dQ(t) are done with once dQ(t) is
-// complete and which the compute groups rewrite only after the reduces have
-// read it (their ds_free wait also counts thread 0's arrival, so their
-// reduces are issued first); the first and fourth quarters wait in
-// registers until H0 is free.  All four quarters are out of TMEM before
+// over the query tile's Q stage, which its last reader dK(t) is done with
+// once dQ(t) is complete and which the producer reloads only after the
+// reduces have read it (the stage's q_empty also counts thread 0's arrival,
+// and their reduces are issued first); the first and fourth quarters wait
+// in registers until H0 is free.  All four quarters are out of TMEM before
 // dq_free, so that dP(t+1), which lands in those columns, never waits for
-// the reduces.  Rows past the tensor's end are clipped by
-// the TMA unit; rows of the tile that belong to the next segment receive
-// exact zeros (their probabilities are 0).
+// the reduces.  Rows past the tensor's end are clipped by the TMA unit;
+// rows of the tile that belong to the next segment receive exact zeros
+// (their probabilities are 0).
 // Ordered modes, as in bwd_drain64: thread 0 waits, before the tile's first
 // reduce, until the contributions of lower rank to the query tile are
 // complete (its counter), and announces its own once it is complete (at the
@@ -899,8 +899,6 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
   const uint32_t tQ = tmem + lane_base + C::kColDQ;
   const uint32_t tDK = tmem + lane_base + C::kColDK;
   uint8_t* h0 = sm + C::kOffDQ;
-  uint8_t* h1 = sm + C::kOffDS;
-  uint8_t* h2 = sm + C::kOffDS + 16384;
   const uint32_t rowoff = static_cast<uint32_t>(r128 * 128);
   const uint32_t swz = static_cast<uint32_t>(r128 & 7);
   auto stage32 = [&](uint8_t* tile, const uint32_t (&a)[32]) {
@@ -951,11 +949,15 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
       const uint32_t seen = kOrd && leader && rank > 0 ? ld_acquire_gpu(cnt) : 0u;
       const bool store = kFirstStore && rank == 0;
       const int row = un.row0 + qt * 128;
+      // H1 / H2: the query tile's Q stage, which its last reader dK(t) is
+      // done with once dQ(t) is complete.
+      uint8_t* h1 = sm + C::kOffQ + (t % C::kQStages) * C::kTile;
+      uint8_t* h2 = h1 + 16384;
       ok = mbar_wait(&bars.dq_full, t & 1, ab, dev_err);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-      // Columns 32-95 into H1 / H2 (the dS^T tile, free once dQ(t) is done),
-      // whose reduces go first: the compute groups wait for them to be read.
+      // Columns 32-95 into H1 / H2, whose reduces go first: the producer
+      // reloads the Q stage once they have been read.
       uint32_t a[32];
       tmem_ld32(tQ + 32, a);
       tmem_wait_ld();
@@ -1000,8 +1002,8 @@ __device__ void bwd_drain128(uint8_t* sm, BwdBars& bars, uint32_t tmem, const W&
         if (store) tma_store_3d(mdq, h0, 0, row, bh);
         else tma_reduce_add_3d(mdq, h0, 0, row, bh);
         bulk_commit_group();
-        bulk_wait_group_read<1>();      // H1 and H2 have been read
-        mbar_arrive(&bars.ds_free[0]);  // the compute groups may rewrite the dS^T tile
+        bulk_wait_group_read<1>();                        // H1 and H2 have been read
+        mbar_arrive(&bars.q_empty[t % C::kQStages]);  // the producer may reload the Q stage
         bulk_wait_group_read0();        // ... and H0
       }
       if (!(ok = drain_sync())) break;
@@ -1385,7 +1387,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t n_rel = C::kSplitIssuers ? 2u : 1u;
     for (int s = 0; s < 3; ++s) {
       mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], 1);  // released after its last product (dK)
+      // Released after its last product (dK); d = 128 also by the drain,
+      // whose reduces read two staging tiles over the stage.
+      mbar_init(&bars.q_empty[s], D == 128 ? 2 : 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.kv_full[s], 1);
@@ -1393,9 +1397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars.kv_mmadone[s], n_rel);  // d = 64: the recompute and the dQ issuers
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], n_rel);
-      // The dQ product (d = 64: dK reads dS^T from TMEM); d = 128 also the
-      // drain, whose reduces read two staging tiles over the dS^T tile.
-      mbar_init(&bars.ds_free[s], D == 128 ? 2 : 1);
+      mbar_init(&bars.ds_free[s], 1);  // the dQ product (d = 64: dK reads dS^T from TMEM)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
