@@ -44,6 +44,14 @@ namespace jattn {
 namespace {
 
 constexpr int kFwdThreads = 384;  // 8 softmax warps, producer, 2 MMA issuers, accumulator zeroing
+// Registers per thread (setmaxnreg): softmax 208, the other warpgroup 88.
+// Each SM sub-partition holds two softmax warps and one other (warp w on
+// w % 4), and an increase draws only on the registers its three warps were
+// launched with, so 2 x 208 + 88 must equal 3 x the launch count (168).  The
+// launcher refuses any build whose register count differs.
+constexpr int kRegLaunchFwd = 168, kRegSoftmax = 208, kRegOtherFwd = 88;
+static_assert(2 * kRegSoftmax + kRegOtherFwd == 3 * kRegLaunchFwd, "forward register split");
+static_assert(kRegSoftmax >= kRegLaunchFwd && kRegOtherFwd <= kRegLaunchFwd, "setmaxnreg direction");
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -603,13 +611,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == 8) {
-    if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, w, dev_err);
-  } else if (warp == 11) {
-    if (dq_zero) fwd_zero_dq<D>(w, dq_zero, zero_count, lane);
-  } else if (warp >= 9) {
-    if (lane == 0) fwd_mma<D>(sm, bars, tmem, warp - 9, w, dev_err);
+  if (warp >= 8) {
+    setmaxnreg_dec<kRegOtherFwd>();
+    if (warp == 8) {
+      if (lane == 0) fwd_producer<D>(&map_q, &map_k, &map_v, sm, bars, w, dev_err);
+    } else if (warp == 11) {
+      if (dq_zero) fwd_zero_dq<D>(w, dq_zero, zero_count, lane);
+    } else {
+      if (lane == 0) fwd_mma<D>(sm, bars, tmem, warp - 9, w, dev_err);
+    }
   } else {
+    setmaxnreg_inc<kRegSoftmax>();
     fwd_softmax<D>(sm, bars, tmem, warp >> 2, w, scale_log2, &map_o, out, lse, dev_err);
   }
   tc_fence_before();
@@ -629,6 +641,12 @@ cudaError_t launch_fwd_w(const W& w, const CUtensorMap& mq, const CUtensorMap& m
   auto kernel = attn_fwd_kernel<D, W>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
+  // The setmaxnreg split is valid only for the register count it was sized
+  // for; any other build is refused rather than launched.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegLaunchFwd) return cudaErrorInvalidConfiguration;
   const int sms = device_sm_count();
   const int grid = w.units < sms ? w.units : sms;
   const float scale_log2 = s.scale * 1.4426950408889634f;
