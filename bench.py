@@ -55,9 +55,9 @@ def flops_bwd(B, H, N, d):
 _CAPTURE = ("ncu --set full --clock-control none -k regex:attn_ -s 2 -c 2, "
             "python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-e2e --no-per-config")
 NCU_TRAFFIC = {
-    "attn_bwd": {"bytes": 197.592064e6 + 65.342208e6, "source": "attn_bwd.cu", "sha1": "f7d6bf58b915",
+    "attn_bwd": {"bytes": 197.58464e6 + 64.802304e6, "source": "attn_bwd.cu", "sha1": "f7d6bf58b915",
                  "capture": _CAPTURE},
-    "attn_fwd": {"bytes": 81.351424e6 + 57.786112e6, "source": "attn_fwd.cu", "sha1": "d52b848c736f",
+    "attn_fwd": {"bytes": 81.322496e6 + 57.446144e6, "source": "attn_fwd.cu", "sha1": "1e3f9884fd9f",
                  "capture": _CAPTURE},
 }
 
